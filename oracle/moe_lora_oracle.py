@@ -1,0 +1,281 @@
+"""CPU oracle for the routed MoE expert layer with per-expert LoRA (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain definition of what the
+layer computes.  Only the test suite, the smoke check and the CPU-baseline leg of
+the benchmark may import it; the product path (the CUDA library and its Python
+binding) never does.  It shares no code with the CUDA path.
+
+Arithmetic: float64 accumulation with bfloat16 rounding exactly at the stage
+boundaries the pages fix -- the gate_up GEMM output and the gate_up LoRA delta are
+bf16 tensors (sglang PR #28466 "bf16 MoE-LoRA for trtllm backend", Files changed,
+launcher row: bf16 Gemm2 gate_up output, bf16 activation; vLLM API page
+"fused_moe/experts/trtllm_lora_moe", TrtLlmBf16LoRAExperts.apply step 1: the
+gemm1_lora_delta tensor is bf16), the activation output is bf16 (same launcher
+row: "bf16 out, no quant"), and the layer output is bf16.  Everything between
+those points (LoRA shrink, down GEMM, down LoRA, finalize sum) stays float64.
+
+The one exception is the DeepSeekV3 selection key: floating point decides an
+integer there (which experts are chosen), so the oracle computes that key in the
+same float32 arithmetic the kernel uses, step by step (see `sigmoid_f32`).
+
+Readings of points the pages leave open (each also listed in the design notes):
+  * w1 rows [0, I) are the gate projection and rows [I, 2I) the up projection
+    (vLLM page, apply step 1: "vLLM's w13 order (gate=w1 first, up=w3 second)").
+  * `scaling[s]` multiplies the whole B.A.x product (standard LoRA alpha/r).
+  * The gate_up delta is not multiplied by the routing weight; the down delta is
+    (vLLM page, apply step 1 comment "do NOT multiply by the routing weight (it is
+    a pre-SwiGLU bias)"; _finalize_with_w2_lora docstring "already-weighted w2_delta").
+  * A token with slot -1, or a slot with scaling 0 or rank 0, gets no delta
+    (sglang PR #28466, §2 routed-expert LoRA bullet: "-1 sentinel" for tokens with
+    no adapter).
+  * Only rows r < ranks[s] of A and columns r < ranks[s] of B are read.
+  * Ties in top-k selection go to the lower expert id; a token's selected experts
+    are listed in selection order (higher key first, lower id first on ties).
+  * The permutation lists pairs expert by expert, ascending expanded index
+    p = t*top_k + j inside each expert (vLLM page, _unpermute_activation
+    docstring: "expanded_idx = token*top_k + k").
+  * Renormalize: weights = softmax over the k selected logits (vLLM page,
+    _supports_routing_method lists Renormalize and RenormalizeNaive; softmax of all
+    logits followed by renormalising the top k gives the same numbers).
+  * DeepSeekV3 with n_group = topk_group = 1: scores s = sigmoid(logit), select on
+    s + correction_bias, weights = s_sel / sum(s_sel) * routed_scaling_factor.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+RENORMALIZE = 0
+DEEPSEEK_V3 = 1
+
+# ----------------------------------------------------------------------------
+# bf16 rounding of float64 values
+# ----------------------------------------------------------------------------
+
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value (8 significant bits,
+    ties to even), returned as float64.  One rounding, straight from float64."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        _, e = np.frexp(x)                    # x = m * 2**e with 0.5 <= |m| < 1
+        e = np.maximum(e, -125)               # below 2**-126 the bf16 grid is fixed at 2**-133
+        q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)
+        q = np.where(np.abs(q) > _BF16_MAX, np.copysign(np.inf, x), q)
+    return np.where(np.isfinite(x), q, x)
+
+
+# ----------------------------------------------------------------------------
+# the float32 sigmoid used for the DeepSeekV3 selection key
+# ----------------------------------------------------------------------------
+# sigma(z) = 1 / (1 + E(-z)), E = exp evaluated by Cody-Waite range reduction
+# (W. J. Cody and W. Waite, "Software Manual for the Elementary Functions", 1980):
+#   n = rint(x * log2(e)),  r = (x - n*C1) - n*C2  with C1 + C2 = ln 2 and C1 short
+#   enough that n*C1 is exact,  exp(x) = 2**n * exp(r),
+# and exp(r) from its degree-7 Taylor polynomial in Horner form.  Every operation
+# is one IEEE float32 operation rounded to nearest (no fused multiply-add), so the
+# CUDA kernel, which spells out the same operations, gets the same bits.
+
+_F = np.float32
+_LOG2E = _F(1.4426950408889634)
+_LN2_HI = _F(0.693359375)                # 355/512: 9 significant bits
+_LN2_LO = _F(-2.12194440054690583e-4)    # ln 2 - 355/512
+_TAYLOR = [_F(1.0) / _F(f) for f in (1.0, 1.0, 2.0, 6.0, 24.0, 120.0, 720.0, 5040.0)]  # 1/k!, k=0..7
+
+
+def exp_f32(x) -> np.ndarray:
+    """exp(x) in float32 by the Cody-Waite scheme above; x clamped to [-86, 88]."""
+    x = np.asarray(x, dtype=np.float32)
+    x = np.minimum(np.maximum(x, _F(-86.0)), _F(88.0))
+    n = np.rint(x * _LOG2E).astype(np.float32)
+    r = (x - n * _LN2_HI).astype(np.float32)
+    r = (r - n * _LN2_LO).astype(np.float32)
+    p = np.full_like(r, _TAYLOR[7])
+    for c in reversed(_TAYLOR[:7]):
+        p = (p * r).astype(np.float32)
+        p = (p + c).astype(np.float32)
+    two_n = np.ldexp(np.ones_like(p), n.astype(np.int32)).astype(np.float32)
+    return (p * two_n).astype(np.float32)
+
+
+def sigmoid_f32(z) -> np.ndarray:
+    """sigma(z) = 1 / (1 + exp(-z)) in float32 (one rounding per operation)."""
+    z = np.asarray(z, dtype=np.float32)
+    e = exp_f32(-z)
+    return (_F(1.0) / (_F(1.0) + e).astype(np.float32)).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------
+# routing
+# ----------------------------------------------------------------------------
+
+def _select_topk(keys: np.ndarray, top_k: int) -> np.ndarray:
+    """Indices of the top_k largest keys per row, larger key first, lower id first
+    on equal keys (a stable sort of -key keeps ids ascending among ties)."""
+    order = np.argsort(-keys, axis=1, kind="stable")
+    return order[:, :top_k].astype(np.int32)
+
+
+def route(router_logits, top_k: int, method: int = RENORMALIZE, correction_bias=None,
+          routed_scaling_factor: float = 1.0, n_group: int = 1, topk_group: int = 1):
+    """Top-k routing of each token (vLLM API page "fused_moe/experts/trtllm_lora_moe",
+    TrtLlmBf16LoRAExperts._supports_routing_method: Renormalize, DeepSeekV3).
+
+    router_logits: [T, E] bf16 values (any float dtype holding them exactly).
+    Returns topk_ids [T, k] int32 and topk_weights [T, k] float64.
+    """
+    if n_group != 1 or topk_group != 1:
+        raise NotImplementedError("only n_group = topk_group = 1")
+    logit = np.asarray(router_logits, dtype=np.float32)
+    logit = np.where(np.isnan(logit), np.float32(-np.inf), logit)   # NaN logits never win
+    T, E = logit.shape
+    if not 1 <= top_k <= E:
+        raise ValueError("need 1 <= top_k <= E")
+    if method == RENORMALIZE:
+        ids = _select_topk(logit.astype(np.float64), top_k)
+        sel = np.take_along_axis(logit.astype(np.float64), ids, axis=1)
+        ex = np.exp(sel - sel[:, :1])
+        w = ex / ex.sum(axis=1, keepdims=True)
+    elif method == DEEPSEEK_V3:
+        bias = np.asarray(correction_bias, dtype=np.float32)
+        s = sigmoid_f32(logit)                                   # [T, E] float32
+        key = (s + bias[None, :]).astype(np.float32)             # float32 add, as the kernel
+        ids = _select_topk(key, top_k)
+        sel = np.take_along_axis(s, ids, axis=1).astype(np.float64)
+        w = sel / sel.sum(axis=1, keepdims=True) * float(routed_scaling_factor)
+    else:
+        raise ValueError("unknown routing method")
+    return ids, w
+
+
+def align(topk_ids, E: int):
+    """Group routed pairs by expert.
+
+    Returns expert_offsets [E+1] (exclusive prefix of per-expert counts),
+    perm [P] (permuted position -> expanded index p = t*k + j) and inv [P]
+    (expanded index -> permuted position; the expanded_idx_to_permuted_idx map of
+    the vLLM page, _unpermute_activation docstring).
+    """
+    flat = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
+    counts = np.bincount(flat, minlength=E)[:E]
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    perm = np.argsort(flat, kind="stable").astype(np.int32)   # by expert, p ascending within
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size, dtype=np.int32)
+    return offsets, perm, inv
+
+
+# ----------------------------------------------------------------------------
+# the layer
+# ----------------------------------------------------------------------------
+
+def silu(z):
+    """SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)), float64."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def moe_lora_forward(hidden, router_logits, w1, w2, top_k, method=RENORMALIZE,
+                     correction_bias=None, routed_scaling_factor=1.0,
+                     lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
+                     slot_idx=None, ranks=(), scalings=(), lora_off=False,
+                     tokens=None, keep_intermediates=False):
+    """Forward of the routed MoE expert layer with per-expert LoRA.
+
+    The stages are those of sglang PR #28466 ("Files changed", launcher row, and
+    §1 flow (A)): routing -> permute -> gate_up GEMM (N = 2I) -> LoRA delta added
+    before SwiGLU -> down GEMM (+ down LoRA delta) -> weighted top-k finalize; the
+    finalize formula is the vLLM page's _finalize_with_w2_lora: for each token, the
+    routing-weighted sum over its top-k pairs of the down output plus the
+    (routing-weighted) down LoRA delta.
+
+    Per pair p = (t, j) with expert e = topk_ids[t, j] and slot s = slot_idx[t]
+    (L = s >= 0 and scalings[s] != 0 and ranks[s] > 0, and not lora_off):
+      g  = bf16(w1[e] @ x_t)                                       [2I]
+      d  = bf16(scaling_s * B_gu[s,e][:, :r] @ (A_gu[s,e][:r] @ x_t))  if L else 0
+      a  = bf16(silu(g[:I] + d[:I]) * (g[I:] + d[I:]))             [I]
+      y  = w2[e] @ a                                               [H]
+      dd = scaling_s * B_dn[s,e][:, :r] @ (A_dn[s,e][:r] @ a)       if L else 0
+      out[t] = bf16(sum_j w[t,j] * (y + dd))
+
+    Arguments are arrays holding bf16 values (w1/w2/LoRA weights may also be any
+    object whose [e] / [s, e] indexing returns such an array, so large weights can
+    be streamed expert by expert).  `tokens` restricts the layer output to those
+    token rows (routing and the permutation are always computed for all tokens;
+    tokens are independent given the routing).
+
+    Returns a dict with out [n_tok, H] (float64 holding bf16 values), topk_ids,
+    topk_weights, expert_offsets, perm, inv and, if keep_intermediates, the
+    per-pair g, d, a, y, dd keyed by expanded index.
+    """
+    x = _f64(hidden)
+    T, H = x.shape
+    ids, w = route(router_logits, top_k, method, correction_bias, routed_scaling_factor)
+    E = np.asarray(router_logits).shape[1]
+    offsets, perm, inv = align(ids, E)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
+    S = len(ranks)
+
+    inter = {} if keep_intermediates else None
+    contrib_of = {}                     # (t, j) -> w[t,j] * (y + dd), float64 [H]
+
+    # pairs of the requested tokens, grouped by expert (one matrix product per expert
+    # evaluates every pair routed to that expert; pairs are independent)
+    pair_t = np.repeat(tok, top_k)
+    pair_j = np.tile(np.arange(top_k), tok.size)
+    pair_e = ids[pair_t, pair_j]
+    for e in np.unique(pair_e):
+        sel = np.nonzero(pair_e == e)[0]
+        ts, js = pair_t[sel], pair_j[sel]
+        xe = x[ts]                                               # [n, H]
+        W1 = _f64(w1[e])                                         # [2I, H]
+        W2 = _f64(w2[e])                                         # [H, I]
+        I = W1.shape[0] // 2
+        g = round_bf16(xe @ W1.T)                                # [n, 2I]
+        d = np.zeros_like(g)
+        lora_rows = []
+        if not lora_off and S > 0:
+            for s in range(S):
+                r = int(ranks[s])
+                sc = float(scalings[s])
+                m = np.nonzero(slots[ts] == s)[0]
+                if m.size == 0 or r == 0 or sc == 0.0:
+                    continue
+                A = _f64(lora_A_gu[s, e])[:r]                    # [r, H]
+                B = _f64(lora_B_gu[s, e])[:, :r]                 # [2I, r]
+                u = xe[m] @ A.T                                  # [m, r]
+                d[m] = round_bf16(sc * (u @ B.T))
+                lora_rows.append((s, r, sc, m))
+        a = round_bf16(silu(g[:, :I] + d[:, :I]) * (g[:, I:] + d[:, I:]))   # [n, I]
+        y = a @ W2.T                                             # [n, H]
+        dd = np.zeros_like(y)
+        for s, r, sc, m in lora_rows:
+            A = _f64(lora_A_dn[s, e])[:r]                        # [r, I]
+            B = _f64(lora_B_dn[s, e])[:, :r]                     # [H, r]
+            v = a[m] @ A.T                                       # [m, r]
+            dd[m] = sc * (v @ B.T)
+        contrib = w[ts, js][:, None] * (y + dd)
+        for i in range(sel.size):
+            contrib_of[(int(ts[i]), int(js[i]))] = contrib[i]
+            if inter is not None:
+                inter[int(ts[i]) * top_k + int(js[i])] = dict(g=g[i], d=d[i], a=a[i], y=y[i], dd=dd[i])
+
+    # finalize: out[t] = bf16(sum over j = 0..k-1, in that order, of w[t,j] * (y + dd))
+    out_acc = np.zeros((tok.size, H), dtype=np.float64)
+    for i, t in enumerate(tok):
+        acc = np.zeros(H, dtype=np.float64)
+        for j in range(top_k):
+            acc = acc + contrib_of[(int(t), j)]
+        out_acc[i] = acc
+    res = dict(out=round_bf16(out_acc), topk_ids=ids, topk_weights=w,
+               expert_offsets=offsets, perm=perm, inv=inv, tokens=tok)
+    if inter is not None:
+        res["pairs"] = inter
+    return res

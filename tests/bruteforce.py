@@ -1,0 +1,88 @@
+"""Independent brute-force evaluation of the layer for tiny inputs (test helper).
+
+Written separately from the oracle, in a different shape: plain Python floats,
+exactly rounded sums (math.fsum), exact bf16 rounding through fractions.Fraction,
+and a DENSE evaluation -- every token goes through every expert and the routing
+only enters as a mask times weight, so the oracle's expert grouping, permutation
+and top-k gather are not reused.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+
+def bf16_exact(x: float) -> float:
+    """Nearest bfloat16 to x (ties to even), via exact rational arithmetic."""
+    if x != x or math.isinf(x) or x == 0.0:
+        return x
+    _, e = math.frexp(x)
+    e = max(e, -125)
+    quantum = Fraction(2) ** (e - 8)
+    return float(round(Fraction(x) / quantum) * quantum)
+
+
+def dot(a, b) -> float:
+    return math.fsum(float(x) * float(y) for x, y in zip(a, b))
+
+
+def sigmoid(z: float) -> float:
+    return 1.0 / (1.0 + math.exp(-z)) if z >= 0 else math.exp(z) / (1.0 + math.exp(z))
+
+
+def topk_bruteforce(keys, k):
+    """Ids of the k largest keys, larger first, lower id first among equal keys."""
+    return sorted(range(len(keys)), key=lambda e: (-keys[e], e))[:k]
+
+
+def dense_layer(x, logits, w1, w2, top_k, method, bias=None, rsf=1.0, A_gu=None, B_gu=None,
+                A_dn=None, B_dn=None, slot_idx=None, ranks=(), scalings=(), keys_fn=None):
+    """Dense evaluation on nested lists.  `keys_fn(logit_row)` gives the DeepSeekV3
+    selection keys (the float32 key definition is pinned separately)."""
+    T, H = len(x), len(x[0])
+    E = len(w1)
+    I = len(w1[0]) // 2
+    out = []
+    ids_all, w_all = [], []
+    for t in range(T):
+        row = [(-math.inf if v != v else float(v)) for v in logits[t]]
+        if method == 0:
+            ids = topk_bruteforce(row, top_k)
+            m = max(row[e] for e in ids)
+            ex = [math.exp(row[e] - m) for e in ids]
+            tot = math.fsum(ex)
+            wts = [v / tot for v in ex]
+        else:
+            keys, scores = keys_fn(row)
+            ids = topk_bruteforce(keys, top_k)
+            tot = math.fsum(scores[e] for e in ids)
+            wts = [scores[e] / tot * rsf for e in ids]
+        ids_all.append(ids)
+        w_all.append(wts)
+        weight_of = {e: wv for e, wv in zip(ids, wts)}
+        s = -1 if slot_idx is None else int(slot_idx[t])
+        use_lora = (s >= 0 and s < len(ranks) and ranks[s] > 0 and scalings[s] != 0.0)
+        terms = []
+        for e in range(E):                       # dense: every expert
+            g = [bf16_exact(dot(w1[e][n], x[t])) for n in range(2 * I)]
+            if use_lora:
+                r, sc = ranks[s], scalings[s]
+                u = [dot(A_gu[s][e][q], x[t]) for q in range(r)]
+                d = [bf16_exact(sc * dot([B_gu[s][e][n][q] for q in range(r)], u)) for n in range(2 * I)]
+            else:
+                d = [0.0] * (2 * I)
+            a = []
+            for i in range(I):
+                zg = g[i] + d[i]
+                a.append(bf16_exact(zg * sigmoid(zg) * (g[I + i] + d[I + i])))
+            y = [dot(w2[e][h], a) for h in range(H)]
+            if use_lora:
+                v = [dot(A_dn[s][e][q], a) for q in range(r)]
+                dd = [sc * dot([B_dn[s][e][h][q] for q in range(r)], v) for h in range(H)]
+            else:
+                dd = [0.0] * H
+            mask = 1.0 if e in weight_of else 0.0
+            wt = weight_of.get(e, 0.0)
+            terms.append([mask * wt * (y[h] + dd[h]) for h in range(H)])
+        out.append([bf16_exact(math.fsum(terms[e][h] for e in range(E))) for h in range(H)])
+    return out, ids_all, w_all

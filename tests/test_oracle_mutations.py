@@ -1,0 +1,130 @@
+"""Planted mistakes: each mutant copy of the oracle must fail at least one pin.
+
+A mutant is the oracle's source with one plausible slip substituted (a swapped
+operand, a dropped term, a wrong sign or index, a different tie rule), executed as
+a separate module on the CPU.  If some mutant passed every check below, the pins
+would not be strong enough to vouch for the oracle.
+"""
+import json
+import os
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import bruteforce as bf
+from routed_moe_expert_gb300 import workloads as wl
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "moe_lora_oracle.py")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_example.json")
+
+MUTATIONS = [
+    ("gate/up swapped", "silu(g[:, :I] + d[:, :I]) * (g[:, I:] + d[:, I:])",
+     "silu(g[:, I:] + d[:, I:]) * (g[:, :I] + d[:, :I])"),
+    ("delta dropped from gate", "silu(g[:, :I] + d[:, :I])", "silu(g[:, :I])"),
+    ("scaling dropped", "d[m] = round_bf16(sc * (u @ B.T))", "d[m] = round_bf16(u @ B.T)"),
+    ("down delta dropped", "contrib = w[ts, js][:, None] * (y + dd)", "contrib = w[ts, js][:, None] * y"),
+    ("routing weight dropped", "contrib = w[ts, js][:, None] * (y + dd)", "contrib = (y + dd)"),
+    ("down weight of the wrong expert", "W2 = _f64(w2[e])", "W2 = _f64(w2[(e + 1) % len(w2)])"),
+    ("silu sign", "return z / (1.0 + np.exp(-z))", "return z / (1.0 + np.exp(z))"),
+    ("rank tail read", "A = _f64(lora_A_gu[s, e])[:r]", "A = _f64(lora_A_gu[s, e])"),
+    ("tie to higher id", "order = np.argsort(-keys, axis=1, kind=\"stable\")",
+     "order = (keys.shape[1] - 1 - np.argsort(-keys[:, ::-1], axis=1, kind=\"stable\"))"),
+    ("softmax over all experts, not renormalised", "w = ex / ex.sum(axis=1, keepdims=True)",
+     "w = ex / np.exp(logit.astype(np.float64) - sel[:, :1]).sum(axis=1, keepdims=True)"),
+    ("deepseek bias ignored", "key = (s + bias[None, :]).astype(np.float32)", "key = s"),
+    ("deepseek rsf dropped", "* float(routed_scaling_factor)", "* 1.0"),
+    ("bf16 truncation", "q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)",
+     "q = np.ldexp(np.trunc(np.ldexp(x, 8 - e)), e - 8)"),
+    ("perm descending in expert", "perm = np.argsort(flat, kind=\"stable\").astype(np.int32)",
+     "perm = (flat.size - 1 - np.argsort(flat[::-1], kind=\"stable\")).astype(np.int32)"),
+    ("no-adapter token gets slot 0", "slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)",
+     "slots = np.maximum(np.asarray(slot_idx, dtype=np.int64), 0)"),
+]
+
+
+def _mutant(old, new):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+def np_(t):
+    return None if t is None else t.float().numpy() if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def _dense_check(orc, seed):
+    cfg = wl.LayerConfig("m", T=5, H=16, I=8, E=4, top_k=2, method=seed % 2,
+                         ranks=(2, 4), scalings=(2.0, 0.5), slot_mode="uniform_none10",
+                         bias_std=0.1, rsf=2.0)
+    inp = wl.make_inputs(cfg, seed=seed)
+    bias = np_(inp["correction_bias"])
+    res = orc.moe_lora_forward(np_(inp["hidden"]), np_(inp["router_logits"]), np_(inp["w1"]),
+                               np_(inp["w2"]), cfg.top_k, cfg.method, bias, cfg.rsf,
+                               np_(inp["lora_A_gu"]), np_(inp["lora_B_gu"]), np_(inp["lora_A_dn"]),
+                               np_(inp["lora_B_dn"]), inp["slot_idx"].numpy(), inp["ranks"], inp["scalings"])
+    from oracle import moe_lora_oracle as good
+
+    def keys_fn(row):
+        s = good.sigmoid_f32(np.asarray(row, np.float32))
+        return list((s + bias).astype(np.float32).astype(np.float64)), list(s.astype(np.float64))
+
+    L = lambda a: None if a is None else np.asarray(a, np.float64).tolist()
+    dense, ids, w = bf.dense_layer(L(np_(inp["hidden"])), L(np_(inp["router_logits"])), L(np_(inp["w1"])),
+                                   L(np_(inp["w2"])), cfg.top_k, cfg.method, rsf=cfg.rsf,
+                                   A_gu=L(np_(inp["lora_A_gu"])), B_gu=L(np_(inp["lora_B_gu"])),
+                                   A_dn=L(np_(inp["lora_A_dn"])), B_dn=L(np_(inp["lora_B_dn"])),
+                                   slot_idx=inp["slot_idx"].tolist(), ranks=inp["ranks"],
+                                   scalings=inp["scalings"], keys_fn=keys_fn)
+    ok = res["topk_ids"].tolist() == ids and np.array_equal(res["out"], np.array(dense))
+    ok = ok and np.allclose(res["topk_weights"], np.array(w), rtol=1e-12)
+    # permutation invariant: ascending expanded index inside each expert
+    off, perm = res["expert_offsets"], res["perm"]
+    ok = ok and all((np.diff(perm[off[e]:off[e + 1]]) > 0).all() for e in range(cfg.E))
+    return ok
+
+
+def _hand_check(orc):
+    G = json.load(open(GOLDEN))
+    for case in G["cases"]:
+        res = orc.moe_lora_forward(
+            np.array(G["hidden"], float), np.array(case["logits"], float), np.array(G["w1"], float),
+            np.array(G["w2"], float), case["top_k"], case["method"],
+            correction_bias=np.array(case.get("bias", [0, 0]), np.float32),
+            routed_scaling_factor=case.get("rsf", 1.0),
+            lora_A_gu=np.array(G["lora_A_gu"], float), lora_B_gu=np.array(G["lora_B_gu"], float),
+            lora_A_dn=np.array(G["lora_A_dn"], float), lora_B_dn=np.array(G["lora_B_dn"], float),
+            slot_idx=np.array(case.get("slot_idx", [0, 0])), ranks=G["ranks"], scalings=G["scalings"],
+            lora_off=not case["lora"])
+        if res["topk_ids"].tolist() != case["topk_ids"] or not np.array_equal(res["out"], np.array(case["out"], float)):
+            return False
+    return True
+
+
+def _bf16_check(orc):
+    vals = np.random.default_rng(0).standard_normal(2000).astype(np.float32)
+    return np.array_equal(orc.round_bf16(vals.astype(np.float64)),
+                          torch.from_numpy(vals).to(torch.bfloat16).double().numpy())
+
+
+def test_unmutated_oracle_passes_the_checks():
+    from oracle import moe_lora_oracle as good
+    assert all(_dense_check(good, s) for s in range(4))
+    assert _hand_check(good) and _bf16_check(good)
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutant_is_caught(name, old, new):
+    m = _mutant(old, new)
+    results = []
+    for check in (lambda: _bf16_check(m), lambda: _hand_check(m),
+                  *[(lambda s=s: _dense_check(m, s)) for s in range(4)]):
+        try:
+            results.append(bool(check()))
+        except Exception:
+            results.append(False)
+    assert not all(results), f"mutant '{name}' passed every pin"
