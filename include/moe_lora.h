@@ -1,0 +1,181 @@
+/*
+ * moe_lora.h -- C ABI of the routed MoE expert layer with per-expert LoRA (bf16, sm_103a).
+ *
+ * The layer (sglang PR #28466 "[LoRA] bf16 MoE-LoRA for trtllm backend with two-stream
+ * overlap + routing opts", section "Files changed", launcher row, and section 1 flow (A);
+ * vLLM API page "vllm.model_executor.layers.fused_moe.experts.trtllm_lora_moe",
+ * TrtLlmBf16LoRAExperts.apply):
+ *
+ *   route      top-k experts per token from the router logits (Renormalize or DeepSeekV3)
+ *   permute    gather token rows into expert-sorted order
+ *   gate_up    per expert  g = x . w1[e]^T                    (N = 2I, bf16 out)
+ *   LoRA gu    d = scaling[s] * B_gu[s,e] (A_gu[s,e] x)       (bf16, NOT routing-weighted)
+ *   activation a = silu(g_gate + d_gate) * (g_up + d_up)        (bf16)
+ *   down       y = a . w2[e]^T, plus dd = scaling[s] * B_dn[s,e] (A_dn[s,e] a)
+ *   finalize   out[t] = sum_j w[t,j] * (y_j + dd_j)             (bf16)
+ *
+ * Conventions for every call below:
+ *   - Pointers are DEVICE pointers unless the name starts with h_ (host memory).
+ *   - bf16 tensors are raw bfloat16 bit patterns (uint16_t), row-major, densely packed,
+ *     16-byte aligned.  int32/float tensors are 4-byte aligned, densely packed.
+ *   - The caller owns every buffer, including the workspace.  No call allocates device
+ *     memory after moe_lora_create, so moe_lora_route/permute/forward can be captured
+ *     in a CUDA graph on `stream` (the side stream is forked from and joined back to it).
+ *   - Calls are asynchronous on `stream`; they return after enqueueing work.
+ *   - Host-side argument checks run before any launch: a bad argument returns
+ *     MOE_LORA_ERR_INVALID_ARG (or MOE_LORA_ERR_UNSUPPORTED) and launches nothing.
+ *   - Conditions only the device can see (a slot index outside [-1, S), a bounded wait
+ *     that ran out) are recorded in a status word inside the workspace and reported by
+ *     moe_lora_check_status; the kernels never trap.
+ *   - A handle serves one stream at a time (its side stream and events are shared).
+ */
+#ifndef MOE_LORA_H
+#define MOE_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_lora_bf16;              /* raw bfloat16 bits */
+typedef struct CUstream_st* moe_lora_stream; /* identical to cudaStream_t */
+typedef struct moe_lora_handle moe_lora_handle;
+
+typedef enum {
+  MOE_LORA_OK = 0,
+  MOE_LORA_ERR_INVALID_ARG = 1,        /* shape, pointer or value rejected on the host */
+  MOE_LORA_ERR_UNSUPPORTED = 2,        /* valid request outside what the kernels cover */
+  MOE_LORA_ERR_WORKSPACE_TOO_SMALL = 3,
+  MOE_LORA_ERR_CUDA = 4,               /* a CUDA runtime call failed (see moe_lora_last_cuda_error) */
+  MOE_LORA_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out */
+  MOE_LORA_ERR_DEVICE_CHECK = 6        /* device saw a bad value (slot index outside [-1, S)) */
+} moe_lora_status;
+
+/* Routing methods (vLLM page, TrtLlmBf16LoRAExperts._supports_routing_method). */
+typedef enum {
+  MOE_LORA_ROUTE_RENORMALIZE = 0,      /* weights = softmax over the k selected logits */
+  MOE_LORA_ROUTE_DEEPSEEK_V3 = 1       /* s = sigmoid(logit); select on s + bias; w = s/sum(s)*rsf */
+} moe_lora_routing;
+
+/* moe_lora_args.flags */
+#define MOE_LORA_FLAG_LORA_OFF            1u /* base layer only: no LoRA work at all */
+#define MOE_LORA_FLAG_FORCE_SINGLE_STREAM 2u /* never fork the LoRA chain to the side stream */
+#define MOE_LORA_FLAG_FORCE_TWO_STREAM    4u /* fork even above 256 tokens */
+
+/* Stages that moe_lora_args.prof_events can bracket (two events per stage). */
+enum {
+  MOE_LORA_STAGE_ROUTE = 0, MOE_LORA_STAGE_PERMUTE = 1, MOE_LORA_STAGE_GATE_UP_GEMM = 2,
+  MOE_LORA_STAGE_LORA_GATE_UP = 3, MOE_LORA_STAGE_ACTIVATION = 4, MOE_LORA_STAGE_DOWN_GEMM = 5,
+  MOE_LORA_STAGE_LORA_DOWN = 6, MOE_LORA_STAGE_FINALIZE = 7, MOE_LORA_NUM_STAGES = 8
+};
+
+/* Sizes that determine the workspace.  S = resident LoRA slots (0 allowed), R = max rank. */
+typedef struct {
+  int T, H, I, E, top_k, S, R;
+} moe_lora_shape;
+
+/* Arguments of moe_lora_forward. */
+typedef struct {
+  int T;                 /* tokens (0 allowed: nothing is launched)                        */
+  int H;                 /* hidden size, multiple of 64, <= 16384                          */
+  int I;                 /* per-expert intermediate size, multiple of 64, <= 16384         */
+  int E;                 /* experts, 1..1024                                               */
+  int top_k;             /* 1..min(E, 32)                                                  */
+  int S;                 /* resident LoRA slots, 0..64                                     */
+  int R;                 /* max LoRA rank (leading size of the stacked adapters), 0..128   */
+  int routing_method;    /* moe_lora_routing                                               */
+  float routed_scaling_factor; /* DeepSeekV3 only (applied once, in the routing weights)   */
+  int n_group, topk_group;     /* DeepSeekV3 grouping; only 1/1 is supported                */
+  const moe_lora_bf16* hidden;        /* [T, H]                                            */
+  const moe_lora_bf16* router_logits; /* [T, E]                                            */
+  const float* correction_bias;       /* [E], DeepSeekV3 only, else NULL                   */
+  const moe_lora_bf16* w1;            /* [E, 2I, H]: rows [0,I) gate, [I,2I) up            */
+  const moe_lora_bf16* w2;            /* [E, H, I]                                         */
+  const moe_lora_bf16* lora_A_gu;     /* [S, E, R, H]  rows r < ranks[s] are read          */
+  const moe_lora_bf16* lora_B_gu;     /* [S, E, 2I, R] cols r < ranks[s] are read          */
+  const moe_lora_bf16* lora_A_dn;     /* [S, E, R, I]                                      */
+  const moe_lora_bf16* lora_B_dn;     /* [S, E, H, R]                                      */
+  const int32_t* slot_idx;            /* [T], slot of each token, -1 = no adapter          */
+  const int32_t* h_ranks;             /* [S] host, 0 <= ranks[s] <= R                      */
+  const float* h_scalings;            /* [S] host, 0 disables the slot                     */
+  unsigned flags;                     /* MOE_LORA_FLAG_*                                   */
+  /* Optional device outputs (NULL: kept in the workspace). */
+  int32_t* topk_ids;                  /* [T, top_k]                                        */
+  float* topk_weights;                /* [T, top_k]                                        */
+  int32_t* expert_offsets;            /* [E + 1]                                           */
+  int32_t* perm;                      /* [T*top_k] permuted position -> expanded index     */
+  int32_t* inv_perm;                  /* [T*top_k] expanded index -> permuted position     */
+  /* Optional profiling: 2*MOE_LORA_NUM_STAGES cudaEvent_t handles (entries may be NULL);
+     events 2i and 2i+1 are recorded around stage i on the stream that runs it. */
+  void* const* prof_events;
+} moe_lora_args;
+
+/* Create a handle on `device`: queries the device, creates the LoRA side stream and the
+   fork/join events, resolves the tensor-map encoder.  Call OUTSIDE stream capture.
+   Errors: MOE_LORA_ERR_INVALID_ARG (null h), MOE_LORA_ERR_UNSUPPORTED (not sm_103),
+   MOE_LORA_ERR_CUDA. */
+moe_lora_status moe_lora_create(moe_lora_handle** h, int device);
+
+/* Destroy a handle (synchronizes its side stream first).  NULL is accepted. */
+moe_lora_status moe_lora_destroy(moe_lora_handle* h);
+
+/* Static text for a status code. */
+const char* moe_lora_status_string(moe_lora_status s);
+
+/* Text of the last CUDA error seen by this library on the calling thread ("" if none). */
+const char* moe_lora_last_cuda_error(void);
+
+/* Host-only: bytes of workspace moe_lora_forward needs for `shape`.  No GPU needed.
+   Errors: MOE_LORA_ERR_INVALID_ARG. */
+moe_lora_status moe_lora_workspace_size(const moe_lora_shape* shape, size_t* bytes);
+
+/* Host-only: the host-side argument checks of moe_lora_forward, without launching.
+   Returns MOE_LORA_OK or the code forward would return. */
+moe_lora_status moe_lora_validate(const moe_lora_args* a);
+
+/* Routing + expert alignment in one launch (sglang PR #27329 "Experimental fast LoRA
+   path", Optimizations: "topk + FlashInfer routed-pack in a single launch", "JIT
+   MoE-align"; vLLM page, _unpermute_activation docstring for the expanded index).
+   Writes topk_ids/topk_weights [T, top_k] in selection order (higher key first, lower
+   expert id first on ties), expert_offsets [E+1] (exclusive prefix of per-expert pair
+   counts), perm [T*top_k] (pairs grouped by expert, ascending expanded index
+   p = t*top_k + j inside an expert) and inv_perm (its inverse).  correction_bias: [E]
+   for DeepSeekV3, else NULL.  `workspace` must hold moe_lora_workspace_size() bytes
+   for this T, E, top_k (H, I, S, R may be 0 there).  Errors: INVALID_ARG, UNSUPPORTED
+   (n_group/topk_group != 1), WORKSPACE_TOO_SMALL, CUDA. */
+moe_lora_status moe_lora_route(moe_lora_handle* h, const moe_lora_bf16* router_logits,
+                               const float* correction_bias, int T, int E, int top_k,
+                               int routing_method, float routed_scaling_factor,
+                               int n_group, int topk_group,
+                               int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                               int32_t* perm, int32_t* inv_perm,
+                               void* workspace, size_t workspace_bytes, moe_lora_stream stream);
+
+/* Token permute (sglang PR #28466, Files changed, launcher row: "moe::dev::permute (bf16
+   gather)"): permuted[q, :] = hidden[perm[q] / top_k, :] for q < T*top_k.
+   H multiple of 8.  Errors: INVALID_ARG, CUDA. */
+moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden,
+                                 const int32_t* perm, int T, int H, int top_k,
+                                 moe_lora_bf16* permuted, moe_lora_stream stream);
+
+/* The whole layer: out [T, H] bf16.  Two-stream (LoRA gate_up chain on the side stream,
+   joined before the activation) when T <= 256 unless FORCE_SINGLE_STREAM (sglang PR
+   #28466, "Which diagram applies when": decode-shaped batches only).  `workspace` holds
+   moe_lora_workspace_size() bytes; its contents on entry do not matter.
+   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out,
+                                 void* workspace, size_t workspace_bytes, moe_lora_stream stream);
+
+/* Synchronizes `stream`, then reads the device status word the last route/forward on this
+   workspace left: MOE_LORA_OK, MOE_LORA_ERR_TIMEOUT or MOE_LORA_ERR_DEVICE_CHECK.
+   *detail (optional) receives the raw word (code in the low byte, where in the high bytes). */
+moe_lora_status moe_lora_check_status(const void* workspace, moe_lora_stream stream,
+                                      uint32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LORA_H */
