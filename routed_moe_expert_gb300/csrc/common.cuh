@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 #define MLDEV __device__ __forceinline__
 
 namespace mlk {
@@ -19,12 +21,6 @@ enum : uint32_t {
   kDevTimeout = 5,      // == MOE_LORA_ERR_TIMEOUT
   kDevBadSlot = 6,      // == MOE_LORA_ERR_DEVICE_CHECK
 };
-enum : uint32_t {      // "where" tags (bits 8..)
-  kWhereRouteBarrier = 1, kWhereGemmProducer = 2, kWhereGemmMma = 3, kWhereGemmEpilogue = 4,
-  kWhereLoraShrinkGu = 5, kWhereLoraExpandGu = 6, kWhereLoraShrinkDn = 7, kWhereFinalize = 8,
-  kWhereGemmDrain = 9,
-};
-
 MLDEV void record_status(uint32_t* status, uint32_t code, uint32_t where) {
   if (status) atomicCAS(status, 0u, code | (where << 8));
 }

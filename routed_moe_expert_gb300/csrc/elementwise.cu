@@ -1,0 +1,153 @@
+// Memory-bound stages of the routed MoE-LoRA layer: token permute, SwiGLU activation
+// with the gate_up LoRA delta, and the weighted top-k finalize with the down LoRA.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mlk {
+
+// ---------------------------------------------------------------------------------
+// permute: xp[q, :] = x[perm[q] / k, :]   (sglang PR #28466, Files changed, launcher
+// row: "moe::dev::permute (bf16 gather)").  One warp per permuted row, 16-byte vectors.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+                                                      int P, int k, int H8, uint4* __restrict__ xp) {
+  const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (q >= P) return;
+  const int t = perm[q] / k;
+  const uint4* src = x + static_cast<size_t>(t) * H8;
+  uint4* dst = xp + static_cast<size_t>(q) * H8;
+  for (int v = threadIdx.x & 31; v < H8; v += 32) dst[v] = __ldg(src + v);
+}
+
+cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
+                           __nv_bfloat16* xp, cudaStream_t stream) {
+  if (P == 0) return cudaSuccess;
+  permute_kernel<<<(P + 7) / 8, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, P, k, H / 8,
+                                                  reinterpret_cast<uint4*>(xp));
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// activation: a[q, i] = bf16( silu(g_gate + d_gate) * (g_up + d_up) )
+// (sglang PR #28466, launcher row: "moe::dev::activation (de-interleaves on read, adds
+// gate_up_lora_delta pre-SwiGLU, captures activation_lora_input, bf16 out)").
+// g is the gated-interleaved GEMM output: row q, block b of 128 columns = 64 gate
+// features [64b, 64b+64) then the matching 64 up features.  d (or null) is the LoRA
+// delta in the logical [gate | up] order.  The output a is also the down-LoRA input.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) activation_kernel(const __nv_bfloat16* __restrict__ g,
+                                                         const __nv_bfloat16* __restrict__ d, int P, int I,
+                                                         __nv_bfloat16* __restrict__ a) {
+  const int I8 = I >> 3;
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(P) * I8) return;
+  const int q = static_cast<int>(idx / I8);
+  const int i0 = static_cast<int>(idx % I8) * 8;
+  const int blk = i0 >> 6, j = i0 & 63;
+  const size_t row = static_cast<size_t>(q) * 2 * I;
+  float gf[8], uf[8];
+  unpack8(*reinterpret_cast<const uint4*>(g + row + blk * 128 + j), gf);
+  unpack8(*reinterpret_cast<const uint4*>(g + row + blk * 128 + 64 + j), uf);
+  if (d != nullptr) {
+    float dg[8], du[8];
+    unpack8(*reinterpret_cast<const uint4*>(d + row + i0), dg);
+    unpack8(*reinterpret_cast<const uint4*>(d + row + I + i0), du);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      gf[i] += dg[i];
+      uf[i] += du[i];
+    }
+  }
+  float out[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = gf[i] / (1.0f + expf(-gf[i])) * uf[i];
+  *reinterpret_cast<uint4*>(a + static_cast<size_t>(q) * I + i0) = pack8(out);
+}
+
+cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
+                              __nv_bfloat16* a, cudaStream_t stream) {
+  const size_t n = static_cast<size_t>(P) * (I / 8);
+  if (n == 0) return cudaSuccess;
+  activation_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(g, d, P, I, a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// finalize: out[t, h] = bf16( sum_{j<k} w[t,j] * ( y[q_j, h] + scaling_s *
+//                              sum_{r<rank_s} B_dn[s, e_j, h, r] * v[q_j, r] ) )
+// with q_j = inv[t*k + j], fixed j order (vLLM API page "fused_moe/experts/
+// trtllm_lora_moe", _finalize_with_w2_lora: routing-weighted sum of the permuted base
+// rows over top_k plus the routing-weighted down-LoRA delta; the down expand of sglang
+// PR #28466's merged_experts_fused_moe_lora_add(down) is fused in here).
+// One CTA per token; each thread owns 8 consecutive h.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeParams p) {
+  __shared__ int q_s[kMaxTopK], e_s[kMaxTopK];
+  __shared__ float w_s[kMaxTopK];
+  __shared__ float v_s[kMaxTopK * kMaxRank];
+  __shared__ int lora_s;
+  const int t = blockIdx.x, k = p.k, tid = threadIdx.x;
+  const LoraSlots& L = p.slots;
+  if (tid == 0) {
+    int use = 0;
+    if (p.v != nullptr) {
+      const int s = p.slot_idx[t];
+      if (s < -1 || s >= L.S) {
+        record_status(p.status, kDevBadSlot, kWhereFinalize);
+      } else if (s >= 0 && L.ranks[s] > 0 && L.scal[s] != 0.0f) {
+        use = s + 1;
+      }
+    }
+    lora_s = use;
+  }
+  if (tid < k) {
+    const size_t pp = static_cast<size_t>(t) * k + tid;
+    q_s[tid] = p.inv[pp];
+    e_s[tid] = p.ids[pp];
+    w_s[tid] = p.weights[pp];
+  }
+  __syncthreads();
+  const int s = lora_s - 1;
+  const int rank = s >= 0 ? L.ranks[s] : 0;
+  if (s >= 0) {
+    for (int i = tid; i < k * rank; i += blockDim.x) {
+      const int j = i / rank, r = i - j * rank;
+      v_s[j * kMaxRank + r] = p.v[static_cast<size_t>(q_s[j]) * L.R + r];
+    }
+  }
+  __syncthreads();
+  const float sc = s >= 0 ? L.scal[s] : 0.0f;
+  const int H8 = p.H >> 3;
+  for (int h8 = tid; h8 < H8; h8 += blockDim.x) {
+    const int h0 = h8 * 8;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float yv[8];
+      unpack8(*reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(q_s[j]) * p.H + h0), yv);
+      if (s >= 0) {
+        const __nv_bfloat16* Bb = p.B + ((static_cast<size_t>(s) * L.E + e_s[j]) * p.H + h0) * L.R;
+        const float* vj = v_s + j * kMaxRank;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const __nv_bfloat16* Brow = Bb + static_cast<size_t>(i) * L.R;
+          float dd = 0.0f;
+          for (int r = 0; r < rank; ++r) dd += bf2f(Brow[r]) * vj[r];
+          yv[i] += sc * dd;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += w_s[j] * yv[i];
+    }
+    *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.H + h0) = pack8(acc);
+  }
+}
+
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream) {
+  if (p.T == 0) return cudaSuccess;
+  finalize_kernel<<<p.T, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mlk

@@ -1,0 +1,286 @@
+// Grouped (per-expert) GEMM on the 5th-generation tensor cores: TMA -> shared memory
+// -> tcgen05.mma -> TMEM -> registers -> global.
+//
+// For every expert e and its routed pairs q in [offsets[e], offsets[e+1]):
+//     out[q, col] = sum_k X[q, k] * W[e*N + row(col), k]
+// which is the gate_up GEMM (W = w1, X = permuted hidden, N = 2I, K = H) and the down
+// GEMM (W = w2, X = activation, N = H, K = I) of the routed MoE layer (sglang PR #28466
+// "bf16 MoE-LoRA for trtllm backend", Files changed, launcher row: "gate_up as raw
+// Gemm2::Runner ... K=hidden, N=2*inter, gated-interleaved out", "down Gemm2::Runner
+// (K=inter, N=hidden)").
+//
+// Orientation: the weights are the MMA "A" operand (M = 128 weight rows per tile) and
+// the expert's tokens are "B" (N = BN token columns), so a decode expert with a handful
+// of tokens still streams full 128-row weight tiles (BN as small as 16).  The TMEM
+// accumulator is [128 lanes = weight rows] x [BN columns = tokens].
+//
+// Persistent CTAs (one per SM) walk a static round-robin list of tiles (e, n-tile,
+// token-tile), token-tile fastest so CTAs that run together share a weight tile in L2.
+// Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warps 2-5 =
+// epilogue (each owns one 32-lane quarter of TMEM).  Two TMEM accumulators let the
+// epilogue of one tile overlap the MMAs of the next.
+//
+// gated = 1 (gate_up): the 128 A rows of n-tile n are the 64 gate rows [64n, 64n+64)
+// and the 64 up rows [N/2 + 64n, ...), so each tile holds matching gate/up features; the
+// output row is stored "gated-interleaved": column 128n + j is gate feature 64n + j for
+// j < 64 and up feature 64n + j - 64 for j >= 64.
+//
+// Every mbarrier wait is bounded (2 s); a timeout records MOE_LORA_ERR_TIMEOUT, raises a
+// CTA-wide abort flag, drains the copies already issued and frees TMEM before returning.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mlk {
+
+constexpr int kGemmThreads = 192;
+constexpr int kAByte = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle row each)
+constexpr int kMaxStages = 16;
+
+int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
+
+int gemm_smem_bytes(int bn, int stages, int E) {
+  // 1 KB alignment slack, stage buffers, barriers, tmem slot + abort flag, schedule
+  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+
+  constexpr uint32_t A_BYTES = kAByte;
+  constexpr uint32_t STAGE = A_BYTES + BN * 128;
+  constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  const int S = p.stages;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;       // [2]
+  uint64_t* tempty = tfull + 2;      // [2]
+  uint64_t* drain = tempty + 2;      // [1], used only after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);   // [E + 1]
+  int* seg = tile_start + (p.E + 1);                         // offsets copy [E + 1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int NT = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);   // 128-row weight tiles per expert
+  const int KB = p.K >> 6;                                    // 64-wide K blocks
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 128);
+    mbar_init(&tempty[1], 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmap_w);
+    tma_prefetch_desc(&p.tmap_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {   // tile schedule: tile_start[e] = sum over e' < e of ceil(M_e'/BN) * NT
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      int cnt = 0;
+      if (e < E) {
+        const int lo = p.offsets[e], hi = p.offsets[e + 1];
+        seg[e] = lo;
+        if (e == E - 1) seg[E] = hi;
+        cnt = ((hi - lo + BN - 1) / BN) * NT;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (e < E) tile_start[e] = carry + incl - cnt;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[E];
+
+  auto decode = [&](int tile, int& e, int& nt, int& qt) {
+    int lo = 0, hi = E - 1;   // last expert with tile_start <= tile (empty experts skipped)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int local = tile - tile_start[e];
+    const int nq = (seg[e + 1] - seg[e] + BN - 1) / BN;
+    nt = local / nq;
+    qt = local - nt * nq;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {   // ---------------------------------------------- TMA producer
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0;       // stages with a load in flight, and their parity
+      uint32_t issued_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int e, nt, qt;
+        decode(tile, e, nt, qt);
+        int wr0, wr1;
+        if (p.gated) {
+          wr0 = e * p.N + nt * 64;
+          wr1 = wr0 + (p.N >> 1);
+        } else {
+          wr0 = e * p.N + nt * 128;
+          wr1 = wr0 + 64;
+        }
+        const int xr = seg[e] + qt * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + stage * STAGE;
+          mbar_arrive_expect_tx(&full[stage], STAGE);
+          tma_load_2d(a, &p.tmap_w, &full[stage], kb * 64, wr0, pol_w);
+          tma_load_2d(a + 8192, &p.tmap_w, &full[stage], kb * 64, wr1, pol_w);
+          tma_load_2d(a + A_BYTES, &p.tmap_x, &full[stage], kb * 64, xr, pol_x);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {   // drain: let every issued copy land before the CTA exits
+        for (int s = 0; s < S; ++s)
+          if ((issued_mask >> s) & 1u) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {   // ---------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWhereGemmMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE);
+          const uint64_t ad = sw128_kmajor_desc(a_addr);
+          const uint64_t bd = sw128_kmajor_desc(a_addr + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+    }
+  } else {   // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;   // weight row inside the tile == TMEM lane
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, qt;
+      decode(tile, e, nt, qt);
+      if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+      tc_fence_after();
+      const int col = nt * 128 + row;
+      const int q0 = seg[e] + qt * BN;
+      const int nvalid = min(BN, seg[e + 1] - q0);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
+        uint32_t r[16];
+        tmem_ld_x16(taddr + c, r);
+        tmem_ld_wait();
+        if (col < p.N) {
+          __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * p.N + col;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c + j < nvalid) o[static_cast<size_t>(j) * p.N] = f2bf(__uint_as_float(r[j]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {   // let the MMAs lane 0 already issued finish before TMEM is released
+      if (lane == 0) {
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int BN>
+static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream) {
+  const int smem = gemm_smem_bytes(BN, p.stages, p.E);
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  grouped_gemm_kernel<BN><<<grid, kGemmThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream) {
+  if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+  switch (bn) {
+    case 16: return launch_bn<16>(p, grid, stream);
+    case 32: return launch_bn<32>(p, grid, stream);
+    case 64: return launch_bn<64>(p, grid, stream);
+    case 128: return launch_bn<128>(p, grid, stream);
+    case 256: return launch_bn<256>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mlk

@@ -14,6 +14,12 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxRouteCtas = 256;
 
+// "where" tags of the device status word (bits 8 and up; the low byte is the code)
+enum : uint32_t {
+  kWhereRouteBarrier = 1, kWhereGemmProducer = 2, kWhereGemmMma = 3, kWhereGemmEpilogue = 4,
+  kWhereLoraShrinkGu = 5, kWhereLoraExpandGu = 6, kWhereLoraShrinkDn = 7, kWhereFinalize = 8,
+};
+
 // ---------------------------------------------------------------- routing + align
 struct RouteParams {
   const __nv_bfloat16* logits;   // [T, E]

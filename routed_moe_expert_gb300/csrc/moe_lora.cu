@@ -1,0 +1,514 @@
+// Host side of the C ABI declared in include/moe_lora.h: argument checks, workspace
+// layout, tensor maps, stream fork/join and the launch sequence of the layer.
+//
+// Launch sequence of moe_lora_forward (sglang PR #28466 "bf16 MoE-LoRA for trtllm
+// backend", section 1 flows (A) single-stream and (B) two-stream):
+//   main: memset(status) -> route_align -> [fork] -> permute -> gate_up GEMM
+//         -> [join on the LoRA-ready event] -> activation -> down GEMM
+//         -> down-LoRA shrink -> finalize (+ down-LoRA expand)
+//   side: [wait fork] -> gate_up LoRA shrink -> expand -> [record ready]
+// Every buffer the side stream touches lives in the caller's workspace, which exists
+// before the fork, so nothing is allocated while a graph may be capturing (the
+// multi-slot replay bug of sglang PR #28091, Motivation 3, cannot arise).
+#include "../../include/moe_lora.h"
+#include "kernels.h"
+
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+using namespace mlk;
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+moe_lora_status cuda_fail(cudaError_t err, const char* what) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", what, cudaGetErrorString(err));
+  return MOE_LORA_ERR_CUDA;
+}
+
+#define ML_CUDA(call, what)                         \
+  do {                                              \
+    cudaError_t _e = (call);                        \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout (all offsets 256-byte aligned).  y (down GEMM output) reuses the
+// permuted-hidden buffer, which is dead once the gate_up GEMM has run.
+struct Layout {
+  size_t header, ids, wts, offsets, perm, inv, hist, base, total;
+  size_t xp, g, d, u, a, v;
+  size_t bytes;
+};
+
+Layout layout_for(int T, int H, int I, int E, int k, int R) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t o = off;
+    off += align_up(n, 256);
+    return o;
+  };
+  const size_t P = static_cast<size_t>(T) * k;
+  L.header = take(256);
+  L.ids = take(P * 4);
+  L.wts = take(P * 4);
+  L.offsets = take((static_cast<size_t>(E) + 1) * 4);
+  L.perm = take(P * 4);
+  L.inv = take(P * 4);
+  L.hist = take(static_cast<size_t>(kMaxRouteCtas) * E * 4);
+  L.base = take(static_cast<size_t>(kMaxRouteCtas) * E * 4);
+  L.total = take(static_cast<size_t>(E) * 4);
+  L.xp = take(P * H * 2);
+  L.g = take(P * 2 * I * 2);
+  L.d = take(R > 0 ? P * 2 * I * 2 : 0);
+  L.u = take(P * R * 4);
+  L.a = take(P * I * 2);
+  L.v = take(P * R * 4);
+  L.bytes = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+moe_lora_status check_routing_args(int T, int E, int top_k, int method, const void* logits, const float* bias,
+                                   int n_group, int topk_group) {
+  if (T < 0 || E < 1 || E > kMaxExperts) return MOE_LORA_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > E || top_k > kMaxTopK) return MOE_LORA_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * top_k > 0x7fffffffLL) return MOE_LORA_ERR_INVALID_ARG;
+  if (method != MOE_LORA_ROUTE_RENORMALIZE && method != MOE_LORA_ROUTE_DEEPSEEK_V3) return MOE_LORA_ERR_INVALID_ARG;
+  if (T > 0 && logits == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (method == MOE_LORA_ROUTE_DEEPSEEK_V3 && bias == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (bias != nullptr && !aligned4(bias)) return MOE_LORA_ERR_INVALID_ARG;
+  if (n_group > 1 || topk_group > 1) return MOE_LORA_ERR_UNSUPPORTED;
+  if (n_group < 0 || topk_group < 0) return MOE_LORA_ERR_INVALID_ARG;
+  return MOE_LORA_OK;
+}
+
+bool lora_active(const moe_lora_args* a) {
+  if ((a->flags & MOE_LORA_FLAG_LORA_OFF) || a->S == 0) return false;
+  for (int s = 0; s < a->S; ++s)
+    if (a->h_ranks[s] > 0 && a->h_scalings[s] != 0.0f) return true;
+  return false;
+}
+
+}  // namespace
+
+struct moe_lora_handle {
+  int device = 0;
+  int num_sms = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_ready = nullptr;
+  EncodeTiledFn encode = nullptr;
+  int coop_ctas[kMaxExperts + 1];   // cache of route_max_coop_ctas by E (0 = unknown)
+};
+
+extern "C" {
+
+const char* moe_lora_status_string(moe_lora_status s) {
+  switch (s) {
+    case MOE_LORA_OK: return "ok";
+    case MOE_LORA_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_LORA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_LORA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_LORA_ERR_CUDA: return "CUDA error";
+    case MOE_LORA_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_LORA_ERR_DEVICE_CHECK: return "device-side check failed (slot index outside [-1, S))";
+  }
+  return "unknown status";
+}
+
+const char* moe_lora_last_cuda_error(void) { return g_last_cuda_error; }
+
+moe_lora_status moe_lora_workspace_size(const moe_lora_shape* s, size_t* bytes) {
+  if (s == nullptr || bytes == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (s->T < 0 || s->H < 0 || s->I < 0 || s->E < 1 || s->E > kMaxExperts || s->top_k < 1 || s->top_k > s->E ||
+      s->S < 0 || s->R < 0 || s->R > kMaxRank)
+    return MOE_LORA_ERR_INVALID_ARG;
+  *bytes = layout_for(s->T, s->H, s->I, s->E, s->top_k, s->S > 0 ? s->R : 0).bytes;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_validate(const moe_lora_args* a) {
+  if (a == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  moe_lora_status st = check_routing_args(a->T, a->E, a->top_k, a->routing_method, a->router_logits,
+                                          a->correction_bias, a->n_group, a->topk_group);
+  if (st != MOE_LORA_OK) return st;
+  if (a->H < 64 || a->H > 16384 || a->H % 64 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (a->I < 64 || a->I > 16384 || a->I % 64 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (a->S < 0 || a->S > kMaxSlots || a->R < 0 || a->R > kMaxRank) return MOE_LORA_ERR_INVALID_ARG;
+  if (static_cast<long long>(a->E) * 2 * a->I > 0x7fffffffLL || static_cast<long long>(a->E) * a->H > 0x7fffffffLL)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (a->T == 0) return MOE_LORA_OK;
+  if (a->hidden == nullptr || a->w1 == nullptr || a->w2 == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (!aligned16(a->hidden) || !aligned16(a->w1) || !aligned16(a->w2)) return MOE_LORA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->router_logits) & 1u) != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (!(a->flags & MOE_LORA_FLAG_LORA_OFF) && a->S > 0) {
+    if (a->h_ranks == nullptr || a->h_scalings == nullptr || a->slot_idx == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+    for (int s = 0; s < a->S; ++s) {
+      if (a->h_ranks[s] < 0 || a->h_ranks[s] > a->R) return MOE_LORA_ERR_INVALID_ARG;
+      if (a->h_scalings[s] != a->h_scalings[s]) return MOE_LORA_ERR_INVALID_ARG;   // NaN scaling
+    }
+    if (lora_active(a)) {
+      if (a->lora_A_gu == nullptr || a->lora_B_gu == nullptr || a->lora_A_dn == nullptr || a->lora_B_dn == nullptr)
+        return MOE_LORA_ERR_INVALID_ARG;
+      if (!aligned16(a->lora_A_gu) || !aligned16(a->lora_A_dn) || !aligned4(a->slot_idx))
+        return MOE_LORA_ERR_INVALID_ARG;
+      if ((reinterpret_cast<uintptr_t>(a->lora_B_gu) & 1u) || (reinterpret_cast<uintptr_t>(a->lora_B_dn) & 1u))
+        return MOE_LORA_ERR_INVALID_ARG;
+    }
+  }
+  const void* opt[] = {a->topk_ids, a->topk_weights, a->expert_offsets, a->perm, a->inv_perm};
+  for (const void* o : opt)
+    if (o != nullptr && !aligned4(o)) return MOE_LORA_ERR_INVALID_ARG;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_create(moe_lora_handle** out, int device) {
+  if (out == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  ML_CUDA(cudaGetDeviceCount(&count), "cudaGetDeviceCount");
+  if (device < 0 || device >= count) return MOE_LORA_ERR_INVALID_ARG;
+  int major = 0, minor = 0, sms = 0;
+  ML_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device), "cudaDeviceGetAttribute");
+  ML_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device), "cudaDeviceGetAttribute");
+  ML_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device), "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3) return MOE_LORA_ERR_UNSUPPORTED;   // built for sm_103a only
+  int prev = 0;
+  ML_CUDA(cudaGetDevice(&prev), "cudaGetDevice");
+  ML_CUDA(cudaSetDevice(device), "cudaSetDevice");
+  moe_lora_handle* h = new moe_lora_handle();
+  h->device = device;
+  h->num_sms = sms;
+  std::memset(h->coop_ctas, 0, sizeof(h->coop_ctas));
+  cudaError_t err = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&h->ev_ready, cudaEventDisableTiming);
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (err == cudaSuccess)
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  cudaSetDevice(prev);
+  if (err != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    moe_lora_destroy(h);
+    return err != cudaSuccess ? cuda_fail(err, "moe_lora_create") : MOE_LORA_ERR_CUDA;
+  }
+  h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  *out = h;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_destroy(moe_lora_handle* h) {
+  if (h == nullptr) return MOE_LORA_OK;
+  if (h->side) {
+    cudaStreamSynchronize(h->side);
+    cudaStreamDestroy(h->side);
+  }
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_ready) cudaEventDestroy(h->ev_ready);
+  delete h;
+  return MOE_LORA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, const float* bias, int T, int E,
+                              int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
+                              int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+  if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
+  int grid = (T + 15) / 16;
+  if (grid > h->coop_ctas[E]) grid = h->coop_ctas[E];
+  if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
+  if (grid < 1) grid = 1;
+  RouteParams p;
+  p.logits = reinterpret_cast<const __nv_bfloat16*>(logits);
+  p.bias = bias;
+  p.T = T;
+  p.E = E;
+  p.k = k;
+  p.method = method;
+  p.rsf = rsf;
+  p.tokens_per_cta = (T + grid - 1) / grid;
+  p.ids = ids;
+  p.weights = wts;
+  p.offsets = offsets;
+  p.perm = perm;
+  p.inv = inv;
+  p.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+  p.base = reinterpret_cast<int32_t*>(ws + L.base);
+  p.total = reinterpret_cast<int32_t*>(ws + L.total);
+  p.status = reinterpret_cast<uint32_t*>(ws + L.header);
+  p.barrier = p.status + 1;
+  ML_CUDA(launch_route_align(p, grid, stream), "route_align launch");
+  return MOE_LORA_OK;
+}
+
+bool make_tmap(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token-tile width from the mean number of pairs per expert.
+int pick_bn(long long P, int E) {
+  const long long m2 = 2 * ((P + E - 1) / E);
+  if (m2 <= 16) return 16;
+  if (m2 <= 32) return 32;
+  if (m2 <= 64) return 64;
+  if (m2 <= 128) return 128;
+  return 256;
+}
+
+int pick_stages(int bn, int E) {
+  const int budget = (bn <= 32 ? 160 : 200) * 1024;
+  const int fixed = gemm_smem_bytes(bn, 0, E);
+  int s = (budget - fixed) / (gemm_stage_bytes(bn) + 16);
+  if (s > 16) s = 16;
+  if (s < 2) s = 2;
+  return s;
+}
+
+moe_lora_status enqueue_gemm(moe_lora_handle* h, const void* W, const void* X, void* out, const int32_t* offsets,
+                             uint32_t* status, int E, int N, int K, int P, int gated, int bn, cudaStream_t stream) {
+  GemmParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(E) * N, K, 64)) return MOE_LORA_ERR_CUDA;
+  if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), K, bn)) return MOE_LORA_ERR_CUDA;
+  gp.out = reinterpret_cast<__nv_bfloat16*>(out);
+  gp.offsets = offsets;
+  gp.status = status;
+  gp.E = E;
+  gp.N = N;
+  gp.K = K;
+  gp.gated = gated;
+  gp.stages = pick_stages(bn, E);
+  ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream), "grouped_gemm launch");
+  return MOE_LORA_OK;
+}
+
+void prof(const moe_lora_args* a, int stage, int which, cudaStream_t s) {
+  if (a->prof_events == nullptr) return;
+  void* ev = a->prof_events[2 * stage + which];
+  if (ev != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
+LoraSlots make_slots(const moe_lora_args* a) {
+  LoraSlots L;
+  std::memset(&L, 0, sizeof(L));
+  L.S = a->S;
+  L.E = a->E;
+  L.R = a->R;
+  for (int s = 0; s < a->S; ++s) {
+    L.ranks[s] = a->h_ranks[s];
+    L.scal[s] = a->h_scalings[s];
+  }
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_lora_status moe_lora_route(moe_lora_handle* h, const moe_lora_bf16* router_logits, const float* correction_bias,
+                               int T, int E, int top_k, int routing_method, float routed_scaling_factor, int n_group,
+                               int topk_group, int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                               int32_t* perm, int32_t* inv_perm, void* workspace, size_t workspace_bytes,
+                               moe_lora_stream stream) {
+  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  moe_lora_status st = check_routing_args(T, E, top_k, routing_method, router_logits, correction_bias, n_group,
+                                          topk_group);
+  if (st != MOE_LORA_OK) return st;
+  if (expert_offsets == nullptr || (T > 0 && (!topk_ids || !topk_weights || !perm || !inv_perm)))
+    return MOE_LORA_ERR_INVALID_ARG;
+  const Layout L = layout_for(T, 0, 0, E, top_k, 0);
+  if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
+  if (T == 0) {
+    ML_CUDA(cudaMemsetAsync(expert_offsets, 0, (static_cast<size_t>(E) + 1) * 4, stream), "cudaMemsetAsync");
+    return MOE_LORA_OK;
+  }
+  return enqueue_route(h, router_logits, correction_bias, T, E, top_k, routing_method, routed_scaling_factor,
+                       topk_ids, topk_weights, expert_offsets, perm, inv_perm, ws, L, stream);
+}
+
+moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden, const int32_t* perm, int T, int H,
+                                 int top_k, moe_lora_bf16* permuted, moe_lora_stream stream) {
+  if (h == nullptr || T < 0 || H < 8 || H % 8 != 0 || top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (T == 0) return MOE_LORA_OK;
+  if (!hidden || !perm || !permuted || !aligned16(hidden) || !aligned16(permuted)) return MOE_LORA_ERR_INVALID_ARG;
+  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(hidden), perm, T * top_k, top_k, H,
+                         reinterpret_cast<__nv_bfloat16*>(permuted), stream),
+          "permute launch");
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out, void* workspace,
+                                 size_t workspace_bytes, moe_lora_stream stream_) {
+  moe_lora_status st = moe_lora_validate(a);
+  if (st != MOE_LORA_OK) return st;
+  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (a->T > 0 && (out == nullptr || !aligned16(out))) return MOE_LORA_ERR_INVALID_ARG;
+  cudaStream_t stream = stream_;
+  const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
+  const bool lora = lora_active(a);
+  const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0);
+  if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
+  if (T == 0) return MOE_LORA_OK;
+
+  const int P = T * k;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.header);
+  int32_t* ids = a->topk_ids ? a->topk_ids : reinterpret_cast<int32_t*>(ws + L.ids);
+  float* wts = a->topk_weights ? a->topk_weights : reinterpret_cast<float*>(ws + L.wts);
+  int32_t* offsets = a->expert_offsets ? a->expert_offsets : reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* perm = a->perm ? a->perm : reinterpret_cast<int32_t*>(ws + L.perm);
+  int32_t* inv = a->inv_perm ? a->inv_perm : reinterpret_cast<int32_t*>(ws + L.inv);
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + L.xp);
+  __nv_bfloat16* g = reinterpret_cast<__nv_bfloat16*>(ws + L.g);
+  __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(ws + L.d);
+  float* u = reinterpret_cast<float*>(ws + L.u);
+  __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
+  float* v = reinterpret_cast<float*>(ws + L.v);
+  __nv_bfloat16* y = xp;   // reuse: xp is dead after the gate_up GEMM
+
+  prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
+  st = enqueue_route(h, a->router_logits, a->correction_bias, T, E, k, a->routing_method, a->routed_scaling_factor,
+                     ids, wts, offsets, perm, inv, ws, L, stream);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_ROUTE, 1, stream);
+
+  LoraSlots slots;
+  if (lora) slots = make_slots(a);
+  const bool two = lora && (((T <= 256) && !(a->flags & MOE_LORA_FLAG_FORCE_SINGLE_STREAM)) ||
+                            (a->flags & MOE_LORA_FLAG_FORCE_TWO_STREAM));
+  cudaStream_t ls = two ? h->side : stream;
+  if (lora) {
+    if (two) {
+      ML_CUDA(cudaEventRecord(h->ev_fork, stream), "cudaEventRecord");
+      ML_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0), "cudaStreamWaitEvent");
+    }
+    prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, ls);
+    ShrinkParams sp;
+    sp.src = reinterpret_cast<const __nv_bfloat16*>(a->hidden);
+    sp.by_token = 1;
+    sp.perm = perm;
+    sp.ids = ids;
+    sp.slot_idx = a->slot_idx;
+    sp.k = k;
+    sp.P = P;
+    sp.K = H;
+    sp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_gu);
+    sp.slots = slots;
+    sp.u = u;
+    sp.status = status;
+    sp.where = kWhereLoraShrinkGu;
+    ML_CUDA(launch_lora_shrink(sp, ls), "lora shrink (gate_up) launch");
+    ExpandParams ep;
+    ep.u = u;
+    ep.perm = perm;
+    ep.ids = ids;
+    ep.slot_idx = a->slot_idx;
+    ep.k = k;
+    ep.P = P;
+    ep.N = 2 * I;
+    ep.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
+    ep.slots = slots;
+    ep.d = d;
+    ep.status = status;
+    ML_CUDA(launch_lora_expand(ep, ls), "lora expand (gate_up) launch");
+    prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, ls);
+    if (two) ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
+  }
+
+  prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
+  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream),
+          "permute launch");
+  prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
+
+  const int bn = pick_bn(P, E);
+  prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
+  st = enqueue_gemm(h, a->w1, xp, g, offsets, status, E, 2 * I, H, P, 1, bn, stream);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
+
+  if (two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
+  ML_CUDA(launch_activation(g, lora ? d : nullptr, P, I, act, stream), "activation launch");
+  prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
+
+  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
+  st = enqueue_gemm(h, a->w2, act, y, offsets, status, E, H, I, P, 0, bn, stream);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+
+  if (lora) {
+    prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
+    ShrinkParams sp;
+    sp.src = act;
+    sp.by_token = 0;
+    sp.perm = perm;
+    sp.ids = ids;
+    sp.slot_idx = a->slot_idx;
+    sp.k = k;
+    sp.P = P;
+    sp.K = I;
+    sp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
+    sp.slots = slots;
+    sp.u = v;
+    sp.status = status;
+    sp.where = kWhereLoraShrinkDn;
+    ML_CUDA(launch_lora_shrink(sp, stream), "lora shrink (down) launch");
+    prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
+  }
+
+  prof(a, MOE_LORA_STAGE_FINALIZE, 0, stream);
+  FinalizeParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.y = y;
+  fp.v = lora ? v : nullptr;
+  fp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
+  fp.ids = ids;
+  fp.weights = wts;
+  fp.inv = inv;
+  fp.slot_idx = a->slot_idx;
+  fp.T = T;
+  fp.H = H;
+  fp.k = k;
+  if (lora) fp.slots = slots;
+  fp.out = reinterpret_cast<__nv_bfloat16*>(out);
+  fp.status = status;
+  ML_CUDA(launch_finalize(fp, stream), "finalize launch");
+  prof(a, MOE_LORA_STAGE_FINALIZE, 1, stream);
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_check_status(const void* workspace, moe_lora_stream stream, uint32_t* detail) {
+  if (workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  ML_CUDA(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  uint32_t word = 0;
+  ML_CUDA(cudaMemcpy(&word, workspace, 4, cudaMemcpyDeviceToHost), "cudaMemcpy");
+  if (detail) *detail = word;
+  const uint32_t code = word & 0xffu;
+  if (code == 0) return MOE_LORA_OK;
+  if (code == MOE_LORA_ERR_TIMEOUT) return MOE_LORA_ERR_TIMEOUT;
+  return MOE_LORA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

@@ -1,0 +1,312 @@
+// Fused routing + expert alignment, one launch.
+//
+// Phase 1: one warp per token selects the top-k experts (warp arg-max rounds, ties to
+//          the lower expert id) and the routing weights; each CTA counts its pairs per
+//          expert in shared memory.
+// Phase 2: (grid barrier) per expert, an exclusive prefix of the per-CTA counts over
+//          the CTAs in order; (grid barrier) every CTA scans the expert totals into
+//          expert_offsets, then scatters its own pairs, in ascending expanded index,
+//          to perm / inv_perm.  Because every CTA owns a contiguous token range and
+//          the per-CTA bases are prefixes in CTA order, the permutation is the unique
+//          "by expert, then by expanded index" order.
+//
+// Stage references: sglang PR #27329 "Experimental fast LoRA path", Optimizations
+// ("topk + FlashInfer routed-pack in a single launch", "JIT MoE-align"); the routing
+// methods of the vLLM API page "fused_moe/experts/trtllm_lora_moe"
+// (_supports_routing_method: Renormalize, DeepSeekV3).
+//
+// With more than one CTA the kernel is launched cooperatively (all CTAs resident), and
+// each grid barrier is a bounded spin: after 2 s it records MOE_LORA_ERR_TIMEOUT in the
+// status word and the kernel returns.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mlk {
+
+constexpr int kRouteThreads = 512;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kInvalidId = 0x7fffffff;
+
+// sigma(z) = 1 / (1 + exp(-z)) in float32, one IEEE rounding per operation, with exp
+// evaluated by Cody-Waite reduction (W. J. Cody and W. Waite, "Software Manual for the
+// Elementary Functions", 1980): n = rint(x log2 e), r = (x - n*C1) - n*C2 where C1 =
+// 355/512 is short enough that n*C1 is exact and C1 + C2 = ln 2, then exp(r) from the
+// degree-7 Taylor polynomial in Horner form and an exact scaling by 2^n.  The input is
+// clamped to [-86, 88] so 2^n stays a normal float.  Written out operation by operation
+// (no contraction into fused multiply-adds) because the DeepSeekV3 key s + bias decides
+// which experts win, and the host-side checker evaluates the same sequence.
+MLDEV float sigmoid_key_f32(float z) {
+  float x = -z;
+  x = fminf(fmaxf(x, -86.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));          // log2(e)
+  float r = __fsub_rn(x, __fmul_rn(n, 0x1.63p-1f));             // 355/512
+  r = __fsub_rn(r, __fmul_rn(n, -0x1.bd0106p-13f));             // ln 2 - 355/512
+  float p = 1.0f / 5040.0f;
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 2.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+  const float e = __fmul_rn(p, two_n);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
+MLDEV float load_logit(const __nv_bfloat16* row, int e) {
+  float l = bf2f(row[e]);
+  return (l != l) ? -INFINITY : l;   // NaN logits never win
+}
+
+// Grid-wide barrier for a cooperative launch; bounded spin.
+MLDEV bool grid_barrier(uint32_t* ctr, uint32_t target, uint32_t* status, volatile int* ok_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const uint64_t t0 = globaltimer_ns();
+    int ok = 1;
+    while (ld_acquire_gpu(ctr) < target) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        ok = 0;
+        record_status(status, kDevTimeout, kWhereRouteBarrier);
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    *ok_s = ok;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
+// Exclusive scan of in[0..n) into out[0..n) (n <= 2 * kRouteThreads); returns the total.
+MLDEV int block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = 2 * tid;
+  const int a = (i0 < n) ? in[i0] : 0;
+  const int b = (i0 + 1 < n) ? in[i0 + 1] : 0;
+  const int s = a + b;
+  int incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < kRouteWarps) ? warp_sums[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += y;
+    }
+    if (lane < kRouteWarps) warp_sums[lane] = wi - w;   // exclusive warp prefix
+    if (lane == kRouteWarps - 1) warp_sums[kRouteWarps] = wi;
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + incl - s;
+  if (i0 < n) out[i0] = excl;
+  if (i0 + 1 < n) out[i0 + 1] = excl + a;
+  const int total = warp_sums[kRouteWarps];
+  __syncthreads();
+  return total;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteParams p) {
+  __shared__ int hist_s[kMaxExperts];
+  __shared__ int cursor_s[kMaxExperts];
+  __shared__ int warp_sums[kRouteWarps + 1];
+  __shared__ int ok_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int E = p.E, k = p.k;
+
+  for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = 0;
+  __syncthreads();
+
+  const int t0 = c * p.tokens_per_cta;
+  const int t1 = min(p.T, t0 + p.tokens_per_cta);
+
+  // ---------------- phase 1: top-k per token, one warp per token
+  for (int t = t0 + warp; t < t1; t += kRouteWarps) {
+    const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
+    float key[EPL];
+    uint32_t avail = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      float kv = -INFINITY;
+      if (e < E) {
+        const float l = load_logit(row, e);
+        kv = (p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l;
+        avail |= 1u << i;
+      }
+      key[i] = kv;
+    }
+    int my_id = kInvalidId;
+    float my_key = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      float bk = -INFINITY;
+      int bid = kInvalidId;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {   // ids ascend with i: strict > keeps the lower id
+        if ((avail >> i) & 1u) {
+          if (bid == kInvalidId || key[i] > bk) {
+            bk = key[i];
+            bid = lane + 32 * i;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+        const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+        if (oid != kInvalidId && (bid == kInvalidId || ok > bk || (ok == bk && oid < bid))) {
+          bk = ok;
+          bid = oid;
+        }
+      }
+      if ((bid & 31) == lane) avail &= ~(1u << (bid >> 5));
+      if (lane == j) {
+        my_id = bid;
+        my_key = bk;
+      }
+    }
+    float wv;
+    if (p.method == 1) {
+      const float s = (lane < k) ? sigmoid_key_f32(load_logit(row, my_id)) : 0.0f;
+      float sum = s;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      wv = s / sum * p.rsf;
+    } else {
+      const float kmax = __shfl_sync(0xffffffffu, my_key, 0);
+      const float ex = (lane < k) ? expf(my_key - kmax) : 0.0f;
+      float sum = ex;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      wv = ex / sum;
+    }
+    if (lane < k) {
+      p.ids[static_cast<size_t>(t) * k + lane] = my_id;
+      p.weights[static_cast<size_t>(t) * k + lane] = wv;
+      atomicAdd(&hist_s[my_id], 1);
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase 2: expert offsets and per-CTA bases
+  if (G > 1) {
+    for (int e = tid; e < E; e += kRouteThreads) p.hist[c * E + e] = hist_s[e];
+    if (!grid_barrier(p.barrier, static_cast<uint32_t>(G), p.status, &ok_s)) return;
+    // warp per expert: prefix of the per-CTA counts in CTA order
+    const int m = (G + 31) / 32;
+    for (int e = c * kRouteWarps + warp; e < E; e += G * kRouteWarps) {
+      int loc = 0;
+      for (int i = 0; i < m; ++i) {
+        const int cc = lane * m + i;
+        if (cc < G) loc += __ldcg(&p.hist[cc * E + e]);
+      }
+      int incl = loc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int run = incl - loc;
+      for (int i = 0; i < m; ++i) {
+        const int cc = lane * m + i;
+        if (cc < G) {
+          p.base[cc * E + e] = run;
+          run += __ldcg(&p.hist[cc * E + e]);
+        }
+      }
+      if (lane == 31) p.total[e] = incl;
+    }
+    if (!grid_barrier(p.barrier, 2u * static_cast<uint32_t>(G), p.status, &ok_s)) return;
+    for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = __ldcg(&p.total[e]);
+    __syncthreads();
+  }
+  const int total = block_exclusive_scan(hist_s, cursor_s, E, warp_sums);
+  if (c == 0) {
+    for (int e = tid; e < E; e += kRouteThreads) p.offsets[e] = cursor_s[e];
+    if (tid == 0) p.offsets[E] = total;
+  }
+  if (G > 1) {
+    for (int e = tid; e < E; e += kRouteThreads) cursor_s[e] += __ldcg(&p.base[c * E + e]);
+  }
+  __syncthreads();
+
+  // ---------------- scatter this CTA's pairs in ascending expanded index
+  if (warp == 0 && t0 < t1) {
+    const int p0 = t0 * k, p1 = t1 * k;
+    for (int pb = p0; pb < p1; pb += 32) {
+      const int pp = pb + lane;
+      const bool valid = pp < p1;
+      const int e = valid ? p.ids[pp] : -1;
+      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      const int q = valid ? cursor_s[e] + rank : 0;
+      __syncwarp();
+      if (valid && rank == 0) cursor_s[e] += __popc(grp);
+      __syncwarp();
+      if (valid) {
+        p.perm[q] = pp;
+        p.inv[pp] = q;
+      }
+    }
+  }
+}
+
+template <int EPL>
+static cudaError_t launch_epl(const RouteParams& p, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = grid > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, route_align_kernel<EPL>, p);
+}
+
+static int epl_for(int E) { return E <= 128 ? 4 : E <= 256 ? 8 : E <= 384 ? 12 : E <= 512 ? 16 : 32; }
+
+int route_max_coop_ctas(int E) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  cudaError_t err;
+  switch (epl_for(E)) {
+    case 4: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<4>, kRouteThreads, 0); break;
+    case 8: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<8>, kRouteThreads, 0); break;
+    case 12: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<12>, kRouteThreads, 0); break;
+    case 16: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<16>, kRouteThreads, 0); break;
+    default: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<32>, kRouteThreads, 0); break;
+  }
+  if (err != cudaSuccess || per_sm < 1) return 1;
+  const int n = sms * per_sm;
+  return n < kMaxRouteCtas ? n : kMaxRouteCtas;
+}
+
+cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stream) {
+  switch (epl_for(p.E)) {
+    case 4: return launch_epl<4>(p, grid, stream);
+    case 8: return launch_epl<8>(p, grid, stream);
+    case 12: return launch_epl<12>(p, grid, stream);
+    case 16: return launch_epl<16>(p, grid, stream);
+    default: return launch_epl<32>(p, grid, stream);
+  }
+}
+
+}  // namespace mlk
