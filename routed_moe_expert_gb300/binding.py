@@ -1,0 +1,275 @@
+"""Thin Python binding of libmoelora.so (ctypes): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module checks tensor
+dtypes/devices/contiguity, passes raw device pointers and the current CUDA stream, and
+turns status codes into exceptions.  PyTorch provides device memory and streams.
+If the library has not been built, every call raises MoELoRAError: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoelora.so")
+
+MOE_LORA_OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL", 4: "CUDA",
+                5: "TIMEOUT", 6: "DEVICE_CHECK"}
+ROUTE_RENORMALIZE = 0
+ROUTE_DEEPSEEK_V3 = 1
+FLAG_LORA_OFF = 1
+FLAG_FORCE_SINGLE_STREAM = 2
+FLAG_FORCE_TWO_STREAM = 4
+STAGES = ["route", "permute", "gate_up_gemm", "lora_gate_up", "activation", "down_gemm",
+          "lora_down", "finalize"]
+NUM_STAGES = len(STAGES)
+
+EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
+            "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
+            "moe_lora_forward", "moe_lora_check_status"]
+
+
+class MoELoRAError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        msg = f"{what}: {STATUS_NAMES.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+c_int, c_float, c_void_p, c_size_t, c_uint = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", c_int), ("H", c_int), ("I", c_int), ("E", c_int), ("top_k", c_int), ("S", c_int), ("R", c_int)]
+
+
+class Args(ctypes.Structure):
+    _fields_ = [
+        ("T", c_int), ("H", c_int), ("I", c_int), ("E", c_int), ("top_k", c_int), ("S", c_int), ("R", c_int),
+        ("routing_method", c_int), ("routed_scaling_factor", c_float), ("n_group", c_int), ("topk_group", c_int),
+        ("hidden", c_void_p), ("router_logits", c_void_p), ("correction_bias", c_void_p),
+        ("w1", c_void_p), ("w2", c_void_p),
+        ("lora_A_gu", c_void_p), ("lora_B_gu", c_void_p), ("lora_A_dn", c_void_p), ("lora_B_dn", c_void_p),
+        ("slot_idx", c_void_p), ("h_ranks", ctypes.POINTER(ctypes.c_int32)),
+        ("h_scalings", ctypes.POINTER(c_float)), ("flags", c_uint),
+        ("topk_ids", c_void_p), ("topk_weights", c_void_p), ("expert_offsets", c_void_p),
+        ("perm", c_void_p), ("inv_perm", c_void_p), ("prof_events", c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoelora.so (raises MoELoRAError if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise MoELoRAError(4, "libmoelora.so not found",
+                           f"{LIB_PATH}; build it with routed_moe_expert_gb300._build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    L.moe_lora_create.argtypes = [ctypes.POINTER(c_void_p), c_int]
+    L.moe_lora_destroy.argtypes = [c_void_p]
+    L.moe_lora_status_string.argtypes = [c_int]
+    L.moe_lora_status_string.restype = ctypes.c_char_p
+    L.moe_lora_last_cuda_error.argtypes = []
+    L.moe_lora_last_cuda_error.restype = ctypes.c_char_p
+    L.moe_lora_workspace_size.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(c_size_t)]
+    L.moe_lora_validate.argtypes = [ctypes.POINTER(Args)]
+    L.moe_lora_route.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_lora_permute.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]
+    L.moe_lora_forward.argtypes = [c_void_p, ctypes.POINTER(Args), c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_lora_check_status.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    for name in EXPORTED:
+        if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
+            getattr(L, name).restype = c_int
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != MOE_LORA_OK:
+        detail = lib().moe_lora_last_cuda_error().decode() if status == 4 else ""
+        raise MoELoRAError(status, what, detail)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Handle:
+    """Owns a moe_lora_handle (side stream + events).  Create outside graph capture."""
+
+    def __init__(self, device: int = 0):
+        h = c_void_p()
+        _check(lib().moe_lora_create(ctypes.byref(h), int(device)), "moe_lora_create")
+        self._h = h
+        self.device = device
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().moe_lora_destroy(self._h)
+            self._h = c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def moe_lora_create(device: int = 0) -> Handle:
+    return Handle(device)
+
+
+def moe_lora_status_string(status: int) -> str:
+    return lib().moe_lora_status_string(int(status)).decode()
+
+
+def moe_lora_workspace_size(T, H, I, E, top_k, S=0, R=0) -> int:
+    n = c_size_t()
+    _check(lib().moe_lora_workspace_size(ctypes.byref(Shape(T, H, I, E, top_k, S, R)), ctypes.byref(n)),
+           "moe_lora_workspace_size")
+    return n.value
+
+
+def alloc_workspace(T, H, I, E, top_k, S=0, R=0, device="cuda") -> torch.Tensor:
+    return torch.empty(moe_lora_workspace_size(T, H, I, E, top_k, S, R), dtype=torch.uint8, device=device)
+
+
+def moe_lora_route(handle: Handle, router_logits: torch.Tensor, top_k: int, routing_method: int = 0,
+                   correction_bias: Optional[torch.Tensor] = None, routed_scaling_factor: float = 1.0,
+                   n_group: int = 1, topk_group: int = 1, outputs: Optional[dict] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    T, E = router_logits.shape
+    dev = router_logits.device
+    P = T * top_k
+    o = dict(outputs or {})
+    o.setdefault("topk_ids", torch.empty((T, top_k), dtype=torch.int32, device=dev))
+    o.setdefault("topk_weights", torch.empty((T, top_k), dtype=torch.float32, device=dev))
+    o.setdefault("expert_offsets", torch.empty((E + 1,), dtype=torch.int32, device=dev))
+    o.setdefault("perm", torch.empty((P,), dtype=torch.int32, device=dev))
+    o.setdefault("inv_perm", torch.empty((P,), dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(T, 0, 0, E, top_k, device=dev)
+    st = lib().moe_lora_route(
+        handle.ptr, _ptr(router_logits, torch.bfloat16, "router_logits"),
+        _ptr(correction_bias, torch.float32, "correction_bias"), T, E, int(top_k), int(routing_method),
+        float(routed_scaling_factor), int(n_group), int(topk_group),
+        _ptr(o["topk_ids"], torch.int32), _ptr(o["topk_weights"], torch.float32),
+        _ptr(o["expert_offsets"], torch.int32), _ptr(o["perm"], torch.int32), _ptr(o["inv_perm"], torch.int32),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "moe_lora_route")
+    o["workspace"] = workspace
+    return o
+
+
+def moe_lora_permute(handle: Handle, hidden: torch.Tensor, perm: torch.Tensor, top_k: int,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    T, H = hidden.shape
+    if out is None:
+        out = torch.empty((T * top_k, H), dtype=torch.bfloat16, device=hidden.device)
+    st = lib().moe_lora_permute(handle.ptr, _ptr(hidden, torch.bfloat16, "hidden"), _ptr(perm, torch.int32, "perm"),
+                                T, H, int(top_k), _ptr(out, torch.bfloat16, "out"), _stream(stream))
+    _check(st, "moe_lora_permute")
+    return out
+
+
+def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction_bias=None,
+              routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
+              slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (), flags=0,
+              outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1):
+    """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
+    T, H = hidden.shape
+    E, twoI, _ = w1.shape
+    S = len(ranks)
+    R = int(lora_A_gu.shape[2]) if (lora_A_gu is not None and S > 0) else 0
+    ranks_arr = (ctypes.c_int32 * max(S, 1))(*[int(r) for r in ranks])
+    scal_arr = (c_float * max(S, 1))(*[float(s) for s in scalings])
+    o = outputs or {}
+    a = Args()
+    a.T, a.H, a.I, a.E, a.top_k, a.S, a.R = T, H, twoI // 2, E, int(top_k), S, R
+    a.routing_method, a.routed_scaling_factor = int(routing_method), float(routed_scaling_factor)
+    a.n_group, a.topk_group = int(n_group), int(topk_group)
+    a.hidden = _ptr(hidden, torch.bfloat16, "hidden")
+    a.router_logits = _ptr(router_logits, torch.bfloat16, "router_logits")
+    a.correction_bias = _ptr(correction_bias, torch.float32, "correction_bias")
+    a.w1 = _ptr(w1, torch.bfloat16, "w1")
+    a.w2 = _ptr(w2, torch.bfloat16, "w2")
+    a.lora_A_gu = _ptr(lora_A_gu, torch.bfloat16, "lora_A_gu")
+    a.lora_B_gu = _ptr(lora_B_gu, torch.bfloat16, "lora_B_gu")
+    a.lora_A_dn = _ptr(lora_A_dn, torch.bfloat16, "lora_A_dn")
+    a.lora_B_dn = _ptr(lora_B_dn, torch.bfloat16, "lora_B_dn")
+    a.slot_idx = _ptr(slot_idx, torch.int32, "slot_idx")
+    a.h_ranks = ranks_arr
+    a.h_scalings = scal_arr
+    a.flags = int(flags)
+    a.topk_ids = _ptr(o.get("topk_ids"), torch.int32)
+    a.topk_weights = _ptr(o.get("topk_weights"), torch.float32)
+    a.expert_offsets = _ptr(o.get("expert_offsets"), torch.int32)
+    a.perm = _ptr(o.get("perm"), torch.int32)
+    a.inv_perm = _ptr(o.get("inv_perm"), torch.int32)
+    ev_arr = None
+    if prof_events is not None:
+        ev_arr = (c_void_p * (2 * NUM_STAGES))(*[(e.cuda_event if e is not None else None) for e in prof_events])
+        a.prof_events = ctypes.cast(ev_arr, c_void_p)
+    return a, (ranks_arr, scal_arr, ev_arr)
+
+
+def moe_lora_forward(handle: Handle, hidden, router_logits, w1, w2, top_k, routing_method=0,
+                     correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None,
+                     lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(), flags=0,
+                     out=None, workspace=None, outputs=None, prof_events=None, stream=None,
+                     n_group=1, topk_group=1) -> torch.Tensor:
+    """The whole layer: returns out [T, H] bf16 (written in place when `out` is given)."""
+    a, keep = make_args(hidden, router_logits, w1, w2, top_k, routing_method, correction_bias,
+                        routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
+                        scalings, flags, outputs, prof_events, n_group, topk_group)
+    if out is None:
+        out = torch.empty((a.T, a.H), dtype=torch.bfloat16, device=hidden.device)
+    if workspace is None:
+        workspace = alloc_workspace(a.T, a.H, a.I, a.E, a.top_k, a.S, a.R, device=hidden.device)
+    st = lib().moe_lora_forward(handle.ptr, ctypes.byref(a), _ptr(out, torch.bfloat16, "out"),
+                                _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "moe_lora_forward")
+    del keep
+    return out
+
+
+def moe_lora_validate(**kwargs) -> int:
+    a, keep = make_args(**kwargs)
+    return lib().moe_lora_validate(ctypes.byref(a))
+
+
+def moe_lora_check_status(workspace: torch.Tensor, stream=None):
+    """Synchronize `stream` and return (status, raw_word) of the last call on `workspace`."""
+    word = ctypes.c_uint32()
+    st = lib().moe_lora_check_status(_ptr(workspace, torch.uint8, "workspace"), _stream(stream), ctypes.byref(word))
+    return st, word.value

@@ -11,3 +11,14 @@ if HERE not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def built_lib():
+    """Build libmoelora.so in-tree (nvcc cross-compiles without a GPU) and load it."""
+    from routed_moe_expert_gb300 import _build, binding
+    _build.build()
+    return binding.lib()

@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared entry
+point, and its host-side argument checks accept and reject what the header says."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routed_moe_expert_gb300 import binding as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "moe_lora.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_lora_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_lora_route", "moe_lora_permute", "moe_lora_forward", "moe_lora_create",
+              "moe_lora_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    for name in declared_functions():
+        assert hasattr(built_lib, name), name
+    assert sorted(declared_functions()) == sorted(B.EXPORTED)
+
+
+def test_status_strings(built_lib):
+    for s in range(7):
+        assert B.moe_lora_status_string(s)
+    assert "invalid" in B.moe_lora_status_string(1)
+
+
+def test_workspace_size_host_only(built_lib):
+    small = B.moe_lora_workspace_size(8, 128, 64, 8, 2, 1, 4)
+    big = B.moe_lora_workspace_size(64, 2048, 768, 128, 8, 1, 16)
+    assert 0 < small < big
+    # the permuted activations alone need T*k*H*2 bytes
+    assert big >= 64 * 8 * 2048 * 2
+    with pytest.raises(B.MoELoRAError):
+        B.moe_lora_workspace_size(8, 128, 64, 8, 9)     # top_k > E
+    with pytest.raises(B.MoELoRAError):
+        B.moe_lora_workspace_size(8, 128, 64, 0, 1)     # no experts
+    assert B.moe_lora_workspace_size(0, 128, 64, 8, 2) > 0
+
+
+FAKE = 0x7f0000000000          # 16-byte aligned fake device address (never dereferenced)
+
+
+def _args(**over):
+    ranks = (ctypes.c_int32 * 2)(4, 2)
+    scal = (ctypes.c_float * 2)(2.0, 1.0)
+    a = B.Args()
+    vals = dict(T=8, H=128, I=64, E=8, top_k=2, S=2, R=4, routing_method=0, routed_scaling_factor=1.0,
+                n_group=1, topk_group=1, hidden=FAKE, router_logits=FAKE, correction_bias=None, w1=FAKE,
+                w2=FAKE, lora_A_gu=FAKE, lora_B_gu=FAKE, lora_A_dn=FAKE, lora_B_dn=FAKE, slot_idx=FAKE,
+                h_ranks=ranks, h_scalings=scal, flags=0)
+    vals.update(over)
+    for k, v in vals.items():
+        setattr(a, k, v)
+    return a, (ranks, scal)
+
+
+def _validate(**over):
+    a, keep = _args(**over)
+    return B.lib().moe_lora_validate(ctypes.byref(a))
+
+
+def test_validate_accepts_a_good_call(built_lib):
+    assert _validate() == 0
+    assert _validate(T=0, hidden=None, w1=None) == 0                  # empty batch
+    assert _validate(routing_method=1, correction_bias=FAKE, routed_scaling_factor=2.5) == 0
+    assert _validate(flags=B.FLAG_LORA_OFF, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None,
+                     lora_B_dn=None, slot_idx=None) == 0
+    assert _validate(S=0, R=0, lora_A_gu=None) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=96), 1), (dict(H=0), 1), (dict(I=32), 1), (dict(E=0), 1), (dict(E=2000), 1),
+    (dict(top_k=9), 1), (dict(top_k=0), 1), (dict(T=-1), 1), (dict(routing_method=3), 1),
+    (dict(routing_method=1), 1),                       # DeepSeekV3 needs the correction bias
+    (dict(n_group=2), 2), (dict(topk_group=4), 2),     # grouped DeepSeekV3 not supported
+    (dict(hidden=None), 1), (dict(w2=None), 1), (dict(hidden=FAKE + 8), 1),
+    (dict(lora_A_gu=None), 1), (dict(slot_idx=None), 1), (dict(S=65), 1), (dict(R=129), 1),
+    (dict(R=3), 1),                                    # ranks[0] = 4 > R
+])
+def test_validate_rejects(built_lib, over, code):
+    assert _validate(**over) == code
+
+
+def test_validate_rejects_nan_scaling(built_lib):
+    a, keep = _args()
+    scal = (ctypes.c_float * 2)(float("nan"), 1.0)
+    a.h_scalings = scal
+    assert B.lib().moe_lora_validate(ctypes.byref(a)) == 1
+
+
+def test_forward_rejects_null_handle_without_launching(built_lib):
+    a, keep = _args()
+    st = B.lib().moe_lora_forward(None, ctypes.byref(a), FAKE, FAKE, 1 << 30, None)
+    assert st == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", "/nonexistent/libmoelora.so")
+    with pytest.raises(B.MoELoRAError):
+        B.lib()
