@@ -1,0 +1,412 @@
+"""Benchmark of the routed MoE-LoRA expert layer on GB300.
+
+One step = one forward of the whole layer (routing, permute, gate_up GEMM, LoRA gate_up
+chain, activation, down GEMM, down LoRA, finalize) over one batch of seeded synthetic
+input already resident in HBM.  Default workload: decode, T=64 tokens, H=2048, I=768,
+E=128 experts, top_k=8, one rank-16 adapter (Qwen3-30B-A3B-like experts).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  For N > 1 it runs under torchrun with one independent
+replica per GPU (the layer has no data-path exchange on one GPU): value = tokens of all
+ranks / max-over-ranks time.  `--impl reference` times the CPU oracle on the host cores
+(the only other arm there is: the pages ship no code) on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-LoRA layer tokens/s (decode T<=256, prefill 8K); % of HBM/bf16 roofline"
+UNIT = "tokens/s"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, steps: int, world: int, seconds_max: float) -> dict:
+    """Whole-job throughput from the per-rank work and the slowest rank's time."""
+    total_tokens = tokens_per_rank * steps * world
+    return dict(value=total_tokens / seconds_max, ms_per_step=1e3 * seconds_max / steps)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def gemm_source_hash():
+    with open(os.path.join(ROOT, "routed_moe_expert_gb300", "csrc", "grouped_gemm.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current GEMM source (else None)."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_src = re.search(r"grouped_gemm\.cu sha256\[:16\]:\s*([0-9a-f]{16})", txt)
+    m_val = re.search(r"dram bytes per launch \(read\+write\):\s*([0-9.eE+]+)", txt)
+    if not m_src or not m_val or m_src.group(1) != gemm_source_hash():
+        return None
+    return float(m_val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=smax, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# ------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import routed_moe_expert_gb300 as pkg
+    from routed_moe_expert_gb300 import _build
+    from routed_moe_expert_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or world > 1:
+        _build.build()
+    cfg = wl.CONFIGS[args.workload]
+    inp = wl.make_inputs(cfg, seed=args.seed, device="cuda")
+    g = inp
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    P = T * k
+    h = pkg.Handle(local)
+    ws = pkg.alloc_workspace(T, H, I, E, k, cfg.S, cfg.R)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
+        return pkg.moe_lora_forward(
+            h, g["hidden"] if hidden is None else hidden, g["router_logits"] if logits is None else logits,
+            g["w1"], g["w2"], k, routing_method=cfg.method, correction_bias=g["correction_bias"],
+            routed_scaling_factor=cfg.rsf, lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"],
+            lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"] if slot is None else slot,
+            ranks=cfg.ranks, scalings=cfg.scalings, flags=flags, out=o, workspace=ws, prof_events=prof,
+            outputs=outputs)
+
+    # touched experts (routing is fixed for the fixed input)
+    fwd(outputs=dict(expert_offsets=offsets))
+    torch.cuda.synchronize()
+    loads = np.diff(offsets.cpu().numpy())
+    touched = int((loads > 0).sum())
+    st, word = pkg.moe_lora_check_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {word:#x}")
+
+    # algorithmic bytes / flops
+    w_bytes_expert = 3 * H * I * 2
+    lora_blocks = 0
+    slots = g["slot_idx"].cpu().numpy()
+    ids_np = None
+    if cfg.S > 0:
+        ids_out = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        fwd(outputs=dict(topk_ids=ids_out))
+        ids_np = ids_out.cpu().numpy()
+        pairs = {(int(slots[t]), int(e)) for t in range(T) for e in ids_np[t] if slots[t] >= 0}
+        lora_blocks = sum(2 * cfg.ranks[s] * (2 * H + 3 * I) for s, _ in pairs)
+    io_bytes = T * H * 2 * 2 + T * E * 2
+    step_bytes = touched * w_bytes_expert + lora_blocks + io_bytes
+    step_flops = 2 * 3 * H * I * P + sum(2 * cfg.ranks[max(int(slots[t]), 0)] * (2 * H + 3 * I) * k
+                                         for t in range(T) if cfg.S > 0 and slots[t] >= 0)
+    gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + P * 2 * I * 2   # weights + xp read + g write
+    gu_flops = 2 * 2 * I * H * P
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: K steps, gate_up GEMM bracketed by events on its stream
+    n_ev = 2 * pkg.NUM_STAGES
+    gu = pkg.STAGES.index("gate_up_gemm")
+    ev_pairs = []
+    for _ in range(args.steps):
+        evs = [None] * n_ev
+        evs[2 * gu] = torch.cuda.Event(enable_timing=True)
+        evs[2 * gu + 1] = torch.cuda.Event(enable_timing=True)
+        for e in (evs[2 * gu], evs[2 * gu + 1]):
+            e.record(stream)          # materialise the CUDA event handle
+        ev_pairs.append(evs)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        fwd(prof=ev_pairs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    sec = t0.elapsed_time(t1) / 1e3
+    sec_max = max_over_ranks(sec, world)
+    agg = aggregate(T, args.steps, world, sec_max)
+    gu_ms = [ev[2 * gu].elapsed_time(ev[2 * gu + 1]) for ev in ev_pairs]
+    gu_avg_s = statistics.mean(gu_ms) / 1e3
+
+    # ---- end-to-end: inputs from pinned host memory each step, result back to host
+    h_hidden = g["hidden"].cpu().pin_memory()
+    h_logits = g["router_logits"].cpu().pin_memory()
+    h_slot = g["slot_idx"].cpu().pin_memory()
+    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    d_hidden = torch.empty_like(g["hidden"])
+    d_logits = torch.empty_like(g["router_logits"])
+    d_slot = torch.empty_like(g["slot_idx"])
+    h2d = h_hidden.numel() * 2 + h_logits.numel() * 2 + h_slot.numel() * 4
+    d2h = h_out.numel() * 2
+    e2e_steps = max(1, args.steps // 4)
+
+    def e2e_step():
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_slot.copy_(h_slot, non_blocking=True)
+        fwd(hidden=d_hidden, logits=d_logits, slot=d_slot)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_val = aggregate(T, e2e_steps, world, e_sec)["value"]
+
+    peaks = load_peaks()
+    achieved = gu_bytes / gu_avg_s / 1e9
+    launches_per_step = 6 + (3 if cfg.S > 0 else 0)
+    traffic = profiled_traffic(f"gate_up_gemm_{args.workload}.md")
+    line = {
+        "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": cfg.describe(), "T": T, "H": H, "I": I, "E": E, "top_k": k,
+            "lora_ranks": list(cfg.ranks), "routing": "DeepSeekV3" if cfg.method else "Renormalize",
+            "l2": f"inputs larger than L2: {touched} touched experts = {touched * w_bytes_expert / 1e9:.2f} GB of weights per step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "step_bytes": step_bytes, "step_flops": step_flops,
+            "step_hbm_roofline_frac": (step_bytes / (agg["ms_per_step"] / 1e3)) / (peaks["hbm_gbs"] * 1e9),
+        },
+        "roofline": {
+            "kernel": "grouped_gemm (gate_up)", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+            "peak_source": f"{peaks['source']} hbm_gbs", "algorithmic_bytes_per_launch": gu_bytes,
+            "avg_launch_us": gu_avg_s * 1e6,
+        },
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if cfg.S > 0:
+        # LoRA-off throughput of the same kernels, for the on/off ratio
+        for _ in range(args.warmup):
+            fwd(flags=pkg.FLAG_LORA_OFF)
+        torch.cuda.synchronize()
+        o0 = torch.cuda.Event(enable_timing=True)
+        o1 = torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for _ in range(max(1, args.steps // 4)):
+            fwd(flags=pkg.FLAG_LORA_OFF)
+        o1.record(stream)
+        torch.cuda.synchronize()
+        off_ms = o0.elapsed_time(o1) / max(1, args.steps // 4)
+        line["config"]["lora_off_ms_per_step"] = off_ms
+        line["config"]["lora_on_over_off"] = off_ms / agg["ms_per_step"]
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle (baseline leg / reference arm)
+# ------------------------------------------------------------------------------------
+
+def _oracle_inputs(cfg, inp):
+    f = lambda t: None if t is None else (t.float().cpu().numpy() if t.dtype.is_floating_point else t.cpu().numpy())
+    return {k: (f(v) if hasattr(v, "dtype") and hasattr(v, "cpu") else v) for k, v in inp.items()}
+
+
+def _oracle_call(cfg, o, tokens):
+    from oracle import moe_lora_oracle as orc
+    return orc.moe_lora_forward(o["hidden"], o["router_logits"], o["w1"], o["w2"], cfg.top_k, cfg.method,
+                                o["correction_bias"], cfg.rsf, o["lora_A_gu"], o["lora_B_gu"], o["lora_A_dn"],
+                                o["lora_B_dn"], o["slot_idx"], cfg.ranks, cfg.scalings, tokens=tokens)
+
+
+def cpu_baseline(cfg, inp, args, budget_s: float = None) -> dict:
+    """Time the oracle, as it stands, on a bounded token sample of the workload."""
+    budget_s = args.cpu_budget if budget_s is None else budget_s
+    o = _oracle_inputs(cfg, inp)
+    n_tok = min(cfg.T, 8)
+    t0 = time.perf_counter()
+    _oracle_call(cfg, o, np.arange(n_tok))
+    dt = time.perf_counter() - t0
+    done, spent = n_tok, dt
+    # grow the sample while it stays inside the budget
+    while spent < budget_s and done < cfg.T:
+        n = min(cfg.T, done * 2)
+        t0 = time.perf_counter()
+        _oracle_call(cfg, o, np.arange(n))
+        dt = time.perf_counter() - t0
+        done, spent = n, dt
+        if dt * 2 > budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dict(value=done / spent, unit=UNIT, cores=cores, kind="oracle",
+                sample=f"first {done} of {cfg.T} tokens of the {cfg.name} workload (full routing of all tokens), "
+                       f"{spent:.1f} s, numpy float64 with its default BLAS threads")
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from routed_moe_expert_gb300 import workloads as wl
+    cfg = wl.CONFIGS[args.workload]
+    inp = wl.make_inputs(cfg, seed=args.seed, device="cpu")
+    o = _oracle_inputs(cfg, inp)
+    n_tok = max(1, min(cfg.T, args.ref_tokens))
+    for _ in range(min(args.warmup, 1)):
+        _oracle_call(cfg, o, np.arange(n_tok))
+    steps = max(1, min(args.steps, args.ref_steps))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _oracle_call(cfg, o, np.arange(n_tok))
+    dt = time.perf_counter() - t0
+    val = n_tok * steps / dt
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = f"{n_tok} of {cfg.T} tokens per step, {steps} steps, CPU oracle (numpy float64)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * dt / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.describe()},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--ref-steps", type=int, default=5)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
