@@ -17,7 +17,8 @@
  * Conventions for every call below:
  *   - Pointers are DEVICE pointers unless the name starts with h_ (host memory).
  *   - bf16 tensors are raw bfloat16 bit patterns (uint16_t), row-major, densely packed,
- *     16-byte aligned.  int32/float tensors are 4-byte aligned, densely packed.
+ *     16-byte aligned (router_logits: 2-byte).  int32/float tensors are 4-byte aligned,
+ *     densely packed.
  *   - The caller owns every buffer, including the workspace.  No call allocates device
  *     memory after moe_lora_create, so moe_lora_route/permute/forward can be captured
  *     in a CUDA graph on `stream` (the side stream is forked from and joined back to it).

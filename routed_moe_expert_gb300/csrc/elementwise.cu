@@ -1,5 +1,5 @@
 // Memory-bound stages of the routed MoE-LoRA layer: token permute, SwiGLU activation
-// with the gate_up LoRA delta, and the weighted top-k finalize with the down LoRA.
+// with the gate_up LoRA delta, and the weighted top-k finalize.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -73,74 +73,39 @@ cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, in
 }
 
 // ---------------------------------------------------------------------------------
-// finalize: out[t, h] = bf16( sum_{j<k} w[t,j] * ( y[q_j, h] + scaling_s *
-//                              sum_{r<rank_s} B_dn[s, e_j, h, r] * v[q_j, r] ) )
-// with q_j = inv[t*k + j], fixed j order (vLLM API page "fused_moe/experts/
-// trtllm_lora_moe", _finalize_with_w2_lora: routing-weighted sum of the permuted base
-// rows over top_k plus the routing-weighted down-LoRA delta; the down expand of sglang
-// PR #28466's merged_experts_fused_moe_lora_add(down) is fused in here).
-// One CTA per token; each thread owns 8 consecutive h.
+// finalize: out[t, h] = bf16( sum_{j<k} w[t,j] * y[inv[t*k + j], h] ), fixed j order.
+// y already holds the down GEMM output plus the (unweighted) down-LoRA delta, added in
+// the down GEMM's epilogue, so this is the vLLM API page's _finalize_with_w2_lora
+// ("fused_moe/experts/trtllm_lora_moe": routing-weighted sum over top_k of the base rows
+// plus the routing-weighted down-LoRA delta).  One CTA per token, 4 floats per thread.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) finalize_kernel(const FinalizeParams p) {
-  __shared__ int q_s[kMaxTopK], e_s[kMaxTopK];
+  __shared__ int q_s[kMaxTopK];
   __shared__ float w_s[kMaxTopK];
-  __shared__ float v_s[kMaxTopK * kMaxRank];
-  __shared__ int lora_s;
   const int t = blockIdx.x, k = p.k, tid = threadIdx.x;
-  const LoraSlots& L = p.slots;
-  if (tid == 0) {
-    int use = 0;
-    if (p.v != nullptr) {
-      const int s = p.slot_idx[t];
-      if (s < -1 || s >= L.S) {
-        record_status(p.status, kDevBadSlot, kWhereFinalize);
-      } else if (s >= 0 && L.ranks[s] > 0 && L.scal[s] != 0.0f) {
-        use = s + 1;
-      }
-    }
-    lora_s = use;
-  }
   if (tid < k) {
     const size_t pp = static_cast<size_t>(t) * k + tid;
     q_s[tid] = p.inv[pp];
-    e_s[tid] = p.ids[pp];
     w_s[tid] = p.weights[pp];
   }
   __syncthreads();
-  const int s = lora_s - 1;
-  const int rank = s >= 0 ? L.ranks[s] : 0;
-  if (s >= 0) {
-    for (int i = tid; i < k * rank; i += blockDim.x) {
-      const int j = i / rank, r = i - j * rank;
-      v_s[j * kMaxRank + r] = p.v[static_cast<size_t>(q_s[j]) * L.R + r];
-    }
-  }
-  __syncthreads();
-  const float sc = s >= 0 ? L.scal[s] : 0.0f;
-  const int H8 = p.H >> 3;
-  for (int h8 = tid; h8 < H8; h8 += blockDim.x) {
-    const int h0 = h8 * 8;
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  const int H4 = p.H >> 2;
+  for (int h4 = tid; h4 < H4; h4 += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
-      float yv[8];
-      unpack8(*reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(q_s[j]) * p.H + h0), yv);
-      if (s >= 0) {
-        const __nv_bfloat16* Bb = p.B + ((static_cast<size_t>(s) * L.E + e_s[j]) * p.H + h0) * L.R;
-        const float* vj = v_s + j * kMaxRank;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const __nv_bfloat16* Brow = Bb + static_cast<size_t>(i) * L.R;
-          float dd = 0.0f;
-          for (int r = 0; r < rank; ++r) dd += bf2f(Brow[r]) * vj[r];
-          yv[i] += sc * dd;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += w_s[j] * yv[i];
+      const float4 y = __ldg(reinterpret_cast<const float4*>(p.y + static_cast<size_t>(q_s[j]) * p.H) + h4);
+      const float w = w_s[j];
+      acc.x += w * y.x;
+      acc.y += w * y.y;
+      acc.z += w * y.z;
+      acc.w += w * y.w;
     }
-    *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.H + h0) = pack8(acc);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[h4] = v;
   }
 }
 

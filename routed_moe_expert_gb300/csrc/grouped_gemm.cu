@@ -38,10 +38,14 @@ constexpr int kMaxStages = 16;
 
 int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
-int gemm_smem_bytes(int bn, int stages, int E) {
-  // 1 KB alignment slack, stage buffers, barriers, tmem slot + abort flag, schedule
-  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1);
+int gemm_smem_bytes(int bn, int stages, int E, int lora_R) {
+  // 1 KB alignment slack, stage buffers, barriers, tmem slot + abort flag, schedule,
+  // and (LoRA epilogue) per-token slots and shrink values of one tile
+  const int lora = lora_R > 0 ? 16 + bn * 4 + bn * lora_R * 4 : 0;
+  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + lora;
 }
+
+MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -63,6 +67,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);   // [E + 1]
   int* seg = tile_start + (p.E + 1);                         // offsets copy [E + 1]
+  int* lslot = seg + (p.E + 1) + 4;                          // [BN] (LoRA epilogue)
+  float* v_s = reinterpret_cast<float*>(lslot + BN);         // [BN][R]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -216,26 +222,102 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   } else {   // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // weight row inside the tile == TMEM lane
+    const int etid = threadIdx.x - 64;     // 0..127 over the epilogue warps
+    const bool lora = p.lora_v != nullptr;
+    const int R = p.slots.R;
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, nt, qt;
       decode(tile, e, nt, qt);
-      if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
-      tc_fence_after();
       const int col = nt * 128 + row;
       const int q0 = seg[e] + qt * BN;
       const int nvalid = min(BN, seg[e + 1] - q0);
+      if (lora) {   // stage the tile's token slots and down-LoRA shrink values
+        epi_bar();
+        for (int j = etid; j < nvalid; j += 128) {
+          const int t = p.perm[q0 + j] / p.k;
+          int sl = p.slot_idx[t];
+          if (sl < -1 || sl >= p.slots.S) {
+            record_status(p.status, kDevBadSlot, kWhereGemmEpilogue);
+            sl = -1;
+          } else if (sl >= 0 && (p.slots.ranks[sl] <= 0 || p.slots.scal[sl] == 0.0f)) {
+            sl = -1;
+          }
+          lslot[j] = sl;
+        }
+        epi_bar();
+        for (int i = etid; i < nvalid * R; i += 128) {
+          const int j = i / R, r = i - j * R;
+          const int sl = lslot[j];
+          v_s[i] = (sl >= 0 && r < p.slots.ranks[sl]) ? p.lora_v[static_cast<size_t>(q0 + j) * R + r] : 0.0f;
+        }
+        epi_bar();
+      }
+      if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+      tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
         uint32_t r[16];
         tmem_ld_x16(taddr + c, r);
         tmem_ld_wait();
-        if (col < p.N) {
-          __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * p.N + col;
+        float val[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c + j < nvalid) o[static_cast<size_t>(j) * p.N] = f2bf(__uint_as_float(r[j]));
+        for (int j = 0; j < 16; ++j) val[j] = __uint_as_float(r[j]);
+        if (lora && col < p.N) {
+          // down-LoRA expand, one slot at a time (slots are uniform across the warp)
+          uint32_t done = 0;
+          for (int j0 = 0; j0 < 16 && c + j0 < nvalid; ++j0) {
+            if ((done >> j0) & 1u) continue;
+            const int sl = lslot[c + j0];
+            uint32_t m = 0;
+            for (int j = j0; j < 16 && c + j < nvalid; ++j)
+              if (lslot[c + j] == sl) m |= 1u << j;
+            done |= m;
+            if (sl < 0) continue;
+            const int rank = p.slots.ranks[sl];
+            const float sc = p.slots.scal[sl];
+            const __nv_bfloat16* Brow =
+                p.lora_B + ((static_cast<size_t>(sl) * p.E + e) * p.N + col) * static_cast<size_t>(R);
+            float dd[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dd[j] = 0.0f;
+            for (int r0 = 0; r0 < rank; r0 += 8) {
+              float b[8];
+              if ((R & 7) == 0 && r0 + 8 <= rank) {
+                unpack8(__ldg(reinterpret_cast<const uint4*>(Brow + r0)), b);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b[i] = (r0 + i < rank) ? bf2f(Brow[r0 + i]) : 0.0f;
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if ((m >> j) & 1u) {
+                  const float* vj = v_s + (c + j) * R + r0;
+                  float sacc = 0.0f;
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) sacc += (r0 + i < rank) ? b[i] * vj[i] : 0.0f;
+                  dd[j] += sacc;
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if ((m >> j) & 1u) val[j] += sc * dd[j];
+          }
+        }
+        if (col < p.N) {
+          if (p.out_f32 != nullptr) {
+            float* o = p.out_f32 + static_cast<size_t>(q0 + c) * p.N + col;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c + j < nvalid) o[static_cast<size_t>(j) * p.N] = val[j];
+          } else {
+            __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * p.N + col;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c + j < nvalid) o[static_cast<size_t>(j) * p.N] = f2bf(val[j]);
+          }
         }
       }
       tc_fence_before();
@@ -264,7 +346,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
 template <int BN>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream) {
-  const int smem = gemm_smem_bytes(BN, p.stages, p.E);
+  const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0);
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   grouped_gemm_kernel<BN><<<grid, kGemmThreads, smem, stream>>>(p);

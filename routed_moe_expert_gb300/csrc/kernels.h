@@ -20,6 +20,12 @@ enum : uint32_t {
   kWhereLoraShrinkGu = 5, kWhereLoraExpandGu = 6, kWhereLoraShrinkDn = 7, kWhereFinalize = 8,
 };
 
+struct LoraSlots {
+  int S, E, R;
+  int ranks[kMaxSlots];
+  float scal[kMaxSlots];
+};
+
 // ---------------------------------------------------------------- routing + align
 struct RouteParams {
   const __nv_bfloat16* logits;   // [T, E]
@@ -49,12 +55,21 @@ int route_max_coop_ctas(int E);
 struct GemmParams {
   CUtensorMap tmap_w;            // weights [E*N rows, K cols], box {64, 64}
   CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN}
-  __nv_bfloat16* out;            // [P, N]
+  __nv_bfloat16* out;            // [P, N] bf16 output, or
+  float* out_f32;                //   fp32 output when non-null
   const int32_t* offsets;        // [E + 1]
   uint32_t* status;
   int E, N, K, gated, stages;
+  // Optional LoRA expand added in the epilogue before the store (down GEMM):
+  // out[q, h] += scaling[s] * sum_{r<ranks[s]} lora_B[s, e, h, r] * lora_v[q, r]
+  const float* lora_v;           // [P, R] or null
+  const __nv_bfloat16* lora_B;   // [S, E, N, R]
+  const int32_t* perm;           // [P]
+  const int32_t* slot_idx;       // [T]
+  int k;
+  LoraSlots slots;
 };
-int gemm_smem_bytes(int bn, int stages, int E);
+int gemm_smem_bytes(int bn, int stages, int E, int lora_R);
 int gemm_stage_bytes(int bn);
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream);
 
@@ -64,54 +79,36 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, i
 cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
                               __nv_bfloat16* a, cudaStream_t stream);
 
-struct LoraSlots {
-  int S, E, R;
-  int ranks[kMaxSlots];
-  float scal[kMaxSlots];
-};
 
 struct FinalizeParams {
-  const __nv_bfloat16* y;        // [P, H] permuted down output
-  const float* v;                // [P, R] down-LoRA shrink (null: no LoRA)
-  const __nv_bfloat16* B;        // [S, E, H, R]
-  const int32_t* ids;            // [T, k]
+  const float* y;                // [P, H] permuted down output (down-LoRA delta included)
   const float* weights;          // [T, k]
   const int32_t* inv;            // [T * k]
-  const int32_t* slot_idx;       // [T]
   int T, H, k;
-  LoraSlots slots;
   __nv_bfloat16* out;            // [T, H]
-  uint32_t* status;
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LoRA
-struct ShrinkParams {
+// Tensor-core LoRA over expert tiles of 8*ntl pairs: shrink u = A . src (fp32) and, when
+// B is set, expand d = bf16(scaling * B . bf16(u)) written in logical [gate | up] order.
+// With B null, u is written to u_out [P, R] (down-LoRA shrink).
+struct LoraParams {
   const __nv_bfloat16* src;      // hidden [T, K] (by_token) or activation [P, K]
   int by_token;
   const int32_t* perm;           // [P]
-  const int32_t* ids;            // [T, k]
   const int32_t* slot_idx;       // [T]
-  int k, P, K;
+  const int32_t* offsets;        // [E + 1]
+  int k, P, K, E, N;             // N: expand output width (2I)
   const __nv_bfloat16* A;        // [S, E, R, K]
+  const __nv_bfloat16* B;        // [S, E, N, R] or null
   LoraSlots slots;
-  float* u;                      // [P, R]
+  float* u_out;                  // [P, R] (shrink only)
+  __nv_bfloat16* d_out;          // [P, N] (expand)
   uint32_t* status;
   uint32_t where;
 };
-cudaError_t launch_lora_shrink(const ShrinkParams& p, cudaStream_t stream);
-
-struct ExpandParams {
-  const float* u;                // [P, R]
-  const int32_t* perm;
-  const int32_t* ids;
-  const int32_t* slot_idx;
-  int k, P, N;                   // N = 2I
-  const __nv_bfloat16* B;        // [S, E, N, R]
-  LoraSlots slots;
-  __nv_bfloat16* d;              // [P, N], logical [gate | up] order
-  uint32_t* status;
-};
-cudaError_t launch_lora_expand(const ExpandParams& p, cudaStream_t stream);
+size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E);
+cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream);
 
 }  // namespace mlk

@@ -1,121 +1,298 @@
-// Per-expert LoRA shrink (A) and expand (B) with per-token adapter slots of mixed rank.
+// Per-expert LoRA shrink (A) and expand (B) on the tensor cores, with per-token adapter
+// slots of mixed rank.
 //
-// shrink: u[q, r] = sum_k A[s, e, r, k] * src[row(q), k]    for r < ranks[s]   (fp32)
-// expand: d[q, n] = bf16( scaling[s] * sum_{r<ranks[s]} B[s, e, n, r] * u[q, r] )
-// for the pair q (permuted order) with expert e and token slot s; pairs whose token
-// has no adapter (slot -1, rank 0 or scaling 0) get d = 0 and no shrink.
+//   shrink: u[q, r] = sum_k A[s, e, r, k] * src[row(q), k]                   (fp32)
+//   expand: d[q, n] = bf16( scaling[s] * sum_{r<ranks[s]} B[s, e, n, r] * bf16(u[q, r]) )
 //
-// The gate_up chain (shrink on the hidden row, expand into the bf16 delta added before
-// SwiGLU) is sglang PR #28466's merged_experts_fused_moe_lora_add(gate_up), section 1
-// flow (B): "gate_up shrink + expand -> gate_up_lora_delta", run on the side stream;
-// the down chain's shrink runs on the activation and its expand is fused into the
-// finalize.  The split of K across the 32 lanes of a warp, reduced in a fixed order,
-// is the split-K shrink of sglang PR #27329 "Experimental fast LoRA path"
-// (Optimizations: "Split-K LoRA shrink with the fp32->bf16 cast fused into the LoRA-B
-// expand"): the fp32 shrink result is read by the expand, which rounds once, on output.
+// for the pair q (permuted order) of expert e whose token has slot s.  Pairs whose
+// token has no adapter (slot -1, rank 0 or scaling 0) get d = 0 and no u.
+//
+// The gate_up chain (shrink on the hidden row, expand into the bf16 delta that the
+// activation adds before SwiGLU) is sglang PR #28466's merged_experts_fused_moe_lora_add
+// (gate_up), section 1 flow (B), run on the side stream; the down chain uses the shrink
+// only (on the activation), and its expand is applied in the down GEMM's epilogue.
+// The shrink splits K across the 8 warps of a CTA and reduces the partial sums in a
+// fixed warp order, and the expand casts the fp32 shrink result to bf16 as it loads it:
+// the split-K shrink with the fp32->bf16 cast fused into the expand of sglang PR #27329
+// "Experimental fast LoRA path" (Optimizations).
+//
+// A CTA tile is one expert and up to 8*NTL consecutive permuted pairs of it, so every
+// (slot, expert) adapter block is read once per tile.  Pairs of different slots share a
+// tile: each slot present is processed in turn with the other pairs' columns zeroed.
 // Only ranks r < ranks[s] are read, so the unused tail of a stacked adapter never
-// enters the result.
+// enters the result.  Tensor-core work is mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+// these are small GEMMs (M = rank, N = 8 pairs) that sit beside the tcgen05 expert GEMMs.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mlk {
 
-// Slot of a pair's token, or -1 when it gets no LoRA.  Records a device-check status
-// for an index outside [-1, S).
-MLDEV int lora_slot(const LoraSlots& L, const int32_t* slot_idx, int t, uint32_t* status, uint32_t where) {
-  const int s = slot_idx[t];
-  if (s < -1 || s >= L.S) {
-    record_status(status, kDevBadSlot, where);
-    return -1;
-  }
-  if (s < 0 || L.ranks[s] <= 0 || L.scal[s] == 0.0f) return -1;
-  return s;
+constexpr int kLoraThreads = 256;
+constexpr int kLoraWarps = 8;
+constexpr int kMaxMT = kMaxRank / 16;   // rank m-tiles of 16
+
+MLDEV void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// One warp per permuted pair q; lanes split K in 8-element vectors.
-__global__ void __launch_bounds__(256) lora_shrink_kernel(const ShrinkParams p) {
-  const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (q >= p.P) return;
-  const int pp = p.perm[q];
-  const int t = pp / p.k;
-  const int s = lora_slot(p.slots, p.slot_idx, t, lane == 0 ? p.status : nullptr, p.where);
-  if (s < 0) return;
-  const int e = p.ids[pp];
-  const int rank = p.slots.ranks[s];
-  const int K8 = p.K >> 3;
-  const int row = p.by_token ? t : q;
-  const uint4* xr = reinterpret_cast<const uint4*>(p.src + static_cast<size_t>(row) * p.K);
-  const uint4* Ab = reinterpret_cast<const uint4*>(
-      p.A + (static_cast<size_t>(s) * p.slots.E + e) * static_cast<size_t>(p.slots.R) * p.K);
-  for (int r0 = 0; r0 < rank; r0 += 4) {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int v = lane; v < K8; v += 32) {
-      float xf[8];
-      unpack8(__ldg(xr + v), xf);
+MLDEV uint32_t ld_b32(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const unsigned int*>(p)); }
+
+MLDEV uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E) {
+  const int PT = 8 * ntl;
+  const int RP = ((R + 15) / 16) * 16;
+  size_t b = 0;
+  b += static_cast<size_t>(kLoraWarps) * RP * PT * 4;     // per-warp partials
+  b += static_cast<size_t>(PT) * RP * 4;                  // u (fp32)
+  b += static_cast<size_t>(PT) * (RP + 8) * 2;            // u as bf16 (padded rows)
+  if (expand) b += static_cast<size_t>(PT) * N * 2;       // staged d rows
+  b += static_cast<size_t>(PT) * 12 + 16;                 // pair info + slot mask
+  b += 4 * (static_cast<size_t>(E) + 1);                  // schedule
+  return b;
+}
+
+template <int NTL>
+__global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams p) {
+  constexpr int PT = 8 * NTL;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int R = p.slots.R;
+  const int RP = ((R + 15) / 16) * 16;
+  const bool expand = p.B != nullptr;
+  float* red = reinterpret_cast<float*>(smem);                                  // [8][RP][PT]
+  float* u_s = red + kLoraWarps * RP * PT;                                      // [PT][RP]
+  __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(u_s + PT * RP);         // [PT][RP+8]
+  __nv_bfloat16* dst = ub + PT * (RP + 8);                                      // [PT][N]
+  int* prow = reinterpret_cast<int*>(dst + (expand ? PT * p.N : 0));            // [PT]
+  int* pslot = prow + PT;                                                       // [PT]
+  int* pq = pslot + PT;                                                         // [PT]
+  unsigned* smask = reinterpret_cast<unsigned*>(pq + PT);                       // [2]: slots 0-31, 32-63
+  int* tile_start = reinterpret_cast<int*>(smask + 4);                          // [E+1]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int E = p.E;
+
+  if (warp == 0) {   // tile schedule over experts: ceil(M_e / PT) tiles each
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int cnt = (e < E) ? (p.offsets[e + 1] - p.offsets[e] + PT - 1) / PT : 0;
+      int incl = cnt;
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        if (r0 + rr < rank) {
-          float af[8];
-          unpack8(__ldg(Ab + static_cast<size_t>(r0 + rr) * K8 + v), af);
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (e < E) tile_start[e] = carry + incl - cnt;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[E] = carry;
+  }
+  __syncthreads();
+  const int total = tile_start[E];
+  const int K16 = p.K >> 4;
+
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int q0 = p.offsets[e] + (tile - tile_start[e]) * PT;
+    const int np = min(PT, p.offsets[e + 1] - q0);
+
+    if (tid == 0) smask[0] = smask[1] = 0u;
+    __syncthreads();
+    if (tid < PT) {
+      int s = -1, row = 0, q = q0 + tid;
+      if (tid < np) {
+        const int pp = p.perm[q];
+        const int t = pp / p.k;
+        row = p.by_token ? t : q;
+        s = p.slot_idx[t];
+        if (s < -1 || s >= p.slots.S) {
+          record_status(p.status, kDevBadSlot, p.where);
+          s = -1;
+        } else if (s >= 0 && (p.slots.ranks[s] <= 0 || p.slots.scal[s] == 0.0f)) {
+          s = -1;
+        }
+        if (s >= 0) atomicOr(&smask[s >> 5], 1u << (s & 31));
+      }
+      prow[tid] = row;
+      pslot[tid] = s;
+      pq[tid] = q;
+    }
+    if (expand) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      for (int i = tid; i < PT * p.N / 8; i += kLoraThreads) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    const unsigned mask0 = smask[0], mask1 = smask[1];
+
+    for (int s = 0; s < p.slots.S; ++s) {
+      if (!(((s < 32 ? mask0 : mask1) >> (s & 31)) & 1u)) continue;
+      const int rank = p.slots.ranks[s];
+      const int MT = (rank + 15) >> 4;
+      const __nv_bfloat16* A = p.A + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(R) * p.K;
+
+      // ---------------- shrink: warps split the K steps; partials to smem
+      float acc[kMaxMT][NTL][4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[rr] += af[i] * xf[i];
+      for (int mt = 0; mt < kMaxMT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.0f;
+      const __nv_bfloat16* xrow[NTL];
+      bool xon[NTL];
+#pragma unroll
+      for (int nt = 0; nt < NTL; ++nt) {
+        const int n = nt * 8 + g;
+        xon[nt] = (n < np) && (pslot[n] == s);
+        xrow[nt] = p.src + static_cast<size_t>(prow[n]) * p.K;
+      }
+      for (int ks = warp; ks < K16; ks += kLoraWarps) {
+        const int k0 = ks * 16 + 2 * c;
+        uint32_t bf[NTL][2];
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+          bf[nt][0] = xon[nt] ? ld_b32(xrow[nt] + k0) : 0u;
+          bf[nt][1] = xon[nt] ? ld_b32(xrow[nt] + k0 + 8) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < kMaxMT; ++mt) {
+          if (mt < MT) {
+            const int r0 = mt * 16 + g, r1 = r0 + 8;
+            uint32_t af[4];
+            af[0] = r0 < rank ? ld_b32(A + static_cast<size_t>(r0) * p.K + k0) : 0u;
+            af[1] = r1 < rank ? ld_b32(A + static_cast<size_t>(r1) * p.K + k0) : 0u;
+            af[2] = r0 < rank ? ld_b32(A + static_cast<size_t>(r0) * p.K + k0 + 8) : 0u;
+            af[3] = r1 < rank ? ld_b32(A + static_cast<size_t>(r1) * p.K + k0 + 8) : 0u;
+#pragma unroll
+            for (int nt = 0; nt < NTL; ++nt) mma_bf16_16816(acc[mt][nt], af, bf[nt]);
+          }
         }
       }
-    }
+      // partial [r][n] of this warp
+      float* rw = red + warp * RP * PT;
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      float v = acc[rr];
+      for (int mt = 0; mt < kMaxMT; ++mt) {
+        if (mt < MT) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0 && r0 + rr < rank) p.u[static_cast<size_t>(q) * p.slots.R + r0 + rr] = v;
+          for (int nt = 0; nt < NTL; ++nt) {
+            const int r0 = mt * 16 + g, n0 = nt * 8 + 2 * c;
+            rw[r0 * PT + n0] = acc[mt][nt][0];
+            rw[r0 * PT + n0 + 1] = acc[mt][nt][1];
+            rw[(r0 + 8) * PT + n0] = acc[mt][nt][2];
+            rw[(r0 + 8) * PT + n0 + 1] = acc[mt][nt][3];
+          }
+        }
+      }
+      __syncthreads();
+      // fixed-order reduction over the 8 warps
+      for (int i = tid; i < MT * 16 * PT; i += kLoraThreads) {
+        const int r = i / PT, n = i - r * PT;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kLoraWarps; ++w) v += red[w * RP * PT + i];
+        const bool mine = (n < np) && (pslot[n] == s) && (r < rank);
+        u_s[n * RP + r] = mine ? v : 0.0f;
+        if (!expand && mine) p.u_out[static_cast<size_t>(pq[n]) * R + r] = v;
+      }
+      __syncthreads();
+      if (!expand) continue;
+
+      // ---------------- expand: B operand = bf16(u), features split across warps
+      for (int i = tid; i < PT * MT * 16; i += kLoraThreads) {
+        const int n = i / (MT * 16), r = i - n * (MT * 16);
+        ub[n * (RP + 8) + r] = __float2bfloat16_rn(u_s[n * RP + r]);
+      }
+      __syncthreads();
+      const float sc = p.slots.scal[s];
+      const __nv_bfloat16* Bm = p.B + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(p.N) * R;
+      const int NM = p.N >> 4;
+      for (int fm = warp; fm < NM; fm += kLoraWarps) {
+        const int f0 = fm * 16 + g, f1 = f0 + 8;
+        float acc2[NTL][4];
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc2[nt][i] = 0.0f;
+        for (int kt = 0; kt < MT; ++kt) {
+          const int r0 = kt * 16 + 2 * c, r1 = r0 + 8;
+          uint32_t af[4];
+          // B rows have stride R (any rank); load element pairs only below the rank
+          const __nv_bfloat16* b0 = Bm + static_cast<size_t>(f0) * R;
+          const __nv_bfloat16* b1 = Bm + static_cast<size_t>(f1) * R;
+          auto pair = [&](const __nv_bfloat16* row, int r) -> uint32_t {
+            if (r + 1 < rank && (R & 1) == 0) return ld_b32(row + r);   // 4-byte aligned pair
+            const float lo = r < rank ? __bfloat162float(row[r]) : 0.0f;
+            const float hi = r + 1 < rank ? __bfloat162float(row[r + 1]) : 0.0f;
+            return pack_bf16x2(lo, hi);
+          };
+          af[0] = pair(b0, r0);
+          af[1] = pair(b1, r0);
+          af[2] = pair(b0, r1);
+          af[3] = pair(b1, r1);
+#pragma unroll
+          for (int nt = 0; nt < NTL; ++nt) {
+            const __nv_bfloat16* urow = ub + (nt * 8 + g) * (RP + 8);
+            uint32_t bfr[2];
+            bfr[0] = *reinterpret_cast<const uint32_t*>(urow + kt * 16 + 2 * c);
+            bfr[1] = *reinterpret_cast<const uint32_t*>(urow + kt * 16 + 2 * c + 8);
+            mma_bf16_16816(acc2[nt], af, bfr);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+          const int n0 = nt * 8 + 2 * c, n1 = n0 + 1;
+          if (n0 < np && pslot[n0] == s) {
+            dst[n0 * p.N + f0] = __float2bfloat16_rn(sc * acc2[nt][0]);
+            dst[n0 * p.N + f1] = __float2bfloat16_rn(sc * acc2[nt][2]);
+          }
+          if (n1 < np && pslot[n1] == s) {
+            dst[n1 * p.N + f0] = __float2bfloat16_rn(sc * acc2[nt][1]);
+            dst[n1 * p.N + f1] = __float2bfloat16_rn(sc * acc2[nt][3]);
+          }
+        }
+      }
+      __syncthreads();
     }
+
+    if (expand) {   // staged rows (zeros for pairs without an adapter) -> d
+      const int N8 = p.N >> 3;
+      const uint4* s4 = reinterpret_cast<const uint4*>(dst);
+      for (int i = tid; i < np * N8; i += kLoraThreads) {
+        const int n = i / N8, j = i - n * N8;
+        reinterpret_cast<uint4*>(p.d_out + static_cast<size_t>(pq[n]) * p.N)[j] = s4[i];
+      }
+    }
+    __syncthreads();
   }
 }
 
-cudaError_t launch_lora_shrink(const ShrinkParams& p, cudaStream_t stream) {
+cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream) {
   if (p.P == 0) return cudaSuccess;
-  lora_shrink_kernel<<<(p.P + 7) / 8, 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-// One CTA per permuted pair q; each thread produces 8 consecutive n.
-__global__ void __launch_bounds__(256) lora_expand_kernel(const ExpandParams p) {
-  __shared__ float u_s[kMaxRank];
-  __shared__ int slot_s;
-  const int q = blockIdx.x, tid = threadIdx.x;
-  const int pp = p.perm[q];
-  if (tid == 0) slot_s = lora_slot(p.slots, p.slot_idx, pp / p.k, p.status, kWhereLoraExpandGu);
-  __syncthreads();
-  const int s = slot_s;
-  const int N8 = p.N >> 3;
-  uint4* drow = reinterpret_cast<uint4*>(p.d + static_cast<size_t>(q) * p.N);
-  if (s < 0) {
-    for (int n8 = tid; n8 < N8; n8 += blockDim.x) drow[n8] = make_uint4(0u, 0u, 0u, 0u);
-    return;
+  const size_t smem = lora_smem_bytes(ntl, p.slots.R, p.N, p.B != nullptr, p.E);
+  cudaError_t err;
+  if (ntl == 1) {
+    err = cudaFuncSetAttribute(lora_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    lora_mma_kernel<1><<<grid, kLoraThreads, smem, stream>>>(p);
+  } else {
+    err = cudaFuncSetAttribute(lora_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    lora_mma_kernel<4><<<grid, kLoraThreads, smem, stream>>>(p);
   }
-  const int rank = p.slots.ranks[s];
-  for (int r = tid; r < rank; r += blockDim.x) u_s[r] = p.u[static_cast<size_t>(q) * p.slots.R + r];
-  __syncthreads();
-  const float sc = p.slots.scal[s];
-  const int e = p.ids[pp];
-  const __nv_bfloat16* Bb = p.B + (static_cast<size_t>(s) * p.slots.E + e) * static_cast<size_t>(p.N) * p.slots.R;
-  for (int n8 = tid; n8 < N8; n8 += blockDim.x) {
-    float out[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __nv_bfloat16* Brow = Bb + static_cast<size_t>(n8 * 8 + i) * p.slots.R;
-      float acc = 0.0f;
-      for (int r = 0; r < rank; ++r) acc += bf2f(Brow[r]) * u_s[r];
-      out[i] = sc * acc;
-    }
-    drow[n8] = pack8(out);
-  }
-}
-
-cudaError_t launch_lora_expand(const ExpandParams& p, cudaStream_t stream) {
-  if (p.P == 0) return cudaSuccess;
-  lora_expand_kernel<<<p.P, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

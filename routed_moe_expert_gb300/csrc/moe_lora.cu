@@ -4,9 +4,9 @@
 // Launch sequence of moe_lora_forward (sglang PR #28466 "bf16 MoE-LoRA for trtllm
 // backend", section 1 flows (A) single-stream and (B) two-stream):
 //   main: memset(status) -> route_align -> [fork] -> permute -> gate_up GEMM
-//         -> [join on the LoRA-ready event] -> activation -> down GEMM
-//         -> down-LoRA shrink -> finalize (+ down-LoRA expand)
-//   side: [wait fork] -> gate_up LoRA shrink -> expand -> [record ready]
+//         -> [join on the LoRA-ready event] -> activation -> down-LoRA shrink
+//         -> down GEMM (down-LoRA expand in its epilogue, fp32 out) -> finalize
+//   side: [wait fork] -> gate_up LoRA shrink + expand (one kernel) -> [record ready]
 // Every buffer the side stream touches lives in the caller's workspace, which exists
 // before the fork, so nothing is allocated while a graph may be capturing (the
 // multi-slot replay bug of sglang PR #28091, Motivation 3, cannot arise).
@@ -40,11 +40,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout (all offsets 256-byte aligned).  y (down GEMM output) reuses the
-// permuted-hidden buffer, which is dead once the gate_up GEMM has run.
+// Workspace layout (all offsets 256-byte aligned).
 struct Layout {
   size_t header, ids, wts, offsets, perm, inv, hist, base, total;
-  size_t xp, g, d, u, a, v;
+  size_t xp, g, d, a, v, y;
   size_t bytes;
 };
 
@@ -69,9 +68,9 @@ Layout layout_for(int T, int H, int I, int E, int k, int R) {
   L.xp = take(P * H * 2);
   L.g = take(P * 2 * I * 2);
   L.d = take(R > 0 ? P * 2 * I * 2 : 0);
-  L.u = take(P * R * 4);
   L.a = take(P * I * 2);
   L.v = take(P * R * 4);
+  L.y = take(P * H * 4);
   L.bytes = off;
   return L;
 }
@@ -160,9 +159,8 @@ moe_lora_status moe_lora_validate(const moe_lora_args* a) {
     if (lora_active(a)) {
       if (a->lora_A_gu == nullptr || a->lora_B_gu == nullptr || a->lora_A_dn == nullptr || a->lora_B_dn == nullptr)
         return MOE_LORA_ERR_INVALID_ARG;
-      if (!aligned16(a->lora_A_gu) || !aligned16(a->lora_A_dn) || !aligned4(a->slot_idx))
-        return MOE_LORA_ERR_INVALID_ARG;
-      if ((reinterpret_cast<uintptr_t>(a->lora_B_gu) & 1u) || (reinterpret_cast<uintptr_t>(a->lora_B_dn) & 1u))
+      if (!aligned16(a->lora_A_gu) || !aligned16(a->lora_A_dn) || !aligned16(a->lora_B_gu) ||
+          !aligned16(a->lora_B_dn) || !aligned4(a->slot_idx))
         return MOE_LORA_ERR_INVALID_ARG;
     }
   }
@@ -274,29 +272,20 @@ int pick_bn(long long P, int E) {
   return 256;
 }
 
-int pick_stages(int bn, int E) {
+int pick_stages(int bn, int E, int lora_R) {
   const int budget = (bn <= 32 ? 160 : 200) * 1024;
-  const int fixed = gemm_smem_bytes(bn, 0, E);
+  const int fixed = gemm_smem_bytes(bn, 0, E, lora_R);
   int s = (budget - fixed) / (gemm_stage_bytes(bn) + 16);
   if (s > 16) s = 16;
   if (s < 2) s = 2;
   return s;
 }
 
-moe_lora_status enqueue_gemm(moe_lora_handle* h, const void* W, const void* X, void* out, const int32_t* offsets,
-                             uint32_t* status, int E, int N, int K, int P, int gated, int bn, cudaStream_t stream) {
-  GemmParams gp;
-  std::memset(&gp, 0, sizeof(gp));
-  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(E) * N, K, 64)) return MOE_LORA_ERR_CUDA;
-  if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), K, bn)) return MOE_LORA_ERR_CUDA;
-  gp.out = reinterpret_cast<__nv_bfloat16*>(out);
-  gp.offsets = offsets;
-  gp.status = status;
-  gp.E = E;
-  gp.N = N;
-  gp.K = K;
-  gp.gated = gated;
-  gp.stages = pick_stages(bn, E);
+moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, const void* X, int P, int bn,
+                             cudaStream_t stream) {
+  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
+  if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
+  gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0);
   ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
@@ -383,10 +372,9 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + L.xp);
   __nv_bfloat16* g = reinterpret_cast<__nv_bfloat16*>(ws + L.g);
   __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(ws + L.d);
-  float* u = reinterpret_cast<float*>(ws + L.u);
   __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
   float* v = reinterpret_cast<float*>(ws + L.v);
-  __nv_bfloat16* y = xp;   // reuse: xp is dead after the gate_up GEMM
+  float* y = reinterpret_cast<float*>(ws + L.y);
 
   prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
   st = enqueue_route(h, a->router_logits, a->correction_bias, T, E, k, a->routing_method, a->routed_scaling_factor,
@@ -395,7 +383,11 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   prof(a, MOE_LORA_STAGE_ROUTE, 1, stream);
 
   LoraSlots slots;
+  std::memset(&slots, 0, sizeof(slots));
   if (lora) slots = make_slots(a);
+  const int lora_ntl = (P >= 32 * E) ? 4 : 1;
+  int lora_grid = (P + 8 * lora_ntl - 1) / (8 * lora_ntl) + E;
+  if (lora_grid > 2 * h->num_sms) lora_grid = 2 * h->num_sms;
   const bool two = lora && (((T <= 256) && !(a->flags & MOE_LORA_FLAG_FORCE_SINGLE_STREAM)) ||
                             (a->flags & MOE_LORA_FLAG_FORCE_TWO_STREAM));
   cudaStream_t ls = two ? h->side : stream;
@@ -405,34 +397,25 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
       ML_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0), "cudaStreamWaitEvent");
     }
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, ls);
-    ShrinkParams sp;
-    sp.src = reinterpret_cast<const __nv_bfloat16*>(a->hidden);
-    sp.by_token = 1;
-    sp.perm = perm;
-    sp.ids = ids;
-    sp.slot_idx = a->slot_idx;
-    sp.k = k;
-    sp.P = P;
-    sp.K = H;
-    sp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_gu);
-    sp.slots = slots;
-    sp.u = u;
-    sp.status = status;
-    sp.where = kWhereLoraShrinkGu;
-    ML_CUDA(launch_lora_shrink(sp, ls), "lora shrink (gate_up) launch");
-    ExpandParams ep;
-    ep.u = u;
-    ep.perm = perm;
-    ep.ids = ids;
-    ep.slot_idx = a->slot_idx;
-    ep.k = k;
-    ep.P = P;
-    ep.N = 2 * I;
-    ep.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
-    ep.slots = slots;
-    ep.d = d;
-    ep.status = status;
-    ML_CUDA(launch_lora_expand(ep, ls), "lora expand (gate_up) launch");
+    LoraParams lp;
+    std::memset(&lp, 0, sizeof(lp));
+    lp.src = reinterpret_cast<const __nv_bfloat16*>(a->hidden);
+    lp.by_token = 1;
+    lp.perm = perm;
+    lp.slot_idx = a->slot_idx;
+    lp.offsets = offsets;
+    lp.k = k;
+    lp.P = P;
+    lp.K = H;
+    lp.E = E;
+    lp.N = 2 * I;
+    lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_gu);
+    lp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
+    lp.slots = slots;
+    lp.d_out = d;
+    lp.status = status;
+    lp.where = kWhereLoraShrinkGu;
+    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, ls), "lora gate_up launch");
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, ls);
     if (two) ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
   }
@@ -444,7 +427,16 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
 
   const int bn = pick_bn(P, E);
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
-  st = enqueue_gemm(h, a->w1, xp, g, offsets, status, E, 2 * I, H, P, 1, bn, stream);
+  GemmParams gu;
+  std::memset(&gu, 0, sizeof(gu));
+  gu.out = g;
+  gu.offsets = offsets;
+  gu.status = status;
+  gu.E = E;
+  gu.N = 2 * I;
+  gu.K = H;
+  gu.gated = 1;
+  st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
@@ -453,47 +445,61 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   ML_CUDA(launch_activation(g, lora ? d : nullptr, P, I, act, stream), "activation launch");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
 
-  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
-  st = enqueue_gemm(h, a->w2, act, y, offsets, status, E, H, I, P, 0, bn, stream);
-  if (st != MOE_LORA_OK) return st;
-  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
-
-  if (lora) {
+  if (lora) {   // down-LoRA shrink v = A_dn . a; its expand runs in the down GEMM epilogue
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
-    ShrinkParams sp;
-    sp.src = act;
-    sp.by_token = 0;
-    sp.perm = perm;
-    sp.ids = ids;
-    sp.slot_idx = a->slot_idx;
-    sp.k = k;
-    sp.P = P;
-    sp.K = I;
-    sp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
-    sp.slots = slots;
-    sp.u = v;
-    sp.status = status;
-    sp.where = kWhereLoraShrinkDn;
-    ML_CUDA(launch_lora_shrink(sp, stream), "lora shrink (down) launch");
+    LoraParams lp;
+    std::memset(&lp, 0, sizeof(lp));
+    lp.src = act;
+    lp.by_token = 0;
+    lp.perm = perm;
+    lp.slot_idx = a->slot_idx;
+    lp.offsets = offsets;
+    lp.k = k;
+    lp.P = P;
+    lp.K = I;
+    lp.E = E;
+    lp.N = 0;
+    lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
+    lp.B = nullptr;
+    lp.slots = slots;
+    lp.u_out = v;
+    lp.status = status;
+    lp.where = kWhereLoraShrinkDn;
+    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, stream), "lora down shrink launch");
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
   }
 
+  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
+  GemmParams dn;
+  std::memset(&dn, 0, sizeof(dn));
+  dn.out_f32 = y;
+  dn.offsets = offsets;
+  dn.status = status;
+  dn.E = E;
+  dn.N = H;
+  dn.K = I;
+  dn.gated = 0;
+  if (lora) {
+    dn.lora_v = v;
+    dn.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
+    dn.perm = perm;
+    dn.slot_idx = a->slot_idx;
+    dn.k = k;
+    dn.slots = slots;
+  }
+  st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+
   prof(a, MOE_LORA_STAGE_FINALIZE, 0, stream);
   FinalizeParams fp;
-  std::memset(&fp, 0, sizeof(fp));
   fp.y = y;
-  fp.v = lora ? v : nullptr;
-  fp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
-  fp.ids = ids;
   fp.weights = wts;
   fp.inv = inv;
-  fp.slot_idx = a->slot_idx;
   fp.T = T;
   fp.H = H;
   fp.k = k;
-  if (lora) fp.slots = slots;
   fp.out = reinterpret_cast<__nv_bfloat16*>(out);
-  fp.status = status;
   ML_CUDA(launch_finalize(fp, stream), "finalize launch");
   prof(a, MOE_LORA_STAGE_FINALIZE, 1, stream);
   return MOE_LORA_OK;
