@@ -385,7 +385,9 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   LoraSlots slots;
   std::memset(&slots, 0, sizeof(slots));
   if (lora) slots = make_slots(a);
-  const int lora_ntl = (P >= 32 * E) ? 4 : 1;
+  // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
+  const int lora_ntl =
+      (P >= 32 * E && lora_smem_bytes(4, a->S > 0 ? a->R : 0, 2 * I, true, E) <= 200 * 1024) ? 4 : 1;
   int lora_grid = (P + 8 * lora_ntl - 1) / (8 * lora_ntl) + E;
   if (lora_grid > 2 * h->num_sms) lora_grid = 2 * h->num_sms;
   const bool two = lora && (((T <= 256) && !(a->flags & MOE_LORA_FLAG_FORCE_SINGLE_STREAM)) ||
