@@ -169,6 +169,25 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
 moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out,
                                  void* workspace, size_t workspace_bytes, moe_lora_stream stream);
 
+/* Routing + expert alignment that allocates nothing and takes no workspace or handle.
+   The pages have no counterpart to this call; it exists for callers that cannot call
+   cudaMalloc or supply a workspace (plug-ins inside a host framework that owns all device
+   memory, allocation-free real-time paths).  Same arguments, outputs and results as
+   moe_lora_route.  The kernel's scratch lives in a 512 KiB array inside the library's
+   device image, held by every GPU that loads the library until the process exits; the
+   routing grid shrinks until its scratch fits (8*E bytes per routing CTA), and a shape
+   that cannot fit is rejected with MOE_LORA_ERR_UNSUPPORTED.  The first call on a device
+   resolves the array's address on the current device (cudaGetSymbolAddress), so make
+   that first call before any stream capture.  All calls share the array: each call
+   clears its status word and barrier counter on `stream`, and calls that overlap on the
+   GPU race.  Device-side wait timeouts are recorded in the shared array, not reported.
+   Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_logits, const float* correction_bias,
+                                       int T, int E, int top_k, int routing_method,
+                                       float routed_scaling_factor, int n_group, int topk_group,
+                                       int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                                       int32_t* perm, int32_t* inv_perm, moe_lora_stream stream);
+
 /* Synchronizes `stream`, then reads the device status word the last route/forward on this
    workspace left: MOE_LORA_OK, MOE_LORA_ERR_TIMEOUT or MOE_LORA_ERR_DEVICE_CHECK.
    *detail (optional) receives the raw word (code in the low byte, where in the high bytes). */

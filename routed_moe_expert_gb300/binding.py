@@ -31,7 +31,7 @@ NUM_STAGES = len(STAGES)
 
 EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
-            "moe_lora_forward", "moe_lora_check_status"]
+            "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc"]
 
 
 class MoELoRAError(RuntimeError):
