@@ -77,9 +77,11 @@ cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, in
 // y already holds the down GEMM output plus the (unweighted) down-LoRA delta, added in
 // the down GEMM's epilogue, so this is the vLLM API page's _finalize_with_w2_lora
 // ("fused_moe/experts/trtllm_lora_moe": routing-weighted sum over top_k of the base rows
-// plus the routing-weighted down-LoRA delta).  One CTA per token, 4 floats per thread.
+// plus the routing-weighted down-LoRA delta).  A CTA covers 512 h of one token.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeParams p) {
+constexpr int kFinThreads = 128;   // 4 floats each: 512 h per CTA
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams p) {
   __shared__ int q_s[kMaxTopK];
   __shared__ float w_s[kMaxTopK];
   const int t = blockIdx.x, k = p.k, tid = threadIdx.x;
@@ -89,29 +91,30 @@ __global__ void __launch_bounds__(256) finalize_kernel(const FinalizeParams p) {
     w_s[tid] = p.weights[pp];
   }
   __syncthreads();
-  const int H4 = p.H >> 2;
-  for (int h4 = tid; h4 < H4; h4 += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const float4 y = __ldg(reinterpret_cast<const float4*>(p.y + static_cast<size_t>(q_s[j]) * p.H) + h4);
-      const float w = w_s[j];
-      acc.x += w * y.x;
-      acc.y += w * y.y;
-      acc.z += w * y.z;
-      acc.w += w * y.w;
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&lo);
-    v.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[h4] = v;
+  const int h4 = blockIdx.y * kFinThreads + tid;
+  if (h4 >= (p.H >> 2)) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int j = 0; j < k; ++j) {
+    const float4 y = __ldg(reinterpret_cast<const float4*>(p.y + static_cast<size_t>(q_s[j]) * p.H) + h4);
+    const float w = w_s[j];
+    acc.x += w * y.x;
+    acc.y += w * y.y;
+    acc.z += w * y.z;
+    acc.w += w * y.w;
   }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 v;
+  v.x = *reinterpret_cast<uint32_t*>(&lo);
+  v.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[h4] = v;
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  finalize_kernel<<<p.T, 256, 0, stream>>>(p);
+  const int H4 = p.H / 4;
+  finalize_kernel<<<dim3(p.T, (H4 + kFinThreads - 1) / kFinThreads), kFinThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -41,14 +41,14 @@ int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 int gemm_smem_bytes(int bn, int stages, int E, int lora_R) {
   // 1 KB alignment slack, stage buffers, barriers, tmem slot + abort flag, schedule,
   // and (LoRA epilogue) per-token slots and shrink values of one tile
-  const int lora = lora_R > 0 ? 16 + bn * 4 + bn * lora_R * 4 : 0;
+  const int lora = lora_R > 0 ? 32 + bn * 4 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + lora;
 }
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
 
 template <int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);   // [E + 1]
   int* seg = tile_start + (p.E + 1);                         // offsets copy [E + 1]
   int* lslot = seg + (p.E + 1) + 4;                          // [BN] (LoRA epilogue)
-  float* v_s = reinterpret_cast<float*>(lslot + BN);         // [BN][R]
+  float* v_s = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(lslot + BN) + 15) & ~static_cast<uintptr_t>(15));
+  // v_s: [BN][RP8] (16-byte aligned), RP8 = R rounded up to 8
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int etid = threadIdx.x - 64;     // 0..127 over the epilogue warps
     const bool lora = p.lora_v != nullptr;
     const int R = p.slots.R;
+    const int RP8 = (R + 7) & ~7;
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -233,22 +235,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       const int col = nt * 128 + row;
       const int q0 = seg[e] + qt * BN;
       const int nvalid = min(BN, seg[e + 1] - q0);
-      if (lora) {   // stage the tile's token slots and down-LoRA shrink values
+      if (lora) {   // stage the tile's pair slots and scaled down-LoRA shrink values
         epi_bar();
-        for (int j = etid; j < nvalid; j += 128) {
-          const int t = p.perm[q0 + j] / p.k;
-          int sl = p.slot_idx[t];
-          if (sl < -1 || sl >= p.slots.S) {
-            record_status(p.status, kDevBadSlot, kWhereGemmEpilogue);
-            sl = -1;
-          } else if (sl >= 0 && (p.slots.ranks[sl] <= 0 || p.slots.scal[sl] == 0.0f)) {
-            sl = -1;
-          }
-          lslot[j] = sl;
-        }
+        for (int j = etid; j < nvalid; j += 128) lslot[j] = p.pair_slot[q0 + j];
         epi_bar();
-        for (int i = etid; i < nvalid * R; i += 128) {
-          const int j = i / R, r = i - j * R;
+        for (int i = etid; i < nvalid * RP8; i += 128) {
+          const int j = i / RP8, r = i - j * RP8;
           const int sl = lslot[j];
           v_s[i] = (sl >= 0 && r < p.slots.ranks[sl]) ? p.lora_v[static_cast<size_t>(q0 + j) * R + r] : 0.0f;
         }
@@ -257,6 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
       for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
         uint32_t r[16];
         tmem_ld_x16(taddr + c, r);
@@ -267,6 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         if (lora && col < p.N) {
           // down-LoRA expand, one slot at a time (slots are uniform across the warp)
           uint32_t done = 0;
+#pragma unroll 1
           for (int j0 = 0; j0 < 16 && c + j0 < nvalid; ++j0) {
             if ((done >> j0) & 1u) continue;
             const int sl = lslot[c + j0];
@@ -276,14 +270,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             done |= m;
             if (sl < 0) continue;
             const int rank = p.slots.ranks[sl];
-            const float sc = p.slots.scal[sl];
             const __nv_bfloat16* Brow =
                 p.lora_B + ((static_cast<size_t>(sl) * p.E + e) * p.N + col) * static_cast<size_t>(R);
-            float dd[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) dd[j] = 0.0f;
+#pragma unroll 1
             for (int r0 = 0; r0 < rank; r0 += 8) {
-              float b[8];
+              float b[8];   // zero past the rank: the stacked tail is never read
               if ((R & 7) == 0 && r0 + 8 <= rank) {
                 unpack8(__ldg(reinterpret_cast<const uint4*>(Brow + r0)), b);
               } else {
@@ -293,17 +284,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 if ((m >> j) & 1u) {
-                  const float* vj = v_s + (c + j) * R + r0;
-                  float sacc = 0.0f;
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) sacc += (r0 + i < rank) ? b[i] * vj[i] : 0.0f;
-                  dd[j] += sacc;
+                  const float4* vj = reinterpret_cast<const float4*>(v_s + (c + j) * RP8 + r0);
+                  const float4 v0 = vj[0], v1 = vj[1];
+                  val[j] += b[0] * v0.x + b[1] * v0.y + b[2] * v0.z + b[3] * v0.w +
+                            b[4] * v1.x + b[5] * v1.y + b[6] * v1.z + b[7] * v1.w;
                 }
               }
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if ((m >> j) & 1u) val[j] += sc * dd[j];
           }
         }
         if (col < p.N) {

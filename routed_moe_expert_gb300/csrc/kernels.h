@@ -61,12 +61,11 @@ struct GemmParams {
   uint32_t* status;
   int E, N, K, gated, stages;
   // Optional LoRA expand added in the epilogue before the store (down GEMM):
-  // out[q, h] += scaling[s] * sum_{r<ranks[s]} lora_B[s, e, h, r] * lora_v[q, r]
+  // out[q, h] += sum_{r<ranks[s]} lora_B[s, e, h, r] * lora_v[q, r]   (s = pair_slot[q])
+  // lora_v holds scaling[s] * (down-LoRA shrink), written with pair_slot by the shrink.
   const float* lora_v;           // [P, R] or null
   const __nv_bfloat16* lora_B;   // [S, E, N, R]
-  const int32_t* perm;           // [P]
-  const int32_t* slot_idx;       // [T]
-  int k;
+  const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
 };
 int gemm_smem_bytes(int bn, int stages, int E, int lora_R);
@@ -103,7 +102,8 @@ struct LoraParams {
   const __nv_bfloat16* A;        // [S, E, R, K]
   const __nv_bfloat16* B;        // [S, E, N, R] or null
   LoraSlots slots;
-  float* u_out;                  // [P, R] (shrink only)
+  float* u_out;                  // [P, R] (shrink only): scaling[s] * u for r < ranks[s]
+  int32_t* pair_slot_out;        // [P] (shrink only): the pair's active slot or -1
   __nv_bfloat16* d_out;          // [P, N] (expand)
   uint32_t* status;
   uint32_t where;

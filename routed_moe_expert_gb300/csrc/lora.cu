@@ -29,7 +29,6 @@ namespace mlk {
 
 constexpr int kLoraThreads = 256;
 constexpr int kLoraWarps = 8;
-constexpr int kMaxMT = kMaxRank / 16;   // rank m-tiles of 16
 
 MLDEV void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(
@@ -59,9 +58,12 @@ size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E) {
   return b;
 }
 
-template <int NTL>
+// NTL: n-tiles of 8 pairs per CTA tile; MTX: rank m-tiles of 16 the kernel is built for
+// (ranks <= 16*MTX).  The shrink loads UK k-steps of fragments before issuing their MMAs.
+template <int NTL, int MTX>
 __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams p) {
   constexpr int PT = 8 * NTL;
+  constexpr int UK = MTX <= 2 ? 4 : (MTX <= 4 ? 2 : 1);
   extern __shared__ __align__(16) uint8_t smem[];
   const int R = p.slots.R;
   const int RP = ((R + 15) / 16) * 16;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       prow[tid] = row;
       pslot[tid] = s;
       pq[tid] = q;
+      if (p.pair_slot_out != nullptr && tid < np) p.pair_slot_out[q] = s;
     }
     if (expand) {
       uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -145,9 +148,9 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       const __nv_bfloat16* A = p.A + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(R) * p.K;
 
       // ---------------- shrink: warps split the K steps; partials to smem
-      float acc[kMaxMT][NTL][4];
+      float acc[MTX][NTL][4];
 #pragma unroll
-      for (int mt = 0; mt < kMaxMT; ++mt)
+      for (int mt = 0; mt < MTX; ++mt)
 #pragma unroll
         for (int nt = 0; nt < NTL; ++nt)
 #pragma unroll
@@ -160,32 +163,41 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
         xon[nt] = (n < np) && (pslot[n] == s);
         xrow[nt] = p.src + static_cast<size_t>(prow[n]) * p.K;
       }
-      for (int ks = warp; ks < K16; ks += kLoraWarps) {
-        const int k0 = ks * 16 + 2 * c;
-        uint32_t bf[NTL][2];
+      for (int ks0 = warp; ks0 < K16; ks0 += kLoraWarps * UK) {
+        uint32_t bf[UK][NTL][2];
+        uint32_t af[UK][MTX][4];
 #pragma unroll
-        for (int nt = 0; nt < NTL; ++nt) {
-          bf[nt][0] = xon[nt] ? ld_b32(xrow[nt] + k0) : 0u;
-          bf[nt][1] = xon[nt] ? ld_b32(xrow[nt] + k0 + 8) : 0u;
-        }
+        for (int u = 0; u < UK; ++u) {   // all loads of UK k-steps first
+          const int ks = ks0 + u * kLoraWarps;
+          const bool kon = ks < K16;
+          const int k0 = ks * 16 + 2 * c;
 #pragma unroll
-        for (int mt = 0; mt < kMaxMT; ++mt) {
-          if (mt < MT) {
+          for (int nt = 0; nt < NTL; ++nt) {
+            bf[u][nt][0] = (kon && xon[nt]) ? ld_b32(xrow[nt] + k0) : 0u;
+            bf[u][nt][1] = (kon && xon[nt]) ? ld_b32(xrow[nt] + k0 + 8) : 0u;
+          }
+#pragma unroll
+          for (int mt = 0; mt < MTX; ++mt) {
             const int r0 = mt * 16 + g, r1 = r0 + 8;
-            uint32_t af[4];
-            af[0] = r0 < rank ? ld_b32(A + static_cast<size_t>(r0) * p.K + k0) : 0u;
-            af[1] = r1 < rank ? ld_b32(A + static_cast<size_t>(r1) * p.K + k0) : 0u;
-            af[2] = r0 < rank ? ld_b32(A + static_cast<size_t>(r0) * p.K + k0 + 8) : 0u;
-            af[3] = r1 < rank ? ld_b32(A + static_cast<size_t>(r1) * p.K + k0 + 8) : 0u;
-#pragma unroll
-            for (int nt = 0; nt < NTL; ++nt) mma_bf16_16816(acc[mt][nt], af, bf[nt]);
+            const bool on0 = kon && r0 < rank, on1 = kon && r1 < rank;
+            af[u][mt][0] = on0 ? ld_b32(A + static_cast<size_t>(r0) * p.K + k0) : 0u;
+            af[u][mt][1] = on1 ? ld_b32(A + static_cast<size_t>(r1) * p.K + k0) : 0u;
+            af[u][mt][2] = on0 ? ld_b32(A + static_cast<size_t>(r0) * p.K + k0 + 8) : 0u;
+            af[u][mt][3] = on1 ? ld_b32(A + static_cast<size_t>(r1) * p.K + k0 + 8) : 0u;
           }
         }
+#pragma unroll
+        for (int u = 0; u < UK; ++u)
+#pragma unroll
+          for (int mt = 0; mt < MTX; ++mt)
+            if (mt < MT)
+#pragma unroll
+              for (int nt = 0; nt < NTL; ++nt) mma_bf16_16816(acc[mt][nt], af[u][mt], bf[u][nt]);
       }
       // partial [r][n] of this warp
       float* rw = red + warp * RP * PT;
 #pragma unroll
-      for (int mt = 0; mt < kMaxMT; ++mt) {
+      for (int mt = 0; mt < MTX; ++mt) {
         if (mt < MT) {
 #pragma unroll
           for (int nt = 0; nt < NTL; ++nt) {
@@ -206,7 +218,7 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
         for (int w = 0; w < kLoraWarps; ++w) v += red[w * RP * PT + i];
         const bool mine = (n < np) && (pslot[n] == s) && (r < rank);
         u_s[n * RP + r] = mine ? v : 0.0f;
-        if (!expand && mine) p.u_out[static_cast<size_t>(pq[n]) * R + r] = v;
+        if (!expand && mine) p.u_out[static_cast<size_t>(pq[n]) * R + r] = p.slots.scal[s] * v;
       }
       __syncthreads();
       if (!expand) continue;
@@ -220,48 +232,64 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       const float sc = p.slots.scal[s];
       const __nv_bfloat16* Bm = p.B + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(p.N) * R;
       const int NM = p.N >> 4;
-      for (int fm = warp; fm < NM; fm += kLoraWarps) {
-        const int f0 = fm * 16 + g, f1 = f0 + 8;
-        float acc2[NTL][4];
+      constexpr int UE = 4;   // feature m-tiles whose B-row loads are issued together
+      for (int fm0 = warp; fm0 < NM; fm0 += kLoraWarps * UE) {
+        float acc2[UE][NTL][4];
 #pragma unroll
-        for (int nt = 0; nt < NTL; ++nt)
+        for (int ue = 0; ue < UE; ++ue)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc2[nt][i] = 0.0f;
+          for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc2[ue][nt][i] = 0.0f;
         for (int kt = 0; kt < MT; ++kt) {
           const int r0 = kt * 16 + 2 * c, r1 = r0 + 8;
-          uint32_t af[4];
-          // B rows have stride R (any rank); load element pairs only below the rank
-          const __nv_bfloat16* b0 = Bm + static_cast<size_t>(f0) * R;
-          const __nv_bfloat16* b1 = Bm + static_cast<size_t>(f1) * R;
+          // B rows have stride R (any rank); pairs past the rank load as zero
           auto pair = [&](const __nv_bfloat16* row, int r) -> uint32_t {
             if (r + 1 < rank && (R & 1) == 0) return ld_b32(row + r);   // 4-byte aligned pair
             const float lo = r < rank ? __bfloat162float(row[r]) : 0.0f;
             const float hi = r + 1 < rank ? __bfloat162float(row[r + 1]) : 0.0f;
             return pack_bf16x2(lo, hi);
           };
-          af[0] = pair(b0, r0);
-          af[1] = pair(b1, r0);
-          af[2] = pair(b0, r1);
-          af[3] = pair(b1, r1);
+          uint32_t af[UE][4];
+#pragma unroll
+          for (int ue = 0; ue < UE; ++ue) {
+            const int fm = fm0 + ue * kLoraWarps;
+            const int f0 = (fm < NM ? fm : 0) * 16 + g;
+            const __nv_bfloat16* b0 = Bm + static_cast<size_t>(f0) * R;
+            const __nv_bfloat16* b1 = Bm + static_cast<size_t>(f0 + 8) * R;
+            af[ue][0] = pair(b0, r0);
+            af[ue][1] = pair(b1, r0);
+            af[ue][2] = pair(b0, r1);
+            af[ue][3] = pair(b1, r1);
+          }
+          uint32_t bfr[NTL][2];
 #pragma unroll
           for (int nt = 0; nt < NTL; ++nt) {
             const __nv_bfloat16* urow = ub + (nt * 8 + g) * (RP + 8);
-            uint32_t bfr[2];
-            bfr[0] = *reinterpret_cast<const uint32_t*>(urow + kt * 16 + 2 * c);
-            bfr[1] = *reinterpret_cast<const uint32_t*>(urow + kt * 16 + 2 * c + 8);
-            mma_bf16_16816(acc2[nt], af, bfr);
+            bfr[nt][0] = *reinterpret_cast<const uint32_t*>(urow + kt * 16 + 2 * c);
+            bfr[nt][1] = *reinterpret_cast<const uint32_t*>(urow + kt * 16 + 2 * c + 8);
           }
+#pragma unroll
+          for (int ue = 0; ue < UE; ++ue)
+#pragma unroll
+            for (int nt = 0; nt < NTL; ++nt) mma_bf16_16816(acc2[ue][nt], af[ue], bfr[nt]);
         }
 #pragma unroll
-        for (int nt = 0; nt < NTL; ++nt) {
-          const int n0 = nt * 8 + 2 * c, n1 = n0 + 1;
-          if (n0 < np && pslot[n0] == s) {
-            dst[n0 * p.N + f0] = __float2bfloat16_rn(sc * acc2[nt][0]);
-            dst[n0 * p.N + f1] = __float2bfloat16_rn(sc * acc2[nt][2]);
-          }
-          if (n1 < np && pslot[n1] == s) {
-            dst[n1 * p.N + f0] = __float2bfloat16_rn(sc * acc2[nt][1]);
-            dst[n1 * p.N + f1] = __float2bfloat16_rn(sc * acc2[nt][3]);
+        for (int ue = 0; ue < UE; ++ue) {
+          const int fm = fm0 + ue * kLoraWarps;
+          if (fm >= NM) continue;
+          const int f0 = fm * 16 + g, f1 = f0 + 8;
+#pragma unroll
+          for (int nt = 0; nt < NTL; ++nt) {
+            const int n0 = nt * 8 + 2 * c, n1 = n0 + 1;
+            if (n0 < np && pslot[n0] == s) {
+              dst[n0 * p.N + f0] = __float2bfloat16_rn(sc * acc2[ue][nt][0]);
+              dst[n0 * p.N + f1] = __float2bfloat16_rn(sc * acc2[ue][nt][2]);
+            }
+            if (n1 < np && pslot[n1] == s) {
+              dst[n1 * p.N + f0] = __float2bfloat16_rn(sc * acc2[ue][nt][1]);
+              dst[n1 * p.N + f1] = __float2bfloat16_rn(sc * acc2[ue][nt][3]);
+            }
           }
         }
       }
@@ -280,20 +308,28 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
   }
 }
 
+template <int NTL, int MTX>
+static cudaError_t launch_t(const LoraParams& p, int grid, size_t smem, cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(lora_mma_kernel<NTL, MTX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  lora_mma_kernel<NTL, MTX><<<grid, kLoraThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int NTL>
+static cudaError_t launch_ntl(const LoraParams& p, int grid, size_t smem, cudaStream_t stream) {
+  const int R = p.slots.R;
+  if (R <= 16) return launch_t<NTL, 1>(p, grid, smem, stream);
+  if (R <= 32) return launch_t<NTL, 2>(p, grid, smem, stream);
+  if (R <= 64) return launch_t<NTL, 4>(p, grid, smem, stream);
+  return launch_t<NTL, 8>(p, grid, smem, stream);
+}
+
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream) {
   if (p.P == 0) return cudaSuccess;
   const size_t smem = lora_smem_bytes(ntl, p.slots.R, p.N, p.B != nullptr, p.E);
-  cudaError_t err;
-  if (ntl == 1) {
-    err = cudaFuncSetAttribute(lora_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    lora_mma_kernel<1><<<grid, kLoraThreads, smem, stream>>>(p);
-  } else {
-    err = cudaFuncSetAttribute(lora_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    lora_mma_kernel<4><<<grid, kLoraThreads, smem, stream>>>(p);
-  }
-  return cudaGetLastError();
+  return ntl == 1 ? launch_ntl<1>(p, grid, smem, stream) : launch_ntl<4>(p, grid, smem, stream);
 }
 
 }  // namespace mlk

@@ -43,7 +43,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace layout (all offsets 256-byte aligned).
 struct Layout {
   size_t header, ids, wts, offsets, perm, inv, hist, base, total;
-  size_t xp, g, d, a, v, y;
+  size_t xp, g, d, a, v, y, pslot;
   size_t bytes;
 };
 
@@ -71,6 +71,7 @@ Layout layout_for(int T, int H, int I, int E, int k, int R) {
   L.a = take(P * I * 2);
   L.v = take(P * R * 4);
   L.y = take(P * H * 4);
+  L.pslot = take(R > 0 ? P * 4 : 0);
   L.bytes = off;
   return L;
 }
@@ -225,7 +226,7 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
                               int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
                               int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream) {
   if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
-  int grid = (T + 15) / 16;
+  int grid = (T + 63) / 64;   // 16 warps x 4 tokens per CTA pass
   if (grid > h->coop_ctas[E]) grid = h->coop_ctas[E];
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
   if (grid < 1) grid = 1;
@@ -375,6 +376,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
   float* v = reinterpret_cast<float*>(ws + L.v);
   float* y = reinterpret_cast<float*>(ws + L.y);
+  int32_t* pair_slot = reinterpret_cast<int32_t*>(ws + L.pslot);
 
   prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
   st = enqueue_route(h, a->router_logits, a->correction_bias, T, E, k, a->routing_method, a->routed_scaling_factor,
@@ -465,6 +467,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     lp.B = nullptr;
     lp.slots = slots;
     lp.u_out = v;
+    lp.pair_slot_out = pair_slot;
     lp.status = status;
     lp.where = kWhereLoraShrinkDn;
     ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, stream), "lora down shrink launch");
@@ -484,9 +487,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   if (lora) {
     dn.lora_v = v;
     dn.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
-    dn.perm = perm;
-    dn.slot_idx = a->slot_idx;
-    dn.k = k;
+    dn.pair_slot = pair_slot;
     dn.slots = slots;
   }
   st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream);

@@ -1,8 +1,8 @@
 // Fused routing + expert alignment, one launch.
 //
-// Phase 1: one warp per token selects the top-k experts (warp arg-max rounds, ties to
-//          the lower expert id) and the routing weights; each CTA counts its pairs per
-//          expert in shared memory.
+// Phase 1: each warp selects the top-k experts of 4 tokens at a time (warp arg-max
+//          rounds, ties to the lower expert id, the 4 tokens interleaved) and the routing
+//          weights; each CTA counts its pairs per expert in shared memory.
 // Phase 2: (grid barrier) per expert, an exclusive prefix of the per-CTA counts over
 //          the CTAs in order; (grid barrier) every CTA scans the expert totals into
 //          expert_offsets, then scatters its own pairs, in ascending expanded index,
@@ -119,6 +119,7 @@ MLDEV int block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
 
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteParams p) {
+  constexpr int kTPW = EPL <= 8 ? 4 : (EPL <= 16 ? 2 : 1);   // tokens per warp, in lockstep
   __shared__ int hist_s[kMaxExperts];
   __shared__ int cursor_s[kMaxExperts];
   __shared__ int warp_sums[kRouteWarps + 1];
@@ -134,70 +135,95 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   const int t0 = c * p.tokens_per_cta;
   const int t1 = min(p.T, t0 + p.tokens_per_cta);
 
-  // ---------------- phase 1: top-k per token, one warp per token
-  for (int t = t0 + warp; t < t1; t += kRouteWarps) {
-    const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
-    float key[EPL];
-    uint32_t avail = 0;
+  // ---------------- phase 1: top-k per token; each warp runs kTPW tokens in lockstep so
+  // the dependent shuffle chains of independent tokens overlap
+  for (int tb = t0 + warp * kTPW; tb < t1; tb += kRouteWarps * kTPW) {
+    float key[kTPW][EPL];
+    uint32_t avail[kTPW];
+    int my_id[kTPW];
+    float my_key[kTPW];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      float kv = -INFINITY;
-      if (e < E) {
-        const float l = load_logit(row, e);
-        kv = (p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l;
-        avail |= 1u << i;
+    for (int u = 0; u < kTPW; ++u) {
+      const int t = tb + u;
+      avail[u] = 0;
+      my_id[u] = kInvalidId;
+      my_key[u] = -INFINITY;
+      const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        float kv = -INFINITY;
+        if (t < t1 && e < E) {
+          const float l = load_logit(row, e);
+          kv = (p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l;
+          avail[u] |= 1u << i;
+        }
+        key[u][i] = kv;
       }
-      key[i] = kv;
     }
-    int my_id = kInvalidId;
-    float my_key = -INFINITY;
     for (int j = 0; j < k; ++j) {
-      float bk = -INFINITY;
-      int bid = kInvalidId;
+      float bk[kTPW];
+      int bid[kTPW];
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {   // ids ascend with i: strict > keeps the lower id
-        if ((avail >> i) & 1u) {
-          if (bid == kInvalidId || key[i] > bk) {
-            bk = key[i];
-            bid = lane + 32 * i;
+      for (int u = 0; u < kTPW; ++u) {
+        bk[u] = -INFINITY;
+        bid[u] = kInvalidId;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {   // ids ascend with i: strict > keeps the lower id
+          if ((avail[u] >> i) & 1u) {
+            if (bid[u] == kInvalidId || key[u][i] > bk[u]) {
+              bk[u] = key[u][i];
+              bid[u] = lane + 32 * i;
+            }
           }
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-        const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
-        if (oid != kInvalidId && (bid == kInvalidId || ok > bk || (ok == bk && oid < bid))) {
-          bk = ok;
-          bid = oid;
+#pragma unroll
+        for (int u = 0; u < kTPW; ++u) {
+          const float ok = __shfl_xor_sync(0xffffffffu, bk[u], off);
+          const int oid = __shfl_xor_sync(0xffffffffu, bid[u], off);
+          if (oid != kInvalidId && (bid[u] == kInvalidId || ok > bk[u] || (ok == bk[u] && oid < bid[u]))) {
+            bk[u] = ok;
+            bid[u] = oid;
+          }
         }
       }
-      if ((bid & 31) == lane) avail &= ~(1u << (bid >> 5));
-      if (lane == j) {
-        my_id = bid;
-        my_key = bk;
+#pragma unroll
+      for (int u = 0; u < kTPW; ++u) {
+        if (bid[u] != kInvalidId && (bid[u] & 31) == lane) avail[u] &= ~(1u << (bid[u] >> 5));
+        if (lane == j) {
+          my_id[u] = bid[u];
+          my_key[u] = bk[u];
+        }
       }
     }
-    float wv;
-    if (p.method == 1) {
-      const float s = (lane < k) ? sigmoid_key_f32(load_logit(row, my_id)) : 0.0f;
-      float sum = s;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      wv = s / sum * p.rsf;
-    } else {
-      const float kmax = __shfl_sync(0xffffffffu, my_key, 0);
-      const float ex = (lane < k) ? expf(my_key - kmax) : 0.0f;
-      float sum = ex;
+    for (int u = 0; u < kTPW; ++u) {
+      const int t = tb + u;
+      if (t >= t1) break;   // uniform across the warp
+      const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
+      float wv;
+      if (p.method == 1) {
+        const float s = (lane < k) ? sigmoid_key_f32(load_logit(row, my_id[u])) : 0.0f;
+        float sum = s;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      wv = ex / sum;
-    }
-    if (lane < k) {
-      p.ids[static_cast<size_t>(t) * k + lane] = my_id;
-      p.weights[static_cast<size_t>(t) * k + lane] = wv;
-      atomicAdd(&hist_s[my_id], 1);
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        wv = s / sum * p.rsf;
+      } else {
+        const float kmax = __shfl_sync(0xffffffffu, my_key[u], 0);
+        const float ex = (lane < k) ? expf(my_key[u] - kmax) : 0.0f;
+        float sum = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        wv = ex / sum;
+      }
+      if (lane < k) {
+        p.ids[static_cast<size_t>(t) * k + lane] = my_id[u];
+        p.weights[static_cast<size_t>(t) * k + lane] = wv;
+        atomicAdd(&hist_s[my_id[u]], 1);
+      }
     }
   }
   __syncthreads();
