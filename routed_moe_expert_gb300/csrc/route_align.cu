@@ -26,6 +26,7 @@ namespace mlk {
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kInvalidId = 0x7fffffff;
+constexpr int kRouteIdsInSmem = 6144;   // pairs per CTA kept in shared memory for the scatter
 
 // sigma(z) = 1 / (1 + exp(-z)) in float32, one IEEE rounding per operation, with exp
 // evaluated by Cody-Waite reduction (W. J. Cody and W. Waite, "Software Manual for the
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   __shared__ int cursor_s[kMaxExperts];
   __shared__ int warp_sums[kRouteWarps + 1];
   __shared__ int ok_s;
+  __shared__ int ids_s[kRouteIdsInSmem];   // this CTA's expert ids, when they fit
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, c = blockIdx.x;
@@ -220,6 +222,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
         wv = ex / sum;
       }
       if (lane < k) {
+        const int pl = (t - t0) * k + lane;   // pair index local to this CTA
+        if (pl < kRouteIdsInSmem) ids_s[pl] = my_id[u];
         p.ids[static_cast<size_t>(t) * k + lane] = my_id[u];
         p.weights[static_cast<size_t>(t) * k + lane] = wv;
         atomicAdd(&hist_s[my_id[u]], 1);
@@ -276,7 +280,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
     for (int pb = p0; pb < p1; pb += 32) {
       const int pp = pb + lane;
       const bool valid = pp < p1;
-      const int e = valid ? p.ids[pp] : -1;
+      const int pl = pp - p0;
+      const int e = valid ? (pl < kRouteIdsInSmem ? ids_s[pl] : p.ids[pp]) : -1;
       const unsigned grp = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(grp & ((1u << lane) - 1u));
       const int q = valid ? cursor_s[e] + rank : 0;
