@@ -55,6 +55,18 @@ MLDEV float sigmoid_key_f32(float z) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 
+// Unsigned integer whose order is the float order of finite and infinite keys; 0 is left
+// free as "no candidate".  -0 is folded to +0 first so that +-0 compare equal.
+MLDEV uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // never 0 for a non-NaN key
+}
+
+MLDEV float from_order_key(uint32_t v) {
+  return __uint_as_float((v & 0x80000000u) ? (v & 0x7fffffffu) : ~v);
+}
+
 MLDEV float load_logit(const __nv_bfloat16* row, int e) {
   float l = bf2f(row[e]);
   return (l != l) ? -INFINITY : l;   // NaN logits never win
@@ -120,7 +132,7 @@ MLDEV int block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
 
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteParams p) {
-  constexpr int kTPW = EPL <= 8 ? 4 : (EPL <= 16 ? 2 : 1);   // tokens per warp, in lockstep
+  constexpr int kTPW = EPL <= 4 ? 4 : (EPL <= 8 ? 2 : 1);   // tokens per warp, in lockstep
   __shared__ int hist_s[kMaxExperts];
   __shared__ int cursor_s[kMaxExperts];
   __shared__ int warp_sums[kRouteWarps + 1];
@@ -137,67 +149,66 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   const int t0 = c * p.tokens_per_cta;
   const int t1 = min(p.T, t0 + p.tokens_per_cta);
 
-  // ---------------- phase 1: top-k per token; each warp runs kTPW tokens in lockstep so
-  // the dependent shuffle chains of independent tokens overlap
+  // ---------------- phase 1: top-k per token; each warp runs kTPW tokens in lockstep.
+  // Keys are mapped to unsigned integers whose order is the float order (-0 folded to +0,
+  // so +-0 ties like equal floats); each round takes the warp maximum with one hardware
+  // reduction and breaks ties with a second (the lowest expert id holding the maximum).
   for (int tb = t0 + warp * kTPW; tb < t1; tb += kRouteWarps * kTPW) {
-    float key[kTPW][EPL];
-    uint32_t avail[kTPW];
+    uint32_t okey[kTPW][EPL];       // 0 = not a candidate (e >= E)
+    uint32_t taken[kTPW];           // bit i: entry i of this lane already selected
     int my_id[kTPW];
     float my_key[kTPW];
 #pragma unroll
     for (int u = 0; u < kTPW; ++u) {
       const int t = tb + u;
-      avail[u] = 0;
       my_id[u] = kInvalidId;
       my_key[u] = -INFINITY;
+      taken[u] = 0u;
       const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         float kv = -INFINITY;
+        uint32_t ok = 0u;
         if (t < t1 && e < E) {
           const float l = load_logit(row, e);
           kv = (p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l;
-          avail[u] |= 1u << i;
+          ok = order_key(kv);
         }
-        key[u][i] = kv;
+        okey[u][i] = ok;
       }
     }
     for (int j = 0; j < k; ++j) {
-      float bk[kTPW];
+      uint32_t best[kTPW];
       int bid[kTPW];
 #pragma unroll
       for (int u = 0; u < kTPW; ++u) {
-        bk[u] = -INFINITY;
+        best[u] = 0u;
         bid[u] = kInvalidId;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {   // ids ascend with i: strict > keeps the lower id
-          if ((avail[u] >> i) & 1u) {
-            if (bid[u] == kInvalidId || key[u][i] > bk[u]) {
-              bk[u] = key[u][i];
-              bid[u] = lane + 32 * i;
-            }
+          const uint32_t ok = ((taken[u] >> i) & 1u) ? 0u : okey[u][i];
+          if (ok > best[u]) {
+            best[u] = ok;
+            bid[u] = lane + 32 * i;
           }
         }
       }
+      uint32_t wmax[kTPW];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
+      for (int u = 0; u < kTPW; ++u) wmax[u] = __reduce_max_sync(0xffffffffu, best[u]);
+      uint32_t win[kTPW];
 #pragma unroll
-        for (int u = 0; u < kTPW; ++u) {
-          const float ok = __shfl_xor_sync(0xffffffffu, bk[u], off);
-          const int oid = __shfl_xor_sync(0xffffffffu, bid[u], off);
-          if (oid != kInvalidId && (bid[u] == kInvalidId || ok > bk[u] || (ok == bk[u] && oid < bid[u]))) {
-            bk[u] = ok;
-            bid[u] = oid;
-          }
-        }
-      }
+      for (int u = 0; u < kTPW; ++u)
+        win[u] = __reduce_min_sync(0xffffffffu, (best[u] == wmax[u] && best[u] != 0u) ? static_cast<uint32_t>(bid[u])
+                                                                                      : 0xffffffffu);
 #pragma unroll
       for (int u = 0; u < kTPW; ++u) {
-        if (bid[u] != kInvalidId && (bid[u] & 31) == lane) avail[u] &= ~(1u << (bid[u] >> 5));
+        const int w = static_cast<int>(win[u]);
+        if (win[u] != 0xffffffffu && (w & 31) == lane) taken[u] |= 1u << (w >> 5);
         if (lane == j) {
-          my_id[u] = bid[u];
-          my_key[u] = bk[u];
+          my_id[u] = w;
+          my_key[u] = from_order_key(wmax[u]);
         }
       }
     }

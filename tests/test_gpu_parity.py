@@ -51,6 +51,9 @@ def test_route_bit_exact(handle, T, E, k, method, scale):
     logits[0, :] = 0.0                                   # a row of ties
     if T > 2:
         logits[1, E // 2] = float("nan")                 # a NaN logit never wins
+    if T > 3:
+        logits[2, :] = -0.0                              # -0 and +0 tie: lower ids win
+        logits[2, 1::3] = 0.0
     bias = (torch.randn(E, generator=g) * 0.1).float() if method == 1 else None
     rsf = 2.827 if method == 1 else 1.0
     out = pkg.moe_lora_route(handle, logits.cuda(), k, method, None if bias is None else bias.cuda(), rsf)
