@@ -226,7 +226,8 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
                               int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
                               int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream) {
   if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
-  int grid = (T + 63) / 64;   // 16 warps x 4 tokens per CTA pass
+  // one CTA (no grid barrier) up to 512 tokens; beyond, about 64 tokens per CTA
+  int grid = T <= 512 ? 1 : (T + 63) / 64;
   if (grid > h->coop_ctas[E]) grid = h->coop_ctas[E];
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
   if (grid < 1) grid = 1;

@@ -26,7 +26,8 @@ namespace mlk {
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kInvalidId = 0x7fffffff;
-constexpr int kRouteIdsInSmem = 6144;   // pairs per CTA kept in shared memory for the scatter
+constexpr int kRouteIdsInSmem = 3072;   // pairs per CTA kept in shared memory for the scatter
+constexpr int kScatterMaxE = 384;       // per-warp expert cursors fit in shared memory up to here
 
 // sigma(z) = 1 / (1 + exp(-z)) in float32, one IEEE rounding per operation, with exp
 // evaluated by Cody-Waite reduction (W. J. Cody and W. Waite, "Software Manual for the
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   __shared__ int warp_sums[kRouteWarps + 1];
   __shared__ int ok_s;
   __shared__ int ids_s[kRouteIdsInSmem];   // this CTA's expert ids, when they fit
+  __shared__ int wcnt[kRouteWarps * kScatterMaxE];   // per-warp expert cursors
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, c = blockIdx.x;
@@ -151,11 +153,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
 
   // ---------------- phase 1: top-k per token; each warp runs kTPW tokens in lockstep.
   // Keys are mapped to unsigned integers whose order is the float order (-0 folded to +0,
-  // so +-0 ties like equal floats); each round takes the warp maximum with one hardware
-  // reduction and breaks ties with a second (the lowest expert id holding the maximum).
+  // so +-0 tie like equal floats).  Each lane first sorts its EPL (key, id) entries
+  // (descending key, ascending id); a selection round is then: the warp maximum of the
+  // lanes' heads (one hardware reduction), the lowest id holding it (a second one), and
+  // the winning lane shifts its list.
   for (int tb = t0 + warp * kTPW; tb < t1; tb += kRouteWarps * kTPW) {
-    uint32_t okey[kTPW][EPL];       // 0 = not a candidate (e >= E)
-    uint32_t taken[kTPW];           // bit i: entry i of this lane already selected
+    uint32_t sk[kTPW][EPL];   // this lane's keys, sorted; 0 = empty
+    int si[kTPW][EPL];        // their expert ids
     int my_id[kTPW];
     float my_key[kTPW];
 #pragma unroll
@@ -163,49 +167,55 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
       const int t = tb + u;
       my_id[u] = kInvalidId;
       my_key[u] = -INFINITY;
-      taken[u] = 0u;
       const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        float kv = -INFINITY;
         uint32_t ok = 0u;
         if (t < t1 && e < E) {
           const float l = load_logit(row, e);
-          kv = (p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l;
-          ok = order_key(kv);
+          ok = order_key((p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l);
         }
-        okey[u][i] = ok;
+        sk[u][i] = ok;
+        si[u][i] = e;
       }
-    }
-    for (int j = 0; j < k; ++j) {
-      uint32_t best[kTPW];
-      int bid[kTPW];
+      // odd-even transposition sort, EPL passes: descending key; equal keys keep the
+      // lower id first (ids start ascending and a swap needs a strictly larger key)
 #pragma unroll
-      for (int u = 0; u < kTPW; ++u) {
-        best[u] = 0u;
-        bid[u] = kInvalidId;
+      for (int pass = 0; pass < EPL; ++pass) {
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {   // ids ascend with i: strict > keeps the lower id
-          const uint32_t ok = ((taken[u] >> i) & 1u) ? 0u : okey[u][i];
-          if (ok > best[u]) {
-            best[u] = ok;
-            bid[u] = lane + 32 * i;
+        for (int i = pass & 1; i + 1 < EPL; i += 2) {
+          if (sk[u][i + 1] > sk[u][i]) {
+            const uint32_t tk = sk[u][i];
+            sk[u][i] = sk[u][i + 1];
+            sk[u][i + 1] = tk;
+            const int ti = si[u][i];
+            si[u][i] = si[u][i + 1];
+            si[u][i + 1] = ti;
           }
         }
       }
+    }
+    for (int j = 0; j < k; ++j) {
       uint32_t wmax[kTPW];
 #pragma unroll
-      for (int u = 0; u < kTPW; ++u) wmax[u] = __reduce_max_sync(0xffffffffu, best[u]);
+      for (int u = 0; u < kTPW; ++u) wmax[u] = __reduce_max_sync(0xffffffffu, sk[u][0]);
       uint32_t win[kTPW];
 #pragma unroll
       for (int u = 0; u < kTPW; ++u)
-        win[u] = __reduce_min_sync(0xffffffffu, (best[u] == wmax[u] && best[u] != 0u) ? static_cast<uint32_t>(bid[u])
-                                                                                      : 0xffffffffu);
+        win[u] = __reduce_min_sync(0xffffffffu, (sk[u][0] == wmax[u] && sk[u][0] != 0u)
+                                                    ? static_cast<uint32_t>(si[u][0]) : 0xffffffffu);
 #pragma unroll
       for (int u = 0; u < kTPW; ++u) {
         const int w = static_cast<int>(win[u]);
-        if (win[u] != 0xffffffffu && (w & 31) == lane) taken[u] |= 1u << (w >> 5);
+        if (win[u] != 0xffffffffu && (w & 31) == lane) {   // pop this lane's head
+#pragma unroll
+          for (int i = 0; i + 1 < EPL; ++i) {
+            sk[u][i] = sk[u][i + 1];
+            si[u][i] = si[u][i + 1];
+          }
+          sk[u][EPL - 1] = 0u;
+        }
         if (lane == j) {
           my_id[u] = w;
           my_key[u] = from_order_key(wmax[u]);
@@ -285,23 +295,52 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   }
   __syncthreads();
 
-  // ---------------- scatter this CTA's pairs in ascending expanded index
-  if (warp == 0 && t0 < t1) {
-    const int p0 = t0 * k, p1 = t1 * k;
-    for (int pb = p0; pb < p1; pb += 32) {
-      const int pp = pb + lane;
-      const bool valid = pp < p1;
-      const int pl = pp - p0;
-      const int e = valid ? (pl < kRouteIdsInSmem ? ids_s[pl] : p.ids[pp]) : -1;
-      const unsigned grp = __match_any_sync(0xffffffffu, e);
+  // ---------------- scatter this CTA's pairs in ascending expanded index.  The pairs are
+  // split into one contiguous chunk per warp; per-warp expert counts and their prefix over
+  // warps (in warp order) give each warp its own cursors, and inside a warp 32 pairs at a
+  // time get their rank among equal experts from ballots over the expert-id bits.
+  const int p0 = t0 * k, p1 = max(t0, t1) * k;
+  const int npairs = p1 - p0;
+  const bool parallel = npairs <= kRouteIdsInSmem && E <= kScatterMaxE;
+  const int chunk = parallel ? (npairs + kRouteWarps - 1) / kRouteWarps : npairs;
+  if (parallel) {
+    for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
+    __syncthreads();
+    for (int pl = tid; pl < npairs; pl += kRouteThreads) atomicAdd(&wcnt[(pl / chunk) * E + ids_s[pl]], 1);
+    __syncthreads();
+    for (int e = tid; e < E; e += kRouteThreads) {   // prefix over warps, in warp order
+      int run = cursor_s[e];
+      for (int w = 0; w < kRouteWarps; ++w) {
+        const int c0 = wcnt[w * E + e];
+        wcnt[w * E + e] = run;
+        run += c0;
+      }
+    }
+    __syncthreads();
+  }
+  if (parallel || warp == 0) {
+    int* cur = parallel ? wcnt + warp * E : cursor_s;
+    const int lo = parallel ? min(npairs, warp * chunk) : 0;
+    const int hi = parallel ? min(npairs, lo + chunk) : npairs;
+    int nbits = 0;
+    while ((1 << nbits) < E) ++nbits;
+    for (int pb = lo; pb < hi; pb += 32) {
+      const int pl = pb + lane;
+      const bool valid = pl < hi;
+      const int e = valid ? (pl < kRouteIdsInSmem ? ids_s[pl] : p.ids[p0 + pl]) : -1;
+      unsigned grp = __ballot_sync(0xffffffffu, valid);   // lanes with the same expert id
+      for (int b = 0; b < nbits; ++b) {
+        const unsigned ones = __ballot_sync(0xffffffffu, valid && ((e >> b) & 1));
+        grp &= ((e >> b) & 1) ? ones : ~ones;
+      }
       const int rank = __popc(grp & ((1u << lane) - 1u));
-      const int q = valid ? cursor_s[e] + rank : 0;
+      const int q = valid ? cur[e] + rank : 0;
       __syncwarp();
-      if (valid && rank == 0) cursor_s[e] += __popc(grp);
+      if (valid && rank == 0) cur[e] += __popc(grp);
       __syncwarp();
       if (valid) {
-        p.perm[q] = pp;
-        p.inv[pp] = q;
+        p.perm[q] = p0 + pl;
+        p.inv[p0 + pl] = q;
       }
     }
   }
