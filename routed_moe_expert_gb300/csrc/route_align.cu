@@ -131,7 +131,7 @@ MLDEV int block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
   return total;
 }
 
-template <int EPL>
+template <int EPL, int METHOD>
 __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteParams p) {
   constexpr int kTPW = EPL <= 4 ? 4 : (EPL <= 8 ? 2 : 1);   // tokens per warp, in lockstep
   __shared__ int hist_s[kMaxExperts];
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
         uint32_t ok = 0u;
         if (t < t1 && e < E) {
           const float l = load_logit(row, e);
-          ok = order_key((p.method == 1) ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l);
+          ok = order_key(METHOD == 1 ? __fadd_rn(sigmoid_key_f32(l), p.bias[e]) : l);
         }
         sk[u][i] = ok;
         si[u][i] = e;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
       if (t >= t1) break;   // uniform across the warp
       const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
       float wv;
-      if (p.method == 1) {
+      if (METHOD == 1) {
         const float s = (lane < k) ? sigmoid_key_f32(load_logit(row, my_id[u])) : 0.0f;
         float sum = s;
 #pragma unroll
@@ -346,7 +346,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   }
 }
 
-template <int EPL>
+static int epl_for(int E) { return E <= 128 ? 4 : E <= 256 ? 8 : E <= 384 ? 12 : E <= 512 ? 16 : 32; }
+
+template <int EPL, int METHOD>
 static cudaError_t launch_epl(const RouteParams& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -358,22 +360,32 @@ static cudaError_t launch_epl(const RouteParams& p, int grid, cudaStream_t strea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = grid > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, route_align_kernel<EPL>, p);
+  return cudaLaunchKernelEx(&cfg, route_align_kernel<EPL, METHOD>, p);
 }
 
-static int epl_for(int E) { return E <= 128 ? 4 : E <= 256 ? 8 : E <= 384 ? 12 : E <= 512 ? 16 : 32; }
+template <int METHOD>
+static cudaError_t launch_method(const RouteParams& p, int grid, cudaStream_t stream) {
+  switch (epl_for(p.E)) {
+    case 4: return launch_epl<4, METHOD>(p, grid, stream);
+    case 8: return launch_epl<8, METHOD>(p, grid, stream);
+    case 12: return launch_epl<12, METHOD>(p, grid, stream);
+    case 16: return launch_epl<16, METHOD>(p, grid, stream);
+    default: return launch_epl<32, METHOD>(p, grid, stream);
+  }
+}
 
 int route_max_coop_ctas(int E) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
   cudaError_t err;
+  // every instantiation has the same block size and static shared memory; use the widest
   switch (epl_for(E)) {
-    case 4: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<4>, kRouteThreads, 0); break;
-    case 8: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<8>, kRouteThreads, 0); break;
-    case 12: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<12>, kRouteThreads, 0); break;
-    case 16: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<16>, kRouteThreads, 0); break;
-    default: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<32>, kRouteThreads, 0); break;
+    case 4: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<4, 1>, kRouteThreads, 0); break;
+    case 8: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<8, 1>, kRouteThreads, 0); break;
+    case 12: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<12, 1>, kRouteThreads, 0); break;
+    case 16: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<16, 1>, kRouteThreads, 0); break;
+    default: err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_align_kernel<32, 1>, kRouteThreads, 0); break;
   }
   if (err != cudaSuccess || per_sm < 1) return 1;
   const int n = sms * per_sm;
@@ -381,13 +393,7 @@ int route_max_coop_ctas(int E) {
 }
 
 cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stream) {
-  switch (epl_for(p.E)) {
-    case 4: return launch_epl<4>(p, grid, stream);
-    case 8: return launch_epl<8>(p, grid, stream);
-    case 12: return launch_epl<12>(p, grid, stream);
-    case 16: return launch_epl<16>(p, grid, stream);
-    default: return launch_epl<32>(p, grid, stream);
-  }
+  return p.method == 1 ? launch_method<1>(p, grid, stream) : launch_method<0>(p, grid, stream);
 }
 
 }  // namespace mlk
