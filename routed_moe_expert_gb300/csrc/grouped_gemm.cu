@@ -138,87 +138,116 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     qt = local - nt * nq;
   };
 
-  if (warp == 0) {
-    if (lane == 0) {   // ---------------------------------------------- TMA producer
-      const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_x = l2_policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0;       // stages with a load in flight, and their parity
-      uint32_t issued_parity = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        int e, nt, qt;
-        decode(tile, e, nt, qt);
-        int wr0, wr1;
-        if (p.gated) {
-          wr0 = e * p.N + nt * 64;
-          wr1 = wr0 + (p.N >> 1);
-        } else {
-          wr0 = e * p.N + nt * 128;
-          wr1 = wr0 + 64;
-        }
-        const int xr = seg[e] + qt * BN;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) {
-            ok = false;
-            break;
-          }
-          uint8_t* a = smem + stage * STAGE;
-          mbar_arrive_expect_tx(&full[stage], STAGE);
-          tma_load_2d(a, &p.tmap_w, &full[stage], kb * 64, wr0, pol_w);
-          tma_load_2d(a + 8192, &p.tmap_w, &full[stage], kb * 64, wr1, pol_w);
-          tma_load_2d(a + A_BYTES, &p.tmap_x, &full[stage], kb * 64, xr, pol_x);
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+  // Slots present among a tile's pairs (fused LoRA stages), computed by a whole warp.
+  auto tile_slots = [&](int q0, int nvalid) -> unsigned {
+    unsigned m = 0;
+    if (p.lora_fused) {
+      for (int j = lane; j < nvalid; j += 32) {
+        const int sl = p.pair_slot[q0 + j];
+        if (sl >= 0 && sl < kMaxFusedSlots) m |= 1u << sl;
       }
-      if (!ok) {   // drain: let every issued copy land before the CTA exits
-        for (int s = 0; s < S; ++s)
-          if ((issued_mask >> s) & 1u) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
-      }
+      m = __reduce_or_sync(0xffffffffu, m);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {   // ---------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWhereGemmMma)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + stage * STAGE);
-          const uint64_t ad = sw128_kmajor_desc(a_addr);
-          const uint64_t bd = sw128_kmajor_desc(a_addr + A_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-          umma_commit(&empty[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(&tfull[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          aphase ^= 1u;
+    return m;
+  };
+
+  if (warp == 0) {   // ------------------------------------------------ TMA producer (lane 0)
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0;       // stages with a load in flight, and their parity
+    uint32_t issued_parity = 0;
+    int ok = 1;
+    auto issue = [&](const CUtensorMap* wmap, int wr0, int wr1, int kx, const CUtensorMap* xmap, int xrow) -> bool {
+      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) return false;
+      uint8_t* a = smem + stage * STAGE;
+      mbar_arrive_expect_tx(&full[stage], STAGE);
+      tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
+      tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
+      tma_load_2d(a + A_BYTES, xmap, &full[stage], kx, xrow, pol_x);
+      issued_mask |= 1u << stage;
+      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      return true;
+    };
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, qt;
+      decode(tile, e, nt, qt);
+      int wr0, wr1;
+      if (p.gated) {
+        wr0 = e * p.N + nt * 64;
+        wr1 = wr0 + (p.N >> 1);
+      } else {
+        wr0 = e * p.N + nt * 128;
+        wr1 = wr0 + 64;
+      }
+      const int xr = seg[e] + qt * BN;
+      const unsigned smask = tile_slots(xr, min(BN, seg[e + 1] - xr));
+      if (lane == 0) {
+        for (int kb = 0; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+        for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
+          if (!((smask >> sl) & 1u)) continue;
+          for (int kb = 0; ok && kb < p.lora_kb; ++kb)
+            ok = issue(&p.tmap_lb[sl], wr0, wr1, kb * 64, &p.tmap_lu, sl * p.P + xr);
         }
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+    if (lane == 0 && !ok) {   // drain: let every issued copy land before the CTA exits
+      for (int s2 = 0; s2 < S; ++s2)
+        if ((issued_mask >> s2) & 1u) mbar_wait_drain(&full[s2], (issued_parity >> s2) & 1u);
+    }
+  } else if (warp == 1) {   // ------------------------------------------ MMA issuer (lane 0)
+    constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    int ok = 1;
+    auto consume = [&](uint32_t d, bool first) -> bool {
+      if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWhereGemmMma)) return false;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + stage * STAGE);
+      const uint64_t ad = sw128_kmajor_desc(a_addr);
+      const uint64_t bd = sw128_kmajor_desc(a_addr + A_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+      umma_commit(&empty[stage]);
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      return true;
+    };
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, qt;
+      decode(tile, e, nt, qt);
+      const int xr = seg[e] + qt * BN;
+      const unsigned smask = tile_slots(xr, min(BN, seg[e + 1] - xr));
+      if (lane == 0) {
+        ok = mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
+          for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
+            if (!((smask >> sl) & 1u)) continue;
+            for (int kb = 0; ok && kb < p.lora_kb; ++kb) ok = consume(d, false);
+          }
+          if (ok) {
+            umma_commit(&tfull[acc]);
+            if (++acc == 2) {
+              acc = 0;
+              aphase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
   } else {   // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;

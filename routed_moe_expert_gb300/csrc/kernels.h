@@ -13,6 +13,7 @@ constexpr int kMaxRank = 128;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxRouteCtas = 256;
+constexpr int kMaxFusedSlots = 8;   // slots the GEMMs can take as extra LoRA MMA stages
 
 // "where" tags of the device status word (bits 8 and up; the low byte is the code)
 enum : uint32_t {
@@ -60,7 +61,17 @@ struct GemmParams {
   const int32_t* offsets;        // [E + 1]
   uint32_t* status;
   int E, N, K, gated, stages;
-  // Optional LoRA expand added in the epilogue before the store (down GEMM):
+  // Optional LoRA expand as extra MMA K-stages of every tile (fused LoRA): for each slot
+  // s present among the tile's pairs, A' = rows of lora B of slot s (tmap_lb[s], inner
+  // extent ranks[s], so the stacked rank tail reads as zero) and B' = the tile's rows of
+  // ub = scaling[s] * bf16(shrink), zero for pairs of other slots (tmap_lu, rows s*P + q).
+  CUtensorMap tmap_lb[kMaxFusedSlots];
+  CUtensorMap tmap_lu;           // [S*P rows, RU cols] bf16, box {64, BN}
+  int lora_fused;                // 1: use the extra stages (pair_slot gives the slots)
+  int lora_kb;                   // 64-wide K blocks per slot: ceil(R / 64)
+  int P;
+  // Optional LoRA expand added in the epilogue before the store (down GEMM, when the
+  // fused stages are not usable):
   // out[q, h] += sum_{r<ranks[s]} lora_B[s, e, h, r] * lora_v[q, r]   (s = pair_slot[q])
   // lora_v holds scaling[s] * (down-LoRA shrink), written with pair_slot by the shrink.
   const float* lora_v;           // [P, R] or null
@@ -103,6 +114,8 @@ struct LoraParams {
   const __nv_bfloat16* B;        // [S, E, N, R] or null
   LoraSlots slots;
   float* u_out;                  // [P, R] (shrink only): scaling[s] * u for r < ranks[s]
+  __nv_bfloat16* ub_out;         // [S*P, RU] (shrink only): bf16(scaling[s] * u), zero elsewhere
+  int RU;                        // row stride of ub_out: R rounded up to 8
   int32_t* pair_slot_out;        // [P] (shrink only): the pair's active slot or -1
   __nv_bfloat16* d_out;          // [P, N] (expand)
   uint32_t* status;

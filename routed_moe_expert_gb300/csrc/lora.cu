@@ -139,6 +139,16 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       for (int i = tid; i < PT * p.N / 8; i += kLoraThreads) d4[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
+    if (p.ub_out != nullptr) {   // every slot's row of these pairs starts at zero
+      const int nz = p.slots.S * np * p.RU;
+      for (int i = tid; i < nz; i += kLoraThreads) {
+        const int sl = i / (np * p.RU);
+        const int rem = i - sl * np * p.RU;
+        const int n = rem / p.RU, r = rem - n * p.RU;
+        p.ub_out[(static_cast<size_t>(sl) * p.P + pq[n]) * p.RU + r] = __float2bfloat16_rn(0.0f);
+      }
+      __syncthreads();
+    }
     const unsigned mask0 = smask[0], mask1 = smask[1];
 
     for (int s = 0; s < p.slots.S; ++s) {
@@ -218,7 +228,12 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
         for (int w = 0; w < kLoraWarps; ++w) v += red[w * RP * PT + i];
         const bool mine = (n < np) && (pslot[n] == s) && (r < rank);
         u_s[n * RP + r] = mine ? v : 0.0f;
-        if (!expand && mine) p.u_out[static_cast<size_t>(pq[n]) * R + r] = p.slots.scal[s] * v;
+        if (!expand && mine) {
+          const float sv = p.slots.scal[s] * v;
+          if (p.u_out != nullptr) p.u_out[static_cast<size_t>(pq[n]) * R + r] = sv;
+          if (p.ub_out != nullptr)
+            p.ub_out[(static_cast<size_t>(s) * p.P + pq[n]) * p.RU + r] = __float2bfloat16_rn(sv);
+        }
       }
       __syncthreads();
       if (!expand) continue;

@@ -43,11 +43,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace layout (all offsets 256-byte aligned).
 struct Layout {
   size_t header, ids, wts, offsets, perm, inv, hist, base, total;
-  size_t xp, g, d, a, v, y, pslot;
+  size_t xp, g, d, a, v, y, pslot, ub;
   size_t bytes;
 };
 
-Layout layout_for(int T, int H, int I, int E, int k, int R) {
+Layout layout_for(int T, int H, int I, int E, int k, int R, int S) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t n) {
@@ -72,6 +72,7 @@ Layout layout_for(int T, int H, int I, int E, int k, int R) {
   L.v = take(P * R * 4);
   L.y = take(P * H * 4);
   L.pslot = take(R > 0 ? P * 4 : 0);
+  L.ub = take(static_cast<size_t>(S) * P * ((R + 7) / 8 * 8) * 2);
   L.bytes = off;
   return L;
 }
@@ -133,7 +134,7 @@ moe_lora_status moe_lora_workspace_size(const moe_lora_shape* s, size_t* bytes) 
   if (s->T < 0 || s->H < 0 || s->I < 0 || s->E < 1 || s->E > kMaxExperts || s->top_k < 1 || s->top_k > s->E ||
       s->S < 0 || s->R < 0 || s->R > kMaxRank)
     return MOE_LORA_ERR_INVALID_ARG;
-  *bytes = layout_for(s->T, s->H, s->I, s->E, s->top_k, s->S > 0 ? s->R : 0).bytes;
+  *bytes = layout_for(s->T, s->H, s->I, s->E, s->top_k, s->S > 0 ? s->R : 0, s->S > 0 ? s->S : 0).bytes;
   return MOE_LORA_OK;
 }
 
@@ -292,6 +293,33 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
   return MOE_LORA_OK;
 }
 
+// Tensor maps of the fused LoRA stages: per active slot, the slot's B rows [E*N, ranks[s]]
+// (the inner extent stops at the slot's rank, so the stacked tail is zero-filled, never
+// read), and the per-slot scaled shrink rows ub [S*P, RU].
+bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* B, int N,
+                    const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn) {
+  const int R = a->R;
+  const int RU = (R + 7) & ~7;
+  for (int s = 0; s < a->S; ++s) {
+    if (a->h_ranks[s] <= 0 || a->h_scalings[s] == 0.0f) continue;   // never in pair_slot
+    const moe_lora_bf16* base = B + static_cast<size_t>(s) * a->E * N * R;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->h_ranks[s]), static_cast<cuuint64_t>(a->E) * N};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(R) * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    if (h->encode(&gp.tmap_lb[s], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<moe_lora_bf16*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  if (!make_tmap(h->encode, &gp.tmap_lu, ub, static_cast<uint64_t>(a->S) * P, RU, bn)) return false;
+  gp.lora_fused = 1;
+  gp.lora_kb = (R + 63) / 64;
+  gp.P = P;
+  gp.pair_slot = pair_slot;
+  return true;
+}
+
 void prof(const moe_lora_args* a, int stage, int which, cudaStream_t s) {
   if (a->prof_events == nullptr) return;
   void* ev = a->prof_events[2 * stage + which];
@@ -326,7 +354,7 @@ moe_lora_status moe_lora_route(moe_lora_handle* h, const moe_lora_bf16* router_l
   if (st != MOE_LORA_OK) return st;
   if (expert_offsets == nullptr || (T > 0 && (!topk_ids || !topk_weights || !perm || !inv_perm)))
     return MOE_LORA_ERR_INVALID_ARG;
-  const Layout L = layout_for(T, 0, 0, E, top_k, 0);
+  const Layout L = layout_for(T, 0, 0, E, top_k, 0, 0);
   if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
@@ -358,7 +386,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   cudaStream_t stream = stream_;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const bool lora = lora_active(a);
-  const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0);
+  const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0, a->S > 0 ? a->S : 0);
   if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
@@ -388,15 +416,20 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   LoraSlots slots;
   std::memset(&slots, 0, sizeof(slots));
   if (lora) slots = make_slots(a);
+  const int R = lora ? a->R : 0;
+  const int RU = (R + 7) & ~7;
+  // LoRA expands inside the GEMMs need a TMA-able rank stride and few enough slots
+  const bool fused = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
+  __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
   // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
   const int lora_ntl =
-      (P >= 32 * E && lora_smem_bytes(4, a->S > 0 ? a->R : 0, 2 * I, true, E) <= 200 * 1024) ? 4 : 1;
+      (P >= 32 * E && (fused || lora_smem_bytes(4, R, 2 * I, true, E) <= 200 * 1024)) ? 4 : 1;
   int lora_grid = (P + 8 * lora_ntl - 1) / (8 * lora_ntl) + E;
   if (lora_grid > 2 * h->num_sms) lora_grid = 2 * h->num_sms;
   const bool two = lora && (((T <= 256) && !(a->flags & MOE_LORA_FLAG_FORCE_SINGLE_STREAM)) ||
                             (a->flags & MOE_LORA_FLAG_FORCE_TWO_STREAM));
   cudaStream_t ls = two ? h->side : stream;
-  if (lora) {
+  if (lora) {   // gate_up LoRA: shrink only (fused) or shrink + expand into d
     if (two) {
       ML_CUDA(cudaEventRecord(h->ev_fork, stream), "cudaEventRecord");
       ML_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0), "cudaStreamWaitEvent");
@@ -413,13 +446,20 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     lp.P = P;
     lp.K = H;
     lp.E = E;
-    lp.N = 2 * I;
     lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_gu);
-    lp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
     lp.slots = slots;
-    lp.d_out = d;
     lp.status = status;
     lp.where = kWhereLoraShrinkGu;
+    if (fused) {
+      lp.N = 0;
+      lp.ub_out = ub;
+      lp.RU = RU;
+      lp.pair_slot_out = pair_slot;
+    } else {
+      lp.N = 2 * I;
+      lp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
+      lp.d_out = d;
+    }
     ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, ls), "lora gate_up launch");
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, ls);
     if (two) ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
@@ -431,6 +471,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
   const int bn = pick_bn(P, E);
+  if (fused && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
   GemmParams gu;
   std::memset(&gu, 0, sizeof(gu));
@@ -441,16 +482,17 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   gu.N = 2 * I;
   gu.K = H;
   gu.gated = 1;
+  if (fused && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
   st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
-  if (two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  if (!fused && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
-  ML_CUDA(launch_activation(g, lora ? d : nullptr, P, I, act, stream), "activation launch");
+  ML_CUDA(launch_activation(g, (lora && !fused) ? d : nullptr, P, I, act, stream), "activation launch");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
 
-  if (lora) {   // down-LoRA shrink v = A_dn . a; its expand runs in the down GEMM epilogue
+  if (lora) {   // down-LoRA shrink on the activation; its expand runs inside the down GEMM
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
     LoraParams lp;
     std::memset(&lp, 0, sizeof(lp));
@@ -465,9 +507,13 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     lp.E = E;
     lp.N = 0;
     lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
-    lp.B = nullptr;
     lp.slots = slots;
-    lp.u_out = v;
+    if (fused) {
+      lp.ub_out = ub;
+      lp.RU = RU;
+    } else {
+      lp.u_out = v;
+    }
     lp.pair_slot_out = pair_slot;
     lp.status = status;
     lp.where = kWhereLoraShrinkDn;
@@ -485,7 +531,9 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   dn.N = H;
   dn.K = I;
   dn.gated = 0;
-  if (lora) {
+  if (fused) {
+    if (!fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
+  } else if (lora) {
     dn.lora_v = v;
     dn.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
     dn.pair_slot = pair_slot;
