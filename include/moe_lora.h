@@ -64,7 +64,7 @@ typedef enum {
 #define MOE_LORA_FLAG_LORA_OFF            1u /* base layer only: no LoRA work at all */
 #define MOE_LORA_FLAG_FORCE_SINGLE_STREAM 2u /* never fork the LoRA chain to the side stream */
 #define MOE_LORA_FLAG_FORCE_TWO_STREAM    4u /* fork even above 256 tokens */
-#define MOE_LORA_FLAG_UNFUSED_LORA        8u /* LoRA expands outside the GEMMs (see forward) */
+#define MOE_LORA_FLAG_UNFUSED_LORA        8u /* down-LoRA expand in the epilogue (see forward) */
 
 /* Stages that moe_lora_args.prof_events can bracket (two events per stage). */
 enum {
@@ -164,13 +164,12 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
 
 /* The whole layer: out [T, H] bf16.  `workspace` holds moe_lora_workspace_size() bytes;
    its contents on entry do not matter.
-   LoRA placement: when R is a multiple of 8 and S <= 8, both LoRA expands run inside the
-   grouped GEMMs as extra tensor-core K-stages (the shrinks are separate launches; the
-   gate_up shrink runs on the side stream beside the permute and joins before the gate_up
-   GEMM).  Otherwise, or with MOE_LORA_FLAG_UNFUSED_LORA, the gate_up LoRA chain (shrink +
-   expand into a bf16 delta) runs on the side stream beside the permute and gate_up GEMM and
-   joins before the activation, as in sglang PR #28466 section 1 flow (B), and the down
-   expand runs in the down GEMM's epilogue.  The side stream is used when T <= 256 unless
+   LoRA placement: the gate_up LoRA chain (shrink + expand into a bf16 delta) runs on the
+   side stream beside the permute and gate_up GEMM and joins before the activation, as in
+   sglang PR #28466 section 1 flow (B).  The down-LoRA shrink runs after the activation;
+   when R is a multiple of 8 and S <= 8 its expand runs inside the down GEMM as extra
+   tensor-core K-stages, otherwise (or with MOE_LORA_FLAG_UNFUSED_LORA) in the down GEMM's
+   epilogue on the CUDA cores.  The side stream is used when T <= 256 unless
    FORCE_SINGLE_STREAM (sglang PR #28466, "Which diagram applies when": decode-shaped
    batches only).
    Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */

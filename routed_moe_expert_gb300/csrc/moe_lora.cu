@@ -418,18 +418,21 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   if (lora) slots = make_slots(a);
   const int R = lora ? a->R : 0;
   const int RU = (R + 7) & ~7;
-  // LoRA expands inside the GEMMs need a TMA-able rank stride and few enough slots
+  // The down-LoRA expand runs inside the down GEMM as extra K-stages when the rank stride is
+  // TMA-able and the slots are few.  The gate_up expand stays a separate kernel writing the
+  // bf16 delta: the pages round the gate_up GEMM output and the delta to bf16 separately,
+  // and adding the delta inside the accumulator would round their sum once instead.
   const bool fused = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
+  const bool fused_gu = false;
   __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
   // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
-  const int lora_ntl =
-      (P >= 32 * E && (fused || lora_smem_bytes(4, R, 2 * I, true, E) <= 200 * 1024)) ? 4 : 1;
+  const int lora_ntl = (P >= 32 * E && lora_smem_bytes(4, R, 2 * I, true, E) <= 200 * 1024) ? 4 : 1;
   int lora_grid = (P + 8 * lora_ntl - 1) / (8 * lora_ntl) + E;
   if (lora_grid > 2 * h->num_sms) lora_grid = 2 * h->num_sms;
   const bool two = lora && (((T <= 256) && !(a->flags & MOE_LORA_FLAG_FORCE_SINGLE_STREAM)) ||
                             (a->flags & MOE_LORA_FLAG_FORCE_TWO_STREAM));
   cudaStream_t ls = two ? h->side : stream;
-  if (lora) {   // gate_up LoRA: shrink only (fused) or shrink + expand into d
+  if (lora) {   // gate_up LoRA: shrink + expand into the bf16 delta d
     if (two) {
       ML_CUDA(cudaEventRecord(h->ev_fork, stream), "cudaEventRecord");
       ML_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0), "cudaStreamWaitEvent");
@@ -450,7 +453,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     lp.slots = slots;
     lp.status = status;
     lp.where = kWhereLoraShrinkGu;
-    if (fused) {
+    if (fused_gu) {
       lp.N = 0;
       lp.ub_out = ub;
       lp.RU = RU;
@@ -471,7 +474,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
   const int bn = pick_bn(P, E);
-  if (fused && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  if (fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
   GemmParams gu;
   std::memset(&gu, 0, sizeof(gu));
@@ -482,14 +485,14 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   gu.N = 2 * I;
   gu.K = H;
   gu.gated = 1;
-  if (fused && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
+  if (fused_gu && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
   st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
-  if (!fused && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  if (!fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
-  ML_CUDA(launch_activation(g, (lora && !fused) ? d : nullptr, P, I, act, stream), "activation launch");
+  ML_CUDA(launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream), "activation launch");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
 
   if (lora) {   // down-LoRA shrink on the activation; its expand runs inside the down GEMM

@@ -170,9 +170,9 @@ def test_kimi_sampled(handle, name):
 
 @pytest.mark.parametrize("flags", [0, 8], ids=["fused", "unfused"])   # 8 = FLAG_UNFUSED_LORA
 def test_both_lora_placements_match_oracle(handle, flags):
-    """LoRA expands inside the GEMMs (default at ranks that are multiples of 8) and outside
-    them (separate gate_up expand + down epilogue), both against the oracle, with four
-    slots of mixed rank, a 10% no-adapter share and the NaN-filled rank tails."""
+    """Down-LoRA expand inside the down GEMM (default at ranks that are multiples of 8) and
+    in its epilogue, both against the oracle, with four slots of mixed rank, a 10%
+    no-adapter share and the NaN-filled rank tails."""
     cfg = wl.LayerConfig("place", T=96, H=512, I=256, E=16, top_k=4, ranks=(8, 16, 32, 64),
                          scalings=(2.0, 1.0, 0.5, 0.25), slot_mode="uniform_none10")
     _run_and_check(handle, cfg, seed=21, flags=flags)
