@@ -35,6 +35,7 @@ namespace mlk {
 constexpr int kGemmThreads = 192;
 constexpr int kAByte = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle row each)
 constexpr int kMaxStages = 16;
+constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxStages tiles ahead
 
 int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
@@ -42,7 +43,7 @@ int gemm_smem_bytes(int bn, int stages, int E, int lora_R) {
   // 1 KB alignment slack, stage buffers, barriers, tmem slot + abort flag, schedule,
   // and (LoRA epilogue) per-token slots and shrink values of one tile
   const int lora = lora_R > 0 ? 32 + bn * 4 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
-  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + lora;
+  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + lora + 4 * kTileRing;
 }
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
@@ -70,6 +71,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
   int* lslot = seg + (p.E + 1) + 4;                          // [BN] (LoRA epilogue)
   float* v_s = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(lslot + BN) + 15) & ~static_cast<uintptr_t>(15));
   // v_s: [BN][RP8] (16-byte aligned), RP8 = R rounded up to 8
+  volatile uint32_t* tile_slot_ring =   // producer -> MMA warp: slot mask of the i-th tile
+      reinterpret_cast<volatile uint32_t*>(v_s + (p.lora_v != nullptr ? BN * ((p.slots.R + 7) & ~7) : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -138,19 +141,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     qt = local - nt * nq;
   };
 
-  // Slots present among a tile's pairs (fused LoRA stages), computed by a whole warp.
-  auto tile_slots = [&](int q0, int nvalid) -> unsigned {
-    unsigned m = 0;
-    if (p.lora_fused) {
-      for (int j = lane; j < nvalid; j += 32) {
-        const int sl = p.pair_slot[q0 + j];
-        if (sl >= 0 && sl < kMaxFusedSlots) m |= 1u << sl;
-      }
-      m = __reduce_or_sync(0xffffffffu, m);
-    }
-    return m;
-  };
-
   if (warp == 0) {   // ------------------------------------------------ TMA producer (lane 0)
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
@@ -174,7 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       }
       return true;
     };
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int it_tile = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it_tile) {
       int e, nt, qt;
       decode(tile, e, nt, qt);
       int wr0, wr1;
@@ -186,9 +177,24 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
         wr1 = wr0 + 64;
       }
       const int xr = seg[e] + qt * BN;
-      const unsigned smask = tile_slots(xr, min(BN, seg[e + 1] - xr));
+      // the tile's pair slots are loaded now and reduced after all but the last main stage
+      // are issued, so their latency hides behind the tile's own copies
+      const int nv = min(BN, seg[e + 1] - xr);
+      unsigned lmask = 0;
+      if (p.lora_fused) {
+        for (int j = lane; j < nv; j += 32) {
+          const int sl = p.pair_slot[xr + j];
+          if (sl >= 0 && sl < kMaxFusedSlots) lmask |= 1u << sl;
+        }
+      }
+      if (lane == 0)
+        for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+      const unsigned smask = p.lora_fused ? __reduce_or_sync(0xffffffffu, lmask) : 0u;
       if (lane == 0) {
-        for (int kb = 0; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+        // published before the tile's last main stage arrives (arrive.expect_tx releases it);
+        // the MMA warp reads it after consuming that stage
+        tile_slot_ring[it_tile % kTileRing] = smask;
+        if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xr);
         for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
           if (!((smask >> sl) & 1u)) continue;
           for (int kb = 0; ok && kb < p.lora_kb; ++kb)
@@ -223,17 +229,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       }
       return true;
     };
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int e, nt, qt;
-      decode(tile, e, nt, qt);
-      const int xr = seg[e] + qt * BN;
-      const unsigned smask = tile_slots(xr, min(BN, seg[e + 1] - xr));
+    int it_tile = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it_tile) {
       if (lane == 0) {
         ok = mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma);
         if (ok) {
           tc_fence_after();
           const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
+          // the tile's first stage has landed, so its slot mask is published
+          const unsigned smask = p.lora_fused ? tile_slot_ring[it_tile % kTileRing] : 0u;
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
             if (!((smask >> sl) & 1u)) continue;
             for (int kb = 0; ok && kb < p.lora_kb; ++kb) ok = consume(d, false);
