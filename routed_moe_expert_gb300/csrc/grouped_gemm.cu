@@ -40,10 +40,13 @@ constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxS
 int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
 int gemm_smem_bytes(int bn, int stages, int E, int lora_R) {
-  // 1 KB alignment slack, stage buffers, barriers, tmem slot + abort flag, schedule,
-  // and (LoRA epilogue) per-token slots and shrink values of one tile
-  const int lora = lora_R > 0 ? 32 + bn * 4 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
-  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + lora + 4 * kTileRing;
+  // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
+  // barriers (2*stages), tfull/tempty (4), drain (1); tmem slot + abort flag (16 B);
+  // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
+  // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes.
+  const int ring = 4 * (kTileRing + 4);
+  const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
+  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + ring + lora;
 }
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
@@ -68,11 +71,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);   // [E + 1]
   int* seg = tile_start + (p.E + 1);                         // offsets copy [E + 1]
-  int* lslot = seg + (p.E + 1) + 4;                          // [BN] (LoRA epilogue)
+  volatile uint32_t* tile_slot_ring =                        // [kTileRing] producer -> MMA warp:
+      reinterpret_cast<volatile uint32_t*>(seg + (p.E + 1));  //   LoRA slot mask of the i-th tile
+  int* lslot = seg + (p.E + 1) + kTileRing + 4;              // [BN] (LoRA epilogue)
   float* v_s = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(lslot + BN) + 15) & ~static_cast<uintptr_t>(15));
   // v_s: [BN][RP8] (16-byte aligned), RP8 = R rounded up to 8
-  volatile uint32_t* tile_slot_ring =   // producer -> MMA warp: slot mask of the i-th tile
-      reinterpret_cast<volatile uint32_t*>(v_s + (p.lora_v != nullptr ? BN * ((p.slots.R + 7) & ~7) : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
