@@ -167,9 +167,9 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
    LoRA placement: the gate_up LoRA chain (shrink + expand into a bf16 delta) runs on the
    side stream beside the permute and gate_up GEMM and joins before the activation, as in
    sglang PR #28466 section 1 flow (B).  The down-LoRA shrink runs after the activation;
-   when R is a multiple of 8 and S <= 8 its expand runs inside the down GEMM as extra
-   tensor-core K-stages, otherwise (or with MOE_LORA_FLAG_UNFUSED_LORA) in the down GEMM's
-   epilogue on the CUDA cores.  The side stream is used when T <= 256 unless
+   when R is a multiple of 8, S <= 8 and the GEMM's token tiles are 32 or wider, its expand
+   runs inside the down GEMM as extra tensor-core K-stages, otherwise (or with
+   MOE_LORA_FLAG_UNFUSED_LORA) in the down GEMM's epilogue on the CUDA cores.  The side stream is used when T <= 256 unless
    FORCE_SINGLE_STREAM (sglang PR #28466, "Which diagram applies when": decode-shaped
    batches only).
    Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */

@@ -422,7 +422,10 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   // TMA-able and the slots are few.  The gate_up expand stays a separate kernel writing the
   // bf16 delta: the pages round the gate_up GEMM output and the delta to bf16 separately,
   // and adding the delta inside the accumulator would round their sum once instead.
-  const bool fused = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
+  // At 16-token tiles (decode) the epilogue expand costs less than an extra K-stage.
+  const int bn = pick_bn(P, E);
+  const bool fused = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && bn >= 32 &&
+                     !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
   const bool fused_gu = false;
   __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
   // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
@@ -473,7 +476,6 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
           "permute launch");
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
-  const int bn = pick_bn(P, E);
   if (fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
   GemmParams gu;
