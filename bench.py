@@ -163,6 +163,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
 
     def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
+        flags |= args.flags
         return pkg.moe_lora_forward(
             h, g["hidden"] if hidden is None else hidden, g["router_logits"] if logits is None else logits,
             g["w1"], g["w2"], k, routing_method=cfg.method, correction_bias=g["correction_bias"],
@@ -283,6 +284,7 @@ def run_gpu(args):
             "lora_ranks": list(cfg.ranks), "routing": "DeepSeekV3" if cfg.method else "Renormalize",
             "l2": f"inputs larger than L2: {touched} touched experts = {touched * w_bytes_expert / 1e9:.2f} GB of weights per step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "forward_flags": args.flags,
             "step_bytes": step_bytes, "step_flops": step_flops,
             "step_roofline_frac": max(step_bytes / (peaks["hbm_gbs"] * 1e9),
                                       step_flops / (peaks["bf16_tflops_sustained"] * 1e12)) / (agg["ms_per_step"] / 1e3),
@@ -410,6 +412,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--ref-steps", type=int, default=5)
+    ap.add_argument("--flags", type=int, default=0, help="extra moe_lora_forward flags (e.g. 8: unfused LoRA)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

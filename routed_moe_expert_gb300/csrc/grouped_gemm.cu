@@ -25,6 +25,13 @@
 // output row is stored "gated-interleaved": column 128n + j is gate feature 64n + j for
 // j < 64 and up feature 64n + j - 64 for j >= 64.
 //
+// gated = 2 (gate_up with the activation fused): each 32-lane TMEM quarter holds 16 gate
+// rows and the matching 16 up rows of the tile's 64 features (eight 16-row TMA copies per
+// stage), fused LoRA stages go to a second accumulator, and the epilogue rounds g and the
+// LoRA delta to bf16 separately (the pages' two bf16 tensors), adds them, pairs gate with up
+// lanes by a shuffle and writes a = bf16(silu(gate) * up) -- the activation of sglang PR
+// #28466's launcher row -- straight to the [P, N/2] output.
+//
 // Every mbarrier wait is bounded (2 s); a timeout records MOE_LORA_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, drains the copies already issued and frees TMEM before returning.
 #include "common.cuh"
@@ -59,7 +66,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
 
   constexpr uint32_t A_BYTES = kAByte;
   constexpr uint32_t STAGE = A_BYTES + BN * 128;
-  constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  // two accumulators (double buffer), plus two for the LoRA delta when the activation is fused
+  const bool delta_acc = p.gated == 2 && p.lora_fused;
+  const uint32_t TMEM_COLS = delta_acc ? ((4 * BN < 32) ? 32u : 4u * BN) : ((2 * BN < 32) ? 32u : 2u * BN);
   const int S = p.stages;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
@@ -79,7 +88,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
+  if (TMEM_COLS > 512u) {   // the host never asks for this; refuse instead of over-allocating
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_status(p.status, kDevTimeout, kWhereGemmMma);
+    return;
+  }
   const int NT = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);   // 128-row weight tiles per expert
+  const bool quad = p.gated == 2;                              // 16-row gate/up interleave
   const int KB = p.K >> 6;                                    // 64-wide K blocks
 
   if (threadIdx.x == 0) {
@@ -156,8 +170,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) return false;
       uint8_t* a = smem + stage * STAGE;
       mbar_arrive_expect_tx(&full[stage], STAGE);
-      tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
-      tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
+      if (quad) {   // quarter qq: 16 gate rows then the 16 matching up rows
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          tma_load_2d(a + qq * 4096, wmap, &full[stage], kx, wr0 + 16 * qq, pol_w);
+          tma_load_2d(a + qq * 4096 + 2048, wmap, &full[stage], kx, wr1 + 16 * qq, pol_w);
+        }
+      } else {
+        tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
+        tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
+      }
       tma_load_2d(a + A_BYTES, xmap, &full[stage], kx, xrow, pol_x);
       issued_mask |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -242,9 +264,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
           for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
           // the tile's first stage has landed, so its slot mask is published
           const unsigned smask = p.lora_fused ? tile_slot_ring[it_tile % kTileRing] : 0u;
+          const uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(2 * BN + acc * BN) : d;
+          bool first_delta = delta_acc;   // the delta accumulator starts fresh each tile
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
             if (!((smask >> sl) & 1u)) continue;
-            for (int kb = 0; ok && kb < p.lora_kb; ++kb) ok = consume(d, false);
+            for (int kb = 0; ok && kb < p.lora_kb; ++kb) {
+              ok = consume(dl, first_delta);
+              first_delta = false;
+            }
           }
           if (ok) {
             umma_commit(&tfull[acc]);
@@ -256,6 +283,60 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+  } else if (quad) {   // ------------------------------------- epilogue, fused activation
+    const int quarter = warp & 3;
+    const int I = p.N >> 1;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, qt;
+      decode(tile, e, nt, qt);
+      const int q0 = seg[e] + qt * BN;
+      const int nvalid = min(BN, seg[e + 1] - q0);
+      // the delta accumulator holds this tile's LoRA only if some slot was present
+      unsigned lmask = 0;
+      if (delta_acc) {
+        for (int j = lane; j < nvalid; j += 32) {
+          const int sl = p.pair_slot[q0 + j];
+          if (sl >= 0 && sl < kMaxFusedSlots) lmask |= 1u << sl;
+        }
+        lmask = __reduce_or_sync(0xffffffffu, lmask);
+      }
+      if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+      tc_fence_after();
+      const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tm = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
+      const uint32_t td = tmem_base + lane_base + static_cast<uint32_t>(2 * BN + acc * BN);
+      const int f = nt * 64 + quarter * 16 + (lane & 15);   // feature; lanes 0-15 gate, 16-31 up
+#pragma unroll 1
+      for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
+        uint32_t gv[16], dv[16];
+        tmem_ld_x16(tm + c, gv);
+        if (lmask) tmem_ld_x16(td + c, dv);
+        tmem_ld_wait();
+        float z[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {   // bf16(g) + bf16(delta), added in fp32
+          z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
+          if (lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
+        }
+        float up[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) up[j] = __shfl_down_sync(0xffffffffu, z[j], 16);
+        if (lane < 16) {
+          __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * I + f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c + j < nvalid) o[static_cast<size_t>(j) * I] = f2bf(z[j] / (1.0f + expf(-z[j])) * up[j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
     }
   } else {   // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;

@@ -19,6 +19,7 @@ constexpr int kMaxFusedSlots = 8;   // slots the GEMMs can take as extra LoRA MM
 enum : uint32_t {
   kWhereRouteBarrier = 1, kWhereGemmProducer = 2, kWhereGemmMma = 3, kWhereGemmEpilogue = 4,
   kWhereLoraShrinkGu = 5, kWhereLoraExpandGu = 6, kWhereLoraShrinkDn = 7, kWhereFinalize = 8,
+  kWhereLoraShrinkTc = 9,
 };
 
 struct LoraSlots {
@@ -122,6 +123,24 @@ struct LoraParams {
   uint32_t where;
 };
 size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E);
+
+// Tensor-core shrink of every slot at once (needs R % 8 == 0 and S*R <= 256): writes
+// ub[s][q][r] = bf16(scaling[s] * A[s,e,r,:] . X[q,:]) for q's own slot s and r < ranks[s],
+// zero for every other (s, r), and pair_slot[q].
+struct ShrinkTcParams {
+  CUtensorMap tmap_x;            // X [P rows, K cols], box {64, 64}
+  CUtensorMap tmap_a;            // A [S*E*R rows, K cols], box {64, R}
+  const int32_t* offsets;        // [E + 1]
+  const int32_t* perm;           // [P]
+  const int32_t* slot_idx;       // [T]
+  int k, P, K, E, S, R;
+  LoraSlots slots;
+  __nv_bfloat16* ub;             // [S, P, R]
+  int32_t* pair_slot;            // [P]
+  uint32_t* status;
+};
+int lora_shrink_tc_nb(int S, int R);
+cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream);
 
 }  // namespace mlk

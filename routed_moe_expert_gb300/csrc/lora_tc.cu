@@ -1,0 +1,281 @@
+// LoRA shrink on the 5th-generation tensor cores, all slots at once.
+//
+//   u[q, s, r] = sum_k X[q, k] * A[s, e, r, k]        (pair q of expert e, fp32 in TMEM)
+//   ub[s, q, r] = bf16( scaling[s] * u[q, s, r] )  for s = the slot of q's token and r < ranks[s]
+//   ub[s', q, r] = 0                               for every other slot s' (and r >= ranks[s])
+//   pair_slot[q] = s, or -1 when q's token has no active adapter
+//
+// This is the shrink (A) half of the per-expert LoRA of sglang PR #28466 (section 1,
+// merged_experts_fused_moe_lora_add) for the gate_up chain (X = permuted hidden) and the
+// down chain (X = activation).  Its output feeds the expand (B) half, which runs inside the
+// grouped GEMMs as extra K-stages.  The tile is M = 128 pairs of one expert (rows of X by
+// TMA) by N = every slot's rank rows of A for that expert, stacked (N = S*R <= 256), so one
+// pass over K serves all slots present; the rank tail of a stacked adapter only produces
+// accumulator columns that are never read.  Warp roles as in the grouped GEMM: TMA
+// producer, MMA issuer + TMEM owner, 4 epilogue warps; bounded waits throughout.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mlk {
+
+constexpr int kShrinkThreads = 192;
+constexpr int kShrinkStages = 6;
+
+int lora_shrink_tc_smem(int nb, int E) {
+  return 1024 + kShrinkStages * (16384 + nb * 128) + (2 * kShrinkStages + 5) * 8 + 16 + 8 * (E + 1) + 16;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const __grid_constant__ ShrinkTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  constexpr uint32_t A_BYTES = 16384;
+  constexpr uint32_t STAGE = A_BYTES + NB * 128;
+  constexpr uint32_t TMEM_COLS = (2 * NB <= 32) ? 32 : (2 * NB <= 64 ? 64 : (2 * NB <= 128 ? 128 : (2 * NB <= 256 ? 256 : 512)));
+  constexpr int S = kShrinkStages;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  int* seg = tile_start + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int KB = p.K >> 6;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 128);
+    mbar_init(&tempty[1], 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmap_x);
+    tma_prefetch_desc(&p.tmap_a);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {   // tiles of 128 pairs per expert
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      int cnt = 0;
+      if (e < E) {
+        const int lo = p.offsets[e], hi = p.offsets[e + 1];
+        seg[e] = lo;
+        if (e == E - 1) seg[E] = hi;
+        cnt = (hi - lo + 127) / 128;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (e < E) tile_start[e] = carry + incl - cnt;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[E];
+  auto decode = [&](int tile, int& e, int& qt) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    qt = tile - tile_start[e];
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {   // ---------------------------------------------- TMA producer
+      const uint64_t pol_x = l2_policy_evict_first();
+      const uint64_t pol_a = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int e, qt;
+        decode(tile, e, qt);
+        const int xr = seg[e] + qt * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereLoraShrinkTc)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + stage * STAGE;
+          // bytes actually copied: 128 rows of X and S*R rows of A (rows S*R..NB-1 of the B
+          // tile stay unwritten; they only feed accumulator columns that are never read)
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + static_cast<uint32_t>(p.S * p.R) * 128u);
+          tma_load_2d(a, &p.tmap_x, &full[stage], kb * 64, xr, pol_x);
+          tma_load_2d(a + 8192, &p.tmap_x, &full[stage], kb * 64, xr + 64, pol_x);
+          for (int s = 0; s < p.S; ++s)   // each slot's R rows of A for expert e, stacked
+            tma_load_2d(a + A_BYTES + s * p.R * 128, &p.tmap_a, &full[stage], kb * 64, (s * E + e) * p.R, pol_a);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < S; ++s)
+          if ((issued_mask >> s) & 1u) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {   // ---------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereLoraShrinkTc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * NB);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWhereLoraShrinkTc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE);
+          const uint64_t ad = sw128_kmajor_desc(a_addr);
+          const uint64_t bd = sw128_kmajor_desc(a_addr + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+    }
+  } else {   // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;   // pair row of the tile == TMEM lane
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, qt;
+      decode(tile, e, qt);
+      const int q = seg[e] + qt * 128 + row;
+      const bool valid = q < seg[e + 1];
+      int sl = -1;
+      if (valid) {
+        sl = p.slot_idx[p.perm[q] / p.k];
+        if (sl < -1 || sl >= p.slots.S) {
+          record_status(p.status, kDevBadSlot, kWhereLoraShrinkTc);
+          sl = -1;
+        } else if (sl >= 0 && (p.slots.ranks[sl] <= 0 || p.slots.scal[sl] == 0.0f)) {
+          sl = -1;
+        }
+      }
+      if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereLoraShrinkTc)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * NB);
+      // Every column (s2, r) of the accumulator goes to ub[s2][q][r]: the scaled value when
+      // s2 is this pair's slot and r < its rank, zero otherwise.  R is a multiple of 8, so
+      // each 8 columns lie in one slot row and leave as one 16-byte store.
+      const float sc = sl >= 0 ? p.slots.scal[sl] : 0.0f;
+      const int rank = sl >= 0 ? p.slots.ranks[sl] : 0;
+      const int ncol = p.S * p.R;
+#pragma unroll 1
+      for (int c = 0; c < ncol; c += 16) {   // tcgen05.ld is warp-wide: same columns in every lane
+        uint32_t v[16];
+        tmem_ld_x16(taddr + c, v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int h8 = 0; h8 < 2; ++h8) {
+            const int col0 = c + 8 * h8;
+            if (col0 >= ncol) break;
+            const int s2 = col0 / p.R, r0 = col0 - s2 * p.R;
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              f[i] = (s2 == sl && r0 + i < rank) ? sc * __uint_as_float(v[8 * h8 + i]) : 0.0f;
+            *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s2) * p.P + q) * p.R + r0) = pack8(f);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+      if (valid) p.pair_slot[q] = sl;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {
+      if (lane == 0) {
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int NB>
+static cudaError_t launch_nb(const ShrinkTcParams& p, int grid, cudaStream_t stream) {
+  const int smem = lora_shrink_tc_smem(NB, p.E);
+  cudaError_t err =
+      cudaFuncSetAttribute(lora_shrink_tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  lora_shrink_tc_kernel<NB><<<grid, kShrinkThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+int lora_shrink_tc_nb(int S, int R) {
+  const int n = S * R;
+  return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 0;
+}
+
+cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream) {
+  if (p.P == 0) return cudaSuccess;
+  switch (lora_shrink_tc_nb(p.S, p.R)) {
+    case 16: return launch_nb<16>(p, grid, stream);
+    case 32: return launch_nb<32>(p, grid, stream);
+    case 64: return launch_nb<64>(p, grid, stream);
+    case 128: return launch_nb<128>(p, grid, stream);
+    case 256: return launch_nb<256>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mlk

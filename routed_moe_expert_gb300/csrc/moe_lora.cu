@@ -286,7 +286,8 @@ int pick_stages(int bn, int E, int lora_R) {
 
 moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, const void* X, int P, int bn,
                              cudaStream_t stream) {
-  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
+  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, gp.gated == 2 ? 16 : 64))
+    return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
   gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0);
   ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream), "grouped_gemm launch");
@@ -298,6 +299,7 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
 // read), and the per-slot scaled shrink rows ub [S*P, RU].
 bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* B, int N,
                     const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn) {
+  const cuuint32_t box_rows = gp.gated == 2 ? 16 : 64;   // 16-row gate/up blocks in the fused-activation mode
   const int R = a->R;
   const int RU = (R + 7) & ~7;
   for (int s = 0; s < a->S; ++s) {
@@ -305,7 +307,7 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
     const moe_lora_bf16* base = B + static_cast<size_t>(s) * a->E * N * R;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->h_ranks[s]), static_cast<cuuint64_t>(a->E) * N};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(R) * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     if (h->encode(&gp.tmap_lb[s], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<moe_lora_bf16*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -318,6 +320,35 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
   gp.P = P;
   gp.pair_slot = pair_slot;
   return true;
+}
+
+// Tensor-core shrink of every slot: X [P, K] (permuted hidden or activation) against the
+// stacked LoRA A [S*E*R, K]; writes ub and pair_slot.
+moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, const void* X, const moe_lora_bf16* A,
+                                  int K, const int32_t* offsets, const int32_t* perm, const LoraSlots& slots,
+                                  __nv_bfloat16* ub, int32_t* pair_slot, uint32_t* status, cudaStream_t stream) {
+  const int P = a->T * a->top_k;
+  ShrinkTcParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  if (!make_tmap(h->encode, &sp.tmap_x, X, static_cast<uint64_t>(P), K, 64)) return MOE_LORA_ERR_CUDA;
+  if (!make_tmap(h->encode, &sp.tmap_a, A, static_cast<uint64_t>(a->S) * a->E * a->R, K, a->R)) return MOE_LORA_ERR_CUDA;
+  sp.offsets = offsets;
+  sp.perm = perm;
+  sp.slot_idx = a->slot_idx;
+  sp.k = a->top_k;
+  sp.P = P;
+  sp.K = K;
+  sp.E = a->E;
+  sp.S = a->S;
+  sp.R = a->R;
+  sp.slots = slots;
+  sp.ub = ub;
+  sp.pair_slot = pair_slot;
+  sp.status = status;
+  int grid = (P + 127) / 128 + a->E;
+  if (grid > h->num_sms) grid = h->num_sms;
+  ML_CUDA(launch_lora_shrink_tc(sp, grid, stream), "lora shrink (tensor cores) launch");
+  return MOE_LORA_OK;
 }
 
 void prof(const moe_lora_args* a, int stage, int which, cudaStream_t s) {
@@ -341,83 +372,27 @@ LoraSlots make_slots(const moe_lora_args* a) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-moe_lora_status moe_lora_route(moe_lora_handle* h, const moe_lora_bf16* router_logits, const float* correction_bias,
-                               int T, int E, int top_k, int routing_method, float routed_scaling_factor, int n_group,
-                               int topk_group, int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
-                               int32_t* perm, int32_t* inv_perm, void* workspace, size_t workspace_bytes,
-                               moe_lora_stream stream) {
-  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
-  moe_lora_status st = check_routing_args(T, E, top_k, routing_method, router_logits, correction_bias, n_group,
-                                          topk_group);
-  if (st != MOE_LORA_OK) return st;
-  if (expert_offsets == nullptr || (T > 0 && (!topk_ids || !topk_weights || !perm || !inv_perm)))
-    return MOE_LORA_ERR_INVALID_ARG;
-  const Layout L = layout_for(T, 0, 0, E, top_k, 0, 0);
-  if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
-  if (T == 0) {
-    ML_CUDA(cudaMemsetAsync(expert_offsets, 0, (static_cast<size_t>(E) + 1) * 4, stream), "cudaMemsetAsync");
-    return MOE_LORA_OK;
-  }
-  return enqueue_route(h, router_logits, correction_bias, T, E, top_k, routing_method, routed_scaling_factor,
-                       topk_ids, topk_weights, expert_offsets, perm, inv_perm, ws, L, stream);
-}
-
-moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden, const int32_t* perm, int T, int H,
-                                 int top_k, moe_lora_bf16* permuted, moe_lora_stream stream) {
-  if (h == nullptr || T < 0 || H < 8 || H % 8 != 0 || top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
-  if (T == 0) return MOE_LORA_OK;
-  if (!hidden || !perm || !permuted || !aligned16(hidden) || !aligned16(permuted)) return MOE_LORA_ERR_INVALID_ARG;
-  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(hidden), perm, T * top_k, top_k, H,
-                         reinterpret_cast<__nv_bfloat16*>(permuted), stream),
-          "permute launch");
-  return MOE_LORA_OK;
-}
-
-moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out, void* workspace,
-                                 size_t workspace_bytes, moe_lora_stream stream_) {
-  moe_lora_status st = moe_lora_validate(a);
-  if (st != MOE_LORA_OK) return st;
-  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
-  if (a->T > 0 && (out == nullptr || !aligned16(out))) return MOE_LORA_ERR_INVALID_ARG;
-  cudaStream_t stream = stream_;
+// The LoRA placement the pages draw (sglang PR #28466 section 1 flow (B)): the gate_up LoRA
+// chain -- shrink and expand into the bf16 delta d -- on the side stream beside the permute
+// and gate_up GEMM, joined before the activation; the down shrink after it; the down expand
+// in the down GEMM (extra K-stages) or its epilogue.  Used when the fully fused path is not
+// (ranks not a multiple of 8, more than 8 slots, or MOE_LORA_FLAG_UNFUSED_LORA).
+moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_args* a, uint8_t* ws, const Layout& L,
+                                          int32_t* perm, int32_t* offsets, int32_t* ids, __nv_bfloat16* xp,
+                                          __nv_bfloat16* g, __nv_bfloat16* d, __nv_bfloat16* act, float* v, float* y,
+                                          int32_t* pair_slot, __nv_bfloat16* ub, const LoraSlots& slots,
+                                          uint32_t* status, cudaStream_t stream) {
+  (void)ws;
+  (void)L;
+  (void)ids;
+  const bool lora = true;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
-  const bool lora = lora_active(a);
-  const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0, a->S > 0 ? a->S : 0);
-  if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
-  if (T == 0) return MOE_LORA_OK;
-
   const int P = T * k;
-  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.header);
-  int32_t* ids = a->topk_ids ? a->topk_ids : reinterpret_cast<int32_t*>(ws + L.ids);
-  float* wts = a->topk_weights ? a->topk_weights : reinterpret_cast<float*>(ws + L.wts);
-  int32_t* offsets = a->expert_offsets ? a->expert_offsets : reinterpret_cast<int32_t*>(ws + L.offsets);
-  int32_t* perm = a->perm ? a->perm : reinterpret_cast<int32_t*>(ws + L.perm);
-  int32_t* inv = a->inv_perm ? a->inv_perm : reinterpret_cast<int32_t*>(ws + L.inv);
-  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + L.xp);
-  __nv_bfloat16* g = reinterpret_cast<__nv_bfloat16*>(ws + L.g);
-  __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(ws + L.d);
-  __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
-  float* v = reinterpret_cast<float*>(ws + L.v);
-  float* y = reinterpret_cast<float*>(ws + L.y);
-  int32_t* pair_slot = reinterpret_cast<int32_t*>(ws + L.pslot);
-
-  prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
-  st = enqueue_route(h, a->router_logits, a->correction_bias, T, E, k, a->routing_method, a->routed_scaling_factor,
-                     ids, wts, offsets, perm, inv, ws, L, stream);
-  if (st != MOE_LORA_OK) return st;
-  prof(a, MOE_LORA_STAGE_ROUTE, 1, stream);
-
-  LoraSlots slots;
-  std::memset(&slots, 0, sizeof(slots));
-  if (lora) slots = make_slots(a);
-  const int R = lora ? a->R : 0;
+  const int R = a->R;
   const int RU = (R + 7) & ~7;
+  moe_lora_status st = MOE_LORA_OK;
   // The down-LoRA expand runs inside the down GEMM as extra K-stages when the rank stride is
   // TMA-able and the slots are few.  The gate_up expand stays a separate kernel writing the
   // bf16 delta: the pages round the gate_up GEMM output and the delta to bf16 separately,
@@ -427,7 +402,6 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   const bool fused = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && bn >= 32 &&
                      !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
   const bool fused_gu = false;
-  __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
   // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
   const int lora_ntl = (P >= 32 * E && lora_smem_bytes(4, R, 2 * I, true, E) <= 200 * 1024) ? 4 : 1;
   int lora_grid = (P + 8 * lora_ntl - 1) / (8 * lora_ntl) + E;
@@ -547,6 +521,147 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+
+  return MOE_LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_lora_status moe_lora_route(moe_lora_handle* h, const moe_lora_bf16* router_logits, const float* correction_bias,
+                               int T, int E, int top_k, int routing_method, float routed_scaling_factor, int n_group,
+                               int topk_group, int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                               int32_t* perm, int32_t* inv_perm, void* workspace, size_t workspace_bytes,
+                               moe_lora_stream stream) {
+  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  moe_lora_status st = check_routing_args(T, E, top_k, routing_method, router_logits, correction_bias, n_group,
+                                          topk_group);
+  if (st != MOE_LORA_OK) return st;
+  if (expert_offsets == nullptr || (T > 0 && (!topk_ids || !topk_weights || !perm || !inv_perm)))
+    return MOE_LORA_ERR_INVALID_ARG;
+  const Layout L = layout_for(T, 0, 0, E, top_k, 0, 0);
+  if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
+  if (T == 0) {
+    ML_CUDA(cudaMemsetAsync(expert_offsets, 0, (static_cast<size_t>(E) + 1) * 4, stream), "cudaMemsetAsync");
+    return MOE_LORA_OK;
+  }
+  return enqueue_route(h, router_logits, correction_bias, T, E, top_k, routing_method, routed_scaling_factor,
+                       topk_ids, topk_weights, expert_offsets, perm, inv_perm, ws, L, stream);
+}
+
+moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden, const int32_t* perm, int T, int H,
+                                 int top_k, moe_lora_bf16* permuted, moe_lora_stream stream) {
+  if (h == nullptr || T < 0 || H < 8 || H % 8 != 0 || top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (T == 0) return MOE_LORA_OK;
+  if (!hidden || !perm || !permuted || !aligned16(hidden) || !aligned16(permuted)) return MOE_LORA_ERR_INVALID_ARG;
+  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(hidden), perm, T * top_k, top_k, H,
+                         reinterpret_cast<__nv_bfloat16*>(permuted), stream),
+          "permute launch");
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out, void* workspace,
+                                 size_t workspace_bytes, moe_lora_stream stream_) {
+  moe_lora_status st = moe_lora_validate(a);
+  if (st != MOE_LORA_OK) return st;
+  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (a->T > 0 && (out == nullptr || !aligned16(out))) return MOE_LORA_ERR_INVALID_ARG;
+  cudaStream_t stream = stream_;
+  const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
+  const bool lora = lora_active(a);
+  const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0, a->S > 0 ? a->S : 0);
+  if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
+  if (T == 0) return MOE_LORA_OK;
+
+  const int P = T * k;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.header);
+  int32_t* ids = a->topk_ids ? a->topk_ids : reinterpret_cast<int32_t*>(ws + L.ids);
+  float* wts = a->topk_weights ? a->topk_weights : reinterpret_cast<float*>(ws + L.wts);
+  int32_t* offsets = a->expert_offsets ? a->expert_offsets : reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* perm = a->perm ? a->perm : reinterpret_cast<int32_t*>(ws + L.perm);
+  int32_t* inv = a->inv_perm ? a->inv_perm : reinterpret_cast<int32_t*>(ws + L.inv);
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + L.xp);
+  __nv_bfloat16* g = reinterpret_cast<__nv_bfloat16*>(ws + L.g);
+  __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(ws + L.d);
+  __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
+  float* v = reinterpret_cast<float*>(ws + L.v);
+  float* y = reinterpret_cast<float*>(ws + L.y);
+  int32_t* pair_slot = reinterpret_cast<int32_t*>(ws + L.pslot);
+
+  prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
+  st = enqueue_route(h, a->router_logits, a->correction_bias, T, E, k, a->routing_method, a->routed_scaling_factor,
+                     ids, wts, offsets, perm, inv, ws, L, stream);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_ROUTE, 1, stream);
+
+  LoraSlots slots;
+  std::memset(&slots, 0, sizeof(slots));
+  if (lora) slots = make_slots(a);
+  const int R = lora ? a->R : 0;
+  const int RU = (R + 7) & ~7;
+  __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
+  // Fully fused LoRA: both shrinks on the tensor cores, both expands inside the GEMMs, the
+  // activation in the gate_up GEMM's epilogue.  Needs a TMA-able rank stride, few slots and
+  // the stacked ranks within one MMA N.
+  const bool fuse_all = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && a->S * R <= 256 &&
+                        !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
+  if (!lora || fuse_all) {
+    int bn = pick_bn(P, E);
+    if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the LoRA delta accumulators
+    prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
+    ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream),
+            "permute launch");
+    prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
+    if (fuse_all) {
+      prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
+      st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream);
+      if (st != MOE_LORA_OK) return st;
+      prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
+    }
+    prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
+    GemmParams gu;
+    std::memset(&gu, 0, sizeof(gu));
+    gu.out = act;   // the activation, written by the GEMM's epilogue
+    gu.offsets = offsets;
+    gu.status = status;
+    gu.E = E;
+    gu.N = 2 * I;
+    gu.K = H;
+    gu.gated = 2;
+    if (fuse_all && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
+    st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream);
+    if (st != MOE_LORA_OK) return st;
+    prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
+    if (fuse_all) {
+      prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
+      st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream);
+      if (st != MOE_LORA_OK) return st;
+      prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
+    }
+    prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
+    GemmParams dn;
+    std::memset(&dn, 0, sizeof(dn));
+    dn.out_f32 = y;
+    dn.offsets = offsets;
+    dn.status = status;
+    dn.E = E;
+    dn.N = H;
+    dn.K = I;
+    dn.gated = 0;
+    if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
+    st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream);
+    if (st != MOE_LORA_OK) return st;
+    prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+  } else {
+    st = enqueue_unfused_lora_path(h, a, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub, slots,
+                                   status, stream);
+    if (st != MOE_LORA_OK) return st;
+  }
 
   prof(a, MOE_LORA_STAGE_FINALIZE, 0, stream);
   FinalizeParams fp;
