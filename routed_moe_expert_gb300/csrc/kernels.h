@@ -134,6 +134,7 @@ struct ShrinkTcParams {
   const int32_t* perm;           // [P]
   const int32_t* slot_idx;       // [T]
   int k, P, K, E, S, R;
+  int stages;                    // pipeline depth (set by the launcher)
   LoraSlots slots;
   __nv_bfloat16* ub;             // [S, P, R]
   int32_t* pair_slot;            // [P]

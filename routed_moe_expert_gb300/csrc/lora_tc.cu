@@ -19,10 +19,16 @@
 namespace mlk {
 
 constexpr int kShrinkThreads = 192;
-constexpr int kShrinkStages = 6;
+constexpr int kShrinkMaxStages = 6;
+
+static int shrink_stages(int nb) {   // as many 16 KB + N*128 B stages as fit in ~200 KB
+  const int s = (200 * 1024) / (16384 + nb * 128);
+  return s < kShrinkMaxStages ? s : kShrinkMaxStages;
+}
 
 int lora_shrink_tc_smem(int nb, int E) {
-  return 1024 + kShrinkStages * (16384 + nb * 128) + (2 * kShrinkStages + 5) * 8 + 16 + 8 * (E + 1) + 16;
+  const int st = shrink_stages(nb);
+  return 1024 + st * (16384 + nb * 128) + (2 * st + 5) * 8 + 16 + 8 * (E + 1) + 16;
 }
 
 template <int NB>
@@ -33,7 +39,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
   constexpr uint32_t A_BYTES = 16384;
   constexpr uint32_t STAGE = A_BYTES + NB * 128;
   constexpr uint32_t TMEM_COLS = (2 * NB <= 32) ? 32 : (2 * NB <= 64 ? 64 : (2 * NB <= 128 ? 128 : (2 * NB <= 256 ? 256 : 512)));
-  constexpr int S = kShrinkStages;
+  const int S = p.stages;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
   uint64_t* empty = full + S;
@@ -252,7 +258,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
 }
 
 template <int NB>
-static cudaError_t launch_nb(const ShrinkTcParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_nb(const ShrinkTcParams& p_in, int grid, cudaStream_t stream) {
+  ShrinkTcParams p = p_in;
+  p.stages = shrink_stages(NB);
   const int smem = lora_shrink_tc_smem(NB, p.E);
   cudaError_t err =
       cudaFuncSetAttribute(lora_shrink_tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
