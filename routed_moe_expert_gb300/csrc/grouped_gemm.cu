@@ -25,12 +25,12 @@
 // output row is stored "gated-interleaved": column 128n + j is gate feature 64n + j for
 // j < 64 and up feature 64n + j - 64 for j >= 64.
 //
-// gated = 2 (gate_up with the activation fused): each 32-lane TMEM quarter holds 16 gate
-// rows and the matching 16 up rows of the tile's 64 features (eight 16-row TMA copies per
-// stage), fused LoRA stages go to a second accumulator, and the epilogue rounds g and the
-// LoRA delta to bf16 separately (the pages' two bf16 tensors), adds them, pairs gate with up
-// lanes by a shuffle and writes a = bf16(silu(gate) * up) -- the activation of sglang PR
-// #28466's launcher row -- straight to the [P, N/2] output.
+// gated = 2 (gate_up with the activation fused): the tile rows are laid out as for gated =
+// 1, fused LoRA stages go to a second accumulator, and the epilogue rounds g and the LoRA
+// delta to bf16 separately (the pages' two bf16 tensors) and adds them; the two gate warps
+// hand their values to the two up warps through shared memory, and the up warps write
+// a = bf16(silu(gate) * up) -- the activation of sglang PR #28466's launcher row -- straight
+// to the [P, N/2] output.
 //
 // Every mbarrier wait is bounded (2 s); a timeout records MOE_LORA_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, drains the copies already issued and frees TMEM before returning.
@@ -43,17 +43,21 @@ constexpr int kGemmThreads = 192;
 constexpr int kAByte = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle row each)
 constexpr int kMaxStages = 16;
 constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxStages tiles ahead
+constexpr int kXchgStride = 17;                       // floats per gate row (padded against bank conflicts)
+constexpr int kXchgFloats = 2 * 64 * kXchgStride;     // two buffers of 64 rows x 16 tokens
 
 int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
-int gemm_smem_bytes(int bn, int stages, int E, int lora_R) {
+int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused) {
   // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
   // barriers (2*stages), tfull/tempty (4), drain (1); tmem slot + abort flag (16 B);
   // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
   // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes.
   const int ring = 4 * (kTileRing + 4);
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
-  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + ring + lora;
+  const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
+  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + ring +
+         (lora > xchg ? lora : xchg);
 }
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
@@ -93,7 +97,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     return;
   }
   const int NT = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);   // 128-row weight tiles per expert
-  const bool quad = p.gated == 2;                              // 16-row gate/up interleave
   const int KB = p.K >> 6;                                    // 64-wide K blocks
 
   if (threadIdx.x == 0) {
@@ -170,16 +173,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) return false;
       uint8_t* a = smem + stage * STAGE;
       mbar_arrive_expect_tx(&full[stage], STAGE);
-      if (quad) {   // quarter qq: 16 gate rows then the 16 matching up rows
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          tma_load_2d(a + qq * 4096, wmap, &full[stage], kx, wr0 + 16 * qq, pol_w);
-          tma_load_2d(a + qq * 4096 + 2048, wmap, &full[stage], kx, wr1 + 16 * qq, pol_w);
-        }
-      } else {
-        tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
-        tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
-      }
+      tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
+      tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
       tma_load_2d(a + A_BYTES, xmap, &full[stage], kx, xrow, pol_x);
       issued_mask |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -284,10 +279,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
-  } else if (quad) {   // ------------------------------------- epilogue, fused activation
+  } else if (p.gated == 2) {   // ----------------------------- epilogue, fused activation
     const int quarter = warp & 3;
+    const bool gate_warp = quarter < 2;      // TMEM lanes 0-63: gate rows; 64-127: up rows
+    const int frow = (quarter & 1) * 32 + lane;   // feature row 0..63 of the tile
     const int I = p.N >> 1;
-    int acc = 0;
+    float* xchg = reinterpret_cast<float*>(lslot);   // [2][64][kXchgStride]
+    int acc = 0, chunk = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, nt, qt;
@@ -308,9 +306,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tm = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
       const uint32_t td = tmem_base + lane_base + static_cast<uint32_t>(2 * BN + acc * BN);
-      const int f = nt * 64 + quarter * 16 + (lane & 15);   // feature; lanes 0-15 gate, 16-31 up
+      const int f = nt * 64 + frow;
 #pragma unroll 1
-      for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
+      for (int c = 0; c < nvalid; c += 16, ++chunk) {   // warp-uniform bound
         uint32_t gv[16], dv[16];
         tmem_ld_x16(tm + c, gv);
         if (lmask) tmem_ld_x16(td + c, dv);
@@ -321,14 +319,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
           z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
           if (lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
         }
-        float up[16];
+        float* buf = xchg + (chunk & 1) * 64 * kXchgStride + frow * kXchgStride;
+        if (gate_warp) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) up[j] = __shfl_down_sync(0xffffffffu, z[j], 16);
-        if (lane < 16) {
+          for (int j = 0; j < 16; ++j) buf[j] = z[j];
+        }
+        epi_bar();   // gate values of this chunk are in; the other buffer is free again
+        if (!gate_warp) {
           __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * I + f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c + j < nvalid) o[static_cast<size_t>(j) * I] = f2bf(z[j] / (1.0f + expf(-z[j])) * up[j]);
+          for (int j = 0; j < 16; ++j) {
+            const float zg = buf[j];
+            if (c + j < nvalid) o[static_cast<size_t>(j) * I] = f2bf(zg / (1.0f + expf(-zg)) * z[j]);
+          }
         }
       }
       tc_fence_before();
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
 
 template <int BN>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream) {
-  const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0);
+  const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   grouped_gemm_kernel<BN><<<grid, kGemmThreads, smem, stream>>>(p);

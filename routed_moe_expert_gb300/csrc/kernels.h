@@ -54,6 +54,8 @@ int route_max_coop_ctas(int E);
 // gated = 1: the 128-row weight tile n holds gate rows [64n, 64n+64) and up rows
 // [N/2 + 64n, N/2 + 64n + 64); the output row is written interleaved in 64-column
 // halves (gate block then up block), i.e. column 128n + j.
+// gated = 2: same tiles; the epilogue applies the activation (plus the LoRA delta of the
+// fused stages, rounded separately) and writes a [P, N/2] bf16.
 struct GemmParams {
   CUtensorMap tmap_w;            // weights [E*N rows, K cols], box {64, 64}
   CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN}
@@ -80,7 +82,7 @@ struct GemmParams {
   const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
 };
-int gemm_smem_bytes(int bn, int stages, int E, int lora_R);
+int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused);
 int gemm_stage_bytes(int bn);
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream);
 

@@ -275,9 +275,9 @@ int pick_bn(long long P, int E) {
   return 256;
 }
 
-int pick_stages(int bn, int E, int lora_R) {
+int pick_stages(int bn, int E, int lora_R, int act_fused) {
   const int budget = (bn <= 32 ? 160 : 200) * 1024;
-  const int fixed = gemm_smem_bytes(bn, 0, E, lora_R);
+  const int fixed = gemm_smem_bytes(bn, 0, E, lora_R, act_fused);
   int s = (budget - fixed) / (gemm_stage_bytes(bn) + 16);
   if (s > 16) s = 16;
   if (s < 2) s = 2;
@@ -286,10 +286,9 @@ int pick_stages(int bn, int E, int lora_R) {
 
 moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, const void* X, int P, int bn,
                              cudaStream_t stream) {
-  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, gp.gated == 2 ? 16 : 64))
-    return MOE_LORA_ERR_CUDA;
+  if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
-  gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0);
+  gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2);
   ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
@@ -299,7 +298,7 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
 // read), and the per-slot scaled shrink rows ub [S*P, RU].
 bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* B, int N,
                     const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn) {
-  const cuuint32_t box_rows = gp.gated == 2 ? 16 : 64;   // 16-row gate/up blocks in the fused-activation mode
+  const cuuint32_t box_rows = 64;
   const int R = a->R;
   const int RU = (R + 7) & ~7;
   for (int s = 0; s < a->S; ++s) {
