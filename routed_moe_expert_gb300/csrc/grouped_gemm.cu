@@ -319,19 +319,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
           z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
           if (lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
         }
+        // gate warps finish tokens 0-7 of the chunk and up warps tokens 8-15: each side
+        // parks the half the other side needs
+        // row layout: [0, 8) gate values of tokens 8-15 (from the gate warp), [8, 16) up
+        // values of tokens 0-7 (from the up warp)
         float* buf = xchg + (chunk & 1) * 64 * kXchgStride + frow * kXchgStride;
-        if (gate_warp) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) buf[j] = z[j];
-        }
-        epi_bar();   // gate values of this chunk are in; the other buffer is free again
-        if (!gate_warp) {
-          __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * I + f;
+        for (int j = 0; j < 8; ++j) buf[(gate_warp ? 0 : 8) + j] = gate_warp ? z[8 + j] : z[j];
+        epi_bar();   // this chunk's hand-off is in; the other buffer is free again
+        const int j0 = gate_warp ? 0 : 8;
+        __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c + j0) * I + f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float zg = buf[j];
-            if (c + j < nvalid) o[static_cast<size_t>(j) * I] = f2bf(zg / (1.0f + expf(-zg)) * z[j]);
-          }
+        for (int j = 0; j < 8; ++j) {
+          const float zo = buf[(gate_warp ? 8 : 0) + j];   // the other side's value
+          const float zg = gate_warp ? z[j] : zo;        // gate of token j0 + j
+          const float zu = gate_warp ? zo : z[8 + j];    // up of token j0 + j
+          if (c + j0 + j < nvalid) o[static_cast<size_t>(j) * I] = f2bf(zg / (1.0f + __expf(-zg)) * zu);
         }
       }
       tc_fence_before();
