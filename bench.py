@@ -321,6 +321,32 @@ def run_gpu(args):
         off_ms = o0.elapsed_time(o1) / max(1, args.steps // 4)
         line["config"]["lora_off_ms_per_step"] = off_ms
         line["config"]["lora_on_over_off"] = off_ms / agg["ms_per_step"]
+    if args.stage_times:
+        # average device time of every stage of the forward (events on the stream that runs
+        # each stage), LoRA on and LoRA off
+        for label, fl in (("lora_on", 0), ("lora_off", pkg.FLAG_LORA_OFF)):
+            n = 50
+            evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n)]
+            for evs in evsets:
+                for e_ in evs:
+                    e_.record(stream)
+            torch.cuda.synchronize()
+            for i in range(n):
+                fwd(flags=fl, prof=evsets[i])
+            torch.cuda.synchronize()
+            st_ms = {}
+            for si, name in enumerate(pkg.STAGES):
+                vals = []
+                for evs in evsets:
+                    try:
+                        v_ = evs[2 * si].elapsed_time(evs[2 * si + 1])
+                    except RuntimeError:
+                        continue
+                    if v_ > 0:
+                        vals.append(v_)
+                if vals:
+                    st_ms[name] = round(1e3 * statistics.median(vals), 2)
+            line.setdefault("stage_us", {})[label] = st_ms
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, args)
     if rank == 0:
@@ -413,6 +439,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--ref-steps", type=int, default=5)
     ap.add_argument("--flags", type=int, default=0, help="extra moe_lora_forward flags (e.g. 8: unfused LoRA)")
+    ap.add_argument("--stage-times", action="store_true", help="add per-stage device times (us) to the line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
