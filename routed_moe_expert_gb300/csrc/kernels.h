@@ -130,8 +130,9 @@ size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E);
 // ub[s][q][r] = bf16(scaling[s] * A[s,e,r,:] . X[q,:]) for q's own slot s and r < ranks[s],
 // zero for every other (s, r), and pair_slot[q].
 struct ShrinkTcParams {
-  CUtensorMap tmap_x;            // X [P rows, K cols], box {64, 64}
+  CUtensorMap tmap_x;            // X [P rows, K cols], box {64, tb}
   CUtensorMap tmap_a;            // A [S*E*R rows, K cols], box {64, R}
+  int tb;                        // pairs (rows of X) per tile: 16, 32, 64 or 128
   const int32_t* offsets;        // [E + 1]
   const int32_t* perm;           // [P]
   const int32_t* slot_idx;       // [T]

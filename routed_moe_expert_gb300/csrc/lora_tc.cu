@@ -8,8 +8,10 @@
 // This is the shrink (A) half of the per-expert LoRA of sglang PR #28466 (section 1,
 // merged_experts_fused_moe_lora_add) for the gate_up chain (X = permuted hidden) and the
 // down chain (X = activation).  Its output feeds the expand (B) half, which runs inside the
-// grouped GEMMs as extra K-stages.  The tile is M = 128 pairs of one expert (rows of X by
-// TMA) by N = every slot's rank rows of A for that expert, stacked (N = S*R <= 256), so one
+// grouped GEMMs as extra K-stages.  The tile is up to TB pairs of one expert (TB rows of X by
+// TMA, TB in {16..128} from the mean pairs per expert; the MMA runs at M = 128 and the rows
+// past TB are never read back) by N = every slot's rank rows of A for that expert, stacked
+// (N = S*R <= 256), so one
 // pass over K serves all slots present; the rank tail of a stacked adapter only produces
 // accumulator columns that are never read.  Warp roles as in the grouped GEMM: TMA
 // producer, MMA issuer + TMEM owner, 4 epilogue warps; bounded waits throughout.
@@ -20,6 +22,7 @@ namespace mlk {
 
 constexpr int kShrinkThreads = 192;
 constexpr int kShrinkMaxStages = 6;
+
 
 static int shrink_stages(int nb) {   // as many 16 KB + N*128 B stages as fit in ~200 KB
   const int s = (200 * 1024) / (16384 + nb * 128);
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) {   // tiles of 128 pairs per expert
+  if (warp == 2) {   // tiles of TB pairs per expert
     int carry = 0;
     for (int b = 0; b < E; b += 32) {
       const int e = b + lane;
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
         const int lo = p.offsets[e], hi = p.offsets[e + 1];
         seg[e] = lo;
         if (e == E - 1) seg[E] = hi;
-        cnt = (hi - lo + 127) / 128;
+        cnt = (hi - lo + p.tb - 1) / p.tb;
       }
       int incl = cnt;
 #pragma unroll
@@ -123,18 +126,18 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, qt;
         decode(tile, e, qt);
-        const int xr = seg[e] + qt * 128;
+        const int xr = seg[e] + qt * p.tb;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereLoraShrinkTc)) {
             ok = false;
             break;
           }
           uint8_t* a = smem + stage * STAGE;
-          // bytes actually copied: 128 rows of X and S*R rows of A (rows S*R..NB-1 of the B
-          // tile stay unwritten; they only feed accumulator columns that are never read)
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + static_cast<uint32_t>(p.S * p.R) * 128u);
+          // bytes actually copied: TB rows of X and S*R rows of A (rows TB..127 of the A tile
+          // and S*R..NB-1 of the B tile keep stale data; they only feed accumulator lanes and
+          // columns that are never read)
+          mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(p.tb + p.S * p.R) * 128u);
           tma_load_2d(a, &p.tmap_x, &full[stage], kb * 64, xr, pol_x);
-          tma_load_2d(a + 8192, &p.tmap_x, &full[stage], kb * 64, xr + 64, pol_x);
           for (int s = 0; s < p.S; ++s)   // each slot's R rows of A for expert e, stacked
             tma_load_2d(a + A_BYTES + s * p.R * 128, &p.tmap_a, &full[stage], kb * 64, (s * E + e) * p.R, pol_a);
           issued_mask |= 1u << stage;
@@ -192,8 +195,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, qt;
       decode(tile, e, qt);
-      const int q = seg[e] + qt * 128 + row;
-      const bool valid = q < seg[e + 1];
+      const int q = seg[e] + qt * p.tb + row;
+      const bool valid = row < p.tb && q < seg[e + 1];
       int sl = -1;
       if (valid) {
         sl = p.slot_idx[p.perm[q] / p.k];

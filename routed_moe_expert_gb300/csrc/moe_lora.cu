@@ -227,8 +227,8 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
                               int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
                               int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream) {
   if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
-  // one CTA (no grid barrier) up to 512 tokens; beyond, about 64 tokens per CTA
-  int grid = T <= 512 ? 1 : (T + 63) / 64;
+  // about 64 tokens per CTA (one CTA, without a grid barrier, up to 64 tokens)
+  int grid = (T + 63) / 64;
   if (grid > h->coop_ctas[E]) grid = h->coop_ctas[E];
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
   if (grid < 1) grid = 1;
@@ -329,7 +329,10 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   const int P = a->T * a->top_k;
   ShrinkTcParams sp;
   std::memset(&sp, 0, sizeof(sp));
-  if (!make_tmap(h->encode, &sp.tmap_x, X, static_cast<uint64_t>(P), K, 64)) return MOE_LORA_ERR_CUDA;
+  // pairs per tile from the mean pairs per expert, so small experts read only their rows
+  const long long m2 = 2LL * ((P + a->E - 1) / a->E);
+  sp.tb = m2 <= 16 ? 16 : m2 <= 32 ? 32 : m2 <= 64 ? 64 : 128;
+  if (!make_tmap(h->encode, &sp.tmap_x, X, static_cast<uint64_t>(P), K, sp.tb)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &sp.tmap_a, A, static_cast<uint64_t>(a->S) * a->E * a->R, K, a->R)) return MOE_LORA_ERR_CUDA;
   sp.offsets = offsets;
   sp.perm = perm;
@@ -344,7 +347,7 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   sp.ub = ub;
   sp.pair_slot = pair_slot;
   sp.status = status;
-  int grid = (P + 127) / 128 + a->E;
+  int grid = (P + sp.tb - 1) / sp.tb + a->E;
   if (grid > h->num_sms) grid = h->num_sms;
   ML_CUDA(launch_lora_shrink_tc(sp, grid, stream), "lora shrink (tensor cores) launch");
   return MOE_LORA_OK;

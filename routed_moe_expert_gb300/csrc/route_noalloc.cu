@@ -87,7 +87,7 @@ extern "C" moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_lo
     return MOE_LORA_OK;
   }
 
-  int grid = T <= 512 ? 1 : (T + 63) / 64;
+  int grid = (T + 63) / 64;
   const int coop = route_max_coop_ctas(E);
   if (grid > coop) grid = coop;
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
