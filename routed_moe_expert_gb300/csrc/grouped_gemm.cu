@@ -27,10 +27,11 @@
 //
 // gated = 2 (gate_up with the activation fused): the tile rows are laid out as for gated =
 // 1, fused LoRA stages go to a second accumulator, and the epilogue rounds g and the LoRA
-// delta to bf16 separately (the pages' two bf16 tensors) and adds them; the two gate warps
-// hand their values to the two up warps through shared memory, and the up warps write
-// a = bf16(silu(gate) * up) -- the activation of sglang PR #28466's launcher row -- straight
-// to the [P, N/2] output.
+// delta to bf16 separately (the pages' two bf16 tensors) and adds them; the four epilogue
+// warps park these values in shared memory as [feature][token] and then each thread forms
+// a = bf16(silu(gate) * up) -- the activation of sglang PR #28466's launcher row -- for 8
+// consecutive features of one token and writes them to the [P, N/2] output in one 16-byte
+// store.
 //
 // Every mbarrier wait is bounded (2 s); a timeout records MOE_LORA_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, drains the copies already issued and frees TMEM before returning.
@@ -43,8 +44,8 @@ constexpr int kGemmThreads = 192;
 constexpr int kAByte = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle row each)
 constexpr int kMaxStages = 16;
 constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxStages tiles ahead
-constexpr int kXchgStride = 17;                       // floats per gate row (padded against bank conflicts)
-constexpr int kXchgFloats = 2 * 64 * kXchgStride;     // two buffers of 64 rows x 16 tokens
+constexpr int kXchgStride = 17;                       // floats per feature row (padded against bank conflicts)
+constexpr int kXchgFloats = 2 * 128 * kXchgStride;    // two buffers of 128 rows (64 gate, 64 up) x 16 tokens
 
 int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
@@ -281,8 +282,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     }
   } else if (p.gated == 2) {   // ----------------------------- epilogue, fused activation
     const int quarter = warp & 3;
-    const bool gate_warp = quarter < 2;      // TMEM lanes 0-63: gate rows; 64-127: up rows
-    const int frow = (quarter & 1) * 32 + lane;   // feature row 0..63 of the tile
     const int I = p.N >> 1;
     float* xchg = reinterpret_cast<float*>(lslot);   // [2][64][kXchgStride]
     int acc = 0, chunk = 0;
@@ -306,7 +305,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tm = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
       const uint32_t td = tmem_base + lane_base + static_cast<uint32_t>(2 * BN + acc * BN);
-      const int f = nt * 64 + frow;
 #pragma unroll 1
       for (int c = 0; c < nvalid; c += 16, ++chunk) {   // warp-uniform bound
         uint32_t gv[16], dv[16];
@@ -319,22 +317,24 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
           z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
           if (lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
         }
-        // gate warps finish tokens 0-7 of the chunk and up warps tokens 8-15: each side
-        // parks the half the other side needs
-        // row layout: [0, 8) gate values of tokens 8-15 (from the gate warp), [8, 16) up
-        // values of tokens 0-7 (from the up warp)
-        float* buf = xchg + (chunk & 1) * 64 * kXchgStride + frow * kXchgStride;
+        // every lane parks its 16 values (feature row = TMEM lane); then thread t computes
+        // token t / 8 of the chunk for features 8 * (t % 8) .. + 8
+        float* buf = xchg + (chunk & 1) * 128 * kXchgStride;
+        float* mine = buf + (quarter * 32 + lane) * kXchgStride;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) buf[(gate_warp ? 0 : 8) + j] = gate_warp ? z[8 + j] : z[j];
-        epi_bar();   // this chunk's hand-off is in; the other buffer is free again
-        const int j0 = gate_warp ? 0 : 8;
-        __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c + j0) * I + f;
+        for (int j = 0; j < 16; ++j) mine[j] = z[j];
+        epi_bar();   // this chunk's values are in; the other buffer is free again
+        const int et = (quarter * 32 + lane);   // 0..127, any fixed numbering of the 128 threads
+        const int tok = et >> 3, f8 = (et & 7) * 8;
+        if (c + tok < nvalid) {
+          float out8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float zo = buf[(gate_warp ? 8 : 0) + j];   // the other side's value
-          const float zg = gate_warp ? z[j] : zo;        // gate of token j0 + j
-          const float zu = gate_warp ? zo : z[8 + j];    // up of token j0 + j
-          if (c + j0 + j < nvalid) o[static_cast<size_t>(j) * I] = f2bf(zg / (1.0f + __expf(-zg)) * zu);
+          for (int i = 0; i < 8; ++i) {
+            const float zg = buf[(f8 + i) * kXchgStride + tok];        // gate rows 0..63
+            const float zu = buf[(64 + f8 + i) * kXchgStride + tok];   // up rows 64..127
+            out8[i] = __fdividef(zg, 1.0f + __expf(-zg)) * zu;
+          }
+          *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(q0 + c + tok) * I + nt * 64 + f8) = pack8(out8);
         }
       }
       tc_fence_before();

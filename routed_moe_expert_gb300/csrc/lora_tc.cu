@@ -21,7 +21,7 @@
 namespace mlk {
 
 constexpr int kShrinkThreads = 192;
-constexpr int kShrinkMaxStages = 6;
+constexpr int kShrinkMaxStages = 12;
 
 
 static int shrink_stages(int nb) {   // as many 16 KB + N*128 B stages as fit in ~200 KB
