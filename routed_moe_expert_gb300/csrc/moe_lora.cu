@@ -378,10 +378,12 @@ namespace {
 
 // The LoRA placement the pages draw (sglang PR #28466 section 1 flow (B)): the gate_up LoRA
 // chain -- shrink and expand into the bf16 delta d -- on the side stream beside the permute
-// and gate_up GEMM, joined before the activation; the down shrink after it; the down expand
-// in the down GEMM (extra K-stages) or its epilogue.  Used when the fully fused path is not
-// (ranks not a multiple of 8, more than 8 slots, or MOE_LORA_FLAG_UNFUSED_LORA).
-moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_args* a, uint8_t* ws, const Layout& L,
+// and gate_up GEMM, joined before the activation kernel; the down shrink after it; the down
+// expand in the down GEMM (extra K-stages) or its epilogue.  Used when the fully fused path
+// is not (16-token tiles, ranks not a multiple of 8, more than 8 slots, or
+// MOE_LORA_FLAG_UNFUSED_LORA), and without LoRA at 16-token tiles.
+moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_args* a, bool lora, uint8_t* ws,
+                                          const Layout& L,
                                           int32_t* perm, int32_t* offsets, int32_t* ids, __nv_bfloat16* xp,
                                           __nv_bfloat16* g, __nv_bfloat16* d, __nv_bfloat16* act, float* v, float* y,
                                           int32_t* pair_slot, __nv_bfloat16* ub, const LoraSlots& slots,
@@ -389,10 +391,9 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   (void)ws;
   (void)L;
   (void)ids;
-  const bool lora = true;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const int P = T * k;
-  const int R = a->R;
+  const int R = lora ? a->R : 0;
   const int RU = (R + 7) & ~7;
   moe_lora_status st = MOE_LORA_OK;
   // The down-LoRA expand runs inside the down GEMM as extra K-stages when the rank stride is
@@ -610,10 +611,15 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   // Fully fused LoRA: both shrinks on the tensor cores, both expands inside the GEMMs, the
   // activation in the gate_up GEMM's epilogue.  Needs a TMA-able rank stride, few slots and
   // the stacked ranks within one MMA N.
-  const bool fuse_all = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && a->S * R <= 256 &&
+  // At 16-token tiles (decode) the separate activation kernel and the side-stream LoRA chain
+  // cost less than the fused epilogue and the serial shrinks, so the fused paths start at
+  // 32-token tiles.
+  const int bn0 = pick_bn(P, E);
+  const bool fuse_all = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && a->S * R <= 256 && bn0 >= 32 &&
                         !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
-  if (!lora || fuse_all) {
-    int bn = pick_bn(P, E);
+  const bool act_in_gemm = fuse_all || (!lora && bn0 >= 32);
+  if (act_in_gemm) {
+    int bn = bn0;
     if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the LoRA delta accumulators
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
     ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream),
@@ -660,8 +666,8 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
   } else {
-    st = enqueue_unfused_lora_path(h, a, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub, slots,
-                                   status, stream);
+    st = enqueue_unfused_lora_path(h, a, lora, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub,
+                                   slots, status, stream);
     if (st != MOE_LORA_OK) return st;
   }
 
