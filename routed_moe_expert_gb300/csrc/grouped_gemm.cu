@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     qt = local - nt * nq;
   };
 
-  if (warp == 0) {   // ------------------------------------------------ TMA producer (lane 0)
+  if (warp == 0) {   // ------------------------------------------------ TMA producer
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
     int stage = 0;
@@ -185,11 +185,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       }
       return true;
     };
-    int it_tile = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it_tile) {
-      int e, nt, qt;
-      decode(tile, e, nt, qt);
-      int wr0, wr1;
+    auto weight_rows = [&](int e, int nt, int& wr0, int& wr1) {
       if (p.gated) {
         wr0 = e * p.N + nt * 64;
         wr1 = wr0 + (p.N >> 1);
@@ -197,32 +193,48 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
         wr0 = e * p.N + nt * 128;
         wr1 = wr0 + 64;
       }
-      const int xr = seg[e] + qt * BN;
-      // the tile's pair slots are loaded now and reduced after all but the last main stage
-      // are issued, so their latency hides behind the tile's own copies
-      const int nv = min(BN, seg[e + 1] - xr);
-      unsigned lmask = 0;
-      if (p.lora_fused) {
+    };
+    if (!p.lora_fused) {   // lane 0 alone: no per-tile warp traffic
+      if (lane == 0) {
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+          int e, nt, qt, wr0, wr1;
+          decode(tile, e, nt, qt);
+          weight_rows(e, nt, wr0, wr1);
+          const int xr = seg[e] + qt * BN;
+          for (int kb = 0; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+        }
+      }
+    } else {   // the whole warp: lanes gather each tile's pair slots for lane 0
+      int it_tile = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it_tile) {
+        int e, nt, qt, wr0, wr1;
+        decode(tile, e, nt, qt);
+        weight_rows(e, nt, wr0, wr1);
+        const int xr = seg[e] + qt * BN;
+        // the tile's pair slots are loaded now and reduced after all but the last main stage
+        // are issued, so their latency hides behind the tile's own copies
+        const int nv = min(BN, seg[e + 1] - xr);
+        unsigned lmask = 0;
         for (int j = lane; j < nv; j += 32) {
           const int sl = p.pair_slot[xr + j];
           if (sl >= 0 && sl < kMaxFusedSlots) lmask |= 1u << sl;
         }
-      }
-      if (lane == 0)
-        for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
-      const unsigned smask = p.lora_fused ? __reduce_or_sync(0xffffffffu, lmask) : 0u;
-      if (lane == 0) {
-        // published before the tile's last main stage arrives (arrive.expect_tx releases it);
-        // the MMA warp reads it after consuming that stage
-        tile_slot_ring[it_tile % kTileRing] = smask;
-        if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xr);
-        for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
-          if (!((smask >> sl) & 1u)) continue;
-          for (int kb = 0; ok && kb < p.lora_kb; ++kb)
-            ok = issue(&p.tmap_lb[sl], wr0, wr1, kb * 64, &p.tmap_lu, sl * p.P + xr);
+        if (lane == 0)
+          for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+        const unsigned smask = __reduce_or_sync(0xffffffffu, lmask);
+        if (lane == 0) {
+          // published before the tile's last main stage arrives (arrive.expect_tx releases it);
+          // the MMA warp reads it after consuming that stage
+          tile_slot_ring[it_tile % kTileRing] = smask;
+          if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xr);
+          for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
+            if (!((smask >> sl) & 1u)) continue;
+            for (int kb = 0; ok && kb < p.lora_kb; ++kb)
+              ok = issue(&p.tmap_lb[sl], wr0, wr1, kb * 64, &p.tmap_lu, sl * p.P + xr);
+          }
         }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
     if (lane == 0 && !ok) {   // drain: let every issued copy land before the CTA exits
       for (int s2 = 0; s2 < S; ++s2)
@@ -250,16 +262,16 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
       }
       return true;
     };
-    int it_tile = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it_tile) {
-      if (lane == 0) {
-        ok = mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma);
-        if (ok) {
-          tc_fence_after();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
+    if (lane == 0) {
+      int it_tile = 0;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it_tile) {
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
+        if (p.lora_fused) {
           // the tile's first stage has landed, so its slot mask is published
-          const unsigned smask = p.lora_fused ? tile_slot_ring[it_tile % kTileRing] : 0u;
+          const unsigned smask = tile_slot_ring[it_tile % kTileRing];
           const uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(2 * BN + acc * BN) : d;
           bool first_delta = delta_acc;   // the delta accumulator starts fresh each tile
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
@@ -269,16 +281,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
               first_delta = false;
             }
           }
-          if (ok) {
-            umma_commit(&tfull[acc]);
-            if (++acc == 2) {
-              acc = 0;
-              aphase ^= 1u;
-            }
-          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
   } else if (p.gated == 2) {   // ----------------------------- epilogue, fused activation
     const int quarter = warp & 3;
