@@ -65,6 +65,7 @@ typedef enum {
 #define MOE_LORA_FLAG_FORCE_SINGLE_STREAM 2u /* never fork the LoRA chain to the side stream */
 #define MOE_LORA_FLAG_FORCE_TWO_STREAM    4u /* fork even above 256 tokens */
 #define MOE_LORA_FLAG_UNFUSED_LORA        8u /* down-LoRA expand in the epilogue (see forward) */
+#define MOE_LORA_FLAG_NO_PDL             16u /* launch every kernel fully behind its predecessor */
 
 /* Stages that moe_lora_args.prof_events can bracket (two events per stage). */
 enum {

@@ -35,6 +35,33 @@ MLDEV uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with launch_k(..., pdl = true) may
+// start while the previous kernel of its stream is still running.  Every kernel calls
+// pdl_wait() before it touches that kernel's output (a no-op without the launch
+// attribute), and pdl_trigger() only after its own pdl_wait(): so when a kernel starts,
+// every kernel two or more places earlier in the stream has completed, and its output
+// (the expert offsets, for instance) may be read at once.
+// ---------------------------------------------------------------------------------
+MLDEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MLDEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 MLDEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

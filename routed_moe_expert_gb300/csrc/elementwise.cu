@@ -11,6 +11,8 @@ namespace mlk {
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                                                       int P, int k, int H8, uint4* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
   const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (q >= P) return;
   const int t = perm[q] / k;
@@ -20,11 +22,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
 }
 
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
-                           __nv_bfloat16* xp, cudaStream_t stream) {
+                           __nv_bfloat16* xp, cudaStream_t stream, bool pdl) {
   if (P == 0) return cudaSuccess;
-  permute_kernel<<<(P + 7) / 8, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, P, k, H / 8,
-                                                  reinterpret_cast<uint4*>(xp));
-  return cudaGetLastError();
+  return launch_k(permute_kernel, dim3((P + 7) / 8), dim3(256), 0, stream, pdl, reinterpret_cast<const uint4*>(x),
+                  perm, P, k, H / 8, reinterpret_cast<uint4*>(xp));
 }
 
 // ---------------------------------------------------------------------------------
@@ -38,6 +39,8 @@ cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, i
 __global__ void __launch_bounds__(256) activation_kernel(const __nv_bfloat16* __restrict__ g,
                                                          const __nv_bfloat16* __restrict__ d, int P, int I,
                                                          __nv_bfloat16* __restrict__ a) {
+  pdl_wait();
+  pdl_trigger();
   const int I8 = I >> 3;
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<size_t>(P) * I8) return;
@@ -65,11 +68,11 @@ __global__ void __launch_bounds__(256) activation_kernel(const __nv_bfloat16* __
 }
 
 cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
-                              __nv_bfloat16* a, cudaStream_t stream) {
+                              __nv_bfloat16* a, cudaStream_t stream, bool pdl) {
   const size_t n = static_cast<size_t>(P) * (I / 8);
   if (n == 0) return cudaSuccess;
-  activation_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(g, d, P, I, a);
-  return cudaGetLastError();
+  return launch_k(activation_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream, pdl, g, d,
+                  P, I, a);
 }
 
 // ---------------------------------------------------------------------------------
@@ -84,6 +87,8 @@ constexpr int kFinThreads = 128;   // 4 floats each: 512 h per CTA
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams p) {
   __shared__ int q_s[kMaxTopK];
   __shared__ float w_s[kMaxTopK];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x, k = p.k, tid = threadIdx.x;
   if (tid < k) {
     const size_t pp = static_cast<size_t>(t) * k + tid;
@@ -111,11 +116,11 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
   reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[h4] = v;
 }
 
-cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream) {
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   if (p.T == 0) return cudaSuccess;
   const int H4 = p.H / 4;
-  finalize_kernel<<<dim3(p.T, (H4 + kFinThreads - 1) / kFinThreads), kFinThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_k(finalize_kernel, dim3(p.T, (H4 + kFinThreads - 1) / kFinThreads), dim3(kFinThreads), 0, stream,
+                  pdl, p);
 }
 
 }  // namespace mlk

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     qt = local - nt * nq;
   };
 
+  if (warp >= 2) pdl_wait();   // the epilogues read the previous kernel's LoRA rows and slots
   if (warp == 0) {   // ------------------------------------------------ TMA producer
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
@@ -170,12 +171,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     uint32_t issued_mask = 0;       // stages with a load in flight, and their parity
     uint32_t issued_parity = 0;
     int ok = 1;
+    int npre = 0, nissued = 0;   // stages whose weight half went out before pdl_wait
     auto issue = [&](const CUtensorMap* wmap, int wr0, int wr1, int kx, const CUtensorMap* xmap, int xrow) -> bool {
       if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) return false;
       uint8_t* a = smem + stage * STAGE;
-      mbar_arrive_expect_tx(&full[stage], STAGE);
-      tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
-      tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
+      if (nissued++ >= npre) {
+        mbar_arrive_expect_tx(&full[stage], STAGE);
+        tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
+        tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
+      }
       tma_load_2d(a + A_BYTES, xmap, &full[stage], kx, xrow, pol_x);
       issued_mask |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -194,6 +198,23 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
         wr1 = wr0 + 64;
       }
     };
+    // Weights are constants of the layer and the tile schedule comes from the expert
+    // offsets, so the weight halves of the first tile's first stages go out before the
+    // previous kernel (which writes the token rows) has finished.
+    if (lane == 0 && static_cast<int>(blockIdx.x) < total) {
+      int e, nt, qt, wr0, wr1;
+      decode(blockIdx.x, e, nt, qt);
+      weight_rows(e, nt, wr0, wr1);
+      npre = min(S, KB);
+      for (int s2 = 0; s2 < npre; ++s2) {
+        uint8_t* a = smem + s2 * STAGE;
+        mbar_arrive_expect_tx(&full[s2], STAGE);
+        tma_load_2d(a, &p.tmap_w, &full[s2], s2 * 64, wr0, pol_w);
+        tma_load_2d(a + 8192, &p.tmap_w, &full[s2], s2 * 64, wr1, pol_w);
+        issued_mask |= 1u << s2;   // phase 0
+      }
+    }
+    pdl_wait();
     if (!p.lora_fused) {   // lane 0 alone: no per-tile warp traffic
       if (lane == 0) {
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -236,6 +257,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
     }
+    pdl_trigger();   // all of this CTA's copies are issued: the next kernel may start
     if (lane == 0 && !ok) {   // drain: let every issued copy land before the CTA exits
       for (int s2 = 0; s2 < S; ++s2)
         if ((issued_mask >> s2) & 1u) mbar_wait_drain(&full[s2], (issued_parity >> s2) & 1u);
@@ -466,22 +488,21 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
 }
 
 template <int BN>
-static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<BN><<<grid, kGemmThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_k(grouped_gemm_kernel<BN>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem), stream, pdl, p);
 }
 
-cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl) {
   if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
   switch (bn) {
-    case 16: return launch_bn<16>(p, grid, stream);
-    case 32: return launch_bn<32>(p, grid, stream);
-    case 64: return launch_bn<64>(p, grid, stream);
-    case 128: return launch_bn<128>(p, grid, stream);
-    case 256: return launch_bn<256>(p, grid, stream);
+    case 16: return launch_bn<16>(p, grid, stream, pdl);
+    case 32: return launch_bn<32>(p, grid, stream, pdl);
+    case 64: return launch_bn<64>(p, grid, stream, pdl);
+    case 128: return launch_bn<128>(p, grid, stream, pdl);
+    case 256: return launch_bn<256>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

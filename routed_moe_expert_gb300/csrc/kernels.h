@@ -84,13 +84,13 @@ struct GemmParams {
 };
 int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused);
 int gemm_stage_bytes(int bn);
-cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 
 // ---------------------------------------------------------------- elementwise
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
-                           __nv_bfloat16* xp, cudaStream_t stream);
+                           __nv_bfloat16* xp, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
-                              __nv_bfloat16* a, cudaStream_t stream);
+                              __nv_bfloat16* a, cudaStream_t stream, bool pdl = false);
 
 
 struct FinalizeParams {
@@ -100,7 +100,7 @@ struct FinalizeParams {
   int T, H, k;
   __nv_bfloat16* out;            // [T, H]
 };
-cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream);
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl = false);
 
 // ---------------------------------------------------------------- LoRA
 // Tensor-core LoRA over expert tiles of 8*ntl pairs: shrink u = A . src (fp32) and, when
@@ -144,7 +144,7 @@ struct ShrinkTcParams {
   uint32_t* status;
 };
 int lora_shrink_tc_nb(int S, int R);
-cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream);
+cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl = false);
+cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl = false);
 
 }  // namespace mlk

@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
   constexpr int PT = 8 * NTL;
   constexpr int UK = MTX <= 2 ? 4 : (MTX <= 4 ? 2 : 1);
   extern __shared__ __align__(16) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
   const int R = p.slots.R;
   const int RP = ((R + 15) / 16) * 16;
   const bool expand = p.B != nullptr;
@@ -324,27 +326,26 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
 }
 
 template <int NTL, int MTX>
-static cudaError_t launch_t(const LoraParams& p, int grid, size_t smem, cudaStream_t stream) {
+static cudaError_t launch_t(const LoraParams& p, int grid, size_t smem, cudaStream_t stream, bool pdl) {
   cudaError_t err = cudaFuncSetAttribute(lora_mma_kernel<NTL, MTX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  lora_mma_kernel<NTL, MTX><<<grid, kLoraThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_k(lora_mma_kernel<NTL, MTX>, dim3(grid), dim3(kLoraThreads), smem, stream, pdl, p);
 }
 
 template <int NTL>
-static cudaError_t launch_ntl(const LoraParams& p, int grid, size_t smem, cudaStream_t stream) {
+static cudaError_t launch_ntl(const LoraParams& p, int grid, size_t smem, cudaStream_t stream, bool pdl) {
   const int R = p.slots.R;
-  if (R <= 16) return launch_t<NTL, 1>(p, grid, smem, stream);
-  if (R <= 32) return launch_t<NTL, 2>(p, grid, smem, stream);
-  if (R <= 64) return launch_t<NTL, 4>(p, grid, smem, stream);
-  return launch_t<NTL, 8>(p, grid, smem, stream);
+  if (R <= 16) return launch_t<NTL, 1>(p, grid, smem, stream, pdl);
+  if (R <= 32) return launch_t<NTL, 2>(p, grid, smem, stream, pdl);
+  if (R <= 64) return launch_t<NTL, 4>(p, grid, smem, stream, pdl);
+  return launch_t<NTL, 8>(p, grid, smem, stream, pdl);
 }
 
-cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream) {
+cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl) {
   if (p.P == 0) return cudaSuccess;
   const size_t smem = lora_smem_bytes(ntl, p.slots.R, p.N, p.B != nullptr, p.E);
-  return ntl == 1 ? launch_ntl<1>(p, grid, smem, stream) : launch_ntl<4>(p, grid, smem, stream);
+  return ntl == 1 ? launch_ntl<1>(p, grid, smem, stream, pdl) : launch_ntl<4>(p, grid, smem, stream, pdl);
 }
 
 }  // namespace mlk

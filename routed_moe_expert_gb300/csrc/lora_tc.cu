@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();   // the rows to shrink come from the previous kernel (expert offsets from earlier)
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_start[E];
   auto decode = [&](int tile, int& e, int& qt) {
@@ -261,15 +263,14 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
 }
 
 template <int NB>
-static cudaError_t launch_nb(const ShrinkTcParams& p_in, int grid, cudaStream_t stream) {
+static cudaError_t launch_nb(const ShrinkTcParams& p_in, int grid, cudaStream_t stream, bool pdl) {
   ShrinkTcParams p = p_in;
   p.stages = shrink_stages(NB);
   const int smem = lora_shrink_tc_smem(NB, p.E);
   cudaError_t err =
       cudaFuncSetAttribute(lora_shrink_tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  lora_shrink_tc_kernel<NB><<<grid, kShrinkThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_k(lora_shrink_tc_kernel<NB>, dim3(grid), dim3(kShrinkThreads), smem, stream, pdl, p);
 }
 
 int lora_shrink_tc_nb(int S, int R) {
@@ -277,14 +278,14 @@ int lora_shrink_tc_nb(int S, int R) {
   return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 0;
 }
 
-cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl) {
   if (p.P == 0) return cudaSuccess;
   switch (lora_shrink_tc_nb(p.S, p.R)) {
-    case 16: return launch_nb<16>(p, grid, stream);
-    case 32: return launch_nb<32>(p, grid, stream);
-    case 64: return launch_nb<64>(p, grid, stream);
-    case 128: return launch_nb<128>(p, grid, stream);
-    case 256: return launch_nb<256>(p, grid, stream);
+    case 16: return launch_nb<16>(p, grid, stream, pdl);
+    case 32: return launch_nb<32>(p, grid, stream, pdl);
+    case 64: return launch_nb<64>(p, grid, stream, pdl);
+    case 128: return launch_nb<128>(p, grid, stream, pdl);
+    case 256: return launch_nb<256>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -284,12 +284,14 @@ int pick_stages(int bn, int E, int lora_R, int act_fused) {
   return s;
 }
 
+// pdl: programmatic launch behind the previous kernel of the stream, which must not be the
+// one that wrote the expert offsets (the GEMM reads them before it waits).
 moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, const void* X, int P, int bn,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool pdl) {
   if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
   gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2);
-  ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream), "grouped_gemm launch");
+  ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
 
@@ -325,7 +327,8 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
 // stacked LoRA A [S*E*R, K]; writes ub and pair_slot.
 moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, const void* X, const moe_lora_bf16* A,
                                   int K, const int32_t* offsets, const int32_t* perm, const LoraSlots& slots,
-                                  __nv_bfloat16* ub, int32_t* pair_slot, uint32_t* status, cudaStream_t stream) {
+                                  __nv_bfloat16* ub, int32_t* pair_slot, uint32_t* status, cudaStream_t stream,
+                                  bool pdl) {
   const int P = a->T * a->top_k;
   ShrinkTcParams sp;
   std::memset(&sp, 0, sizeof(sp));
@@ -349,7 +352,7 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   sp.status = status;
   int grid = (P + sp.tb - 1) / sp.tb + a->E;
   if (grid > h->num_sms) grid = h->num_sms;
-  ML_CUDA(launch_lora_shrink_tc(sp, grid, stream), "lora shrink (tensor cores) launch");
+  ML_CUDA(launch_lora_shrink_tc(sp, grid, stream, pdl), "lora shrink (tensor cores) launch");
   return MOE_LORA_OK;
 }
 
@@ -395,6 +398,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   const int P = T * k;
   const int R = lora ? a->R : 0;
   const int RU = (R + 7) & ~7;
+  const bool pdl = !(a->flags & MOE_LORA_FLAG_NO_PDL);
   moe_lora_status st = MOE_LORA_OK;
   // The down-LoRA expand runs inside the down GEMM as extra K-stages when the rank stride is
   // TMA-able and the slots are few.  The gate_up expand stays a separate kernel writing the
@@ -443,13 +447,13 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
       lp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
       lp.d_out = d;
     }
-    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, ls), "lora gate_up launch");
+    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, ls, pdl && !two), "lora gate_up launch");
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, ls);
     if (two) ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
   }
 
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
-  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream),
+  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
           "permute launch");
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
@@ -465,13 +469,15 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   gu.K = H;
   gu.gated = 1;
   if (fused_gu && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
-  st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream);
+  st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl && !(fused_gu && two));
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
   if (!fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
-  ML_CUDA(launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream), "activation launch");
+  // (no programmatic launch right behind a wait on the side stream)
+  ML_CUDA(launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream, pdl && !two),
+          "activation launch");
   prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
 
   if (lora) {   // down-LoRA shrink on the activation; its expand runs inside the down GEMM
@@ -499,7 +505,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     lp.pair_slot_out = pair_slot;
     lp.status = status;
     lp.where = kWhereLoraShrinkDn;
-    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, stream), "lora down shrink launch");
+    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, stream, pdl), "lora down shrink launch");
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
   }
 
@@ -521,7 +527,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     dn.pair_slot = pair_slot;
     dn.slots = slots;
   }
-  st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream);
+  st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream, pdl);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
 
@@ -575,6 +581,8 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   cudaStream_t stream = stream_;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const bool lora = lora_active(a);
+  // programmatic launches: each kernel after the routing starts behind its predecessor
+  const bool pdl = !(a->flags & MOE_LORA_FLAG_NO_PDL);
   const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0, a->S > 0 ? a->S : 0);
   if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -622,12 +630,12 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     int bn = bn0;
     if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the LoRA delta accumulators
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
-    ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream),
+    ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
             "permute launch");
     prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     if (fuse_all) {
       prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
-      st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream);
+      st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl);
       if (st != MOE_LORA_OK) return st;
       prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
     }
@@ -642,12 +650,12 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     gu.K = H;
     gu.gated = 2;
     if (fuse_all && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
-    st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream);
+    st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
     if (fuse_all) {
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
-      st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream);
+      st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl);
       if (st != MOE_LORA_OK) return st;
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
     }
@@ -662,7 +670,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     dn.K = I;
     dn.gated = 0;
     if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
-    st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream);
+    st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
   } else {
@@ -680,7 +688,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   fp.H = H;
   fp.k = k;
   fp.out = reinterpret_cast<__nv_bfloat16*>(out);
-  ML_CUDA(launch_finalize(fp, stream), "finalize launch");
+  ML_CUDA(launch_finalize(fp, stream, pdl), "finalize launch");
   prof(a, MOE_LORA_STAGE_FINALIZE, 1, stream);
   return MOE_LORA_OK;
 }

@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   }
   __syncthreads();
 
+  pdl_trigger();   // the permute may launch now; it waits for this kernel to finish
+
   // ---------------- phase 2: expert offsets and per-CTA bases
   if (G > 1) {
     for (int e = tid; e < E; e += kRouteThreads) p.hist[c * E + e] = hist_s[e];
