@@ -62,6 +62,28 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Expert tile schedule from offsets staged in shared memory (seg[e] = first permuted pair
+// of expert e, seg[E] = P): tile_start[e] = sum over e' < e of ceil(M_e' / tile) * mult,
+// tile_start[E] = the total.  Run by one warp.  Callers stage seg with one round of loads
+// by every thread first, so the offsets cost one memory latency, not one per 32 experts.
+MLDEV void scan_tile_schedule(const int* seg, int E, int tile, int mult, int* tile_start) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  for (int b = 0; b < E; b += 32) {
+    const int e = b + lane;
+    const int cnt = (e < E) ? ((seg[e + 1] - seg[e] + tile - 1) / tile) * mult : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (e < E) tile_start[e] = carry + incl - cnt;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) tile_start[E] = carry;
+}
+
 MLDEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

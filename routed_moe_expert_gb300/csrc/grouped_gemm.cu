@@ -121,28 +121,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) {   // tile schedule: tile_start[e] = sum over e' < e of ceil(M_e'/BN) * NT
-    int carry = 0;
-    for (int b = 0; b < E; b += 32) {
-      const int e = b + lane;
-      int cnt = 0;
-      if (e < E) {
-        const int lo = p.offsets[e], hi = p.offsets[e + 1];
-        seg[e] = lo;
-        if (e == E - 1) seg[E] = hi;
-        cnt = ((hi - lo + BN - 1) / BN) * NT;
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      if (e < E) tile_start[e] = carry + incl - cnt;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) tile_start[E] = carry;
-  }
+  for (int i = threadIdx.x; i <= E; i += kGemmThreads) seg[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 2) scan_tile_schedule(seg, E, BN, NT, tile_start);   // ceil(M_e/BN) * NT tiles each
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

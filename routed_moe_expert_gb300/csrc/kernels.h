@@ -47,6 +47,10 @@ struct RouteParams {
   uint32_t* status;
 };
 cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stream);
+// Routing as one thread-block cluster of route_cluster_ctas(T) CTAs (no global scratch,
+// no grid barrier); 0 when T is too large and the cooperative grid is used instead.
+int route_cluster_ctas(int T);
+cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream);
 int route_max_coop_ctas(int E);
 
 // ---------------------------------------------------------------- grouped GEMM
@@ -88,7 +92,8 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStrea
 
 // ---------------------------------------------------------------- elementwise
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
-                           __nv_bfloat16* xp, cudaStream_t stream, bool pdl = false);
+                           __nv_bfloat16* xp, cudaStream_t stream, bool pdl = false,
+                           const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr);
 cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
                               __nv_bfloat16* a, cudaStream_t stream, bool pdl = false);
 
@@ -146,5 +151,23 @@ struct ShrinkTcParams {
 int lora_shrink_tc_nb(int S, int R);
 cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl = false);
+
+// Activation (gate_up output g plus the bf16 gate_up LoRA delta d, SwiGLU, bf16 out)
+// fused with the down-LoRA shrink v = scaling * a . A_dn^T, over expert tiles of up to 8
+// pairs.  Writes a [P, I] and v [P, R] (fp32, pairs with an adapter); pair_slot holds each
+// pair's slot as the permute gathered it and is rewritten checked (-1 for no adapter).
+struct ActShrinkParams {
+  const __nv_bfloat16* g;        // [P, 2I] gated-interleaved gate_up output
+  const __nv_bfloat16* d;        // [P, 2I] gate_up LoRA delta, logical [gate | up]
+  const int32_t* offsets;        // [E+1]
+  const __nv_bfloat16* A;        // down LoRA A [S, E, R, I]
+  LoraSlots slots;
+  int P, I, E;
+  __nv_bfloat16* a;              // [P, I]
+  float* v;                      // [P, R]
+  int32_t* pair_slot;            // [P] in: slot_idx of the pair's token; out: checked slot
+  uint32_t* status;
+};
+cudaError_t launch_act_shrink(const ActShrinkParams& p, int grid, cudaStream_t stream, bool pdl = false);
 
 }  // namespace mlk

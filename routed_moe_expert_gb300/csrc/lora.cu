@@ -54,7 +54,7 @@ size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E) {
   b += static_cast<size_t>(PT) * (RP + 8) * 2;            // u as bf16 (padded rows)
   if (expand) b += static_cast<size_t>(PT) * N * 2;       // staged d rows
   b += static_cast<size_t>(PT) * 12 + 16;                 // pair info + slot mask
-  b += 4 * (static_cast<size_t>(E) + 1);                  // schedule
+  b += 8 * (static_cast<size_t>(E) + 1);                  // schedule and staged offsets
   return b;
 }
 
@@ -79,27 +79,15 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
   int* pq = pslot + PT;                                                         // [PT]
   unsigned* smask = reinterpret_cast<unsigned*>(pq + PT);                       // [2]: slots 0-31, 32-63
   int* tile_start = reinterpret_cast<int*>(smask + 4);                          // [E+1]
+  int* seg = tile_start + (p.E + 1);                                            // [E+1] offsets
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int E = p.E;
 
-  if (warp == 0) {   // tile schedule over experts: ceil(M_e / PT) tiles each
-    int carry = 0;
-    for (int b = 0; b < E; b += 32) {
-      const int e = b + lane;
-      const int cnt = (e < E) ? (p.offsets[e + 1] - p.offsets[e] + PT - 1) / PT : 0;
-      int incl = cnt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      if (e < E) tile_start[e] = carry + incl - cnt;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) tile_start[E] = carry;
-  }
+  for (int i = tid; i <= E; i += kLoraThreads) seg[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 0) scan_tile_schedule(seg, E, PT, 1, tile_start);   // ceil(M_e / PT) tiles each
   __syncthreads();
   const int total = tile_start[E];
   const int K16 = p.K >> 4;
@@ -111,8 +99,8 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
     }
     const int e = lo;
-    const int q0 = p.offsets[e] + (tile - tile_start[e]) * PT;
-    const int np = min(PT, p.offsets[e + 1] - q0);
+    const int q0 = seg[e] + (tile - tile_start[e]) * PT;
+    const int np = min(PT, seg[e + 1] - q0);
 
     if (tid == 0) smask[0] = smask[1] = 0u;
     __syncthreads();
@@ -346,6 +334,168 @@ cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t str
   if (p.P == 0) return cudaSuccess;
   const size_t smem = lora_smem_bytes(ntl, p.slots.R, p.N, p.B != nullptr, p.E);
   return ntl == 1 ? launch_ntl<1>(p, grid, smem, stream, pdl) : launch_ntl<4>(p, grid, smem, stream, pdl);
+}
+
+// ---------------------------------------------------------------------------------
+// Activation with the down-LoRA shrink in the same pass (narrow expert tiles): for a tile
+// of up to 8 pairs of one expert,
+//   a[q, i] = bf16( silu(g_gate + d_gate) * (g_up + d_up) )      (as activation_kernel)
+//   v[q, r] = scaling[s] * sum_i a[q, i] * A_dn[s, e, r, i]       (fp32, r < ranks[s])
+// with the bf16 activation rows kept in shared memory for the shrink.  The shrink runs on
+// the tensor cores (mma.sync m16n8k16: M = rank rows of the slot's A block, N = the 8
+// pairs, K = I split over the 8 warps), one slot present in the tile at a time; the warps'
+// partial sums are added in warp order.  Rank rows past the slot's rank are never loaded
+// and their results never stored.  The down GEMM's epilogue applies the expand from v.
+// Pairs without an adapter get pair_slot -1 and no v.
+// ---------------------------------------------------------------------------------
+constexpr int kActTile = 8;
+
+template <int MTX>
+__global__ void __launch_bounds__(kLoraThreads) act_shrink_kernel(const ActShrinkParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
+  const int E = p.E, I = p.I, I8 = p.I >> 3, R = p.slots.R;
+  const int AS = I + 8;   // activation row stride in shared memory (bank-conflict padding)
+  __nv_bfloat16* a_s = reinterpret_cast<__nv_bfloat16*>(smem);                 // [8][AS]
+  float* red = reinterpret_cast<float*>(a_s + kActTile * AS);                   // [8 warps][16*MTX][8]
+  int* pslot = reinterpret_cast<int*>(red + kLoraWarps * 16 * MTX * kActTile); // [8]
+  unsigned* smask = reinterpret_cast<unsigned*>(pslot + kActTile);              // [2]
+  int* tile_start = reinterpret_cast<int*>(smask + 2);                          // [E+1]
+  int* seg = tile_start + (E + 1);                                              // [E+1] offsets
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+
+  for (int i = tid; i <= E; i += kLoraThreads) seg[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 0) scan_tile_schedule(seg, E, kActTile, 1, tile_start);   // ceil(M_e / 8) tiles each
+  __syncthreads();
+  const int total = tile_start[E];
+
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int q0 = seg[e] + (tile - tile_start[e]) * kActTile;
+    const int np = min(kActTile, seg[e + 1] - q0);
+    if (tid == 0) smask[0] = smask[1] = 0u;
+    __syncthreads();
+    if (tid < np) {
+      const int q = q0 + tid;
+      int s = p.pair_slot[q];
+      if (s < -1 || s >= p.slots.S) {
+        record_status(p.status, kDevBadSlot, kWhereLoraShrinkDn);
+        s = -1;
+      } else if (s >= 0 && (p.slots.ranks[s] <= 0 || p.slots.scal[s] == 0.0f)) {
+        s = -1;
+      }
+      pslot[tid] = s;
+      p.pair_slot[q] = s;
+      if (s >= 0) atomicOr(&smask[s >> 5], 1u << (s & 31));
+    }
+    // activation rows of the tile -> global and shared memory
+    for (int i = tid; i < np * I8; i += kLoraThreads) {
+      const int n = i / I8, i0 = (i - n * I8) * 8;
+      const int blk = i0 >> 6, j = i0 & 63;
+      const size_t row = static_cast<size_t>(q0 + n) * 2 * I;
+      float gf[8], uf[8], dg[8], du[8];
+      unpack8(*reinterpret_cast<const uint4*>(p.g + row + blk * 128 + j), gf);
+      unpack8(*reinterpret_cast<const uint4*>(p.g + row + blk * 128 + 64 + j), uf);
+      unpack8(*reinterpret_cast<const uint4*>(p.d + row + i0), dg);
+      unpack8(*reinterpret_cast<const uint4*>(p.d + row + I + i0), du);
+      float out[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float zg = gf[m] + dg[m], zu = uf[m] + du[m];
+        out[m] = __fdividef(zg, 1.0f + __expf(-zg)) * zu;
+      }
+      const uint4 v = pack8(out);
+      *reinterpret_cast<uint4*>(p.a + static_cast<size_t>(q0 + n) * I + i0) = v;
+      *reinterpret_cast<uint4*>(a_s + n * AS + i0) = v;
+    }
+    __syncthreads();
+    const unsigned m0 = smask[0], m1 = smask[1];
+    for (int s = 0; s < p.slots.S; ++s) {
+      if (!(((s < 32 ? m0 : m1) >> (s & 31)) & 1u)) continue;
+      const int rank = p.slots.ranks[s];
+      const int MT = (rank + 15) >> 4;
+      const __nv_bfloat16* A = p.A + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(R) * I;
+      float acc[MTX][4];
+#pragma unroll
+      for (int mt = 0; mt < MTX; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
+      for (int ks = warp; ks < (I >> 4); ks += kLoraWarps) {
+        const int k0 = ks * 16 + 2 * c;
+        uint32_t bf[2];
+        bf[0] = *reinterpret_cast<const uint32_t*>(a_s + g * AS + k0);
+        bf[1] = *reinterpret_cast<const uint32_t*>(a_s + g * AS + k0 + 8);
+        uint32_t af[MTX][4];
+#pragma unroll
+        for (int mt = 0; mt < MTX; ++mt) {
+          const int r0 = mt * 16 + g, r1 = r0 + 8;
+          const bool ok0 = mt < MT && r0 < rank, ok1 = mt < MT && r1 < rank;
+          const __nv_bfloat16* A0 = A + static_cast<size_t>(r0) * I + k0;
+          const __nv_bfloat16* A1 = A + static_cast<size_t>(r1) * I + k0;
+          af[mt][0] = ok0 ? ld_b32(A0) : 0u;
+          af[mt][1] = ok1 ? ld_b32(A1) : 0u;
+          af[mt][2] = ok0 ? ld_b32(A0 + 8) : 0u;
+          af[mt][3] = ok1 ? ld_b32(A1 + 8) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MTX; ++mt)
+          if (mt < MT) mma_bf16_16816(acc[mt], af[mt], bf);
+      }
+      // partials [row][pair] of this warp, then the fixed-order sum over warps
+      float* rw = red + warp * 16 * MTX * kActTile;
+#pragma unroll
+      for (int mt = 0; mt < MTX; ++mt) {
+        if (mt < MT) {
+          rw[(mt * 16 + g) * kActTile + 2 * c] = acc[mt][0];
+          rw[(mt * 16 + g) * kActTile + 2 * c + 1] = acc[mt][1];
+          rw[(mt * 16 + g + 8) * kActTile + 2 * c] = acc[mt][2];
+          rw[(mt * 16 + g + 8) * kActTile + 2 * c + 1] = acc[mt][3];
+        }
+      }
+      __syncthreads();
+      for (int i = tid; i < np * rank; i += kLoraThreads) {
+        const int n = i / rank, r = i - n * rank;
+        if (pslot[n] != s) continue;
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kLoraWarps; ++w) sum += red[(w * 16 * MTX + r) * kActTile + n];
+        p.v[static_cast<size_t>(q0 + n) * R + r] = p.slots.scal[s] * sum;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <int MTX>
+static size_t act_shrink_smem(int I, int E) {
+  return static_cast<size_t>(kActTile) * (I + 8) * 2 + static_cast<size_t>(kLoraWarps) * 16 * MTX * kActTile * 4 +
+         4 * (kActTile + 2 + 2 * (static_cast<size_t>(E) + 1));
+}
+
+template <int MTX>
+static cudaError_t launch_act_mtx(const ActShrinkParams& p, int grid, cudaStream_t stream, bool pdl) {
+  const size_t smem = act_shrink_smem<MTX>(p.I, p.E);
+  cudaError_t err = cudaFuncSetAttribute(act_shrink_kernel<MTX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_k(act_shrink_kernel<MTX>, dim3(grid), dim3(kLoraThreads), smem, stream, pdl, p);
+}
+
+cudaError_t launch_act_shrink(const ActShrinkParams& p, int grid, cudaStream_t stream, bool pdl) {
+  if (p.P == 0) return cudaSuccess;
+  const int R = p.slots.R;
+  if (R <= 16) return launch_act_mtx<1>(p, grid, stream, pdl);
+  if (R <= 32) return launch_act_mtx<2>(p, grid, stream, pdl);
+  if (R <= 64) return launch_act_mtx<4>(p, grid, stream, pdl);
+  return launch_act_mtx<8>(p, grid, stream, pdl);
 }
 
 }  // namespace mlk

@@ -227,7 +227,7 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
                               int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
                               int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream) {
   if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
-  // about 64 tokens per CTA (one CTA, without a grid barrier, up to 64 tokens)
+  // above 512 tokens: a cooperative grid of about 64 tokens per CTA
   int grid = (T + 63) / 64;
   if (grid > h->coop_ctas[E]) grid = h->coop_ctas[E];
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
@@ -251,6 +251,12 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
   p.total = reinterpret_cast<int32_t*>(ws + L.total);
   p.status = reinterpret_cast<uint32_t*>(ws + L.header);
   p.barrier = p.status + 1;
+  const int ctas = route_cluster_ctas(T);   // one thread-block cluster up to 512 tokens
+  if (ctas > 0) {
+    p.tokens_per_cta = (T + ctas - 1) / ctas;
+    ML_CUDA(launch_route_cluster(p, ctas, stream), "route cluster launch");
+    return MOE_LORA_OK;
+  }
   ML_CUDA(launch_route_align(p, grid, stream), "route_align launch");
   return MOE_LORA_OK;
 }
@@ -275,8 +281,10 @@ int pick_bn(long long P, int E) {
   return 256;
 }
 
-int pick_stages(int bn, int E, int lora_R, int act_fused) {
-  const int budget = (bn <= 32 ? 160 : 200) * 1024;
+// Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
+// room for the side-stream LoRA kernel that runs beside it; the down GEMM runs alone.
+int pick_stages(int bn, int E, int lora_R, int act_fused, bool alone) {
+  const int budget = (bn <= 32 && !alone ? 160 : 200) * 1024;
   const int fixed = gemm_smem_bytes(bn, 0, E, lora_R, act_fused);
   int s = (budget - fixed) / (gemm_stage_bytes(bn) + 16);
   if (s > 16) s = 16;
@@ -290,7 +298,7 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
                              cudaStream_t stream, bool pdl) {
   if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
-  gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2);
+  gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0);
   ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
@@ -453,7 +461,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   }
 
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
-  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
+  // the pairs' adapter slots ride along with the permute for the activation + down shrink
+  const bool act_shrink = lora && !fused && !fused_gu;
+  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
+                         a->slot_idx, act_shrink ? pair_slot : nullptr),
           "permute launch");
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
@@ -474,13 +485,37 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
   if (!fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
-  prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
   // (no programmatic launch right behind a wait on the side stream)
-  ML_CUDA(launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream, pdl && !two),
-          "activation launch");
-  prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
+  const bool pdl_act = pdl && !two;
+  if (act_shrink) {
+    // activation and down-LoRA shrink in one pass; the expand runs in the down GEMM's epilogue
+    prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
+    ActShrinkParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.g = g;
+    ap.d = d;
+    ap.offsets = offsets;
+    ap.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
+    ap.slots = slots;
+    ap.P = P;
+    ap.I = I;
+    ap.E = E;
+    ap.a = act;
+    ap.v = v;
+    ap.pair_slot = pair_slot;
+    ap.status = status;
+    int grid = (P + 7) / 8 + E;
+    if (grid > 4 * h->num_sms) grid = 4 * h->num_sms;
+    ML_CUDA(launch_act_shrink(ap, grid, stream, pdl_act), "activation + down shrink launch");
+    prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
+  } else {
+    prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
+    ML_CUDA(launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream, pdl_act),
+            "activation launch");
+    prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
+  }
 
-  if (lora) {   // down-LoRA shrink on the activation; its expand runs inside the down GEMM
+  if (lora && fused) {   // down-LoRA shrink on the activation; its expand runs inside the down GEMM
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
     LoraParams lp;
     std::memset(&lp, 0, sizeof(lp));
@@ -496,12 +531,8 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     lp.N = 0;
     lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
     lp.slots = slots;
-    if (fused) {
-      lp.ub_out = ub;
-      lp.RU = RU;
-    } else {
-      lp.u_out = v;
-    }
+    lp.ub_out = ub;
+    lp.RU = RU;
     lp.pair_slot_out = pair_slot;
     lp.status = status;
     lp.where = kWhereLoraShrinkDn;

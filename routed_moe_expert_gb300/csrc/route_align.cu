@@ -28,6 +28,7 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kInvalidId = 0x7fffffff;
 constexpr int kRouteIdsInSmem = 3072;   // pairs per CTA kept in shared memory for the scatter
 constexpr int kScatterMaxE = 384;       // per-warp expert cursors fit in shared memory up to here
+constexpr int kRouteClusterMax = 8;     // CTAs of the single-cluster routing (portable size)
 
 // sigma(z) = 1 / (1 + exp(-z)) in float32, one IEEE rounding per operation, with exp
 // evaluated by Cody-Waite reduction (W. J. Cody and W. Waite, "Software Manual for the
@@ -131,26 +132,94 @@ MLDEV int block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
   return total;
 }
 
-template <int EPL, int METHOD>
-__global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteParams p) {
-  constexpr int kTPW = EPL <= 4 ? 4 : (EPL <= 8 ? 2 : 1);   // tokens per warp, in lockstep
-  __shared__ int hist_s[kMaxExperts];
-  __shared__ int cursor_s[kMaxExperts];
-  __shared__ int warp_sums[kRouteWarps + 1];
-  __shared__ int ok_s;
-  __shared__ int ids_s[kRouteIdsInSmem];   // this CTA's expert ids, when they fit
-  __shared__ int wcnt[kRouteWarps * kScatterMaxE];   // per-warp expert cursors
+// Renormalize selection key: the 16-bit order key of the bf16 logit (NaN as -inf, -0 as +0)
+// above 0xFFFF - e, so one unsigned maximum picks the largest logit and, among equal
+// logits, the lowest expert id.  Never 0 ("no candidate").
+MLDEV uint32_t packed_logit_key(const __nv_bfloat16* row, int e) {
+  uint32_t u = static_cast<uint32_t>(__bfloat16_as_ushort(row[e]));
+  if ((u & 0x7fffu) > 0x7f80u) u = 0xff80u;   // NaN -> -inf
+  if (u == 0x8000u) u = 0u;                    // -0 -> +0
+  const uint32_t o = (u & 0x8000u) ? (~u & 0xffffu) : (u | 0x8000u);
+  return (o << 16) | (0xffffu - static_cast<uint32_t>(e));
+}
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = gridDim.x, c = blockIdx.x;
+MLDEV float packed_key_logit(uint32_t v) {
+  const uint32_t o = v >> 16;
+  const uint32_t u = (o & 0x8000u) ? (o & 0x7fffu) : (~o & 0xffffu);
+  return __uint_as_float(u << 16);
+}
+
+// Top-k of the tokens [t0, t1): each warp runs kTPW tokens in lockstep, writes ids and
+// weights, records the CTA-local pair ids in ids_s and counts pairs per expert in hist_s.
+template <int EPL, int METHOD, int kTPW>
+MLDEV void select_topk(const RouteParams& p, int t0, int t1, int* ids_s, int* hist_s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = p.E, k = p.k;
-
-  for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = 0;
-  __syncthreads();
-
-  const int t0 = c * p.tokens_per_cta;
-  const int t1 = min(p.T, t0 + p.tokens_per_cta);
-
+  if constexpr (METHOD == 0) {
+    // Renormalize: packed (logit, id) keys are all distinct, so a round is one hardware
+    // maximum over the lanes' list heads and the one lane holding it shifts its list.
+    for (int tb = t0 + warp * kTPW; tb < t1; tb += kRouteWarps * kTPW) {
+      uint32_t sk[kTPW][EPL];   // this lane's packed keys, descending; 0 = empty
+      int my_id[kTPW];
+      float my_key[kTPW];
+#pragma unroll
+      for (int u = 0; u < kTPW; ++u) {
+        const int t = tb + u;
+        my_id[u] = kInvalidId;
+        my_key[u] = -INFINITY;
+        const __nv_bfloat16* row = p.logits + static_cast<size_t>(t) * E;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          sk[u][i] = (t < t1 && e < E) ? packed_logit_key(row, e) : 0u;
+        }
+#pragma unroll
+        for (int pass = 0; pass < EPL; ++pass) {   // odd-even transposition sort
+#pragma unroll
+          for (int i = pass & 1; i + 1 < EPL; i += 2) {
+            const uint32_t a = sk[u][i], b = sk[u][i + 1];
+            sk[u][i] = max(a, b);
+            sk[u][i + 1] = min(a, b);
+          }
+        }
+      }
+      for (int j = 0; j < k; ++j) {
+        uint32_t wmax[kTPW];
+#pragma unroll
+        for (int u = 0; u < kTPW; ++u) wmax[u] = __reduce_max_sync(0xffffffffu, sk[u][0]);
+#pragma unroll
+        for (int u = 0; u < kTPW; ++u) {
+          if (wmax[u] != 0u && sk[u][0] == wmax[u]) {   // pop this lane's head
+#pragma unroll
+            for (int i = 0; i + 1 < EPL; ++i) sk[u][i] = sk[u][i + 1];
+            sk[u][EPL - 1] = 0u;
+          }
+          if (lane == j && wmax[u] != 0u) {
+            my_id[u] = static_cast<int>(0xffffu - (wmax[u] & 0xffffu));
+            my_key[u] = packed_key_logit(wmax[u]);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kTPW; ++u) {
+        const int t = tb + u;
+        if (t >= t1) break;   // uniform across the warp
+        const float kmax = __shfl_sync(0xffffffffu, my_key[u], 0);
+        const float ex = (lane < k) ? expf(my_key[u] - kmax) : 0.0f;
+        float sum = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        const float wv = ex / sum;
+        if (lane < k) {
+          const int pl = (t - t0) * k + lane;   // pair index local to this CTA
+          if (pl < kRouteIdsInSmem) ids_s[pl] = my_id[u];
+          p.ids[static_cast<size_t>(t) * k + lane] = my_id[u];
+          p.weights[static_cast<size_t>(t) * k + lane] = wv;
+          atomicAdd(&hist_s[my_id[u]], 1);
+        }
+      }
+    }
+  } else {
   // ---------------- phase 1: top-k per token; each warp runs kTPW tokens in lockstep.
   // Keys are mapped to unsigned integers whose order is the float order (-0 folded to +0,
   // so +-0 tie like equal floats).  Each lane first sorts its EPL (key, id) entries
@@ -251,52 +320,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
       }
     }
   }
-  __syncthreads();
-
-  pdl_trigger();   // the permute may launch now; it waits for this kernel to finish
-
-  // ---------------- phase 2: expert offsets and per-CTA bases
-  if (G > 1) {
-    for (int e = tid; e < E; e += kRouteThreads) p.hist[c * E + e] = hist_s[e];
-    if (!grid_barrier(p.barrier, static_cast<uint32_t>(G), p.status, &ok_s)) return;
-    // warp per expert: prefix of the per-CTA counts in CTA order
-    const int m = (G + 31) / 32;
-    for (int e = c * kRouteWarps + warp; e < E; e += G * kRouteWarps) {
-      int loc = 0;
-      for (int i = 0; i < m; ++i) {
-        const int cc = lane * m + i;
-        if (cc < G) loc += __ldcg(&p.hist[cc * E + e]);
-      }
-      int incl = loc;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      int run = incl - loc;
-      for (int i = 0; i < m; ++i) {
-        const int cc = lane * m + i;
-        if (cc < G) {
-          p.base[cc * E + e] = run;
-          run += __ldcg(&p.hist[cc * E + e]);
-        }
-      }
-      if (lane == 31) p.total[e] = incl;
-    }
-    if (!grid_barrier(p.barrier, 2u * static_cast<uint32_t>(G), p.status, &ok_s)) return;
-    for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = __ldcg(&p.total[e]);
-    __syncthreads();
   }
-  const int total = block_exclusive_scan(hist_s, cursor_s, E, warp_sums);
-  if (c == 0) {
-    for (int e = tid; e < E; e += kRouteThreads) p.offsets[e] = cursor_s[e];
-    if (tid == 0) p.offsets[E] = total;
-  }
-  if (G > 1) {
-    for (int e = tid; e < E; e += kRouteThreads) cursor_s[e] += __ldcg(&p.base[c * E + e]);
-  }
-  __syncthreads();
+}
 
+// Scatter the pairs of tokens [t0, t1) to perm / inv_perm in ascending expanded index;
+// cursor_s[e] holds the first permuted slot of this CTA's pairs of expert e.  wcnt is
+// scratch of kRouteWarps * kScatterMaxE ints.
+MLDEV void scatter_pairs(const RouteParams& p, int t0, int t1, const int* ids_s, int* cursor_s, int* wcnt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E, k = p.k;
   // ---------------- scatter this CTA's pairs in ascending expanded index.  The pairs are
   // split into one contiguous chunk per warp; per-warp expert counts and their prefix over
   // warps (in warp order) give each warp its own cursors, and inside a warp 32 pairs at a
@@ -348,6 +380,174 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   }
 }
 
+template <int EPL, int METHOD>
+__global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteParams p) {
+  constexpr int kTPW = EPL <= 4 ? 4 : (EPL <= 8 ? 2 : 1);   // tokens per warp, in lockstep
+  __shared__ int hist_s[kMaxExperts];
+  __shared__ int cursor_s[kMaxExperts];
+  __shared__ int warp_sums[kRouteWarps + 1];
+  __shared__ int ok_s;
+  __shared__ int ids_s[kRouteIdsInSmem];   // this CTA's expert ids, when they fit
+  __shared__ int wcnt[kRouteWarps * kScatterMaxE];   // per-warp expert cursors
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int E = p.E;
+
+  for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = 0;
+  __syncthreads();
+
+  const int t0 = c * p.tokens_per_cta;
+  const int t1 = min(p.T, t0 + p.tokens_per_cta);
+
+  select_topk<EPL, METHOD, kTPW>(p, t0, t1, ids_s, hist_s);
+  __syncthreads();
+
+  pdl_trigger();   // the permute may launch now; it waits for this kernel to finish
+
+  // ---------------- phase 2: expert offsets and per-CTA bases
+  if (G > 1) {
+    for (int e = tid; e < E; e += kRouteThreads) p.hist[c * E + e] = hist_s[e];
+    if (!grid_barrier(p.barrier, static_cast<uint32_t>(G), p.status, &ok_s)) return;
+    // warp per expert: prefix of the per-CTA counts in CTA order
+    const int m = (G + 31) / 32;
+    for (int e = c * kRouteWarps + warp; e < E; e += G * kRouteWarps) {
+      int loc = 0;
+      for (int i = 0; i < m; ++i) {
+        const int cc = lane * m + i;
+        if (cc < G) loc += __ldcg(&p.hist[cc * E + e]);
+      }
+      int incl = loc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int run = incl - loc;
+      for (int i = 0; i < m; ++i) {
+        const int cc = lane * m + i;
+        if (cc < G) {
+          p.base[cc * E + e] = run;
+          run += __ldcg(&p.hist[cc * E + e]);
+        }
+      }
+      if (lane == 31) p.total[e] = incl;
+    }
+    if (!grid_barrier(p.barrier, 2u * static_cast<uint32_t>(G), p.status, &ok_s)) return;
+    for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = __ldcg(&p.total[e]);
+    __syncthreads();
+  }
+  const int total = block_exclusive_scan(hist_s, cursor_s, E, warp_sums);
+  if (c == 0) {
+    for (int e = tid; e < E; e += kRouteThreads) p.offsets[e] = cursor_s[e];
+    if (tid == 0) p.offsets[E] = total;
+  }
+  if (G > 1) {
+    for (int e = tid; e < E; e += kRouteThreads) cursor_s[e] += __ldcg(&p.base[c * E + e]);
+  }
+  __syncthreads();
+
+  scatter_pairs(p, t0, t1, ids_s, cursor_s, wcnt);
+}
+
+// ---------------------------------------------------------------------------------
+// Up to kRouteClusterMax CTAs of one thread-block cluster (up to 512 tokens): the same
+// top-k and scatter, with the per-CTA expert counts exchanged through distributed shared
+// memory between two cluster barriers instead of global scratch and grid barriers.  Every
+// CTA reads all CTAs' counts (C x E loads), so each forms the expert offsets itself and
+// its own per-expert base, the prefix of the counts of the CTAs before it.
+// ---------------------------------------------------------------------------------
+MLDEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+MLDEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+MLDEV int ld_dsmem(const int* local, uint32_t rank) {   // the same variable in CTA `rank`
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+MLDEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+template <int EPL, int METHOD>
+__global__ void __launch_bounds__(kRouteThreads) route_cluster_kernel(const RouteParams p) {
+  __shared__ int hist_s[kMaxExperts];
+  __shared__ int cursor_s[kMaxExperts];
+  __shared__ int warp_sums[kRouteWarps + 1];
+  __shared__ int ids_s[kRouteIdsInSmem];
+  __shared__ int wcnt[kRouteWarps * kScatterMaxE];   // expert totals and bases, then scatter cursors
+
+  const int tid = threadIdx.x;
+  const int C = gridDim.x;   // the grid is one cluster
+  const uint32_t c = cluster_ctarank();
+  const int E = p.E;
+
+  for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = 0;
+  __syncthreads();
+  const int t0 = static_cast<int>(c) * p.tokens_per_cta;
+  const int t1 = min(p.T, t0 + p.tokens_per_cta);
+  select_topk<EPL, METHOD, 1>(p, t0, t1, ids_s, hist_s);
+  pdl_trigger();   // the permute may launch now; it waits for this kernel to finish
+
+  cluster_arrive();   // this CTA's counts are final ...
+  cluster_wait();     // ... and so are everyone's
+  int* tot_s = wcnt;          // [E] expert totals over the cluster
+  int* base_s = wcnt + E;     // [E] pairs of the CTAs before this one
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int base = 0, tot = 0;
+    for (int cc = 0; cc < C; ++cc) {
+      const int v = ld_dsmem(&hist_s[e], static_cast<uint32_t>(cc));
+      base += (cc < static_cast<int>(c)) ? v : 0;
+      tot += v;
+    }
+    tot_s[e] = tot;
+    base_s[e] = base;
+  }
+  cluster_arrive();   // done reading the other CTAs' counts (waited for before exit)
+  __syncthreads();
+  const int total = block_exclusive_scan(tot_s, cursor_s, E, warp_sums);
+  if (c == 0) {
+    for (int e = tid; e < E; e += kRouteThreads) p.offsets[e] = cursor_s[e];
+    if (tid == 0) p.offsets[E] = total;
+  }
+  for (int e = tid; e < E; e += kRouteThreads) cursor_s[e] += base_s[e];
+  __syncthreads();
+  scatter_pairs(p, t0, t1, ids_s, cursor_s, wcnt);
+  cluster_wait();     // no CTA leaves while another may still read its counts
+}
+
+int route_cluster_ctas(int T) {
+  if (T > kRouteClusterMax * 64) return 0;
+  int c = (T + 15) / 16;
+  if (c > kRouteClusterMax) c = kRouteClusterMax;
+  return c < 1 ? 1 : c;
+}
+
+template <int EPL, int METHOD>
+static cudaError_t launch_cluster_epl(const RouteParams& p, int ctas, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_cluster_kernel<EPL, METHOD>, p);
+}
+
+template <int METHOD>
+static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream);
+
 static int epl_for(int E) { return E <= 128 ? 4 : E <= 256 ? 8 : E <= 384 ? 12 : E <= 512 ? 16 : 32; }
 
 template <int EPL, int METHOD>
@@ -396,6 +596,22 @@ int route_max_coop_ctas(int E) {
 
 cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stream) {
   return p.method == 1 ? launch_method<1>(p, grid, stream) : launch_method<0>(p, grid, stream);
+}
+
+template <int METHOD>
+static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream) {
+  switch (epl_for(p.E)) {
+    case 4: return launch_cluster_epl<4, METHOD>(p, ctas, stream);
+    case 8: return launch_cluster_epl<8, METHOD>(p, ctas, stream);
+    case 12: return launch_cluster_epl<12, METHOD>(p, ctas, stream);
+    case 16: return launch_cluster_epl<16, METHOD>(p, ctas, stream);
+    default: return launch_cluster_epl<32, METHOD>(p, ctas, stream);
+  }
+}
+
+cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream) {
+  if (ctas < 1 || ctas > kRouteClusterMax) return cudaErrorInvalidValue;
+  return p.method == 1 ? launch_cluster_method<1>(p, ctas, stream) : launch_cluster_method<0>(p, ctas, stream);
 }
 
 }  // namespace mlk

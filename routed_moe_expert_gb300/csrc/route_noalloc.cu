@@ -115,6 +115,12 @@ extern "C" moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_lo
   p.total = reinterpret_cast<int32_t*>(scratch + kHeaderBytes);
   p.hist = p.total + E;
   p.base = p.hist + static_cast<size_t>(grid) * E;
+  const int ctas = route_cluster_ctas(T);   // one cluster up to 512 tokens: no scratch beyond the header
+  if (ctas > 0) {
+    p.tokens_per_cta = (T + ctas - 1) / ctas;
+    if (launch_route_cluster(p, ctas, stream) != cudaSuccess) return MOE_LORA_ERR_CUDA;
+    return MOE_LORA_OK;
+  }
   if (launch_route_align(p, grid, stream) != cudaSuccess) return MOE_LORA_ERR_CUDA;
   return MOE_LORA_OK;
 }
