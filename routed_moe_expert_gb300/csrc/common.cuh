@@ -62,12 +62,15 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Expert tile schedule from offsets staged in shared memory (seg[e] = first permuted pair
-// of expert e, seg[E] = P): tile_start[e] = sum over e' < e of ceil(M_e' / tile) * mult,
-// tile_start[E] = the total.  Run by one warp.  Callers stage seg with one round of loads
-// by every thread first, so the offsets cost one memory latency, not one per 32 experts.
-MLDEV void scan_tile_schedule(const int* seg, int E, int tile, int mult, int* tile_start) {
+// Expert tile schedule, built by one warp: seg[e] = offsets[e] (e <= E, staged in shared
+// memory with all loads in flight at once, so the offsets cost one memory latency rather
+// than one per 32 experts), tile_start[e] = sum over e' < e of ceil(M_e' / tile) * mult,
+// tile_start[E] = the total.  The caller's next __syncthreads publishes both.
+MLDEV void build_tile_schedule(const int32_t* offsets, int E, int tile, int mult, int* seg, int* tile_start) {
   const int lane = threadIdx.x & 31;
+#pragma unroll 4
+  for (int i = lane; i <= E; i += 32) seg[i] = offsets[i];
+  __syncwarp();
   int carry = 0;
   for (int b = 0; b < E; b += 32) {
     const int e = b + lane;

@@ -121,9 +121,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= E; i += kGemmThreads) seg[i] = p.offsets[i];
-  __syncthreads();
-  if (warp == 2) scan_tile_schedule(seg, E, BN, NT, tile_start);   // ceil(M_e/BN) * NT tiles each
+  if (warp == 2) build_tile_schedule(p.offsets, E, BN, NT, seg, tile_start);   // ceil(M_e/BN) * NT tiles each
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

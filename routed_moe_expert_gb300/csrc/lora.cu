@@ -85,9 +85,7 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
   const int g = lane >> 2, c = lane & 3;
   const int E = p.E;
 
-  for (int i = tid; i <= E; i += kLoraThreads) seg[i] = p.offsets[i];
-  __syncthreads();
-  if (warp == 0) scan_tile_schedule(seg, E, PT, 1, tile_start);   // ceil(M_e / PT) tiles each
+  if (warp == 0) build_tile_schedule(p.offsets, E, PT, 1, seg, tile_start);   // ceil(M_e / PT) tiles each
   __syncthreads();
   const int total = tile_start[E];
   const int K16 = p.K >> 4;
@@ -366,9 +364,7 @@ __global__ void __launch_bounds__(kLoraThreads) act_shrink_kernel(const ActShrin
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
 
-  for (int i = tid; i <= E; i += kLoraThreads) seg[i] = p.offsets[i];
-  __syncthreads();
-  if (warp == 0) scan_tile_schedule(seg, E, kActTile, 1, tile_start);   // ceil(M_e / 8) tiles each
+  if (warp == 0) build_tile_schedule(p.offsets, E, kActTile, 1, seg, tile_start);   // ceil(M_e / 8) tiles each
   __syncthreads();
   const int total = tile_start[E];
 

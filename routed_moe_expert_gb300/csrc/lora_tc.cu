@@ -79,9 +79,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= E; i += kShrinkThreads) seg[i] = p.offsets[i];
-  __syncthreads();
-  if (warp == 2) scan_tile_schedule(seg, E, p.tb, 1, tile_start);   // tiles of TB pairs per expert
+  if (warp == 2) build_tile_schedule(p.offsets, E, p.tb, 1, seg, tile_start);   // tiles of TB pairs per expert
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
