@@ -137,6 +137,9 @@ size_t lora_smem_bytes(int ntl, int R, int N, bool expand, int E);
 struct ShrinkTcParams {
   CUtensorMap tmap_x;            // X [P rows, K cols], box {64, tb}
   CUtensorMap tmap_a;            // A [S*E*R rows, K cols], box {64, R}
+  CUtensorMap tmap_a_slot[kMaxFusedSlots];   // the same rows, box {64, rows of slot s} (per_slot)
+  int row_off[kMaxFusedSlots + 1];           // per_slot: first stacked B row of slot s
+  int per_slot;                  // 1: only each active slot's rank rows are loaded
   int tb;                        // pairs (rows of X) per tile: 16, 32, 64 or 128
   const int32_t* offsets;        // [E + 1]
   const int32_t* perm;           // [P]
@@ -148,7 +151,7 @@ struct ShrinkTcParams {
   int32_t* pair_slot;            // [P]
   uint32_t* status;
 };
-int lora_shrink_tc_nb(int S, int R);
+int lora_shrink_tc_nb(int rows);
 cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl = false);
 

@@ -11,10 +11,13 @@
 // grouped GEMMs as extra K-stages.  The tile is up to TB pairs of one expert (TB rows of X by
 // TMA, TB in {16..128} from the mean pairs per expert; the MMA runs at M = 128 and the rows
 // past TB are never read back) by N = every slot's rank rows of A for that expert, stacked
-// (N = S*R <= 256), so one
-// pass over K serves all slots present; the rank tail of a stacked adapter only produces
-// accumulator columns that are never read.  Warp roles as in the grouped GEMM: TMA
-// producer, MMA issuer + TMEM owner, 4 epilogue warps; bounded waits throughout.
+// (N <= 256), so one pass over K serves all slots present.  When every active rank is a
+// multiple of 8, each slot's block is loaded with its own tensor map whose box is exactly
+// its rank rows, packed one after another (each at a 1024-byte swizzle-atom boundary), so
+// the padding rows of a stacked adapter are never fetched; otherwise all R rows of every
+// slot are loaded and the tails only produce accumulator columns that are never read.
+// Warp roles as in the grouped GEMM: TMA producer, MMA issuer + TMEM owner, 4 epilogue
+// warps; bounded waits throughout.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -73,7 +76,12 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmap_x);
-    tma_prefetch_desc(&p.tmap_a);
+    if (p.per_slot) {
+      for (int s = 0; s < p.S; ++s)
+        if (p.row_off[s + 1] > p.row_off[s]) tma_prefetch_desc(&p.tmap_a_slot[s]);
+    } else {
+      tma_prefetch_desc(&p.tmap_a);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -87,6 +95,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
   pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_start[E];
+  const int nrows = p.per_slot ? p.row_off[p.S] : p.S * p.R;   // stacked B rows actually loaded
   auto decode = [&](int tile, int& e, int& qt) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -114,13 +123,20 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
             break;
           }
           uint8_t* a = smem + stage * STAGE;
-          // bytes actually copied: TB rows of X and S*R rows of A (rows TB..127 of the A tile
-          // and S*R..NB-1 of the B tile keep stale data; they only feed accumulator lanes and
-          // columns that are never read)
-          mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(p.tb + p.S * p.R) * 128u);
+          // bytes actually copied: TB rows of X and nrows rows of A (rows TB..127 of the A
+          // tile and nrows..NB-1 of the B tile keep stale data; they only feed accumulator
+          // lanes and columns that are never read)
+          mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(p.tb + nrows) * 128u);
           tma_load_2d(a, &p.tmap_x, &full[stage], kb * 64, xr, pol_x);
-          for (int s = 0; s < p.S; ++s)   // each slot's R rows of A for expert e, stacked
-            tma_load_2d(a + A_BYTES + s * p.R * 128, &p.tmap_a, &full[stage], kb * 64, (s * E + e) * p.R, pol_a);
+          if (p.per_slot) {   // each active slot's rank rows of A for expert e, packed
+            for (int s = 0; s < p.S; ++s)
+              if (p.row_off[s + 1] > p.row_off[s])
+                tma_load_2d(a + A_BYTES + p.row_off[s] * 128, &p.tmap_a_slot[s], &full[stage], kb * 64,
+                            (s * E + e) * p.R, pol_a);
+          } else {            // each slot's R rows of A for expert e, stacked
+            for (int s = 0; s < p.S; ++s)
+              tma_load_2d(a + A_BYTES + s * p.R * 128, &p.tmap_a, &full[stage], kb * 64, (s * E + e) * p.R, pol_a);
+          }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -192,11 +208,12 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * NB);
       // Every column (s2, r) of the accumulator goes to ub[s2][q][r]: the scaled value when
-      // s2 is this pair's slot and r < its rank, zero otherwise.  R is a multiple of 8, so
-      // each 8 columns lie in one slot row and leave as one 16-byte store.
+      // s2 is this pair's slot and r < its rank, zero otherwise.  Ranks (per_slot) and R are
+      // multiples of 8, so each 8 columns lie in one slot row and leave as one 16-byte store;
+      // with per_slot the rows past a slot's loaded rows are written as zeros afterwards.
       const float sc = sl >= 0 ? p.slots.scal[sl] : 0.0f;
       const int rank = sl >= 0 ? p.slots.ranks[sl] : 0;
-      const int ncol = p.S * p.R;
+      const int ncol = nrows;
 #pragma unroll 1
       for (int c = 0; c < ncol; c += 16) {   // tcgen05.ld is warp-wide: same columns in every lane
         uint32_t v[16];
@@ -207,7 +224,15 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
           for (int h8 = 0; h8 < 2; ++h8) {
             const int col0 = c + 8 * h8;
             if (col0 >= ncol) break;
-            const int s2 = col0 / p.R, r0 = col0 - s2 * p.R;
+            int s2, r0;
+            if (p.per_slot) {
+              s2 = 0;
+              while (p.row_off[s2 + 1] <= col0) ++s2;
+              r0 = col0 - p.row_off[s2];
+            } else {
+              s2 = col0 / p.R;
+              r0 = col0 - s2 * p.R;
+            }
             float f[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -215,6 +240,12 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
             *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s2) * p.P + q) * p.R + r0) = pack8(f);
           }
         }
+      }
+      if (valid && p.per_slot) {
+        for (int s2 = 0; s2 < p.S; ++s2)
+          for (int r0 = p.row_off[s2 + 1] - p.row_off[s2]; r0 < p.R; r0 += 8)
+            *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s2) * p.P + q) * p.R + r0) =
+                make_uint4(0u, 0u, 0u, 0u);
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -252,14 +283,14 @@ static cudaError_t launch_nb(const ShrinkTcParams& p_in, int grid, cudaStream_t 
   return launch_k(lora_shrink_tc_kernel<NB>, dim3(grid), dim3(kShrinkThreads), smem, stream, pdl, p);
 }
 
-int lora_shrink_tc_nb(int S, int R) {
-  const int n = S * R;
+int lora_shrink_tc_nb(int rows) {
+  const int n = rows;
   return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 0;
 }
 
 cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl) {
   if (p.P == 0) return cudaSuccess;
-  switch (lora_shrink_tc_nb(p.S, p.R)) {
+  switch (lora_shrink_tc_nb(p.per_slot ? p.row_off[p.S] : p.S * p.R)) {
     case 16: return launch_nb<16>(p, grid, stream, pdl);
     case 32: return launch_nb<32>(p, grid, stream, pdl);
     case 64: return launch_nb<64>(p, grid, stream, pdl);

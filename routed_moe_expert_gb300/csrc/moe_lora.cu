@@ -345,6 +345,18 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   sp.tb = m2 <= 16 ? 16 : m2 <= 32 ? 32 : m2 <= 64 ? 64 : 128;
   if (!make_tmap(h->encode, &sp.tmap_x, X, static_cast<uint64_t>(P), K, sp.tb)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &sp.tmap_a, A, static_cast<uint64_t>(a->S) * a->E * a->R, K, a->R)) return MOE_LORA_ERR_CUDA;
+  // only the active slots' rank rows, when every such rank is a multiple of 8 (each slot's
+  // rows then start on a swizzle-atom boundary of the stacked tile)
+  sp.per_slot = a->S <= kMaxFusedSlots ? 1 : 0;
+  sp.row_off[0] = 0;
+  for (int s = 0; s < a->S && sp.per_slot; ++s) {
+    const int rows = (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) ? slots.ranks[s] : 0;
+    if (rows % 8 != 0) sp.per_slot = 0;
+    sp.row_off[s + 1] = sp.row_off[s] + rows;
+    if (rows > 0 && !make_tmap(h->encode, &sp.tmap_a_slot[s], A, static_cast<uint64_t>(a->S) * a->E * a->R, K,
+                               static_cast<uint32_t>(rows)))
+      return MOE_LORA_ERR_CUDA;
+  }
   sp.offsets = offsets;
   sp.perm = perm;
   sp.slot_idx = a->slot_idx;
