@@ -424,26 +424,35 @@ __global__ void __launch_bounds__(kLoraThreads) act_shrink_kernel(const ActShrin
       for (int mt = 0; mt < MTX; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
-      for (int ks = warp; ks < (I >> 4); ks += kLoraWarps) {
-        const int k0 = ks * 16 + 2 * c;
-        uint32_t bf[2];
-        bf[0] = *reinterpret_cast<const uint32_t*>(a_s + g * AS + k0);
-        bf[1] = *reinterpret_cast<const uint32_t*>(a_s + g * AS + k0 + 8);
-        uint32_t af[MTX][4];
+      // the A fragments of KU k-steps are loaded before their MMAs, so their latencies overlap
+      constexpr int KU = MTX >= 8 ? 1 : 8 / MTX;
+      const int nks = I >> 4;
+      for (int ks0 = warp; ks0 < nks; ks0 += kLoraWarps * KU) {
+        uint32_t af[KU][MTX][4], bf[KU][2];
 #pragma unroll
-        for (int mt = 0; mt < MTX; ++mt) {
-          const int r0 = mt * 16 + g, r1 = r0 + 8;
-          const bool ok0 = mt < MT && r0 < rank, ok1 = mt < MT && r1 < rank;
-          const __nv_bfloat16* A0 = A + static_cast<size_t>(r0) * I + k0;
-          const __nv_bfloat16* A1 = A + static_cast<size_t>(r1) * I + k0;
-          af[mt][0] = ok0 ? ld_b32(A0) : 0u;
-          af[mt][1] = ok1 ? ld_b32(A1) : 0u;
-          af[mt][2] = ok0 ? ld_b32(A0 + 8) : 0u;
-          af[mt][3] = ok1 ? ld_b32(A1 + 8) : 0u;
+        for (int u = 0; u < KU; ++u) {
+          const int ks = ks0 + u * kLoraWarps;
+          const bool kin = ks < nks;
+          const int k0 = (kin ? ks : 0) * 16 + 2 * c;
+          bf[u][0] = kin ? *reinterpret_cast<const uint32_t*>(a_s + g * AS + k0) : 0u;
+          bf[u][1] = kin ? *reinterpret_cast<const uint32_t*>(a_s + g * AS + k0 + 8) : 0u;
+#pragma unroll
+          for (int mt = 0; mt < MTX; ++mt) {
+            const int r0 = mt * 16 + g, r1 = r0 + 8;
+            const bool ok0 = kin && mt < MT && r0 < rank, ok1 = kin && mt < MT && r1 < rank;
+            const __nv_bfloat16* A0 = A + static_cast<size_t>(r0) * I + k0;
+            const __nv_bfloat16* A1 = A + static_cast<size_t>(r1) * I + k0;
+            af[u][mt][0] = ok0 ? ld_b32(A0) : 0u;
+            af[u][mt][1] = ok1 ? ld_b32(A1) : 0u;
+            af[u][mt][2] = ok0 ? ld_b32(A0 + 8) : 0u;
+            af[u][mt][3] = ok1 ? ld_b32(A1 + 8) : 0u;
+          }
         }
 #pragma unroll
-        for (int mt = 0; mt < MTX; ++mt)
-          if (mt < MT) mma_bf16_16816(acc[mt], af[mt], bf);
+        for (int u = 0; u < KU; ++u)
+#pragma unroll
+          for (int mt = 0; mt < MTX; ++mt)
+            if (ks0 + u * kLoraWarps < nks && mt < MT) mma_bf16_16816(acc[mt], af[u][mt], bf[u]);
       }
       // partials [row][pair] of this warp, then the fixed-order sum over warps
       float* rw = red + warp * 16 * MTX * kActTile;
