@@ -165,14 +165,23 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
 
 /* The whole layer: out [T, H] bf16.  `workspace` holds moe_lora_workspace_size() bytes;
    its contents on entry do not matter.
-   LoRA placement: the gate_up LoRA chain (shrink + expand into a bf16 delta) runs on the
-   side stream beside the permute and gate_up GEMM and joins before the activation, as in
-   sglang PR #28466 section 1 flow (B).  The down-LoRA shrink runs after the activation;
-   when R is a multiple of 8, S <= 8 and the GEMM's token tiles are 32 or wider, its expand
-   runs inside the down GEMM as extra tensor-core K-stages, otherwise (or with
-   MOE_LORA_FLAG_UNFUSED_LORA) in the down GEMM's epilogue on the CUDA cores.  The side stream is used when T <= 256 unless
-   FORCE_SINGLE_STREAM (sglang PR #28466, "Which diagram applies when": decode-shaped
-   batches only).
+   LoRA placement follows the GEMMs' token tile BN (twice the mean pairs per expert,
+   rounded up to 16..256):
+   - BN >= 32, R a multiple of 8, S <= 8 and S*R <= 256 (unless MOE_LORA_FLAG_UNFUSED_LORA):
+     both LoRA shrinks run on the tensor cores over every active slot at once, both
+     expands run inside the expert GEMMs as extra tensor-core K-stages (the gate_up delta
+     in its own accumulator, so the GEMM output and the delta are rounded to bf16
+     separately, as the pages do), and the activation runs in the gate_up GEMM's epilogue.
+   - otherwise: the gate_up LoRA chain (shrink + expand into a bf16 delta) runs on the side
+     stream beside the permute and gate_up GEMM and joins before the activation (sglang PR
+     #28466 section 1 flow (B)).  When the down expand cannot be K-stages (BN 16, R not a
+     multiple of 8, S > 8, or MOE_LORA_FLAG_UNFUSED_LORA) the activation and the down
+     shrink run as one kernel and the expand runs in the down GEMM's epilogue on the CUDA
+     cores; else the down shrink runs after the activation and its expand inside the down
+     GEMM.  The side stream is used when T <= 256 unless FORCE_SINGLE_STREAM (sglang PR
+     #28466, "Which diagram applies when": decode-shaped batches only).
+   Kernels after the routing start as programmatic dependents of the previous kernel on
+   the stream unless MOE_LORA_FLAG_NO_PDL.
    Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
 moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out,
                                  void* workspace, size_t workspace_bytes, moe_lora_stream stream);
@@ -182,9 +191,10 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
    cudaMalloc or supply a workspace (plug-ins inside a host framework that owns all device
    memory, allocation-free real-time paths).  Same arguments, outputs and results as
    moe_lora_route.  The kernel's scratch lives in a 512 KiB array inside the library's
-   device image, held by every GPU that loads the library until the process exits; the
-   routing grid shrinks until its scratch fits (8*E bytes per routing CTA), and a shape
-   that cannot fit is rejected with MOE_LORA_ERR_UNSUPPORTED.  The first call on a device
+   device image, held by every GPU that loads the library until the process exits.  Up to
+   512 tokens the routing runs as one thread-block cluster and uses only the array's
+   header; above that the routing grid shrinks until its scratch fits (8*E bytes per
+   routing CTA), and a shape that cannot fit is rejected with MOE_LORA_ERR_UNSUPPORTED.  The first call on a device
    resolves the array's address on the current device (cudaGetSymbolAddress), so make
    that first call before any stream capture.  All calls share the array: each call
    clears its status word and barrier counter on `stream`, and calls that overlap on the
