@@ -671,7 +671,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   const bool act_in_gemm = fuse_all || (!lora && bn0 >= 32);
   if (act_in_gemm) {
     int bn = bn0;
-    if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the LoRA delta accumulators
+    if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the gate_up LoRA delta accumulators
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
     ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
             "permute launch");
@@ -712,8 +712,9 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     dn.N = H;
     dn.K = I;
     dn.gated = 0;
-    if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
-    st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream, pdl);
+    // the down GEMM adds its LoRA stages to the main accumulator, so it keeps the full tile
+    if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0)) return MOE_LORA_ERR_CUDA;
+    st = enqueue_gemm(h, dn, a->w2, act, P, bn0, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
   } else {
