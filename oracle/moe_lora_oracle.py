@@ -39,6 +39,12 @@ Readings of points the pages leave open (each also listed in the design notes):
     logits followed by renormalising the top k gives the same numbers).
   * DeepSeekV3 with n_group = topk_group = 1: scores s = sigmoid(logit), select on
     s + correction_bias, weights = s_sel / sum(s_sel) * routed_scaling_factor.
+  * Externally routed entry (moe_lora_forward_routed): the packed word is the expert id
+    in the high 16 bits and the bf16 bits of the routing weight (nearest even) in the low
+    16 bits; pairs of experts outside the local range are dropped (they add nothing and
+    map to permuted index -1) and are aligned after the last local expert; with
+    do_finalize=False the returned per-pair down output already holds the down-LoRA
+    delta, unweighted (what the vLLM page's _finalize_with_w2_lora adds back).
 """
 from __future__ import annotations
 
@@ -181,6 +187,72 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
+def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slots,
+             ranks, scalings, lora_off, inter, local=None):
+    """Per-pair expert math for the pairs of tokens `tok` (see moe_lora_forward).  With
+    `local` (a bool mask [T, k]) only those pairs are evaluated.  Returns
+    {(t, j): (y + dd, a)} in float64 (a holds bf16 values)."""
+    S = len(ranks)
+    res = {}
+    pair_t = np.repeat(tok, top_k)
+    pair_j = np.tile(np.arange(top_k), tok.size)
+    if local is not None:
+        keep = local[pair_t, pair_j]
+        pair_t, pair_j = pair_t[keep], pair_j[keep]
+    pair_e = ids[pair_t, pair_j]
+    # pairs grouped by expert: one matrix product per expert evaluates every pair routed
+    # to that expert; pairs are independent
+    for e in np.unique(pair_e):
+        sel = np.nonzero(pair_e == e)[0]
+        ts, js = pair_t[sel], pair_j[sel]
+        xe = x[ts]                                               # [n, H]
+        W1 = _f64(w1[e])                                         # [2I, H]
+        W2 = _f64(w2[e])                                         # [H, I]
+        I = W1.shape[0] // 2
+        g = round_bf16(xe @ W1.T)                                # [n, 2I]
+        d = np.zeros_like(g)
+        lora_rows = []
+        if not lora_off and S > 0:
+            for s in range(S):
+                r = int(ranks[s])
+                sc = float(scalings[s])
+                m = np.nonzero(slots[ts] == s)[0]
+                if m.size == 0 or r == 0 or sc == 0.0:
+                    continue
+                A = _f64(lora_A_gu[s, e])[:r]                    # [r, H]
+                B = _f64(lora_B_gu[s, e])[:, :r]                 # [2I, r]
+                u = xe[m] @ A.T                                  # [m, r]
+                d[m] = round_bf16(sc * (u @ B.T))
+                lora_rows.append((s, r, sc, m))
+        a = round_bf16(silu(g[:, :I] + d[:, :I]) * (g[:, I:] + d[:, I:]))   # [n, I]
+        y = a @ W2.T                                             # [n, H]
+        dd = np.zeros_like(y)
+        for s, r, sc, m in lora_rows:
+            A = _f64(lora_A_dn[s, e])[:r]                        # [r, I]
+            B = _f64(lora_B_dn[s, e])[:, :r]                     # [H, r]
+            v = a[m] @ A.T                                       # [m, r]
+            dd[m] = sc * (v @ B.T)
+        for i in range(sel.size):
+            res[(int(ts[i]), int(js[i]))] = (y[i] + dd[i], a[i])
+            if inter is not None:
+                inter[int(ts[i]) * top_k + int(js[i])] = dict(g=g[i], d=d[i], a=a[i], y=y[i], dd=dd[i])
+    return res
+
+
+def _finalize(tok, top_k, H, w, rows, local=None):
+    """out_acc[t] = sum over j = 0..k-1, in that order, of w[t,j] * (y + dd) (float64),
+    skipping pairs outside `local`."""
+    out_acc = np.zeros((tok.size, H), dtype=np.float64)
+    for i, t in enumerate(tok):
+        acc = np.zeros(H, dtype=np.float64)
+        for j in range(top_k):
+            if local is not None and not local[t, j]:
+                continue
+            acc = acc + w[t, j] * rows[(int(t), j)][0]
+        out_acc[i] = acc
+    return out_acc
+
+
 def moe_lora_forward(hidden, router_logits, w1, w2, top_k, method=RENORMALIZE,
                      correction_bias=None, routed_scaling_factor=1.0,
                      lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
@@ -221,61 +293,97 @@ def moe_lora_forward(hidden, router_logits, w1, w2, top_k, method=RENORMALIZE,
     offsets, perm, inv = align(ids, E)
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
-    S = len(ranks)
-
     inter = {} if keep_intermediates else None
-    contrib_of = {}                     # (t, j) -> w[t,j] * (y + dd), float64 [H]
-
-    # pairs of the requested tokens, grouped by expert (one matrix product per expert
-    # evaluates every pair routed to that expert; pairs are independent)
-    pair_t = np.repeat(tok, top_k)
-    pair_j = np.tile(np.arange(top_k), tok.size)
-    pair_e = ids[pair_t, pair_j]
-    for e in np.unique(pair_e):
-        sel = np.nonzero(pair_e == e)[0]
-        ts, js = pair_t[sel], pair_j[sel]
-        xe = x[ts]                                               # [n, H]
-        W1 = _f64(w1[e])                                         # [2I, H]
-        W2 = _f64(w2[e])                                         # [H, I]
-        I = W1.shape[0] // 2
-        g = round_bf16(xe @ W1.T)                                # [n, 2I]
-        d = np.zeros_like(g)
-        lora_rows = []
-        if not lora_off and S > 0:
-            for s in range(S):
-                r = int(ranks[s])
-                sc = float(scalings[s])
-                m = np.nonzero(slots[ts] == s)[0]
-                if m.size == 0 or r == 0 or sc == 0.0:
-                    continue
-                A = _f64(lora_A_gu[s, e])[:r]                    # [r, H]
-                B = _f64(lora_B_gu[s, e])[:, :r]                 # [2I, r]
-                u = xe[m] @ A.T                                  # [m, r]
-                d[m] = round_bf16(sc * (u @ B.T))
-                lora_rows.append((s, r, sc, m))
-        a = round_bf16(silu(g[:, :I] + d[:, :I]) * (g[:, I:] + d[:, I:]))   # [n, I]
-        y = a @ W2.T                                             # [n, H]
-        dd = np.zeros_like(y)
-        for s, r, sc, m in lora_rows:
-            A = _f64(lora_A_dn[s, e])[:r]                        # [r, I]
-            B = _f64(lora_B_dn[s, e])[:, :r]                     # [H, r]
-            v = a[m] @ A.T                                       # [m, r]
-            dd[m] = sc * (v @ B.T)
-        contrib = w[ts, js][:, None] * (y + dd)
-        for i in range(sel.size):
-            contrib_of[(int(ts[i]), int(js[i]))] = contrib[i]
-            if inter is not None:
-                inter[int(ts[i]) * top_k + int(js[i])] = dict(g=g[i], d=d[i], a=a[i], y=y[i], dd=dd[i])
-
+    rows = _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slots,
+                    ranks, scalings, lora_off, inter)
     # finalize: out[t] = bf16(sum over j = 0..k-1, in that order, of w[t,j] * (y + dd))
-    out_acc = np.zeros((tok.size, H), dtype=np.float64)
-    for i, t in enumerate(tok):
-        acc = np.zeros(H, dtype=np.float64)
-        for j in range(top_k):
-            acc = acc + contrib_of[(int(t), j)]
-        out_acc[i] = acc
+    out_acc = _finalize(tok, top_k, H, w, rows)
     res = dict(out=round_bf16(out_acc), topk_ids=ids, topk_weights=w,
                expert_offsets=offsets, perm=perm, inv=inv, tokens=tok)
     if inter is not None:
         res["pairs"] = inter
     return res
+
+
+# ----------------------------------------------------------------------------
+# externally routed entry (routing computed outside the layer)
+# ----------------------------------------------------------------------------
+
+def pack_topk(topk_ids, topk_weights):
+    """Packed top-k words of the externally-routed API (vLLM API page
+    "fused_moe/experts/trtllm_lora_moe", TrtLlmBf16LoRAExperts.apply: "pack it into the
+    (eid<<16)|w.bf16 format the routed API expects"): the expert id in the high 16 bits
+    and the bf16 bit pattern of the routing weight (rounded to nearest even) in the low
+    16 bits, as an int32."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    w = round_bf16(np.asarray(topk_weights, dtype=np.float64)).astype(np.float32)
+    bits = (w.view(np.uint32) >> 16).astype(np.int64)
+    return ((ids << 16) | bits).astype(np.uint32).view(np.int32)
+
+
+def unpack_topk(packed):
+    """Inverse of pack_topk: expert ids [T, k] int64 and routing weights [T, k] float64."""
+    u = np.asarray(packed).astype(np.int32).view(np.uint32).astype(np.int64)
+    ids = u >> 16
+    w = ((u & 0xFFFF) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    return ids, w
+
+
+def moe_lora_forward_routed(hidden, packed_topk_ids, w1, w2, top_k, num_experts, local_expert_offset=0,
+                            lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
+                            slot_idx=None, ranks=(), scalings=(), lora_off=False, do_finalize=True,
+                            tokens=None):
+    """The layer with routing given from outside (vLLM API page "fused_moe/experts/
+    trtllm_lora_moe": invoke_routed_moe / trtllm_bf16_routed_moe with packed_topk_ids,
+    local_expert_offset, local_num_experts and do_finalize).
+
+    packed_topk_ids [T, k]: (global expert id << 16) | bf16 bits of the weight.  w1/w2 and
+    the LoRA weights hold the E_loc = len(w1) local experts, global ids
+    [local_expert_offset, local_expert_offset + E_loc).  A pair routed to any other expert
+    is dropped here: it contributes nothing and its expanded_idx_to_permuted_idx is -1
+    (another rank owns that expert; the ranks' partial outputs are summed outside).
+
+    The local pairs are aligned exactly as in moe_lora_forward (by local expert, then
+    expanded index); the dropped ones follow after the last local expert.
+
+    do_finalize=True: out[t] = bf16(sum over local j, in j order, of w[t,j] * (y + dd)).
+    do_finalize=False: the unfinalized tuple of the page's invoke_routed_moe --
+    gemm2_output [P, H] (row q = y + dd of the pair at permuted position q, unweighted;
+    the down-LoRA delta is already inside, which is what the page's
+    _finalize_with_w2_lora adds), expert_weights [T, k], expanded_idx_to_permuted_idx
+    [T*k] (-1 for dropped pairs) and activation [P, I] (rows of dropped pairs are zero).
+    `tokens` restricts the evaluated pairs to those tokens' rows (the others are zero).
+    """
+    x = _f64(hidden)
+    T, H = x.shape
+    E_loc = len(w1)
+    gid, w = unpack_topk(packed_topk_ids)
+    if np.any((gid < 0) | (gid >= num_experts)):
+        raise ValueError("expert id outside [0, num_experts)")
+    lid = gid - int(local_expert_offset)
+    local = (lid >= 0) & (lid < E_loc)
+    bucket = np.where(local, lid, E_loc)                          # dropped pairs after the local ones
+    offsets, perm, inv = align(bucket, E_loc + 1)
+    idx_map = np.where(local.reshape(-1), inv, -1).astype(np.int32)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
+    rows = _experts(x, np.where(local, lid, 0), w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn,
+                    lora_B_dn, slots, ranks, scalings, lora_off, None, local=local)
+    res = dict(topk_ids=gid, topk_weights=w, expert_offsets=offsets[:E_loc + 1], perm=perm,
+               expanded_idx_to_permuted_idx=idx_map, local=local, tokens=tok)
+    if do_finalize:
+        out_acc = _finalize(tok, top_k, H, w, rows, local=local)
+        res["out"] = round_bf16(out_acc)
+        res["out_acc"] = out_acc
+        return res
+    P = T * top_k
+    I = _f64(w1[0]).shape[0] // 2 if E_loc > 0 else 0
+    gemm2 = np.zeros((P, H), dtype=np.float64)
+    act = np.zeros((P, I), dtype=np.float64)
+    for (t, j), (yd, a) in rows.items():
+        q = int(idx_map[t * top_k + j])
+        gemm2[q] = yd
+        act[q] = a
+    res.update(gemm2_output=gemm2, activation=act, expert_weights=w)
+    return res
+

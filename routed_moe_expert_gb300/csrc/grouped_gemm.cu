@@ -63,8 +63,51 @@ int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused) {
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
 
+// LoRA expand of one 16-token chunk on the CUDA cores, for output feature `feat` (this
+// thread's weight row): val[j] += sum_{r < ranks[s]} lora_B[s, e, feat, r] * v_s[c + j][r]
+// for each token j of the chunk with slot s = lslot[c + j] >= 0.  Tokens are taken slot by
+// slot (the slots are the same in every lane of the warp); v_s rows are staged per tile,
+// RP8 = R rounded up to 8 floats each, zero past the slot's rank.
+MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float* v_s, int c, int nvalid, int e,
+                             int feat, float (&val)[16]) {
+  const int R = p.slots.R;
+  const int RP8 = (R + 7) & ~7;
+  uint32_t done = 0;
+#pragma unroll 1
+  for (int j0 = 0; j0 < 16 && c + j0 < nvalid; ++j0) {
+    if ((done >> j0) & 1u) continue;
+    const int sl = lslot[c + j0];
+    uint32_t m = 0;
+    for (int j = j0; j < 16 && c + j < nvalid; ++j)
+      if (lslot[c + j] == sl) m |= 1u << j;
+    done |= m;
+    if (sl < 0) continue;
+    const int rank = p.slots.ranks[sl];
+    const __nv_bfloat16* Brow = p.lora_B + ((static_cast<size_t>(sl) * p.E + e) * p.N + feat) * static_cast<size_t>(R);
+#pragma unroll 1
+    for (int r0 = 0; r0 < rank; r0 += 8) {
+      float b[8];   // zero past the rank: the stacked tail is never read
+      if ((R & 7) == 0 && r0 + 8 <= rank) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(Brow + r0)), b);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = (r0 + i < rank) ? bf2f(Brow[r0 + i]) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if ((m >> j) & 1u) {
+          const float4* vj = reinterpret_cast<const float4*>(v_s + (c + j) * RP8 + r0);
+          const float4 v0 = vj[0], v1 = vj[1];
+          val[j] += b[0] * v0.x + b[1] * v0.y + b[2] * v0.z + b[3] * v0.w + b[4] * v1.x + b[5] * v1.y +
+                    b[6] * v1.z + b[7] * v1.w;
+        }
+      }
+    }
+  }
+}
+
 template <int BN>
-__global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -392,42 +435,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2) grouped_gemm_kernel(const __g
         float val[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) val[j] = __uint_as_float(r[j]);
-        if (lora && col < p.N) {
-          // down-LoRA expand, one slot at a time (slots are uniform across the warp)
-          uint32_t done = 0;
-#pragma unroll 1
-          for (int j0 = 0; j0 < 16 && c + j0 < nvalid; ++j0) {
-            if ((done >> j0) & 1u) continue;
-            const int sl = lslot[c + j0];
-            uint32_t m = 0;
-            for (int j = j0; j < 16 && c + j < nvalid; ++j)
-              if (lslot[c + j] == sl) m |= 1u << j;
-            done |= m;
-            if (sl < 0) continue;
-            const int rank = p.slots.ranks[sl];
-            const __nv_bfloat16* Brow =
-                p.lora_B + ((static_cast<size_t>(sl) * p.E + e) * p.N + col) * static_cast<size_t>(R);
-#pragma unroll 1
-            for (int r0 = 0; r0 < rank; r0 += 8) {
-              float b[8];   // zero past the rank: the stacked tail is never read
-              if ((R & 7) == 0 && r0 + 8 <= rank) {
-                unpack8(__ldg(reinterpret_cast<const uint4*>(Brow + r0)), b);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) b[i] = (r0 + i < rank) ? bf2f(Brow[r0 + i]) : 0.0f;
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                if ((m >> j) & 1u) {
-                  const float4* vj = reinterpret_cast<const float4*>(v_s + (c + j) * RP8 + r0);
-                  const float4 v0 = vj[0], v1 = vj[1];
-                  val[j] += b[0] * v0.x + b[1] * v0.y + b[2] * v0.z + b[3] * v0.w +
-                            b[4] * v1.x + b[5] * v1.y + b[6] * v1.z + b[7] * v1.w;
-                }
-              }
-            }
-          }
-        }
+        if (lora && col < p.N) lora_expand_chunk(p, lslot, v_s, c, nvalid, e, col, val);
         if (col < p.N) {
           if (p.out_f32 != nullptr) {
             float* o = p.out_f32 + static_cast<size_t>(q0 + c) * p.N + col;

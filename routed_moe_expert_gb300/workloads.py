@@ -170,3 +170,15 @@ def random_small_config(rng, max_T=12, max_E=8) -> LayerConfig:
                        I=64, E=E, top_k=k, ranks=ranks, scalings=scal,
                        slot_mode="uniform_none10",
                        method=int(rng.integers(0, 2)), bias_std=0.1, rsf=float(rng.choice([1.0, 2.5])))
+
+
+def make_routing(T: int, num_experts: int, top_k: int, seed: int = 0):
+    """Routing drawn from outside the layer, for the externally-routed entry: per token
+    top_k distinct global expert ids (uniform, seeded) and positive weights uniform in
+    [0.05, 1).  Returns (ids int32 [T, k], weights float32 [T, k]) on the CPU."""
+    gen = torch.Generator().manual_seed(seed)
+    ids = torch.stack([torch.randperm(num_experts, generator=gen)[:top_k] for _ in range(T)]) if T > 0 \
+        else torch.zeros((0, top_k), dtype=torch.int64)
+    w = torch.rand((T, top_k), generator=gen) * 0.95 + 0.05
+    return ids.to(torch.int32), w.to(torch.float32)
+

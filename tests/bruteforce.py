@@ -61,28 +61,51 @@ def dense_layer(x, logits, w1, w2, top_k, method, bias=None, rsf=1.0, A_gu=None,
         w_all.append(wts)
         weight_of = {e: wv for e, wv in zip(ids, wts)}
         s = -1 if slot_idx is None else int(slot_idx[t])
-        use_lora = (s >= 0 and s < len(ranks) and ranks[s] > 0 and scalings[s] != 0.0)
-        terms = []
-        for e in range(E):                       # dense: every expert
-            g = [bf16_exact(dot(w1[e][n], x[t])) for n in range(2 * I)]
-            if use_lora:
-                r, sc = ranks[s], scalings[s]
-                u = [dot(A_gu[s][e][q], x[t]) for q in range(r)]
-                d = [bf16_exact(sc * dot([B_gu[s][e][n][q] for q in range(r)], u)) for n in range(2 * I)]
-            else:
-                d = [0.0] * (2 * I)
-            a = []
-            for i in range(I):
-                zg = g[i] + d[i]
-                a.append(bf16_exact(zg * sigmoid(zg) * (g[I + i] + d[I + i])))
-            y = [dot(w2[e][h], a) for h in range(H)]
-            if use_lora:
-                v = [dot(A_dn[s][e][q], a) for q in range(r)]
-                dd = [sc * dot([B_dn[s][e][h][q] for q in range(r)], v) for h in range(H)]
-            else:
-                dd = [0.0] * H
-            mask = 1.0 if e in weight_of else 0.0
-            wt = weight_of.get(e, 0.0)
-            terms.append([mask * wt * (y[h] + dd[h]) for h in range(H)])
-        out.append([bf16_exact(math.fsum(terms[e][h] for e in range(E))) for h in range(H)])
+        out.append(_dense_token(x[t], range(E), weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings))
     return out, ids_all, w_all
+
+
+def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings, gid=lambda e: e):
+    """One token through every expert e in `experts` (weight index e, routing id gid(e)),
+    masked by the routing: bf16(fsum over e of mask * w * (y + dd))."""
+    H = len(xt)
+    I = len(w1[0]) // 2
+    use_lora = (s >= 0 and s < len(ranks) and ranks[s] > 0 and scalings[s] != 0.0)
+    terms = []
+    for e in experts:                            # dense: every expert
+        g = [bf16_exact(dot(w1[e][n], xt)) for n in range(2 * I)]
+        if use_lora:
+            r, sc = ranks[s], scalings[s]
+            u = [dot(A_gu[s][e][q], xt) for q in range(r)]
+            d = [bf16_exact(sc * dot([B_gu[s][e][n][q] for q in range(r)], u)) for n in range(2 * I)]
+        else:
+            d = [0.0] * (2 * I)
+        a = []
+        for i in range(I):
+            zg = g[i] + d[i]
+            a.append(bf16_exact(zg * sigmoid(zg) * (g[I + i] + d[I + i])))
+        y = [dot(w2[e][h], a) for h in range(H)]
+        if use_lora:
+            v = [dot(A_dn[s][e][q], a) for q in range(r)]
+            dd = [sc * dot([B_dn[s][e][h][q] for q in range(r)], v) for h in range(H)]
+        else:
+            dd = [0.0] * H
+        mask = 1.0 if gid(e) in weight_of else 0.0
+        wt = weight_of.get(gid(e), 0.0)
+        terms.append([mask * wt * (y[h] + dd[h]) for h in range(H)])
+    return [bf16_exact(math.fsum(terms[i][h] for i in range(len(terms)))) for h in range(H)]
+
+
+def dense_layer_routed(x, ids_all, w_all, local_offset, w1, w2, A_gu=None, B_gu=None, A_dn=None, B_dn=None,
+                       slot_idx=None, ranks=(), scalings=()):
+    """Dense evaluation with the routing given (global ids and weights per token) and only
+    the local experts present: weight index e has global id local_offset + e; a routed
+    pair whose expert is not local contributes nothing."""
+    out = []
+    for t in range(len(x)):
+        weight_of = {int(e): float(wv) for e, wv in zip(ids_all[t], w_all[t])}
+        s = -1 if slot_idx is None else int(slot_idx[t])
+        out.append(_dense_token(x[t], range(len(w1)), weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks,
+                                scalings, gid=lambda e: local_offset + e))
+    return out
+

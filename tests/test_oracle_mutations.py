@@ -24,8 +24,9 @@ MUTATIONS = [
      "silu(g[:, I:] + d[:, I:]) * (g[:, :I] + d[:, :I])"),
     ("delta dropped from gate", "silu(g[:, :I] + d[:, :I])", "silu(g[:, :I])"),
     ("scaling dropped", "d[m] = round_bf16(sc * (u @ B.T))", "d[m] = round_bf16(u @ B.T)"),
-    ("down delta dropped", "contrib = w[ts, js][:, None] * (y + dd)", "contrib = w[ts, js][:, None] * y"),
-    ("routing weight dropped", "contrib = w[ts, js][:, None] * (y + dd)", "contrib = (y + dd)"),
+    ("down delta dropped", "res[(int(ts[i]), int(js[i]))] = (y[i] + dd[i], a[i])",
+     "res[(int(ts[i]), int(js[i]))] = (y[i], a[i])"),
+    ("routing weight dropped", "acc = acc + w[t, j] * rows[(int(t), j)][0]", "acc = acc + rows[(int(t), j)][0]"),
     ("down weight of the wrong expert", "W2 = _f64(w2[e])", "W2 = _f64(w2[(e + 1) % len(w2)])"),
     ("silu sign", "return z / (1.0 + np.exp(-z))", "return z / (1.0 + np.exp(z))"),
     ("rank tail read", "A = _f64(lora_A_gu[s, e])[:r]", "A = _f64(lora_A_gu[s, e])"),
@@ -39,8 +40,13 @@ MUTATIONS = [
      "q = np.ldexp(np.trunc(np.ldexp(x, 8 - e)), e - 8)"),
     ("perm descending in expert", "perm = np.argsort(flat, kind=\"stable\").astype(np.int32)",
      "perm = (flat.size - 1 - np.argsort(flat[::-1], kind=\"stable\")).astype(np.int32)"),
-    ("no-adapter token gets slot 0", "slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)",
-     "slots = np.maximum(np.asarray(slot_idx, dtype=np.int64), 0)"),
+    ("no-adapter token gets slot 0", "slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)\n    inter",
+     "slots = np.maximum(np.asarray(slot_idx, dtype=np.int64), 0)\n    inter"),
+    # the externally routed entry
+    ("packed weight read from the id half", "w = ((u & 0xFFFF) << 16)", "w = ((u >> 16) << 16)"),
+    ("packed weight truncated", "w = round_bf16(np.asarray(topk_weights, dtype=np.float64)).astype(np.float32)",
+     "w = np.asarray(topk_weights, dtype=np.float32)"),
+    ("experts below the local range kept", "local = (lid >= 0) & (lid < E_loc)", "local = lid < E_loc"),
 ]
 
 
@@ -104,6 +110,30 @@ def _hand_check(orc):
     return True
 
 
+def _routed_check(orc, seed):
+    cfg = wl.LayerConfig("mr", T=5, H=16, I=8, E=3, top_k=2, ranks=(2, 4), scalings=(2.0, 0.5),
+                         slot_mode="uniform_none10")
+    inp = wl.make_inputs(cfg, seed=seed)
+    ids, w = wl.make_routing(5, 6, 2, seed=seed)
+    w = w.numpy().astype(np.float64) * 0.7 + 0.013      # not bf16-exact: packing must round
+    from oracle import moe_lora_oracle as good
+    packed = orc.pack_topk(ids.numpy(), w)
+    if not np.array_equal(packed, good.pack_topk(ids.numpy(), w)):
+        return False
+    lora = dict(lora_A_gu=np_(inp["lora_A_gu"]), lora_B_gu=np_(inp["lora_B_gu"]),
+                lora_A_dn=np_(inp["lora_A_dn"]), lora_B_dn=np_(inp["lora_B_dn"]),
+                slot_idx=inp["slot_idx"].numpy(), ranks=inp["ranks"], scalings=inp["scalings"])
+    res = orc.moe_lora_forward_routed(np_(inp["hidden"]), packed, np_(inp["w1"]), np_(inp["w2"]), 2,
+                                      num_experts=6, local_expert_offset=2, **lora)
+    L = lambda a: None if a is None else np.asarray(a, np.float64).tolist()
+    wb = good.round_bf16(w)
+    dense = bf.dense_layer_routed(L(np_(inp["hidden"])), ids.tolist(), wb.tolist(), 2, L(np_(inp["w1"])),
+                                  L(np_(inp["w2"])), A_gu=L(lora["lora_A_gu"]), B_gu=L(lora["lora_B_gu"]),
+                                  A_dn=L(lora["lora_A_dn"]), B_dn=L(lora["lora_B_dn"]),
+                                  slot_idx=lora["slot_idx"].tolist(), ranks=lora["ranks"], scalings=lora["scalings"])
+    return np.array_equal(res["out"], np.array(dense))
+
+
 def _bf16_check(orc):
     vals = np.random.default_rng(0).standard_normal(2000).astype(np.float32)
     return np.array_equal(orc.round_bf16(vals.astype(np.float64)),
@@ -113,6 +143,7 @@ def _bf16_check(orc):
 def test_unmutated_oracle_passes_the_checks():
     from oracle import moe_lora_oracle as good
     assert all(_dense_check(good, s) for s in range(4))
+    assert all(_routed_check(good, s) for s in range(2))
     assert _hand_check(good) and _bf16_check(good)
 
 
@@ -122,7 +153,8 @@ def test_mutant_is_caught(name, old, new):
     m = _mutant(old, new)
     results = []
     for check in (lambda: _bf16_check(m), lambda: _hand_check(m),
-                  *[(lambda s=s: _dense_check(m, s)) for s in range(4)]):
+                  *[(lambda s=s: _dense_check(m, s)) for s in range(4)],
+                  *[(lambda s=s: _routed_check(m, s)) for s in range(2)]):
         try:
             results.append(bool(check()))
         except Exception:

@@ -352,6 +352,108 @@ def test_slot_permutation_permutes_outputs():
     assert len(set(int(s) for s in inp["slot_idx"])) > 2
 
 
+# ---------------------------------------------------------------- externally routed entry
+
+def test_pack_topk_golden():
+    """(expert << 16) | bf16 bits of the weight, written out by hand: 5 with 0.5 is
+    0x00053F00, 1023 with -1.0 is 0x03FFBF80, 2 with 0.1 is 0x00023DCD (0.1 rounds to the
+    bf16 0x3DCD = 0.10009765625); unpacking returns the ids and those bf16 values."""
+    packed = orc.pack_topk(np.array([[5, 1023, 2]]), np.array([[0.5, -1.0, 0.1]]))
+    assert [int(v) & 0xFFFFFFFF for v in packed.reshape(-1)] == [0x00053F00, 0x03FFBF80, 0x00023DCD]
+    ids, w = orc.unpack_topk(packed)
+    assert ids.tolist() == [[5, 1023, 2]]
+    assert w.tolist() == [[0.5, -1.0, 0.10009765625]]
+
+
+def _routed_case(seed, E_loc, E_glob, offset, T=5, k=2):
+    rng = np.random.default_rng(300 + seed)
+    cfg = wl.LayerConfig("rt", T=T, H=16, I=8, E=E_loc, top_k=k, ranks=(4, 2), scalings=(2.0, 0.5),
+                         slot_mode="uniform_none10")
+    inp = wl.make_inputs(cfg, seed=seed)
+    ids, w = wl.make_routing(T, E_glob, k, seed=int(rng.integers(1 << 30)))
+    packed = orc.pack_topk(ids.numpy(), w.numpy())
+    lora = dict(lora_A_gu=np_(inp["lora_A_gu"]), lora_B_gu=np_(inp["lora_B_gu"]),
+                lora_A_dn=np_(inp["lora_A_dn"]), lora_B_dn=np_(inp["lora_B_dn"]),
+                slot_idx=inp["slot_idx"].numpy(), ranks=inp["ranks"], scalings=inp["scalings"])
+    return inp, packed, lora
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_routed_matches_dense_bruteforce_with_dropped_experts(seed):
+    """Given routing over 6 global experts of which 3 are local (offset 2): every token
+    through every local expert, masked by the given routing, exact sums.  Pairs routed
+    to other experts contribute nothing."""
+    inp, packed, lora = _routed_case(seed, E_loc=3, E_glob=6, offset=2)
+    res = orc.moe_lora_forward_routed(np_(inp["hidden"]), packed, np_(inp["w1"]), np_(inp["w2"]), 2,
+                                      num_experts=6, local_expert_offset=2, **lora)
+    gid, w = orc.unpack_topk(packed)
+    dense = bf.dense_layer_routed(
+        _to_lists(np_(inp["hidden"])), gid.tolist(), w.tolist(), 2, _to_lists(np_(inp["w1"])),
+        _to_lists(np_(inp["w2"])), A_gu=_to_lists(lora["lora_A_gu"]), B_gu=_to_lists(lora["lora_B_gu"]),
+        A_dn=_to_lists(lora["lora_A_dn"]), B_dn=_to_lists(lora["lora_B_dn"]),
+        slot_idx=lora["slot_idx"].tolist(), ranks=lora["ranks"], scalings=lora["scalings"])
+    np.testing.assert_array_equal(res["out"], np.array(dense))
+    local = (gid >= 2) & (gid < 5)
+    assert np.array_equal(res["expanded_idx_to_permuted_idx"] >= 0, local.reshape(-1))
+
+
+def test_routed_expert_parallel_partials_sum_to_one_rank():
+    """Two ranks owning experts [0, 3) and [3, 6): their unrounded partial outputs add up
+    to the single-rank output (the all-reduce of the pages' expert-parallel layout)."""
+    inp, packed, lora = _routed_case(7, E_loc=6, E_glob=6, offset=0, T=8, k=3)
+    x, w1, w2 = np_(inp["hidden"]), np_(inp["w1"]), np_(inp["w2"])
+
+    def part(lo, hi):
+        sub = {key: (v[:, lo:hi] if key.startswith("lora_") else v) for key, v in lora.items()}
+        return orc.moe_lora_forward_routed(x, packed, w1[lo:hi], w2[lo:hi], 3, num_experts=6,
+                                           local_expert_offset=lo, **sub)["out_acc"]
+
+    full = part(0, 6)
+    np.testing.assert_allclose(part(0, 3) + part(3, 6), full, rtol=1e-12, atol=1e-14)
+
+
+def test_unfinalized_outputs_refinalize_to_the_output():
+    """do_finalize=False: summing w[t,j] * gemm2_output[idx[t*k+j]] over the pairs with
+    idx >= 0, in j order, gives exactly the do_finalize=True accumulator; dropped pairs
+    have idx -1 and zero activation rows."""
+    inp, packed, lora = _routed_case(3, E_loc=4, E_glob=7, offset=1, T=6, k=3)
+    args = (np_(inp["hidden"]), packed, np_(inp["w1"]), np_(inp["w2"]), 3)
+    fin = orc.moe_lora_forward_routed(*args, num_experts=7, local_expert_offset=1, **lora)
+    nf = orc.moe_lora_forward_routed(*args, num_experts=7, local_expert_offset=1, do_finalize=False, **lora)
+    idx = nf["expanded_idx_to_permuted_idx"]
+    w = nf["expert_weights"]
+    acc = np.zeros_like(fin["out_acc"])
+    for t in range(6):
+        row = np.zeros(acc.shape[1])
+        for j in range(3):
+            if idx[t * 3 + j] >= 0:
+                row = row + w[t, j] * nf["gemm2_output"][idx[t * 3 + j]]
+        acc[t] = row
+    np.testing.assert_array_equal(acc, fin["out_acc"])
+    P_loc = int(fin["expert_offsets"][-1])
+    assert sorted(idx[idx >= 0].tolist()) == list(range(P_loc))
+    assert not np.any(nf["activation"][P_loc:])
+
+
+def test_routed_all_local_equals_logit_routing():
+    """All experts local and the packed routing taken from the logit routing with weights
+    that bf16 holds exactly (constant logits, k = 2: ids 0 and 1, weights 1/2): the same
+    outputs as the logit-routed layer, bit for bit."""
+    cfg = wl.LayerConfig("rt1", T=4, H=16, I=8, E=4, top_k=2, ranks=(4,), scalings=(2.0,))
+    inp = wl.make_inputs(cfg, seed=2)
+    logits = np.zeros((4, 4))
+    ids, w = orc.route(logits, 2)
+    assert ids.tolist() == [[0, 1]] * 4 and w.tolist() == [[0.5, 0.5]] * 4
+    lora = dict(lora_A_gu=np_(inp["lora_A_gu"]), lora_B_gu=np_(inp["lora_B_gu"]),
+                lora_A_dn=np_(inp["lora_A_dn"]), lora_B_dn=np_(inp["lora_B_dn"]),
+                slot_idx=inp["slot_idx"].numpy(), ranks=inp["ranks"], scalings=inp["scalings"])
+    a = orc.moe_lora_forward(np_(inp["hidden"]), logits, np_(inp["w1"]), np_(inp["w2"]), 2, **lora)
+    b = orc.moe_lora_forward_routed(np_(inp["hidden"]), orc.pack_topk(ids, w), np_(inp["w1"]), np_(inp["w2"]),
+                                    2, num_experts=4, **lora)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["perm"], b["perm"])
+
+
 def test_token_subset_rows_equal_full_rows():
     cfg = wl.CONFIGS["tiny"]
     inp = wl.make_inputs(cfg, seed=5)
