@@ -51,7 +51,7 @@ typedef enum {
   MOE_LORA_ERR_WORKSPACE_TOO_SMALL = 3,
   MOE_LORA_ERR_CUDA = 4,               /* a CUDA runtime call failed (see moe_lora_last_cuda_error) */
   MOE_LORA_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out */
-  MOE_LORA_ERR_DEVICE_CHECK = 6        /* device saw a bad value (slot index outside [-1, S)) */
+  MOE_LORA_ERR_DEVICE_CHECK = 6        /* device saw a bad value: a slot index outside [-1, S) or a given expert id >= num_experts */
 } moe_lora_status;
 
 /* Routing methods (vLLM page, TrtLlmBf16LoRAExperts._supports_routing_method). */
@@ -185,6 +185,43 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
    Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
 moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out,
                                  void* workspace, size_t workspace_bytes, moe_lora_stream stream);
+
+/* Routing given from outside the layer (the vLLM API page "fused_moe/experts/
+   trtllm_lora_moe": TrtLlmBf16LoRAExperts.apply packs the top-k as (eid << 16) | w.bf16
+   and calls invoke_routed_moe / trtllm_bf16_routed_moe with local_expert_offset,
+   local_num_experts and do_finalize).  All pointers are device pointers owned by the
+   caller. */
+typedef struct {
+  const int32_t* packed_topk_ids;   /* [T, top_k]: (global expert id << 16) | bf16 bits of the
+                                       routing weight (the id in the high 16 bits, unsigned) */
+  int num_experts;                  /* global expert count: ids must lie in [0, num_experts) */
+  int local_expert_offset;          /* global id of local expert 0; moe_lora_args.E experts are local */
+  int do_finalize;                  /* 1: write `out`; 0: write the unfinalized outputs below */
+  float* gemm2_output;              /* [T*top_k, H] fp32 (do_finalize = 0, required): row q = the
+                                       down output of the pair at permuted position q, unweighted,
+                                       down-LoRA delta included; rows of dropped pairs undefined */
+  moe_lora_bf16* activation_output; /* [T*top_k, I] bf16 (do_finalize = 0, optional, 16-byte
+                                       aligned): the SwiGLU output of each permuted pair */
+  float* expert_weights;            /* [T, top_k] fp32 routing weights (optional) */
+  int32_t* expanded_idx_to_permuted_idx; /* [T*top_k] (required for do_finalize = 0): permuted
+                                       position of expanded pair t*top_k + j, or -1 when its
+                                       expert is not local */
+} moe_lora_routed;
+
+/* The layer with the routing given (see moe_lora_routed).  `a` is used as for
+   moe_lora_forward except that router_logits, correction_bias, routing_method,
+   routed_scaling_factor, n_group, topk_group and the optional routing outputs (topk_ids,
+   topk_weights, expert_offsets, perm, inv_perm) are ignored; a->E counts the local experts
+   (w1, w2 and the LoRA weights hold those only) and a->E + 1 <= 1024.  A pair whose expert
+   is not local is dropped: it adds nothing to `out` (the caller sums the ranks' outputs)
+   and maps to -1.  Local pairs are permuted by local expert, then expanded index; the
+   dropped pairs follow.  An expert id >= num_experts is reported as
+   MOE_LORA_ERR_DEVICE_CHECK by moe_lora_check_status and treated as not local.  The
+   workspace size is moe_lora_workspace_size() of the same shape.
+   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+moe_lora_status moe_lora_forward_routed(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_routed* r,
+                                        moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
+                                        moe_lora_stream stream);
 
 /* Routing + expert alignment that allocates nothing and takes no workspace or handle.
    The pages have no counterpart to this call; it exists for callers that cannot call

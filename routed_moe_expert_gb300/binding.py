@@ -33,7 +33,7 @@ NUM_STAGES = len(STAGES)
 
 EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
-            "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc"]
+            "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed"]
 
 
 class MoELoRAError(RuntimeError):
@@ -66,6 +66,14 @@ class Args(ctypes.Structure):
     ]
 
 
+class Routed(ctypes.Structure):
+    _fields_ = [
+        ("packed_topk_ids", c_void_p), ("num_experts", c_int), ("local_expert_offset", c_int),
+        ("do_finalize", c_int), ("gemm2_output", c_void_p), ("activation_output", c_void_p),
+        ("expert_weights", c_void_p), ("expanded_idx_to_permuted_idx", c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -91,6 +99,8 @@ def lib() -> ctypes.CDLL:
     L.moe_lora_permute.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]
     L.moe_lora_forward.argtypes = [c_void_p, ctypes.POINTER(Args), c_void_p, c_void_p, c_size_t, c_void_p]
     L.moe_lora_check_status.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    L.moe_lora_forward_routed.argtypes = [c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Routed), c_void_p, c_void_p,
+                                          c_size_t, c_void_p]
     for name in EXPORTED:
         if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
             getattr(L, name).restype = c_int
@@ -263,6 +273,55 @@ def moe_lora_forward(handle: Handle, hidden, router_logits, w1, w2, top_k, routi
     _check(st, "moe_lora_forward")
     del keep
     return out
+
+
+def moe_lora_forward_routed(handle: Handle, hidden, packed_topk_ids, w1, w2, top_k, num_experts,
+                            local_expert_offset=0, do_finalize=True, lora_A_gu=None, lora_B_gu=None,
+                            lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(), flags=0,
+                            out=None, gemm2_output=None, activation_output=None, expert_weights=None,
+                            expanded_idx_to_permuted_idx=None, workspace=None, stream=None):
+    """The layer with the routing given as packed top-k words [T, top_k] int32
+    ((global expert << 16) | bf16 weight bits); w1/w2/LoRA hold the local experts
+    [local_expert_offset, local_expert_offset + E).  do_finalize=True returns out [T, H]
+    bf16; False returns a dict of gemm2_output [T*k, H] fp32, activation_output [T*k, I]
+    bf16, expert_weights [T, k] fp32 and expanded_idx_to_permuted_idx [T*k] int32 (-1 for
+    pairs of non-local experts)."""
+    T, H = hidden.shape
+    E, twoI, _ = w1.shape
+    dev = hidden.device
+    a, keep = make_args(hidden, None, w1, w2, top_k, 0, None, 1.0, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn,
+                        slot_idx, ranks, scalings, flags)
+    P = T * int(top_k)
+    r = Routed()
+    r.packed_topk_ids = _ptr(packed_topk_ids, torch.int32, "packed_topk_ids")
+    r.num_experts, r.local_expert_offset, r.do_finalize = int(num_experts), int(local_expert_offset), int(bool(do_finalize))
+    if expert_weights is None:
+        expert_weights = torch.empty((T, top_k), dtype=torch.float32, device=dev)
+    if expanded_idx_to_permuted_idx is None:
+        expanded_idx_to_permuted_idx = torch.empty((P,), dtype=torch.int32, device=dev)
+    r.expert_weights = _ptr(expert_weights, torch.float32, "expert_weights")
+    r.expanded_idx_to_permuted_idx = _ptr(expanded_idx_to_permuted_idx, torch.int32, "expanded_idx_to_permuted_idx")
+    if do_finalize:
+        if out is None:
+            out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    else:
+        if gemm2_output is None:
+            gemm2_output = torch.empty((P, H), dtype=torch.float32, device=dev)
+        if activation_output is None:
+            activation_output = torch.empty((P, twoI // 2), dtype=torch.bfloat16, device=dev)
+        r.gemm2_output = _ptr(gemm2_output, torch.float32, "gemm2_output")
+        r.activation_output = _ptr(activation_output, torch.bfloat16, "activation_output")
+    if workspace is None:
+        workspace = alloc_workspace(T, H, twoI // 2, E, top_k, a.S, a.R, device=dev)
+    st = lib().moe_lora_forward_routed(handle.ptr, ctypes.byref(a), ctypes.byref(r),
+                                       _ptr(out, torch.bfloat16, "out") if do_finalize else None,
+                                       _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "moe_lora_forward_routed")
+    del keep
+    if do_finalize:
+        return out
+    return dict(gemm2_output=gemm2_output, activation_output=activation_output, expert_weights=expert_weights,
+                expanded_idx_to_permuted_idx=expanded_idx_to_permuted_idx)
 
 
 def moe_lora_validate(**kwargs) -> int:

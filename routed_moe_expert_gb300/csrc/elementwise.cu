@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
   for (int j = 0; j < k; ++j) {
+    if (q_s[j] < 0) continue;   // a pair of an expert outside the local range (routed entry)
     const float4 y = __ldg(reinterpret_cast<const float4*>(p.y + static_cast<size_t>(q_s[j]) * p.H) + h4);
     const float w = w_s[j];
     acc.x += w * y.x;

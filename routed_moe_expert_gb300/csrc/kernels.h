@@ -19,7 +19,7 @@ constexpr int kMaxFusedSlots = 8;   // slots the GEMMs can take as extra LoRA MM
 enum : uint32_t {
   kWhereRouteBarrier = 1, kWhereGemmProducer = 2, kWhereGemmMma = 3, kWhereGemmEpilogue = 4,
   kWhereLoraShrinkGu = 5, kWhereLoraExpandGu = 6, kWhereLoraShrinkDn = 7, kWhereFinalize = 8,
-  kWhereLoraShrinkTc = 9,
+  kWhereLoraShrinkTc = 9, kWhereRouteExpert = 10,
 };
 
 struct LoraSlots {
@@ -45,6 +45,12 @@ struct RouteParams {
   int32_t* total;                // [E] scratch
   uint32_t* barrier;             // zeroed before the launch
   uint32_t* status;
+  // method 2 (routing given from outside): packed[t*k + j] = (global expert << 16) | bf16
+  // weight bits.  Experts [local_offset, local_offset + E - 1) map to buckets 0..E-2; every
+  // other pair goes to the last bucket E - 1 and gets inv = -1.
+  const int32_t* packed;         // [T, k]
+  int ext_experts;               // global expert ids must lie in [0, ext_experts)
+  int local_offset;
 };
 cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stream);
 // Routing as one thread-block cluster of route_cluster_ctas(T) CTAs (no global scratch,

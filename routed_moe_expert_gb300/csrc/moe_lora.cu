@@ -59,12 +59,14 @@ Layout layout_for(int T, int H, int I, int E, int k, int R, int S) {
   L.header = take(256);
   L.ids = take(P * 4);
   L.wts = take(P * 4);
-  L.offsets = take((static_cast<size_t>(E) + 1) * 4);
+  const size_t Eb = static_cast<size_t>(E) + 1;   // routing buckets: the experts plus the
+                                                  // dropped pairs of the routed entry
+  L.offsets = take((Eb + 1) * 4);
   L.perm = take(P * 4);
   L.inv = take(P * 4);
-  L.hist = take(static_cast<size_t>(kMaxRouteCtas) * E * 4);
-  L.base = take(static_cast<size_t>(kMaxRouteCtas) * E * 4);
-  L.total = take(static_cast<size_t>(E) * 4);
+  L.hist = take(static_cast<size_t>(kMaxRouteCtas) * Eb * 4);
+  L.base = take(static_cast<size_t>(kMaxRouteCtas) * Eb * 4);
+  L.total = take(Eb * 4);
   L.xp = take(P * H * 2);
   L.g = take(P * 2 * I * 2);
   L.d = take(R > 0 ? P * 2 * I * 2 : 0);
@@ -122,7 +124,7 @@ const char* moe_lora_status_string(moe_lora_status s) {
     case MOE_LORA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MOE_LORA_ERR_CUDA: return "CUDA error";
     case MOE_LORA_ERR_TIMEOUT: return "device-side wait timed out";
-    case MOE_LORA_ERR_DEVICE_CHECK: return "device-side check failed (slot index outside [-1, S))";
+    case MOE_LORA_ERR_DEVICE_CHECK: return "device-side check failed (slot index outside [-1, S) or expert id out of range)";
   }
   return "unknown status";
 }
@@ -223,9 +225,12 @@ moe_lora_status moe_lora_destroy(moe_lora_handle* h) {
 
 namespace {
 
+// Routing + align.  With `ext` the top-k comes packed from outside: E is then the number of
+// buckets (the local experts plus one for the dropped pairs).
 moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, const float* bias, int T, int E,
                               int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
-                              int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+                              int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream,
+                              const moe_lora_routed* ext = nullptr) {
   if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
   // above 512 tokens: a cooperative grid of about 64 tokens per CTA
   int grid = (T + 63) / 64;
@@ -233,12 +238,19 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
   if (grid < 1) grid = 1;
   RouteParams p;
+  std::memset(&p, 0, sizeof(p));
   p.logits = reinterpret_cast<const __nv_bfloat16*>(logits);
   p.bias = bias;
   p.T = T;
   p.E = E;
   p.k = k;
   p.method = method;
+  if (ext != nullptr) {
+    p.method = 2;
+    p.packed = ext->packed_topk_ids;
+    p.ext_experts = ext->num_experts;
+    p.local_offset = ext->local_expert_offset;
+  }
   p.rsf = rsf;
   p.tokens_per_cta = (T + grid - 1) / grid;
   p.ids = ids;
@@ -615,13 +627,15 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
   return MOE_LORA_OK;
 }
 
-moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out, void* workspace,
-                                 size_t workspace_bytes, moe_lora_stream stream_) {
-  moe_lora_status st = moe_lora_validate(a);
-  if (st != MOE_LORA_OK) return st;
-  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
-  if (a->T > 0 && (out == nullptr || !aligned16(out))) return MOE_LORA_ERR_INVALID_ARG;
-  cudaStream_t stream = stream_;
+}  // extern "C"
+
+namespace {
+
+// The forward of moe_lora_forward and moe_lora_forward_routed (`ext` set: the routing
+// comes packed and the output may stay unfinalized).  Arguments are validated.
+moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_routed* ext,
+                             moe_lora_bf16* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  moe_lora_status st = MOE_LORA_OK;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const bool lora = lora_active(a);
   // programmatic launches: each kernel after the routing starts behind its predecessor
@@ -634,22 +648,28 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
 
   const int P = T * k;
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.header);
-  int32_t* ids = a->topk_ids ? a->topk_ids : reinterpret_cast<int32_t*>(ws + L.ids);
-  float* wts = a->topk_weights ? a->topk_weights : reinterpret_cast<float*>(ws + L.wts);
-  int32_t* offsets = a->expert_offsets ? a->expert_offsets : reinterpret_cast<int32_t*>(ws + L.offsets);
-  int32_t* perm = a->perm ? a->perm : reinterpret_cast<int32_t*>(ws + L.perm);
-  int32_t* inv = a->inv_perm ? a->inv_perm : reinterpret_cast<int32_t*>(ws + L.inv);
+  const bool ext_out = ext != nullptr;                       // outputs of the routed entry
+  const bool finalize = ext == nullptr || ext->do_finalize != 0;
+  auto pick = [](auto* user, bool use, auto* own) { return (use && user != nullptr) ? user : own; };
+  int32_t* ids = pick(a->topk_ids, !ext_out, reinterpret_cast<int32_t*>(ws + L.ids));
+  float* wts = ext_out ? pick(ext->expert_weights, true, reinterpret_cast<float*>(ws + L.wts))
+                       : pick(a->topk_weights, true, reinterpret_cast<float*>(ws + L.wts));
+  int32_t* offsets = pick(a->expert_offsets, !ext_out, reinterpret_cast<int32_t*>(ws + L.offsets));
+  int32_t* perm = pick(a->perm, !ext_out, reinterpret_cast<int32_t*>(ws + L.perm));
+  int32_t* inv = ext_out ? pick(ext->expanded_idx_to_permuted_idx, true, reinterpret_cast<int32_t*>(ws + L.inv))
+                         : pick(a->inv_perm, true, reinterpret_cast<int32_t*>(ws + L.inv));
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + L.xp);
   __nv_bfloat16* g = reinterpret_cast<__nv_bfloat16*>(ws + L.g);
   __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(ws + L.d);
   __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
+  if (!finalize && ext->activation_output != nullptr) act = reinterpret_cast<__nv_bfloat16*>(ext->activation_output);
   float* v = reinterpret_cast<float*>(ws + L.v);
-  float* y = reinterpret_cast<float*>(ws + L.y);
+  float* y = finalize ? reinterpret_cast<float*>(ws + L.y) : ext->gemm2_output;
   int32_t* pair_slot = reinterpret_cast<int32_t*>(ws + L.pslot);
 
   prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
-  st = enqueue_route(h, a->router_logits, a->correction_bias, T, E, k, a->routing_method, a->routed_scaling_factor,
-                     ids, wts, offsets, perm, inv, ws, L, stream);
+  st = enqueue_route(h, a->router_logits, a->correction_bias, T, ext ? E + 1 : E, k, a->routing_method,
+                     a->routed_scaling_factor, ids, wts, offsets, perm, inv, ws, L, stream, ext);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_ROUTE, 1, stream);
 
@@ -723,6 +743,7 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
     if (st != MOE_LORA_OK) return st;
   }
 
+  if (!finalize) return MOE_LORA_OK;   // the routed entry's unfinalized outputs are written
   prof(a, MOE_LORA_STAGE_FINALIZE, 0, stream);
   FinalizeParams fp;
   fp.y = y;
@@ -735,6 +756,58 @@ moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe
   ML_CUDA(launch_finalize(fp, stream, pdl), "finalize launch");
   prof(a, MOE_LORA_STAGE_FINALIZE, 1, stream);
   return MOE_LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_lora_status moe_lora_forward(moe_lora_handle* h, const moe_lora_args* a, moe_lora_bf16* out, void* workspace,
+                                 size_t workspace_bytes, moe_lora_stream stream) {
+  moe_lora_status st = moe_lora_validate(a);
+  if (st != MOE_LORA_OK) return st;
+  if (h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  if (a->T > 0 && (out == nullptr || !aligned16(out))) return MOE_LORA_ERR_INVALID_ARG;
+  return forward_impl(h, a, nullptr, out, workspace, workspace_bytes, stream);
+}
+
+moe_lora_status moe_lora_forward_routed(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_routed* r,
+                                        moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
+                                        moe_lora_stream stream) {
+  if (a == nullptr || r == nullptr || h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  // the routing arguments of `a` are not used: check the rest with a stand-in routing
+  moe_lora_args b = *a;
+  b.router_logits = nullptr;
+  b.correction_bias = nullptr;
+  b.routing_method = MOE_LORA_ROUTE_RENORMALIZE;
+  b.n_group = b.topk_group = 1;
+  b.topk_ids = nullptr;
+  b.topk_weights = nullptr;
+  b.expert_offsets = nullptr;
+  b.perm = nullptr;
+  b.inv_perm = nullptr;
+  if (b.T > 0) b.router_logits = reinterpret_cast<const moe_lora_bf16*>(r->packed_topk_ids);   // any non-null
+  moe_lora_status st = moe_lora_validate(&b);
+  if (st != MOE_LORA_OK) return st;
+  if (b.E + 1 > kMaxExperts) return MOE_LORA_ERR_INVALID_ARG;
+  if (r->num_experts < 1 || r->num_experts > 65536 || r->local_expert_offset < 0 ||
+      static_cast<long long>(r->local_expert_offset) + b.E > r->num_experts || b.top_k > r->num_experts)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (r->do_finalize != 0 && r->do_finalize != 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (b.T > 0) {
+    if (r->packed_topk_ids == nullptr || !aligned4(r->packed_topk_ids)) return MOE_LORA_ERR_INVALID_ARG;
+    if (r->do_finalize) {
+      if (out == nullptr || !aligned16(out)) return MOE_LORA_ERR_INVALID_ARG;
+    } else {
+      if (r->gemm2_output == nullptr || !aligned16(r->gemm2_output)) return MOE_LORA_ERR_INVALID_ARG;
+      if (r->expanded_idx_to_permuted_idx == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+      if (r->activation_output != nullptr && !aligned16(r->activation_output)) return MOE_LORA_ERR_INVALID_ARG;
+    }
+    if (r->expert_weights != nullptr && !aligned4(r->expert_weights)) return MOE_LORA_ERR_INVALID_ARG;
+    if (r->expanded_idx_to_permuted_idx != nullptr && !aligned4(r->expanded_idx_to_permuted_idx))
+      return MOE_LORA_ERR_INVALID_ARG;
+  }
+  return forward_impl(h, &b, r, out, workspace, workspace_bytes, stream);
 }
 
 moe_lora_status moe_lora_check_status(const void* workspace, moe_lora_stream stream, uint32_t* detail) {

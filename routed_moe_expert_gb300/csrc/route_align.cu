@@ -155,7 +155,33 @@ template <int EPL, int METHOD, int kTPW>
 MLDEV void select_topk(const RouteParams& p, int t0, int t1, int* ids_s, int* hist_s) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = p.E, k = p.k;
-  if constexpr (METHOD == 0) {
+  if constexpr (METHOD == 2) {
+    // routing given from outside: each pair's global expert and bf16 weight come packed;
+    // experts outside the local range (and invalid ids, which are also reported) go to
+    // the last bucket
+    for (int tb = t0 + warp * kTPW; tb < t1; tb += kRouteWarps * kTPW) {
+#pragma unroll
+      for (int u = 0; u < kTPW; ++u) {
+        const int t = tb + u;
+        if (t >= t1 || lane >= k) continue;
+        const size_t pp = static_cast<size_t>(t) * k + lane;
+        const uint32_t word = static_cast<uint32_t>(p.packed[pp]);
+        const int gid = static_cast<int>(word >> 16);
+        int e = gid - p.local_offset;
+        if (gid >= p.ext_experts) {
+          record_status(p.status, kDevBadSlot, kWhereRouteExpert);
+          e = E - 1;
+        } else if (e < 0 || e >= E - 1) {
+          e = E - 1;
+        }
+        const int pl = (t - t0) * k + lane;   // pair index local to this CTA
+        if (pl < kRouteIdsInSmem) ids_s[pl] = e;
+        p.ids[pp] = e;
+        p.weights[pp] = __uint_as_float((word & 0xffffu) << 16);
+        atomicAdd(&hist_s[e], 1);
+      }
+    }
+  } else if constexpr (METHOD == 0) {
     // Renormalize: packed (logit, id) keys are all distinct, so a round is one hardware
     // maximum over the lanes' list heads and the one lane holding it shifts its list.
     for (int tb = t0 + warp * kTPW; tb < t1; tb += kRouteWarps * kTPW) {
@@ -374,7 +400,7 @@ MLDEV void scatter_pairs(const RouteParams& p, int t0, int t1, const int* ids_s,
       __syncwarp();
       if (valid) {
         p.perm[q] = p0 + pl;
-        p.inv[p0 + pl] = q;
+        p.inv[p0 + pl] = (p.packed != nullptr && e == E - 1) ? -1 : q;   // dropped pair (method 2)
       }
     }
   }
@@ -567,6 +593,7 @@ static cudaError_t launch_epl(const RouteParams& p, int grid, cudaStream_t strea
 
 template <int METHOD>
 static cudaError_t launch_method(const RouteParams& p, int grid, cudaStream_t stream) {
+  if (METHOD == 2) return launch_epl<4, METHOD>(p, grid, stream);   // no candidate lists
   switch (epl_for(p.E)) {
     case 4: return launch_epl<4, METHOD>(p, grid, stream);
     case 8: return launch_epl<8, METHOD>(p, grid, stream);
@@ -595,11 +622,13 @@ int route_max_coop_ctas(int E) {
 }
 
 cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stream) {
+  if (p.method == 2) return launch_method<2>(p, grid, stream);
   return p.method == 1 ? launch_method<1>(p, grid, stream) : launch_method<0>(p, grid, stream);
 }
 
 template <int METHOD>
 static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream) {
+  if (METHOD == 2) return launch_cluster_epl<4, METHOD>(p, ctas, stream);
   switch (epl_for(p.E)) {
     case 4: return launch_cluster_epl<4, METHOD>(p, ctas, stream);
     case 8: return launch_cluster_epl<8, METHOD>(p, ctas, stream);
@@ -611,6 +640,7 @@ static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStr
 
 cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream) {
   if (ctas < 1 || ctas > kRouteClusterMax) return cudaErrorInvalidValue;
+  if (p.method == 2) return launch_cluster_method<2>(p, ctas, stream);
   return p.method == 1 ? launch_cluster_method<1>(p, ctas, stream) : launch_cluster_method<0>(p, ctas, stream);
 }
 

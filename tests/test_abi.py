@@ -106,6 +106,31 @@ def test_forward_rejects_null_handle_without_launching(built_lib):
     assert st == 1
 
 
+@pytest.mark.parametrize("over,rover", [
+    (dict(), dict(num_experts=8, local_expert_offset=1)),          # local range [1, 9) past 8 experts
+    (dict(), dict(num_experts=0)),
+    (dict(), dict(do_finalize=2)),
+    (dict(), dict(packed_topk_ids=None)),
+    (dict(), dict(do_finalize=0, gemm2_output=None)),
+    (dict(), dict(do_finalize=0, expanded_idx_to_permuted_idx=None)),
+    (dict(E=1024), dict(num_experts=2048)),                        # E + 1 routing buckets > 1024
+    (dict(H=96), dict()),                                          # the forward's own shape checks
+])
+def test_forward_routed_rejects_without_launching(built_lib, over, rover):
+    """Host checks of moe_lora_forward_routed return INVALID_ARG before any device work (the
+    handle and device addresses passed here are never dereferenced)."""
+    a, keep = _args(router_logits=None, **over)
+    r = B.Routed()
+    vals = dict(packed_topk_ids=FAKE, num_experts=16, local_expert_offset=0, do_finalize=1,
+                gemm2_output=FAKE, activation_output=None, expert_weights=None, expanded_idx_to_permuted_idx=FAKE)
+    vals.update(rover)
+    for k, v in vals.items():
+        setattr(r, k, v)
+    st = B.lib().moe_lora_forward_routed(ctypes.c_void_p(FAKE), ctypes.byref(a), ctypes.byref(r),
+                                         ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 30, None)
+    assert st == 1
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(B, "_lib", None)
     monkeypatch.setattr(B, "LIB_PATH", "/nonexistent/libmoelora.so")
