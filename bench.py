@@ -429,6 +429,58 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_routed(args):
+    """Auxiliary line: the externally routed entry on the same workload, with the routing
+    given as packed top-k words (seeded, every expert local) and do_finalize as asked.
+    Not the headline metric: it times the layer without its router."""
+    import torch
+    import routed_moe_expert_gb300 as pkg
+    from routed_moe_expert_gb300 import _build
+    from routed_moe_expert_gb300 import workloads as wl
+
+    _build.build()
+    cfg = wl.CONFIGS[args.workload]
+    g = wl.make_inputs(cfg, seed=args.seed, device="cuda")
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    ids, w = wl.make_routing(T, E, k, seed=args.seed + 1)
+    packed = wl.packed_routing_words(ids, w).cuda()
+    h = pkg.Handle(0)
+    ws = pkg.alloc_workspace(T, H, I, E, k, cfg.S, cfg.R)
+    fin = args.routed == "finalize"
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    extra = {} if fin else dict(gemm2_output=torch.empty((T * k, H), dtype=torch.float32, device="cuda"),
+                                activation_output=torch.empty((T * k, I), dtype=torch.bfloat16, device="cuda"))
+
+    def fwd():
+        pkg.moe_lora_forward_routed(h, g["hidden"], packed, g["w1"], g["w2"], k, E, do_finalize=fin,
+                                    lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
+                                    lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=cfg.ranks,
+                                    scalings=cfg.scalings, flags=args.flags, out=out, workspace=ws, **extra)
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    st, word = pkg.moe_lora_check_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {word:#x}")
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        fwd()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sec = t0.elapsed_time(t1) / 1e3
+    print(json.dumps({
+        "metric": METRIC, "value": T * args.steps / sec, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3 / args.steps, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} through moe_lora_forward_routed (packed top-k, every expert "
+                               f"local, do_finalize={int(fin)})", "T": T, "H": H, "I": I, "E": E, "top_k": k},
+        "entry": "routed"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,11 +495,15 @@ def main():
     ap.add_argument("--ref-steps", type=int, default=5)
     ap.add_argument("--flags", type=int, default=0, help="extra moe_lora_forward flags (e.g. 8: unfused LoRA)")
     ap.add_argument("--stage-times", action="store_true", help="add per-stage device times (us) to the line")
+    ap.add_argument("--routed", choices=["finalize", "unfinalized"], default=None,
+                    help="time the externally routed entry instead (auxiliary line, not the headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.routed:
+        run_routed(args)
     else:
         run_gpu(args)
 

@@ -182,3 +182,12 @@ def make_routing(T: int, num_experts: int, top_k: int, seed: int = 0):
     w = torch.rand((T, top_k), generator=gen) * 0.95 + 0.05
     return ids.to(torch.int32), w.to(torch.float32)
 
+
+def packed_routing_words(ids: torch.Tensor, weights: torch.Tensor) -> torch.Tensor:
+    """The routed entry's input encoding of a given routing: int32 words with the expert id
+    in the high 16 bits and the weight's bfloat16 bit pattern (torch's round-to-nearest
+    conversion) in the low 16 bits."""
+    bits = weights.to(torch.bfloat16).view(torch.int16).to(torch.int64) & 0xFFFF
+    v = (ids.to(torch.int64) << 16) | bits
+    v = torch.where(v >= 2 ** 31, v - 2 ** 32, v)      # the same 32 bits as a signed int32
+    return v.to(torch.int32)

@@ -365,6 +365,15 @@ def test_pack_topk_golden():
     assert w.tolist() == [[0.5, -1.0, 0.10009765625]]
 
 
+def test_pack_topk_equals_the_input_encoding():
+    """The oracle's packing (numpy, bf16 by frexp/rint) and the seeded input generator's
+    (torch bfloat16 conversion and int64 shifts) agree on every word, ids up to 65535."""
+    ids, w = wl.make_routing(200, 40000, 8, seed=4)
+    ids[0, 0] = 65535
+    w[1, 0] = 0.1
+    np.testing.assert_array_equal(orc.pack_topk(ids.numpy(), w.numpy()), wl.packed_routing_words(ids, w).numpy())
+
+
 def _routed_case(seed, E_loc, E_glob, offset, T=5, k=2):
     rng = np.random.default_rng(300 + seed)
     cfg = wl.LayerConfig("rt", T=T, H=16, I=8, E=E_loc, top_k=k, ranks=(4, 2), scalings=(2.0, 0.5),
