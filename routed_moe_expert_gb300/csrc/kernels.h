@@ -92,6 +92,7 @@ struct GemmParams {
   const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
 };
+constexpr int kMaxGemmSmem = 227 * 1024;   // dynamic shared memory a CTA may have
 int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused);
 int gemm_stage_bytes(int bn);
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl = false);

@@ -296,7 +296,9 @@ int pick_bn(long long P, int E) {
 // Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
 // room for the side-stream LoRA kernel that runs beside it; the down GEMM runs alone.
 int pick_stages(int bn, int E, int lora_R, int act_fused, bool alone) {
-  const int budget = (bn <= 32 && !alone ? 160 : 200) * 1024;
+  // Wide tiles (prefill) keep too few stages in flight to cover the load latency at 200 KB,
+  // so they take the whole 227 KB a CTA may have.
+  const int budget = bn >= 64 ? kMaxGemmSmem : (bn <= 32 && !alone ? 160 : 200) * 1024;
   const int fixed = gemm_smem_bytes(bn, 0, E, lora_R, act_fused);
   int s = (budget - fixed) / (gemm_stage_bytes(bn) + 16);
   if (s > 16) s = 16;
@@ -582,7 +584,12 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     dn.pair_slot = pair_slot;
     dn.slots = slots;
   }
-  st = enqueue_gemm(h, dn, a->w2, act, P, bn, stream, pdl);
+  // the epilogue's staged LoRA rows grow with the tile: narrow it until two stages fit
+  int bn_dn = bn;
+  while (!fused && lora && bn_dn > 16 &&
+         gemm_smem_bytes(bn_dn, 2, E, R, 0) > kMaxGemmSmem)
+    bn_dn >>= 1;
+  st = enqueue_gemm(h, dn, a->w2, act, P, bn_dn, stream, pdl);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
 

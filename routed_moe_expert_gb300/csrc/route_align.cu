@@ -483,8 +483,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
 // CTA reads all CTAs' counts (C x E loads), so each forms the expert offsets itself and
 // its own per-expert base, the prefix of the counts of the CTAs before it.
 // ---------------------------------------------------------------------------------
-MLDEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-MLDEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 MLDEV int ld_dsmem(const int* local, uint32_t rank) {   // the same variable in CTA `rank`
   uint32_t remote;
@@ -494,11 +492,6 @@ MLDEV int ld_dsmem(const int* local, uint32_t rank) {   // the same variable in 
   return v;
 }
 
-MLDEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 
 template <int EPL, int METHOD>
 __global__ void __launch_bounds__(kRouteThreads) route_cluster_kernel(const RouteParams p) {
