@@ -39,6 +39,10 @@ Readings of points the pages leave open (each also listed in the design notes):
     logits followed by renormalising the top k gives the same numbers).
   * DeepSeekV3 with n_group = topk_group = 1: scores s = sigmoid(logit), select on
     s + correction_bias, weights = s_sel / sum(s_sel) * routed_scaling_factor.
+  * Shared-outer LoRA (sglang PR #28466 section 2: "shared A on gate_up / shared B on
+    down", one weight set for every expert): lora_A_gu is [S, 1, R, H] and lora_B_dn
+    [S, 1, H, R]; the gate_up expand (B_gu) and the down shrink (A_dn) stay per expert, and
+    every other rule (slots, ranks, scaling, rounding) is that of the per-expert mode.
   * Externally routed entry (moe_lora_forward_routed): the packed word is the expert id
     in the high 16 bits and the bf16 bits of the routing weight (nearest even) in the low
     16 bits; pairs of experts outside the local range are dropped (they add nothing and
@@ -188,11 +192,12 @@ def _f64(a):
 
 
 def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slots,
-             ranks, scalings, lora_off, inter, local=None):
+             ranks, scalings, lora_off, inter, local=None, shared_outer=False):
     """Per-pair expert math for the pairs of tokens `tok` (see moe_lora_forward).  With
     `local` (a bool mask [T, k]) only those pairs are evaluated.  Returns
     {(t, j): (y + dd, a)} in float64 (a holds bf16 values)."""
     S = len(ranks)
+    eo = (lambda e: 0) if shared_outer else (lambda e: e)   # expert index of A_gu and B_dn
     res = {}
     pair_t = np.repeat(tok, top_k)
     pair_j = np.tile(np.arange(top_k), tok.size)
@@ -219,7 +224,7 @@ def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lor
                 m = np.nonzero(slots[ts] == s)[0]
                 if m.size == 0 or r == 0 or sc == 0.0:
                     continue
-                A = _f64(lora_A_gu[s, e])[:r]                    # [r, H]
+                A = _f64(lora_A_gu[s, eo(e)])[:r]                # [r, H]
                 B = _f64(lora_B_gu[s, e])[:, :r]                 # [2I, r]
                 u = xe[m] @ A.T                                  # [m, r]
                 d[m] = round_bf16(sc * (u @ B.T))
@@ -229,7 +234,7 @@ def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lor
         dd = np.zeros_like(y)
         for s, r, sc, m in lora_rows:
             A = _f64(lora_A_dn[s, e])[:r]                        # [r, I]
-            B = _f64(lora_B_dn[s, e])[:, :r]                     # [H, r]
+            B = _f64(lora_B_dn[s, eo(e)])[:, :r]                 # [H, r]
             v = a[m] @ A.T                                       # [m, r]
             dd[m] = sc * (v @ B.T)
         for i in range(sel.size):
@@ -257,7 +262,7 @@ def moe_lora_forward(hidden, router_logits, w1, w2, top_k, method=RENORMALIZE,
                      correction_bias=None, routed_scaling_factor=1.0,
                      lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
                      slot_idx=None, ranks=(), scalings=(), lora_off=False,
-                     tokens=None, keep_intermediates=False):
+                     tokens=None, keep_intermediates=False, shared_outer=False):
     """Forward of the routed MoE expert layer with per-expert LoRA.
 
     The stages are those of sglang PR #28466 ("Files changed", launcher row, and
@@ -295,7 +300,7 @@ def moe_lora_forward(hidden, router_logits, w1, w2, top_k, method=RENORMALIZE,
     slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
     inter = {} if keep_intermediates else None
     rows = _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slots,
-                    ranks, scalings, lora_off, inter)
+                    ranks, scalings, lora_off, inter, shared_outer=shared_outer)
     # finalize: out[t] = bf16(sum over j = 0..k-1, in that order, of w[t,j] * (y + dd))
     out_acc = _finalize(tok, top_k, H, w, rows)
     res = dict(out=round_bf16(out_acc), topk_ids=ids, topk_weights=w,
@@ -332,7 +337,7 @@ def unpack_topk(packed):
 def moe_lora_forward_routed(hidden, packed_topk_ids, w1, w2, top_k, num_experts, local_expert_offset=0,
                             lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
                             slot_idx=None, ranks=(), scalings=(), lora_off=False, do_finalize=True,
-                            tokens=None):
+                            tokens=None, shared_outer=False):
     """The layer with routing given from outside (vLLM API page "fused_moe/experts/
     trtllm_lora_moe": invoke_routed_moe / trtllm_bf16_routed_moe with packed_topk_ids,
     local_expert_offset, local_num_experts and do_finalize).
@@ -368,7 +373,7 @@ def moe_lora_forward_routed(hidden, packed_topk_ids, w1, w2, top_k, num_experts,
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
     rows = _experts(x, np.where(local, lid, 0), w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn,
-                    lora_B_dn, slots, ranks, scalings, lora_off, None, local=local)
+                    lora_B_dn, slots, ranks, scalings, lora_off, None, local=local, shared_outer=shared_outer)
     res = dict(topk_ids=gid, topk_weights=w, expert_offsets=offsets[:E_loc + 1], perm=perm,
                expanded_idx_to_permuted_idx=idx_map, local=local, tokens=tok)
     if do_finalize:

@@ -45,6 +45,7 @@ class LayerConfig:
     zipf_bias: bool = False          # per-expert bias 1.5*log(1/rank_e) on the logits
     bias_std: float = 0.0            # DeepSeekV3 correction bias ~ N(0, bias_std)
     rsf: float = 1.0                 # routed_scaling_factor (DeepSeekV3)
+    shared_outer: bool = False       # one A_gu and one B_dn per slot ([S, 1, ...]) for all experts
 
     @property
     def S(self) -> int:
@@ -118,10 +119,11 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device: str = "cpu",
     w1 = _randn((E, 2 * I, H), 1.0 / math.sqrt(H), gen, device)
     w2 = _randn((E, H, I), 1.0 / math.sqrt(I), gen, device)
     if S > 0:
-        A_gu = _randn((S, E, R, H), 1.0 / math.sqrt(H), gen, device)
+        Eo = 1 if cfg.shared_outer else E   # experts of the shared-outer weights (A_gu, B_dn)
+        A_gu = _randn((S, Eo, R, H), 1.0 / math.sqrt(H), gen, device)
         B_gu = _randn((S, E, 2 * I, R), 0.02, gen, device)
         A_dn = _randn((S, E, R, I), 1.0 / math.sqrt(I), gen, device)
-        B_dn = _randn((S, E, H, R), 0.02, gen, device)
+        B_dn = _randn((S, Eo, H, R), 0.02, gen, device)
         if nan_rank_tail:
             for s, r in enumerate(cfg.ranks):
                 if r < R:
@@ -142,6 +144,7 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device: str = "cpu",
         correction_bias=corr, slot_idx=slot_idx.to(device),
         ranks=list(cfg.ranks), scalings=[float(s) for s in cfg.scalings],
         T=T, H=H, I=I, E=E, top_k=k, S=S, R=R, method=cfg.method, rsf=cfg.rsf,
+        shared_outer=cfg.shared_outer,
     )
 
 

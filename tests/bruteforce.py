@@ -36,7 +36,7 @@ def topk_bruteforce(keys, k):
 
 
 def dense_layer(x, logits, w1, w2, top_k, method, bias=None, rsf=1.0, A_gu=None, B_gu=None,
-                A_dn=None, B_dn=None, slot_idx=None, ranks=(), scalings=(), keys_fn=None):
+                A_dn=None, B_dn=None, slot_idx=None, ranks=(), scalings=(), keys_fn=None, shared_outer=False):
     """Dense evaluation on nested lists.  `keys_fn(logit_row)` gives the DeepSeekV3
     selection keys (the float32 key definition is pinned separately)."""
     T, H = len(x), len(x[0])
@@ -61,13 +61,16 @@ def dense_layer(x, logits, w1, w2, top_k, method, bias=None, rsf=1.0, A_gu=None,
         w_all.append(wts)
         weight_of = {e: wv for e, wv in zip(ids, wts)}
         s = -1 if slot_idx is None else int(slot_idx[t])
-        out.append(_dense_token(x[t], range(E), weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings))
+        out.append(_dense_token(x[t], range(E), weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings,
+                                shared_outer=shared_outer))
     return out, ids_all, w_all
 
 
-def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings, gid=lambda e: e):
+def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings, gid=lambda e: e,
+                 shared_outer=False):
     """One token through every expert e in `experts` (weight index e, routing id gid(e)),
-    masked by the routing: bf16(fsum over e of mask * w * (y + dd))."""
+    masked by the routing: bf16(fsum over e of mask * w * (y + dd)).  shared_outer: A_gu
+    and B_dn hold one weight set per slot (index 0) used by every expert."""
     H = len(xt)
     I = len(w1[0]) // 2
     use_lora = (s >= 0 and s < len(ranks) and ranks[s] > 0 and scalings[s] != 0.0)
@@ -76,7 +79,7 @@ def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, rank
         g = [bf16_exact(dot(w1[e][n], xt)) for n in range(2 * I)]
         if use_lora:
             r, sc = ranks[s], scalings[s]
-            u = [dot(A_gu[s][e][q], xt) for q in range(r)]
+            u = [dot(A_gu[s][0 if shared_outer else e][q], xt) for q in range(r)]
             d = [bf16_exact(sc * dot([B_gu[s][e][n][q] for q in range(r)], u)) for n in range(2 * I)]
         else:
             d = [0.0] * (2 * I)
@@ -87,7 +90,7 @@ def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, rank
         y = [dot(w2[e][h], a) for h in range(H)]
         if use_lora:
             v = [dot(A_dn[s][e][q], a) for q in range(r)]
-            dd = [sc * dot([B_dn[s][e][h][q] for q in range(r)], v) for h in range(H)]
+            dd = [sc * dot([B_dn[s][0 if shared_outer else e][h][q] for q in range(r)], v) for h in range(H)]
         else:
             dd = [0.0] * H
         mask = 1.0 if gid(e) in weight_of else 0.0

@@ -29,7 +29,7 @@ MUTATIONS = [
     ("routing weight dropped", "acc = acc + w[t, j] * rows[(int(t), j)][0]", "acc = acc + rows[(int(t), j)][0]"),
     ("down weight of the wrong expert", "W2 = _f64(w2[e])", "W2 = _f64(w2[(e + 1) % len(w2)])"),
     ("silu sign", "return z / (1.0 + np.exp(-z))", "return z / (1.0 + np.exp(z))"),
-    ("rank tail read", "A = _f64(lora_A_gu[s, e])[:r]", "A = _f64(lora_A_gu[s, e])"),
+    ("rank tail read", "A = _f64(lora_A_gu[s, eo(e)])[:r]", "A = _f64(lora_A_gu[s, eo(e)])"),
     ("tie to higher id", "order = np.argsort(-keys, axis=1, kind=\"stable\")",
      "order = (keys.shape[1] - 1 - np.argsort(-keys[:, ::-1], axis=1, kind=\"stable\"))"),
     ("softmax over all experts, not renormalised", "w = ex / ex.sum(axis=1, keepdims=True)",
@@ -47,6 +47,11 @@ MUTATIONS = [
     ("packed weight truncated", "w = round_bf16(np.asarray(topk_weights, dtype=np.float64)).astype(np.float32)",
      "w = np.asarray(topk_weights, dtype=np.float32)"),
     ("experts below the local range kept", "local = (lid >= 0) & (lid < E_loc)", "local = lid < E_loc"),
+    # shared-outer LoRA
+    ("shared-outer weights read per expert", "eo = (lambda e: 0) if shared_outer else (lambda e: e)",
+     "eo = lambda e: e"),
+    ("shared-outer down LoRA from the per-expert weights", "B = _f64(lora_B_dn[s, eo(e)])[:, :r]",
+     "B = _f64(lora_B_dn[s, 0])[:, :r]"),
 ]
 
 
@@ -134,6 +139,24 @@ def _routed_check(orc, seed):
     return np.array_equal(res["out"], np.array(dense))
 
 
+def _shared_check(orc, seed):
+    cfg = wl.LayerConfig("ms", T=5, H=16, I=8, E=3, top_k=2, ranks=(2, 4), scalings=(2.0, 0.5),
+                         slot_mode="uniform_none10", shared_outer=(seed % 2 == 0))
+    inp = wl.make_inputs(cfg, seed=seed)
+    L = lambda a: None if a is None else np.asarray(a, np.float64).tolist()
+    lora = dict(lora_A_gu=np_(inp["lora_A_gu"]), lora_B_gu=np_(inp["lora_B_gu"]),
+                lora_A_dn=np_(inp["lora_A_dn"]), lora_B_dn=np_(inp["lora_B_dn"]))
+    res = orc.moe_lora_forward(np_(inp["hidden"]), np_(inp["router_logits"]), np_(inp["w1"]), np_(inp["w2"]), 2,
+                               slot_idx=inp["slot_idx"].numpy(), ranks=inp["ranks"], scalings=inp["scalings"],
+                               shared_outer=cfg.shared_outer, **lora)
+    dense, _, _ = bf.dense_layer(L(np_(inp["hidden"])), L(np_(inp["router_logits"])), L(np_(inp["w1"])),
+                                 L(np_(inp["w2"])), 2, 0, A_gu=L(lora["lora_A_gu"]), B_gu=L(lora["lora_B_gu"]),
+                                 A_dn=L(lora["lora_A_dn"]), B_dn=L(lora["lora_B_dn"]),
+                                 slot_idx=inp["slot_idx"].tolist(), ranks=inp["ranks"], scalings=inp["scalings"],
+                                 shared_outer=cfg.shared_outer)
+    return np.array_equal(res["out"], np.array(dense))
+
+
 def _bf16_check(orc):
     vals = np.random.default_rng(0).standard_normal(2000).astype(np.float32)
     return np.array_equal(orc.round_bf16(vals.astype(np.float64)),
@@ -144,6 +167,7 @@ def test_unmutated_oracle_passes_the_checks():
     from oracle import moe_lora_oracle as good
     assert all(_dense_check(good, s) for s in range(4))
     assert all(_routed_check(good, s) for s in range(2))
+    assert all(_shared_check(good, s) for s in range(2))
     assert _hand_check(good) and _bf16_check(good)
 
 
@@ -154,7 +178,8 @@ def test_mutant_is_caught(name, old, new):
     results = []
     for check in (lambda: _bf16_check(m), lambda: _hand_check(m),
                   *[(lambda s=s: _dense_check(m, s)) for s in range(4)],
-                  *[(lambda s=s: _routed_check(m, s)) for s in range(2)]):
+                  *[(lambda s=s: _routed_check(m, s)) for s in range(2)],
+                  *[(lambda s=s: _shared_check(m, s)) for s in range(2)]):
         try:
             results.append(bool(check()))
         except Exception:

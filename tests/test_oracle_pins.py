@@ -352,6 +352,47 @@ def test_slot_permutation_permutes_outputs():
     assert len(set(int(s) for s in inp["slot_idx"])) > 2
 
 
+# ---------------------------------------------------------------- shared-outer LoRA
+
+@pytest.mark.parametrize("seed", range(4))
+def test_shared_outer_matches_dense_bruteforce(seed):
+    """One A_gu and one B_dn per slot for every expert: the dense brute force (every token
+    through every expert, exact sums) gives the same bf16 outputs."""
+    rng = np.random.default_rng(400 + seed)
+    base = wl.random_small_config(rng, max_T=6, max_E=5)
+    cfg = wl.LayerConfig("so", T=base.T, H=16, I=8, E=base.E, top_k=base.top_k, ranks=(4, 2),
+                         scalings=(2.0, 0.5), slot_mode="uniform_none10", shared_outer=True)
+    inp = wl.make_inputs(cfg, seed=seed)
+    assert tuple(inp["lora_A_gu"].shape[:2]) == (2, 1) and tuple(inp["lora_B_dn"].shape[:2]) == (2, 1)
+    lora = dict(lora_A_gu=np_(inp["lora_A_gu"]), lora_B_gu=np_(inp["lora_B_gu"]),
+                lora_A_dn=np_(inp["lora_A_dn"]), lora_B_dn=np_(inp["lora_B_dn"]))
+    res = orc.moe_lora_forward(np_(inp["hidden"]), np_(inp["router_logits"]), np_(inp["w1"]), np_(inp["w2"]),
+                               cfg.top_k, slot_idx=inp["slot_idx"].numpy(), ranks=inp["ranks"],
+                               scalings=inp["scalings"], shared_outer=True, **lora)
+    dense, _, _ = bf.dense_layer(
+        _to_lists(np_(inp["hidden"])), _to_lists(np_(inp["router_logits"])), _to_lists(np_(inp["w1"])),
+        _to_lists(np_(inp["w2"])), cfg.top_k, 0, A_gu=_to_lists(lora["lora_A_gu"]),
+        B_gu=_to_lists(lora["lora_B_gu"]), A_dn=_to_lists(lora["lora_A_dn"]), B_dn=_to_lists(lora["lora_B_dn"]),
+        slot_idx=inp["slot_idx"].tolist(), ranks=inp["ranks"], scalings=inp["scalings"], shared_outer=True)
+    np.testing.assert_array_equal(res["out"], np.array(dense))
+
+
+def test_shared_outer_equals_per_expert_with_copies():
+    """Shared-outer is the per-expert layer whose A_gu and B_dn are the same for every
+    expert: copying the shared weights to every expert gives the same bits."""
+    cfg = wl.LayerConfig("so2", T=7, H=16, I=8, E=4, top_k=2, ranks=(4,), scalings=(1.5,), shared_outer=True)
+    inp = wl.make_inputs(cfg, seed=3)
+    E = cfg.E
+    A_gu, B_dn = np_(inp["lora_A_gu"]), np_(inp["lora_B_dn"])
+    common = dict(lora_B_gu=np_(inp["lora_B_gu"]), lora_A_dn=np_(inp["lora_A_dn"]), slot_idx=inp["slot_idx"].numpy(),
+                  ranks=inp["ranks"], scalings=inp["scalings"])
+    args = (np_(inp["hidden"]), np_(inp["router_logits"]), np_(inp["w1"]), np_(inp["w2"]), 2)
+    a = orc.moe_lora_forward(*args, lora_A_gu=A_gu, lora_B_dn=B_dn, shared_outer=True, **common)
+    b = orc.moe_lora_forward(*args, lora_A_gu=np.repeat(A_gu, E, axis=1), lora_B_dn=np.repeat(B_dn, E, axis=1),
+                             **common)
+    np.testing.assert_array_equal(a["out"], b["out"])
+
+
 # ---------------------------------------------------------------- externally routed entry
 
 def test_pack_topk_golden():
