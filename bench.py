@@ -164,7 +164,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
 
     def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
-        flags |= args.flags
+        flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
         return pkg.moe_lora_forward(
             h, g["hidden"] if hidden is None else hidden, g["router_logits"] if logits is None else logits,
             g["w1"], g["w2"], k, routing_method=cfg.method, correction_bias=g["correction_bias"],
@@ -192,7 +192,11 @@ def run_gpu(args):
         fwd(outputs=dict(topk_ids=ids_out))
         ids_np = ids_out.cpu().numpy()
         pairs = {(int(slots[t]), int(e)) for t in range(T) for e in ids_np[t] if slots[t] >= 0}
-        lora_blocks = sum(2 * cfg.ranks[s] * (2 * H + 3 * I) for s, _ in pairs)
+        if cfg.shared_outer:   # per (slot, expert): B_gu and A_dn; per slot: A_gu and B_dn
+            lora_blocks = sum(2 * cfg.ranks[s] * (2 * I + I) for s, _ in pairs) + \
+                sum(2 * cfg.ranks[s] * (H + H) for s in {s for s, _ in pairs})
+        else:
+            lora_blocks = sum(2 * cfg.ranks[s] * (2 * H + 3 * I) for s, _ in pairs)
     io_bytes = T * H * 2 * 2 + T * E * 2
     step_bytes = touched * w_bytes_expert + lora_blocks + io_bytes
     step_flops = 2 * 3 * H * I * P + sum(2 * cfg.ranks[max(int(slots[t]), 0)] * (2 * H + 3 * I) * k
@@ -372,7 +376,8 @@ def _oracle_call(cfg, o, tokens):
     from oracle import moe_lora_oracle as orc
     return orc.moe_lora_forward(o["hidden"], o["router_logits"], o["w1"], o["w2"], cfg.top_k, cfg.method,
                                 o["correction_bias"], cfg.rsf, o["lora_A_gu"], o["lora_B_gu"], o["lora_A_dn"],
-                                o["lora_B_dn"], o["slot_idx"], cfg.ranks, cfg.scalings, tokens=tokens)
+                                o["lora_B_dn"], o["slot_idx"], cfg.ranks, cfg.scalings, tokens=tokens,
+                                shared_outer=cfg.shared_outer)
 
 
 def cpu_baseline(cfg, inp, args, budget_s: float = None) -> dict:
@@ -455,7 +460,8 @@ def run_routed(args):
         pkg.moe_lora_forward_routed(h, g["hidden"], packed, g["w1"], g["w2"], k, E, do_finalize=fin,
                                     lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
                                     lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=cfg.ranks,
-                                    scalings=cfg.scalings, flags=args.flags, out=out, workspace=ws, **extra)
+                                    scalings=cfg.scalings, out=out, workspace=ws, **extra,
+                                    flags=args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0))
 
     for _ in range(args.warmup):
         fwd()

@@ -66,6 +66,7 @@ typedef enum {
 #define MOE_LORA_FLAG_FORCE_TWO_STREAM    4u /* fork even above 256 tokens */
 #define MOE_LORA_FLAG_UNFUSED_LORA        8u /* down-LoRA expand in the epilogue (see forward) */
 #define MOE_LORA_FLAG_NO_PDL             16u /* launch every kernel fully behind its predecessor */
+#define MOE_LORA_FLAG_SHARED_OUTER       32u /* shared-outer LoRA: lora_A_gu [S,1,R,H], lora_B_dn [S,1,H,R] */
 
 /* Stages that moe_lora_args.prof_events can bracket (two events per stage). */
 enum {
@@ -96,10 +97,10 @@ typedef struct {
   const float* correction_bias;       /* [E], DeepSeekV3 only, else NULL                   */
   const moe_lora_bf16* w1;            /* [E, 2I, H]: rows [0,I) gate, [I,2I) up            */
   const moe_lora_bf16* w2;            /* [E, H, I]                                         */
-  const moe_lora_bf16* lora_A_gu;     /* [S, E, R, H]  rows r < ranks[s] are read          */
+  const moe_lora_bf16* lora_A_gu;     /* [S, E, R, H] ([S, 1, R, H] shared-outer); rows r < ranks[s] read */
   const moe_lora_bf16* lora_B_gu;     /* [S, E, 2I, R] cols r < ranks[s] are read          */
   const moe_lora_bf16* lora_A_dn;     /* [S, E, R, I]                                      */
-  const moe_lora_bf16* lora_B_dn;     /* [S, E, H, R]                                      */
+  const moe_lora_bf16* lora_B_dn;     /* [S, E, H, R] ([S, 1, H, R] shared-outer)            */
   const int32_t* slot_idx;            /* [T], slot of each token, -1 = no adapter          */
   const int32_t* h_ranks;             /* [S] host, 0 <= ranks[s] <= R                      */
   const float* h_scalings;            /* [S] host, 0 disables the slot                     */

@@ -83,7 +83,8 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
     done |= m;
     if (sl < 0) continue;
     const int rank = p.slots.ranks[sl];
-    const __nv_bfloat16* Brow = p.lora_B + ((static_cast<size_t>(sl) * p.E + e) * p.N + feat) * static_cast<size_t>(R);
+    const size_t be = p.lora_b_e1 ? static_cast<size_t>(sl) : static_cast<size_t>(sl) * p.E + e;
+    const __nv_bfloat16* Brow = p.lora_B + (be * p.N + feat) * static_cast<size_t>(R);
 #pragma unroll 1
     for (int r0 = 0; r0 < rank; r0 += 8) {
       float b[8];   // zero past the rank: the stacked tail is never read
@@ -269,11 +270,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           // published before the tile's last main stage arrives (arrive.expect_tx releases it);
           // the MMA warp reads it after consuming that stage
           tile_slot_ring[it_tile % kTileRing] = smask;
+          const int lb_off = p.lora_b_e1 ? e * p.N : 0;   // a shared B has one expert's rows
           if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xr);
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
             if (!((smask >> sl) & 1u)) continue;
             for (int kb = 0; ok && kb < p.lora_kb; ++kb)
-              ok = issue(&p.tmap_lb[sl], wr0, wr1, kb * 64, &p.tmap_lu, sl * p.P + xr);
+              ok = issue(&p.tmap_lb[sl], wr0 - lb_off, wr1 - lb_off, kb * 64, &p.tmap_lu, sl * p.P + xr);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;

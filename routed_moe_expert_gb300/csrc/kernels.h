@@ -88,7 +88,8 @@ struct GemmParams {
   // out[q, h] += sum_{r<ranks[s]} lora_B[s, e, h, r] * lora_v[q, r]   (s = pair_slot[q])
   // lora_v holds scaling[s] * (down-LoRA shrink), written with pair_slot by the shrink.
   const float* lora_v;           // [P, R] or null
-  const __nv_bfloat16* lora_B;   // [S, E, N, R]
+  const __nv_bfloat16* lora_B;   // [S, E, N, R], or [S, 1, N, R] with lora_b_e1
+  int lora_b_e1;                 // 1: the LoRA B (epilogue or fused stages) is one set per slot
   const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
 };
@@ -125,8 +126,9 @@ struct LoraParams {
   const int32_t* slot_idx;       // [T]
   const int32_t* offsets;        // [E + 1]
   int k, P, K, E, N;             // N: expand output width (2I)
-  const __nv_bfloat16* A;        // [S, E, R, K]
-  const __nv_bfloat16* B;        // [S, E, N, R] or null
+  const __nv_bfloat16* A;        // [S, E, R, K], or [S, 1, R, K] with a_e1
+  const __nv_bfloat16* B;        // [S, E, N, R] or null, or [S, 1, N, R] with b_e1
+  int a_e1, b_e1;                // 1: that weight holds one set per slot for every expert
   LoraSlots slots;
   float* u_out;                  // [P, R] (shrink only): scaling[s] * u for r < ranks[s]
   __nv_bfloat16* ub_out;         // [S*P, RU] (shrink only): bf16(scaling[s] * u), zero elsewhere
@@ -147,6 +149,7 @@ struct ShrinkTcParams {
   CUtensorMap tmap_a_slot[kMaxFusedSlots];   // the same rows, box {64, rows of slot s} (per_slot)
   int row_off[kMaxFusedSlots + 1];           // per_slot: first stacked B row of slot s
   int per_slot;                  // 1: only each active slot's rank rows are loaded
+  int a_e1;                      // 1: A is [S, 1, R, K], one set per slot for every expert
   int tb;                        // pairs (rows of X) per tile: 16, 32, 64 or 128
   const int32_t* offsets;        // [E + 1]
   const int32_t* perm;           // [P]

@@ -143,7 +143,8 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       if (!(((s < 32 ? mask0 : mask1) >> (s & 31)) & 1u)) continue;
       const int rank = p.slots.ranks[s];
       const int MT = (rank + 15) >> 4;
-      const __nv_bfloat16* A = p.A + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(R) * p.K;
+      const __nv_bfloat16* A =
+          p.A + (static_cast<size_t>(s) * (p.a_e1 ? 1 : E) + (p.a_e1 ? 0 : e)) * static_cast<size_t>(R) * p.K;
 
       // ---------------- shrink: warps split the K steps; partials to smem
       float acc[MTX][NTL][4];
@@ -233,7 +234,8 @@ __global__ void __launch_bounds__(kLoraThreads) lora_mma_kernel(const LoraParams
       }
       __syncthreads();
       const float sc = p.slots.scal[s];
-      const __nv_bfloat16* Bm = p.B + (static_cast<size_t>(s) * E + e) * static_cast<size_t>(p.N) * R;
+      const __nv_bfloat16* Bm =
+          p.B + (static_cast<size_t>(s) * (p.b_e1 ? 1 : E) + (p.b_e1 ? 0 : e)) * static_cast<size_t>(p.N) * R;
       const int NM = p.N >> 4;
       constexpr int UE = 4;   // feature m-tiles whose B-row loads are issued together
       for (int fm0 = warp; fm0 < NM; fm0 += kLoraWarps * UE) {

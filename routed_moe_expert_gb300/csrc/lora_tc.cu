@@ -132,10 +132,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
             for (int s = 0; s < p.S; ++s)
               if (p.row_off[s + 1] > p.row_off[s])
                 tma_load_2d(a + A_BYTES + p.row_off[s] * 128, &p.tmap_a_slot[s], &full[stage], kb * 64,
-                            (s * E + e) * p.R, pol_a);
+                            (s * (p.a_e1 ? 1 : E) + (p.a_e1 ? 0 : e)) * p.R, pol_a);
           } else {            // each slot's R rows of A for expert e, stacked
             for (int s = 0; s < p.S; ++s)
-              tma_load_2d(a + A_BYTES + s * p.R * 128, &p.tmap_a, &full[stage], kb * 64, (s * E + e) * p.R, pol_a);
+              tma_load_2d(a + A_BYTES + s * p.R * 128, &p.tmap_a, &full[stage], kb * 64, (s * (p.a_e1 ? 1 : E) + (p.a_e1 ? 0 : e)) * p.R, pol_a);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);

@@ -321,14 +321,15 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
 // (the inner extent stops at the slot's rank, so the stacked tail is zero-filled, never
 // read), and the per-slot scaled shrink rows ub [S*P, RU].
 bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* B, int N,
-                    const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn) {
+                    const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn, bool b_e1 = false) {
   const cuuint32_t box_rows = 64;
   const int R = a->R;
   const int RU = (R + 7) & ~7;
+  const int Eb = b_e1 ? 1 : a->E;   // expert sets in B (one per slot when shared)
   for (int s = 0; s < a->S; ++s) {
     if (a->h_ranks[s] <= 0 || a->h_scalings[s] == 0.0f) continue;   // never in pair_slot
-    const moe_lora_bf16* base = B + static_cast<size_t>(s) * a->E * N * R;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->h_ranks[s]), static_cast<cuuint64_t>(a->E) * N};
+    const moe_lora_bf16* base = B + static_cast<size_t>(s) * Eb * N * R;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a->h_ranks[s]), static_cast<cuuint64_t>(Eb) * N};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(R) * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
@@ -339,6 +340,7 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
   }
   if (!make_tmap(h->encode, &gp.tmap_lu, ub, static_cast<uint64_t>(a->S) * P, RU, bn)) return false;
   gp.lora_fused = 1;
+  gp.lora_b_e1 = b_e1 ? 1 : 0;
   gp.lora_kb = (R + 63) / 64;
   gp.P = P;
   gp.pair_slot = pair_slot;
@@ -350,7 +352,7 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
 moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, const void* X, const moe_lora_bf16* A,
                                   int K, const int32_t* offsets, const int32_t* perm, const LoraSlots& slots,
                                   __nv_bfloat16* ub, int32_t* pair_slot, uint32_t* status, cudaStream_t stream,
-                                  bool pdl) {
+                                  bool pdl, bool a_e1 = false) {
   const int P = a->T * a->top_k;
   ShrinkTcParams sp;
   std::memset(&sp, 0, sizeof(sp));
@@ -358,7 +360,9 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   const long long m2 = 2LL * ((P + a->E - 1) / a->E);
   sp.tb = m2 <= 16 ? 16 : m2 <= 32 ? 32 : m2 <= 64 ? 64 : 128;
   if (!make_tmap(h->encode, &sp.tmap_x, X, static_cast<uint64_t>(P), K, sp.tb)) return MOE_LORA_ERR_CUDA;
-  if (!make_tmap(h->encode, &sp.tmap_a, A, static_cast<uint64_t>(a->S) * a->E * a->R, K, a->R)) return MOE_LORA_ERR_CUDA;
+  const uint64_t a_rows = static_cast<uint64_t>(a->S) * (a_e1 ? 1 : a->E) * a->R;
+  sp.a_e1 = a_e1 ? 1 : 0;
+  if (!make_tmap(h->encode, &sp.tmap_a, A, a_rows, K, a->R)) return MOE_LORA_ERR_CUDA;
   // only the active slots' rank rows, when every such rank is a multiple of 8 (each slot's
   // rows then start on a swizzle-atom boundary of the stacked tile)
   sp.per_slot = a->S <= kMaxFusedSlots ? 1 : 0;
@@ -367,7 +371,7 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
     const int rows = (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) ? slots.ranks[s] : 0;
     if (rows % 8 != 0) sp.per_slot = 0;
     sp.row_off[s + 1] = sp.row_off[s] + rows;
-    if (rows > 0 && !make_tmap(h->encode, &sp.tmap_a_slot[s], A, static_cast<uint64_t>(a->S) * a->E * a->R, K,
+    if (rows > 0 && !make_tmap(h->encode, &sp.tmap_a_slot[s], A, a_rows, K,
                                static_cast<uint32_t>(rows)))
       return MOE_LORA_ERR_CUDA;
   }
@@ -431,6 +435,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const int P = T * k;
   const int R = lora ? a->R : 0;
+  const bool so = (a->flags & MOE_LORA_FLAG_SHARED_OUTER) != 0;   // one A_gu, one B_dn per slot
   const int RU = (R + 7) & ~7;
   const bool pdl = !(a->flags & MOE_LORA_FLAG_NO_PDL);
   moe_lora_status st = MOE_LORA_OK;
@@ -468,6 +473,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     lp.K = H;
     lp.E = E;
     lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_gu);
+    lp.a_e1 = so ? 1 : 0;   // shared-outer: one A_gu per slot
     lp.slots = slots;
     lp.status = status;
     lp.where = kWhereLoraShrinkGu;
@@ -577,10 +583,11 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   dn.K = I;
   dn.gated = 0;
   if (fused) {
-    if (!fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
+    if (!fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn, so)) return MOE_LORA_ERR_CUDA;
   } else if (lora) {
     dn.lora_v = v;
     dn.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
+    dn.lora_b_e1 = so ? 1 : 0;   // shared-outer: one B_dn per slot
     dn.pair_slot = pair_slot;
     dn.slots = slots;
   }
@@ -684,6 +691,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   std::memset(&slots, 0, sizeof(slots));
   if (lora) slots = make_slots(a);
   const int R = lora ? a->R : 0;
+  const bool so = (a->flags & MOE_LORA_FLAG_SHARED_OUTER) != 0;   // one A_gu, one B_dn per slot
   const int RU = (R + 7) & ~7;
   __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
   // Fully fused LoRA: both shrinks on the tensor cores, both expands inside the GEMMs, the
@@ -705,7 +713,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     if (fuse_all) {
       prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
-      st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl);
+      st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl, so);
       if (st != MOE_LORA_OK) return st;
       prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
     }
@@ -740,7 +748,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     dn.K = I;
     dn.gated = 0;
     // the down GEMM adds its LoRA stages to the main accumulator, so it keeps the full tile
-    if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0)) return MOE_LORA_ERR_CUDA;
+    if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)) return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, dn, a->w2, act, P, bn0, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);

@@ -83,6 +83,9 @@ CONFIGS = {
                                method=DEEPSEEK_V3, bias_std=0.1, rsf=2.827),
     "kimi_prefill": LayerConfig("kimi_prefill", T=4096, H=7168, I=2048, E=384, top_k=8,
                                 method=DEEPSEEK_V3, bias_std=0.1, rsf=2.827),
+    # decode with a shared-outer adapter of rank 32 (one A on gate_up, one B on down)
+    "shared_outer_decode": LayerConfig("shared_outer_decode", T=64, H=2048, I=768, E=128, top_k=8,
+                                       ranks=(32,), scalings=(2.0,), shared_outer=True),
 }
 
 

@@ -51,7 +51,8 @@ def oracle(inp: dict, tokens=None, lora_off=False, lazy=False):
     return orc.moe_lora_forward(
         np_(inp["hidden"]), np_(inp["router_logits"]), W(inp["w1"]), W(inp["w2"]), inp["top_k"], inp["method"],
         np_(inp["correction_bias"]), inp["rsf"], W(inp["lora_A_gu"]), W(inp["lora_B_gu"]), W(inp["lora_A_dn"]),
-        W(inp["lora_B_dn"]), np_(inp["slot_idx"]), inp["ranks"], inp["scalings"], lora_off=lora_off, tokens=tokens)
+        W(inp["lora_B_dn"]), np_(inp["slot_idx"]), inp["ranks"], inp["scalings"], lora_off=lora_off, tokens=tokens,
+        shared_outer=bool(inp.get("shared_outer", False)))
 
 
 def assert_close(got, ref, what="output"):

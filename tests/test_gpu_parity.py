@@ -178,6 +178,17 @@ def test_both_lora_placements_match_oracle(handle, flags):
     _run_and_check(handle, cfg, seed=21, flags=flags)
 
 
+@pytest.mark.parametrize("T,E,k,flags", [(64, 16, 4, 0), (64, 16, 4, 8), (256, 8, 4, 0), (600, 8, 2, 0)],
+                         ids=["narrow", "narrow-unfused", "wide-fused", "wide-256"])
+def test_shared_outer_lora_matches_oracle(handle, T, E, k, flags):
+    """Shared-outer LoRA (one A_gu and one B_dn per slot for every expert) on each LoRA
+    placement: the narrow-tile side-stream chain, the unfused placement, and the fused
+    tensor-core shrink with LoRA K-stages at 32- and 256-token tiles."""
+    cfg = wl.LayerConfig("so", T=T, H=512, I=256, E=E, top_k=k, ranks=(8, 32), scalings=(2.0, 0.5),
+                         slot_mode="uniform_none10", shared_outer=True)
+    _run_and_check(handle, cfg, seed=T + flags, flags=flags | pkg.FLAG_SHARED_OUTER)
+
+
 def test_lora_off_matches_oracle_base(handle):
     cfg = wl.LayerConfig("off", T=48, H=256, I=128, E=8, top_k=2, ranks=(8,), scalings=(2.0,))
     _run_and_check(handle, cfg, flags=pkg.FLAG_LORA_OFF, lora_off=True)

@@ -19,9 +19,9 @@ def handle():
     return pkg.Handle(0)
 
 
-def _case(T, H, I, E_loc, E_glob, k, ranks=(8, 16), scalings=(2.0, 0.5), seed=0):
+def _case(T, H, I, E_loc, E_glob, k, ranks=(8, 16), scalings=(2.0, 0.5), seed=0, shared_outer=False):
     cfg = wl.LayerConfig("routed", T=T, H=H, I=I, E=E_loc, top_k=k, ranks=ranks, scalings=scalings,
-                         slot_mode="uniform_none10")
+                         slot_mode="uniform_none10", shared_outer=shared_outer)
     inp = wl.make_inputs(cfg, seed=seed)
     ids, w = wl.make_routing(T, E_glob, k, seed=seed + 1)
     packed = orc.pack_topk(ids.numpy(), w.numpy())
@@ -36,14 +36,15 @@ def _run(h, inp, packed, E_glob, offset, do_finalize, flags=0, tokens=None):
         h, g["hidden"], torch.from_numpy(packed).cuda(), g["w1"], g["w2"], inp["top_k"], E_glob,
         local_expert_offset=offset, do_finalize=do_finalize, lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"],
         lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=inp["ranks"],
-        scalings=inp["scalings"], flags=flags, workspace=ws)
+        scalings=inp["scalings"], flags=flags | (pkg.FLAG_SHARED_OUTER if inp["shared_outer"] else 0), workspace=ws)
     torch.cuda.synchronize()
     st, word = pkg.moe_lora_check_status(ws)
     ref = orc.moe_lora_forward_routed(
         gh.np_(inp["hidden"]), packed, gh.np_(inp["w1"]), gh.np_(inp["w2"]), inp["top_k"], E_glob,
         local_expert_offset=offset, lora_A_gu=gh.np_(inp["lora_A_gu"]), lora_B_gu=gh.np_(inp["lora_B_gu"]),
         lora_A_dn=gh.np_(inp["lora_A_dn"]), lora_B_dn=gh.np_(inp["lora_B_dn"]), slot_idx=gh.np_(inp["slot_idx"]),
-        ranks=inp["ranks"], scalings=inp["scalings"], do_finalize=do_finalize, tokens=tokens)
+        ranks=inp["ranks"], scalings=inp["scalings"], do_finalize=do_finalize, tokens=tokens,
+        shared_outer=inp["shared_outer"])
     return res, ref, st
 
 
@@ -55,6 +56,13 @@ def test_routed_finalized_matches_oracle(handle, T, E_loc, E_glob, offset, k):
     out, ref, st = _run(handle, inp, packed, E_glob, offset, True)
     assert st == 0
     gh.assert_close(out.float().cpu().numpy(), ref["out"], "routed out")
+
+
+def test_routed_shared_outer_matches_oracle(handle):
+    inp, packed = _case(96, 512, 256, 8, 16, 4, seed=11, shared_outer=True)
+    out, ref, st = _run(handle, inp, packed, 16, 8, True)
+    assert st == 0
+    gh.assert_close(out.float().cpu().numpy(), ref["out"], "routed shared-outer out")
 
 
 def test_routed_unfinalized_outputs_match_oracle(handle):
