@@ -107,8 +107,13 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
   }
 }
 
-template <int BN>
+// MODE: 0 plain epilogue, 1 CUDA-core LoRA expand in the epilogue, 2 fused LoRA K-stages,
+// 3 activation epilogue, 4 activation epilogue with fused LoRA K-stages into a delta
+// accumulator.  Each mode is its own instantiation, so a launch carries only its own code.
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool kFused = MODE == 2 || MODE == 4;
+  constexpr bool kAct = MODE >= 3;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   constexpr uint32_t A_BYTES = kAByte;
   constexpr uint32_t STAGE = A_BYTES + BN * 128;
   // two accumulators (double buffer), plus two for the LoRA delta when the activation is fused
-  const bool delta_acc = p.gated == 2 && p.lora_fused;
+  constexpr bool delta_acc = MODE == 4;
   const uint32_t TMEM_COLS = delta_acc ? ((4 * BN < 32) ? 32u : 4u * BN) : ((2 * BN < 32) ? 32u : 2u * BN);
   const int S = p.stages;
 
@@ -238,7 +243,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
     }
     pdl_wait();
-    if (!p.lora_fused) {   // lane 0 alone: no per-tile warp traffic
+    if constexpr (!kFused) {   // lane 0 alone: no per-tile warp traffic
       if (lane == 0) {
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
           int e, nt, qt, wr0, wr1;
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
-        if (p.lora_fused) {
+        if constexpr (kFused) {
           // the tile's first stage has landed, so its slot mask is published
           const unsigned smask = tile_slot_ring[it_tile % kTileRing];
           const uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(2 * BN + acc * BN) : d;
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
     }
-  } else if (p.gated == 2) {   // ----------------------------- epilogue, fused activation
+  } else if constexpr (kAct) {   // --------------------------- epilogue, fused activation
     const int quarter = warp & 3;
     const int I = p.N >> 1;
     float* xchg = reinterpret_cast<float*>(lslot);   // [2][64][kXchgStride]
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // weight row inside the tile == TMEM lane
     const int etid = threadIdx.x - 64;     // 0..127 over the epilogue warps
-    const bool lora = p.lora_v != nullptr;
+    constexpr bool lora = MODE == 1;
     const int R = p.slots.R;
     const int RP8 = (R + 7) & ~7;
     int acc = 0;
@@ -476,12 +481,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   }
 }
 
+template <int BN, int MODE>
+static cudaError_t launch_mode(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
+  const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
+  cudaError_t err =
+      cudaFuncSetAttribute(grouped_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  return launch_k(grouped_gemm_kernel<BN, MODE>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem), stream,
+                  pdl, p);
+}
+
 template <int BN>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
-  return launch_k(grouped_gemm_kernel<BN>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem), stream, pdl, p);
+  if (p.gated == 2) return p.lora_fused ? launch_mode<BN, 4>(p, grid, stream, pdl) : launch_mode<BN, 3>(p, grid, stream, pdl);
+  if (p.lora_fused) return launch_mode<BN, 2>(p, grid, stream, pdl);
+  return p.lora_v != nullptr ? launch_mode<BN, 1>(p, grid, stream, pdl) : launch_mode<BN, 0>(p, grid, stream, pdl);
 }
 
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl) {
