@@ -244,6 +244,11 @@ moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_logits, const
                                        int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
                                        int32_t* perm, int32_t* inv_perm, moe_lora_stream stream);
 
+/* Cumulative number of this library's kernels launched through `h` (each route, permute,
+   forward or routed forward adds the kernels it enqueued; a memset is not counted).  For
+   measurement; the pages have no counterpart.  Host-only.  Errors: INVALID_ARG. */
+moe_lora_status moe_lora_launch_count(const moe_lora_handle* h, uint64_t* count);
+
 /* Synchronizes `stream`, then reads the device status word the last route/forward on this
    workspace left: MOE_LORA_OK, MOE_LORA_ERR_TIMEOUT or MOE_LORA_ERR_DEVICE_CHECK.
    *detail (optional) receives the raw word (code in the low byte, where in the high bytes). */

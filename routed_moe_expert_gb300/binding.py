@@ -34,7 +34,8 @@ NUM_STAGES = len(STAGES)
 
 EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
-            "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed"]
+            "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed",
+            "moe_lora_launch_count"]
 
 
 class MoELoRAError(RuntimeError):
@@ -100,6 +101,7 @@ def lib() -> ctypes.CDLL:
     L.moe_lora_permute.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]
     L.moe_lora_forward.argtypes = [c_void_p, ctypes.POINTER(Args), c_void_p, c_void_p, c_size_t, c_void_p]
     L.moe_lora_check_status.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    L.moe_lora_launch_count.argtypes = [c_void_p, ctypes.POINTER(ctypes.c_uint64)]
     L.moe_lora_forward_routed.argtypes = [c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Routed), c_void_p, c_void_p,
                                           c_size_t, c_void_p]
     for name in EXPORTED:
@@ -145,6 +147,12 @@ class Handle:
     @property
     def ptr(self):
         return self._h
+
+    def launch_count(self) -> int:
+        """Kernels launched through this handle so far."""
+        n = ctypes.c_uint64()
+        _check(lib().moe_lora_launch_count(self._h, ctypes.byref(n)), "moe_lora_launch_count")
+        return n.value
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -34,6 +34,13 @@ moe_lora_status cuda_fail(cudaError_t err, const char* what) {
     if (_e != cudaSuccess) return cuda_fail(_e, what); \
   } while (0)
 
+// A launch of one of this library's kernels, counted on the handle (moe_lora_launch_count).
+#define ML_LAUNCH(h, call, what)                    \
+  do {                                              \
+    ML_CUDA(call, what);                            \
+    ++(h)->launches;                                \
+  } while (0)
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -112,6 +119,7 @@ struct moe_lora_handle {
   cudaEvent_t ev_fork = nullptr, ev_ready = nullptr;
   EncodeTiledFn encode = nullptr;
   int coop_ctas[kMaxExperts + 1];   // cache of route_max_coop_ctas by E (0 = unknown)
+  uint64_t launches = 0;             // kernels launched through this handle
 };
 
 extern "C" {
@@ -266,10 +274,10 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
   const int ctas = route_cluster_ctas(T);   // one thread-block cluster up to 512 tokens
   if (ctas > 0) {
     p.tokens_per_cta = (T + ctas - 1) / ctas;
-    ML_CUDA(launch_route_cluster(p, ctas, stream), "route cluster launch");
+    ML_LAUNCH(h, launch_route_cluster(p, ctas, stream), "route cluster launch");
     return MOE_LORA_OK;
   }
-  ML_CUDA(launch_route_align(p, grid, stream), "route_align launch");
+  ML_LAUNCH(h, launch_route_align(p, grid, stream), "route_align launch");
   return MOE_LORA_OK;
 }
 
@@ -313,7 +321,7 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
   if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
   gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0);
-  ML_CUDA(launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
+  ML_LAUNCH(h, launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
 
@@ -390,7 +398,7 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   sp.status = status;
   int grid = (P + sp.tb - 1) / sp.tb + a->E;
   if (grid > h->num_sms) grid = h->num_sms;
-  ML_CUDA(launch_lora_shrink_tc(sp, grid, stream, pdl), "lora shrink (tensor cores) launch");
+  ML_LAUNCH(h, launch_lora_shrink_tc(sp, grid, stream, pdl), "lora shrink (tensor cores) launch");
   return MOE_LORA_OK;
 }
 
@@ -487,7 +495,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
       lp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_gu);
       lp.d_out = d;
     }
-    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, ls, pdl && !two), "lora gate_up launch");
+    ML_LAUNCH(h, launch_lora(lp, lora_ntl, lora_grid, ls, pdl && !two), "lora gate_up launch");
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, ls);
     if (two) ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
   }
@@ -495,7 +503,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
   // the pairs' adapter slots ride along with the permute for the activation + down shrink
   const bool act_shrink = lora && !fused && !fused_gu;
-  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
+  ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
                          a->slot_idx, act_shrink ? pair_slot : nullptr),
           "permute launch");
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
@@ -538,11 +546,11 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     ap.status = status;
     int grid = (P + 7) / 8 + E;
     if (grid > 4 * h->num_sms) grid = 4 * h->num_sms;
-    ML_CUDA(launch_act_shrink(ap, grid, stream, pdl_act), "activation + down shrink launch");
+    ML_LAUNCH(h, launch_act_shrink(ap, grid, stream, pdl_act), "activation + down shrink launch");
     prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
   } else {
     prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
-    ML_CUDA(launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream, pdl_act),
+    ML_LAUNCH(h, launch_activation(g, (lora && !fused_gu) ? d : nullptr, P, I, act, stream, pdl_act),
             "activation launch");
     prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
   }
@@ -568,7 +576,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     lp.pair_slot_out = pair_slot;
     lp.status = status;
     lp.where = kWhereLoraShrinkDn;
-    ML_CUDA(launch_lora(lp, lora_ntl, lora_grid, stream, pdl), "lora down shrink launch");
+    ML_LAUNCH(h, launch_lora(lp, lora_ntl, lora_grid, stream, pdl), "lora down shrink launch");
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
   }
 
@@ -635,7 +643,7 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
   if (h == nullptr || T < 0 || H < 8 || H % 8 != 0 || top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
   if (T == 0) return MOE_LORA_OK;
   if (!hidden || !perm || !permuted || !aligned16(hidden) || !aligned16(permuted)) return MOE_LORA_ERR_INVALID_ARG;
-  ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(hidden), perm, T * top_k, top_k, H,
+  ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(hidden), perm, T * top_k, top_k, H,
                          reinterpret_cast<__nv_bfloat16*>(permuted), stream),
           "permute launch");
   return MOE_LORA_OK;
@@ -708,7 +716,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     int bn = bn0;
     if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the gate_up LoRA delta accumulators
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
-    ML_CUDA(launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
+    ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
             "permute launch");
     prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     if (fuse_all) {
@@ -768,7 +776,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   fp.H = H;
   fp.k = k;
   fp.out = reinterpret_cast<__nv_bfloat16*>(out);
-  ML_CUDA(launch_finalize(fp, stream, pdl), "finalize launch");
+  ML_LAUNCH(h, launch_finalize(fp, stream, pdl), "finalize launch");
   prof(a, MOE_LORA_STAGE_FINALIZE, 1, stream);
   return MOE_LORA_OK;
 }
@@ -823,6 +831,12 @@ moe_lora_status moe_lora_forward_routed(moe_lora_handle* h, const moe_lora_args*
       return MOE_LORA_ERR_INVALID_ARG;
   }
   return forward_impl(h, &b, r, out, workspace, workspace_bytes, stream);
+}
+
+moe_lora_status moe_lora_launch_count(const moe_lora_handle* h, uint64_t* count) {
+  if (h == nullptr || count == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  *count = h->launches;
+  return MOE_LORA_OK;
 }
 
 moe_lora_status moe_lora_check_status(const void* workspace, moe_lora_stream stream, uint32_t* detail) {
