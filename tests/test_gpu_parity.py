@@ -219,6 +219,21 @@ def test_single_and_two_stream_agree_bitwise(handle):
     assert torch.equal(one, two) and torch.equal(one, dflt)
 
 
+def test_launch_count_per_forward(handle):
+    """One forward launches the kernels its placement draws: narrow tiles with LoRA = route,
+    side-stream LoRA, permute, gate_up GEMM, activation + down shrink, down GEMM, finalize;
+    LoRA off drops the LoRA kernel and fuses nothing else; wide tiles = route, permute,
+    two tensor-core shrinks, two GEMMs, finalize."""
+    narrow = wl.LayerConfig("n", T=64, H=256, I=128, E=32, top_k=4, ranks=(8,), scalings=(1.0,))
+    wide = wl.LayerConfig("w", T=256, H=256, I=128, E=8, top_k=4, ranks=(8,), scalings=(1.0,))
+    for cfg, flags, want in ((narrow, 0, 7), (narrow, pkg.FLAG_LORA_OFF, 6), (wide, 0, 7)):
+        g = gh.to_dev(wl.make_inputs(cfg, seed=1))
+        n0 = handle.launch_count()
+        gh.forward(handle, g, flags=flags)
+        torch.cuda.synchronize()
+        assert handle.launch_count() - n0 == want, (cfg.name, flags)
+
+
 def test_slot_out_of_range_reported(handle):
     cfg = wl.LayerConfig("bad", T=16, H=128, I=64, E=4, top_k=2, ranks=(4,), scalings=(1.0,))
     inp = wl.make_inputs(cfg, seed=1)
