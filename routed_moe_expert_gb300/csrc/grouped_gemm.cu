@@ -51,13 +51,13 @@ int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
 int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused) {
   // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
-  // barriers (2*stages), tfull/tempty (4), drain (1); tmem slot + abort flag (16 B);
+  // barriers (2*stages), tfull/tempty (4), drain (1), dempty (1); tmem slot + abort flag (16 B);
   // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
   // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes.
   const int ring = 4 * (kTileRing + 4);
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
-  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 5) * 8 + 16 + 8 * (E + 1) + ring +
+  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
          (lora > xchg ? lora : xchg);
 }
 
@@ -109,7 +109,13 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
 
 // MODE: 0 plain epilogue, 1 CUDA-core LoRA expand in the epilogue, 2 fused LoRA K-stages,
 // 3 activation epilogue, 4 activation epilogue with fused LoRA K-stages into a delta
-// accumulator.  Each mode is its own instantiation, so a launch carries only its own code.
+// accumulator (so g and the delta are rounded to bf16 separately).  Each mode is its own
+// instantiation, so a launch carries only its own code.
+//
+// TMEM (512 columns): kAccBufs accumulators of BN columns, then kDeltaBufs delta accumulators.
+// Two of each up to BN = 128; at BN = 160 the single delta buffer is guarded by `dempty`
+// (the LoRA stages of tile i wait until the epilogue has read tile i-1's delta, which
+// it did while tile i's main loop ran); at BN = 256 MODE 4 has one of each.
 template <int BN, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool kFused = MODE == 2 || MODE == 4;
@@ -120,9 +126,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
   constexpr uint32_t A_BYTES = kAByte;
   constexpr uint32_t STAGE = A_BYTES + BN * 128;
-  // two accumulators (double buffer), plus two for the LoRA delta when the activation is fused
   constexpr bool delta_acc = MODE == 4;
-  const uint32_t TMEM_COLS = delta_acc ? ((4 * BN < 32) ? 32u : 4u * BN) : ((2 * BN < 32) ? 32u : 2u * BN);
+  constexpr int kAccBufs = (2 * BN + (delta_acc ? BN : 0) <= 512) ? 2 : 1;
+  constexpr int kDeltaBufs = !delta_acc ? 0 : (kAccBufs * BN + 2 * BN <= 512) ? 2 : 1;
+  constexpr uint32_t kColsUsed = static_cast<uint32_t>((kAccBufs + kDeltaBufs) * BN);
+  static_assert(kColsUsed <= 512u, "accumulators exceed TMEM");
+  constexpr uint32_t TMEM_COLS = kColsUsed <= 32u ? 32u : kColsUsed <= 64u ? 64u : kColsUsed <= 128u ? 128u
+                                 : kColsUsed <= 256u ? 256u : 512u;   // a power of two
   const int S = p.stages;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
@@ -130,7 +140,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   uint64_t* tfull = empty + S;       // [2]
   uint64_t* tempty = tfull + 2;      // [2]
   uint64_t* drain = tempty + 2;      // [1], used only after an abort
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* dempty = drain + 1;      // [1], the single delta buffer is free (kDeltaBufs == 1)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);   // [E + 1]
   int* seg = tile_start + (p.E + 1);                         // offsets copy [E + 1]
@@ -142,10 +153,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
-  if (TMEM_COLS > 512u) {   // the host never asks for this; refuse instead of over-allocating
-    if (threadIdx.x == 0 && blockIdx.x == 0) record_status(p.status, kDevTimeout, kWhereGemmMma);
-    return;
-  }
   const int NT = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);   // 128-row weight tiles per expert
   const int KB = p.K >> 6;                                    // 64-wide K blocks
 
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     mbar_init(&tempty[0], 128);
     mbar_init(&tempty[1], 128);
     mbar_init(drain, 1);
+    mbar_init(dempty, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -260,16 +268,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         decode(tile, e, nt, qt);
         weight_rows(e, nt, wr0, wr1);
         const int xr = seg[e] + qt * BN;
-        // the tile's pair slots are loaded now and reduced after all but the last main stage
-        // are issued, so their latency hides behind the tile's own copies
+        // the tile's pair slots are loaded now (all loads in flight at once) and reduced only
+        // after all but the last main stage are issued, so their latency hides behind the
+        // tile's own copies
         const int nv = min(BN, seg[e + 1] - xr);
-        unsigned lmask = 0;
-        for (int j = lane; j < nv; j += 32) {
-          const int sl = p.pair_slot[xr + j];
-          if (sl >= 0 && sl < kMaxFusedSlots) lmask |= 1u << sl;
+        constexpr int kSlotLoads = (BN + 31) / 32;
+        int slv[kSlotLoads];
+#pragma unroll
+        for (int u = 0; u < kSlotLoads; ++u) {
+          const int j = lane + 32 * u;
+          slv[u] = j < nv ? p.pair_slot[xr + j] : -1;
         }
         if (lane == 0)
           for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+        unsigned lmask = 0;
+#pragma unroll
+        for (int u = 0; u < kSlotLoads; ++u)
+          if (slv[u] >= 0 && slv[u] < kMaxFusedSlots) lmask |= 1u << slv[u];
         const unsigned smask = __reduce_or_sync(0xffffffffu, lmask);
         if (lane == 0) {
           // published before the tile's last main stage arrives (arrive.expect_tx releases it);
@@ -297,6 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     uint32_t phase = 0;
     int acc = 0;
     uint32_t aphase = 0;
+    uint32_t dphase = 0;
     int ok = 1;
     auto consume = [&](uint32_t d, bool first) -> bool {
       if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWhereGemmMma)) return false;
@@ -323,8 +339,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         if constexpr (kFused) {
           // the tile's first stage has landed, so its slot mask is published
           const unsigned smask = tile_slot_ring[it_tile % kTileRing];
-          const uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(2 * BN + acc * BN) : d;
+          const uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(kAccBufs * BN + (kDeltaBufs == 2 ? acc * BN : 0)) : d;
           bool first_delta = delta_acc;   // the delta accumulator starts fresh each tile
+          if constexpr (delta_acc && kDeltaBufs == 1) {   // every tile, LoRA or not
+            ok = mbar_wait(dempty, dphase ^ 1u, abort_flag, p.status, kWhereGemmMma);
+            dphase ^= 1u;
+            tc_fence_after();
+          }
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
             if (!((smask >> sl) & 1u)) continue;
             for (int kb = 0; ok && kb < p.lora_kb; ++kb) {
@@ -335,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
-        if (++acc == 2) {
+        if (++acc == kAccBufs) {
           acc = 0;
           aphase ^= 1u;
         }
@@ -365,7 +386,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       tc_fence_after();
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tm = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
-      const uint32_t td = tmem_base + lane_base + static_cast<uint32_t>(2 * BN + acc * BN);
+      const uint32_t td = tmem_base + lane_base + static_cast<uint32_t>(kAccBufs * BN + (kDeltaBufs == 2 ? acc * BN : 0));
 #pragma unroll 1
       for (int c = 0; c < nvalid; c += 16, ++chunk) {   // warp-uniform bound
         uint32_t gv[16], dv[16];
@@ -399,8 +420,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       tc_fence_before();
+      if constexpr (kDeltaBufs == 1) mbar_arrive(dempty);
       mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
+      if (++acc == kAccBufs) {
         acc = 0;
         aphase ^= 1u;
       }
@@ -459,7 +481,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
+      if (++acc == kAccBufs) {
         acc = 0;
         aphase ^= 1u;
       }
@@ -505,6 +527,8 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStrea
     case 32: return launch_bn<32>(p, grid, stream, pdl);
     case 64: return launch_bn<64>(p, grid, stream, pdl);
     case 128: return launch_bn<128>(p, grid, stream, pdl);
+    case 160:   // the fused gate_up with LoRA only: room in TMEM for two accumulators and a delta
+      return (p.gated == 2 && p.lora_fused) ? launch_mode<160, 4>(p, grid, stream, pdl) : cudaErrorInvalidValue;
     case 256: return launch_bn<256>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }

@@ -714,7 +714,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   const bool act_in_gemm = fuse_all || (!lora && bn0 >= 32);
   if (act_in_gemm) {
     int bn = bn0;
-    if (fuse_all && bn > 128) bn = 128;   // room in TMEM for the gate_up LoRA delta accumulators
+    if (fuse_all && bn > 160) bn = 160;   // room in TMEM for two accumulators and the LoRA delta
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
     ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
             "permute launch");

@@ -133,7 +133,8 @@ def test_random_small_layers(handle, seed):
 @pytest.mark.parametrize("T,E,k", [(40, 8, 4), (130, 8, 4), (260, 8, 4), (520, 8, 4), (1500, 6, 3)])
 def test_token_tile_widths_and_ragged_tails(handle, T, E, k):
     """T*k/E pairs per expert of about 20, 65, 130, 260, 750 select token tiles of
-    32, 128, 256, 256 (several per expert) with ragged tails."""
+    32, 128, 256, 256 (several per expert) with ragged tails; with LoRA the fused gate_up
+    takes 160-token tiles at the last three (one delta accumulator)."""
     cfg = wl.LayerConfig("tiles", T=T, H=256, I=192, E=E, top_k=k, ranks=(8, 16), scalings=(1.0, 0.5),
                          slot_mode="uniform_none10")
     _run_and_check(handle, cfg, seed=T)
