@@ -288,6 +288,13 @@ MLDEV uint4 pack8(const float (&f)[8]) {
   for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
   return v;
 }
+MLDEV uint2 pack4(const float (&f)[4]) {
+  uint2 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+  h[0] = __floats2bfloat162_rn(f[0], f[1]);
+  h[1] = __floats2bfloat162_rn(f[2], f[3]);
+  return v;
+}
 
 MLDEV uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;

@@ -46,6 +46,7 @@ constexpr int kMaxStages = 16;
 constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxStages tiles ahead
 constexpr int kXchgStride = 17;                       // floats per feature row (padded against bank conflicts)
 constexpr int kXchgFloats = 2 * 128 * kXchgStride;    // two buffers of 128 rows (64 gate, 64 up) x 16 tokens
+constexpr int kYbufFloats = 4 * 16 * 32;              // per epilogue warp: 16 tokens x 32 features
 
 int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
 
@@ -53,12 +54,14 @@ int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused) {
   // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
   // barriers (2*stages), tfull/tempty (4), drain (1), dempty (1); tmem slot + abort flag (16 B);
   // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
-  // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes.
+  // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes; then,
+  // for the plain epilogues, the four warps' 16 x 32 float store buffers.
   const int ring = 4 * (kTileRing + 4);
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
+  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + kYbufFloats * 4;
   return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
-         (lora > xchg ? lora : xchg);
+         (lora > xchg ? lora : xchg) + ybuf;
 }
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
@@ -434,6 +437,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     constexpr bool lora = MODE == 1;
     const int R = p.slots.R;
     const int RP8 = (R + 7) & ~7;
+    // this warp's store buffer: [16 tokens][32 features] (its TMEM lane quarter)
+    float* yb = v_s + (lora ? BN * RP8 : 0) + quarter * 512;
+    const int f4 = (lane & 7) * 4;   // the 4 features this lane stores per token row
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -465,17 +471,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
         for (int j = 0; j < 16; ++j) val[j] = __uint_as_float(r[j]);
         if (lora && col < p.N) lora_expand_chunk(p, lslot, v_s, c, nvalid, e, col, val);
-        if (col < p.N) {
-          if (p.out_f32 != nullptr) {
-            float* o = p.out_f32 + static_cast<size_t>(q0 + c) * p.N + col;
+        // transpose through the warp's buffer (lane = feature on the way in), then each lane
+        // stores 4 consecutive features of a token: 4 token rows of 128 B per instruction
+        __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < nvalid) o[static_cast<size_t>(j) * p.N] = val[j];
-          } else {
-            __nv_bfloat16* o = p.out + static_cast<size_t>(q0 + c) * p.N + col;
+        for (int j = 0; j < 16; ++j) yb[j * 32 + lane] = val[j];
+        __syncwarp();
+        const int fcol = nt * 128 + quarter * 32 + f4;
+        if (fcol < p.N) {   // N is a multiple of 4, so the whole vector is in range
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < nvalid) o[static_cast<size_t>(j) * p.N] = f2bf(val[j]);
+          for (int i = 0; i < 4; ++i) {
+            const int tok = (lane >> 3) + 4 * i;
+            if (c + tok < nvalid) {
+              const float4 v = *reinterpret_cast<const float4*>(yb + tok * 32 + f4);
+              const size_t off = static_cast<size_t>(q0 + c + tok) * p.N + fcol;
+              if (p.out_f32 != nullptr) {
+                *reinterpret_cast<float4*>(p.out_f32 + off) = v;
+              } else {
+                const float v4[4] = {v.x, v.y, v.z, v.w};
+                *reinterpret_cast<uint2*>(p.out + off) = pack4(v4);
+              }
+            }
           }
         }
       }
