@@ -47,10 +47,11 @@ constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxS
 constexpr int kXchgStride = 17;                       // floats per feature row (padded against bank conflicts)
 constexpr int kXchgFloats = 2 * 128 * kXchgStride;    // two buffers of 128 rows (64 gate, 64 up) x 16 tokens
 constexpr int kYbufFloats = 4 * 16 * 32;              // per epilogue warp: 16 tokens x 32 features
+constexpr uint64_t kPeerDrainNs = 100000;             // 100 us for an aborted odd CTA's copies to land
 
-int gemm_stage_bytes(int bn) { return kAByte + bn * 128; }
+int gemm_stage_bytes(int rows) { return kAByte + rows * 128; }
 
-int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused) {
+int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused) {
   // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
   // barriers (2*stages), tfull/tempty (4), drain (1), dempty (1); tmem slot + abort flag (16 B);
   // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
@@ -60,7 +61,7 @@ int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused) {
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
   const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + kYbufFloats * 4;
-  return 1024 + stages * gemm_stage_bytes(bn) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
+  return 1024 + stages * gemm_stage_bytes(bn / cg) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
          (lora > xchg ? lora : xchg) + ybuf;
 }
 
@@ -119,8 +120,18 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
 // Two of each up to BN = 128; at BN = 160 the single delta buffer is guarded by `dempty`
 // (the LoRA stages of tile i wait until the epilogue has read tile i-1's delta, which
 // it did while tile i's main loop ran); at BN = 256 MODE 4 has one of each.
-template <int BN, int MODE>
+//
+// CG = 2: clusters of two CTAs (one TPC) share each tile as an M = 256 tcgen05 pair MMA.
+// A tile is then two consecutive 128-row weight tiles (the even CTA's, then the odd CTA's)
+// x BN tokens; each CTA loads its 128 weight rows and BN/2 of the token rows, so each SM
+// takes in a third less per MMA than with 128 x BN tiles.  The even CTA's producer expects
+// both CTAs' bytes on its full barriers, its MMA warp issues for the pair and multicasts
+// the commits, and both CTAs' epilogue warps release the even CTA's accumulator barriers.
+template <int BN, int MODE, int CG>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
+  constexpr int BNH = BN / CG;   // token rows this CTA loads per stage
+  static_assert(BNH % 8 == 0, "stage buffers stay 1024-byte aligned");
   constexpr bool kFused = MODE == 2 || MODE == 4;
   constexpr bool kAct = MODE >= 3;
   extern __shared__ uint8_t smem_raw[];
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
 
   constexpr uint32_t A_BYTES = kAByte;
-  constexpr uint32_t STAGE = A_BYTES + BN * 128;
+  constexpr uint32_t STAGE = A_BYTES + BNH * 128;
   constexpr bool delta_acc = MODE == 4;
   constexpr int kAccBufs = (2 * BN + (delta_acc ? BN : 0) <= 512) ? 2 : 1;
   constexpr int kDeltaBufs = !delta_acc ? 0 : (kAccBufs * BN + 2 * BN <= 512) ? 2 : 1;
@@ -137,6 +148,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   constexpr uint32_t TMEM_COLS = kColsUsed <= 32u ? 32u : kColsUsed <= 64u ? 64u : kColsUsed <= 128u ? 128u
                                  : kColsUsed <= 256u ? 256u : 512u;   // a power of two
   const int S = p.stages;
+  // accumulator releases: every epilogue thread of a single CTA, or one per epilogue warp
+  // of the pair (the odd CTA's warps arrive remotely)
+  constexpr uint32_t kRelease = CG == 2 ? 8u : 128u;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
   uint64_t* empty = full + S;
@@ -155,6 +169,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   // v_s: [BN][RP8] (16-byte aligned), RP8 = R rounded up to 8
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;   // 0: the pair's MMA issuer
+  const bool leader = crank == 0;
+  const int cta0 = static_cast<int>(blockIdx.x) / CG, ncta = static_cast<int>(gridDim.x) / CG;
   const int E = p.E;
   const int NT = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);   // 128-row weight tiles per expert
   const int KB = p.K >> 6;                                    // 64-wide K blocks
@@ -166,10 +183,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     }
     mbar_init(&tfull[0], 1);
     mbar_init(&tfull[1], 1);
-    mbar_init(&tempty[0], 128);
-    mbar_init(&tempty[1], 128);
+    mbar_init(&tempty[0], kRelease);
+    mbar_init(&tempty[1], kRelease);
     mbar_init(drain, 1);
-    mbar_init(dempty, 128);
+    mbar_init(dempty, kRelease);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -178,12 +195,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     tma_prefetch_desc(&p.tmap_x);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
-  if (warp == 2) build_tile_schedule(p.offsets, E, BN, NT, seg, tile_start);   // ceil(M_e/BN) * NT tiles each
+  // ceil(M_e/BN) * NT/CG tiles per expert
+  if (warp == 2) build_tile_schedule(p.offsets, E, BN, NT / CG, seg, tile_start);
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {   // the peer's barriers are initialised before any remote use
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_start[E];
@@ -197,8 +225,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     e = lo;
     const int local = tile - tile_start[e];
     const int nq = (seg[e + 1] - seg[e] + BN - 1) / BN;
-    nt = local / nq;
-    qt = local - nt * nq;
+    const int ntp = local / nq;
+    qt = local - ntp * nq;
+    nt = ntp * CG + static_cast<int>(crank);   // this CTA's 128-row weight tile
+  };
+
+  // an epilogue thread's release of an accumulator barrier (kRelease arrivals complete it)
+  auto release = [&](uint64_t* bar) {
+    if constexpr (CG == 2) {   // one arrival per warp, on the pair's (even CTA's) barrier
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(bar, 0));
+    } else {
+      mbar_arrive(bar);
+    }
   };
 
   if (warp >= 2) pdl_wait();   // the epilogues read the previous kernel's LoRA rows and slots
@@ -211,15 +250,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     uint32_t issued_parity = 0;
     int ok = 1;
     int npre = 0, nissued = 0;   // stages whose weight half went out before pdl_wait
+    // a copy into this CTA's stage s, counted on the pair's (even CTA's) full barrier s
+    auto load = [&](void* dst, const CUtensorMap* map, int s, int x, int y, uint64_t pol) {
+      if constexpr (CG == 2) tma_load_2d_pair(dst, map, cluster_addr(&full[s], 0), x, y, pol);
+      else tma_load_2d(dst, map, &full[s], x, y, pol);
+    };
     auto issue = [&](const CUtensorMap* wmap, int wr0, int wr1, int kx, const CUtensorMap* xmap, int xrow) -> bool {
       if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) return false;
       uint8_t* a = smem + stage * STAGE;
       if (nissued++ >= npre) {
-        mbar_arrive_expect_tx(&full[stage], STAGE);
-        tma_load_2d(a, wmap, &full[stage], kx, wr0, pol_w);
-        tma_load_2d(a + 8192, wmap, &full[stage], kx, wr1, pol_w);
+        if (leader) mbar_arrive_expect_tx(&full[stage], CG * STAGE);
+        load(a, wmap, stage, kx, wr0, pol_w);
+        load(a + 8192, wmap, stage, kx, wr1, pol_w);
       }
-      tma_load_2d(a + A_BYTES, xmap, &full[stage], kx, xrow, pol_x);
+      load(a + A_BYTES, xmap, stage, kx, xrow, pol_x);
       issued_mask |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == S) {
@@ -240,37 +284,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     // Weights are constants of the layer and the tile schedule comes from the expert
     // offsets, so the weight halves of the first tile's first stages go out before the
     // previous kernel (which writes the token rows) has finished.
-    if (lane == 0 && static_cast<int>(blockIdx.x) < total) {
+    if (lane == 0 && cta0 < total) {
       int e, nt, qt, wr0, wr1;
-      decode(blockIdx.x, e, nt, qt);
+      decode(cta0, e, nt, qt);
       weight_rows(e, nt, wr0, wr1);
       npre = min(S, KB);
       for (int s2 = 0; s2 < npre; ++s2) {
         uint8_t* a = smem + s2 * STAGE;
-        mbar_arrive_expect_tx(&full[s2], STAGE);
-        tma_load_2d(a, &p.tmap_w, &full[s2], s2 * 64, wr0, pol_w);
-        tma_load_2d(a + 8192, &p.tmap_w, &full[s2], s2 * 64, wr1, pol_w);
+        if (leader) mbar_arrive_expect_tx(&full[s2], CG * STAGE);
+        load(a, &p.tmap_w, s2, s2 * 64, wr0, pol_w);
+        load(a + 8192, &p.tmap_w, s2, s2 * 64, wr1, pol_w);
         issued_mask |= 1u << s2;   // phase 0
       }
     }
     pdl_wait();
     if constexpr (!kFused) {   // lane 0 alone: no per-tile warp traffic
       if (lane == 0) {
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        for (int tile = cta0; ok && tile < total; tile += ncta) {
           int e, nt, qt, wr0, wr1;
           decode(tile, e, nt, qt);
           weight_rows(e, nt, wr0, wr1);
           const int xr = seg[e] + qt * BN;
-          for (int kb = 0; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+          const int xh = xr + static_cast<int>(crank) * BNH;   // this CTA's token rows
+          for (int kb = 0; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xh);
         }
       }
     } else {   // the whole warp: lanes gather each tile's pair slots for lane 0
       int it_tile = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it_tile) {
+      for (int tile = cta0; tile < total; tile += ncta, ++it_tile) {
         int e, nt, qt, wr0, wr1;
         decode(tile, e, nt, qt);
         weight_rows(e, nt, wr0, wr1);
         const int xr = seg[e] + qt * BN;
+        const int xh = xr + static_cast<int>(crank) * BNH;   // this CTA's token rows
         // the tile's pair slots are loaded now (all loads in flight at once) and reduced only
         // after all but the last main stage are issued, so their latency hides behind the
         // tile's own copies
@@ -283,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           slv[u] = j < nv ? p.pair_slot[xr + j] : -1;
         }
         if (lane == 0)
-          for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xr);
+          for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xh);
         unsigned lmask = 0;
 #pragma unroll
         for (int u = 0; u < kSlotLoads; ++u)
@@ -294,11 +340,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           // the MMA warp reads it after consuming that stage
           tile_slot_ring[it_tile % kTileRing] = smask;
           const int lb_off = p.lora_b_e1 ? e * p.N : 0;   // a shared B has one expert's rows
-          if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xr);
+          if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xh);
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
             if (!((smask >> sl) & 1u)) continue;
             for (int kb = 0; ok && kb < p.lora_kb; ++kb)
-              ok = issue(&p.tmap_lb[sl], wr0 - lb_off, wr1 - lb_off, kb * 64, &p.tmap_lu, sl * p.P + xr);
+              ok = issue(&p.tmap_lb[sl], wr0 - lb_off, wr1 - lb_off, kb * 64, &p.tmap_lu, sl * p.P + xh);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -306,11 +352,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     }
     pdl_trigger();   // all of this CTA's copies are issued: the next kernel may start
     if (lane == 0 && !ok) {   // drain: let every issued copy land before the CTA exits
-      for (int s2 = 0; s2 < S; ++s2)
-        if ((issued_mask >> s2) & 1u) mbar_wait_drain(&full[s2], (issued_parity >> s2) & 1u);
+      if (leader) {   // the pair's full barriers count both CTAs' bytes
+        for (int s2 = 0; s2 < S; ++s2)
+          if ((issued_mask >> s2) & 1u) mbar_wait_drain(&full[s2], (issued_parity >> s2) & 1u);
+      } else {        // the odd CTA's copies are counted in the even CTA: give them time to land
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kPeerDrainNs) {
+        }
+      }
     }
   } else if (warp == 1) {   // ------------------------------------------ MMA issuer (lane 0)
-    constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+    constexpr uint32_t idesc = idesc_bf16_f32(128 * CG, BN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -324,17 +376,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       const uint64_t ad = sw128_kmajor_desc(a_addr);
       const uint64_t bd = sw128_kmajor_desc(a_addr + A_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
-      umma_commit(&empty[stage]);
+      for (int kk = 0; kk < 4; ++kk) {
+        if constexpr (CG == 2) umma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+        else umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+      }
+      if constexpr (CG == 2) umma_commit_pair_mc(&empty[stage], 0x3);   // both CTAs' stage s is free
+      else umma_commit(&empty[stage]);
       if (++stage == S) {
         stage = 0;
         phase ^= 1u;
       }
       return true;
     };
-    if (lane == 0) {
+    if (lane == 0 && leader) {   // the pair's MMAs are issued by its even CTA
       int it_tile = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it_tile) {
+      for (int tile = cta0; ok && tile < total; tile += ncta, ++it_tile) {
         if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -358,7 +414,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (CG == 2) umma_commit_pair_mc(&tfull[acc], 0x3);   // both CTAs' epilogues
+        else umma_commit(&tfull[acc]);
         if (++acc == kAccBufs) {
           acc = 0;
           aphase ^= 1u;
@@ -371,7 +428,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     float* xchg = reinterpret_cast<float*>(lslot);   // [2][64][kXchgStride]
     int acc = 0, chunk = 0;
     uint32_t aphase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = cta0; tile < total; tile += ncta) {
       int e, nt, qt;
       decode(tile, e, nt, qt);
       const int q0 = seg[e] + qt * BN;
@@ -423,8 +480,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       tc_fence_before();
-      if constexpr (kDeltaBufs == 1) mbar_arrive(dempty);
-      mbar_arrive(&tempty[acc]);
+      if constexpr (kDeltaBufs == 1) release(dempty);   // done with the accumulator and the delta
+      release(&tempty[acc]);
       if (++acc == kAccBufs) {
         acc = 0;
         aphase ^= 1u;
@@ -442,7 +499,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int f4 = (lane & 7) * 4;   // the 4 features this lane stores per token row
     int acc = 0;
     uint32_t aphase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = cta0; tile < total; tile += ncta) {
       int e, nt, qt;
       decode(tile, e, nt, qt);
       const int col = nt * 128 + row;
@@ -496,7 +553,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      release(&tempty[acc]);   // done with the accumulator
       if (++acc == kAccBufs) {
         acc = 0;
         aphase ^= 1u;
@@ -505,47 +562,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {   // neither CTA leaves while the pair's MMAs may touch its memory
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
-    if (*abort_flag) {   // let the MMAs lane 0 already issued finish before TMEM is released
+    if (*abort_flag && leader) {   // let the MMAs lane 0 already issued finish before TMEM is released
       if (lane == 0) {
-        umma_commit(drain);
+        if constexpr (CG == 2) umma_commit_pair(drain);
+        else umma_commit(drain);
         mbar_wait_drain(drain, 0);
       }
       __syncwarp();
     }
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, int CG>
 static cudaError_t launch_mode(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  const int smem = gemm_smem_bytes(BN, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
+  const int smem = gemm_smem_bytes(BN, CG, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
   cudaError_t err =
-      cudaFuncSetAttribute(grouped_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(grouped_gemm_kernel<BN, MODE, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  return launch_k(grouped_gemm_kernel<BN, MODE>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem), stream,
-                  pdl, p);
+  grid = grid / CG * CG;   // whole clusters
+  if (grid < CG) return cudaErrorInvalidValue;
+  return launch_kc(grouped_gemm_kernel<BN, MODE, CG>, dim3(grid), dim3(kGemmThreads), static_cast<size_t>(smem),
+                   stream, pdl, CG, p);
 }
 
-template <int BN>
+template <int BN, int CG>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  if (p.gated == 2) return p.lora_fused ? launch_mode<BN, 4>(p, grid, stream, pdl) : launch_mode<BN, 3>(p, grid, stream, pdl);
-  if (p.lora_fused) return launch_mode<BN, 2>(p, grid, stream, pdl);
-  return p.lora_v != nullptr ? launch_mode<BN, 1>(p, grid, stream, pdl) : launch_mode<BN, 0>(p, grid, stream, pdl);
+  if (p.gated == 2)
+    return p.lora_fused ? launch_mode<BN, 4, CG>(p, grid, stream, pdl) : launch_mode<BN, 3, CG>(p, grid, stream, pdl);
+  if (p.lora_fused) return launch_mode<BN, 2, CG>(p, grid, stream, pdl);
+  if (p.lora_v != nullptr) {   // the CUDA-core LoRA epilogue runs on single-CTA tiles only
+    if constexpr (CG == 1) return launch_mode<BN, 1, 1>(p, grid, stream, pdl);
+    else return cudaErrorInvalidValue;
+  }
+  return launch_mode<BN, 0, CG>(p, grid, stream, pdl);
 }
 
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl) {
   if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
+  const bool fused_act_lora = p.gated == 2 && p.lora_fused;
+  if (p.cta_pair == 2) {
+    const int nt = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);
+    if (nt % 2 != 0) return cudaErrorInvalidValue;   // a pair covers two weight tiles
+    switch (bn) {
+      case 128: return launch_bn<128, 2>(p, grid, stream, pdl);
+      case 160: return fused_act_lora ? launch_mode<160, 4, 2>(p, grid, stream, pdl) : cudaErrorInvalidValue;
+      case 256: return launch_bn<256, 2>(p, grid, stream, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
-    case 16: return launch_bn<16>(p, grid, stream, pdl);
-    case 32: return launch_bn<32>(p, grid, stream, pdl);
-    case 64: return launch_bn<64>(p, grid, stream, pdl);
-    case 128: return launch_bn<128>(p, grid, stream, pdl);
+    case 16: return launch_bn<16, 1>(p, grid, stream, pdl);
+    case 32: return launch_bn<32, 1>(p, grid, stream, pdl);
+    case 64: return launch_bn<64, 1>(p, grid, stream, pdl);
+    case 128: return launch_bn<128, 1>(p, grid, stream, pdl);
     case 160:   // the fused gate_up with LoRA only: room in TMEM for two accumulators and a delta
-      return (p.gated == 2 && p.lora_fused) ? launch_mode<160, 4>(p, grid, stream, pdl) : cudaErrorInvalidValue;
-    case 256: return launch_bn<256>(p, grid, stream, pdl);
+      return fused_act_lora ? launch_mode<160, 4, 1>(p, grid, stream, pdl) : cudaErrorInvalidValue;
+    case 256: return launch_bn<256, 1>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -68,18 +68,19 @@ int route_max_coop_ctas(int E);
 // fused stages, rounded separately) and writes a [P, N/2] bf16.
 struct GemmParams {
   CUtensorMap tmap_w;            // weights [E*N rows, K cols], box {64, 64}
-  CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN}
+  CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN / cta_pair}
   __nv_bfloat16* out;            // [P, N] bf16 output, or
   float* out_f32;                //   fp32 output when non-null
   const int32_t* offsets;        // [E + 1]
   uint32_t* status;
   int E, N, K, gated, stages;
+  int cta_pair;                  // 2: CTA pairs share each tile (M = 256; N/128 even); else 1
   // Optional LoRA expand as extra MMA K-stages of every tile (fused LoRA): for each slot
   // s present among the tile's pairs, A' = rows of lora B of slot s (tmap_lb[s], inner
   // extent ranks[s], so the stacked rank tail reads as zero) and B' = the tile's rows of
   // ub = scaling[s] * bf16(shrink), zero for pairs of other slots (tmap_lu, rows s*P + q).
   CUtensorMap tmap_lb[kMaxFusedSlots];
-  CUtensorMap tmap_lu;           // [S*P rows, RU cols] bf16, box {64, BN}
+  CUtensorMap tmap_lu;           // [S*P rows, RU cols] bf16, box {64, BN / cta_pair}
   int lora_fused;                // 1: use the extra stages (pair_slot gives the slots)
   int lora_kb;                   // 64-wide K blocks per slot: ceil(R / 64)
   int P;
@@ -94,8 +95,8 @@ struct GemmParams {
   LoraSlots slots;
 };
 constexpr int kMaxGemmSmem = 227 * 1024;   // dynamic shared memory a CTA may have
-int gemm_smem_bytes(int bn, int stages, int E, int lora_R, int act_fused);
-int gemm_stage_bytes(int bn);
+int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused);
+int gemm_stage_bytes(int rows);   // one stage: 128 weight rows + `rows` token rows, 64 wide
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 
 // ---------------------------------------------------------------- elementwise

@@ -301,14 +301,19 @@ int pick_bn(long long P, int E) {
   return 256;
 }
 
+// Wide token tiles run on CTA pairs (M = 256 tcgen05 pair MMAs, each SM loading half the
+// token rows) when the weight rows split into an even number of 128-row tiles.
+constexpr int kPairMinBn = 128;
+int pair_tiles(int bn, int N) { return (bn >= kPairMinBn && N % 256 == 0) ? 2 : 1; }
+
 // Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
 // room for the side-stream LoRA kernel that runs beside it; the down GEMM runs alone.
-int pick_stages(int bn, int E, int lora_R, int act_fused, bool alone) {
+int pick_stages(int bn, int cg, int E, int lora_R, int act_fused, bool alone) {
   // Wide tiles (prefill) keep too few stages in flight to cover the load latency at 200 KB,
   // so they take the whole 227 KB a CTA may have.
   const int budget = bn >= 64 ? kMaxGemmSmem : (bn <= 32 && !alone ? 160 : 200) * 1024;
-  const int fixed = gemm_smem_bytes(bn, 0, E, lora_R, act_fused);
-  int s = (budget - fixed) / (gemm_stage_bytes(bn) + 16);
+  const int fixed = gemm_smem_bytes(bn, cg, 0, E, lora_R, act_fused);
+  int s = (budget - fixed) / (gemm_stage_bytes(bn / cg) + 16);
   if (s > 16) s = 16;
   if (s < 2) s = 2;
   return s;
@@ -318,9 +323,10 @@ int pick_stages(int bn, int E, int lora_R, int act_fused, bool alone) {
 // one that wrote the expert offsets (the GEMM reads them before it waits).
 moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, const void* X, int P, int bn,
                              cudaStream_t stream, bool pdl) {
+  const int cg = gp.cta_pair == 2 ? 2 : 1;
   if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
-  if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
-  gp.stages = pick_stages(bn, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0);
+  if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn / cg)) return MOE_LORA_ERR_CUDA;
+  gp.stages = pick_stages(bn, cg, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0);
   ML_LAUNCH(h, launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
@@ -346,7 +352,8 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
-  if (!make_tmap(h->encode, &gp.tmap_lu, ub, static_cast<uint64_t>(a->S) * P, RU, bn)) return false;
+  if (!make_tmap(h->encode, &gp.tmap_lu, ub, static_cast<uint64_t>(a->S) * P, RU, bn / (gp.cta_pair == 2 ? 2 : 1)))
+    return false;
   gp.lora_fused = 1;
   gp.lora_b_e1 = b_e1 ? 1 : 0;
   gp.lora_kb = (R + 63) / 64;
@@ -602,7 +609,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   // the epilogue's staged LoRA rows grow with the tile: narrow it until two stages fit
   int bn_dn = bn;
   while (!fused && lora && bn_dn > 16 &&
-         gemm_smem_bytes(bn_dn, 2, E, R, 0) > kMaxGemmSmem)
+         gemm_smem_bytes(bn_dn, 1, 2, E, R, 0) > kMaxGemmSmem)
     bn_dn >>= 1;
   st = enqueue_gemm(h, dn, a->w2, act, P, bn_dn, stream, pdl);
   if (st != MOE_LORA_OK) return st;
@@ -735,6 +742,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     gu.N = 2 * I;
     gu.K = H;
     gu.gated = 2;
+    gu.cta_pair = pair_tiles(bn, 2 * I);
     if (fuse_all && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl);
     if (st != MOE_LORA_OK) return st;
@@ -755,6 +763,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     dn.N = H;
     dn.K = I;
     dn.gated = 0;
+    dn.cta_pair = pair_tiles(bn0, H);
     // the down GEMM adds its LoRA stages to the main accumulator, so it keeps the full tile
     if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)) return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, dn, a->w2, act, P, bn0, stream, pdl);

@@ -140,6 +140,20 @@ def test_token_tile_widths_and_ragged_tails(handle, T, E, k):
     _run_and_check(handle, cfg, seed=T)
 
 
+@pytest.mark.parametrize("T,E,k,ranks,flags", [
+    (100, 8, 4, (8, 16), 0),                    # 128-token tiles, fused LoRA, two accumulators + two deltas
+    (520, 8, 4, (8, 16), 0),                    # 160-token gate_up tiles (one delta), 256-token down tiles
+    (520, 8, 4, (8, 16), pkg.FLAG_LORA_OFF),    # 256-token tiles, activation epilogue, plain down
+    (1500, 6, 3, (8, 16, 32, 64), 0),           # several tiles per expert, four slots, ragged tails
+])
+def test_cta_pair_tiles(handle, T, E, k, ranks, flags):
+    """Wide token tiles on CTA pairs (I and H multiples of 128 and 256): each tile's weight
+    rows span two CTAs of a cluster, each loading half the token rows."""
+    cfg = wl.LayerConfig("pair", T=T, H=512, I=256, E=E, top_k=k, ranks=ranks,
+                         scalings=tuple(1.0 / (i + 1) for i in range(len(ranks))), slot_mode="uniform_none10")
+    _run_and_check(handle, cfg, seed=T + flags, flags=flags, lora_off=bool(flags & pkg.FLAG_LORA_OFF))
+
+
 def test_decode_config_full(handle):
     _run_and_check(handle, wl.CONFIGS["decode"], device_inputs=True)
 
