@@ -188,6 +188,20 @@ MLDEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// TMA store of a tile of this CTA's shared memory (row-major, no swizzle) to the tensor at
+// (x, y); completion is tracked per thread with bulk async-groups.
+MLDEV void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+MLDEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+MLDEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }   // <= 1 reading
+MLDEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+MLDEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 MLDEV uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -46,7 +46,7 @@ constexpr int kMaxStages = 16;
 constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxStages tiles ahead
 constexpr int kXchgStride = 17;                       // floats per feature row (padded against bank conflicts)
 constexpr int kXchgFloats = 2 * 128 * kXchgStride;    // two buffers of 128 rows (64 gate, 64 up) x 16 tokens
-constexpr int kYbufFloats = 4 * 16 * 32;              // per epilogue warp: 16 tokens x 32 features
+constexpr int kYbufFloats = 2 * 4 * 16 * 32;          // per epilogue warp, two of: 16 tokens x 32 features
 constexpr uint64_t kPeerDrainNs = 100000;             // 100 us for an aborted odd CTA's copies to land
 
 int gemm_stage_bytes(int rows) { return kAByte + rows * 128; }
@@ -60,7 +60,7 @@ int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused
   const int ring = 4 * (kTileRing + 4);
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
-  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + kYbufFloats * 4;
+  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + 128 + kYbufFloats * 4;   // 128-B aligned
   return 1024 + stages * gemm_stage_bytes(bn / cg) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
          (lora > xchg ? lora : xchg) + ybuf;
 }
@@ -494,9 +494,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     constexpr bool lora = MODE == 1;
     const int R = p.slots.R;
     const int RP8 = (R + 7) & ~7;
-    // this warp's store buffer: [16 tokens][32 features] (its TMEM lane quarter)
-    float* yb = v_s + (lora ? BN * RP8 : 0) + quarter * 512;
+    // this warp's two store buffers: [16 tokens][32 features] (its TMEM lane quarter)
+    float* yb2 = reinterpret_cast<float*>(
+                     (reinterpret_cast<uintptr_t>(v_s + (lora ? BN * RP8 : 0)) + 127) & ~static_cast<uintptr_t>(127)) +
+                 quarter * 1024;   // TMA sources start on 128-byte boundaries
     const int f4 = (lane & 7) * 4;   // the 4 features this lane stores per token row
+    int ychunk = 0;                  // chunks staged so far (alternating buffers)
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = cta0; tile < total; tile += ncta) {
@@ -528,13 +531,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
         for (int j = 0; j < 16; ++j) val[j] = __uint_as_float(r[j]);
         if (lora && col < p.N) lora_expand_chunk(p, lslot, v_s, c, nvalid, e, col, val);
-        // transpose through the warp's buffer (lane = feature on the way in), then each lane
+        // transpose through the warp's buffer (lane = feature on the way in).  A whole fp32
+        // chunk of 16 tokens leaves as one TMA store of 16 x 32 floats; otherwise each lane
         // stores 4 consecutive features of a token: 4 token rows of 128 B per instruction
+        float* yb = yb2 + (ychunk++ & 1) * 512;
+        if (lane == 0) bulk_wait_read_1();   // the store that last read this buffer is done
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 16; ++j) yb[j * 32 + lane] = val[j];
+        const int fcol0 = nt * 128 + quarter * 32;
+        if (p.out_f32 != nullptr && c + 16 <= nvalid) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && fcol0 < p.N) {
+            tma_store_2d(&p.tmap_y, yb, fcol0, q0 + c);
+            bulk_commit();
+          }
+          continue;
+        }
         __syncwarp();
-        const int fcol = nt * 128 + quarter * 32 + f4;
+        const int fcol = fcol0 + f4;
         if (fcol < p.N) {   // N is a multiple of 4, so the whole vector is in range
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -561,6 +577,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     }
   }
 
+  bulk_wait_all();   // the epilogue's TMA stores have read their buffers and landed
   tc_fence_before();
   if constexpr (CG == 2) {   // neither CTA leaves while the pair's MMAs may touch its memory
     cluster_arrive();

@@ -71,6 +71,7 @@ struct GemmParams {
   CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN / cta_pair}
   __nv_bfloat16* out;            // [P, N] bf16 output, or
   float* out_f32;                //   fp32 output when non-null
+  CUtensorMap tmap_y;            // out_f32 [P rows, N cols] fp32, box {32, 16}: full 16-token chunks
   const int32_t* offsets;        // [E + 1]
   uint32_t* status;
   int E, N, K, gated, stages;

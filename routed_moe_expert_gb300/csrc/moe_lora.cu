@@ -326,6 +326,16 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
   const int cg = gp.cta_pair == 2 ? 2 : 1;
   if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn / cg)) return MOE_LORA_ERR_CUDA;
+  if (gp.out_f32 != nullptr && P >= 16) {   // the epilogue stores whole 16-token chunks with TMA
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(gp.N), static_cast<cuuint64_t>(P)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(gp.N) * 4};
+    cuuint32_t box[2] = {32, 16};
+    cuuint32_t estr[2] = {1, 1};
+    if (h->encode(&gp.tmap_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, gp.out_f32, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_LORA_ERR_CUDA;
+  }
   gp.stages = pick_stages(bn, cg, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0);
   ML_LAUNCH(h, launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
