@@ -46,21 +46,22 @@ constexpr int kMaxStages = 16;
 constexpr int kTileRing = 32;   // > kMaxStages: the producer runs at most kMaxStages tiles ahead
 constexpr int kXchgStride = 17;                       // floats per feature row (padded against bank conflicts)
 constexpr int kXchgFloats = 2 * 128 * kXchgStride;    // two buffers of 128 rows (64 gate, 64 up) x 16 tokens
-constexpr int kYbufFloats = 2 * 4 * 16 * 32;          // per epilogue warp, two of: 16 tokens x 32 features
+constexpr int kYbufFloats = 4 * 16 * 32;              // per epilogue warp: 16 tokens x 32 features (x2 for fp32)
 constexpr uint64_t kPeerDrainNs = 100000;             // 100 us for an aborted odd CTA's copies to land
 
 int gemm_stage_bytes(int rows) { return kAByte + rows * 128; }
 
-int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused) {
+int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int f32_out) {
   // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
   // barriers (2*stages), tfull/tempty (4), drain (1), dempty (1); tmem slot + abort flag (16 B);
   // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
   // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes; then,
-  // for the plain epilogues, the four warps' 16 x 32 float store buffers.
+  // for the plain epilogues, the four warps' 16 x 32 float store buffers (two each for an fp32
+  // output, whose whole chunks leave by TMA while the next one is staged).
   const int ring = 4 * (kTileRing + 4);
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
-  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + 128 + kYbufFloats * 4;   // 128-B aligned
+  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + 128 + (f32_out ? 2 : 1) * kYbufFloats * 4;
   return 1024 + stages * gemm_stage_bytes(bn / cg) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
          (lora > xchg ? lora : xchg) + ybuf;
 }
@@ -494,10 +495,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     constexpr bool lora = MODE == 1;
     const int R = p.slots.R;
     const int RP8 = (R + 7) & ~7;
-    // this warp's two store buffers: [16 tokens][32 features] (its TMEM lane quarter)
+    // this warp's store buffers: [16 tokens][32 features] (its TMEM lane quarter), two for fp32
+    const int nybuf = p.out_f32 != nullptr ? 2 : 1;   // as sized by the host
     float* yb2 = reinterpret_cast<float*>(
                      (reinterpret_cast<uintptr_t>(v_s + (lora ? BN * RP8 : 0)) + 127) & ~static_cast<uintptr_t>(127)) +
-                 quarter * 1024;   // TMA sources start on 128-byte boundaries
+                 quarter * nybuf * 512;   // TMA sources start on 128-byte boundaries
     const int f4 = (lane & 7) * 4;   // the 4 features this lane stores per token row
     int ychunk = 0;                  // chunks staged so far (alternating buffers)
     int acc = 0;
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         // transpose through the warp's buffer (lane = feature on the way in).  A whole fp32
         // chunk of 16 tokens leaves as one TMA store of 16 x 32 floats; otherwise each lane
         // stores 4 consecutive features of a token: 4 token rows of 128 B per instruction
-        float* yb = yb2 + (ychunk++ & 1) * 512;
+        float* yb = yb2 + (p.out_f32 != nullptr ? (ychunk++ & 1) * 512 : 0);
         if (lane == 0) bulk_wait_read_1();   // the store that last read this buffer is done
         __syncwarp();
 #pragma unroll
@@ -602,7 +604,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
 template <int BN, int MODE, int CG>
 static cudaError_t launch_mode(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  const int smem = gemm_smem_bytes(BN, CG, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2);
+  const int smem = gemm_smem_bytes(BN, CG, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2,
+                                   p.out_f32 != nullptr);
   cudaError_t err =
       cudaFuncSetAttribute(grouped_gemm_kernel<BN, MODE, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;

@@ -96,7 +96,7 @@ struct GemmParams {
   LoraSlots slots;
 };
 constexpr int kMaxGemmSmem = 227 * 1024;   // dynamic shared memory a CTA may have
-int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused);
+int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int f32_out);
 int gemm_stage_bytes(int rows);   // one stage: 128 weight rows + `rows` token rows, 64 wide
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 

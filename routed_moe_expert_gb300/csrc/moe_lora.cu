@@ -308,11 +308,11 @@ int pair_tiles(int bn, int N) { return (bn >= kPairMinBn && N % 256 == 0) ? 2 : 
 
 // Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
 // room for the side-stream LoRA kernel that runs beside it; the down GEMM runs alone.
-int pick_stages(int bn, int cg, int E, int lora_R, int act_fused, bool alone) {
+int pick_stages(int bn, int cg, int E, int lora_R, int act_fused, bool alone, bool f32_out) {
   // Wide tiles (prefill) keep too few stages in flight to cover the load latency at 200 KB,
   // so they take the whole 227 KB a CTA may have.
   const int budget = bn >= 64 ? kMaxGemmSmem : (bn <= 32 && !alone ? 160 : 200) * 1024;
-  const int fixed = gemm_smem_bytes(bn, cg, 0, E, lora_R, act_fused);
+  const int fixed = gemm_smem_bytes(bn, cg, 0, E, lora_R, act_fused, f32_out);
   int s = (budget - fixed) / (gemm_stage_bytes(bn / cg) + 16);
   if (s > 16) s = 16;
   if (s < 2) s = 2;
@@ -336,7 +336,8 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MOE_LORA_ERR_CUDA;
   }
-  gp.stages = pick_stages(bn, cg, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0);
+  gp.stages = pick_stages(bn, cg, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0,
+                          gp.out_f32 != nullptr);
   ML_LAUNCH(h, launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
@@ -619,7 +620,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   // the epilogue's staged LoRA rows grow with the tile: narrow it until two stages fit
   int bn_dn = bn;
   while (!fused && lora && bn_dn > 16 &&
-         gemm_smem_bytes(bn_dn, 1, 2, E, R, 0) > kMaxGemmSmem)
+         gemm_smem_bytes(bn_dn, 1, 2, E, R, 0, 1) > kMaxGemmSmem)
     bn_dn >>= 1;
   st = enqueue_gemm(h, dn, a->w2, act, P, bn_dn, stream, pdl);
   if (st != MOE_LORA_OK) return st;
