@@ -223,11 +223,55 @@ def moe_lora_permute(handle: Handle, hidden: torch.Tensor, perm: torch.Tensor, t
     return out
 
 
+def check_shapes(hidden, router_logits, w1, w2, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None,
+                 lora_B_dn=None, slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (),
+                 flags=0, num_experts=None):
+    """Raise ValueError unless every tensor has the shape the C ABI reads through its pointer:
+    hidden [T, H], router_logits [T, E], w1 [E, 2I, H], w2 [E, H, I] and, with adapters,
+    lora_A_gu [S, E', R, H], lora_B_gu [S, E, 2I, R], lora_A_dn [S, E, R, I],
+    lora_B_dn [S, E', H, R] (E' = 1 with FLAG_SHARED_OUTER, else E) and slot_idx [T].
+    The library takes raw pointers and cannot check these itself."""
+    def need(t, shape, name):
+        if t is None:
+            raise ValueError(f"{name} is required")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if hidden.dim() != 2 or w1.dim() != 3:
+        raise ValueError("hidden must be [T, H] and w1 [E, 2I, H]")
+    T, H = hidden.shape
+    E, twoI = w1.shape[0], w1.shape[1]
+    if twoI % 2:
+        raise ValueError(f"w1's second dimension (2I) must be even, got {twoI}")
+    I = twoI // 2
+    need(w1, (E, twoI, H), "w1")
+    need(w2, (E, H, I), "w2")
+    if router_logits is not None:
+        need(router_logits, (T, num_experts if num_experts is not None else E), "router_logits")
+    S = len(ranks)
+    if len(scalings) != S:
+        raise ValueError(f"ranks and scalings must have the same length, got {S} and {len(scalings)}")
+    if S == 0:
+        return
+    if lora_A_gu is None or lora_A_gu.dim() != 4:
+        raise ValueError("lora_A_gu [S, E, R, H] is required with adapters")
+    R = lora_A_gu.shape[2]
+    Eo = 1 if (int(flags) & FLAG_SHARED_OUTER) else E
+    need(lora_A_gu, (S, Eo, R, H), "lora_A_gu")
+    need(lora_B_gu, (S, E, twoI, R), "lora_B_gu")
+    need(lora_A_dn, (S, E, R, I), "lora_A_dn")
+    need(lora_B_dn, (S, Eo, H, R), "lora_B_dn")
+    need(slot_idx, (T,), "slot_idx")
+    if any(int(r) > R or int(r) < 0 for r in ranks):
+        raise ValueError(f"every rank must lie in [0, R = {R}], got {list(ranks)}")
+
+
 def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction_bias=None,
               routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
               slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (), flags=0,
               outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1):
     """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
+    check_shapes(hidden, router_logits, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
+                 scalings, flags)
     T, H = hidden.shape
     E, twoI, _ = w1.shape
     S = len(ranks)

@@ -136,3 +136,47 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(B, "LIB_PATH", "/nonexistent/libmoelora.so")
     with pytest.raises(B.MoELoRAError):
         B.lib()
+
+
+def _shape_args(E=4, T=3, H=64, I=32, S=2, R=8, shared=False):
+    import torch
+    Eo = 1 if shared else E
+    return dict(hidden=torch.zeros(T, H), router_logits=torch.zeros(T, E), w1=torch.zeros(E, 2 * I, H),
+                w2=torch.zeros(E, H, I), lora_A_gu=torch.zeros(S, Eo, R, H), lora_B_gu=torch.zeros(S, E, 2 * I, R),
+                lora_A_dn=torch.zeros(S, E, R, I), lora_B_dn=torch.zeros(S, Eo, H, R),
+                slot_idx=torch.zeros(T, dtype=torch.int32), ranks=(8, 4), scalings=(1.0, 0.5),
+                flags=B.FLAG_SHARED_OUTER if shared else 0)
+
+
+def test_binding_checks_shapes_before_taking_pointers():
+    """The library reads every tensor through a raw pointer at the size the shape arguments
+    imply, so the binding rejects any tensor whose shape disagrees (host only, no launch)."""
+    import torch
+    B.check_shapes(**_shape_args())
+    B.check_shapes(**_shape_args(shared=True))
+    bad = [
+        ("lora_A_gu", torch.zeros(2, 1, 8, 64)),     # shared-outer layout without the flag
+        ("lora_B_dn", torch.zeros(2, 1, 64, 8)),
+        ("lora_B_gu", torch.zeros(2, 4, 64, 4)),     # rank dimension disagrees with A
+        ("lora_A_dn", torch.zeros(2, 4, 8, 64)),     # K of the down shrink is I, not H
+        ("w2", torch.zeros(4, 32, 64)),              # transposed
+        ("router_logits", torch.zeros(3, 5)),
+        ("slot_idx", torch.zeros(4, dtype=torch.int32)),
+    ]
+    for name, t in bad:
+        kw = _shape_args()
+        kw[name] = t
+        with pytest.raises(ValueError, match=name):
+            B.check_shapes(**kw)
+    kw = _shape_args(shared=True)
+    kw["flags"] = 0                                  # per-expert flag with shared-outer tensors
+    with pytest.raises(ValueError, match="lora_A_gu"):
+        B.check_shapes(**kw)
+    kw = _shape_args()
+    kw["ranks"] = (8, 16)                            # a rank above R
+    with pytest.raises(ValueError, match="rank"):
+        B.check_shapes(**kw)
+    kw = _shape_args()
+    kw["scalings"] = (1.0,)
+    with pytest.raises(ValueError, match="same length"):
+        B.check_shapes(**kw)
