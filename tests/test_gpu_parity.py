@@ -154,6 +154,20 @@ def test_cta_pair_tiles(handle, T, E, k, ranks, flags):
     _run_and_check(handle, cfg, seed=T + flags, flags=flags, lora_off=bool(flags & pkg.FLAG_LORA_OFF))
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (520, 384, 192, 8, 4),    # neither GEMM can pair (2I/128 and H/128 odd): single-CTA wide tiles
+    (64, 512, 256, 2, 2),     # pair tiles, far fewer tiles than clusters
+    (300, 640, 256, 4, 3),    # gate_up on pairs, down on single CTAs (H/128 = 5 weight tiles)
+])
+def test_wide_tiles_with_and_without_pairs(handle, T, H, I, E, k):
+    """Wide token tiles where the CTA-pair path does not apply (or leaves most clusters
+    idle) give the same results as the oracle."""
+    for flags in (0, pkg.FLAG_LORA_OFF):
+        cfg = wl.LayerConfig("wide", T=T, H=H, I=I, E=E, top_k=k, ranks=(8, 16), scalings=(1.0, 0.5),
+                             slot_mode="uniform_none10")
+        _run_and_check(handle, cfg, seed=T + H + flags, flags=flags, lora_off=bool(flags & pkg.FLAG_LORA_OFF))
+
+
 def test_decode_config_full(handle):
     _run_and_check(handle, wl.CONFIGS["decode"], device_inputs=True)
 
