@@ -249,29 +249,46 @@ def run_gpu(args):
     h_logits = g["router_logits"].cpu().pin_memory()
     h_slot = g["slot_idx"].cpu().pin_memory()
     h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    d_hidden = torch.empty_like(g["hidden"])
-    d_logits = torch.empty_like(g["router_logits"])
-    d_slot = torch.empty_like(g["slot_idx"])
     h2d = h_hidden.numel() * 2 + h_logits.numel() * 2 + h_slot.numel() * 4
     d2h = h_out.numel() * 2
     e2e_steps = max(1, args.steps // 4)
+    # Each step copies its inputs in and its output back.  The copies run on two copy
+    # streams against double-buffered device inputs and outputs, so step i's copies overlap
+    # the neighbouring steps' forwards (which stay in order on the compute stream, sharing
+    # one workspace), as a serving loop would run them.
+    bufs = [dict(hidden=torch.empty_like(g["hidden"]), logits=torch.empty_like(g["router_logits"]),
+                 slot=torch.empty_like(g["slot_idx"]), out=torch.empty_like(out)) for _ in range(2)]
+    cs_in, cs_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in, ev_fwd, ev_d2h = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
 
-    def e2e_step():
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_slot.copy_(h_slot, non_blocking=True)
-        fwd(hidden=d_hidden, logits=d_logits, slot=d_slot)
-        h_out.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b, j = bufs[i % 2], i % 2
+        with torch.cuda.stream(cs_in):
+            cs_in.wait_event(ev_fwd[j])        # the forward that last read these inputs is done
+            b["hidden"].copy_(h_hidden, non_blocking=True)
+            b["logits"].copy_(h_logits, non_blocking=True)
+            b["slot"].copy_(h_slot, non_blocking=True)
+            ev_in[j].record(cs_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_d2h[j])           # this output buffer has been read back
+        fwd(hidden=b["hidden"], logits=b["logits"], slot=b["slot"], o=b["out"])
+        ev_fwd[j].record(stream)
+        with torch.cuda.stream(cs_out):
+            cs_out.wait_event(ev_fwd[j])
+            h_out.copy_(b["out"], non_blocking=True)
+            ev_d2h[j].record(cs_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    cs_in.wait_event(e0)                       # the first copy starts inside the timed region
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_event(ev_d2h[(e2e_steps - 1) % 2])   # ... and the last read-back ends in it
     e1.record(stream)
     torch.cuda.synchronize()
     e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
