@@ -286,12 +286,14 @@ def test_empty_batch(handle):
     assert out.shape == (0, 128)
 
 
-def test_graph_capture_and_replay(handle):
-    """Capture the two-stream forward once, replay with new inputs and slot maps; every
-    replay must match the oracle (regression for the capture-time allocation race of
-    sglang PR #28091, Motivation 3)."""
-    cfg = wl.LayerConfig("graph", T=64, H=512, I=256, E=16, top_k=4, ranks=(8, 16, 32, 4),
-                         scalings=(2.0, 1.0, 0.5, 0.25), slot_mode="uniform_none10")
+@pytest.mark.parametrize("T", [64, 520], ids=["two-stream-narrow", "wide-cta-pairs"])
+def test_graph_capture_and_replay(handle, T):
+    """Capture the forward once, replay with new inputs and slot maps; every replay must
+    match the oracle (regression for the capture-time allocation race of sglang PR #28091,
+    Motivation 3).  At 64 tokens the forward forks the side stream; at 520 tokens both GEMMs
+    run on CTA pairs (cluster launches) with the fused LoRA stages."""
+    cfg = wl.LayerConfig("graph", T=T, H=512, I=256, E=16 if T == 64 else 8, top_k=4, ranks=(8, 16, 32, 4) if T == 64 else (8, 16),
+                         scalings=(2.0, 1.0, 0.5, 0.25) if T == 64 else (1.0, 0.5), slot_mode="uniform_none10")
     inp = wl.make_inputs(cfg, seed=11)
     g = gh.to_dev(inp)
     ws = pkg.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
@@ -305,7 +307,7 @@ def test_graph_capture_and_replay(handle):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         gh.forward(handle, g, out=out, workspace=ws)
-    for i in range(10):
+    for i in range(10 if T == 64 else 3):
         new = wl.make_inputs(cfg, seed=100 + i)
         g["hidden"].copy_(new["hidden"])
         g["router_logits"].copy_(new["router_logits"])
