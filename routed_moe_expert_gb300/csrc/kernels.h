@@ -56,7 +56,9 @@ cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stre
 // Routing as one thread-block cluster of route_cluster_ctas(T) CTAs (no global scratch,
 // no grid barrier); 0 when T is too large and the cooperative grid is used instead.
 int route_cluster_ctas(int T);
-cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream);
+// One thread-block cluster (<= 512 tokens).  It writes the status word once (0 or the first
+// routing error), so with pdl it may start behind the previous forward without a memset.
+cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream, bool pdl = false);
 int route_max_coop_ctas(int E);
 
 // ---------------------------------------------------------------- grouped GEMM

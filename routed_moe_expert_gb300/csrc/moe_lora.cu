@@ -238,7 +238,7 @@ namespace {
 moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, const float* bias, int T, int E,
                               int k, int method, float rsf, int32_t* ids, float* wts, int32_t* offsets,
                               int32_t* perm, int32_t* inv, uint8_t* ws, const Layout& L, cudaStream_t stream,
-                              const moe_lora_routed* ext = nullptr) {
+                              const moe_lora_routed* ext = nullptr, bool pdl = false) {
   if (h->coop_ctas[E] == 0) h->coop_ctas[E] = route_max_coop_ctas(E);
   // above 512 tokens: a cooperative grid of about 64 tokens per CTA
   int grid = (T + 63) / 64;
@@ -274,7 +274,7 @@ moe_lora_status enqueue_route(moe_lora_handle* h, const moe_lora_bf16* logits, c
   const int ctas = route_cluster_ctas(T);   // one thread-block cluster up to 512 tokens
   if (ctas > 0) {
     p.tokens_per_cta = (T + ctas - 1) / ctas;
-    ML_LAUNCH(h, launch_route_cluster(p, ctas, stream), "route cluster launch");
+    ML_LAUNCH(h, launch_route_cluster(p, ctas, stream, pdl), "route cluster launch");
     return MOE_LORA_OK;
   }
   ML_LAUNCH(h, launch_route_align(p, grid, stream), "route_align launch");
@@ -683,7 +683,10 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   const Layout L = layout_for(T, H, I, E, k, a->S > 0 ? a->R : 0, a->S > 0 ? a->S : 0);
   if (workspace_bytes < L.bytes) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
+  // Up to 512 tokens the routing cluster writes the status word itself, so it is launched
+  // behind the previous forward's last kernel with no header memset in between.
+  const bool route_pdl = pdl && T > 0 && route_cluster_ctas(T) > 0;
+  if (!route_pdl) ML_CUDA(cudaMemsetAsync(ws, 0, 256, stream), "cudaMemsetAsync");
   if (T == 0) return MOE_LORA_OK;
 
   const int P = T * k;
@@ -709,7 +712,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
 
   prof(a, MOE_LORA_STAGE_ROUTE, 0, stream);
   st = enqueue_route(h, a->router_logits, a->correction_bias, T, ext ? E + 1 : E, k, a->routing_method,
-                     a->routed_scaling_factor, ids, wts, offsets, perm, inv, ws, L, stream, ext);
+                     a->routed_scaling_factor, ids, wts, offsets, perm, inv, ws, L, stream, ext, route_pdl);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_ROUTE, 1, stream);
 

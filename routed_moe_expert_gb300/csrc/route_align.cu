@@ -151,8 +151,10 @@ MLDEV float packed_key_logit(uint32_t v) {
 
 // Top-k of the tokens [t0, t1): each warp runs kTPW tokens in lockstep, writes ids and
 // weights, records the CTA-local pair ids in ids_s and counts pairs per expert in hist_s.
+// Routing errors (an expert id out of range) are recorded in `err`: the status word, or a
+// per-CTA shared word that the cluster kernel publishes once.
 template <int EPL, int METHOD, int kTPW>
-MLDEV void select_topk(const RouteParams& p, int t0, int t1, int* ids_s, int* hist_s) {
+MLDEV void select_topk(const RouteParams& p, int t0, int t1, int* ids_s, int* hist_s, uint32_t* err) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = p.E, k = p.k;
   if constexpr (METHOD == 2) {
@@ -169,7 +171,7 @@ MLDEV void select_topk(const RouteParams& p, int t0, int t1, int* ids_s, int* hi
         const int gid = static_cast<int>(word >> 16);
         int e = gid - p.local_offset;
         if (gid >= p.ext_experts) {
-          record_status(p.status, kDevBadSlot, kWhereRouteExpert);
+          record_status(err, kDevBadSlot, kWhereRouteExpert);
           e = E - 1;
         } else if (e < 0 || e >= E - 1) {
           e = E - 1;
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_align_kernel(const RouteP
   const int t0 = c * p.tokens_per_cta;
   const int t1 = min(p.T, t0 + p.tokens_per_cta);
 
-  select_topk<EPL, METHOD, kTPW>(p, t0, t1, ids_s, hist_s);
+  select_topk<EPL, METHOD, kTPW>(p, t0, t1, ids_s, hist_s, p.status);
   __syncthreads();
 
   pdl_trigger();   // the permute may launch now; it waits for this kernel to finish
@@ -500,6 +502,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_cluster_kernel(const Rout
   __shared__ int warp_sums[kRouteWarps + 1];
   __shared__ int ids_s[kRouteIdsInSmem];
   __shared__ int wcnt[kRouteWarps * kScatterMaxE];   // expert totals and bases, then scatter cursors
+  __shared__ int err_s;                               // this CTA's first routing error (0: none)
 
   const int tid = threadIdx.x;
   const int C = gridDim.x;   // the grid is one cluster
@@ -507,14 +510,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_cluster_kernel(const Rout
   const int E = p.E;
 
   for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = 0;
+  if (tid == 0) err_s = 0;
+  // Launched behind the previous forward's last kernel: nothing global is read or written
+  // before it has finished.
+  pdl_wait();
   __syncthreads();
   const int t0 = static_cast<int>(c) * p.tokens_per_cta;
   const int t1 = min(p.T, t0 + p.tokens_per_cta);
-  select_topk<EPL, METHOD, 1>(p, t0, t1, ids_s, hist_s);
+  select_topk<EPL, METHOD, 1>(p, t0, t1, ids_s, hist_s, reinterpret_cast<uint32_t*>(&err_s));
   pdl_trigger();   // the permute may launch now; it waits for this kernel to finish
 
   cluster_arrive();   // this CTA's counts are final ...
   cluster_wait();     // ... and so are everyone's
+  // This forward's status word starts here, written once: the first CTA's error, or 0.
+  // Every later kernel touches it only after its own griddepcontrol.wait.
+  if (c == 0 && tid == 0) {
+    uint32_t w = 0;
+    for (int cc = 0; cc < C; ++cc) {
+      const uint32_t v = static_cast<uint32_t>(ld_dsmem(&err_s, static_cast<uint32_t>(cc)));
+      if (w == 0) w = v;
+    }
+    *p.status = w;
+  }
   int* tot_s = wcnt;          // [E] expert totals over the cluster
   int* base_s = wcnt + E;     // [E] pairs of the CTAs before this one
   for (int e = tid; e < E; e += kRouteThreads) {
@@ -548,24 +565,26 @@ int route_cluster_ctas(int T) {
 }
 
 template <int EPL, int METHOD>
-static cudaError_t launch_cluster_epl(const RouteParams& p, int ctas, cudaStream_t stream) {
+static cudaError_t launch_cluster_epl(const RouteParams& p, int ctas, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, route_cluster_kernel<EPL, METHOD>, p);
 }
 
 template <int METHOD>
-static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream);
+static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream, bool pdl);
 
 static int epl_for(int E) { return E <= 128 ? 4 : E <= 256 ? 8 : E <= 384 ? 12 : E <= 512 ? 16 : 32; }
 
@@ -620,21 +639,22 @@ cudaError_t launch_route_align(const RouteParams& p, int grid, cudaStream_t stre
 }
 
 template <int METHOD>
-static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream) {
-  if (METHOD == 2) return launch_cluster_epl<4, METHOD>(p, ctas, stream);
+static cudaError_t launch_cluster_method(const RouteParams& p, int ctas, cudaStream_t stream, bool pdl) {
+  if (METHOD == 2) return launch_cluster_epl<4, METHOD>(p, ctas, stream, pdl);
   switch (epl_for(p.E)) {
-    case 4: return launch_cluster_epl<4, METHOD>(p, ctas, stream);
-    case 8: return launch_cluster_epl<8, METHOD>(p, ctas, stream);
-    case 12: return launch_cluster_epl<12, METHOD>(p, ctas, stream);
-    case 16: return launch_cluster_epl<16, METHOD>(p, ctas, stream);
-    default: return launch_cluster_epl<32, METHOD>(p, ctas, stream);
+    case 4: return launch_cluster_epl<4, METHOD>(p, ctas, stream, pdl);
+    case 8: return launch_cluster_epl<8, METHOD>(p, ctas, stream, pdl);
+    case 12: return launch_cluster_epl<12, METHOD>(p, ctas, stream, pdl);
+    case 16: return launch_cluster_epl<16, METHOD>(p, ctas, stream, pdl);
+    default: return launch_cluster_epl<32, METHOD>(p, ctas, stream, pdl);
   }
 }
 
-cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream) {
+cudaError_t launch_route_cluster(const RouteParams& p, int ctas, cudaStream_t stream, bool pdl) {
   if (ctas < 1 || ctas > kRouteClusterMax) return cudaErrorInvalidValue;
-  if (p.method == 2) return launch_cluster_method<2>(p, ctas, stream);
-  return p.method == 1 ? launch_cluster_method<1>(p, ctas, stream) : launch_cluster_method<0>(p, ctas, stream);
+  if (p.method == 2) return launch_cluster_method<2>(p, ctas, stream, pdl);
+  return p.method == 1 ? launch_cluster_method<1>(p, ctas, stream, pdl)
+                       : launch_cluster_method<0>(p, ctas, stream, pdl);
 }
 
 }  // namespace mlk
