@@ -278,6 +278,25 @@ def test_slot_out_of_range_reported(handle):
     assert pkg.moe_lora_check_status(ws)[0] == 0
 
 
+@pytest.mark.parametrize("T,E", [(64, 32), (256, 16)], ids=["narrow-two-stream", "wide-cta-pairs"])
+def test_back_to_back_forwards_share_a_workspace(handle, T, E):
+    """Three forwards enqueued on one stream and one workspace with no sync between them.
+    Each routing cluster starts behind the previous forward's finalize (a programmatic
+    launch), so it must not disturb the routing buffers that finalize still reads."""
+    cfg = wl.LayerConfig("b2b", T=T, H=512, I=256, E=E, top_k=4, ranks=(8, 16), scalings=(1.0, 0.5),
+                         slot_mode="uniform_none10")
+    ins = [wl.make_inputs(cfg, seed=s) for s in (31, 32, 33)]
+    gs = [gh.to_dev(i) for i in ins]
+    ws = pkg.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
+    outs = [torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda") for _ in gs]
+    for g, o in zip(gs, outs):
+        gh.forward(handle, g, out=o, workspace=ws)
+    st, word = pkg.moe_lora_check_status(ws)
+    assert st == 0, f"device status {word:#x}"
+    for i, (inp, o) in enumerate(zip(ins, outs)):
+        gh.assert_close(o.float().cpu().numpy(), gh.oracle(inp)["out"], f"forward {i}")
+
+
 def test_empty_batch(handle):
     cfg = wl.LayerConfig("empty", T=0, H=128, I=64, E=4, top_k=2, ranks=(4,), scalings=(1.0,))
     g = gh.to_dev(wl.make_inputs(cfg, seed=1))
