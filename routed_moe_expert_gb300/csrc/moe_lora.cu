@@ -2,11 +2,15 @@
 // layout, tensor maps, stream fork/join and the launch sequence of the layer.
 //
 // Launch sequence of moe_lora_forward (sglang PR #28466 "bf16 MoE-LoRA for trtllm
-// backend", section 1 flows (A) single-stream and (B) two-stream):
-//   main: memset(status) -> route_align -> [fork] -> permute -> gate_up GEMM
-//         -> [join on the LoRA-ready event] -> activation -> down-LoRA shrink
-//         -> down GEMM (down-LoRA expand in its epilogue, fp32 out) -> finalize
+// backend", section 1 flows (A) single-stream and (B) two-stream), narrow token tiles:
+//   main: route -> [fork] -> permute -> gate_up GEMM -> [join on the LoRA-ready event]
+//         -> activation + down-LoRA shrink -> down GEMM (down-LoRA expand in its
+//         epilogue, fp32 out) -> finalize
 //   side: [wait fork] -> gate_up LoRA shrink + expand (one kernel) -> [record ready]
+// Wide token tiles, one stream: route -> permute -> tensor-core shrink -> gate_up GEMM
+// (LoRA expand stages, activation epilogue) -> tensor-core shrink -> down GEMM (LoRA
+// expand stages) -> finalize.  Kernels are programmatic dependents of their predecessors;
+// above 512 tokens a memset of the workspace header precedes the (cooperative) routing.
 // Every buffer the side stream touches lives in the caller's workspace, which exists
 // before the fork, so nothing is allocated while a graph may be capturing (the
 // multi-slot replay bug of sglang PR #28091, Motivation 3, cannot arise).
