@@ -725,7 +725,6 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   if (lora) slots = make_slots(a);
   const int R = lora ? a->R : 0;
   const bool so = (a->flags & MOE_LORA_FLAG_SHARED_OUTER) != 0;   // one A_gu, one B_dn per slot
-  const int RU = (R + 7) & ~7;
   __nv_bfloat16* ub = reinterpret_cast<__nv_bfloat16*>(ws + L.ub);
   // Fully fused LoRA: both shrinks on the tensor cores, both expands inside the GEMMs, the
   // activation in the gate_up GEMM's epilogue.  Needs a TMA-able rank stride, few slots and
