@@ -297,6 +297,23 @@ def test_back_to_back_forwards_share_a_workspace(handle, T, E):
         gh.assert_close(o.float().cpu().numpy(), gh.oracle(inp)["out"], f"forward {i}")
 
 
+@pytest.mark.parametrize("T,E", [(64, 32), (96, 16), (520, 8), (1024, 8)],
+                         ids=["narrow", "wide-32", "wide-cta-pairs", "cooperative-routing"])
+def test_programmatic_launches_change_nothing(handle, T, E):
+    """The programmatic launch chain only moves kernel start times: with MOE_LORA_FLAG_NO_PDL
+    (plain stream order, the header memset before the routing) every output is bitwise the
+    same, on every placement and both routing paths."""
+    cfg = wl.LayerConfig("pdl", T=T, H=512, I=256, E=E, top_k=4, ranks=(8, 16), scalings=(1.0, 0.5),
+                         slot_mode="uniform_none10")
+    g = gh.to_dev(wl.make_inputs(cfg, seed=T))
+    ws = pkg.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
+    a = gh.forward(handle, g, workspace=ws).clone()
+    b = gh.forward(handle, g, workspace=ws, flags=pkg.FLAG_NO_PDL).clone()
+    c = gh.forward(handle, g, workspace=ws).clone()
+    assert pkg.moe_lora_check_status(ws)[0] == 0
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
 def test_empty_batch(handle):
     cfg = wl.LayerConfig("empty", T=0, H=128, I=64, E=4, top_k=2, ranks=(4,), scalings=(1.0,))
     g = gh.to_dev(wl.make_inputs(cfg, seed=1))
