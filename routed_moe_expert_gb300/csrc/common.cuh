@@ -196,6 +196,13 @@ MLDEV void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int
                "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                : "memory");
 }
+// The same with an L2 policy for the stored lines.
+MLDEV void tma_store_2d_hint(const CUtensorMap* map, const void* smem_src, int x, int y, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "l"(policy)
+               : "memory");
+}
 MLDEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 MLDEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }   // <= 1 reading
 MLDEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

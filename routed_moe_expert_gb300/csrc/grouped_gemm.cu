@@ -546,7 +546,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && fcol0 < p.N) {
-            tma_store_2d(&p.tmap_y, yb, fcol0, q0 + c);
+            // wide tiles: fp32 y stays in L2 as long as it can, since the finalize reads it next
+            if constexpr (BN >= 64) tma_store_2d_hint(&p.tmap_y, yb, fcol0, q0 + c, l2_policy_evict_last());
+            else tma_store_2d(&p.tmap_y, yb, fcol0, q0 + c);
             bulk_commit();
           }
           continue;
