@@ -203,6 +203,12 @@ MLDEV void tma_store_2d_hint(const CUtensorMap* map, const void* smem_src, int x
                "r"(smem_u32(smem_src)), "r"(x), "r"(y), "l"(policy)
                : "memory");
 }
+// 16-byte global store with an L2 policy for the stored line.
+MLDEV void st_global_v4_hint(void* p, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(policy)
+               : "memory");
+}
 MLDEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 MLDEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }   // <= 1 reading
 MLDEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

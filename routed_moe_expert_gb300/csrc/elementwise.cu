@@ -22,7 +22,9 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
   if (slot_out != nullptr && (threadIdx.x & 31) == 0) slot_out[q] = slot_idx[t];
   const uint4* src = x + static_cast<size_t>(t) * H8;
   uint4* dst = xp + static_cast<size_t>(q) * H8;
-  for (int v = threadIdx.x & 31; v < H8; v += 32) dst[v] = __ldg(src + v);
+  // the permuted rows are read next (LoRA shrink, gate_up GEMM): keep them in L2 if they fit
+  const uint64_t pol = l2_policy_evict_last();
+  for (int v = threadIdx.x & 31; v < H8; v += 32) st_global_v4_hint(dst + v, __ldg(src + v), pol);
 }
 
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
