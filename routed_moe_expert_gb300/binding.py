@@ -225,7 +225,7 @@ def moe_lora_permute(handle: Handle, hidden: torch.Tensor, perm: torch.Tensor, t
 
 def check_shapes(hidden, router_logits, w1, w2, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None,
                  lora_B_dn=None, slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (),
-                 flags=0, num_experts=None):
+                 flags=0, num_experts=None, correction_bias=None):
     """Raise ValueError unless every tensor has the shape the C ABI reads through its pointer:
     hidden [T, H], router_logits [T, E], w1 [E, 2I, H], w2 [E, H, I] and, with adapters,
     lora_A_gu [S, E', R, H], lora_B_gu [S, E, 2I, R], lora_A_dn [S, E, R, I],
@@ -247,6 +247,8 @@ def check_shapes(hidden, router_logits, w1, w2, lora_A_gu=None, lora_B_gu=None, 
     need(w2, (E, H, I), "w2")
     if router_logits is not None:
         need(router_logits, (T, num_experts if num_experts is not None else E), "router_logits")
+    if correction_bias is not None:
+        need(correction_bias, (router_logits.shape[1] if router_logits is not None else E,), "correction_bias")
     S = len(ranks)
     if len(scalings) != S:
         raise ValueError(f"ranks and scalings must have the same length, got {S} and {len(scalings)}")
@@ -271,7 +273,7 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
               outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1):
     """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
     check_shapes(hidden, router_logits, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
-                 scalings, flags)
+                 scalings, flags, correction_bias=correction_bias)
     T, H = hidden.shape
     E, twoI, _ = w1.shape
     S = len(ranks)

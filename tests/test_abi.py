@@ -180,3 +180,9 @@ def test_binding_checks_shapes_before_taking_pointers():
     kw["scalings"] = (1.0,)
     with pytest.raises(ValueError, match="same length"):
         B.check_shapes(**kw)
+    kw = _shape_args()
+    kw["correction_bias"] = torch.zeros(4)           # [E]
+    B.check_shapes(**kw)
+    kw["correction_bias"] = torch.zeros(5)
+    with pytest.raises(ValueError, match="correction_bias"):
+        B.check_shapes(**kw)
