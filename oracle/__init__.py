@@ -4,4 +4,6 @@ benchmark's CPU-baseline leg; never by the product path."""
 from .moe_lora_oracle import (  # noqa: F401
     RENORMALIZE, DEEPSEEK_V3, round_bf16, exp_f32, sigmoid_f32, route, align, silu,
     moe_lora_forward, pack_topk, unpack_topk, moe_lora_forward_routed,
+    E4M3_MAX, FP8_BLOCK, e4m3_decode, round_e4m3, quant_act_fp8, dequant_act_fp8, fake_quant_act_fp8,
+    dequant_weight_fp8, Fp8Experts, moe_lora_forward_fp8,
 )

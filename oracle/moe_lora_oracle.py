@@ -49,6 +49,12 @@ Readings of points the pages leave open (each also listed in the design notes):
     map to permuted index -1) and are aligned after the last local expert; with
     do_finalize=False the returned per-pair down output already holds the down-LoRA
     delta, unweighted (what the vLLM page's _finalize_with_w2_lora adds back).
+  * FP8 path (moe_lora_forward_fp8): e4m3 codes without infinities (largest finite
+    value 448); one float32 weight scale per 128 x 128 block; the gate_up and down GEMM
+    inputs quantised per token in groups of 128 along K with scale
+    max(amax, 1e-10) / 448 and codes e4m3(v / s), both float32 operations, rounded to
+    nearest even and saturated at +-448; the down GEMM's input is the bf16 activation;
+    the LoRA chain reads the unquantised bf16 x and a; the LoRA weights stay bf16.
 """
 from __future__ import annotations
 
@@ -192,10 +198,12 @@ def _f64(a):
 
 
 def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slots,
-             ranks, scalings, lora_off, inter, local=None, shared_outer=False):
+             ranks, scalings, lora_off, inter, local=None, shared_outer=False, act_quant=None):
     """Per-pair expert math for the pairs of tokens `tok` (see moe_lora_forward).  With
-    `local` (a bool mask [T, k]) only those pairs are evaluated.  Returns
-    {(t, j): (y + dd, a)} in float64 (a holds bf16 values)."""
+    `local` (a bool mask [T, k]) only those pairs are evaluated.  With `act_quant` (the
+    FP8 path) the two base GEMMs read act_quant(x) and act_quant(a) instead of x and a;
+    the LoRA shrinks still read x and a.  Returns {(t, j): (y + dd, a)} in float64 (a
+    holds bf16 values)."""
     S = len(ranks)
     eo = (lambda e: 0) if shared_outer else (lambda e: e)   # expert index of A_gu and B_dn
     res = {}
@@ -214,7 +222,8 @@ def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lor
         W1 = _f64(w1[e])                                         # [2I, H]
         W2 = _f64(w2[e])                                         # [H, I]
         I = W1.shape[0] // 2
-        g = round_bf16(xe @ W1.T)                                # [n, 2I]
+        xg = xe if act_quant is None else act_quant(xe)          # the gate_up GEMM's input
+        g = round_bf16(xg @ W1.T)                                # [n, 2I]
         d = np.zeros_like(g)
         lora_rows = []
         if not lora_off and S > 0:
@@ -230,7 +239,8 @@ def _experts(x, ids, w, top_k, tok, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lor
                 d[m] = round_bf16(sc * (u @ B.T))
                 lora_rows.append((s, r, sc, m))
         a = round_bf16(silu(g[:, :I] + d[:, :I]) * (g[:, I:] + d[:, I:]))   # [n, I]
-        y = a @ W2.T                                             # [n, H]
+        ag = a if act_quant is None else act_quant(a)            # the down GEMM's input
+        y = ag @ W2.T                                            # [n, H]
         dd = np.zeros_like(y)
         for s, r, sc, m in lora_rows:
             A = _f64(lora_A_dn[s, e])[:r]                        # [r, I]
@@ -392,3 +402,137 @@ def moe_lora_forward_routed(hidden, packed_topk_ids, w1, w2, top_k, num_experts,
     res.update(gemm2_output=gemm2, activation=act, expert_weights=w)
     return res
 
+
+
+# ----------------------------------------------------------------------------
+# FP8 block-scale path: e4m3 weights with one float32 scale per 128 x 128 block, and
+# the two GEMM inputs quantised per token in groups of 128 along K
+# ----------------------------------------------------------------------------
+# The pages' FP8 flow (sglang PR #28466, section 1 flow (A) diagram: the FP8 flow has a
+# per_token_group_quant_fp8 step before the MoE op and a post-activation quant before
+# the down GEMM; its summary: that path "requires FP8 block quant"; sglang PR #27329
+# "Experimental fast LoRA path", Optimizations: the FP8 target checkpoint
+# Qwen3.5-35B-A3B-FP8).  The LoRA chain of that flow runs on the bf16 hidden states and
+# on the bf16 activation (the activation kernel "writes activation_lora_input" before
+# the quant), so only the base GEMMs see quantised inputs.
+
+E4M3_MAX = 448.0          # largest finite e4m3 value
+FP8_BLOCK = 128           # weight blocks are 128 x 128; activation groups are 128 wide
+FP8_EPS = np.float32(1e-10)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each e4m3 code byte (the OCP 8-bit floating point format E4M3: a sign bit,
+    4 exponent bits with bias 7 and 3 mantissa bits; exponent field 0 holds the
+    subnormals m * 2**-9; there are no infinities and S.1111.111 is NaN), float64."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where((c >> 7) != 0, -1.0, 1.0)
+    ex = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(ex == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(ex - 7.0))
+    mag = np.where((ex == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Nearest e4m3 value of each float64 value, ties to the even mantissa, saturating at
+    +-448 (a "satfinite" conversion); NaN stays NaN."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    with np.errstate(invalid="ignore", over="ignore"):
+        _, e = np.frexp(ax)             # ax = f * 2**e with 0.5 <= f < 1
+        e = np.maximum(e - 1, -6)       # leading-bit exponent; below 2**-6 the step is 2**-9
+        quantum = np.exp2(e - 3.0)      # 3 mantissa bits
+        q = np.rint(ax / quantum) * quantum
+    q = np.minimum(q, E4M3_MAX)
+    q = np.where(np.isnan(x), np.nan, q)
+    return np.copysign(q, x)
+
+
+def quant_act_fp8(v, group: int = FP8_BLOCK):
+    """Quantise rows of activations per token in groups of `group` consecutive values.
+
+    For a group with largest magnitude amax, the scale is s = max(amax, 1e-10) / 448, and
+    the code of a value v is e4m3(v / s).  The scale and the quotient are float32
+    operations rounded to nearest, so the codes are a function of the float32 inputs.
+    Returns (q [n, K] float64 values on the e4m3 grid, s [n, K / group] float32).
+    """
+    v32 = np.asarray(v, dtype=np.float32)
+    n, K = v32.shape
+    if K % group:
+        raise ValueError("K must be a multiple of the group size")
+    g = v32.reshape(n, K // group, group)
+    amax = np.abs(g).max(axis=2)
+    s = (np.maximum(amax, FP8_EPS) / np.float32(E4M3_MAX)).astype(np.float32)
+    quot = (g / s[:, :, None]).astype(np.float32)
+    q = round_e4m3(quot.astype(np.float64))
+    return q.reshape(n, K), s
+
+
+def dequant_act_fp8(q, s, group: int = FP8_BLOCK) -> np.ndarray:
+    """q * s with each value's group scale (float64; the products are exact)."""
+    q = np.asarray(q, dtype=np.float64)
+    n, K = q.shape
+    return (q.reshape(n, K // group, group) * np.asarray(s, np.float64)[:, :, None]).reshape(n, K)
+
+
+def fake_quant_act_fp8(v, group: int = FP8_BLOCK) -> np.ndarray:
+    """The values a base GEMM of the FP8 path reads for activations v: dequant(quant(v))."""
+    q, s = quant_act_fp8(v, group)
+    return dequant_act_fp8(q, s, group)
+
+
+def dequant_weight_fp8(codes, scale, block: int = FP8_BLOCK) -> np.ndarray:
+    """W[n, k] = e4m3(codes[n, k]) * scale[n // block, k // block], float64."""
+    w = e4m3_decode(codes)
+    N, K = w.shape
+    sc = np.asarray(scale, dtype=np.float64)
+    rows = np.arange(N) // block
+    cols = np.arange(K) // block
+    return w * sc[rows[:, None], cols[None, :]]
+
+
+class Fp8Experts:
+    """w[e] -> the dequantised float64 weight of expert e, from codes [E, N, K] (uint8
+    e4m3 bit patterns) and scales [E, N/128, K/128] (any arrays or CPU tensors indexable
+    by expert, so large weights can be streamed expert by expert)."""
+
+    def __init__(self, codes, scales):
+        self.codes, self.scales = codes, scales
+
+    def __getitem__(self, e):
+        return dequant_weight_fp8(np.asarray(self.codes[e]), np.asarray(self.scales[e]))
+
+    def __len__(self):
+        return len(self.codes)
+
+
+def moe_lora_forward_fp8(hidden, router_logits, w1_q, w1_scale, w2_q, w2_scale, top_k, method=RENORMALIZE,
+                         correction_bias=None, routed_scaling_factor=1.0,
+                         lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
+                         slot_idx=None, ranks=(), scalings=(), lora_off=False, tokens=None,
+                         shared_outer=False):
+    """The layer of moe_lora_forward with FP8 block-scale expert weights.
+
+    w1_q [E, 2I, H] and w2_q [E, H, I] hold e4m3 codes, w1_scale [E, 2I/128, H/128] and
+    w2_scale [E, H/128, I/128] their block scales.  Per pair, with every other step as in
+    moe_lora_forward:
+      g  = bf16(W1[e] @ fq(x_t))      W1 = dequant(w1_q[e], w1_scale[e]), fq = fake_quant_act_fp8
+      y  = W2[e] @ fq(a)              W2 = dequant(w2_q[e], w2_scale[e])
+    The LoRA shrinks read the bf16 x_t and a.  Since sum_b s_x[b] s_w[b] sum_{k in b} q_x q_w
+    equals the product of the two dequantised operands, the block-scaled GEMM is written as
+    that product.
+    """
+    x = _f64(hidden)
+    T, H = x.shape
+    ids, w = route(router_logits, top_k, method, correction_bias, routed_scaling_factor)
+    E = np.asarray(router_logits).shape[1]
+    offsets, perm, inv = align(ids, E)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
+    rows = _experts(x, ids, w, top_k, tok, Fp8Experts(w1_q, w1_scale), Fp8Experts(w2_q, w2_scale), lora_A_gu,
+                    lora_B_gu, lora_A_dn, lora_B_dn, slots, ranks, scalings, lora_off, None,
+                    shared_outer=shared_outer, act_quant=fake_quant_act_fp8)
+    out_acc = _finalize(tok, top_k, H, w, rows)
+    return dict(out=round_bf16(out_acc), topk_ids=ids, topk_weights=w, expert_offsets=offsets, perm=perm,
+                inv=inv, tokens=tok)

@@ -197,3 +197,24 @@ def packed_routing_words(ids: torch.Tensor, weights: torch.Tensor) -> torch.Tens
     v = (ids.to(torch.int64) << 16) | bits
     v = torch.where(v >= 2 ** 31, v - 2 ** 32, v)      # the same 32 bits as a signed int32
     return v.to(torch.int32)
+
+
+def quantize_weights_fp8(w: torch.Tensor, block: int = 128):
+    """Block-FP8 copy of expert weights w [E, N, K] (N, K multiples of `block`), as an FP8
+    block-quantised checkpoint stores them: per block x block tile a float32 scale
+    amax / 448 and e4m3 codes of w / scale (torch's float8_e4m3fn conversion).  Returns
+    (codes [E, N, K] uint8 bit patterns, scales [E, N/block, K/block] float32) on w's
+    device, one expert at a time so the float32 temporaries stay small."""
+    E, N, K = w.shape
+    if N % block or K % block:
+        raise ValueError("N and K must be multiples of the block size")
+    codes = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((E, N // block, K // block), dtype=torch.float32, device=w.device)
+    for e in range(E):
+        wb = w[e].float().reshape(N // block, block, K // block, block)
+        amax = wb.abs().amax(dim=(1, 3)).clamp(min=1e-12)
+        s = amax / 448.0
+        q = (wb / s[:, None, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+        codes[e] = q.reshape(N, K).view(torch.uint8)
+        scales[e] = s
+    return codes, scales

@@ -36,9 +36,11 @@ def topk_bruteforce(keys, k):
 
 
 def dense_layer(x, logits, w1, w2, top_k, method, bias=None, rsf=1.0, A_gu=None, B_gu=None,
-                A_dn=None, B_dn=None, slot_idx=None, ranks=(), scalings=(), keys_fn=None, shared_outer=False):
+                A_dn=None, B_dn=None, slot_idx=None, ranks=(), scalings=(), keys_fn=None, shared_outer=False,
+                quant=None):
     """Dense evaluation on nested lists.  `keys_fn(logit_row)` gives the DeepSeekV3
-    selection keys (the float32 key definition is pinned separately)."""
+    selection keys (the float32 key definition is pinned separately).  `quant(row)`, if
+    given, is applied to the two base GEMMs' inputs (the FP8 path)."""
     T, H = len(x), len(x[0])
     E = len(w1)
     I = len(w1[0]) // 2
@@ -62,12 +64,12 @@ def dense_layer(x, logits, w1, w2, top_k, method, bias=None, rsf=1.0, A_gu=None,
         weight_of = {e: wv for e, wv in zip(ids, wts)}
         s = -1 if slot_idx is None else int(slot_idx[t])
         out.append(_dense_token(x[t], range(E), weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings,
-                                shared_outer=shared_outer))
+                                shared_outer=shared_outer, quant=quant))
     return out, ids_all, w_all
 
 
 def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, ranks, scalings, gid=lambda e: e,
-                 shared_outer=False):
+                 shared_outer=False, quant=None):
     """One token through every expert e in `experts` (weight index e, routing id gid(e)),
     masked by the routing: bf16(fsum over e of mask * w * (y + dd)).  shared_outer: A_gu
     and B_dn hold one weight set per slot (index 0) used by every expert."""
@@ -75,8 +77,9 @@ def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, rank
     I = len(w1[0]) // 2
     use_lora = (s >= 0 and s < len(ranks) and ranks[s] > 0 and scalings[s] != 0.0)
     terms = []
+    xg = xt if quant is None else quant(xt)      # the gate_up GEMM's input
     for e in experts:                            # dense: every expert
-        g = [bf16_exact(dot(w1[e][n], xt)) for n in range(2 * I)]
+        g = [bf16_exact(dot(w1[e][n], xg)) for n in range(2 * I)]
         if use_lora:
             r, sc = ranks[s], scalings[s]
             u = [dot(A_gu[s][0 if shared_outer else e][q], xt) for q in range(r)]
@@ -87,7 +90,8 @@ def _dense_token(xt, experts, weight_of, w1, w2, s, A_gu, B_gu, A_dn, B_dn, rank
         for i in range(I):
             zg = g[i] + d[i]
             a.append(bf16_exact(zg * sigmoid(zg) * (g[I + i] + d[I + i])))
-        y = [dot(w2[e][h], a) for h in range(H)]
+        ag = a if quant is None else quant(a)    # the down GEMM's input
+        y = [dot(w2[e][h], ag) for h in range(H)]
         if use_lora:
             v = [dot(A_dn[s][e][q], a) for q in range(r)]
             dd = [sc * dot([B_dn[s][0 if shared_outer else e][h][q] for q in range(r)], v) for h in range(H)]
@@ -112,3 +116,30 @@ def dense_layer_routed(x, ids_all, w_all, local_offset, w1, w2, A_gu=None, B_gu=
                                 scalings, gid=lambda e: local_offset + e))
     return out
 
+
+
+def fake_quant_torch(row, group=128):
+    """FP8 group quantisation of one row, built on torch's float8_e4m3fn conversion
+    instead of the oracle's own e4m3 rounding: per group of `group` values,
+    s = max(amax, 1e-10) / 448 and q = fp8(clamp(v / s, +-448)) in float32, returned
+    dequantised (q * s, exact in Python floats)."""
+    import torch
+    out = []
+    for g0 in range(0, len(row), group):
+        t = torch.tensor(row[g0:g0 + group], dtype=torch.float32)
+        amax = t.abs().max()
+        s = torch.maximum(amax, torch.tensor(1e-10, dtype=torch.float32)) / torch.tensor(448.0)
+        q = (t / s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).to(torch.float64)
+        out.extend(float(v) * float(s) for v in q)
+    return out
+
+
+def dequant_weight_torch(codes, scales, block=128):
+    """Nested-list weight [N][K] from uint8 codes [N, K] and block scales, decoded by
+    torch's float8_e4m3fn view (not the oracle's decoder)."""
+    import torch
+    c = torch.as_tensor(codes, dtype=torch.uint8)
+    w = c.view(torch.float8_e4m3fn).to(torch.float64)
+    s = torch.as_tensor(scales, dtype=torch.float64)
+    N, K = w.shape
+    return [[float(w[n, k]) * float(s[n // block, k // block]) for k in range(K)] for n in range(N)]

@@ -185,3 +185,53 @@ def test_mutant_is_caught(name, old, new):
         except Exception:
             results.append(False)
     assert not all(results), f"mutant '{name}' passed every pin"
+
+
+# FP8 block-scale path: each mutant must fail the e4m3 pins or the FP8 dense brute force
+FP8_MUTATIONS = [
+    ("e4m3 exponent bias 8", "(1.0 + m / 8.0) * np.exp2(ex - 7.0)", "(1.0 + m / 8.0) * np.exp2(ex - 8.0)"),
+    ("e4m3 ties away from zero", "q = np.rint(ax / quantum) * quantum", "q = np.floor(ax / quantum + 0.5) * quantum"),
+    ("e4m3 without saturation", "q = np.minimum(q, E4M3_MAX)", "q = q"),
+    ("e4m3 without the subnormal step", "e = np.maximum(e - 1, -6)", "e = e - 1"),
+    ("weight block scale transposed", "return w * sc[rows[:, None], cols[None, :]]",
+     "return w * sc.T[rows[:, None] % sc.shape[1], cols[None, :] % sc.shape[0]]"),
+    ("activation scale from the whole row", "amax = np.abs(g).max(axis=2)",
+     "amax = np.repeat(np.abs(g).max(axis=(1, 2))[:, None], K // group, axis=1)"),
+    ("scale without the 448", "s = (np.maximum(amax, FP8_EPS) / np.float32(E4M3_MAX)).astype(np.float32)",
+     "s = np.maximum(amax, FP8_EPS).astype(np.float32)"),
+    ("down GEMM input not quantised", "ag = a if act_quant is None else act_quant(a)", "ag = a"),
+    ("gate_up LoRA shrink reads the quantised input", "u = xe[m] @ A.T", "u = xg[m] @ A.T"),
+]
+
+
+def _e4m3_check(orc):
+    codes = np.arange(256)
+    d = orc.e4m3_decode(codes)
+    ref = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    if not (np.array_equal(np.isnan(d), np.isnan(ref)) and np.array_equal(d[~np.isnan(d)], ref[~np.isnan(ref)])):
+        return False
+    x = np.random.default_rng(0).uniform(-500, 500, 4000).astype(np.float32)
+    x = np.concatenate([x, x * 1e-3]).astype(np.float32)
+    ref = torch.from_numpy(x).clamp(-448, 448).to(torch.float8_e4m3fn).double().numpy()
+    return np.array_equal(orc.round_e4m3(x.astype(np.float64)), ref)
+
+
+def test_unmutated_oracle_passes_the_fp8_checks():
+    from oracle import moe_lora_oracle as good
+    from test_oracle_fp8 import fp8_dense_check
+    assert _e4m3_check(good)
+    assert all(fp8_dense_check(good, s) for s in range(2))
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name,old,new", FP8_MUTATIONS, ids=[m[0] for m in FP8_MUTATIONS])
+def test_fp8_mutant_is_caught(name, old, new):
+    from test_oracle_fp8 import fp8_dense_check
+    m = _mutant(old, new)
+    results = []
+    for check in (lambda: _e4m3_check(m), *[(lambda s=s: fp8_dense_check(m, s)) for s in range(2)]):
+        try:
+            results.append(bool(check()))
+        except Exception:
+            results.append(False)
+    assert not all(results), f"mutant '{name}' passed every FP8 pin"
