@@ -156,6 +156,12 @@ def run_gpu(args):
     inp = wl.make_inputs(cfg, seed=args.seed, device="cuda")
     g = inp
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    # --fp8: the same layer with block-FP8 expert weights quantised from the drawn ones
+    w8 = None
+    if args.fp8:
+        w1q, w1s = wl.quantize_weights_fp8(g["w1"])
+        w2q, w2s = wl.quantize_weights_fp8(g["w2"])
+        w8 = (w1q, w1s, w2q, w2s)
     P = T * k
     h = pkg.Handle(local)
     ws = pkg.alloc_workspace(T, H, I, E, k, cfg.S, cfg.R)
@@ -165,13 +171,16 @@ def run_gpu(args):
 
     def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
         flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
-        return pkg.moe_lora_forward(
-            h, g["hidden"] if hidden is None else hidden, g["router_logits"] if logits is None else logits,
-            g["w1"], g["w2"], k, routing_method=cfg.method, correction_bias=g["correction_bias"],
-            routed_scaling_factor=cfg.rsf, lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"],
-            lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"] if slot is None else slot,
-            ranks=cfg.ranks, scalings=cfg.scalings, flags=flags, out=o, workspace=ws, prof_events=prof,
-            outputs=outputs)
+        hid = g["hidden"] if hidden is None else hidden
+        lg = g["router_logits"] if logits is None else logits
+        kw = dict(routing_method=cfg.method, correction_bias=g["correction_bias"],
+                  routed_scaling_factor=cfg.rsf, lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"],
+                  lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"],
+                  slot_idx=g["slot_idx"] if slot is None else slot, ranks=cfg.ranks, scalings=cfg.scalings,
+                  flags=flags, out=o, workspace=ws, prof_events=prof, outputs=outputs)
+        if w8 is not None:
+            return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw)
+        return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw)
 
     # touched experts (routing is fixed for the fixed input)
     fwd(outputs=dict(expert_offsets=offsets))
@@ -182,8 +191,10 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {word:#x}")
 
-    # algorithmic bytes / flops
-    w_bytes_expert = 3 * H * I * 2
+    # algorithmic bytes / flops (FP8: one byte per weight plus a float per 128 x 128 block,
+    # the permuted hidden rows as codes plus a float per 128 values)
+    wb = 1 if w8 is not None else 2
+    w_bytes_expert = 3 * H * I * wb + (3 * H * I // (128 * 128) * 4 if w8 is not None else 0)
     lora_blocks = 0
     slots = g["slot_idx"].cpu().numpy()
     ids_np = None
@@ -201,7 +212,10 @@ def run_gpu(args):
     step_bytes = touched * w_bytes_expert + lora_blocks + io_bytes
     step_flops = 2 * 3 * H * I * P + sum(2 * cfg.ranks[max(int(slots[t]), 0)] * (2 * H + 3 * I) * k
                                          for t in range(T) if cfg.S > 0 and slots[t] >= 0)
-    gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + P * 2 * I * 2   # weights + xp read + g write
+    if w8 is None:
+        gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + P * 2 * I * 2   # weights + xp read + g write
+    else:
+        gu_bytes = touched * (2 * I * H + 2 * I * H // (128 * 128) * 4) + P * H + P * H // 128 * 4 + P * 2 * I * 2
     gu_flops = 2 * 2 * I * H * P
 
     for _ in range(args.warmup):
@@ -297,13 +311,20 @@ def run_gpu(args):
     peaks = load_peaks()
     # the gate_up GEMM is HBM-bound when its bytes take longer than its flops at peak
     t_hbm = gu_bytes / (peaks["hbm_gbs"] * 1e9)
-    t_tc = gu_flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    # the ncu summaries cover the bf16 GEMM only
+    traffic = profiled_traffic(f"gate_up_gemm_{args.workload}.md") if w8 is None else None
+    kname = "grouped_gemm_fp8 (gate_up)" if w8 is not None else "grouped_gemm (gate_up)"
+    # an e4m3 contraction's peak: the measured bf16 peak times the nominal fp8 / bf16 ratio (2)
+    tc_peak = peaks["bf16_tflops_sustained"] * (2 if w8 is not None else 1)
+    tc_src = (f"{peaks['source']} bf16_tflops_sustained x 2 (nominal e4m3 / bf16 ratio)" if w8 is not None
+              else f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long loop)")
+    t_tc = gu_flops / (tc_peak * 1e12)
     tensor_bound = t_tc > t_hbm
-    traffic = profiled_traffic(f"gate_up_gemm_{args.workload}.md")
     line = {
         "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 expert weights and GEMM inputs, bf16 LoRA" if w8 is not None else "bf16", "data": "synthetic",
         "config": {
             "workload": cfg.describe(), "T": T, "H": H, "I": I, "E": E, "top_k": k,
             "lora_ranks": list(cfg.ranks), "routing": "DeepSeekV3" if cfg.method else "Renormalize",
@@ -312,17 +333,17 @@ def run_gpu(args):
             "forward_flags": args.flags,
             "step_bytes": step_bytes, "step_flops": step_flops,
             "step_roofline_frac": max(step_bytes / (peaks["hbm_gbs"] * 1e9),
-                                      step_flops / (peaks["bf16_tflops_sustained"] * 1e12)) / (agg["ms_per_step"] / 1e3),
+                                      step_flops / (tc_peak * 1e12)) / (agg["ms_per_step"] / 1e3),
         },
         "roofline": ({
-            "kernel": "grouped_gemm (gate_up)", "bound": "tensor", "achieved": gu_flops / gu_avg_s / 1e12,
-            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": gu_flops / gu_avg_s / 1e12 / peaks["bf16_tflops_sustained"], "traffic": traffic,
-            "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long loop)",
+            "kernel": kname, "bound": "tensor", "achieved": gu_flops / gu_avg_s / 1e12,
+            "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": gu_flops / gu_avg_s / 1e12 / tc_peak, "traffic": traffic,
+            "peak_source": tc_src,
             "algorithmic_flops_per_launch": gu_flops, "algorithmic_bytes_per_launch": gu_bytes,
             "avg_launch_us": gu_avg_s * 1e6,
         } if tensor_bound else {
-            "kernel": "grouped_gemm (gate_up)", "bound": "hbm", "achieved": gu_bytes / gu_avg_s / 1e9,
+            "kernel": kname, "bound": "hbm", "achieved": gu_bytes / gu_avg_s / 1e9,
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gu_bytes / gu_avg_s / 1e9 / peaks["hbm_gbs"],
             "traffic": traffic, "peak_source": f"{peaks['source']} hbm_gbs",
             "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_us": gu_avg_s * 1e6,
@@ -373,7 +394,7 @@ def run_gpu(args):
                     st_ms[name] = round(1e3 * statistics.median(vals), 2)
             line.setdefault("stage_us", {})[label] = st_ms
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, inp, args)
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args, w8=w8)
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()
@@ -392,18 +413,28 @@ def _oracle_inputs(cfg, inp):
 
 def _oracle_call(cfg, o, tokens):
     from oracle import moe_lora_oracle as orc
+    if "w1q" in o:   # block-FP8 expert weights
+        return orc.moe_lora_forward_fp8(o["hidden"], o["router_logits"], o["w1q"], o["w1s"], o["w2q"], o["w2s"],
+                                        cfg.top_k, cfg.method, o["correction_bias"], cfg.rsf, o["lora_A_gu"],
+                                        o["lora_B_gu"], o["lora_A_dn"], o["lora_B_dn"], o["slot_idx"], cfg.ranks,
+                                        cfg.scalings, tokens=tokens, shared_outer=cfg.shared_outer)
     return orc.moe_lora_forward(o["hidden"], o["router_logits"], o["w1"], o["w2"], cfg.top_k, cfg.method,
                                 o["correction_bias"], cfg.rsf, o["lora_A_gu"], o["lora_B_gu"], o["lora_A_dn"],
                                 o["lora_B_dn"], o["slot_idx"], cfg.ranks, cfg.scalings, tokens=tokens,
                                 shared_outer=cfg.shared_outer)
 
 
-def cpu_baseline(cfg, inp, args, budget_s: float = None) -> dict:
+def cpu_baseline(cfg, inp, args, budget_s: float = None, w8=None) -> dict:
     """Time the oracle, as it stands, on a bounded sample of the workload: a token subset
     that grows until one call takes a good part of the budget, then repeated calls until
-    about `budget_s` seconds of CPU work are done (tokens/s over all of them)."""
+    about `budget_s` seconds of CPU work are done (tokens/s over all of them).  With w8
+    (block-FP8 weights) the oracle's FP8 layer runs on those codes and scales."""
     budget_s = args.cpu_budget if budget_s is None else budget_s
+    if w8 is not None:
+        inp = {k_: v for k_, v in inp.items() if k_ not in ("w1", "w2")}
     o = _oracle_inputs(cfg, inp)
+    if w8 is not None:
+        o.update(w1q=w8[0].cpu().numpy(), w1s=w8[1].cpu().numpy(), w2q=w8[2].cpu().numpy(), w2s=w8[3].cpu().numpy())
     n_tok = min(cfg.T, 8)
     t0 = time.perf_counter()
     _oracle_call(cfg, o, np.arange(n_tok))
@@ -524,6 +555,8 @@ def main():
     ap.add_argument("--ref-steps", type=int, default=5)
     ap.add_argument("--flags", type=int, default=0, help="extra moe_lora_forward flags (e.g. 8: unfused LoRA)")
     ap.add_argument("--stage-times", action="store_true", help="add per-stage device times (us) to the line")
+    ap.add_argument("--fp8", action="store_true",
+                    help="block-FP8 expert weights (e4m3, 128x128 scales) quantised from the drawn bf16 ones")
     ap.add_argument("--routed", choices=["finalize", "unfinalized"], default=None,
                     help="time the externally routed entry instead (auxiliary line, not the headline)")
     args = ap.parse_args()

@@ -224,6 +224,45 @@ moe_lora_status moe_lora_forward_routed(moe_lora_handle* h, const moe_lora_args*
                                         moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
                                         moe_lora_stream stream);
 
+/* FP8 block-scale expert weights, as FP8 block-quantised checkpoints store them (the pages'
+   FP8 path: sglang PR #28466, summary, the FP8 path "requires FP8 block quant"; section 1
+   flow (A) diagram, the FP8 flow's per_token_group_quant_fp8 before the MoE op and its
+   post-activation quant before the down GEMM).  e4m3 codes are the OCP 8-bit float E4M3
+   bit patterns (no infinities, largest finite value 448).  Device pointers owned by the
+   caller; codes 16-byte aligned, scales 4-byte aligned. */
+typedef struct {
+  const uint8_t* w1;        /* [E, 2I, H] e4m3 codes: rows [0,I) gate, [I,2I) up              */
+  const float* w1_scale;    /* [E, 2I/128, H/128]: w1 = code * scale of its 128 x 128 block   */
+  const uint8_t* w2;        /* [E, H, I] e4m3 codes                                           */
+  const float* w2_scale;    /* [E, H/128, I/128]                                              */
+} moe_lora_fp8_weights;
+
+/* The layer of moe_lora_forward with FP8 block-scale expert weights `w` (a->w1 and a->w2
+   are not read).  The two base GEMMs read their inputs quantised per token in groups of
+   128 along K (s = max(amax, 1e-10) / 448 per group, codes e4m3(v / s) rounded to nearest
+   even and saturated, both float32 operations): the permuted hidden rows for the gate_up
+   GEMM and the bf16 activation for the down GEMM; each GEMM sums, per 128-wide K block,
+   the e4m3 products times the two block scales, in fp32.  The LoRA weights and the LoRA
+   chain stay bf16 and read the unquantised hidden rows and activation, as in the pages'
+   FP8 flow.  Every other rule (routing, rounding points, slots, ranks, scalings, flags
+   except MOE_LORA_FLAG_UNFUSED_LORA, which is implied) is that of moe_lora_forward; the
+   LoRA placement is the narrow one (side-stream gate_up LoRA, down expand in the down
+   GEMM's epilogue) at every token count, with token tiles of at most 64.  H and I must
+   be multiples of 128.  The workspace is moe_lora_workspace_size() of the same shape.
+   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+moe_lora_status moe_lora_forward_fp8(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_fp8_weights* w,
+                                     moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
+                                     moe_lora_stream stream);
+
+/* The FP8 group quantisation of moe_lora_forward_fp8 on its own: codes [rows, K] (e4m3,
+   16-byte aligned) and scales [K/128, rows] float32 (scales[g * rows + q] is the scale of
+   group g of output row q) of bf16 rows src (16-byte aligned).  With perm (the routing's
+   permuted -> expanded map) output row q quantises src row perm[q] / top_k, the permute and
+   quant of the gate_up GEMM's input; with perm NULL it quantises src row q.  K a multiple
+   of 128.  Errors: INVALID_ARG, CUDA. */
+moe_lora_status moe_lora_quant_fp8(moe_lora_handle* h, const moe_lora_bf16* src, const int32_t* perm, int rows,
+                                   int K, int top_k, uint8_t* codes, float* scales, moe_lora_stream stream);
+
 /* Routing + expert alignment that allocates nothing and takes no workspace or handle.
    The pages have no counterpart to this call; it exists for callers that cannot call
    cudaMalloc or supply a workspace (plug-ins inside a host framework that owns all device

@@ -35,7 +35,7 @@ NUM_STAGES = len(STAGES)
 EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
             "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed",
-            "moe_lora_launch_count"]
+            "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8"]
 
 
 class MoELoRAError(RuntimeError):
@@ -76,6 +76,10 @@ class Routed(ctypes.Structure):
     ]
 
 
+class Fp8Weights(ctypes.Structure):
+    _fields_ = [("w1", c_void_p), ("w1_scale", c_void_p), ("w2", c_void_p), ("w2_scale", c_void_p)]
+
+
 _lib = None
 
 
@@ -104,6 +108,9 @@ def lib() -> ctypes.CDLL:
     L.moe_lora_launch_count.argtypes = [c_void_p, ctypes.POINTER(ctypes.c_uint64)]
     L.moe_lora_forward_routed.argtypes = [c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Routed), c_void_p, c_void_p,
                                           c_size_t, c_void_p]
+    L.moe_lora_forward_fp8.argtypes = [c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Fp8Weights), c_void_p,
+                                       c_void_p, c_size_t, c_void_p]
+    L.moe_lora_quant_fp8.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
     for name in EXPORTED:
         if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
             getattr(L, name).restype = c_int
@@ -270,7 +277,8 @@ def check_shapes(hidden, router_logits, w1, w2, lora_A_gu=None, lora_B_gu=None, 
 def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction_bias=None,
               routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
               slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (), flags=0,
-              outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1):
+              outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1,
+              weight_dtype=torch.bfloat16):
     """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
     check_shapes(hidden, router_logits, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
                  scalings, flags, correction_bias=correction_bias)
@@ -288,8 +296,8 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
     a.hidden = _ptr(hidden, torch.bfloat16, "hidden")
     a.router_logits = _ptr(router_logits, torch.bfloat16, "router_logits")
     a.correction_bias = _ptr(correction_bias, torch.float32, "correction_bias")
-    a.w1 = _ptr(w1, torch.bfloat16, "w1")
-    a.w2 = _ptr(w2, torch.bfloat16, "w2")
+    a.w1 = _ptr(w1, weight_dtype, "w1")
+    a.w2 = _ptr(w2, weight_dtype, "w2")
     a.lora_A_gu = _ptr(lora_A_gu, torch.bfloat16, "lora_A_gu")
     a.lora_B_gu = _ptr(lora_B_gu, torch.bfloat16, "lora_B_gu")
     a.lora_A_dn = _ptr(lora_A_dn, torch.bfloat16, "lora_A_dn")
@@ -377,6 +385,66 @@ def moe_lora_forward_routed(handle: Handle, hidden, packed_topk_ids, w1, w2, top
         return out
     return dict(gemm2_output=gemm2_output, activation_output=activation_output, expert_weights=expert_weights,
                 expanded_idx_to_permuted_idx=expanded_idx_to_permuted_idx)
+
+
+def check_fp8_weights(w1_q, w1_scale, w2_q, w2_scale):
+    """Raise ValueError unless the FP8 weights have the shapes the C ABI reads: codes
+    w1_q [E, 2I, H] and w2_q [E, H, I] (uint8), block scales w1_scale [E, 2I/128, H/128]
+    and w2_scale [E, H/128, I/128] (float32), H and I multiples of 128."""
+    if w1_q.dim() != 3 or w2_q.dim() != 3:
+        raise ValueError("w1_q must be [E, 2I, H] and w2_q [E, H, I]")
+    E, twoI, H = w1_q.shape
+    I = twoI // 2
+    if H % 128 or I % 128 or twoI % 2:
+        raise ValueError(f"H and I must be multiples of 128, got H={H}, I={I}")
+    for t, shape, name in ((w2_q, (E, H, I), "w2_q"), (w1_scale, (E, twoI // 128, H // 128), "w1_scale"),
+                           (w2_scale, (E, H // 128, I // 128), "w2_scale")):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+
+
+def moe_lora_forward_fp8(handle: Handle, hidden, router_logits, w1_q, w1_scale, w2_q, w2_scale, top_k,
+                         routing_method=0, correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None,
+                         lora_B_gu=None, lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(),
+                         flags=0, out=None, workspace=None, outputs=None, prof_events=None, stream=None,
+                         n_group=1, topk_group=1) -> torch.Tensor:
+    """The layer with FP8 block-scale expert weights: w1_q [E, 2I, H] and w2_q [E, H, I] hold
+    e4m3 bit patterns (uint8), w1_scale [E, 2I/128, H/128] and w2_scale [E, H/128, I/128]
+    the float32 scales of their 128 x 128 blocks.  Returns out [T, H] bf16."""
+    check_fp8_weights(w1_q, w1_scale, w2_q, w2_scale)
+    a, keep = make_args(hidden, router_logits, w1_q, w2_q, top_k, routing_method, correction_bias,
+                        routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
+                        scalings, flags, outputs, prof_events, n_group, topk_group, weight_dtype=torch.uint8)
+    w = Fp8Weights()
+    w.w1 = _ptr(w1_q, torch.uint8, "w1_q")
+    w.w1_scale = _ptr(w1_scale, torch.float32, "w1_scale")
+    w.w2 = _ptr(w2_q, torch.uint8, "w2_q")
+    w.w2_scale = _ptr(w2_scale, torch.float32, "w2_scale")
+    if out is None:
+        out = torch.empty((a.T, a.H), dtype=torch.bfloat16, device=hidden.device)
+    if workspace is None:
+        workspace = alloc_workspace(a.T, a.H, a.I, a.E, a.top_k, a.S, a.R, device=hidden.device)
+    st = lib().moe_lora_forward_fp8(handle.ptr, ctypes.byref(a), ctypes.byref(w), _ptr(out, torch.bfloat16, "out"),
+                                    _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "moe_lora_forward_fp8")
+    del keep
+    return out
+
+
+def moe_lora_quant_fp8(handle: Handle, src: torch.Tensor, perm: Optional[torch.Tensor] = None, top_k: int = 1,
+                       stream=None):
+    """FP8 group quantisation of bf16 rows src [T, K]: returns (codes [rows, K] uint8 e4m3
+    bit patterns, scales [K/128, rows] float32).  With perm [T*top_k], output row q
+    quantises src row perm[q] // top_k (rows = T*top_k); without it rows = T."""
+    T, K = src.shape
+    rows = perm.numel() if perm is not None else T
+    codes = torch.empty((rows, K), dtype=torch.uint8, device=src.device)
+    scales = torch.empty((K // 128, rows), dtype=torch.float32, device=src.device)
+    st = lib().moe_lora_quant_fp8(handle.ptr, _ptr(src, torch.bfloat16, "src"), _ptr(perm, torch.int32, "perm"),
+                                  rows, K, int(top_k), _ptr(codes, torch.uint8), _ptr(scales, torch.float32),
+                                  _stream(stream))
+    _check(st, "moe_lora_quant_fp8")
+    return codes, scales
 
 
 def moe_lora_validate(**kwargs) -> int:

@@ -1,5 +1,7 @@
 // Memory-bound stages of the routed MoE-LoRA layer: token permute, SwiGLU activation
 // with the gate_up LoRA delta, and the weighted top-k finalize.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -129,6 +131,58 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool p
   const int H4 = p.H / 4;
   return launch_k(finalize_kernel, dim3(p.T, (H4 + kFinThreads - 1) / kFinThreads), dim3(kFinThreads), 0, stream,
                   pdl, p);
+}
+
+// ---------------------------------------------------------------------------------
+// FP8 group quantisation, with an optional gather: the per_token_group_quant_fp8 step
+// and the post-activation quant of the pages' FP8 flow (sglang PR #28466, section 1 flow
+// (A) diagram).  Row q of the output comes from source row t = perm[q] / k (or t = q
+// without perm).  Per group g of 128 consecutive values v of that row:
+//   s = max(amax, 1e-10) / 448,   codes[q, 128g + i] = e4m3(v_i / s),   scale[g * P + q] = s,
+// with the scale and the quotients IEEE float32 divisions rounded to nearest and the
+// conversion rounded to nearest even and saturated at +-448.  One warp per row, 4 values
+// per lane and group.  With slot_out set it also gathers each pair's adapter slot.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_fp8_kernel(const __nv_bfloat16* __restrict__ src,
+                                                        const int32_t* __restrict__ perm, int k, int P, int K,
+                                                        uint8_t* __restrict__ codes, float* __restrict__ scale,
+                                                        const int32_t* __restrict__ slot_idx, int32_t* slot_out) {
+  pdl_wait();
+  pdl_trigger();
+  const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (q >= P) return;
+  const int t = perm != nullptr ? perm[q] / k : q;
+  if (slot_out != nullptr && lane == 0) slot_out[q] = slot_idx[t];
+  const uint2* s = reinterpret_cast<const uint2*>(src + static_cast<size_t>(t) * K);
+  uint32_t* d = reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(q) * K);
+  const int G = K >> 7;
+#pragma unroll 4
+  for (int g = 0; g < G; ++g) {
+    const uint2 v = __ldg(s + g * 32 + lane);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    const float f[4] = {lo.x, lo.y, hi.x, hi.y};
+    float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      packed |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(f[i], sc), __NV_SATFINITE, __NV_E4M3))
+                << (8 * i);
+    d[g * 32 + lane] = packed;
+    if (lane == 0) scale[static_cast<size_t>(g) * P + q] = sc;
+  }
+}
+
+cudaError_t launch_quant_fp8(const __nv_bfloat16* src, const int32_t* perm, int k, int P, int K, uint8_t* codes,
+                             float* scale, cudaStream_t stream, bool pdl, const int32_t* slot_idx, int32_t* slot_out) {
+  if (P == 0) return cudaSuccess;
+  if (K % 128 != 0) return cudaErrorInvalidValue;
+  return launch_k(quant_fp8_kernel, dim3((P + 7) / 8), dim3(256), 0, stream, pdl, src, perm, k, P, K, codes, scale,
+                  slot_idx, slot_out);
 }
 
 }  // namespace mlk

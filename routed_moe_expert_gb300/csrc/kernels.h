@@ -102,12 +102,43 @@ int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused
 int gemm_stage_bytes(int rows);   // one stage: 128 weight rows + `rows` token rows, 64 wide
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 
+// ---------------------------------------------------------------- FP8 grouped GEMM
+// out[q, col] = sum_b x_scale[b*P + q] * w_scale[e, n/128, b] * sum_{k in block b}
+// X8[q, k] * W8[e*N + n, k] over the 128-wide K blocks b, n = row(col) (gated as in
+// GemmParams).  N and K multiples of 128; token tiles of 16, 32 or 64.
+struct GemmF8Params {
+  CUtensorMap tmap_w;            // e4m3 weights [E*N rows, K cols] (bytes), box {128, 64}
+  CUtensorMap tmap_x;            // e4m3 activations [P rows, K cols], box {128, BN}
+  const float* w_scale;          // [E, N/128, K/128]
+  const float* x_scale;          // [K/128, P]
+  __nv_bfloat16* out;            // [P, N] bf16 output, or
+  float* out_f32;                //   fp32 output when non-null
+  const int32_t* offsets;        // [E + 1]
+  uint32_t* status;
+  int E, N, K, P, gated, stages;
+  // Optional down-LoRA expand in the epilogue (as GemmParams' lora_v path):
+  // out[q, n] += sum_{r<ranks[s]} lora_B[s, e, n, r] * lora_v[q, r]   (s = pair_slot[q])
+  const float* lora_v;           // [P, R] or null
+  const __nv_bfloat16* lora_B;   // [S, E, N, R], or [S, 1, N, R] with lora_b_e1
+  int lora_b_e1;
+  const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
+  LoraSlots slots;
+};
+int gemm_fp8_smem_bytes(int bn, int stages, int E, int lora_R);
+int gemm_fp8_stage_bytes(int bn);
+cudaError_t launch_grouped_gemm_fp8(const GemmF8Params& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
+
 // ---------------------------------------------------------------- elementwise
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
                            __nv_bfloat16* xp, cudaStream_t stream, bool pdl = false,
                            const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr);
 cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
                               __nv_bfloat16* a, cudaStream_t stream, bool pdl = false);
+// FP8 group quantisation of rows (gathered through perm[q] / k when perm is set):
+// codes [P, K] e4m3, scale [K/128, P]; K a multiple of 128.
+cudaError_t launch_quant_fp8(const __nv_bfloat16* src, const int32_t* perm, int k, int P, int K, uint8_t* codes,
+                             float* scale, cudaStream_t stream, bool pdl = false,
+                             const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr);
 
 
 struct FinalizeParams {

@@ -17,6 +17,7 @@
 #include "../../include/moe_lora.h"
 #include "kernels.h"
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -55,6 +56,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
   size_t header, ids, wts, offsets, perm, inv, hist, base, total;
   size_t xp, g, d, a, v, y, pslot, ub;
+  size_t sx, sa;   // FP8 path: group scales of the gate_up and down GEMM inputs
   size_t bytes;
 };
 
@@ -86,6 +88,10 @@ Layout layout_for(int T, int H, int I, int E, int k, int R, int S) {
   L.y = take(P * H * 4);
   L.pslot = take(R > 0 ? P * 4 : 0);
   L.ub = take(static_cast<size_t>(S) * P * ((R + 7) / 8 * 8) * 2);
+  // The FP8 path keeps its e4m3 GEMM inputs in the xp region ([P, H] bytes) and in the g
+  // region ([P, I] bytes, written after the activation has read g); their group scales:
+  L.sx = take(P * ((static_cast<size_t>(H) + 127) / 128) * 4);
+  L.sa = take(P * ((static_cast<size_t>(I) + 127) / 128) * 4);
   L.bytes = off;
   return L;
 }
@@ -346,6 +352,36 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
   return MOE_LORA_OK;
 }
 
+// e4m3 rows [rows, cols] (one byte each) in 128-byte-swizzled boxes of 128 x box_rows.
+bool make_tmap_e4m3(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The FP8 grouped GEMM: weights W8 [E*N, K], inputs X8 [P, K], token tiles of bn (16..64).
+// Pipeline depth from the same shared-memory budgets as the bf16 GEMM.
+moe_lora_status enqueue_gemm_fp8(moe_lora_handle* h, GemmF8Params& gp, const uint8_t* W, const uint8_t* X, int P,
+                                 int bn, cudaStream_t stream, bool pdl) {
+  if (!make_tmap_e4m3(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64))
+    return MOE_LORA_ERR_CUDA;
+  if (!make_tmap_e4m3(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
+  const int lora_R = gp.lora_v != nullptr ? gp.slots.R : 0;
+  const int budget = (bn <= 32 && gp.gated != 0 ? 160 : 200) * 1024;
+  int stages = (budget - gemm_fp8_smem_bytes(bn, 0, gp.E, lora_R)) / (gemm_fp8_stage_bytes(bn) + 16);
+  if (stages > 16) stages = 16;
+  if (stages < 2) stages = 2;
+  gp.stages = stages;
+  gp.P = P;
+  ML_LAUNCH(h, launch_grouped_gemm_fp8(gp, bn, h->num_sms, stream, pdl), "grouped_gemm_fp8 launch");
+  return MOE_LORA_OK;
+}
+
 // Tensor maps of the fused LoRA stages: per active slot, the slot's B rows [E*N, ranks[s]]
 // (the inner extent stops at the slot's rank, so the stacked tail is zero-filled, never
 // read), and the per-slot scaled shrink rows ub [S*P, RU].
@@ -458,9 +494,8 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
                                           int32_t* perm, int32_t* offsets, int32_t* ids, __nv_bfloat16* xp,
                                           __nv_bfloat16* g, __nv_bfloat16* d, __nv_bfloat16* act, float* v, float* y,
                                           int32_t* pair_slot, __nv_bfloat16* ub, const LoraSlots& slots,
-                                          uint32_t* status, cudaStream_t stream) {
-  (void)ws;
-  (void)L;
+                                          uint32_t* status, cudaStream_t stream,
+                                          const moe_lora_fp8_weights* f8 = nullptr) {
   (void)ids;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const int P = T * k;
@@ -474,9 +509,16 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   // bf16 delta: the pages round the gate_up GEMM output and the delta to bf16 separately,
   // and adding the delta inside the accumulator would round their sum once instead.
   // At 16-token tiles (decode) the epilogue expand costs less than an extra K-stage.
-  const int bn = pick_bn(P, E);
-  const bool fused = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && bn >= 32 &&
+  // FP8 weights: token tiles of at most 64 and the down expand in the GEMM's epilogue
+  const int bn = f8 != nullptr ? std::min(pick_bn(P, E), 64) : pick_bn(P, E);
+  const bool fused = f8 == nullptr && lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && bn >= 32 &&
                      !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
+  // FP8 GEMM inputs: the permuted hidden codes in the xp region, the activation codes in
+  // the g region (written after the activation has read g), and their group scales
+  uint8_t* xp8 = reinterpret_cast<uint8_t*>(xp);
+  uint8_t* a8 = reinterpret_cast<uint8_t*>(g);
+  float* sx = reinterpret_cast<float*>(ws + L.sx);
+  float* sa = reinterpret_cast<float*>(ws + L.sa);
   const bool fused_gu = false;
   // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
   const int lora_ntl = (P >= 32 * E && lora_smem_bytes(4, R, 2 * I, true, E) <= 200 * 1024) ? 4 : 1;
@@ -525,9 +567,15 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
   // the pairs' adapter slots ride along with the permute for the activation + down shrink
   const bool act_shrink = lora && !fused && !fused_gu;
-  ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
-                         a->slot_idx, act_shrink ? pair_slot : nullptr),
-          "permute launch");
+  if (f8 != nullptr) {   // permute and quantise in one pass
+    ML_LAUNCH(h, launch_quant_fp8(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, k, P, H, xp8, sx, stream,
+                                  pdl, a->slot_idx, act_shrink ? pair_slot : nullptr),
+              "permute + quant launch");
+  } else {
+    ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
+                                a->slot_idx, act_shrink ? pair_slot : nullptr),
+              "permute launch");
+  }
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
   if (fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
@@ -542,7 +590,22 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   gu.K = H;
   gu.gated = 1;
   if (fused_gu && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
-  st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl && !(fused_gu && two));
+  if (f8 != nullptr) {
+    GemmF8Params gq;
+    std::memset(&gq, 0, sizeof(gq));
+    gq.w_scale = f8->w1_scale;
+    gq.x_scale = sx;
+    gq.out = g;
+    gq.offsets = offsets;
+    gq.status = status;
+    gq.E = E;
+    gq.N = 2 * I;
+    gq.K = H;
+    gq.gated = 1;
+    st = enqueue_gemm_fp8(h, gq, f8->w1, xp8, P, bn, stream, pdl);
+  } else {
+    st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl && !(fused_gu && two));
+  }
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
@@ -624,8 +687,34 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   // the epilogue's staged LoRA rows grow with the tile: narrow it until two stages fit
   int bn_dn = bn;
   while (!fused && lora && bn_dn > 16 &&
-         gemm_smem_bytes(bn_dn, 1, 2, E, R, 0, 1) > kMaxGemmSmem)
+         (f8 != nullptr ? gemm_fp8_smem_bytes(bn_dn, 2, E, R) : gemm_smem_bytes(bn_dn, 1, 2, E, R, 0, 1)) >
+             kMaxGemmSmem)
     bn_dn >>= 1;
+  if (f8 != nullptr) {   // the activation's group quantisation, then the FP8 down GEMM
+    ML_LAUNCH(h, launch_quant_fp8(act, nullptr, 1, P, I, a8, sa, stream, pdl), "activation quant launch");
+    GemmF8Params dq;
+    std::memset(&dq, 0, sizeof(dq));
+    dq.w_scale = f8->w2_scale;
+    dq.x_scale = sa;
+    dq.out_f32 = y;
+    dq.offsets = offsets;
+    dq.status = status;
+    dq.E = E;
+    dq.N = H;
+    dq.K = I;
+    dq.gated = 0;
+    if (lora) {
+      dq.lora_v = v;
+      dq.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
+      dq.lora_b_e1 = so ? 1 : 0;
+      dq.pair_slot = pair_slot;
+      dq.slots = slots;
+    }
+    st = enqueue_gemm_fp8(h, dq, f8->w2, a8, P, bn_dn, stream, pdl);
+    if (st != MOE_LORA_OK) return st;
+    prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+    return MOE_LORA_OK;
+  }
   st = enqueue_gemm(h, dn, a->w2, act, P, bn_dn, stream, pdl);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
@@ -678,7 +767,8 @@ namespace {
 // The forward of moe_lora_forward and moe_lora_forward_routed (`ext` set: the routing
 // comes packed and the output may stay unfinalized).  Arguments are validated.
 moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_routed* ext,
-                             moe_lora_bf16* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                             moe_lora_bf16* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                             const moe_lora_fp8_weights* f8 = nullptr) {
   moe_lora_status st = MOE_LORA_OK;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const bool lora = lora_active(a);
@@ -735,7 +825,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   const int bn0 = pick_bn(P, E);
   const bool fuse_all = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && a->S * R <= 256 && bn0 >= 32 &&
                         !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
-  const bool act_in_gemm = fuse_all || (!lora && bn0 >= 32);
+  const bool act_in_gemm = f8 == nullptr && (fuse_all || (!lora && bn0 >= 32));
   if (act_in_gemm) {
     int bn = bn0;
     if (fuse_all && bn > 160) bn = 160;   // room in TMEM for two accumulators and the LoRA delta
@@ -788,7 +878,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
   } else {
     st = enqueue_unfused_lora_path(h, a, lora, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub,
-                                   slots, status, stream);
+                                   slots, status, stream, f8);
     if (st != MOE_LORA_OK) return st;
   }
 
@@ -857,6 +947,40 @@ moe_lora_status moe_lora_forward_routed(moe_lora_handle* h, const moe_lora_args*
       return MOE_LORA_ERR_INVALID_ARG;
   }
   return forward_impl(h, &b, r, out, workspace, workspace_bytes, stream);
+}
+
+moe_lora_status moe_lora_forward_fp8(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_fp8_weights* w,
+                                     moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
+                                     moe_lora_stream stream) {
+  if (a == nullptr || w == nullptr || h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  // a->w1 / a->w2 are not read: check the rest with the FP8 codes in their place
+  moe_lora_args b = *a;
+  b.w1 = reinterpret_cast<const moe_lora_bf16*>(w->w1);
+  b.w2 = reinterpret_cast<const moe_lora_bf16*>(w->w2);
+  b.flags |= MOE_LORA_FLAG_UNFUSED_LORA;
+  moe_lora_status st = moe_lora_validate(&b);
+  if (st != MOE_LORA_OK) return st;
+  if (b.H % 128 != 0 || b.I % 128 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (b.T > 0) {
+    if (out == nullptr || !aligned16(out)) return MOE_LORA_ERR_INVALID_ARG;
+    if (w->w1_scale == nullptr || w->w2_scale == nullptr || !aligned4(w->w1_scale) || !aligned4(w->w2_scale))
+      return MOE_LORA_ERR_INVALID_ARG;
+  }
+  return forward_impl(h, &b, nullptr, out, workspace, workspace_bytes, stream, w);
+}
+
+moe_lora_status moe_lora_quant_fp8(moe_lora_handle* h, const moe_lora_bf16* src, const int32_t* perm, int rows,
+                                   int K, int top_k, uint8_t* codes, float* scales, moe_lora_stream stream) {
+  if (h == nullptr || rows < 0 || K < 128 || K % 128 != 0 || K > 16384) return MOE_LORA_ERR_INVALID_ARG;
+  if (perm != nullptr && top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_LORA_OK;
+  if (src == nullptr || codes == nullptr || scales == nullptr || !aligned16(src) || !aligned16(codes) ||
+      !aligned4(scales) || (perm != nullptr && !aligned4(perm)))
+    return MOE_LORA_ERR_INVALID_ARG;
+  ML_LAUNCH(h, launch_quant_fp8(reinterpret_cast<const __nv_bfloat16*>(src), perm, perm != nullptr ? top_k : 1, rows, K,
+                                codes, scales, stream),
+            "quant launch");
+  return MOE_LORA_OK;
 }
 
 moe_lora_status moe_lora_launch_count(const moe_lora_handle* h, uint64_t* count) {

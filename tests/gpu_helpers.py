@@ -11,6 +11,12 @@ from oracle import moe_lora_oracle as orc
 # Float tolerance of the layer output: |gpu - ref| <= ATOL + RTOL * |ref| elementwise,
 # and relative L2 error <= REL_L2.
 ATOL, RTOL, REL_L2 = 1e-2, 2e-2, 5e-3
+# The FP8 path: three times the bf16 bounds.  Its activation is quantised to e4m3 after the
+# bf16 rounding, so a rounding difference upstream (the e4m3 tensor-core accumulation of
+# the gate_up GEMM) comes out about three times larger than in the bf16 layer; the
+# derivation is pinned on the CPU by
+# tests/test_oracle_fp8.py::test_fp8_tolerance_covers_accumulation_noise.
+ATOL_FP8, RTOL_FP8, REL_L2_FP8 = 3e-2, 6e-2, 1.5e-2
 
 
 def to_dev(inp: dict, device="cuda") -> dict:
@@ -55,17 +61,17 @@ def oracle(inp: dict, tokens=None, lora_off=False, lazy=False):
         shared_outer=bool(inp.get("shared_outer", False)))
 
 
-def assert_close(got, ref, what="output"):
+def assert_close(got, ref, what="output", atol=ATOL, rtol=RTOL, rel_l2=REL_L2):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
     err = np.abs(got - ref)
-    bad = err > ATOL + RTOL * np.abs(ref)
+    bad = err > atol + rtol * np.abs(ref)
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance, "
                            f"max err {err.max():.4g}, rel L2 {rel:.3g}")
-    assert rel <= REL_L2, f"{what}: relative L2 error {rel:.4g} > {REL_L2}"
+    assert rel <= rel_l2, f"{what}: relative L2 error {rel:.4g} > {rel_l2}"
     return float(err.max()), float(rel)
 
 

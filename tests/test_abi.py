@@ -14,7 +14,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mo
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_lora_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_lora_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -186,3 +186,53 @@ def test_binding_checks_shapes_before_taking_pointers():
     kw["correction_bias"] = torch.zeros(5)
     with pytest.raises(ValueError, match="correction_bias"):
         B.check_shapes(**kw)
+
+
+@pytest.mark.parametrize("over,wover", [
+    (dict(H=192), dict()),                                         # H not a multiple of 128
+    (dict(I=64), dict()),                                          # I not a multiple of 128
+    (dict(), dict(w1_scale=None)),
+    (dict(), dict(w2_scale=FAKE + 2)),                             # misaligned scales
+    (dict(), dict(w1=None)),
+    (dict(top_k=9), dict()),                                       # the forward's own checks
+])
+def test_forward_fp8_rejects_without_launching(built_lib, over, wover):
+    """Host checks of moe_lora_forward_fp8 return INVALID_ARG before any device work (the
+    handle and device addresses passed here are never dereferenced)."""
+    a, keep = _args(**{**dict(H=256, I=128), **over})
+    w = B.Fp8Weights()
+    vals = dict(w1=FAKE, w1_scale=FAKE, w2=FAKE, w2_scale=FAKE)
+    vals.update(wover)
+    for k, v in vals.items():
+        setattr(w, k, v)
+    st = B.lib().moe_lora_forward_fp8(ctypes.c_void_p(FAKE), ctypes.byref(a), ctypes.byref(w),
+                                      ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 30, None)
+    assert st == 1
+
+
+def test_quant_fp8_host_checks(built_lib):
+    L = B.lib()
+    h = ctypes.c_void_p(FAKE)
+    assert L.moe_lora_quant_fp8(None, FAKE, None, 4, 256, 1, FAKE, FAKE, None) == 1        # no handle
+    assert L.moe_lora_quant_fp8(h, FAKE, None, 4, 192, 1, FAKE, FAKE, None) == 1           # K % 128
+    assert L.moe_lora_quant_fp8(h, FAKE, None, -1, 256, 1, FAKE, FAKE, None) == 1          # rows < 0
+    assert L.moe_lora_quant_fp8(h, FAKE, FAKE, 4, 256, 0, FAKE, FAKE, None) == 1           # top_k with perm
+    assert L.moe_lora_quant_fp8(h, FAKE + 8, None, 4, 256, 1, FAKE, FAKE, None) == 1       # misaligned rows
+    assert L.moe_lora_quant_fp8(h, None, None, 0, 256, 1, None, None, None) == 0           # nothing to do
+
+
+def test_binding_checks_fp8_weight_shapes():
+    import torch
+    E, H, I = 3, 256, 128
+    good = dict(w1_q=torch.zeros(E, 2 * I, H, dtype=torch.uint8), w1_scale=torch.zeros(E, 2, 2),
+                w2_q=torch.zeros(E, H, I, dtype=torch.uint8), w2_scale=torch.zeros(E, 2, 1))
+    B.check_fp8_weights(**good)
+    for name, t in [("w2_q", torch.zeros(E, I, H, dtype=torch.uint8)), ("w1_scale", torch.zeros(E, 2, 1)),
+                    ("w2_scale", torch.zeros(E, 1, 2))]:
+        kw = dict(good)
+        kw[name] = t
+        with pytest.raises(ValueError, match=name):
+            B.check_fp8_weights(**kw)
+    with pytest.raises(ValueError, match="multiples of 128"):
+        B.check_fp8_weights(torch.zeros(E, 128, 192, dtype=torch.uint8), torch.zeros(E, 1, 1),
+                            torch.zeros(E, 192, 64, dtype=torch.uint8), torch.zeros(E, 1, 1))

@@ -187,3 +187,54 @@ def test_fp8_layer_differs_from_bf16_layer_only_by_quantisation():
         for j in range(k):
             acc[t] += ref["topk_weights"][t, j] * ref["pairs"][t * k + j]["y8"]
     assert np.array_equal(f8["out"], orc.round_bf16(acc))
+
+
+def test_fp8_tolerance_covers_accumulation_noise():
+    """Derivation of the FP8 parity bounds (three times the bf16 ones).  The tensor cores
+    sum each 128-wide block of e4m3 products with fewer bits than float32 keeps, which is
+    why the FP8 recipe promotes every block to float32 with its scales.  Model that as a
+    relative error of 1e-4 on the gate_up GEMM's output before its bf16 rounding, planted
+    in a copy of the oracle.  The bf16 layer then stays inside the bf16 bounds, while the FP8
+    layer moves about three times as far: its activation is re-quantised to e4m3, where a
+    one-ulp bf16 change can move a code by a whole e4m3 step (2^-3 instead of 2^-8).  Such
+    a change of the group's largest value moves every code's scale.  The FP8 bounds cover
+    that model with room to spare, and the bf16 bounds do not."""
+    import types
+    import os
+    import gpu_helpers as gh
+
+    src = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "moe_lora_oracle.py")).read()
+    anchor = "g = round_bf16(xg @ W1.T)"
+    assert src.count(anchor) == 1
+    noisy = types.ModuleType("oracle_noisy")
+    exec(compile(src.replace(anchor, "g = round_bf16((xg @ W1.T) * (1 + 1e-4 * _NOISE.standard_normal("
+                                     "(xg.shape[0], W1.shape[0]))))"), "oracle_noisy", "exec"), noisy.__dict__)
+    cfg = wl.LayerConfig("f8n", T=40, H=256, I=256, E=8, top_k=2, ranks=(8, 16), scalings=(2.0, 0.5),
+                         slot_mode="uniform_none10")
+    inp = wl.make_inputs(cfg, seed=11)
+    w1q, w1s = wl.quantize_weights_fp8(inp["w1"])
+    w2q, w2s = wl.quantize_weights_fp8(inp["w2"])
+    W1 = np.stack([orc.dequant_weight_fp8(w1q[e].numpy(), w1s[e].numpy()) for e in range(cfg.E)])
+    W2 = np.stack([orc.dequant_weight_fp8(w2q[e].numpy(), w2s[e].numpy()) for e in range(cfg.E)])
+    lora = (np_(inp["lora_A_gu"]), np_(inp["lora_B_gu"]), np_(inp["lora_A_dn"]), np_(inp["lora_B_dn"]),
+            inp["slot_idx"].numpy(), inp["ranks"], inp["scalings"])
+    x, lg = np_(inp["hidden"]), np_(inp["router_logits"])
+
+    def rel(a, b):
+        return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+    def within(got, ref, atol, rtol, rl):
+        return bool(np.all(np.abs(got - ref) <= atol + rtol * np.abs(ref))) and rel(got, ref) <= rl
+
+    noisy._NOISE = np.random.default_rng(0)
+    f8_noisy = noisy.moe_lora_forward_fp8(x, lg, w1q.numpy(), w1s.numpy(), w2q.numpy(), w2s.numpy(), 2, 0, None,
+                                          1.0, *lora)["out"]
+    f8 = orc.moe_lora_forward_fp8(x, lg, w1q.numpy(), w1s.numpy(), w2q.numpy(), w2s.numpy(), 2, 0, None, 1.0,
+                                  *lora)["out"]
+    noisy._NOISE = np.random.default_rng(0)
+    b16_noisy = noisy.moe_lora_forward(x, lg, W1, W2, 2, 0, None, 1.0, *lora)["out"]
+    b16 = orc.moe_lora_forward(x, lg, W1, W2, 2, 0, None, 1.0, *lora)["out"]
+    assert within(b16_noisy, b16, gh.ATOL, gh.RTOL, gh.REL_L2)
+    assert not within(f8_noisy, f8, gh.ATOL, gh.RTOL, gh.REL_L2)
+    assert within(f8_noisy, f8, gh.ATOL_FP8 / 1.2, gh.RTOL_FP8 / 1.2, gh.REL_L2_FP8 / 2)
+    assert 2.0 < rel(f8_noisy, f8) / rel(b16_noisy, b16) < 4.5
