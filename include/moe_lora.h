@@ -1,5 +1,6 @@
 /*
- * moe_lora.h -- C ABI of the routed MoE expert layer with per-expert LoRA (bf16, sm_103a).
+ * moe_lora.h -- C ABI of the routed MoE expert layer with per-expert LoRA (sm_103a): bf16
+ * expert weights (moe_lora_forward) or FP8 block-scale ones (moe_lora_forward_fp8).
  *
  * The layer (sglang PR #28466 "[LoRA] bf16 MoE-LoRA for trtllm backend with two-stream
  * overlap + routing opts", section "Files changed", launcher row, and section 1 flow (A);
