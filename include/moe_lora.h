@@ -226,7 +226,7 @@ moe_lora_status moe_lora_forward_routed(moe_lora_handle* h, const moe_lora_args*
                                         moe_lora_stream stream);
 
 /* FP8 block-scale expert weights, as FP8 block-quantised checkpoints store them (the pages'
-   FP8 path: sglang PR #28466, summary, the FP8 path "requires FP8 block quant"; section 1
+   FP8 path: sglang PR #28466, summary, where the FP8 path needs block-quantised weights; section 1
    flow (A) diagram, the FP8 flow's per_token_group_quant_fp8 before the MoE op and its
    post-activation quant before the down GEMM).  e4m3 codes are the OCP 8-bit float E4M3
    bit patterns (no infinities, largest finite value 448).  Device pointers owned by the

@@ -410,10 +410,10 @@ def moe_lora_forward_routed(hidden, packed_topk_ids, w1, w2, top_k, num_experts,
 # ----------------------------------------------------------------------------
 # The pages' FP8 flow (sglang PR #28466, section 1 flow (A) diagram: the FP8 flow has a
 # per_token_group_quant_fp8 step before the MoE op and a post-activation quant before
-# the down GEMM; its summary: that path "requires FP8 block quant"; sglang PR #27329
+# the down GEMM; its summary: the FP8 path works on block-quantised checkpoints; sglang PR #27329
 # "Experimental fast LoRA path", Optimizations: the FP8 target checkpoint
 # Qwen3.5-35B-A3B-FP8).  The LoRA chain of that flow runs on the bf16 hidden states and
-# on the bf16 activation (the activation kernel "writes activation_lora_input" before
+# on the bf16 activation (the activation kernel hands the down LoRA its input before
 # the quant), so only the base GEMMs see quantised inputs.
 
 E4M3_MAX = 448.0          # largest finite e4m3 value

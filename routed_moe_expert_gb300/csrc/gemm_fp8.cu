@@ -8,8 +8,8 @@
 // and W8 are e4m3 codes, sw one float32 scale per 128 x 128 weight block and sx one per
 // pair and K block: the base GEMMs of the pages' FP8 flow (sglang PR #28466, section 1
 // flow (A): the FP8 flow quantises the hidden states per token group before the MoE op
-// and the activation before the down GEMM; its summary: that path "requires FP8 block
-// quant").
+// and the activation before the down GEMM; its summary ties that path to block-quantised
+// weights).
 //
 // Orientation, tile schedule and warp roles are those of the bf16 grouped GEMM: the
 // weights are the MMA "A" operand (M = 128 rows), the expert's tokens are "B" (N = BN
