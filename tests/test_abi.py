@@ -236,3 +236,16 @@ def test_binding_checks_fp8_weight_shapes():
     with pytest.raises(ValueError, match="multiples of 128"):
         B.check_fp8_weights(torch.zeros(E, 128, 192, dtype=torch.uint8), torch.zeros(E, 1, 1),
                             torch.zeros(E, 192, 64, dtype=torch.uint8), torch.zeros(E, 1, 1))
+
+
+def test_validate_accepts_every_stated_maximum(built_lib):
+    """The header's limits are inclusive: E 1024, top_k 32, S 64, R 128, H and I 16384."""
+    ranks = (ctypes.c_int32 * 64)(*([128] * 64))
+    scal = (ctypes.c_float * 64)(*([0.5] * 64))
+    a, keep = _args(E=1024, top_k=32, S=64, R=128, H=16384, I=16384)
+    a.h_ranks, a.h_scalings = ranks, scal
+    assert B.lib().moe_lora_validate(ctypes.byref(a)) == 0
+    for name, bad in (("top_k", 33), ("E", 1025), ("S", 65), ("R", 129), ("H", 16384 + 64), ("I", 16384 + 64)):
+        setattr(a, name, bad)
+        assert B.lib().moe_lora_validate(ctypes.byref(a)) == 1, name
+        setattr(a, name, dict(top_k=32, E=1024, S=64, R=128, H=16384, I=16384)[name])
