@@ -55,6 +55,13 @@ Readings of points the pages leave open (each also listed in the design notes):
     max(amax, 1e-10) / 448 and codes e4m3(v / s), both float32 operations, rounded to
     nearest even and saturated at +-448; the down GEMM's input is the bf16 activation;
     the LoRA chain reads the unquantised bf16 x and a; the LoRA weights stay bf16.
+  * NVFP4 path (moe_lora_forward_nvfp4): e2m1 values in blocks of 16 along K with an e4m3
+    block scale and one float32 tensor scale (per expert for the weights, per token for
+    the activations); the token scale is max(amax, 1e-10) / (6 * 448), the block scale
+    e4m3(amax_block / (6 * token scale)), the codes e2m1(v / (block scale * token scale)),
+    every step a float32 operation, roundings to nearest even with saturation; packed
+    codes hold element 2i in the low nibble; the quant points and the LoRA chain are those
+    of the FP8 path.
 """
 from __future__ import annotations
 
@@ -533,6 +540,151 @@ def moe_lora_forward_fp8(hidden, router_logits, w1_q, w1_scale, w2_q, w2_scale, 
     rows = _experts(x, ids, w, top_k, tok, Fp8Experts(w1_q, w1_scale), Fp8Experts(w2_q, w2_scale), lora_A_gu,
                     lora_B_gu, lora_A_dn, lora_B_dn, slots, ranks, scalings, lora_off, None,
                     shared_outer=shared_outer, act_quant=fake_quant_act_fp8)
+    out_acc = _finalize(tok, top_k, H, w, rows)
+    return dict(out=round_bf16(out_acc), topk_ids=ids, topk_weights=w, expert_offsets=offsets, perm=perm,
+                inv=inv, tokens=tok)
+
+
+# ----------------------------------------------------------------------------
+# NVFP4 path: e2m1 values in blocks of 16 along K, each block with an e4m3 scale, and one
+# float32 scale per tensor (per expert weight; per token for the activations)
+# ----------------------------------------------------------------------------
+# The pages' other target checkpoint is NVFP4 (sglang PR #27329, Optimizations: the
+# Kimi-K2.5-NVFP4 target, "modelopt_fp4" quantisation in its launch commands, with
+# activations quantised per token under the per-token activation switch; for NVFP4 the
+# permute and the down quantisation are fused with their neighbours).  The pages fix the
+# format only by name: NVIDIA's NVFP4, whose element is the OCP FP4 E2M1 value (sign,
+# 2 exponent bits with bias 1, 1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6), grouped in
+# blocks of 16 that share an e4m3 scale, times one float32 scale per tensor.
+
+E2M1_MAX = 6.0
+NVFP4_BLOCK = 16
+_NVFP4_RANGE = np.float32(E2M1_MAX * E4M3_MAX)   # 2688: what one tensor scale spans
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of each 4-bit e2m1 code (bit 3 sign, bits 2-1 exponent with bias 1, bit 0
+    mantissa; exponent field 0 holds the subnormals 0 and 0.5), float64."""
+    c = np.asarray(codes).astype(np.int64) & 0xF
+    sign = np.where((c >> 3) != 0, -1.0, 1.0)
+    ex = (c >> 1) & 0x3
+    m = (c & 0x1).astype(np.float64)
+    mag = np.where(ex == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(ex - 1.0))
+    return sign * mag
+
+
+def unpack_nvfp4(packed) -> np.ndarray:
+    """Codes of a packed NVFP4 tensor [..., K/2] (uint8): element 2i is the low nibble of
+    byte i and element 2i+1 its high nibble.  Returns codes [..., K]."""
+    b = np.asarray(packed).astype(np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
+
+
+def round_e2m1(x) -> np.ndarray:
+    """Nearest e2m1 value of each float64 value, ties to the even mantissa, saturating at
+    +-6 (below 1 the step is 0.5, in [2^e, 2^(e+1)) it is 2^(e-1))."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        _, e = np.frexp(ax)              # ax = f * 2**e with 0.5 <= f < 1
+        e = np.maximum(e - 1, 0)         # leading-bit exponent; below 1 the step is 0.5
+        quantum = np.exp2(e - 1.0)       # 1 mantissa bit
+        q = np.rint(ax / quantum) * quantum
+    q = np.minimum(q, E2M1_MAX)
+    return np.copysign(q, x)
+
+
+def quant_act_nvfp4(v, block: int = NVFP4_BLOCK):
+    """Quantise rows of activations to NVFP4 with one tensor scale per row (per token).
+
+    With amax_t the row's largest magnitude and amax_b a block's, all float32 operations
+    rounded to nearest:
+      g   = max(amax_t, 1e-10) / 2688                       (the token's scale, 2688 = 6 * 448)
+      s_b = e4m3(amax_b / (6 * g))                          (the block's scale, rounded to nearest
+                                                              even and saturated at 448)
+      q   = e2m1(v / (s_b * g))  (0 where s_b is 0)         (rounded to nearest even, saturated at 6)
+    Returns (q [n, K] float64 e2m1 values, s_b [n, K/block] float64 e4m3 values, g [n] float32).
+    """
+    v32 = np.asarray(v, dtype=np.float32)
+    n, K = v32.shape
+    if K % block:
+        raise ValueError("K must be a multiple of the block size")
+    amax_t = np.abs(v32).max(axis=1)
+    g = (np.maximum(amax_t, FP8_EPS) / _NVFP4_RANGE).astype(np.float32)            # [n]
+    blk = v32.reshape(n, K // block, block)
+    amax_b = np.abs(blk).max(axis=2)                                                # [n, K/block]
+    six_g = (np.float32(E2M1_MAX) * g).astype(np.float32)
+    sb = round_e4m3((amax_b / six_g[:, None]).astype(np.float32).astype(np.float64))  # e4m3 values
+    eff = (sb.astype(np.float32) * g[:, None]).astype(np.float32)                  # [n, K/block]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        quot = (blk / eff[:, :, None]).astype(np.float32)
+    q = np.where(eff[:, :, None] > 0, round_e2m1(quot.astype(np.float64)), 0.0)
+    return q.reshape(n, K), sb, g
+
+
+def dequant_act_nvfp4(q, sb, g, block: int = NVFP4_BLOCK) -> np.ndarray:
+    """q * s_b * g for every value (float64; the products are exact)."""
+    q = np.asarray(q, dtype=np.float64)
+    n, K = q.shape
+    s = np.asarray(sb, np.float64)[:, :, None] * np.asarray(g, np.float64)[:, None, None]
+    return (q.reshape(n, K // block, block) * s).reshape(n, K)
+
+
+def fake_quant_act_nvfp4(v, block: int = NVFP4_BLOCK) -> np.ndarray:
+    """The values a base GEMM of the NVFP4 path reads for activations v."""
+    return dequant_act_nvfp4(*quant_act_nvfp4(v, block), block=block)
+
+
+def dequant_weight_nvfp4(packed, scale_codes, global_scale, block: int = NVFP4_BLOCK) -> np.ndarray:
+    """W[n, k] = e2m1(code[n, k]) * e4m3(scale_codes[n, k // 16]) * global_scale, float64,
+    from the packed codes [N, K/2] (uint8), the block scales' e4m3 bit patterns
+    [N, K/16] (uint8) and the expert's float32 tensor scale."""
+    w = e2m1_decode(unpack_nvfp4(packed))
+    N, K = w.shape
+    sb = e4m3_decode(scale_codes)
+    return w * np.repeat(sb, block, axis=1)[:, :K] * float(np.float32(global_scale))
+
+
+class Nvfp4Experts:
+    """w[e] -> the dequantised float64 weight of expert e, from packed codes [E, N, K/2],
+    block scale codes [E, N, K/16] and tensor scales [E]."""
+
+    def __init__(self, packed, scale_codes, global_scales):
+        self.packed, self.scale_codes, self.global_scales = packed, scale_codes, global_scales
+
+    def __getitem__(self, e):
+        return dequant_weight_nvfp4(np.asarray(self.packed[e]), np.asarray(self.scale_codes[e]),
+                                    np.asarray(self.global_scales)[e])
+
+    def __len__(self):
+        return len(self.packed)
+
+
+def moe_lora_forward_nvfp4(hidden, router_logits, w1, w2, top_k, method=RENORMALIZE, correction_bias=None,
+                           routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None,
+                           lora_B_dn=None, slot_idx=None, ranks=(), scalings=(), lora_off=False, tokens=None,
+                           shared_outer=False):
+    """The layer of moe_lora_forward with NVFP4 expert weights.
+
+    w1 and w2 are (packed codes, block scale codes, tensor scales) triples: w1 packed
+    [E, 2I, H/2], scales [E, 2I, H/16], tensor scales [E]; w2 the same with [E, H, I/2],
+    [E, H, I/16].  The two base GEMMs read NVFP4-quantised inputs (quant_act_nvfp4 per
+    token: the permuted hidden rows and the bf16 activation); the LoRA chain reads the
+    bf16 values, and every other rule is that of moe_lora_forward.
+    """
+    x = _f64(hidden)
+    T, H = x.shape
+    ids, w = route(router_logits, top_k, method, correction_bias, routed_scaling_factor)
+    E = np.asarray(router_logits).shape[1]
+    offsets, perm, inv = align(ids, E)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    slots = np.full(T, -1, dtype=np.int64) if slot_idx is None else np.asarray(slot_idx, dtype=np.int64)
+    rows = _experts(x, ids, w, top_k, tok, Nvfp4Experts(*w1), Nvfp4Experts(*w2), lora_A_gu, lora_B_gu,
+                    lora_A_dn, lora_B_dn, slots, ranks, scalings, lora_off, None, shared_outer=shared_outer,
+                    act_quant=fake_quant_act_nvfp4)
     out_acc = _finalize(tok, top_k, H, w, rows)
     return dict(out=round_bf16(out_acc), topk_ids=ids, topk_weights=w, expert_offsets=offsets, perm=perm,
                 inv=inv, tokens=tok)

@@ -218,3 +218,34 @@ def quantize_weights_fp8(w: torch.Tensor, block: int = 128):
         codes[e] = q.reshape(N, K).view(torch.uint8)
         scales[e] = s
     return codes, scales
+
+
+def quantize_weights_nvfp4(w: torch.Tensor, block: int = 16):
+    """NVFP4 copy of expert weights w [E, N, K] (K a multiple of `block`), as
+    an NVFP4 checkpoint stores them: per expert a float32 tensor scale gs = amax / (6 * 448),
+    per block of 16 values along K an e4m3 scale of amax_block / (6 * gs) (torch's
+    float8_e4m3fn conversion), and e2m1 codes of w / (scale * gs), the nearest of
+    0, 0.5, 1, 1.5, 2, 3, 4, 6, packed two per byte (element 2i in the low nibble).
+    Returns (packed [E, N, K/2] uint8, scale codes [E, N, K/block] uint8, tensor scales [E]
+    float32) on w's device, one expert at a time."""
+    E, N, K = w.shape
+    if K % block or block % 2:
+        raise ValueError("K must be a multiple of the (even) block size")
+    dev = w.device
+    grid = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=dev)
+    packed = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
+    scodes = torch.empty((E, N, K // block), dtype=torch.uint8, device=dev)
+    gscale = torch.empty((E,), dtype=torch.float32, device=dev)
+    for e in range(E):
+        wf = w[e].float()
+        gs = (wf.abs().max() / 2688.0).clamp(min=1e-12)
+        blk = wf.reshape(N, K // block, block)
+        sb = (blk.abs().amax(dim=2) / (6.0 * gs)).clamp(max=448.0).to(torch.float8_e4m3fn)
+        eff = (sb.float() * gs).clamp(min=1e-30)
+        q = blk / eff[:, :, None]
+        idx = (q.abs().clamp(max=6.0)[..., None] - grid).abs().argmin(dim=-1)   # nearest magnitude
+        code = (idx | ((q < 0).to(torch.int64) << 3)).to(torch.uint8).reshape(N, K)
+        packed[e] = code[:, 0::2] | (code[:, 1::2] << 4)
+        scodes[e] = sb.view(torch.uint8)
+        gscale[e] = gs
+    return packed, scodes, gscale

@@ -143,3 +143,56 @@ def dequant_weight_torch(codes, scales, block=128):
     s = torch.as_tensor(scales, dtype=torch.float64)
     N, K = w.shape
     return [[float(w[n, k]) * float(s[n // block, k // block]) for k in range(K)] for n in range(N)]
+
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]   # the format's magnitudes, code order
+
+
+def e2m1_nearest(y: float) -> float:
+    """Nearest e2m1 value by exhaustive search over the 8 magnitudes (ties to the code
+    with the even last bit), saturating at 6."""
+    a = min(abs(y), 6.0)
+    best = min(range(8), key=lambda c: (abs(a - E2M1_TABLE[c]), c & 1))
+    return math.copysign(E2M1_TABLE[best], y)
+
+
+def fake_quant_nvfp4(row, block=16):
+    """NVFP4 quantisation of one row with a per-row tensor scale, built on torch's float8
+    conversion for the block scales and an exhaustive nearest search for the codes
+    (instead of the oracle's own roundings); returns the dequantised values."""
+    import torch
+    t = torch.tensor(row, dtype=torch.float32)
+    g = torch.maximum(t.abs().max(), torch.tensor(1e-10, dtype=torch.float32)) / torch.tensor(2688.0)
+    six_g = torch.tensor(6.0) * g
+    out = []
+    for b0 in range(0, len(row), block):
+        blk = t[b0:b0 + block]
+        sb = (blk.abs().max() / six_g).to(torch.float8_e4m3fn).to(torch.float32)
+        eff = sb * g
+        for v in blk:
+            if float(eff) == 0.0:
+                out.append(0.0)
+            else:
+                y = float((v / eff).to(torch.float32))
+                out.append(e2m1_nearest(y) * float(sb) * float(g))
+    return out
+
+
+def dequant_weight_nvfp4_bruteforce(packed, scale_codes, gscale, block=16):
+    """Nested-list weight [N][K] decoded nibble by nibble from the table and the block
+    scales by torch's float8_e4m3fn view."""
+    import torch
+    p = torch.as_tensor(packed, dtype=torch.uint8)
+    s = torch.as_tensor(scale_codes, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    N, K2 = p.shape
+    gs = float(torch.as_tensor(gscale, dtype=torch.float32))
+    rows = []
+    for n in range(N):
+        r = []
+        for i in range(K2):
+            byte = int(p[n, i])
+            for k, c in ((2 * i, byte & 0xF), (2 * i + 1, byte >> 4)):
+                val = E2M1_TABLE[c & 7] * (-1.0 if c & 8 else 1.0)
+                r.append(val * float(s[n, k // block]) * gs)
+        rows.append(r)
+    return rows

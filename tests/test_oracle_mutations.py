@@ -235,3 +235,52 @@ def test_fp8_mutant_is_caught(name, old, new):
         except Exception:
             results.append(False)
     assert not all(results), f"mutant '{name}' passed every FP8 pin"
+
+
+# NVFP4 path: each mutant must fail the e2m1 pins or the NVFP4 dense brute force
+NVFP4_MUTATIONS = [
+    ("e2m1 exponent bias 0", "(1.0 + m / 2.0) * np.exp2(ex - 1.0)", "(1.0 + m / 2.0) * np.exp2(ex)"),
+    ("e2m1 ties away from zero", "quantum = np.exp2(e - 1.0)       # 1 mantissa bit\n        q = np.rint(ax / quantum) * quantum",
+     "quantum = np.exp2(e - 1.0)       # 1 mantissa bit\n        q = np.floor(ax / quantum + 0.5) * quantum"),
+    ("e2m1 without saturation", "q = np.minimum(q, E2M1_MAX)", "q = q"),
+    ("e2m1 without the subnormal step", "e = np.maximum(e - 1, 0)", "e = e - 1"),
+    ("nibbles swapped", "out[..., 0::2] = b & 0xF\n    out[..., 1::2] = b >> 4",
+     "out[..., 0::2] = b >> 4\n    out[..., 1::2] = b & 0xF"),
+    ("block scale not rounded to e4m3",
+     "sb = round_e4m3((amax_b / six_g[:, None]).astype(np.float32).astype(np.float64))",
+     "sb = (amax_b / six_g[:, None]).astype(np.float64)"),
+    ("token scale from the first block", "amax_t = np.abs(v32).max(axis=1)",
+     "amax_t = np.abs(v32[:, :block]).max(axis=1)"),
+    ("weight tensor scale dropped", "return w * np.repeat(sb, block, axis=1)[:, :K] * float(np.float32(global_scale))",
+     "return w * np.repeat(sb, block, axis=1)[:, :K]"),
+]
+
+
+def _e2m1_check(orc):
+    if orc.e2m1_decode(np.arange(16)).tolist() != bf.E2M1_TABLE + [-v for v in bf.E2M1_TABLE]:
+        return False
+    x = np.concatenate([np.random.default_rng(0).uniform(-8, 8, 2000), np.arange(-7, 7.25, 0.25)])
+    if orc.round_e2m1(x).tolist() != [bf.e2m1_nearest(float(v)) for v in x]:
+        return False
+    return orc.unpack_nvfp4(np.array([[0x21]], dtype=np.uint8)).tolist() == [[1, 2]]
+
+
+def test_unmutated_oracle_passes_the_nvfp4_checks():
+    from oracle import moe_lora_oracle as good
+    from test_oracle_nvfp4 import nvfp4_dense_check
+    assert _e2m1_check(good)
+    assert all(nvfp4_dense_check(good, s) for s in range(2))
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name,old,new", NVFP4_MUTATIONS, ids=[m[0] for m in NVFP4_MUTATIONS])
+def test_nvfp4_mutant_is_caught(name, old, new):
+    from test_oracle_nvfp4 import nvfp4_dense_check
+    m = _mutant(old, new)
+    results = []
+    for check in (lambda: _e2m1_check(m), *[(lambda s=s: nvfp4_dense_check(m, s)) for s in range(2)]):
+        try:
+            results.append(bool(check()))
+        except Exception:
+            results.append(False)
+    assert not all(results), f"mutant '{name}' passed every NVFP4 pin"
