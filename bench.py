@@ -560,6 +560,9 @@ def main():
     ap.add_argument("--routed", choices=["finalize", "unfinalized"], default=None,
                     help="time the externally routed entry instead (auxiliary line, not the headline)")
     args = ap.parse_args()
+    if args.fp8 and (args.routed or args.impl == "reference"):
+        ap.error("--fp8 times the FP8 layer through moe_lora_forward_fp8; it does not combine with "
+                 "--routed or --impl reference")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
