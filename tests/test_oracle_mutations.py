@@ -190,7 +190,8 @@ def test_mutant_is_caught(name, old, new):
 # FP8 block-scale path: each mutant must fail the e4m3 pins or the FP8 dense brute force
 FP8_MUTATIONS = [
     ("e4m3 exponent bias 8", "(1.0 + m / 8.0) * np.exp2(ex - 7.0)", "(1.0 + m / 8.0) * np.exp2(ex - 8.0)"),
-    ("e4m3 ties away from zero", "q = np.rint(ax / quantum) * quantum", "q = np.floor(ax / quantum + 0.5) * quantum"),
+    ("e4m3 ties away from zero", "quantum = np.exp2(e - 3.0)      # 3 mantissa bits\n        q = np.rint(ax / quantum) * quantum",
+     "quantum = np.exp2(e - 3.0)      # 3 mantissa bits\n        q = np.floor(ax / quantum + 0.5) * quantum"),
     ("e4m3 without saturation", "q = np.minimum(q, E4M3_MAX)", "q = q"),
     ("e4m3 without the subnormal step", "e = np.maximum(e - 1, -6)", "e = e - 1"),
     ("weight block scale transposed", "return w * sc[rows[:, None], cols[None, :]]",
