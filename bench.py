@@ -139,6 +139,201 @@ class ClockSampler:
 # GPU arm
 # ------------------------------------------------------------------------------------
 
+def _touched_and_lora(cfg, fwd, pkg, ws, T, E, k, I, H, g, torch):
+    """Touched experts and touched (slot, expert) LoRA bytes of the drawn routing."""
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+    fwd(outputs=dict(expert_offsets=offsets))
+    torch.cuda.synchronize()
+    loads = np.diff(offsets.cpu().numpy())
+    touched = int((loads > 0).sum())
+    st, word = pkg.moe_lora_check_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {word:#x}")
+    lora_blocks = 0
+    slots = g["slot_idx"].cpu().numpy()
+    if cfg.S > 0:
+        ids_out = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        fwd(outputs=dict(topk_ids=ids_out))
+        ids_np = ids_out.cpu().numpy()
+        pairs = {(int(slots[t]), int(e)) for t in range(T) for e in ids_np[t] if slots[t] >= 0}
+        if cfg.shared_outer:   # per (slot, expert): B_gu and A_dn; per slot: A_gu and B_dn
+            lora_blocks = sum(2 * cfg.ranks[s] * (2 * I + I) for s, _ in pairs) + \
+                sum(2 * cfg.ranks[s] * (H + H) for s in {s for s, _ in pairs})
+        else:
+            lora_blocks = sum(2 * cfg.ranks[s] * (2 * H + 3 * I) for s, _ in pairs)
+    return touched, lora_blocks, loads
+
+
+def _act_in_gate_up(P, E):
+    """True where the library runs the activation in the gate_up GEMM's epilogue (token
+    tiles of 32 or more: twice the mean pairs per expert above 16), so that GEMM writes the
+    [P, I] activation instead of the [P, 2I] gate_up output."""
+    return 2 * ((P + E - 1) // E) > 16
+
+
+def _gemm_roofline(name, flops, nbytes, avg_s, peaks, tc_peak, tc_src):
+    """Roofline block of one GEMM launch: tensor-bound when its flops at the tensor peak take
+    longer than its algorithmic bytes at the HBM peak, else HBM-bound."""
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
+    if t_tc > t_hbm:
+        ach = flops / avg_s / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": ach / tc_peak, "peak_source": tc_src, "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": nbytes, "avg_launch_us": avg_s * 1e6}
+    ach = nbytes / avg_s / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} hbm_gbs",
+            "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+            "avg_launch_us": avg_s * 1e6}
+
+
+def _timed_steps(fwd, stream, steps, torch, pkg, clock_index=None, world=1):
+    """Time `steps` forwards between CUDA events on `stream`.  On every EV_EVERY-th step the
+    gate_up and down GEMMs are bracketed by events on their stream (an event between two
+    kernels holds the second one back from starting early, so not on every step).
+    Returns (seconds, mean gate_up GEMM seconds, mean down GEMM seconds, clocks)."""
+    n_ev = 2 * pkg.NUM_STAGES
+    gu = pkg.STAGES.index("gate_up_gemm")
+    dn = pkg.STAGES.index("down_gemm")
+    ev_sets = []
+    for _ in range((steps + EV_EVERY - 1) // EV_EVERY):
+        evs = [None] * n_ev
+        for i in (2 * gu, 2 * gu + 1, 2 * dn, 2 * dn + 1):
+            evs[i] = torch.cuda.Event(enable_timing=True)
+            evs[i].record(stream)          # materialise the CUDA event handle
+        ev_sets.append(evs)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(clock_index) if clock_index is not None else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        fwd(prof=ev_sets[i // EV_EVERY] if i % EV_EVERY == 0 else None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    sec = t0.elapsed_time(t1) / 1e3
+    gu_s = statistics.mean(ev[2 * gu].elapsed_time(ev[2 * gu + 1]) for ev in ev_sets) / 1e3
+    dn_s = statistics.mean(ev[2 * dn].elapsed_time(ev[2 * dn + 1]) for ev in ev_sets) / 1e3
+    return sec, gu_s, dn_s, clk
+
+
+def _lora_off_ms(fwd, stream, steps, warmup, torch, pkg):
+    for _ in range(warmup):
+        fwd(flags=pkg.FLAG_LORA_OFF)
+    torch.cuda.synchronize()
+    o0 = torch.cuda.Event(enable_timing=True)
+    o1 = torch.cuda.Event(enable_timing=True)
+    o0.record(stream)
+    for _ in range(steps):
+        fwd(flags=pkg.FLAG_LORA_OFF)
+    o1.record(stream)
+    torch.cuda.synchronize()
+    return o0.elapsed_time(o1) / steps
+
+
+def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None):
+    def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
+        flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
+        hid = g["hidden"] if hidden is None else hidden
+        lg = g["router_logits"] if logits is None else logits
+        kw = dict(routing_method=cfg.method, correction_bias=g["correction_bias"],
+                  routed_scaling_factor=cfg.rsf, lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"],
+                  lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"],
+                  slot_idx=g["slot_idx"] if slot is None else slot, ranks=cfg.ranks, scalings=cfg.scalings,
+                  flags=flags, out=o, workspace=ws, prof_events=prof, outputs=outputs)
+        if w8 is not None:
+            return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw)
+        return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw)
+    return fwd
+
+
+# the BASELINE configurations timed beside the headline decode workload, in this order
+SIDE_WORKLOADS = ["multi_slot", "prefill_zipf", "kimi_decode", "kimi_prefill"]
+SIDE_BUDGET_S = 4.0   # timed seconds per side workload (LoRA on); steps are capped to fit
+
+
+def measure_side_workload(name, args, h, local, peaks):
+    """One entry of the line's `workloads` object: the same measurements as the headline
+    (device-timed steps with inputs resident in HBM, LoRA-on / LoRA-off, the step's roofline
+    fraction and both GEMMs' roofline blocks) on another configuration.  Steps are the run's
+    --steps, capped so the timed region stays near SIDE_BUDGET_S; warm-up is the run's."""
+    import torch
+    import routed_moe_expert_gb300 as pkg
+    from routed_moe_expert_gb300 import workloads as wl
+
+    cfg = wl.CONFIGS[name]
+    g = wl.make_inputs(cfg, seed=args.seed, device="cuda")
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    P = T * k
+    ws = pkg.alloc_workspace(T, H, I, E, k, cfg.S, cfg.R)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    fwd = _make_fwd(pkg, h, cfg, g, ws, out, k, args)
+    touched, lora_blocks, loads = _touched_and_lora(cfg, fwd, pkg, ws, T, E, k, I, H, g, torch)
+    slots = g["slot_idx"].cpu().numpy()
+    w_bytes_expert = 3 * H * I * 2
+    io_bytes = T * H * 2 * 2 + T * E * 2
+    step_bytes = touched * w_bytes_expert + lora_blocks + io_bytes
+    step_flops = 2 * 3 * H * I * P + sum(2 * cfg.ranks[int(slots[t])] * (2 * H + 3 * I) * k
+                                         for t in range(T) if cfg.S > 0 and slots[t] >= 0)
+    act_fused = _act_in_gate_up(P, E)
+    gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + (P * I * 2 if act_fused else P * 2 * I * 2)
+    gu_flops = 2 * 2 * I * H * P
+    dn_bytes = touched * (H * I * 2) + P * I * 2 + P * H * 4
+    dn_flops = 2 * H * I * P
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - w0) / 3
+    steps = int(max(args.warmup, min(args.steps, SIDE_BUDGET_S / max(est, 1e-6))))
+    sec, gu_s, dn_s, clk = _timed_steps(fwd, stream, steps, torch, pkg, clock_index=local)
+    ms = 1e3 * sec / steps
+    tc_peak = peaks["bf16_tflops_sustained"]
+    tc_src = f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long loop)"
+    t_hbm = step_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = step_flops / (tc_peak * 1e12)
+    entry = {
+        "workload": cfg.describe(), "T": T, "H": H, "I": I, "E": E, "top_k": k,
+        "lora_ranks": list(cfg.ranks), "routing": "DeepSeekV3" if cfg.method else "Renormalize",
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
+        "touched_experts": touched, "max_over_mean_expert_load": float(loads.max() / max(loads.mean(), 1e-9)),
+        "step_bytes": step_bytes, "step_flops": step_flops,
+        "step_bound": "tensor" if t_tc > t_hbm else "hbm",
+        "step_roofline_frac": max(t_hbm, t_tc) / (ms / 1e3),
+        "step_roofline_peak": (f"{tc_peak} TFLOP/s ({tc_src})" if t_tc > t_hbm
+                               else f"{peaks['hbm_gbs']} GB/s ({peaks['source']} hbm_gbs)"),
+        "l2": f"inputs larger than L2: {touched} touched experts = {touched * w_bytes_expert / 1e9:.2f} GB "
+              f"of weights per step",
+        "gate_up_gemm": _gemm_roofline("grouped_gemm (gate_up)", gu_flops, gu_bytes, gu_s, peaks, tc_peak, tc_src),
+        "down_gemm": _gemm_roofline("grouped_gemm (down)", dn_flops, dn_bytes, dn_s, peaks, tc_peak, tc_src),
+        "clocks": clk,
+    }
+    if cfg.S > 0:
+        off_ms = _lora_off_ms(fwd, stream, max(1, steps // 2), args.warmup, torch, pkg)
+        entry["lora_off_ms_per_step"] = off_ms
+        entry["lora_on_over_off"] = off_ms / ms
+    st, word = pkg.moe_lora_check_status(ws)
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {word:#x}")
+    del g, ws, out, fwd
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -166,54 +361,25 @@ def run_gpu(args):
     h = pkg.Handle(local)
     ws = pkg.alloc_workspace(T, H, I, E, k, cfg.S, cfg.R)
     out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
-
-    def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
-        flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
-        hid = g["hidden"] if hidden is None else hidden
-        lg = g["router_logits"] if logits is None else logits
-        kw = dict(routing_method=cfg.method, correction_bias=g["correction_bias"],
-                  routed_scaling_factor=cfg.rsf, lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"],
-                  lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"],
-                  slot_idx=g["slot_idx"] if slot is None else slot, ranks=cfg.ranks, scalings=cfg.scalings,
-                  flags=flags, out=o, workspace=ws, prof_events=prof, outputs=outputs)
-        if w8 is not None:
-            return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw)
-        return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw)
+    fwd = _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8)
 
     # touched experts (routing is fixed for the fixed input)
-    fwd(outputs=dict(expert_offsets=offsets))
-    torch.cuda.synchronize()
-    loads = np.diff(offsets.cpu().numpy())
-    touched = int((loads > 0).sum())
-    st, word = pkg.moe_lora_check_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status {word:#x}")
+    touched, lora_blocks, _ = _touched_and_lora(cfg, fwd, pkg, ws, T, E, k, I, H, g, torch)
+    slots = g["slot_idx"].cpu().numpy()
 
     # algorithmic bytes / flops (FP8: one byte per weight plus a float per 128 x 128 block,
     # the permuted hidden rows as codes plus a float per 128 values)
     wb = 1 if w8 is not None else 2
     w_bytes_expert = 3 * H * I * wb + (3 * H * I // (128 * 128) * 4 if w8 is not None else 0)
-    lora_blocks = 0
-    slots = g["slot_idx"].cpu().numpy()
-    ids_np = None
-    if cfg.S > 0:
-        ids_out = torch.empty((T, k), dtype=torch.int32, device="cuda")
-        fwd(outputs=dict(topk_ids=ids_out))
-        ids_np = ids_out.cpu().numpy()
-        pairs = {(int(slots[t]), int(e)) for t in range(T) for e in ids_np[t] if slots[t] >= 0}
-        if cfg.shared_outer:   # per (slot, expert): B_gu and A_dn; per slot: A_gu and B_dn
-            lora_blocks = sum(2 * cfg.ranks[s] * (2 * I + I) for s, _ in pairs) + \
-                sum(2 * cfg.ranks[s] * (H + H) for s in {s for s, _ in pairs})
-        else:
-            lora_blocks = sum(2 * cfg.ranks[s] * (2 * H + 3 * I) for s, _ in pairs)
     io_bytes = T * H * 2 * 2 + T * E * 2
     step_bytes = touched * w_bytes_expert + lora_blocks + io_bytes
     step_flops = 2 * 3 * H * I * P + sum(2 * cfg.ranks[max(int(slots[t]), 0)] * (2 * H + 3 * I) * k
                                          for t in range(T) if cfg.S > 0 and slots[t] >= 0)
+    act_fused = w8 is None and _act_in_gate_up(P, E)
+    g_out = P * I * 2 if act_fused else P * 2 * I * 2
     if w8 is None:
-        gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + P * 2 * I * 2   # weights + xp read + g write
+        gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + g_out   # weights + xp read + g (or a) write
     else:
         gu_bytes = touched * (2 * I * H + 2 * I * H // (128 * 128) * 4) + P * H + P * H // 128 * 4 + P * 2 * I * 2
     gu_flops = 2 * 2 * I * H * P
@@ -222,41 +388,13 @@ def run_gpu(args):
         fwd()
     torch.cuda.synchronize()
 
-    # ---- device-timed region: K steps; on every EV_EVERY-th step the gate_up GEMM is
-    # bracketed by events on its stream (an event between two kernels holds the second
-    # one back from starting early, so not on every step)
-    n_ev = 2 * pkg.NUM_STAGES
-    gu = pkg.STAGES.index("gate_up_gemm")
-    ev_pairs = []
-    for _ in range((args.steps + EV_EVERY - 1) // EV_EVERY):
-        evs = [None] * n_ev
-        evs[2 * gu] = torch.cuda.Event(enable_timing=True)
-        evs[2 * gu + 1] = torch.cuda.Event(enable_timing=True)
-        for e in (evs[2 * gu], evs[2 * gu + 1]):
-            e.record(stream)          # materialise the CUDA event handle
-        ev_pairs.append(evs)
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    # ---- device-timed region: K steps (gate_up and down GEMM events on every 16th step)
     launches0 = h.launch_count()
-    t0.record(stream)
-    for i in range(args.steps):
-        fwd(prof=ev_pairs[i // EV_EVERY] if i % EV_EVERY == 0 else None)
-    t1.record(stream)
+    sec, gu_avg_s, dn_avg_s, clk = _timed_steps(fwd, stream, args.steps, torch, pkg, clock_index=local,
+                                                world=world)
     launches = h.launch_count() - launches0
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    sec = t0.elapsed_time(t1) / 1e3
     sec_max = max_over_ranks(sec, world)
     agg = aggregate(T, args.steps, world, sec_max)
-    gu_ms = [ev[2 * gu].elapsed_time(ev[2 * gu + 1]) for ev in ev_pairs]
-    gu_avg_s = statistics.mean(gu_ms) / 1e3
 
     # ---- end-to-end: inputs from pinned host memory each step, result back to host
     h_hidden = g["hidden"].cpu().pin_memory()
@@ -354,22 +492,13 @@ def run_gpu(args):
     }
     if cfg.S > 0:
         # LoRA-off throughput of the same kernels, for the on/off ratio
-        for _ in range(args.warmup):
-            fwd(flags=pkg.FLAG_LORA_OFF)
-        torch.cuda.synchronize()
-        o0 = torch.cuda.Event(enable_timing=True)
-        o1 = torch.cuda.Event(enable_timing=True)
-        o0.record(stream)
-        for _ in range(max(1, args.steps // 4)):
-            fwd(flags=pkg.FLAG_LORA_OFF)
-        o1.record(stream)
-        torch.cuda.synchronize()
-        off_ms = o0.elapsed_time(o1) / max(1, args.steps // 4)
+        off_ms = _lora_off_ms(fwd, stream, max(1, args.steps // 4), args.warmup, torch, pkg)
         line["config"]["lora_off_ms_per_step"] = off_ms
         line["config"]["lora_on_over_off"] = off_ms / agg["ms_per_step"]
     if args.stage_times:
         # average device time of every stage of the forward (events on the stream that runs
         # each stage), LoRA on and LoRA off
+        n_ev = 2 * pkg.NUM_STAGES
         for label, fl in (("lora_on", 0), ("lora_off", pkg.FLAG_LORA_OFF)):
             n = 50
             evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n)]
@@ -393,6 +522,17 @@ def run_gpu(args):
                 if vals:
                     st_ms[name] = round(1e3 * statistics.median(vals), 2)
             line.setdefault("stage_us", {})[label] = st_ms
+    # the other BASELINE configurations, one after another on the same GPU (rank 0 of a
+    # single-GPU run only: replicas would repeat the same numbers), each freed before the next
+    side = [] if (w8 is not None or world > 1 or args.workload != "decode" or args.no_workloads) else \
+        [w for w in SIDE_WORKLOADS if args.only_workloads is None or w in args.only_workloads.split(",")]
+    if side:
+        del fwd, ws, out, bufs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name in side:
+            line["workloads"][name] = measure_side_workload(name, args, h, local, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, args, w8=w8)
     if rank == 0:
@@ -559,6 +699,10 @@ def main():
                     help="block-FP8 expert weights (e4m3, 128x128 scales) quantised from the drawn bf16 ones")
     ap.add_argument("--routed", choices=["finalize", "unfinalized"], default=None,
                     help="time the externally routed entry instead (auxiliary line, not the headline)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the decode headline only (no `workloads` object for the other configurations)")
+    ap.add_argument("--only-workloads", default=None,
+                    help="comma-separated subset of the other configurations to time")
     args = ap.parse_args()
     if args.fp8 and (args.routed or args.impl == "reference"):
         ap.error("--fp8 times the FP8 layer through moe_lora_forward_fp8; it does not combine with "

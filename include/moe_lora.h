@@ -276,7 +276,11 @@ moe_lora_status moe_lora_quant_fp8(moe_lora_handle* h, const moe_lora_bf16* src,
    resolves the array's address on the current device (cudaGetSymbolAddress), so make
    that first call before any stream capture.  All calls share the array: each call
    clears its status word and barrier counter on `stream`, and calls that overlap on the
-   GPU race.  Device-side wait timeouts are recorded in the shared array, not reported.
+   GPU race.  A device-side wait that runs out (which such a race can cause) is recorded
+   only in the shared array, which no call reads back: the outputs of that call are then
+   wrong and nothing reports it.  The array's address is looked up once per device and
+   kept for the life of the process, so do not call this on a device after
+   cudaDeviceReset (or another reset of its primary context) in the same process.
    Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_logits, const float* correction_bias,
                                        int T, int E, int top_k, int routing_method,

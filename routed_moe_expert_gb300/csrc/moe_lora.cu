@@ -527,10 +527,24 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   const bool two = lora && (((T <= 256) && !(a->flags & MOE_LORA_FLAG_FORCE_SINGLE_STREAM)) ||
                             (a->flags & MOE_LORA_FLAG_FORCE_TWO_STREAM));
   cudaStream_t ls = two ? h->side : stream;
+  // Once the side stream has been forked, every return before the join below still joins
+  // it back (recording the ready event on the side stream first if that has not happened),
+  // so a failed enqueue never leaves a capture on `stream` with an unjoined fork.
+  struct ForkJoin {
+    moe_lora_handle* h;
+    cudaStream_t main;
+    bool forked = false, ready = false, joined = false;
+    ~ForkJoin() {
+      if (!forked || joined) return;
+      if (!ready) cudaEventRecord(h->ev_ready, h->side);
+      cudaStreamWaitEvent(main, h->ev_ready, 0);
+    }
+  } fj{h, stream};
   if (lora) {   // gate_up LoRA: shrink + expand into the bf16 delta d
     if (two) {
       ML_CUDA(cudaEventRecord(h->ev_fork, stream), "cudaEventRecord");
       ML_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0), "cudaStreamWaitEvent");
+      fj.forked = true;
     }
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, ls);
     LoraParams lp;
@@ -561,7 +575,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     }
     ML_LAUNCH(h, launch_lora(lp, lora_ntl, lora_grid, ls, pdl && !two), "lora gate_up launch");
     prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, ls);
-    if (two) ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
+    if (two) {
+      ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
+      fj.ready = true;
+    }
   }
 
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
@@ -578,7 +595,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   }
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
 
-  if (fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  if (fused_gu && two) {
+    fj.joined = true;
+    ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  }
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
   GemmParams gu;
   std::memset(&gu, 0, sizeof(gu));
@@ -609,7 +629,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
 
-  if (!fused_gu && two) ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  if (!fused_gu && two) {
+    fj.joined = true;
+    ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  }
   // (no programmatic launch right behind a wait on the side stream)
   const bool pdl_act = pdl && !two;
   if (act_shrink) {

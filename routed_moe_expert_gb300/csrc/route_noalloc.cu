@@ -15,6 +15,10 @@
 // All calls share the array and it keeps the previous call's contents: the status word
 // and barrier counter are cleared on `stream` at the start of every call, and calls whose
 // work overlaps on the GPU (different streams, or different threads) race on it.
+// The array's address is looked up once per device and kept for the life of the process,
+// so the entry point must not be called on a device after cudaDeviceReset (or any other
+// reset of its primary context) in the same process: the kept address would belong to the
+// context that was torn down.
 #include "../../include/moe_lora.h"
 #include "kernels.h"
 
@@ -36,9 +40,13 @@ static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBy
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char* g_scratch_ptr[kMaxDevices] = {};
+// Cooperative routing CTAs that fit on the device, per expert count (0 = not yet asked),
+// so a call after the first does no occupancy query.
+int g_coop_ctas[kMaxDevices][kMaxExperts + 1] = {};
 
-// Once per device, with that device current: resolve the array's device address.
-moe_lora_status setup_device(int dev, unsigned char** ptr) {
+// Once per device, with that device current: resolve the array's device address; and
+// once per (device, E): the cooperative grid limit of the routing kernel.
+moe_lora_status setup_device(int dev, int E, unsigned char** ptr, int* coop) {
   if (dev < 0 || dev >= kMaxDevices) return MOE_LORA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
@@ -46,7 +54,9 @@ moe_lora_status setup_device(int dev, unsigned char** ptr) {
     if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_LORA_ERR_CUDA;
     g_scratch_ptr[dev] = static_cast<unsigned char*>(p);
   }
+  if (g_coop_ctas[dev][E] == 0) g_coop_ctas[dev][E] = route_max_coop_ctas(E);
   *ptr = g_scratch_ptr[dev];
+  *coop = g_coop_ctas[dev][E];
   return MOE_LORA_OK;
 }
 
@@ -77,7 +87,8 @@ extern "C" moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_lo
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_LORA_ERR_CUDA;
   unsigned char* scratch = nullptr;
-  moe_lora_status st = setup_device(dev, &scratch);
+  int coop = 0;
+  moe_lora_status st = setup_device(dev, E, &scratch, &coop);
   if (st != MOE_LORA_OK) return st;
 
   if (cudaMemsetAsync(scratch, 0, kHeaderBytes, stream) != cudaSuccess) return MOE_LORA_ERR_CUDA;
@@ -88,7 +99,6 @@ extern "C" moe_lora_status moe_lora_route_noalloc(const moe_lora_bf16* router_lo
   }
 
   int grid = (T + 63) / 64;
-  const int coop = route_max_coop_ctas(E);
   if (grid > coop) grid = coop;
   if (grid > kMaxRouteCtas) grid = kMaxRouteCtas;
   const int fit = static_cast<int>((kNoAllocScratchBytes - fixed) / per_cta);
