@@ -85,15 +85,27 @@ cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, in
 }
 
 // ---------------------------------------------------------------------------------
-// finalize: out[t, h] = bf16( sum_{j<k} w[t,j] * y[inv[t*k + j], h] ), fixed j order.
-// y already holds the down GEMM output plus the (unweighted) down-LoRA delta, added in
-// the down GEMM's epilogue, so this is the vLLM API page's _finalize_with_w2_lora
+// finalize: out[t, h] = bf16( sum_{j<k} w[t,j] * y[inv[t*k + j], h] ), fixed j order, fp32.
+// y (fp32, or bf16 at wide token tiles) already holds the down GEMM output plus the
+// (unweighted) down-LoRA delta, added in the down GEMM's epilogue, so this is the vLLM API
+// page's _finalize_with_w2_lora
 // ("fused_moe/experts/trtllm_lora_moe": routing-weighted sum over top_k of the base rows
 // plus the routing-weighted down-LoRA delta).  A CTA covers 512 h of one token.
 // ---------------------------------------------------------------------------------
-constexpr int kFinThreads = 128;   // 4 floats each: 512 h per CTA
+constexpr int kFinThreads = 128;   // 4 values each: 512 h per CTA
 
-__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams p) {
+MLDEV float4 load_y4(const float* y, size_t row, int H, int h4) {
+  return __ldg(reinterpret_cast<const float4*>(y + row * H) + h4);
+}
+MLDEV float4 load_y4(const __nv_bfloat16* y, size_t row, int H, int h4) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(y + row * H) + h4);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+template <typename YT>
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams p, const YT* __restrict__ y) {
   __shared__ int q_s[kMaxTopK];
   __shared__ float w_s[kMaxTopK];
   pdl_wait();
@@ -111,12 +123,12 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
 #pragma unroll 8
   for (int j = 0; j < k; ++j) {
     if (q_s[j] < 0) continue;   // a pair of an expert outside the local range (routed entry)
-    const float4 y = __ldg(reinterpret_cast<const float4*>(p.y + static_cast<size_t>(q_s[j]) * p.H) + h4);
+    const float4 v = load_y4(y, static_cast<size_t>(q_s[j]), p.H, h4);
     const float w = w_s[j];
-    acc.x += w * y.x;
-    acc.y += w * y.y;
-    acc.z += w * y.z;
-    acc.w += w * y.w;
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
   }
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
@@ -129,8 +141,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   if (p.T == 0) return cudaSuccess;
   const int H4 = p.H / 4;
-  return launch_k(finalize_kernel, dim3(p.T, (H4 + kFinThreads - 1) / kFinThreads), dim3(kFinThreads), 0, stream,
-                  pdl, p);
+  const dim3 grid(p.T, (H4 + kFinThreads - 1) / kFinThreads);
+  if (p.y != nullptr) return launch_k(finalize_kernel<float>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y);
+  return launch_k(finalize_kernel<__nv_bfloat16>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y_bf16);
 }
 
 // ---------------------------------------------------------------------------------

@@ -51,22 +51,32 @@ constexpr uint64_t kPeerDrainNs = 100000;             // 100 us for an aborted o
 
 int gemm_stage_bytes(int rows) { return kAByte + rows * 128; }
 
-int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int f32_out) {
+int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int y_tma) {
   // Carve-up, in order (see the kernel): 1 KB alignment slack; stage buffers; full/empty
-  // barriers (2*stages), tfull/tempty (4), drain (1), dempty (1); tmem slot + abort flag (16 B);
-  // tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for the
-  // CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes; then,
-  // for the plain epilogues, the four warps' 16 x 32 float store buffers (two each for an fp32
-  // output, whose whole chunks leave by TMA while the next one is staged).
+  // barriers (2*stages), tfull/tempty (4), drain (1), dfull/dfree (2); tmem slot + abort flag
+  // (16 B); tile_start and seg (E+1 ints each); the tile slot ring; 4 ints of padding; and, for
+  // the CUDA-core LoRA epilogue, BN token slots then BN x RP8 floats aligned to 16 bytes; then,
+  // for the plain epilogues, the four warps' 16 x 32 float store buffers (two each when whole
+  // chunks leave by TMA, one staged while the previous one is stored).
   const int ring = 4 * (kTileRing + 4);
   const int lora = lora_R > 0 ? bn * 4 + 16 + bn * ((lora_R + 7) / 8 * 8) * 4 : 0;
   const int xchg = act_fused ? kXchgFloats * 4 : 0;   // gate -> up hand-off (fused activation)
-  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + 128 + (f32_out ? 2 : 1) * kYbufFloats * 4;
-  return 1024 + stages * gemm_stage_bytes(bn / cg) + (2 * stages + 6) * 8 + 16 + 8 * (E + 1) + ring +
+  const int ybuf = act_fused ? 0 : (lora_R > 0 ? 0 : bn * 4 + 16) + 128 + (y_tma ? 2 : 1) * kYbufFloats * 4;
+  return 1024 + stages * gemm_stage_bytes(bn / cg) + (2 * stages + 7) * 8 + 16 + 8 * (E + 1) + ring +
          (lora > xchg ? lora : xchg) + ybuf;
 }
 
 MLDEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // the 4 epilogue warps
+
+// Fused LoRA expand stages sit after this many of a tile's KB main K-stages (at least one main
+// stage goes first, so the main accumulator is initialised by a main MMA).  Placed before the
+// end of the main loop, their MMAs (and, at 256-token tiles, the wait for the idle accumulator)
+// overlap the tile's remaining main stages instead of following them.
+__host__ __device__ constexpr int lora_stage_pos(int KB) { return KB >= 4 ? (3 * KB) / 4 : 1; }
+// 64-wide K blocks of slot `rank`'s LoRA stage that hold data (the rest is zero fill), and the
+// 16-deep MMA steps of block kb that do.
+MLDEV int lora_blocks(int rank, int lora_kb) { return min(lora_kb, (rank + 63) >> 6); }
+MLDEV int lora_ksteps(int rank, int kb) { return min(4, (rank - 64 * kb + 15) >> 4); }
 
 // LoRA expand of one 16-token chunk on the CUDA cores, for output feature `feat` (this
 // thread's weight row): val[j] += sum_{r < ranks[s]} lora_B[s, e, feat, r] * v_s[c + j][r]
@@ -117,10 +127,12 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
 // accumulator (so g and the delta are rounded to bf16 separately).  Each mode is its own
 // instantiation, so a launch carries only its own code.
 //
-// TMEM (512 columns): kAccBufs accumulators of BN columns, then kDeltaBufs delta accumulators.
-// Two of each up to BN = 128; at BN = 160 the single delta buffer is guarded by `dempty`
-// (the LoRA stages of tile i wait until the epilogue has read tile i-1's delta, which
-// it did while tile i's main loop ran); at BN = 256 MODE 4 has one of each.
+// TMEM (512 columns): two accumulators of BN columns, and in MODE 4 up to BN = 128 two delta
+// accumulators after them.  At wider tiles MODE 4 has no room for a delta buffer, so tile i's
+// LoRA stages go into the idle accumulator (the one tile i+1 will use) once tile i-1's
+// activation has left it: the epilogue first merges bf16(g) + bf16(delta) back into tile i's
+// accumulator (tcgen05.st) and hands the idle buffer back (`dfree`), then forms the
+// activation.  The main loop of tile i+1 waits only for that merge, a short pass over TMEM.
 //
 // CG = 2: clusters of two CTAs (one TPC) share each tile as an M = 256 tcgen05 pair MMA.
 // A tile is then two consecutive 128-row weight tiles (the even CTA's, then the odd CTA's)
@@ -142,8 +154,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   constexpr uint32_t A_BYTES = kAByte;
   constexpr uint32_t STAGE = A_BYTES + BNH * 128;
   constexpr bool delta_acc = MODE == 4;
-  constexpr int kAccBufs = (2 * BN + (delta_acc ? BN : 0) <= 512) ? 2 : 1;
-  constexpr int kDeltaBufs = !delta_acc ? 0 : (kAccBufs * BN + 2 * BN <= 512) ? 2 : 1;
+  constexpr int kAccBufs = 2;
+  static_assert(2 * BN <= 512, "two accumulators fit TMEM");
+  constexpr bool kDeltaIdle = delta_acc && 4 * BN > 512;   // the delta goes into the idle accumulator
+  constexpr int kDeltaBufs = (delta_acc && !kDeltaIdle) ? 2 : 0;
   constexpr uint32_t kColsUsed = static_cast<uint32_t>((kAccBufs + kDeltaBufs) * BN);
   static_assert(kColsUsed <= 512u, "accumulators exceed TMEM");
   constexpr uint32_t TMEM_COLS = kColsUsed <= 32u ? 32u : kColsUsed <= 64u ? 64u : kColsUsed <= 128u ? 128u
@@ -158,8 +172,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   uint64_t* tfull = empty + S;       // [2]
   uint64_t* tempty = tfull + 2;      // [2]
   uint64_t* drain = tempty + 2;      // [1], used only after an abort
-  uint64_t* dempty = drain + 1;      // [1], the single delta buffer is free (kDeltaBufs == 1)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
+  uint64_t* dfull = drain + 1;       // [1], MODE 4 with kDeltaIdle: the tile's delta is complete
+  uint64_t* dfree = dfull + 1;       // [1], ... and merged: the idle accumulator is free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);   // [E + 1]
   int* seg = tile_start + (p.E + 1);                         // offsets copy [E + 1]
@@ -187,7 +202,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     mbar_init(&tempty[0], kRelease);
     mbar_init(&tempty[1], kRelease);
     mbar_init(drain, 1);
-    mbar_init(dempty, kRelease);
+    mbar_init(dfull, 1);
+    mbar_init(dfree, kRelease);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -289,7 +305,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       int e, nt, qt, wr0, wr1;
       decode(cta0, e, nt, qt);
       weight_rows(e, nt, wr0, wr1);
-      npre = min(S, KB);
+      npre = min(S, kFused ? lora_stage_pos(KB) : KB);   // main stages only: the LoRA stages follow later
       for (int s2 = 0; s2 < npre; ++s2) {
         uint8_t* a = smem + s2 * STAGE;
         if (leader) mbar_arrive_expect_tx(&full[s2], CG * STAGE);
@@ -329,24 +345,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const int j = lane + 32 * u;
           slv[u] = j < nv ? p.pair_slot[xr + j] : -1;
         }
+        const int kb_lora = lora_stage_pos(KB);
         if (lane == 0)
-          for (int kb = 0; ok && kb < KB - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xh);
+          for (int kb = 0; ok && kb < kb_lora - 1; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xh);
         unsigned lmask = 0;
 #pragma unroll
         for (int u = 0; u < kSlotLoads; ++u)
           if (slv[u] >= 0 && slv[u] < kMaxFusedSlots) lmask |= 1u << slv[u];
         const unsigned smask = __reduce_or_sync(0xffffffffu, lmask);
         if (lane == 0) {
-          // published before the tile's last main stage arrives (arrive.expect_tx releases it);
-          // the MMA warp reads it after consuming that stage
+          // published before the main stage in front of the LoRA stages arrives
+          // (arrive.expect_tx releases it); the MMA warp reads it after consuming that stage
           tile_slot_ring[it_tile % kTileRing] = smask;
           const int lb_off = p.lora_b_e1 ? e * p.N : 0;   // a shared B has one expert's rows
-          if (ok) ok = issue(&p.tmap_w, wr0, wr1, (KB - 1) * 64, &p.tmap_x, xh);
+          if (ok) ok = issue(&p.tmap_w, wr0, wr1, (kb_lora - 1) * 64, &p.tmap_x, xh);
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
             if (!((smask >> sl) & 1u)) continue;
-            for (int kb = 0; ok && kb < p.lora_kb; ++kb)
+            const int nkb = lora_blocks(p.slots.ranks[sl], p.lora_kb);
+            for (int kb = 0; ok && kb < nkb; ++kb)
               ok = issue(&p.tmap_lb[sl], wr0 - lb_off, wr1 - lb_off, kb * 64, &p.tmap_lu, sl * p.P + xh);
           }
+          for (int kb = kb_lora; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xh);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
@@ -370,7 +389,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     uint32_t aphase = 0;
     uint32_t dphase = 0;
     int ok = 1;
-    auto consume = [&](uint32_t d, bool first) -> bool {
+    auto consume = [&](uint32_t d, bool first, int nk = 4) -> bool {   // nk: 16-deep steps with data
       if (!mbar_wait(&full[stage], phase, abort_flag, p.status, kWhereGemmMma)) return false;
       tc_fence_after();
       const uint32_t a_addr = smem_u32(smem + stage * STAGE);
@@ -378,6 +397,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       const uint64_t bd = sw128_kmajor_desc(a_addr + A_BYTES);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
+        if (kk >= nk) break;
         if constexpr (CG == 2) umma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
         else umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
       }
@@ -389,34 +409,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
       return true;
     };
+    auto commit_all = [&](uint64_t* bar) {   // arrive on `bar` in the epilogue's CTA(s)
+      if constexpr (CG == 2) umma_commit_pair_mc(bar, 0x3);
+      else umma_commit(bar);
+    };
     if (lane == 0 && leader) {   // the pair's MMAs are issued by its even CTA
       int it_tile = 0;
       for (int tile = cta0; ok && tile < total; tile += ncta, ++it_tile) {
         if (!mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, p.status, kWhereGemmMma)) break;
+        if constexpr (kDeltaIdle) {   // the previous tile's delta has been merged out of this buffer
+          if (it_tile > 0) {
+            if (!mbar_wait(dfree, dphase, abort_flag, p.status, kWhereGemmMma)) break;
+            dphase ^= 1u;
+          }
+        }
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; ok && kb < KB; ++kb) ok = consume(d, kb == 0);
+        const int kb_lora = kFused ? lora_stage_pos(KB) : KB;
+        for (int kb = 0; ok && kb < kb_lora; ++kb) ok = consume(d, kb == 0);
         if constexpr (kFused) {
-          // the tile's first stage has landed, so its slot mask is published
+          // the stage in front of the LoRA stages has landed, so the slot mask is published
           const unsigned smask = tile_slot_ring[it_tile % kTileRing];
-          const uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(kAccBufs * BN + (kDeltaBufs == 2 ? acc * BN : 0)) : d;
-          bool first_delta = delta_acc;   // the delta accumulator starts fresh each tile
-          if constexpr (delta_acc && kDeltaBufs == 1) {   // every tile, LoRA or not
-            ok = mbar_wait(dempty, dphase ^ 1u, abort_flag, p.status, kWhereGemmMma);
-            dphase ^= 1u;
-            tc_fence_after();
+          uint32_t dl = delta_acc ? tmem_base + static_cast<uint32_t>(kAccBufs * BN + acc * BN) : d;
+          if constexpr (kDeltaIdle) {
+            dl = tmem_base + static_cast<uint32_t>((acc ^ 1) * BN);
+            if (ok && smask != 0u) {   // the idle buffer, once tile i-1's activation has left it
+              const uint32_t xpar = ((static_cast<uint32_t>(it_tile + 1) >> 1) & 1u) ^ 1u;
+              ok = mbar_wait(&tempty[acc ^ 1], xpar, abort_flag, p.status, kWhereGemmMma);
+              tc_fence_after();
+            }
           }
+          bool first_delta = delta_acc;   // the delta accumulator starts fresh each tile
           for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
             if (!((smask >> sl) & 1u)) continue;
-            for (int kb = 0; ok && kb < p.lora_kb; ++kb) {
-              ok = consume(dl, first_delta);
+            const int rank = p.slots.ranks[sl];
+            const int nkb = lora_blocks(rank, p.lora_kb);
+            for (int kb = 0; ok && kb < nkb; ++kb) {
+              ok = consume(dl, first_delta, lora_ksteps(rank, kb));
               first_delta = false;
             }
           }
         }
+        for (int kb = kb_lora; ok && kb < KB; ++kb) ok = consume(d, false);
         if (!ok) break;
-        if constexpr (CG == 2) umma_commit_pair_mc(&tfull[acc], 0x3);   // both CTAs' epilogues
-        else umma_commit(&tfull[acc]);
+        commit_all(&tfull[acc]);   // both CTAs' epilogues
+        if constexpr (kDeltaIdle) commit_all(dfull);   // every tile, LoRA or not
         if (++acc == kAccBufs) {
           acc = 0;
           aphase ^= 1u;
@@ -428,7 +465,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int I = p.N >> 1;
     float* xchg = reinterpret_cast<float*>(lslot);   // [2][64][kXchgStride]
     int acc = 0, chunk = 0;
-    uint32_t aphase = 0;
+    uint32_t aphase = 0, dfphase = 0;
     for (int tile = cta0; tile < total; tile += ncta) {
       int e, nt, qt;
       decode(tile, e, nt, qt);
@@ -447,18 +484,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       tc_fence_after();
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tm = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
-      const uint32_t td = tmem_base + lane_base + static_cast<uint32_t>(kAccBufs * BN + (kDeltaBufs == 2 ? acc * BN : 0));
+      const uint32_t td = tmem_base + lane_base +
+                          static_cast<uint32_t>(kDeltaIdle ? (acc ^ 1) * BN : kAccBufs * BN + acc * BN);
+      // With the delta in the idle accumulator: z = bf16(g) + bf16(delta) goes back into this
+      // tile's accumulator first, and the idle buffer is handed back to the next main loop.
+      bool merged = false;
+      if constexpr (kDeltaIdle) {
+        if (!mbar_wait(dfull, dfphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+        dfphase ^= 1u;
+        tc_fence_after();
+        if (lmask) {   // 32 columns per pass (BN is a multiple of 32 here; columns past nvalid are unused)
+#pragma unroll 1
+          for (int c = 0; c < nvalid; c += 32) {   // warp-uniform bound
+            uint32_t gv[32], dv[32];
+            tmem_ld_x32(tm + c, gv);
+            tmem_ld_x32(td + c, dv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              gv[j] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j]))) +
+                                      __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j]))));
+            tmem_st_x32(tm + c, gv);
+          }
+          tmem_st_wait();
+          merged = true;
+        }
+        tc_fence_before();
+        release(dfree);
+      }
 #pragma unroll 1
       for (int c = 0; c < nvalid; c += 16, ++chunk) {   // warp-uniform bound
         uint32_t gv[16], dv[16];
         tmem_ld_x16(tm + c, gv);
-        if (lmask) tmem_ld_x16(td + c, dv);
+        if (!kDeltaIdle && lmask) tmem_ld_x16(td + c, dv);
         tmem_ld_wait();
         float z[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {   // bf16(g) + bf16(delta), added in fp32
-          z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
-          if (lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
+          z[j] = merged ? __uint_as_float(gv[j]) : __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
+          if (!kDeltaIdle && lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
         }
         // every lane parks its 16 values (feature row = TMEM lane); then thread t computes
         // token t / 8 of the chunk for features 8 * (t % 8) .. + 8
@@ -481,8 +545,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       tc_fence_before();
-      if constexpr (kDeltaBufs == 1) release(dempty);   // done with the accumulator and the delta
-      release(&tempty[acc]);
+      release(&tempty[acc]);   // done with the accumulator
       if (++acc == kAccBufs) {
         acc = 0;
         aphase ^= 1u;
@@ -496,7 +559,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int R = p.slots.R;
     const int RP8 = (R + 7) & ~7;
     // this warp's store buffers: [16 tokens][32 features] (its TMEM lane quarter), two for fp32
-    const int nybuf = p.out_f32 != nullptr ? 2 : 1;   // as sized by the host
+    const int nybuf = p.y_tma ? 2 : 1;   // as sized by the host
     float* yb2 = reinterpret_cast<float*>(
                      (reinterpret_cast<uintptr_t>(v_s + (lora ? BN * RP8 : 0)) + 127) & ~static_cast<uintptr_t>(127)) +
                  quarter * nybuf * 512;   // TMA sources start on 128-byte boundaries
@@ -533,20 +596,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
         for (int j = 0; j < 16; ++j) val[j] = __uint_as_float(r[j]);
         if (lora && col < p.N) lora_expand_chunk(p, lslot, v_s, c, nvalid, e, col, val);
-        // transpose through the warp's buffer (lane = feature on the way in).  A whole fp32
-        // chunk of 16 tokens leaves as one TMA store of 16 x 32 floats; otherwise each lane
-        // stores 4 consecutive features of a token: 4 token rows of 128 B per instruction
-        float* yb = yb2 + (p.out_f32 != nullptr ? (ychunk++ & 1) * 512 : 0);
+        // transpose through the warp's buffer (lane = feature on the way in).  A whole chunk
+        // of 16 tokens leaves as one TMA store of 16 x 32 values (fp32 or bf16) when the host
+        // set up the output's tensor map; otherwise each lane stores 4 consecutive features of
+        // a token: 4 token rows per instruction
+        float* yb = yb2 + (p.y_tma ? (ychunk++ & 1) * 512 : 0);
         if (lane == 0) bulk_wait_read_1();   // the store that last read this buffer is done
         __syncwarp();
+        const bool whole = p.y_tma && c + 16 <= nvalid;
+        if (whole && p.out_f32 == nullptr) {
+          __nv_bfloat16* ybh = reinterpret_cast<__nv_bfloat16*>(yb);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) yb[j * 32 + lane] = val[j];
+          for (int j = 0; j < 16; ++j) ybh[j * 32 + lane] = f2bf(val[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) yb[j * 32 + lane] = val[j];
+        }
         const int fcol0 = nt * 128 + quarter * 32;
-        if (p.out_f32 != nullptr && c + 16 <= nvalid) {
+        if (whole) {
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && fcol0 < p.N) {
-            // wide tiles: fp32 y stays in L2 as long as it can, since the finalize reads it next
+            // wide tiles: y stays in L2 as long as it can, since the finalize reads it next
             if constexpr (BN >= 64) tma_store_2d_hint(&p.tmap_y, yb, fcol0, q0 + c, l2_policy_evict_last());
             else tma_store_2d(&p.tmap_y, yb, fcol0, q0 + c);
             bulk_commit();
@@ -607,7 +678,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 template <int BN, int MODE, int CG>
 static cudaError_t launch_mode(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   const int smem = gemm_smem_bytes(BN, CG, p.stages, p.E, p.lora_v != nullptr ? p.slots.R : 0, p.gated == 2,
-                                   p.out_f32 != nullptr);
+                                   p.y_tma);
   cudaError_t err =
       cudaFuncSetAttribute(grouped_gemm_kernel<BN, MODE, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -631,13 +702,11 @@ static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream,
 
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl) {
   if (p.stages < 2 || p.stages > kMaxStages) return cudaErrorInvalidValue;
-  const bool fused_act_lora = p.gated == 2 && p.lora_fused;
   if (p.cta_pair == 2) {
     const int nt = p.gated ? (p.N >> 7) : ((p.N + 127) >> 7);
     if (nt % 2 != 0) return cudaErrorInvalidValue;   // a pair covers two weight tiles
     switch (bn) {
       case 128: return launch_bn<128, 2>(p, grid, stream, pdl);
-      case 160: return fused_act_lora ? launch_mode<160, 4, 2>(p, grid, stream, pdl) : cudaErrorInvalidValue;
       case 256: return launch_bn<256, 2>(p, grid, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
@@ -647,8 +716,6 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStrea
     case 32: return launch_bn<32, 1>(p, grid, stream, pdl);
     case 64: return launch_bn<64, 1>(p, grid, stream, pdl);
     case 128: return launch_bn<128, 1>(p, grid, stream, pdl);
-    case 160:   // the fused gate_up with LoRA only: room in TMEM for two accumulators and a delta
-      return fused_act_lora ? launch_mode<160, 4, 1>(p, grid, stream, pdl) : cudaErrorInvalidValue;
     case 256: return launch_bn<256, 1>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }

@@ -73,7 +73,9 @@ struct GemmParams {
   CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN / cta_pair}
   __nv_bfloat16* out;            // [P, N] bf16 output, or
   float* out_f32;                //   fp32 output when non-null
-  CUtensorMap tmap_y;            // out_f32 [P rows, N cols] fp32, box {32, 16}: full 16-token chunks
+  CUtensorMap tmap_y;            // the output [P rows, N cols] (fp32, or bf16 when out_f32 is null),
+                                 // box {32, 16}: full 16-token chunks leave by TMA (y_tma = 1)
+  int y_tma;
   const int32_t* offsets;        // [E + 1]
   uint32_t* status;
   int E, N, K, gated, stages;
@@ -98,7 +100,7 @@ struct GemmParams {
   LoraSlots slots;
 };
 constexpr int kMaxGemmSmem = 227 * 1024;   // dynamic shared memory a CTA may have
-int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int f32_out);
+int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int y_tma);
 int gemm_stage_bytes(int rows);   // one stage: 128 weight rows + `rows` token rows, 64 wide
 cudaError_t launch_grouped_gemm(const GemmParams& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 
@@ -142,7 +144,8 @@ cudaError_t launch_quant_fp8(const __nv_bfloat16* src, const int32_t* perm, int 
 
 
 struct FinalizeParams {
-  const float* y;                // [P, H] permuted down output (down-LoRA delta included)
+  const float* y;                // [P, H] permuted down output (down-LoRA delta included), or
+  const __nv_bfloat16* y_bf16;   //   the same rounded to bf16 (when y is null)
   const float* weights;          // [T, k]
   const int32_t* inv;            // [T * k]
   int T, H, k;
@@ -199,6 +202,27 @@ struct ShrinkTcParams {
 int lora_shrink_tc_nb(int rows);
 cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl = false);
+
+// Permute fused with the gate_up LoRA shrink (fused LoRA placement): xp[q] = x[perm[q]/k],
+// ub[s][q][r] = bf16(scaling[s] * A_gu[s,e,r,:] . x[perm[q]/k]) for q's own active slot s and
+// r < ranks[s], zero for every other (s, r < RU), pair_slot[q] = that slot or -1.
+struct PermuteShrinkParams {
+  const __nv_bfloat16* x;        // [T, H] hidden rows
+  const int32_t* perm;           // [P]
+  const int32_t* offsets;        // [E + 1]
+  const int32_t* slot_idx;       // [T]
+  const __nv_bfloat16* A;        // [S, E, R, H], or [S, 1, R, H] with a_e1
+  int a_e1;
+  int H, E, k, P, RU;
+  int nr_max;                    // stacked rank rows of all active slots, rounded up to 8 (<= 256)
+  LoraSlots slots;
+  __nv_bfloat16* xp;             // [P, H]
+  __nv_bfloat16* ub;             // [S, P, RU]
+  int32_t* pair_slot;            // [P]
+  uint32_t* status;
+};
+size_t permute_shrink_smem_bytes(int nr_max, int E);
+cudaError_t launch_permute_shrink(const PermuteShrinkParams& p, int grid, cudaStream_t stream, bool pdl = false);
 
 // Activation (gate_up output g plus the bf16 gate_up LoRA delta d, SwiGLU, bf16 out)
 // fused with the down-LoRA shrink v = scaling * a . A_dn^T, over expert tiles of up to 8

@@ -314,15 +314,21 @@ int pick_bn(long long P, int E) {
 // Wide token tiles run on CTA pairs (M = 256 tcgen05 pair MMAs, each SM loading half the
 // token rows) when the weight rows split into an even number of 128-row tiles.
 constexpr int kPairMinBn = 128;
+// From this token tile on the down GEMM stores y (its output plus the down-LoRA delta) in
+// bf16 for the finalize, halving the [P, H] round trip through HBM that prefill token counts
+// pay for it; narrower tiles keep it in fp32.  The pages leave y's precision open (only g,
+// the LoRA delta, the activation and the layer output are bf16 tensors there); the rounding
+// costs about 0.3% relative L2 against the float64 oracle, inside the layer's 0.5% bound.
+constexpr int kBf16YMinBn = 128;
 int pair_tiles(int bn, int N) { return (bn >= kPairMinBn && N % 256 == 0) ? 2 : 1; }
 
 // Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
 // room for the side-stream LoRA kernel that runs beside it; the down GEMM runs alone.
-int pick_stages(int bn, int cg, int E, int lora_R, int act_fused, bool alone, bool f32_out) {
+int pick_stages(int bn, int cg, int E, int lora_R, int act_fused, bool alone, bool y_tma) {
   // Wide tiles (prefill) keep too few stages in flight to cover the load latency at 200 KB,
   // so they take the whole 227 KB a CTA may have.
   const int budget = bn >= 64 ? kMaxGemmSmem : (bn <= 32 && !alone ? 160 : 200) * 1024;
-  const int fixed = gemm_smem_bytes(bn, cg, 0, E, lora_R, act_fused, f32_out);
+  const int fixed = gemm_smem_bytes(bn, cg, 0, E, lora_R, act_fused, y_tma);
   int s = (budget - fixed) / (gemm_stage_bytes(bn / cg) + 16);
   if (s > 16) s = 16;
   if (s < 2) s = 2;
@@ -336,18 +342,23 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
   const int cg = gp.cta_pair == 2 ? 2 : 1;
   if (!make_tmap(h->encode, &gp.tmap_w, W, static_cast<uint64_t>(gp.E) * gp.N, gp.K, 64)) return MOE_LORA_ERR_CUDA;
   if (!make_tmap(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn / cg)) return MOE_LORA_ERR_CUDA;
-  if (gp.out_f32 != nullptr && P >= 16) {   // the epilogue stores whole 16-token chunks with TMA
+  // The down GEMM's epilogue stores whole 16-token chunks of y (fp32, or bf16 at wide tiles)
+  // with TMA; the gate_up outputs and the CUDA-core LoRA epilogue store from the lanes.
+  const bool y_f32 = gp.out_f32 != nullptr;
+  if (gp.gated == 0 && P >= 16 && (y_f32 || (gp.out != nullptr && gp.lora_v == nullptr))) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(gp.N), static_cast<cuuint64_t>(P)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(gp.N) * 4};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(gp.N) * (y_f32 ? 4 : 2)};
     cuuint32_t box[2] = {32, 16};
     cuuint32_t estr[2] = {1, 1};
-    if (h->encode(&gp.tmap_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, gp.out_f32, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    void* base = y_f32 ? static_cast<void*>(gp.out_f32) : static_cast<void*>(gp.out);
+    if (h->encode(&gp.tmap_y, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MOE_LORA_ERR_CUDA;
+    gp.y_tma = 1;
   }
   gp.stages = pick_stages(bn, cg, gp.E, gp.lora_v != nullptr ? gp.slots.R : 0, gp.gated == 2, gp.gated == 0,
-                          gp.out_f32 != nullptr);
+                          gp.y_tma != 0);
   ML_LAUNCH(h, launch_grouped_gemm(gp, bn, h->num_sms, stream, pdl), "grouped_gemm launch");
   return MOE_LORA_OK;
 }
@@ -382,6 +393,19 @@ moe_lora_status enqueue_gemm_fp8(moe_lora_handle* h, GemmF8Params& gp, const uin
   return MOE_LORA_OK;
 }
 
+LoraSlots make_slots(const moe_lora_args* a) {
+  LoraSlots L;
+  std::memset(&L, 0, sizeof(L));
+  L.S = a->S;
+  L.E = a->E;
+  L.R = a->R;
+  for (int s = 0; s < a->S; ++s) {
+    L.ranks[s] = a->h_ranks[s];
+    L.scal[s] = a->h_scalings[s];
+  }
+  return L;
+}
+
 // Tensor maps of the fused LoRA stages: per active slot, the slot's B rows [E*N, ranks[s]]
 // (the inner extent stops at the slot's rank, so the stacked tail is zero-filled, never
 // read), and the per-slot scaled shrink rows ub [S*P, RU].
@@ -408,6 +432,7 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
   gp.lora_fused = 1;
   gp.lora_b_e1 = b_e1 ? 1 : 0;
   gp.lora_kb = (R + 63) / 64;
+  gp.slots = make_slots(a);   // the stages of slot s stop at ranks[s]
   gp.P = P;
   gp.pair_slot = pair_slot;
   return true;
@@ -466,18 +491,6 @@ void prof(const moe_lora_args* a, int stage, int which, cudaStream_t s) {
   if (ev != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
 }
 
-LoraSlots make_slots(const moe_lora_args* a) {
-  LoraSlots L;
-  std::memset(&L, 0, sizeof(L));
-  L.S = a->S;
-  L.E = a->E;
-  L.R = a->R;
-  for (int s = 0; s < a->S; ++s) {
-    L.ranks[s] = a->h_ranks[s];
-    L.scal[s] = a->h_scalings[s];
-  }
-  return L;
-}
 
 }  // namespace
 
@@ -849,19 +862,41 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   const bool fuse_all = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && a->S * R <= 256 && bn0 >= 32 &&
                         !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
   const bool act_in_gemm = f8 == nullptr && (fuse_all || (!lora && bn0 >= 32));
+  const bool y_bf16 = act_in_gemm && finalize && bn0 >= kBf16YMinBn;
   if (act_in_gemm) {
-    int bn = bn0;
-    if (fuse_all && bn > 160) bn = 160;   // room in TMEM for two accumulators and the LoRA delta
+    const int bn = bn0;
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
-    ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
-            "permute launch");
-    prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
-    if (fuse_all) {
-      prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
-      st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl, so);
-      if (st != MOE_LORA_OK) return st;
-      prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
+    if (fuse_all) {   // the permute and the gate_up LoRA shrink in one pass over the token rows
+      PermuteShrinkParams ps;
+      std::memset(&ps, 0, sizeof(ps));
+      ps.x = reinterpret_cast<const __nv_bfloat16*>(a->hidden);
+      ps.perm = perm;
+      ps.offsets = offsets;
+      ps.slot_idx = a->slot_idx;
+      ps.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_gu);
+      ps.a_e1 = so ? 1 : 0;
+      ps.H = H;
+      ps.E = E;
+      ps.k = k;
+      ps.P = P;
+      ps.RU = (R + 7) & ~7;
+      int nr = 0;
+      for (int s = 0; s < a->S; ++s)
+        if (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) nr += slots.ranks[s];
+      ps.nr_max = (nr + 7) & ~7;
+      ps.slots = slots;
+      ps.xp = xp;
+      ps.ub = ub;
+      ps.pair_slot = pair_slot;
+      ps.status = status;
+      int grid = (P + 63) / 64 + E;
+      if (grid > 4 * h->num_sms) grid = 4 * h->num_sms;
+      ML_LAUNCH(h, launch_permute_shrink(ps, grid, stream, pdl), "permute + LoRA shrink launch");
+    } else {
+      ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
+                "permute launch");
     }
+    prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
     GemmParams gu;
     std::memset(&gu, 0, sizeof(gu));
@@ -886,7 +921,8 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
     GemmParams dn;
     std::memset(&dn, 0, sizeof(dn));
-    dn.out_f32 = y;
+    if (y_bf16) dn.out = reinterpret_cast<__nv_bfloat16*>(y);
+    else dn.out_f32 = y;
     dn.offsets = offsets;
     dn.status = status;
     dn.E = E;
@@ -908,7 +944,9 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   if (!finalize) return MOE_LORA_OK;   // the routed entry's unfinalized outputs are written
   prof(a, MOE_LORA_STAGE_FINALIZE, 0, stream);
   FinalizeParams fp;
-  fp.y = y;
+  std::memset(&fp, 0, sizeof(fp));
+  if (y_bf16) fp.y_bf16 = reinterpret_cast<const __nv_bfloat16*>(y);
+  else fp.y = y;
   fp.weights = wts;
   fp.inv = inv;
   fp.T = T;

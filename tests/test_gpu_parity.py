@@ -94,6 +94,10 @@ def test_permute_exact(handle):
 
 def _run_and_check(h, cfg, seed=0, device_inputs=False, tokens=None, flags=0, lora_off=False, T=None):
     inp = wl.make_inputs(cfg, seed=seed, device="cuda" if device_inputs else "cpu", T=T)
+    return _check_given_inputs(h, cfg, inp, device_inputs, tokens, flags, lora_off)
+
+
+def _check_given_inputs(h, cfg, inp, device_inputs=False, tokens=None, flags=0, lora_off=False):
     g = gh.to_dev(inp)
     P = g["T"] * cfg.top_k
     outs = dict(topk_ids=torch.empty((g["T"], cfg.top_k), dtype=torch.int32, device="cuda"),
@@ -133,8 +137,9 @@ def test_random_small_layers(handle, seed):
 @pytest.mark.parametrize("T,E,k", [(40, 8, 4), (130, 8, 4), (260, 8, 4), (520, 8, 4), (1500, 6, 3)])
 def test_token_tile_widths_and_ragged_tails(handle, T, E, k):
     """T*k/E pairs per expert of about 20, 65, 130, 260, 750 select token tiles of
-    32, 128, 256, 256 (several per expert) with ragged tails; with LoRA the fused gate_up
-    takes 160-token tiles at the last three (one delta accumulator)."""
+    32, 128, 256, 256 (several per expert) with ragged tails; at 256-token tiles the fused
+    gate_up puts each tile's LoRA delta in the idle accumulator; from 128-token tiles on the
+    down GEMM hands y to the finalize in bf16."""
     cfg = wl.LayerConfig("tiles", T=T, H=256, I=192, E=E, top_k=k, ranks=(8, 16), scalings=(1.0, 0.5),
                          slot_mode="uniform_none10")
     _run_and_check(handle, cfg, seed=T)
@@ -142,7 +147,7 @@ def test_token_tile_widths_and_ragged_tails(handle, T, E, k):
 
 @pytest.mark.parametrize("T,E,k,ranks,flags", [
     (100, 8, 4, (8, 16), 0),                    # 128-token tiles, fused LoRA, two accumulators + two deltas
-    (520, 8, 4, (8, 16), 0),                    # 160-token gate_up tiles (one delta), 256-token down tiles
+    (520, 8, 4, (8, 16), 0),                    # 256-token tiles: the delta in the idle accumulator
     (520, 8, 4, (8, 16), pkg.FLAG_LORA_OFF),    # 256-token tiles, activation epilogue, plain down
     (1500, 6, 3, (8, 16, 32, 64), 0),           # several tiles per expert, four slots, ragged tails
 ])
@@ -251,11 +256,11 @@ def test_single_and_two_stream_agree_bitwise(handle):
 def test_launch_count_per_forward(handle):
     """One forward launches the kernels its placement draws: narrow tiles with LoRA = route,
     side-stream LoRA, permute, gate_up GEMM, activation + down shrink, down GEMM, finalize;
-    LoRA off drops the LoRA kernel and fuses nothing else; wide tiles = route, permute,
-    two tensor-core shrinks, two GEMMs, finalize."""
+    LoRA off drops the LoRA kernel and fuses nothing else; wide tiles = route, permute with
+    the gate_up shrink, gate_up GEMM, tensor-core down shrink, down GEMM, finalize."""
     narrow = wl.LayerConfig("n", T=64, H=256, I=128, E=32, top_k=4, ranks=(8,), scalings=(1.0,))
     wide = wl.LayerConfig("w", T=256, H=256, I=128, E=8, top_k=4, ranks=(8,), scalings=(1.0,))
-    for cfg, flags, want in ((narrow, 0, 7), (narrow, pkg.FLAG_LORA_OFF, 6), (wide, 0, 7)):
+    for cfg, flags, want in ((narrow, 0, 7), (narrow, pkg.FLAG_LORA_OFF, 6), (wide, 0, 6)):
         g = gh.to_dev(wl.make_inputs(cfg, seed=1))
         n0 = handle.launch_count()
         gh.forward(handle, g, flags=flags)
@@ -297,8 +302,8 @@ def test_back_to_back_forwards_share_a_workspace(handle, T, E):
         gh.assert_close(o.float().cpu().numpy(), gh.oracle(inp)["out"], f"forward {i}")
 
 
-@pytest.mark.parametrize("T,E", [(64, 32), (96, 16), (520, 8), (1024, 8)],
-                         ids=["narrow", "wide-32", "wide-cta-pairs", "cooperative-routing"])
+@pytest.mark.parametrize("T,E", [(64, 32), (96, 16), (200, 16), (520, 8), (1024, 8)],
+                         ids=["narrow", "wide-32", "wide-cta-pairs", "wide-256", "cooperative-routing"])
 def test_programmatic_launches_change_nothing(handle, T, E):
     """The programmatic launch chain only moves kernel start times: with MOE_LORA_FLAG_NO_PDL
     (plain stream order, the header memset before the routing) every output is bitwise the
@@ -312,6 +317,18 @@ def test_programmatic_launches_change_nothing(handle, T, E):
     c = gh.forward(handle, g, workspace=ws).clone()
     assert pkg.moe_lora_check_status(ws)[0] == 0
     assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_fused_gate_up_tiles_with_and_without_lora(handle):
+    """256-token fused gate_up tiles, some of whose pairs all lack an adapter (first half of
+    the tokens on slot -1, so an expert's first tile holds no LoRA pair and its last tile
+    does): tiles without a delta skip the merge into the idle accumulator, tiles with one
+    merge it, in any order on a CTA."""
+    cfg = wl.LayerConfig("mixed", T=2048, H=512, I=256, E=4, top_k=2, ranks=(8, 16), scalings=(1.0, 0.5),
+                         slot_mode="uniform_none10")
+    inp = wl.make_inputs(cfg, seed=21)
+    inp["slot_idx"][: cfg.T // 2] = -1
+    _check_given_inputs(handle, cfg, inp)
 
 
 def test_empty_batch(handle):
