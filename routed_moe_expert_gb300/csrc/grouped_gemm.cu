@@ -130,9 +130,9 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
 // TMEM (512 columns): two accumulators of BN columns, and in MODE 4 up to BN = 128 two delta
 // accumulators after them.  At wider tiles MODE 4 has no room for a delta buffer, so tile i's
 // LoRA stages go into the idle accumulator (the one tile i+1 will use) once tile i-1's
-// activation has left it: the epilogue first merges bf16(g) + bf16(delta) back into tile i's
-// accumulator (tcgen05.st) and hands the idle buffer back (`dfree`), then forms the
-// activation.  The main loop of tile i+1 waits only for that merge, a short pass over TMEM.
+// activation has left it; they sit in the middle of tile i's main loop, and as soon as they
+// are done (`dfull`) the epilogue copies the delta, rounded to bf16, into registers and hands
+// the idle buffer back (`dfree`) while tile i's last main stages still run.
 //
 // CG = 2: clusters of two CTAs (one TPC) share each tile as an M = 256 tcgen05 pair MMA.
 // A tile is then two consecutive 128-row weight tiles (the even CTA's, then the odd CTA's)
@@ -449,11 +449,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
               first_delta = false;
             }
           }
+          // the delta is complete before the tile's last main stages: the epilogue can take it
+          // out of the idle buffer while they run (every tile, LoRA or not)
+          if constexpr (kDeltaIdle) {
+            if (ok) commit_all(dfull);
+          }
         }
         for (int kb = kb_lora; ok && kb < KB; ++kb) ok = consume(d, false);
         if (!ok) break;
         commit_all(&tfull[acc]);   // both CTAs' epilogues
-        if constexpr (kDeltaIdle) commit_all(dfull);   // every tile, LoRA or not
         if (++acc == kAccBufs) {
           acc = 0;
           aphase ^= 1u;
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int quarter = warp & 3;
     const int I = p.N >> 1;
     float* xchg = reinterpret_cast<float*>(lslot);   // [2][64][kXchgStride]
-    int acc = 0, chunk = 0;
+    int acc = 0, chunk = 0;   // chunk: the xchg buffer alternates per 16-token chunk
     uint32_t aphase = 0, dfphase = 0;
     for (int tile = cta0; tile < total; tile += ncta) {
       int e, nt, qt;
@@ -480,53 +484,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
         lmask = __reduce_or_sync(0xffffffffu, lmask);
       }
-      if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
-      tc_fence_after();
       const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tm = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
       const uint32_t td = tmem_base + lane_base +
                           static_cast<uint32_t>(kDeltaIdle ? (acc ^ 1) * BN : kAccBufs * BN + acc * BN);
-      // With the delta in the idle accumulator: z = bf16(g) + bf16(delta) goes back into this
-      // tile's accumulator first, and the idle buffer is handed back to the next main loop.
-      bool merged = false;
-      if constexpr (kDeltaIdle) {
-        if (!mbar_wait(dfull, dfphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
-        dfphase ^= 1u;
-        tc_fence_after();
-        if (lmask) {   // 32 columns per pass (BN is a multiple of 32 here; columns past nvalid are unused)
-#pragma unroll 1
-          for (int c = 0; c < nvalid; c += 32) {   // warp-uniform bound
-            uint32_t gv[32], dv[32];
-            tmem_ld_x32(tm + c, gv);
-            tmem_ld_x32(td + c, dv);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              gv[j] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j]))) +
-                                      __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j]))));
-            tmem_st_x32(tm + c, gv);
-          }
-          tmem_st_wait();
-          merged = true;
-        }
-        tc_fence_before();
-        release(dfree);
-      }
-#pragma unroll 1
-      for (int c = 0; c < nvalid; c += 16, ++chunk) {   // warp-uniform bound
-        uint32_t gv[16], dv[16];
-        tmem_ld_x16(tm + c, gv);
-        if (!kDeltaIdle && lmask) tmem_ld_x16(td + c, dv);
-        tmem_ld_wait();
-        float z[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {   // bf16(g) + bf16(delta), added in fp32
-          z[j] = merged ? __uint_as_float(gv[j]) : __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
-          if (!kDeltaIdle && lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
-        }
-        // every lane parks its 16 values (feature row = TMEM lane); then thread t computes
-        // token t / 8 of the chunk for features 8 * (t % 8) .. + 8
+      // One 16-token chunk of z = bf16(g) + bf16(delta): every lane parks its 16 values
+      // (feature row = TMEM lane); then thread t computes token t / 8 of the chunk for
+      // features 8 * (t % 8) .. + 8 and writes them in one 16-byte store.
+      auto act_chunk = [&](int c, const float (&z)[16]) {
         float* buf = xchg + (chunk & 1) * 128 * kXchgStride;
+        ++chunk;
         float* mine = buf + (quarter * 32 + lane) * kXchgStride;
 #pragma unroll
         for (int j = 0; j < 16; ++j) mine[j] = z[j];
@@ -542,6 +509,67 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             out8[i] = __fdividef(zg, 1.0f + __expf(-zg)) * zu;
           }
           *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(q0 + c + tok) * I + nt * 64 + f8) = pack8(out8);
+        }
+      };
+      if constexpr (kDeltaIdle) {
+        // The delta of this tile leaves the idle accumulator as soon as its MMAs are done (in
+        // the middle of the tile's main loop): rounded to bf16 and held in registers as pairs,
+        // so the buffer goes back to the next tile's main loop at once.
+        uint32_t dpk[BN / 2];
+        if (!mbar_wait(dfull, dfphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+        dfphase ^= 1u;
+        tc_fence_after();
+        if (lmask) {
+#pragma unroll
+          for (int cc = 0; cc < BN / 32; ++cc) {
+            uint32_t t[32];
+            tmem_ld_x32(td + 32 * cc, t);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(t[2 * j]), __uint_as_float(t[2 * j + 1]));
+              dpk[16 * cc + j] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+          }
+        }
+        tc_fence_before();
+        release(dfree);
+        if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cu = 0; cu < BN / 16; ++cu) {   // unrolled: dpk is indexed statically
+          const int c = cu * 16;
+          if (c >= nvalid) break;                 // warp-uniform
+          uint32_t gv[16];
+          tmem_ld_x16(tm + c, gv);
+          tmem_ld_wait();
+          float z[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {   // bf16(g) + bf16(delta), added in fp32
+            z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
+            if (lmask) {
+              const uint32_t dw = dpk[8 * cu + (j >> 1)];
+              z[j] += __uint_as_float((j & 1) ? (dw & 0xffff0000u) : (dw << 16));
+            }
+          }
+          act_chunk(c, z);
+        }
+      } else {
+        if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
+          uint32_t gv[16], dv[16];
+          tmem_ld_x16(tm + c, gv);
+          if (lmask) tmem_ld_x16(td + c, dv);
+          tmem_ld_wait();
+          float z[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {   // bf16(g) + bf16(delta), added in fp32
+            z[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[j])));
+            if (lmask) z[j] += __bfloat162float(__float2bfloat16_rn(__uint_as_float(dv[j])));
+          }
+          act_chunk(c, z);
         }
       }
       tc_fence_before();
