@@ -332,6 +332,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) grouped_gemm_fp8_kernel(const _
           break;
         }
         tc_fence_after();
+        __syncwarp();   // the lanes left the barrier wait one by one: tcgen05.ld is .aligned
         uint32_t r[BN / 16][16];
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c)

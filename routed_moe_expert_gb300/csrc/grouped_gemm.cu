@@ -541,6 +541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const int c = cu * 16;
           if (c >= nvalid) break;                 // warp-uniform
           uint32_t gv[16];
+          __syncwarp();   // the last chunk's stores branched per lane; tcgen05.ld is .aligned
           tmem_ld_x16(tm + c, gv);
           tmem_ld_wait();
           float z[16];
@@ -560,6 +561,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll 1
         for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
           uint32_t gv[16], dv[16];
+          __syncwarp();   // the last chunk's stores branched per lane; tcgen05.ld is .aligned
           tmem_ld_x16(tm + c, gv);
           if (lmask) tmem_ld_x16(td + c, dv);
           tmem_ld_wait();
@@ -618,6 +620,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll 1
       for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
         uint32_t r[16];
+        __syncwarp();   // the last chunk's stores branched per lane; tcgen05.ld is .aligned
         tmem_ld_x16(taddr + c, r);
         tmem_ld_wait();
         float val[16];

@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
 #pragma unroll 1
       for (int c = 0; c < ncol; c += 16) {   // tcgen05.ld is warp-wide: same columns in every lane
         uint32_t v[16];
+        __syncwarp();   // after the per-lane wait and stores: tcgen05.ld is .aligned
         tmem_ld_x16(taddr + c, v);
         tmem_ld_wait();
         if (valid) {

@@ -16,8 +16,8 @@
 // A CTA tile is up to 64 consecutive permuted pairs of one expert; the rank rows of every
 // slot present among them are stacked as the N side of mma.sync m16n8k16 (M = the pairs, K = H
 // in 64-wide chunks).  Chunks of the token rows and adapter rows move by cp.async through a
-// 4-deep ring (16-byte pieces, 128-byte rows with the 16-byte chunk index XORed with the row
-// index, so ldmatrix reads them without bank conflicts).
+// ring of 4 or 8 stages (16-byte pieces, 128-byte rows with the 16-byte chunk index XORed with
+// the row index, so ldmatrix reads them without bank conflicts).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -25,11 +25,12 @@ namespace mlk {
 
 constexpr int kPsThreads = 256;
 constexpr int kPsTile = 64;     // pairs per tile
-constexpr int kPsStages = 4;
+constexpr int kPsMaxStages = 8;
 constexpr int kPsMaxRows = 256; // stacked rank rows per tile (S * R <= 256 on the fused path)
 
-MLDEV void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+MLDEV void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
 }
 MLDEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -53,15 +54,24 @@ MLDEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[
 // byte offset of 16-byte piece c of row r in a tile of 128-byte rows
 MLDEV uint32_t sw_off(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
 
+// The ring is as deep as fits 200 KB (at most 8 stages, at least 4): the adapter rows of a tile
+// stream from HBM chunk by chunk, so the bytes in flight set its speed.
+int permute_shrink_stages(int nr_max) {
+  const int stage = (kPsTile + ((nr_max + 7) & ~7)) * 128;
+  return 8 * stage <= 200 * 1024 ? 8 : 4;
+}
+
 size_t permute_shrink_smem_bytes(int nr_max, int E) {
   const int nr = (nr_max + 7) & ~7;
-  return 128 + static_cast<size_t>(kPsStages) * (kPsTile + nr) * 128 + kPsTile * 8 + nr * 8 +
+  return 128 + static_cast<size_t>(permute_shrink_stages(nr_max)) * (kPsTile + nr) * 128 + kPsTile * 8 + nr * 8 +
          4 * (4 + kMaxFusedSlots) + 8 * (static_cast<size_t>(E) + 1);
 }
 
-// NT8: n8 tiles of stacked rank rows each warp covers (two warps per 16-pair m-tile).
-template <int NT8>
+// NT8: n8 tiles of stacked rank rows each warp covers (two warps per 16-pair m-tile);
+// NS: depth of the cp.async ring.
+template <int NT8, int NS>
 __global__ void __launch_bounds__(kPsThreads) permute_shrink_kernel(const PermuteShrinkParams p) {
+  constexpr int kPsStages = NS;
   extern __shared__ __align__(128) uint8_t ps_smem[];
   uint8_t* smem = ps_smem + ((128u - (smem_u32(ps_smem) & 127u)) & 127u);
   const int NRMAX = p.nr_max;                               // stacked rows the stages hold (multiple of 8)
@@ -79,6 +89,13 @@ __global__ void __launch_bounds__(kPsThreads) permute_shrink_kernel(const Permut
   const int R = p.slots.R;
   const int Ea = p.a_e1 ? 1 : E;
 
+  // The hidden rows are read k times (once per pair of the token): keep them in L2.  The
+  // permuted rows are written once here and read next by the gate_up GEMM from HBM anyway:
+  // stream them, so they do not push the hidden rows out of L2.
+  const uint64_t pol_keep = l2_policy_evict_last();
+  const uint64_t pol_stream = l2_policy_evict_first();
+  uint64_t pol_normal;   // the adapter rows: reused across an expert's tiles, or read once
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol_normal));
   pdl_wait();    // the routing (perm, offsets) comes from the previous kernel
   pdl_trigger();
   if (warp == 0) build_tile_schedule(p.offsets, E, kPsTile, 1, seg, tile_start);
@@ -137,11 +154,11 @@ __global__ void __launch_bounds__(kPsThreads) permute_shrink_kernel(const Permut
       const uint32_t sa = sx + kPsTile * 128;
       for (int i = tid; i < np * 8; i += kPsThreads) {
         const int r = i >> 3, c = i & 7;
-        cp_async16(sx + sw_off(r, c), p.x + static_cast<size_t>(prow[r]) * H + kc * 64 + c * 8);
+        cp_async16(sx + sw_off(r, c), p.x + static_cast<size_t>(prow[r]) * H + kc * 64 + c * 8, pol_keep);
       }
       for (int i = tid; i < nr * 8; i += kPsThreads) {
         const int r = i >> 3, c = i & 7;
-        cp_async16(sa + sw_off(r, c), p.A + arow[r] + kc * 64 + c * 8);
+        cp_async16(sa + sw_off(r, c), p.A + arow[r] + kc * 64 + c * 8, pol_normal);
       }
     };
     // warp w: m-tile (w & 3) of 16 pairs, n8 tiles [(w >> 2) * NT8, +NT8) of the stacked rows
@@ -164,7 +181,7 @@ __global__ void __launch_bounds__(kPsThreads) permute_shrink_kernel(const Permut
       for (int i = tid; i < np * 8; i += kPsThreads) {
         const int r = i >> 3, c = i & 7;
         const uint4 v = *reinterpret_cast<const uint4*>(st + sw_off(r, c));
-        *reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(q0 + r) * H + kc * 64 + c * 8) = v;
+        st_global_v4_hint(p.xp + static_cast<size_t>(q0 + r) * H + kc * 64 + c * 8, v, pol_stream);
       }
       if (nr > 0 && mt * 16 < np) {
         const uint32_t sx = smem_u32(st), sa = sx + kPsTile * 128;
@@ -237,16 +254,17 @@ cudaError_t launch_permute_shrink(const PermuteShrinkParams& p, int grid, cudaSt
     return cudaErrorInvalidValue;
   const int smem = static_cast<int>(permute_shrink_smem_bytes(p.nr_max, p.E));
   const int n8 = p.nr_max / 8;   // two warps share an m-tile: each covers half the n8 tiles
+  const bool deep = permute_shrink_stages(p.nr_max) == 8;
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     return launch_k(kern, dim3(grid), dim3(kPsThreads), static_cast<size_t>(smem), stream, pdl, p);
   };
-  if (n8 <= 2) return go(permute_shrink_kernel<1>);
-  if (n8 <= 4) return go(permute_shrink_kernel<2>);
-  if (n8 <= 8) return go(permute_shrink_kernel<4>);
-  if (n8 <= 16) return go(permute_shrink_kernel<8>);
-  return go(permute_shrink_kernel<16>);
+  if (n8 <= 2) return deep ? go(permute_shrink_kernel<1, 8>) : go(permute_shrink_kernel<1, 4>);
+  if (n8 <= 4) return deep ? go(permute_shrink_kernel<2, 8>) : go(permute_shrink_kernel<2, 4>);
+  if (n8 <= 8) return deep ? go(permute_shrink_kernel<4, 8>) : go(permute_shrink_kernel<4, 4>);
+  if (n8 <= 16) return deep ? go(permute_shrink_kernel<8, 8>) : go(permute_shrink_kernel<8, 4>);
+  return deep ? go(permute_shrink_kernel<16, 8>) : go(permute_shrink_kernel<16, 4>);
 }
 
 }  // namespace mlk
