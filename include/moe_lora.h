@@ -264,6 +264,20 @@ moe_lora_status moe_lora_forward_fp8(moe_lora_handle* h, const moe_lora_args* a,
 moe_lora_status moe_lora_quant_fp8(moe_lora_handle* h, const moe_lora_bf16* src, const int32_t* perm, int rows,
                                    int K, int top_k, uint8_t* codes, float* scales, moe_lora_stream stream);
 
+/* The FP8 grouped GEMM of moe_lora_forward_fp8 on its own (its down GEMM: fp32 output, no
+   LoRA): for every expert e and its rows q in [expert_offsets[e], expert_offsets[e+1]),
+     out[q, n] = sum over 128-wide K blocks b of  x_scale[b * P + q] * w_scale[e, n/128, b]
+                 * sum_{k in b} e4m3(x[q, k]) * e4m3(w[e*N + n, k])
+   (the block-scaled product of FP8 block-quantised checkpoints, sglang PR #28466 summary;
+   the tensor cores sum each 128-wide block of e4m3 products, the scales are applied in fp32).
+   w [E, N, K] and x [P, K] are e4m3 codes (16-byte aligned), w_scale [E, N/128, K/128] and
+   x_scale [K/128, P] float32, expert_offsets [E + 1] int32 (non-decreasing, offsets[E] = P),
+   out [P, N] float32 (16-byte aligned).  N and K multiples of 128, P >= 0.  Rows of no
+   expert are not written.  Errors: INVALID_ARG, CUDA. */
+moe_lora_status moe_lora_grouped_gemm_fp8(moe_lora_handle* h, const uint8_t* w, const float* w_scale,
+                                          const uint8_t* x, const float* x_scale, const int32_t* expert_offsets,
+                                          int E, int N, int K, int P, float* out, moe_lora_stream stream);
+
 /* Routing + expert alignment that allocates nothing and takes no workspace or handle.
    The pages have no counterpart to this call; it exists for callers that cannot call
    cudaMalloc or supply a workspace (plug-ins inside a host framework that owns all device

@@ -35,7 +35,7 @@ NUM_STAGES = len(STAGES)
 EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
             "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed",
-            "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8"]
+            "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8", "moe_lora_grouped_gemm_fp8"]
 
 
 class MoELoRAError(RuntimeError):
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
     L.moe_lora_forward_fp8.argtypes = [c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Fp8Weights), c_void_p,
                                        c_void_p, c_size_t, c_void_p]
     L.moe_lora_quant_fp8.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
+    L.moe_lora_grouped_gemm_fp8.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                            c_int, c_int, c_void_p, c_void_p]
     for name in EXPORTED:
         if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
             getattr(L, name).restype = c_int
@@ -445,6 +447,28 @@ def moe_lora_quant_fp8(handle: Handle, src: torch.Tensor, perm: Optional[torch.T
                                   _stream(stream))
     _check(st, "moe_lora_quant_fp8")
     return codes, scales
+
+
+def moe_lora_grouped_gemm_fp8(handle: Handle, w_q: torch.Tensor, w_scale: torch.Tensor, x_q: torch.Tensor,
+                              x_scale: torch.Tensor, expert_offsets: torch.Tensor, stream=None) -> torch.Tensor:
+    """The FP8 block-scaled grouped GEMM on its own: w_q [E, N, K] and x_q [P, K] e4m3 codes
+    (uint8), w_scale [E, N/128, K/128] and x_scale [K/128, P] float32, expert_offsets [E + 1]
+    int32.  Returns out [P, N] float32 (rows outside every expert's range are left as zero)."""
+    if w_q.dim() != 3 or x_q.dim() != 2:
+        raise ValueError("w_q must be [E, N, K] and x_q [P, K]")
+    E, N, K = w_q.shape
+    P = x_q.shape[0]
+    for t, shape, name in ((x_q, (P, K), "x_q"), (w_scale, (E, N // 128, K // 128), "w_scale"),
+                           (x_scale, (K // 128, P), "x_scale"), (expert_offsets, (E + 1,), "expert_offsets")):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    out = torch.zeros((P, N), dtype=torch.float32, device=w_q.device)
+    st = lib().moe_lora_grouped_gemm_fp8(handle.ptr, _ptr(w_q, torch.uint8, "w_q"), _ptr(w_scale, torch.float32, "w_scale"),
+                                         _ptr(x_q, torch.uint8, "x_q"), _ptr(x_scale, torch.float32, "x_scale"),
+                                         _ptr(expert_offsets, torch.int32, "expert_offsets"), E, N, K, P,
+                                         _ptr(out, torch.float32, "out"), _stream(stream))
+    _check(st, "moe_lora_grouped_gemm_fp8")
+    return out
 
 
 def moe_lora_validate(**kwargs) -> int:

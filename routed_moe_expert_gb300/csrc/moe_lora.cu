@@ -1044,6 +1044,30 @@ moe_lora_status moe_lora_quant_fp8(moe_lora_handle* h, const moe_lora_bf16* src,
   return MOE_LORA_OK;
 }
 
+moe_lora_status moe_lora_grouped_gemm_fp8(moe_lora_handle* h, const uint8_t* w, const float* w_scale,
+                                          const uint8_t* x, const float* x_scale, const int32_t* expert_offsets,
+                                          int E, int N, int K, int P, float* out, moe_lora_stream stream) {
+  if (h == nullptr || E < 1 || E > kMaxExperts || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0 || P < 0 ||
+      N > 65536 || K > 65536)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (static_cast<long long>(E) * N > 0x7fffffffLL) return MOE_LORA_ERR_INVALID_ARG;
+  if (P == 0) return MOE_LORA_OK;
+  if (!w || !w_scale || !x || !x_scale || !expert_offsets || !out || !aligned16(w) || !aligned16(x) ||
+      !aligned16(out) || !aligned4(w_scale) || !aligned4(x_scale) || !aligned4(expert_offsets))
+    return MOE_LORA_ERR_INVALID_ARG;
+  GemmF8Params gq;
+  std::memset(&gq, 0, sizeof(gq));
+  gq.w_scale = w_scale;
+  gq.x_scale = x_scale;
+  gq.out_f32 = out;
+  gq.offsets = expert_offsets;
+  gq.E = E;
+  gq.N = N;
+  gq.K = K;
+  gq.gated = 0;
+  return enqueue_gemm_fp8(h, gq, w, x, P, std::min(pick_bn(P, E), 64), stream, false);
+}
+
 moe_lora_status moe_lora_launch_count(const moe_lora_handle* h, uint64_t* count) {
   if (h == nullptr || count == nullptr) return MOE_LORA_ERR_INVALID_ARG;
   *count = h->launches;

@@ -221,6 +221,27 @@ def test_quant_fp8_host_checks(built_lib):
     assert L.moe_lora_quant_fp8(h, None, None, 0, 256, 1, None, None, None) == 0           # nothing to do
 
 
+def test_grouped_gemm_fp8_host_checks(built_lib):
+    """Host checks of the FP8 grouped GEMM return INVALID_ARG before any device work."""
+    L = B.lib()
+    h = ctypes.c_void_p(FAKE)
+    ok = dict(w=FAKE, ws=FAKE, x=FAKE, xs=FAKE, off=FAKE, E=4, N=256, K=384, P=32, out=FAKE)
+
+    def call(**over):
+        v = {**ok, **over}
+        return L.moe_lora_grouped_gemm_fp8(over.get("h", h), v["w"], v["ws"], v["x"], v["xs"], v["off"], v["E"],
+                                           v["N"], v["K"], v["P"], v["out"], None)
+    assert call(h=None) == 1                  # no handle
+    assert call(N=192) == 1                   # N % 128
+    assert call(K=64) == 1                    # K % 128
+    assert call(E=0) == 1 and call(E=1025) == 1
+    assert call(P=-1) == 1
+    assert call(x=FAKE + 8) == 1              # misaligned codes
+    assert call(out=FAKE + 4) == 1            # misaligned output
+    assert call(off=None) == 1
+    assert call(P=0, w=None, x=None, out=None) == 0   # nothing to do
+
+
 def test_binding_checks_fp8_weight_shapes():
     import torch
     E, H, I = 3, 256, 128

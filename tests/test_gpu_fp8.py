@@ -123,6 +123,74 @@ def test_fp8_layer_matches_oracle(handle, cfg):
                     gh.REL_L2_FP8)
 
 
+# The accumulation model of the FP8 GEMM (gpu_helpers.FP8_ACC_BITS): exact e4m3 products, each
+# 128-wide block summed as a tree of depth 7 with at least FP8_ACC_BITS significant bits
+# (error <= 7 * 2^-FP8_ACC_BITS * sum of |products|), block sums scaled and added in fp32.
+FP8_ACC_BITS = gh.FP8_ACC_BITS
+
+
+def _fp8_gemm_reference(wq, ws, xq, xs, offsets):
+    """Float64 block-scaled product of the FP8 grouped GEMM and its error bound under the
+    accumulation model above, from the e4m3 codes (decoded by the oracle's decoder)."""
+    E, N, K = wq.shape
+    P = xq.shape[0]
+    KB = K // 128
+    W = orc.e4m3_decode(wq).astype(np.float64)
+    X = orc.e4m3_decode(xq).astype(np.float64)
+    ref = np.zeros((P, N))
+    bnd = np.zeros((P, N))
+    for e in range(E):
+        q0, q1 = int(offsets[e]), int(offsets[e + 1])
+        if q1 == q0:
+            continue
+        xe = X[q0:q1]
+        scaled_abs = np.zeros((q1 - q0, N))
+        for b in range(KB):
+            kb = slice(128 * b, 128 * b + 128)
+            part = xe[:, kb] @ W[e, :, kb].T                              # exact block sums
+            absp = np.abs(xe[:, kb]) @ np.abs(W[e, :, kb]).T             # sums of |products|
+            sc = xs[b, q0:q1][:, None].astype(np.float64) * np.repeat(ws[e, :, b], 128)[None, :]
+            ref[q0:q1] += sc * part
+            bnd[q0:q1] += np.abs(sc) * absp * 7.0 * 2.0 ** -FP8_ACC_BITS
+            scaled_abs += np.abs(sc * part)
+        bnd[q0:q1] += (KB + 2) * 2.0 ** -24 * scaled_abs + 1e-30
+    return ref, bnd
+
+
+def test_fp8_grouped_gemm_within_accumulation_bound(handle):
+    """The FP8 grouped GEMM alone (moe_lora_grouped_gemm_fp8), element by element against the
+    float64 block-scaled product: random e4m3 codes over the whole finite range (subnormals
+    included), random block scales, five experts of ragged sizes with one empty; every output
+    within the bound of the accumulation model (FP8_ACC_BITS).  The same data with the weight
+    block scales read transposed (a plausible indexing slip) lies far outside that bound."""
+    g = torch.Generator().manual_seed(123)
+    E, N, K, P = 5, 384, 1024, 130
+    offsets = np.array([0, 17, 17, 60, 96, 130], dtype=np.int32)
+
+    def codes(shape):
+        c = torch.randint(0, 256, shape, generator=g, dtype=torch.int32)
+        c = torch.where((c & 0x7F) == 0x7F, c - 1, c)   # no NaN codes
+        return c.to(torch.uint8)
+
+    wq, xq = codes((E, N, K)), codes((P, K))
+    ws = torch.exp2(torch.empty((E, N // 128, K // 128)).uniform_(-12, -2, generator=g)).float()
+    xs = torch.exp2(torch.empty((K // 128, P)).uniform_(-10, 0, generator=g)).float()
+    out = pkg.moe_lora_grouped_gemm_fp8(handle, wq.cuda(), ws.cuda(), xq.cuda(), xs.cuda(),
+                                        torch.from_numpy(offsets).cuda())
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    ref, bnd = _fp8_gemm_reference(wq.numpy(), ws.numpy(), xq.numpy(), xs.numpy(), offsets)
+    err = np.abs(got - ref)
+    worst = float((err / bnd).max())
+    assert np.isfinite(got).all()
+    assert (err <= bnd).all(), f"{int((err > bnd).sum())} of {err.size} outputs outside the bound, worst {worst:.3g}x"
+    # the bound has teeth: a transposed block-scale index is caught
+    ws_t = ws.numpy().copy()
+    ws_t[:, :, :3] = ws_t[:, :, :3][:, ::-1, :]
+    ref_t, _ = _fp8_gemm_reference(wq.numpy(), ws_t, xq.numpy(), xs.numpy(), offsets)
+    assert (np.abs(got - ref_t) > bnd).mean() > 0.5
+
+
 def test_fp8_layer_lora_off(handle):
     cfg = FP8_CASES[0]
     inp = wl.make_inputs(cfg, seed=3)
@@ -145,7 +213,7 @@ def test_fp8_empty_batch_launches_nothing(handle):
 
 def test_fp8_graph_capture_and_replay(handle):
     """One capture, replayed with new hidden states in the captured buffers: each replay
-    matches an eager forward on the same inputs bit for bit."""
+    matches the oracle on those inputs, and an eager forward on them bit for bit."""
     cfg = wl.CONFIGS["decode"]
     inp = wl.make_inputs(cfg, seed=5)
     g = gh.to_dev(inp)
@@ -162,10 +230,16 @@ def test_fp8_graph_capture_and_replay(handle):
     with torch.cuda.graph(graph, stream=s):
         _forward_fp8(handle, g, w8, out=out, workspace=ws, stream=s)
     for it in range(3):
-        g["hidden"].copy_((torch.randn(cfg.T, cfg.H, generator=torch.Generator().manual_seed(it)) * (it + 1))
+        # fresh hidden states of the workload's distribution, N(0, 1): the FP8 bounds are
+        # derived for it (larger inputs raise the absolute error floor with them)
+        g["hidden"].copy_(torch.randn(cfg.T, cfg.H, generator=torch.Generator().manual_seed(it))
                           .to(torch.bfloat16).cuda())
         graph.replay()
         torch.cuda.synchronize()
+        ref_inp = dict(inp)
+        ref_inp["hidden"] = g["hidden"].cpu()
+        gh.assert_close(out.float().cpu().numpy(), _oracle_fp8(ref_inp, w8)["out"], f"replay {it}", gh.ATOL_FP8,
+                        gh.RTOL_FP8, gh.REL_L2_FP8)
         eager = _forward_fp8(handle, g, w8)
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
