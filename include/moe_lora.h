@@ -68,6 +68,8 @@ typedef enum {
 #define MOE_LORA_FLAG_UNFUSED_LORA        8u /* down-LoRA expand in the epilogue (see forward) */
 #define MOE_LORA_FLAG_NO_PDL             16u /* launch every kernel fully behind its predecessor */
 #define MOE_LORA_FLAG_SHARED_OUTER       32u /* shared-outer LoRA: lora_A_gu [S,1,R,H], lora_B_dn [S,1,H,R] */
+#define MOE_LORA_FLAG_DOWN_LORA_SIDE     64u /* narrow placement, two streams: the down LoRA on the side
+                                                 stream beside the down GEMM (see forward) */
 
 /* Stages that moe_lora_args.prof_events can bracket (two events per stage). */
 enum {
@@ -182,6 +184,12 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
      cores; else the down shrink runs after the activation and its expand inside the down
      GEMM.  The side stream is used when T <= 256 unless FORCE_SINGLE_STREAM (sglang PR
      #28466, "Which diagram applies when": decode-shaped batches only).
+   With MOE_LORA_FLAG_DOWN_LORA_SIDE on the side-stream placement (bf16 weights), the down
+   LoRA (shrink and expand, one kernel, into a bf16 delta per pair) runs on the side stream
+   beside the down GEMM and joins before the finalize, which adds it (sglang PR #28466
+   section 1 flow (B), the gemm2_done_event overlap the pages left unwired); without the
+   flag it stays in the activation kernel and the down GEMM's epilogue.  Elsewhere the flag
+   is ignored.
    Kernels after the routing start as programmatic dependents of the previous kernel on
    the stream unless MOE_LORA_FLAG_NO_PDL.
    Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */

@@ -123,7 +123,14 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
 #pragma unroll 8
   for (int j = 0; j < k; ++j) {
     if (q_s[j] < 0) continue;   // a pair of an expert outside the local range (routed entry)
-    const float4 v = load_y4(y, static_cast<size_t>(q_s[j]), p.H, h4);
+    float4 v = load_y4(y, static_cast<size_t>(q_s[j]), p.H, h4);
+    if (p.dd != nullptr) {   // the down-LoRA delta computed beside the down GEMM
+      const float4 d = load_y4(p.dd, static_cast<size_t>(q_s[j]), p.H, h4);
+      v.x += d.x;
+      v.y += d.y;
+      v.z += d.z;
+      v.w += d.w;
+    }
     const float w = w_s[j];
     acc.x += w * v.x;
     acc.y += w * v.y;

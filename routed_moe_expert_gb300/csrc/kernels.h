@@ -150,6 +150,7 @@ struct FinalizeParams {
   const int32_t* inv;            // [T * k]
   int T, H, k;
   __nv_bfloat16* out;            // [T, H]
+  const __nv_bfloat16* dd;       // [P, H] down-LoRA delta per permuted pair, added to y (or null)
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl = false);
 

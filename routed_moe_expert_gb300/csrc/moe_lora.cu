@@ -320,6 +320,8 @@ constexpr int kPairMinBn = 128;
 // the LoRA delta, the activation and the layer output are bf16 tensors there); the rounding
 // costs about 0.3% relative L2 against the float64 oracle, inside the layer's 0.5% bound.
 constexpr int kBf16YMinBn = 128;
+// Stacked active ranks up to which the gate_up LoRA shrink runs inside the permute.
+constexpr int kPermuteShrinkMaxRows = 64;
 int pair_tiles(int bn, int N) { return (bn >= kPairMinBn && N % 256 == 0) ? 2 : 1; }
 
 // Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
@@ -508,7 +510,8 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
                                           __nv_bfloat16* g, __nv_bfloat16* d, __nv_bfloat16* act, float* v, float* y,
                                           int32_t* pair_slot, __nv_bfloat16* ub, const LoraSlots& slots,
                                           uint32_t* status, cudaStream_t stream,
-                                          const moe_lora_fp8_weights* f8 = nullptr) {
+                                          const moe_lora_fp8_weights* f8 = nullptr,
+                                          const __nv_bfloat16** dn_delta = nullptr) {
   (void)ids;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const int P = T * k;
@@ -595,8 +598,11 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   }
 
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
+  // The down LoRA beside the down GEMM (flag): shrink and expand in one kernel on the side
+  // stream, into a bf16 delta per pair that the finalize adds; the activation runs alone.
+  const bool dn_side = lora && two && !fused && f8 == nullptr && (a->flags & MOE_LORA_FLAG_DOWN_LORA_SIDE);
   // the pairs' adapter slots ride along with the permute for the activation + down shrink
-  const bool act_shrink = lora && !fused && !fused_gu;
+  const bool act_shrink = lora && !fused && !fused_gu && !dn_side;
   if (f8 != nullptr) {   // permute and quantise in one pass
     ML_LAUNCH(h, launch_quant_fp8(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, k, P, H, xp8, sx, stream,
                                   pdl, a->slot_idx, act_shrink ? pair_slot : nullptr),
@@ -676,6 +682,41 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
   }
 
+  // second fork: the side stream takes the down LoRA once the activation is written
+  ForkJoin fj2{h, stream};
+  if (dn_side) {
+    __nv_bfloat16* dd = xp;   // the permuted hidden rows are dead after the gate_up GEMM: [P, H]
+    ML_CUDA(cudaEventRecord(h->ev_fork, stream), "cudaEventRecord");
+    ML_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0), "cudaStreamWaitEvent");
+    fj2.forked = true;
+    prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, h->side);
+    LoraParams lp;
+    std::memset(&lp, 0, sizeof(lp));
+    lp.src = act;
+    lp.by_token = 0;
+    lp.perm = perm;
+    lp.slot_idx = a->slot_idx;
+    lp.offsets = offsets;
+    lp.k = k;
+    lp.P = P;
+    lp.K = I;
+    lp.E = E;
+    lp.N = H;
+    lp.A = reinterpret_cast<const __nv_bfloat16*>(a->lora_A_dn);
+    lp.B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
+    lp.b_e1 = so ? 1 : 0;   // shared-outer: one B_dn per slot
+    lp.slots = slots;
+    lp.d_out = dd;
+    lp.status = status;
+    lp.where = kWhereLoraShrinkDn;
+    const int ntl_dn = (P >= 32 * E && lora_smem_bytes(4, R, H, true, E) <= 200 * 1024) ? 4 : 1;
+    ML_LAUNCH(h, launch_lora(lp, ntl_dn, lora_grid, h->side, false), "lora down (side stream) launch");
+    prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, h->side);
+    ML_CUDA(cudaEventRecord(h->ev_ready, h->side), "cudaEventRecord");
+    fj2.ready = true;
+    if (dn_delta != nullptr) *dn_delta = dd;
+  }
+
   if (lora && fused) {   // down-LoRA shrink on the activation; its expand runs inside the down GEMM
     prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
     LoraParams lp;
@@ -713,7 +754,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   dn.gated = 0;
   if (fused) {
     if (!fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn, so)) return MOE_LORA_ERR_CUDA;
-  } else if (lora) {
+  } else if (lora && !dn_side) {
     dn.lora_v = v;
     dn.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
     dn.lora_b_e1 = so ? 1 : 0;   // shared-outer: one B_dn per slot
@@ -722,7 +763,7 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   }
   // the epilogue's staged LoRA rows grow with the tile: narrow it until two stages fit
   int bn_dn = bn;
-  while (!fused && lora && bn_dn > 16 &&
+  while (!fused && lora && !dn_side && bn_dn > 16 &&
          (f8 != nullptr ? gemm_fp8_smem_bytes(bn_dn, 2, E, R) : gemm_smem_bytes(bn_dn, 1, 2, E, R, 0, 1)) >
              kMaxGemmSmem)
     bn_dn >>= 1;
@@ -754,6 +795,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   st = enqueue_gemm(h, dn, a->w2, act, P, bn_dn, stream, pdl);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+  if (dn_side) {   // join: the finalize adds the side stream's delta
+    fj2.joined = true;
+    ML_CUDA(cudaStreamWaitEvent(stream, h->ev_ready, 0), "cudaStreamWaitEvent");
+  }
 
   return MOE_LORA_OK;
 }
@@ -863,10 +908,18 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
                         !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
   const bool act_in_gemm = f8 == nullptr && (fuse_all || (!lora && bn0 >= 32));
   const bool y_bf16 = act_in_gemm && finalize && bn0 >= kBf16YMinBn;
+  const __nv_bfloat16* dn_delta = nullptr;   // the down-LoRA delta computed beside the down GEMM
   if (act_in_gemm) {
     const int bn = bn0;
     prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
-    if (fuse_all) {   // the permute and the gate_up LoRA shrink in one pass over the token rows
+    // The gate_up LoRA shrink: fused into the permute while the active slots' stacked ranks
+    // are few (the fused kernel's MMAs then fit two warps per 16-pair tile); many stacked
+    // ranks (several adapters) keep the tensor-core shrink kernel after a plain permute.
+    int nr_active = 0;
+    for (int s = 0; s < a->S && lora; ++s)
+      if (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) nr_active += slots.ranks[s];
+    const bool permute_shrink = fuse_all && nr_active <= kPermuteShrinkMaxRows;
+    if (permute_shrink) {   // the permute and the gate_up LoRA shrink in one pass over the token rows
       PermuteShrinkParams ps;
       std::memset(&ps, 0, sizeof(ps));
       ps.x = reinterpret_cast<const __nv_bfloat16*>(a->hidden);
@@ -880,10 +933,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       ps.k = k;
       ps.P = P;
       ps.RU = (R + 7) & ~7;
-      int nr = 0;
-      for (int s = 0; s < a->S; ++s)
-        if (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) nr += slots.ranks[s];
-      ps.nr_max = (nr + 7) & ~7;
+      ps.nr_max = (nr_active + 7) & ~7;
       ps.slots = slots;
       ps.xp = xp;
       ps.ub = ub;
@@ -892,11 +942,19 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       int grid = (P + 63) / 64 + E;
       if (grid > 4 * h->num_sms) grid = 4 * h->num_sms;
       ML_LAUNCH(h, launch_permute_shrink(ps, grid, stream, pdl), "permute + LoRA shrink launch");
+      prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     } else {
       ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
                 "permute launch");
+      prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
+      if (fuse_all) {
+        prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
+        st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
+                               so);
+        if (st != MOE_LORA_OK) return st;
+        prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
+      }
     }
-    prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
     GemmParams gu;
     std::memset(&gu, 0, sizeof(gu));
@@ -937,7 +995,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
   } else {
     st = enqueue_unfused_lora_path(h, a, lora, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub,
-                                   slots, status, stream, f8);
+                                   slots, status, stream, f8, &dn_delta);
     if (st != MOE_LORA_OK) return st;
   }
 
@@ -953,7 +1011,9 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   fp.H = H;
   fp.k = k;
   fp.out = reinterpret_cast<__nv_bfloat16*>(out);
-  ML_LAUNCH(h, launch_finalize(fp, stream, pdl), "finalize launch");
+  fp.dd = dn_delta;
+  // (no programmatic launch right behind the join on the side stream)
+  ML_LAUNCH(h, launch_finalize(fp, stream, pdl && dn_delta == nullptr), "finalize launch");
   prof(a, MOE_LORA_STAGE_FINALIZE, 1, stream);
   return MOE_LORA_OK;
 }

@@ -223,6 +223,42 @@ def test_shared_outer_lora_matches_oracle(handle, T, E, k, flags):
     _run_and_check(handle, cfg, seed=T + flags, flags=flags | pkg.FLAG_SHARED_OUTER)
 
 
+@pytest.mark.parametrize("T,E,k,ranks,shared", [(64, 128, 8, (16,), False), (40, 16, 4, (8, 16, 4), False),
+                                                 (64, 32, 4, (16, 8), True)],
+                         ids=["decode-shape", "mixed-ranks", "shared-outer"])
+def test_down_lora_on_side_stream_matches_oracle(handle, T, E, k, ranks, shared):
+    """MOE_LORA_FLAG_DOWN_LORA_SIDE: on the side-stream placement the down LoRA (shrink and
+    expand into a bf16 delta per pair) runs beside the down GEMM and the finalize adds it;
+    the layer still matches the oracle, eagerly and under CUDA-graph replay."""
+    cfg = wl.LayerConfig("dnside", T=T, H=512 if T < 64 else 2048, I=256 if T < 64 else 768, E=E, top_k=k,
+                         ranks=ranks, scalings=tuple(1.0 / (i + 1) for i in range(len(ranks))),
+                         slot_mode="uniform_none10", shared_outer=shared)
+    inp = wl.make_inputs(cfg, seed=T + E)
+    g = gh.to_dev(inp)
+    flags = pkg.FLAG_DOWN_LORA_SIDE | (pkg.FLAG_SHARED_OUTER if shared else 0)
+    ws = pkg.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
+    out = gh.forward(handle, g, flags=flags, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkg.moe_lora_check_status(ws)[0] == 0
+    ref = gh.oracle(inp)["out"]
+    gh.assert_close(out.float().cpu().numpy(), ref, "down LoRA on the side stream")
+    # the same forward captured once and replayed
+    out2 = torch.empty_like(out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gh.forward(handle, g, flags=flags, out=out2, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        gh.forward(handle, g, flags=flags, out=out2, workspace=ws, stream=s)
+    out2.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out)
+
+
 def test_lora_off_matches_oracle_base(handle):
     cfg = wl.LayerConfig("off", T=48, H=256, I=128, E=8, top_k=2, ranks=(8,), scalings=(2.0,))
     _run_and_check(handle, cfg, flags=pkg.FLAG_LORA_OFF, lora_off=True)
@@ -257,10 +293,16 @@ def test_launch_count_per_forward(handle):
     """One forward launches the kernels its placement draws: narrow tiles with LoRA = route,
     side-stream LoRA, permute, gate_up GEMM, activation + down shrink, down GEMM, finalize;
     LoRA off drops the LoRA kernel and fuses nothing else; wide tiles = route, permute with
-    the gate_up shrink, gate_up GEMM, tensor-core down shrink, down GEMM, finalize."""
+    the gate_up shrink, gate_up GEMM, tensor-core down shrink, down GEMM, finalize, with the
+    gate_up shrink as its own kernel after a plain permute when many ranks are stacked; the
+    down LoRA on the side stream replaces the activation + down shrink kernel by a plain
+    activation and one side-stream LoRA kernel."""
     narrow = wl.LayerConfig("n", T=64, H=256, I=128, E=32, top_k=4, ranks=(8,), scalings=(1.0,))
     wide = wl.LayerConfig("w", T=256, H=256, I=128, E=8, top_k=4, ranks=(8,), scalings=(1.0,))
-    for cfg, flags, want in ((narrow, 0, 7), (narrow, pkg.FLAG_LORA_OFF, 6), (wide, 0, 6)):
+    wide_many = wl.LayerConfig("wm", T=256, H=256, I=128, E=8, top_k=4, ranks=(8, 16, 32, 64),
+                               scalings=(1.0, 1.0, 1.0, 1.0))
+    for cfg, flags, want in ((narrow, 0, 7), (narrow, pkg.FLAG_LORA_OFF, 6), (wide, 0, 6), (wide_many, 0, 7),
+                             (narrow, pkg.FLAG_DOWN_LORA_SIDE, 8)):
         g = gh.to_dev(wl.make_inputs(cfg, seed=1))
         n0 = handle.launch_count()
         gh.forward(handle, g, flags=flags)
