@@ -617,8 +617,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      int c0 = 0;
+      if (!lora && p.y_tma && p.out_f32 == nullptr) {
+        // bf16 output (y at wide tiles): whole 32-token chunks, each one 32 x 32 TMA store, so
+        // a tile takes half the TMEM round trips and stores of 16-token chunks
 #pragma unroll 1
-      for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
+        for (; c0 + 32 <= nvalid; c0 += 32) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld_x32(taddr + c0, r);
+          tmem_ld_wait();
+          __nv_bfloat16* ybh = reinterpret_cast<__nv_bfloat16*>(yb2 + (ychunk++ & 1) * 512);
+          if (lane == 0) bulk_wait_read_1();   // the store that last read this buffer is done
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ybh[j * 32 + lane] = f2bf(__uint_as_float(r[j]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int fcol0 = nt * 128 + quarter * 32;
+          if (lane == 0 && fcol0 < p.N) {
+            tma_store_2d_hint(&p.tmap_y, ybh, fcol0, q0 + c0, l2_policy_evict_last());
+            bulk_commit();
+          }
+        }
+      }
+#pragma unroll 1
+      for (int c = c0; c < nvalid; c += 16) {   // warp-uniform bound
         uint32_t r[16];
         __syncwarp();   // the last chunk's stores branched per lane; tcgen05.ld is .aligned
         tmem_ld_x16(taddr + c, r);
@@ -627,22 +651,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
         for (int j = 0; j < 16; ++j) val[j] = __uint_as_float(r[j]);
         if (lora && col < p.N) lora_expand_chunk(p, lslot, v_s, c, nvalid, e, col, val);
-        // transpose through the warp's buffer (lane = feature on the way in).  A whole chunk
-        // of 16 tokens leaves as one TMA store of 16 x 32 values (fp32 or bf16) when the host
-        // set up the output's tensor map; otherwise each lane stores 4 consecutive features of
-        // a token: 4 token rows per instruction
+        // transpose through the warp's buffer (lane = feature on the way in).  A whole fp32
+        // chunk of 16 tokens leaves as one TMA store of 16 x 32 values when the host set up the
+        // output's tensor map; otherwise (bf16 tails included: their map's box is 32 tokens)
+        // each lane stores 4 consecutive features of a token: 4 token rows per instruction
         float* yb = yb2 + (p.y_tma ? (ychunk++ & 1) * 512 : 0);
         if (lane == 0) bulk_wait_read_1();   // the store that last read this buffer is done
         __syncwarp();
-        const bool whole = p.y_tma && c + 16 <= nvalid;
-        if (whole && p.out_f32 == nullptr) {
-          __nv_bfloat16* ybh = reinterpret_cast<__nv_bfloat16*>(yb);
+        const bool whole = p.y_tma && p.out_f32 != nullptr && c + 16 <= nvalid;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ybh[j * 32 + lane] = f2bf(val[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) yb[j * 32 + lane] = val[j];
-        }
+        for (int j = 0; j < 16; ++j) yb[j * 32 + lane] = val[j];
         const int fcol0 = nt * 128 + quarter * 32;
         if (whole) {
           fence_proxy_async_smem();

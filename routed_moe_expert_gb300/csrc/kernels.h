@@ -73,8 +73,8 @@ struct GemmParams {
   CUtensorMap tmap_x;            // activations [P rows, K cols], box {64, BN / cta_pair}
   __nv_bfloat16* out;            // [P, N] bf16 output, or
   float* out_f32;                //   fp32 output when non-null
-  CUtensorMap tmap_y;            // the output [P rows, N cols] (fp32, or bf16 when out_f32 is null),
-                                 // box {32, 16}: full 16-token chunks leave by TMA (y_tma = 1)
+  CUtensorMap tmap_y;            // the output [P rows, N cols]: fp32 with box {32, 16}, or bf16 (out_f32
+                                 // null) with box {32, 32}; whole chunks leave by TMA (y_tma = 1)
   int y_tma;
   const int32_t* offsets;        // [E + 1]
   uint32_t* status;

@@ -350,7 +350,7 @@ moe_lora_status enqueue_gemm(moe_lora_handle* h, GemmParams& gp, const void* W, 
   if (gp.gated == 0 && P >= 16 && (y_f32 || (gp.out != nullptr && gp.lora_v == nullptr))) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(gp.N), static_cast<cuuint64_t>(P)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(gp.N) * (y_f32 ? 4 : 2)};
-    cuuint32_t box[2] = {32, 16};
+    cuuint32_t box[2] = {32, y_f32 ? 16u : 32u};   // fp32: 16-token chunks; bf16: 32-token chunks
     cuuint32_t estr[2] = {1, 1};
     void* base = y_f32 ? static_cast<void*>(gp.out_f32) : static_cast<void*>(gp.out);
     if (h->encode(&gp.tmap_y, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
