@@ -83,6 +83,10 @@ CONFIGS = {
                                method=DEEPSEEK_V3, bias_std=0.1, rsf=2.827),
     "kimi_prefill": LayerConfig("kimi_prefill", T=4096, H=7168, I=2048, E=384, top_k=8,
                                 method=DEEPSEEK_V3, bias_std=0.1, rsf=2.827),
+    # the Kimi-like expert shape with 32 experts (2.8 GB of weights): the same GEMM shapes
+    # at a size an ncu capture of every counter can hold
+    "kimi_prefill_e32": LayerConfig("kimi_prefill_e32", T=512, H=7168, I=2048, E=32, top_k=8,
+                                    method=DEEPSEEK_V3, bias_std=0.1, rsf=2.827),
     # decode with a shared-outer adapter of rank 32 (one A on gate_up, one B on down)
     "shared_outer_decode": LayerConfig("shared_outer_decode", T=64, H=2048, I=768, E=128, top_k=8,
                                        ranks=(32,), scalings=(2.0,), shared_outer=True),
