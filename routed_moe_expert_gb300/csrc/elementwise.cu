@@ -2,6 +2,8 @@
 // with the gate_up LoRA delta, and the weighted top-k finalize.
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -90,22 +92,25 @@ cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, in
 // (unweighted) down-LoRA delta, added in the down GEMM's epilogue, so this is the vLLM API
 // page's _finalize_with_w2_lora
 // ("fused_moe/experts/trtllm_lora_moe": routing-weighted sum over top_k of the base rows
-// plus the routing-weighted down-LoRA delta).  A CTA covers 512 h of one token.
+// plus the routing-weighted down-LoRA delta).  A CTA covers 512 h (fp32 y) or 1024 h (bf16 y)
+// of one token.
 // ---------------------------------------------------------------------------------
-constexpr int kFinThreads = 128;   // 4 values each: 512 h per CTA
+constexpr int kFinThreads = 128;   // one 16-byte vector of y each: 512 h (fp32) or 1024 h (bf16) per CTA
 
-MLDEV float4 load_y4(const float* y, size_t row, int H, int h4) {
-  return __ldg(reinterpret_cast<const float4*>(y + row * H) + h4);
+MLDEV void unpack_y(const uint4& v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
 }
-MLDEV float4 load_y4(const __nv_bfloat16* y, size_t row, int H, int h4) {
-  const uint2 v = __ldg(reinterpret_cast<const uint2*>(y + row * H) + h4);
-  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-  return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
+MLDEV void unpack_y(const uint4& v, float (&f)[8]) { unpack8(v, f); }
 
-template <typename YT>
+// Each thread sums one 16-byte vector of the token's k rows of y (4 fp32 or 8 bf16 values):
+// the k loads (and those of the side-stream delta) go out together, 8 pairs at a time, and
+// are added in the fixed order j = 0, 1, ..., k - 1.
+template <typename YT, bool DD>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams p, const YT* __restrict__ y) {
+  constexpr int V = 16 / sizeof(YT);
   __shared__ int q_s[kMaxTopK];
   __shared__ float w_s[kMaxTopK];
   pdl_wait();
@@ -117,40 +122,70 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
     w_s[tid] = p.weights[pp];
   }
   __syncthreads();
-  const int h4 = blockIdx.y * kFinThreads + tid;
-  if (h4 >= (p.H >> 2)) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int j = 0; j < k; ++j) {
-    if (q_s[j] < 0) continue;   // a pair of an expert outside the local range (routed entry)
-    float4 v = load_y4(y, static_cast<size_t>(q_s[j]), p.H, h4);
-    if (p.dd != nullptr) {   // the down-LoRA delta computed beside the down GEMM
-      const float4 d = load_y4(p.dd, static_cast<size_t>(q_s[j]), p.H, h4);
-      v.x += d.x;
-      v.y += d.y;
-      v.z += d.z;
-      v.w += d.w;
+  const int hv = blockIdx.y * kFinThreads + tid;   // vector index within the row
+  if (hv >= p.H / V) return;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+  const uint4* yv = reinterpret_cast<const uint4*>(y);
+  // the down-LoRA delta computed beside the down GEMM (bf16 [P, H]): V values = 2V bytes
+  using DT = typename std::conditional<V == 8, uint4, uint2>::type;
+  const DT* dv = DD ? reinterpret_cast<const DT*>(p.dd) : nullptr;
+  const size_t HV = static_cast<size_t>(p.H / V);
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    uint4 raw[8];
+    DT rawd[DD ? 8 : 1];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = j0 + jj;
+      // a pair of an expert outside the local range (routed entry) has q < 0: skipped
+      const int q = j < k ? q_s[j] : -1;
+      raw[jj] = q >= 0 ? __ldg(yv + static_cast<size_t>(q) * HV + hv) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (DD) rawd[jj] = q >= 0 ? __ldg(dv + static_cast<size_t>(q) * HV + hv) : DT{};
     }
-    const float w = w_s[j];
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = j0 + jj;
+      if (j >= k || q_s[j] < 0) continue;
+      float v[V];
+      unpack_y(raw[jj], v);
+      if constexpr (DD) {
+        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&rawd[jj]);
+#pragma unroll
+        for (int i = 0; i < V / 2; ++i) {
+          const float2 d = __bfloat1622float2(d2[i]);
+          v[2 * i] += d.x;
+          v[2 * i + 1] += d.y;
+        }
+      }
+      const float w = w_s[j];
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += w * v[i];
+    }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 v;
-  v.x = *reinterpret_cast<uint32_t*>(&lo);
-  v.y = *reinterpret_cast<uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[h4] = v;
+  if constexpr (V == 8) {
+    reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.H)[hv] = pack8(acc);
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t) * p.H)[hv] = o;
+  }
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   if (p.T == 0) return cudaSuccess;
-  const int H4 = p.H / 4;
-  const dim3 grid(p.T, (H4 + kFinThreads - 1) / kFinThreads);
-  if (p.y != nullptr) return launch_k(finalize_kernel<float>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y);
-  return launch_k(finalize_kernel<__nv_bfloat16>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y_bf16);
+  const bool f32 = p.y != nullptr;
+  const int HV = p.H / (f32 ? 4 : 8);
+  const dim3 grid(p.T, (HV + kFinThreads - 1) / kFinThreads);
+  const bool dd = p.dd != nullptr;
+  if (f32)
+    return dd ? launch_k(finalize_kernel<float, true>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y)
+              : launch_k(finalize_kernel<float, false>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y);
+  return dd ? launch_k(finalize_kernel<__nv_bfloat16, true>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y_bf16)
+            : launch_k(finalize_kernel<__nv_bfloat16, false>, grid, dim3(kFinThreads), 0, stream, pdl, p, p.y_bf16);
 }
 
 // ---------------------------------------------------------------------------------

@@ -215,14 +215,15 @@ struct PermuteShrinkParams {
   const __nv_bfloat16* A;        // [S, E, R, H], or [S, 1, R, H] with a_e1
   int a_e1;
   int H, E, k, P, RU;
-  int nr_max;                    // stacked rank rows of all active slots, rounded up to 8 (<= 256)
+  int nr_max;                    // stacked rank rows of all active slots, rounded up to 8 (<= 32)
   LoraSlots slots;
   __nv_bfloat16* xp;             // [P, H]
   __nv_bfloat16* ub;             // [S, P, RU]
   int32_t* pair_slot;            // [P]
   uint32_t* status;
 };
-size_t permute_shrink_smem_bytes(int nr_max, int E);
+constexpr int kPermuteShrinkMaxRows = 32;   // stacked active rank rows the fused kernel takes
+size_t permute_shrink_smem_bytes(int nr_max, int E, int H);
 cudaError_t launch_permute_shrink(const PermuteShrinkParams& p, int grid, cudaStream_t stream, bool pdl = false);
 
 // Activation (gate_up output g plus the bf16 gate_up LoRA delta d, SwiGLU, bf16 out)

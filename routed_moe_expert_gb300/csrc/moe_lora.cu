@@ -320,8 +320,6 @@ constexpr int kPairMinBn = 128;
 // the LoRA delta, the activation and the layer output are bf16 tensors there); the rounding
 // costs about 0.3% relative L2 against the float64 oracle, inside the layer's 0.5% bound.
 constexpr int kBf16YMinBn = 128;
-// Stacked active ranks up to which the gate_up LoRA shrink runs inside the permute.
-constexpr int kPermuteShrinkMaxRows = 64;
 int pair_tiles(int bn, int N) { return (bn >= kPairMinBn && N % 256 == 0) ? 2 : 1; }
 
 // Pipeline depth from a shared-memory budget.  At narrow token tiles the gate_up GEMM leaves
@@ -939,8 +937,8 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       ps.ub = ub;
       ps.pair_slot = pair_slot;
       ps.status = status;
-      int grid = (P + 63) / 64 + E;
-      if (grid > 4 * h->num_sms) grid = 4 * h->num_sms;
+      int grid = (P + 63) / 64 + E;   // tiles of 64 pairs (at most), two CTAs per SM
+      if (grid > 2 * h->num_sms) grid = 2 * h->num_sms;
       ML_LAUNCH(h, launch_permute_shrink(ps, grid, stream, pdl), "permute + LoRA shrink launch");
       prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     } else {
