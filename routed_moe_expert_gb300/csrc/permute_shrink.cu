@@ -10,25 +10,29 @@
 // LoRA (section 1, merged_experts_fused_moe_lora_add); its expand runs inside the gate_up
 // GEMM.  Both read the same token rows, so one pass does both: each hidden row is read once
 // per pair (from L2: every token is read by k pairs), written out as the permuted row and
-// kept in shared memory long enough to be multiplied by the adapter rows.
+// kept in shared memory long enough for the tensor cores to multiply it by the adapter rows.
 //
 // A CTA tile is up to 64 consecutive permuted pairs of one expert, taken in chunks of CW
 // columns.  Warp w moves the tile's rows 8w..8w+7: each lane loads the same 16-byte pieces
-// of those rows in every chunk into registers (the next chunk's loads are in flight while
-// the tensor cores work on the current one), then stores them to xp and to shared memory,
-// in rows of CW*2 bytes with the 16-byte piece index XORed with the row index so ldmatrix
-// reads them without bank conflicts.  A piece costs one load, one global store and one
-// shared store; its addresses move by a constant from chunk to chunk.  The adapter rows of
-// every slot present in the tile are stacked as the N side of mma.sync m16n8k16 (M = the
-// pairs); the eight warps split each chunk as four 16-pair m-tiles by two halves of its
-// k-steps, and the two halves' sums are added in a fixed order at the end of the tile.
+// of those rows in every chunk into registers (two chunks in flight: the next chunk's loads
+// while the current one is stored), then stores them to xp and into one of two shared-memory
+// chunk buffers, laid out as 64-column panels with the 128-byte swizzle (the K-major operand
+// layout of tcgen05.mma).  The adapter rows of every slot present in the tile are stacked
+// into the same buffer as NB (16 or 32) more rows per panel.  One thread then issues the
+// chunk's tcgen05.mma (M = 128: the tile's 64 pairs and 64 rows that are never read back,
+// N = NB, K = CW) into a TMEM accumulator and commits it to the buffer's mbarrier; the
+// copying warps go on with the next chunk and only wait for that mbarrier before they refill
+// the same buffer two chunks later.  At the end of the tile two warps read the 64 pair rows
+// of the accumulator.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mlk {
 
 constexpr int kPsThreads = 256;
-constexpr int kPsTile = 64;   // pairs per tile
+constexpr int kPsTile = 64;         // pairs per tile
+constexpr int kPsPanel = 64 * 128;  // one 64-column panel of the tile's token rows (bytes)
+constexpr uint32_t kPsTmemCols = 32;
 
 MLDEV uint4 ld_global_nc_v4_hint(const void* p, uint64_t policy) {
   uint4 v;
@@ -37,56 +41,46 @@ MLDEV uint4 ld_global_nc_v4_hint(const void* p, uint64_t policy) {
                : "l"(p), "l"(policy));
   return v;
 }
-MLDEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-MLDEV void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
-}
-MLDEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
-// Stacked adapter rows a tile holds: 8, 16 or 32 (the kernel's n8 tiles times 8).
-static int ps_rows8(int nr_max) { return nr_max <= 8 ? 8 : nr_max <= 16 ? 16 : 32; }
-// Chunk width: the widest of 512, 256, 128, 64 columns that divides H; 512-wide chunks (16
-// pieces in flight per lane) only up to 16 stacked rows, where the registers still hold them.
-static int ps_chunk(int H, int rows8) {
-  return (H % 512 == 0 && rows8 <= 16) ? 512 : H % 256 == 0 ? 256 : H % 128 == 0 ? 128 : 64;
-}
+// Stacked adapter rows of the MMA's N: 16 or 32.
+static int ps_nb(int nr_max) { return nr_max <= 16 ? 16 : 32; }
+// Chunk width: 256 columns when H allows, else 128 or 64.
+static int ps_chunk(int H) { return H % 256 == 0 ? 256 : H % 128 == 0 ? 128 : 64; }
+// One chunk buffer: CW/64 token-row panels, then CW/64 adapter-row panels of NB rows.
+static int ps_buf_bytes(int cw, int nb) { return (cw / 64) * (kPsPanel + nb * 128); }
 
 size_t permute_shrink_smem_bytes(int nr_max, int E, int H) {
-  const int rows8 = ps_rows8(nr_max);
-  return 128 + static_cast<size_t>(kPsTile + rows8) * ps_chunk(H, rows8) * 2 + kPsTile * 16 * 4 + 2 * kPsTile * 4 +
-         rows8 * 8 + 4 * (4 + kMaxFusedSlots) + 8 * (static_cast<size_t>(E) + 1);
+  const int nb = ps_nb(nr_max);
+  // 1024 for the alignment of the buffers, two buffers, 8 KB read past the last token-row
+  // panel by the M = 128 MMAs (rows 64..127, never read back), then the tile's bookkeeping
+  return 1024 + 2 * static_cast<size_t>(ps_buf_bytes(ps_chunk(H), nb)) + kPsPanel + 2 * 8 + 16 +
+         kPsTile * nb * 4 + 2 * kPsTile * 4 + nb * 8 + 4 * (4 + kMaxFusedSlots) + 8 * (static_cast<size_t>(E) + 1);
 }
 
-// CW: chunk width (columns); NT8: n8 tiles of stacked adapter rows.
-template <int CW, int NT8>
+// CW: chunk width (columns); NB: stacked adapter rows (the MMA's N).
+template <int CW, int NB>
 __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const PermuteShrinkParams p) {
-  constexpr int kRowBytes = CW * 2;                  // one row of a chunk in shared memory
   constexpr int kPieces = CW / 8;                    // 16-byte pieces per row of a chunk
   constexpr int kPerRow = kPieces >= 32 ? kPieces / 32 : 1;   // pieces of one row per lane
   constexpr int kLanesPerRow = kPieces / kPerRow;    // lanes sharing one row
   constexpr int kRowsPerStep = 32 / kLanesPerRow;    // rows the warp covers in one step
   constexpr int kSteps = 8 / kRowsPerStep;           // steps over the warp's 8 rows
   constexpr int kXPer = kSteps * kPerRow;            // token-row pieces per lane and chunk
-  constexpr int kRows8 = NT8 * 8;                    // stacked adapter rows in shared memory
-  constexpr int kAPer = (kRows8 * kPieces + kPsThreads - 1) / kPsThreads;   // adapter pieces per thread
-  constexpr int kHalfSteps = CW / 32;                // k-steps of 16 per half chunk
-  extern __shared__ __align__(128) uint8_t ps_smem[];
-  uint8_t* smem = ps_smem + ((128u - (smem_u32(ps_smem) & 127u)) & 127u);
-  float* part = reinterpret_cast<float*>(smem + (kPsTile + kRows8) * kRowBytes);   // [64][16] k-half 1 sums
-  int* prow = reinterpret_cast<int*>(part + kPsTile * 16);         // [64] source token row
+  constexpr int kAPer = (NB * kPieces + kPsThreads - 1) / kPsThreads;   // adapter pieces per thread
+  constexpr int kPanels = CW / 64;
+  constexpr int kABase = kPanels * kPsPanel;         // adapter panels after the token-row panels
+  constexpr int kBuf = kPanels * (kPsPanel + NB * 128);
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, NB);
+  extern __shared__ __align__(1024) uint8_t ps_smem[];
+  uint8_t* smem = ps_smem + ((1024u - (smem_u32(ps_smem) & 1023u)) & 1023u);
+  uint64_t* mma_done = reinterpret_cast<uint64_t*>(smem + 2 * kBuf + kPsPanel);   // [2] per buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* u_s = reinterpret_cast<float*>(tmem_slot + 4);            // [64][NB] the tile's shrink, fp32
+  int* prow = reinterpret_cast<int*>(u_s + kPsTile * NB);          // [64] source token row
   int* pslot = prow + kPsTile;                                     // [64] active slot or -1
-  long long* arow = reinterpret_cast<long long*>(pslot + kPsTile);   // [kRows8] A row element offsets, -1 = padding
-  int* sinfo = reinterpret_cast<int*>(arow + kRows8);              // [4]: slot mask, rows
+  long long* arow = reinterpret_cast<long long*>(pslot + kPsTile);   // [NB] A row element offsets, -1 = padding
+  int* sinfo = reinterpret_cast<int*>(arow + NB);                  // [4]: slot mask, rows
   int* soff = sinfo + 4;                                           // [8] first stacked row per slot
   int* tile_start = soff + kMaxFusedSlots;                         // [E+1]
   int* seg = tile_start + (p.E + 1);                               // [E+1]
@@ -97,6 +91,16 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
   const int Ea = p.a_e1 ? 1 : E;
   const int lr = lane / kLanesPerRow, lc = lane % kLanesPerRow;   // row within a step, first piece
 
+  if (tid == 0) {
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kPsTmemCols);
+    tmem_relinquish();
+  }
   // The hidden rows are read k times (once per pair of the token): keep them in L2.  The
   // permuted rows are written once here and read next by the gate_up GEMM from HBM anyway:
   // stream them, so they do not push the hidden rows out of L2.
@@ -104,13 +108,16 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
   const uint64_t pol_stream = l2_policy_evict_first();
   pdl_wait();    // the routing (perm, offsets) comes from the previous kernel
   pdl_trigger();
-  if (warp == 0) build_tile_schedule(p.offsets, E, kPsTile, 1, seg, tile_start);
+  if (warp == 1) build_tile_schedule(p.offsets, E, kPsTile, 1, seg, tile_start);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   const int total = tile_start[E];
-  const int mt = warp & 3, kh = warp >> 2;   // the warp's m-tile and k-half of every chunk
-  const uint32_t xs_u = smem_u32(smem), as_u = xs_u + kPsTile * kRowBytes;
+  const uint32_t smem0 = smem_u32(smem);
+  uint32_t cc = 0;   // chunks issued by this CTA so far: buffer cc & 1, its use cc >> 1
 
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -147,14 +154,13 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
         soff[s] = j;
         if (!((smask >> s) & 1u)) continue;
         const long long base = (static_cast<long long>(s) * Ea + (p.a_e1 ? 0 : e)) * R;
-        for (int r = 0; r < p.slots.ranks[s] && j < kRows8; ++r, ++j) arow[j] = (base + r) * H;
+        for (int r = 0; r < p.slots.ranks[s] && j < NB; ++r, ++j) arow[j] = (base + r) * H;
       }
-      for (int r = j; r < kRows8; ++r) arow[r] = -1;   // padding rows: zeros in shared memory
+      for (int r = j; r < NB; ++r) arow[r] = -1;   // padding rows: zeros in shared memory
       sinfo[1] = j;
     }
     __syncthreads();
     const int nr = sinfo[1];                 // stacked rows of this tile (0: no adapter at all)
-    const int nr8 = (nr + 7) & ~7;
 
     // this lane's token rows (one per step) and their 16-byte pieces lc + kLanesPerRow * u
     int trow[kSteps];
@@ -162,16 +168,12 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
     for (int st = 0; st < kSteps; ++st) trow[st] = prow[8 * warp + st * kRowsPerStep + lr];
     __nv_bfloat16* drow = p.xp + static_cast<size_t>(q0 + 8 * warp + lr) * H + lc * 8;
 
-    float acc[NT8][4];
-#pragma unroll
-    for (int j = 0; j < NT8; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[j][i] = 0.0f;
-
-    uint4 xv[kXPer], av[kAPer];
-    // this thread's adapter-row pieces: stacked row pi / kPieces, piece pi % kPieces (rows
-    // past the stack are not loaded, padding rows load as zeros)
-    auto load_chunk = [&](int kc) {
+    // Two register sets: chunk kc + 1 is in flight while chunk kc is stored, and a set is
+    // refilled (chunk kc + 2) as soon as its chunk is in shared memory.
+    uint4 xa[kXPer], aa[kAPer], xb[kXPer], ab[kAPer];
+    // this thread's adapter-row pieces: stacked row pi / kPieces, piece pi % kPieces (padding
+    // rows load as zeros)
+    auto load_chunk = [&](uint4 (&xv)[kXPer], uint4 (&av)[kAPer], int kc) {
 #pragma unroll
       for (int st = 0; st < kSteps; ++st)
 #pragma unroll
@@ -183,15 +185,24 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
         const int pi = tid + kPsThreads * i;
         const int r = pi / kPieces;
         av[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < kRows8) {
+        if (r < NB && nr > 0) {
           const long long off = arow[r];
           if (off >= 0) av[i] = ld_global_nc_v4_hint(p.A + off + (pi % kPieces) * 8 + kc * CW, pol_keep);
         }
       }
     };
-    load_chunk(0);
-    for (int kc = 0; kc < KCH; ++kc) {
-      // the chunk's rows: out to the permuted copy and into shared memory
+    // byte offset of piece c (0 <= c < kPieces) of row r in a region of 64-column panels
+    auto panel_off = [](int r, int c, int panel_bytes) -> uint32_t {
+      return static_cast<uint32_t>((c >> 3) * panel_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    };
+    bool ok = true;
+    auto step = [&](uint4 (&xv)[kXPer], uint4 (&av)[kAPer], int kc) {
+      const uint32_t buf = cc & 1u;
+      uint8_t* bp = smem + buf * kBuf;
+      // the buffer's previous chunk (two chunks ago) has been multiplied
+      if (cc >= 2 && !mbar_wait(&mma_done[buf], ((cc >> 1) - 1) & 1u, abort_flag, p.status, kWhereLoraShrinkGu))
+        ok = false;
+      // the chunk's rows: out to the permuted copy and into the buffer
 #pragma unroll
       for (int st = 0; st < kSteps; ++st) {
         const int r = 8 * warp + st * kRowsPerStep + lr;
@@ -202,72 +213,57 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
           if (r < np)
             st_global_v4_hint(drow + static_cast<size_t>(st * kRowsPerStep) * H + kc * CW + u * kLanesPerRow * 8, v,
                               pol_stream);
-          *reinterpret_cast<uint4*>(smem + r * kRowBytes + ((c ^ (r & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(bp + panel_off(r, c, kPsPanel)) = v;
         }
       }
 #pragma unroll
       for (int i = 0; i < kAPer; ++i) {
         const int pi = tid + kPsThreads * i;
         const int r = pi / kPieces, c = pi % kPieces;
-        if (r < kRows8) *reinterpret_cast<uint4*>(smem + (kPsTile + r) * kRowBytes + ((c ^ (r & 7)) << 4)) = av[i];
+        if (r < NB) *reinterpret_cast<uint4*>(bp + kABase + panel_off(r, c, NB * 128)) = av[i];
       }
-      __syncthreads();   // chunk kc is in shared memory
-      if (kc + 1 < KCH) load_chunk(kc + 1);   // in flight during the MMAs
-      __syncwarp();   // the loads above branch per thread; ldmatrix and mma.sync are .aligned
-      if (nr > 0 && mt * 16 < np) {
-        const int ar = mt * 16 + (lane & 15);
+      fence_proxy_async_smem();   // the generic-proxy stores above are read by tcgen05.mma
+      __syncthreads();            // chunk kc is in the buffer
+      if (kc + 2 < KCH) load_chunk(xv, av, kc + 2);   // this set's next chunk
+      if (tid == 0) {
+        if (nr > 0) {
+          tc_fence_after();
+          const uint32_t xb0 = smem0 + buf * kBuf, ab0 = xb0 + kABase;
 #pragma unroll
-        for (int k2 = 0; k2 < kHalfSteps; ++k2) {
-          const int kk = kh * kHalfSteps + k2;
-          uint32_t af[4];
-          ldsm_x4(xs_u + ar * kRowBytes + (((kk * 2 + (lane >> 4)) ^ (ar & 7)) << 4), af);
-#pragma unroll
-          for (int j = 0; j < NT8; ++j) {
-            if (j * 8 < nr8) {   // warp-uniform
-              uint32_t bfr[2];
-              const int br = j * 8 + (lane & 7);
-              ldsm_x2(as_u + br * kRowBytes + (((kk * 2 + ((lane >> 3) & 1)) ^ (br & 7)) << 4), bfr);
-              mma_16816(acc[j], af, bfr);
-            }
+          for (int kk = 0; kk < CW / 16; ++kk) {
+            const uint64_t ad = sw128_kmajor_desc(xb0 + (kk >> 2) * kPsPanel) + 2 * (kk & 3);
+            const uint64_t bd = sw128_kmajor_desc(ab0 + (kk >> 2) * NB * 128) + 2 * (kk & 3);
+            umma_bf16(tmem, ad, bd, kIdesc, (kc | kk) != 0 ? 1u : 0u);
           }
         }
+        umma_commit(&mma_done[buf]);   // (with no MMA issued since the last commit it completes at once)
       }
-      __syncthreads();   // every warp is done with chunk kc's shared memory
+      ++cc;
+    };
+    load_chunk(xa, aa, 0);
+    if (KCH > 1) load_chunk(xb, ab, 1);
+    for (int kc = 0; kc < KCH; kc += 2) {
+      step(xa, aa, kc);
+      if (kc + 1 < KCH) step(xb, ab, kc + 1);
     }
 
-    // ---------------- k-half 1 parks its sums, k-half 0 adds them (a fixed order), 16 columns at a time
-    float* u_s = reinterpret_cast<float*>(smem);   // [64][nr8] fp32 (the chunk buffer is free)
-    const int g = lane >> 2, c4 = lane & 3;
-    const bool mm = nr > 0 && mt * 16 < np;
+    // ---------------- the tile's shrink: wait for its last chunk's MMAs, read the 64 pair rows
+    if (!mbar_wait(&mma_done[(cc - 1) & 1u], ((cc - 1) >> 1) & 1u, abort_flag, p.status, kWhereLoraShrinkGu))
+      ok = false;
+    tc_fence_after();
+    __syncwarp();   // the waits above end per thread; tcgen05.ld is .aligned
+    if (warp < 2 && nr > 0) {   // TMEM lanes 0..63 = the tile's pairs
+      uint32_t v[16];
 #pragma unroll
-    for (int j0 = 0; j0 < NT8; j0 += 2) {
-      if (mm && kh == 1) {
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        tmem_ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+        tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          if (j0 + jj < NT8) {
-            const int r0 = mt * 16 + g, n0 = jj * 8 + 2 * c4;
-            part[r0 * 16 + n0] = acc[j0 + jj][0];
-            part[r0 * 16 + n0 + 1] = acc[j0 + jj][1];
-            part[(r0 + 8) * 16 + n0] = acc[j0 + jj][2];
-            part[(r0 + 8) * 16 + n0 + 1] = acc[j0 + jj][3];
-          }
-        }
+        for (int i = 0; i < 16; ++i) u_s[(warp * 32 + lane) * NB + c0 + i] = __uint_as_float(v[i]);
       }
-      __syncthreads();
-      if (mm && kh == 0) {
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          if (j0 + jj < NT8 && (j0 + jj) * 8 < nr8) {
-            const int r0 = mt * 16 + g, n0 = jj * 8 + 2 * c4, col = (j0 + jj) * 8 + 2 * c4;
-            u_s[r0 * nr8 + col] = acc[j0 + jj][0] + part[r0 * 16 + n0];
-            u_s[r0 * nr8 + col + 1] = acc[j0 + jj][1] + part[r0 * 16 + n0 + 1];
-            u_s[(r0 + 8) * nr8 + col] = acc[j0 + jj][2] + part[(r0 + 8) * 16 + n0];
-            u_s[(r0 + 8) * nr8 + col + 1] = acc[j0 + jj][3] + part[(r0 + 8) * 16 + n0 + 1];
-          }
-        }
-      }
-      __syncthreads();
     }
+    tc_fence_before();
+    __syncthreads();   // u_s is complete; the accumulator may be overwritten by the next tile
 
     // ---------------- ub rows: the pair's own slot gets bf16(scaling * u), every other zero
     const int RU8 = p.RU >> 3;   // 16-byte pieces per ub row
@@ -282,7 +278,7 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
       if (pslot[n] == s) {
         const float sc = p.slots.scal[s];
         const int rank = p.slots.ranks[s];
-        const float* ur = u_s + n * nr8 + soff[s];   // s is an active slot below kMaxFusedSlots
+        const float* ur = u_s + n * NB + soff[s];   // s is an active slot below kMaxFusedSlots
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           if (r0 + u < rank) v[u] = sc * ur[r0 + u];
@@ -290,6 +286,13 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
       *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s) * p.P + q0 + n) * p.RU + r0) = pack8(v);
     }
     __syncthreads();   // u_s and the pair info are rewritten by the next tile
+    if (!ok) break;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*tmem_slot, kPsTmemCols);
   }
 }
 
@@ -299,24 +302,16 @@ cudaError_t launch_permute_shrink(const PermuteShrinkParams& p, int grid, cudaSt
       p.slots.S > kMaxFusedSlots)
     return cudaErrorInvalidValue;
   const int smem = static_cast<int>(permute_shrink_smem_bytes(p.nr_max, p.E, p.H));
-  const int rows8 = ps_rows8(p.nr_max);
+  const int nb = ps_nb(p.nr_max);
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     return launch_k(kern, dim3(grid), dim3(kPsThreads), static_cast<size_t>(smem), stream, pdl, p);
   };
-  auto by_rows = [&](auto cw) -> cudaError_t {
-    constexpr int C = decltype(cw)::value;
-    if (rows8 == 8) return go(permute_shrink_kernel<C, 1>);
-    if (rows8 == 16) return go(permute_shrink_kernel<C, 2>);
-    return go(permute_shrink_kernel<C, 4>);
-  };
-  switch (ps_chunk(p.H, rows8)) {
-    case 512:   // (rows8 <= 16 here)
-      return rows8 == 8 ? go(permute_shrink_kernel<512, 1>) : go(permute_shrink_kernel<512, 2>);
-    case 256: return by_rows(std::integral_constant<int, 256>());
-    case 128: return by_rows(std::integral_constant<int, 128>());
-    default: return by_rows(std::integral_constant<int, 64>());
+  switch (ps_chunk(p.H)) {
+    case 256: return nb == 16 ? go(permute_shrink_kernel<256, 16>) : go(permute_shrink_kernel<256, 32>);
+    case 128: return nb == 16 ? go(permute_shrink_kernel<128, 16>) : go(permute_shrink_kernel<128, 32>);
+    default: return nb == 16 ? go(permute_shrink_kernel<64, 16>) : go(permute_shrink_kernel<64, 32>);
   }
 }
 
