@@ -239,7 +239,7 @@ def _lora_off_ms(fwd, stream, steps, warmup, torch, pkg):
     return o0.elapsed_time(o1) / steps
 
 
-def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None):
+def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
     def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
         flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
         hid = g["hidden"] if hidden is None else hidden
@@ -251,6 +251,8 @@ def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None):
                   flags=flags, out=o, workspace=ws, prof_events=prof, outputs=outputs)
         if w8 is not None:
             return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw)
+        if w4 is not None:
+            return pkg.moe_lora_forward_nvfp4(h, hid, lg, *w4, k, **kw)
         return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw)
     return fwd
 
@@ -357,28 +359,40 @@ def run_gpu(args):
         w1q, w1s = wl.quantize_weights_fp8(g["w1"])
         w2q, w2s = wl.quantize_weights_fp8(g["w2"])
         w8 = (w1q, w1s, w2q, w2s)
+    # --nvfp4: the same layer with NVFP4 expert weights quantised from the drawn ones
+    w4 = None
+    if args.nvfp4:
+        w4 = wl.quantize_weights_nvfp4(g["w1"]) + wl.quantize_weights_nvfp4(g["w2"])
+    quant = w8 is not None or w4 is not None
     P = T * k
     h = pkg.Handle(local)
     ws = pkg.alloc_workspace(T, H, I, E, k, cfg.S, cfg.R)
     out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
-    fwd = _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8)
+    fwd = _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8, w4)
 
     # touched experts (routing is fixed for the fixed input)
     touched, lora_blocks, _ = _touched_and_lora(cfg, fwd, pkg, ws, T, E, k, I, H, g, torch)
     slots = g["slot_idx"].cpu().numpy()
 
     # algorithmic bytes / flops (FP8: one byte per weight plus a float per 128 x 128 block,
-    # the permuted hidden rows as codes plus a float per 128 values)
-    wb = 1 if w8 is not None else 2
-    w_bytes_expert = 3 * H * I * wb + (3 * H * I // (128 * 128) * 4 if w8 is not None else 0)
+    # the permuted hidden rows as codes plus a float per 128 values; NVFP4: half a byte per
+    # weight plus a byte per 16 and two floats per expert, the permuted hidden rows as the
+    # f16 values the GEMM reads plus a float per row)
+    if w4 is not None:
+        w_bytes_expert = 3 * H * I // 2 + 3 * H * I // 16 + 8
+    else:
+        wb = 1 if w8 is not None else 2
+        w_bytes_expert = 3 * H * I * wb + (3 * H * I // (128 * 128) * 4 if w8 is not None else 0)
     io_bytes = T * H * 2 * 2 + T * E * 2
     step_bytes = touched * w_bytes_expert + lora_blocks + io_bytes
     step_flops = 2 * 3 * H * I * P + sum(2 * cfg.ranks[max(int(slots[t]), 0)] * (2 * H + 3 * I) * k
                                          for t in range(T) if cfg.S > 0 and slots[t] >= 0)
-    act_fused = w8 is None and _act_in_gate_up(P, E)
+    act_fused = not quant and _act_in_gate_up(P, E)
     g_out = P * I * 2 if act_fused else P * 2 * I * 2
-    if w8 is None:
+    if w4 is not None:
+        gu_bytes = touched * (2 * I * H // 2 + 2 * I * H // 16 + 4) + P * H * 2 + P * 4 + P * 2 * I * 2
+    elif w8 is None:
         gu_bytes = touched * (2 * I * H * 2) + P * H * 2 + g_out   # weights + xp read + g (or a) write
     else:
         gu_bytes = touched * (2 * I * H + 2 * I * H // (128 * 128) * 4) + P * H + P * H // 128 * 4 + P * 2 * I * 2
@@ -450,8 +464,9 @@ def run_gpu(args):
     # the gate_up GEMM is HBM-bound when its bytes take longer than its flops at peak
     t_hbm = gu_bytes / (peaks["hbm_gbs"] * 1e9)
     # the ncu summaries cover the bf16 GEMM only
-    traffic = profiled_traffic(f"gate_up_gemm_{args.workload}.md") if w8 is None else None
-    kname = "grouped_gemm_fp8 (gate_up)" if w8 is not None else "grouped_gemm (gate_up)"
+    traffic = profiled_traffic(f"gate_up_gemm_{args.workload}.md") if not quant else None
+    kname = ("grouped_gemm_fp8 (gate_up)" if w8 is not None else
+             "grouped_gemm_nvfp4 (gate_up)" if w4 is not None else "grouped_gemm (gate_up)")
     # an e4m3 contraction's peak: the measured bf16 peak times the nominal fp8 / bf16 ratio (2)
     tc_peak = peaks["bf16_tflops_sustained"] * (2 if w8 is not None else 1)
     tc_src = (f"{peaks['source']} bf16_tflops_sustained x 2 (nominal e4m3 / bf16 ratio)" if w8 is not None
@@ -462,7 +477,9 @@ def run_gpu(args):
         "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 expert weights and GEMM inputs, bf16 LoRA" if w8 is not None else "bf16", "data": "synthetic",
+        "dtype": ("e4m3 expert weights and GEMM inputs, bf16 LoRA" if w8 is not None else
+                  "NVFP4 (e2m1, e4m3 per 16 values) expert weights and GEMM inputs, f16 tensor-core products, "
+                  "bf16 LoRA" if w4 is not None else "bf16"), "data": "synthetic",
         "config": {
             "workload": cfg.describe(), "T": T, "H": H, "I": I, "E": E, "top_k": k,
             "lora_ranks": list(cfg.ranks), "routing": "DeepSeekV3" if cfg.method else "Renormalize",
@@ -524,7 +541,7 @@ def run_gpu(args):
             line.setdefault("stage_us", {})[label] = st_ms
     # the other BASELINE configurations, one after another on the same GPU (rank 0 of a
     # single-GPU run only: replicas would repeat the same numbers), each freed before the next
-    side = [] if (w8 is not None or world > 1 or args.workload != "decode" or args.no_workloads) else \
+    side = [] if (quant or world > 1 or args.workload != "decode" or args.no_workloads) else \
         [w for w in SIDE_WORKLOADS if args.only_workloads is None or w in args.only_workloads.split(",")]
     if side:
         del fwd, ws, out, bufs
@@ -534,7 +551,7 @@ def run_gpu(args):
         for name in side:
             line["workloads"][name] = measure_side_workload(name, args, h, local, peaks)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, inp, args, w8=w8)
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args, w8=w8, w4=w4)
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()
@@ -553,6 +570,11 @@ def _oracle_inputs(cfg, inp):
 
 def _oracle_call(cfg, o, tokens):
     from oracle import moe_lora_oracle as orc
+    if "w1nv" in o:   # NVFP4 expert weights
+        return orc.moe_lora_forward_nvfp4(o["hidden"], o["router_logits"], o["w1nv"], o["w2nv"], cfg.top_k,
+                                          cfg.method, o["correction_bias"], cfg.rsf, o["lora_A_gu"], o["lora_B_gu"],
+                                          o["lora_A_dn"], o["lora_B_dn"], o["slot_idx"], cfg.ranks, cfg.scalings,
+                                          tokens=tokens, shared_outer=cfg.shared_outer)
     if "w1q" in o:   # block-FP8 expert weights
         return orc.moe_lora_forward_fp8(o["hidden"], o["router_logits"], o["w1q"], o["w1s"], o["w2q"], o["w2s"],
                                         cfg.top_k, cfg.method, o["correction_bias"], cfg.rsf, o["lora_A_gu"],
@@ -564,17 +586,21 @@ def _oracle_call(cfg, o, tokens):
                                 shared_outer=cfg.shared_outer)
 
 
-def cpu_baseline(cfg, inp, args, budget_s: float = None, w8=None) -> dict:
+def cpu_baseline(cfg, inp, args, budget_s: float = None, w8=None, w4=None) -> dict:
     """Time the oracle, as it stands, on a bounded sample of the workload: a token subset
     that grows until one call takes a good part of the budget, then repeated calls until
     about `budget_s` seconds of CPU work are done (tokens/s over all of them).  With w8
-    (block-FP8 weights) the oracle's FP8 layer runs on those codes and scales."""
+    (block-FP8 weights) the oracle's FP8 layer runs on those codes and scales, with w4 (NVFP4
+    weights) its NVFP4 layer."""
     budget_s = args.cpu_budget if budget_s is None else budget_s
-    if w8 is not None:
+    if w8 is not None or w4 is not None:
         inp = {k_: v for k_, v in inp.items() if k_ not in ("w1", "w2")}
     o = _oracle_inputs(cfg, inp)
     if w8 is not None:
         o.update(w1q=w8[0].cpu().numpy(), w1s=w8[1].cpu().numpy(), w2q=w8[2].cpu().numpy(), w2s=w8[3].cpu().numpy())
+    if w4 is not None:
+        c = [t.cpu().numpy() for t in w4]
+        o.update(w1nv=tuple(c[:3]), w2nv=tuple(c[3:]))
     n_tok = min(cfg.T, 8)
     t0 = time.perf_counter()
     _oracle_call(cfg, o, np.arange(n_tok))
@@ -697,6 +723,9 @@ def main():
     ap.add_argument("--stage-times", action="store_true", help="add per-stage device times (us) to the line")
     ap.add_argument("--fp8", action="store_true",
                     help="block-FP8 expert weights (e4m3, 128x128 scales) quantised from the drawn bf16 ones")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="NVFP4 expert weights (e2m1, e4m3 scale per 16, float32 per expert) quantised from the "
+                         "drawn bf16 ones")
     ap.add_argument("--routed", choices=["finalize", "unfinalized"], default=None,
                     help="time the externally routed entry instead (auxiliary line, not the headline)")
     ap.add_argument("--no-workloads", action="store_true",
@@ -704,9 +733,11 @@ def main():
     ap.add_argument("--only-workloads", default=None,
                     help="comma-separated subset of the other configurations to time")
     args = ap.parse_args()
-    if args.fp8 and (args.routed or args.impl == "reference"):
-        ap.error("--fp8 times the FP8 layer through moe_lora_forward_fp8; it does not combine with "
-                 "--routed or --impl reference")
+    if (args.fp8 or args.nvfp4) and (args.routed or args.impl == "reference"):
+        ap.error("--fp8 / --nvfp4 time the quantised layers through moe_lora_forward_fp8 / _nvfp4; they do not "
+                 "combine with --routed or --impl reference")
+    if args.fp8 and args.nvfp4:
+        ap.error("choose one of --fp8 and --nvfp4")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

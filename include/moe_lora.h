@@ -286,6 +286,68 @@ moe_lora_status moe_lora_grouped_gemm_fp8(moe_lora_handle* h, const uint8_t* w, 
                                           const uint8_t* x, const float* x_scale, const int32_t* expert_offsets,
                                           int E, int N, int K, int P, float* out, moe_lora_stream stream);
 
+/* NVFP4 expert weights, as NVFP4 checkpoints store them (the pages' other target checkpoint:
+   sglang PR #27329, Optimizations, the Kimi-K2.5-NVFP4 target and its "modelopt_fp4"
+   quantisation).  Each weight is e2m1(code) * e4m3(block scale) * tensor scale: e2m1 codes
+   are the OCP FP4 E2M1 values (sign, 2 exponent bits with bias 1, 1 mantissa bit: 0, 0.5, 1,
+   1.5, 2, 3, 4, 6), two per byte with element 2i in the low nibble of byte i; one e4m3 block
+   scale (OCP E4M3 bit pattern) per 16 consecutive values along K; one float32 tensor scale
+   per expert.  Device pointers owned by the caller; codes 16-byte aligned, block scales and
+   tensor scales 4-byte aligned. */
+typedef struct {
+  const uint8_t* w1;        /* [E, 2I, H/2] packed codes: rows [0,I) gate, [I,2I) up          */
+  const uint8_t* w1_sf;     /* [E, 2I, H/16] e4m3 block scales                                */
+  const float* w1_gs;       /* [E] tensor scales                                              */
+  const uint8_t* w2;        /* [E, H, I/2] packed codes                                       */
+  const uint8_t* w2_sf;     /* [E, H, I/16]                                                   */
+  const float* w2_gs;       /* [E]                                                            */
+} moe_lora_nvfp4_weights;
+
+/* The layer of moe_lora_forward with NVFP4 expert weights `w` (a->w1 and a->w2 are not read).
+   The two base GEMMs read their inputs quantised to NVFP4 per row (per token: the permuted
+   hidden rows for the gate_up GEMM, the bf16 activation for the down GEMM), all float32
+   operations rounded to nearest:
+     g = max(amax_row, 1e-10) / 2688;  per 16 values s = e4m3(amax_16 / (6 g)) (nearest even,
+     saturated at 448);  q = e2m1(v / (s g)) (nearest even on the e2m1 grid, saturated at 6;
+     0 where s g is 0),
+   and each GEMM sums, in fp32, the exact products (q s) * (weight code * block scale), then
+   multiplies by g and the expert's tensor scale.  The LoRA weights and chain stay bf16 and read
+   the unquantised hidden rows and activation.  Every other rule (routing, rounding points,
+   slots, ranks, scalings, flags except MOE_LORA_FLAG_UNFUSED_LORA, which is implied) is that of
+   moe_lora_forward; the LoRA placement is the narrow one at every token count, with token
+   tiles of at most 64.  H must be a multiple of 128 and I of 64.  The workspace is
+   moe_lora_workspace_size() of the same shape.  Errors: INVALID_ARG, UNSUPPORTED,
+   WORKSPACE_TOO_SMALL, CUDA. */
+moe_lora_status moe_lora_forward_nvfp4(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_nvfp4_weights* w,
+                                       moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
+                                       moe_lora_stream stream);
+
+/* The NVFP4 row quantisation of moe_lora_forward_nvfp4 on its own, for bf16 rows src (16-byte
+   aligned): row scales g [rows] float32, and any of the packed codes [rows, K/2] (element 2i
+   in the low nibble of byte i), the e4m3 block scales [rows, K/16] and the exact f16 values
+   q * s [rows, K] that the GEMMs read (each NULL to skip; codes and f16 values 16-byte aligned,
+   g 4-byte aligned).  With perm (the routing's permuted -> expanded map) output row q
+   quantises src row perm[q] / top_k, the permute and quant of the gate_up GEMM's input; with
+   perm NULL it quantises src row q.  K a multiple of 16 (of 32 with codes).  Errors:
+   INVALID_ARG, CUDA. */
+moe_lora_status moe_lora_quant_nvfp4(moe_lora_handle* h, const moe_lora_bf16* src, const int32_t* perm, int rows,
+                                     int K, int top_k, float* g, uint8_t* codes, uint8_t* block_scales,
+                                     uint16_t* deq_f16, moe_lora_stream stream);
+
+/* The NVFP4 grouped GEMM of moe_lora_forward_nvfp4 on its own (its down GEMM: fp32 output, no
+   LoRA): for every expert e and its rows q in [expert_offsets[e], expert_offsets[e+1]),
+     out[q, n] = x_gs[q] * w_gs[e] * sum_k x[q, k] * e2m1(w[e*N + n, k]) * e4m3(w_sf[e*N + n, k/16])
+   with x [P, K] the f16 values of moe_lora_quant_nvfp4 (16-byte aligned), w [E, N, K/2] packed
+   codes (16-byte aligned), w_sf [E, N, K/16] e4m3 block scales and w_gs [E], x_gs [P] float32
+   (4-byte aligned), expert_offsets [E + 1] int32 (non-decreasing, offsets[E] = P), out [P, N]
+   float32 (16-byte aligned).  The products are exact; the tensor cores sum them in fp32.  N a
+   multiple of 128, K of 64, P >= 0.  Rows of no expert are not written.  Errors: INVALID_ARG,
+   UNSUPPORTED, CUDA. */
+moe_lora_status moe_lora_grouped_gemm_nvfp4(moe_lora_handle* h, const uint8_t* w, const uint8_t* w_sf,
+                                            const float* w_gs, const uint16_t* x, const float* x_gs,
+                                            const int32_t* expert_offsets, int E, int N, int K, int P, float* out,
+                                            moe_lora_stream stream);
+
 /* Routing + expert alignment that allocates nothing and takes no workspace or handle.
    The pages have no counterpart to this call; it exists for callers that cannot call
    cudaMalloc or supply a workspace (plug-ins inside a host framework that owns all device

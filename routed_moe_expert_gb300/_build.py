@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoelora.so")
 SOURCES = ["moe_lora.cu", "route_align.cu", "grouped_gemm.cu", "gemm_fp8.cu", "elementwise.cu", "lora.cu", "route_noalloc.cu",
-           "lora_tc.cu", "permute_shrink.cu"]
+           "lora_tc.cu", "permute_shrink.cu", "nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

@@ -36,7 +36,8 @@ NUM_STAGES = len(STAGES)
 EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "moe_lora_last_cuda_error",
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
             "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed",
-            "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8", "moe_lora_grouped_gemm_fp8"]
+            "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8", "moe_lora_grouped_gemm_fp8",
+            "moe_lora_forward_nvfp4", "moe_lora_quant_nvfp4", "moe_lora_grouped_gemm_nvfp4"]
 
 
 class MoELoRAError(RuntimeError):
@@ -81,6 +82,11 @@ class Fp8Weights(ctypes.Structure):
     _fields_ = [("w1", c_void_p), ("w1_scale", c_void_p), ("w2", c_void_p), ("w2_scale", c_void_p)]
 
 
+class Nvfp4Weights(ctypes.Structure):
+    _fields_ = [("w1", c_void_p), ("w1_sf", c_void_p), ("w1_gs", c_void_p), ("w2", c_void_p), ("w2_sf", c_void_p),
+                ("w2_gs", c_void_p)]
+
+
 _lib = None
 
 
@@ -114,6 +120,12 @@ def lib() -> ctypes.CDLL:
     L.moe_lora_quant_fp8.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
     L.moe_lora_grouped_gemm_fp8.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                             c_int, c_int, c_void_p, c_void_p]
+    L.moe_lora_forward_nvfp4.argtypes = [c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Nvfp4Weights), c_void_p,
+                                         c_void_p, c_size_t, c_void_p]
+    L.moe_lora_quant_nvfp4.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                                       c_void_p, c_void_p, c_void_p]
+    L.moe_lora_grouped_gemm_nvfp4.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                              c_int, c_int, c_int, c_int, c_void_p, c_void_p]
     for name in EXPORTED:
         if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
             getattr(L, name).restype = c_int
@@ -235,9 +247,10 @@ def moe_lora_permute(handle: Handle, hidden: torch.Tensor, perm: torch.Tensor, t
 
 def check_shapes(hidden, router_logits, w1, w2, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None,
                  lora_B_dn=None, slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (),
-                 flags=0, num_experts=None, correction_bias=None):
+                 flags=0, num_experts=None, correction_bias=None, packed_k=False):
     """Raise ValueError unless every tensor has the shape the C ABI reads through its pointer:
-    hidden [T, H], router_logits [T, E], w1 [E, 2I, H], w2 [E, H, I] and, with adapters,
+    hidden [T, H], router_logits [T, E], w1 [E, 2I, H], w2 [E, H, I] (with packed_k, two values
+    per byte along K: w1 [E, 2I, H/2], w2 [E, H, I/2]) and, with adapters,
     lora_A_gu [S, E', R, H], lora_B_gu [S, E, 2I, R], lora_A_dn [S, E, R, I],
     lora_B_dn [S, E', H, R] (E' = 1 with FLAG_SHARED_OUTER, else E) and slot_idx [T].
     The library takes raw pointers and cannot check these itself."""
@@ -253,8 +266,17 @@ def check_shapes(hidden, router_logits, w1, w2, lora_A_gu=None, lora_B_gu=None, 
     if twoI % 2:
         raise ValueError(f"w1's second dimension (2I) must be even, got {twoI}")
     I = twoI // 2
-    need(w1, (E, twoI, H), "w1")
-    need(w2, (E, H, I), "w2")
+    if packed_k:
+        if H % 2:
+            raise ValueError(f"H must be even, got {H}")
+        need(w1, (E, twoI, H // 2), "w1")
+        if w2.dim() != 3 or w2.shape[:2] != (E, H):
+            raise ValueError(f"w2 must have shape ({E}, {H}, I/2), got {tuple(w2.shape)}")
+        if w2.shape[2] * 2 != I:
+            raise ValueError(f"w2's last dimension must be I/2 = {I // 2}, got {w2.shape[2]}")
+    else:
+        need(w1, (E, twoI, H), "w1")
+        need(w2, (E, H, I), "w2")
     if router_logits is not None:
         need(router_logits, (T, num_experts if num_experts is not None else E), "router_logits")
     if correction_bias is not None:
@@ -281,10 +303,10 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
               routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
               slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (), flags=0,
               outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1,
-              weight_dtype=torch.bfloat16):
+              weight_dtype=torch.bfloat16, packed_k=False):
     """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
     check_shapes(hidden, router_logits, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
-                 scalings, flags, correction_bias=correction_bias)
+                 scalings, flags, correction_bias=correction_bias, packed_k=packed_k)
     T, H = hidden.shape
     E, twoI, _ = w1.shape
     S = len(ranks)
@@ -469,6 +491,102 @@ def moe_lora_grouped_gemm_fp8(handle: Handle, w_q: torch.Tensor, w_scale: torch.
                                          _ptr(expert_offsets, torch.int32, "expert_offsets"), E, N, K, P,
                                          _ptr(out, torch.float32, "out"), _stream(stream))
     _check(st, "moe_lora_grouped_gemm_fp8")
+    return out
+
+
+def check_nvfp4_weights(w1_q, w1_sf, w1_gs, w2_q, w2_sf, w2_gs):
+    """Raise ValueError unless the NVFP4 weights have the shapes the C ABI reads: packed codes
+    w1_q [E, 2I, H/2] and w2_q [E, H, I/2] (uint8), block scales w1_sf [E, 2I, H/16] and
+    w2_sf [E, H, I/16] (uint8 e4m3 bit patterns), tensor scales w1_gs and w2_gs [E] (float32);
+    H a multiple of 128, I of 64."""
+    if w1_q.dim() != 3 or w2_q.dim() != 3:
+        raise ValueError("w1_q must be [E, 2I, H/2] and w2_q [E, H, I/2]")
+    E, twoI, H2 = w1_q.shape
+    H, I = 2 * H2, twoI // 2
+    if H % 128 or I % 64 or twoI % 2:
+        raise ValueError(f"H must be a multiple of 128 and I of 64, got H={H}, I={I}")
+    for t, shape, name in ((w2_q, (E, H, I // 2), "w2_q"), (w1_sf, (E, twoI, H // 16), "w1_sf"),
+                           (w2_sf, (E, H, I // 16), "w2_sf"), (w1_gs, (E,), "w1_gs"), (w2_gs, (E,), "w2_gs")):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+
+
+def moe_lora_forward_nvfp4(handle: Handle, hidden, router_logits, w1_q, w1_sf, w1_gs, w2_q, w2_sf, w2_gs, top_k,
+                           routing_method=0, correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None,
+                           lora_B_gu=None, lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(),
+                           flags=0, out=None, workspace=None, outputs=None, prof_events=None, stream=None,
+                           n_group=1, topk_group=1) -> torch.Tensor:
+    """The layer with NVFP4 expert weights: packed e2m1 codes w1_q [E, 2I, H/2] and
+    w2_q [E, H, I/2] (uint8, element 2i in the low nibble of byte i), e4m3 block scales
+    w1_sf [E, 2I, H/16] and w2_sf [E, H, I/16] (uint8 bit patterns), float32 tensor scales
+    w1_gs and w2_gs [E].  Returns out [T, H] bf16."""
+    check_nvfp4_weights(w1_q, w1_sf, w1_gs, w2_q, w2_sf, w2_gs)
+    a, keep = make_args(hidden, router_logits, w1_q, w2_q, top_k, routing_method, correction_bias,
+                        routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
+                        scalings, flags, outputs, prof_events, n_group, topk_group, weight_dtype=torch.uint8,
+                        packed_k=True)
+    w = Nvfp4Weights()
+    w.w1 = _ptr(w1_q, torch.uint8, "w1_q")
+    w.w1_sf = _ptr(w1_sf, torch.uint8, "w1_sf")
+    w.w1_gs = _ptr(w1_gs, torch.float32, "w1_gs")
+    w.w2 = _ptr(w2_q, torch.uint8, "w2_q")
+    w.w2_sf = _ptr(w2_sf, torch.uint8, "w2_sf")
+    w.w2_gs = _ptr(w2_gs, torch.float32, "w2_gs")
+    if out is None:
+        out = torch.empty((a.T, a.H), dtype=torch.bfloat16, device=hidden.device)
+    if workspace is None:
+        workspace = alloc_workspace(a.T, a.H, a.I, a.E, a.top_k, a.S, a.R, device=hidden.device)
+    st = lib().moe_lora_forward_nvfp4(handle.ptr, ctypes.byref(a), ctypes.byref(w), _ptr(out, torch.bfloat16, "out"),
+                                      _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "moe_lora_forward_nvfp4")
+    del keep
+    return out
+
+
+def moe_lora_quant_nvfp4(handle: Handle, src: torch.Tensor, perm: Optional[torch.Tensor] = None, top_k: int = 1,
+                         stream=None):
+    """NVFP4 row quantisation of bf16 rows src [T, K]: returns (g [rows] float32 row scales,
+    codes [rows, K/2] uint8 packed e2m1, block_scales [rows, K/16] uint8 e4m3 bit patterns,
+    deq [rows, K] float16 = e2m1 * block scale, the values the GEMMs read).  With perm
+    [T*top_k], output row q quantises src row perm[q] // top_k (rows = T*top_k); without it
+    rows = T."""
+    T, K = src.shape
+    rows = perm.numel() if perm is not None else T
+    dev = src.device
+    g = torch.empty((rows,), dtype=torch.float32, device=dev)
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty((rows, K // 16), dtype=torch.uint8, device=dev)
+    deq = torch.empty((rows, K), dtype=torch.float16, device=dev)
+    st = lib().moe_lora_quant_nvfp4(handle.ptr, _ptr(src, torch.bfloat16, "src"), _ptr(perm, torch.int32, "perm"),
+                                    rows, K, int(top_k), _ptr(g, torch.float32), _ptr(codes, torch.uint8),
+                                    _ptr(sf, torch.uint8), _ptr(deq, torch.float16), _stream(stream))
+    _check(st, "moe_lora_quant_nvfp4")
+    return g, codes, sf, deq
+
+
+def moe_lora_grouped_gemm_nvfp4(handle: Handle, w_q: torch.Tensor, w_sf: torch.Tensor, w_gs: torch.Tensor,
+                                x: torch.Tensor, x_gs: torch.Tensor, expert_offsets: torch.Tensor,
+                                stream=None) -> torch.Tensor:
+    """The NVFP4 grouped GEMM on its own: packed codes w_q [E, N, K/2], block scales
+    w_sf [E, N, K/16] (uint8), tensor scales w_gs [E] and row scales x_gs [P] (float32),
+    inputs x [P, K] float16 (the exact values of moe_lora_quant_nvfp4), expert_offsets [E + 1]
+    int32.  Returns out [P, N] float32 (rows outside every expert's range are left as zero)."""
+    if w_q.dim() != 3 or x.dim() != 2:
+        raise ValueError("w_q must be [E, N, K/2] and x [P, K]")
+    E, N, K2 = w_q.shape
+    K = 2 * K2
+    P = x.shape[0]
+    for t, shape, name in ((x, (P, K), "x"), (w_sf, (E, N, K // 16), "w_sf"), (w_gs, (E,), "w_gs"),
+                           (x_gs, (P,), "x_gs"), (expert_offsets, (E + 1,), "expert_offsets")):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    out = torch.zeros((P, N), dtype=torch.float32, device=w_q.device)
+    st = lib().moe_lora_grouped_gemm_nvfp4(handle.ptr, _ptr(w_q, torch.uint8, "w_q"), _ptr(w_sf, torch.uint8, "w_sf"),
+                                           _ptr(w_gs, torch.float32, "w_gs"), _ptr(x, torch.float16, "x"),
+                                           _ptr(x_gs, torch.float32, "x_gs"),
+                                           _ptr(expert_offsets, torch.int32, "expert_offsets"), E, N, K, P,
+                                           _ptr(out, torch.float32, "out"), _stream(stream))
+    _check(st, "moe_lora_grouped_gemm_nvfp4")
     return out
 
 

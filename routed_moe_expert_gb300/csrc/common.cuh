@@ -131,6 +131,10 @@ MLDEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// Register `bytes` more of the current phase's transaction count without arriving.
+MLDEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
 MLDEV void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -154,6 +158,35 @@ MLDEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, u
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      record_status(status, kDevTimeout, where);
+      return false;
+    }
+  }
+}
+
+// mbar_wait for threads that have nothing else to issue: each try_wait suspends the thread
+// for up to `hint_ns` until the phase completes, so waiting warps take no issue slots from
+// the warps that share their scheduler.  Same bound and error behaviour as mbar_wait.
+MLDEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+MLDEV bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* status,
+                           uint32_t where, uint32_t hint_ns = 20000) {
+  if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;

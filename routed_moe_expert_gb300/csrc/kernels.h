@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace mlk {
@@ -141,6 +142,48 @@ cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, in
 cudaError_t launch_quant_fp8(const __nv_bfloat16* src, const int32_t* perm, int k, int P, int K, uint8_t* codes,
                              float* scale, cudaStream_t stream, bool pdl = false,
                              const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr);
+
+// ---------------------------------------------------------------- NVFP4 path
+// NVFP4 grouped GEMM: the weights are e2m1 codes (two per byte, element 2i in the low nibble)
+// with an e4m3 scale per 16 values along K and a float32 scale per expert; the inputs are f16
+// rows holding e2m1 * e4m3 values exactly (the NVFP4 quantisation of each row without its
+// float32 row scale), with that row scale apart.  Per expert e and its rows q:
+//   out[q, col] = x_gs[q] * w_gs[e] * sum_k X[q, k] * e2m1(W[e*N + n, k]) * e4m3(SF[e*N + n, k/16])
+// with n = row(col) (gated as in GemmParams).  N a multiple of 128, K of 64; token tiles of
+// 16, 32 or 64.
+struct GemmNv4Params {
+  CUtensorMap tmap_w;            // packed codes [E*N rows, K/2 bytes], box {128, 64}, 128-byte swizzle
+  CUtensorMap tmap_x;            // f16 inputs [P rows, K cols], box {64, BN}, 128-byte swizzle
+  const uint8_t* w_sf;           // [E, N, K/16] e4m3 block scales
+  const float* w_gs;             // [E] expert scales
+  const float* x_gs;             // [P] row scales of the inputs
+  __nv_bfloat16* out;            // [P, N] bf16 output, or
+  float* out_f32;                //   fp32 output when non-null
+  const int32_t* offsets;        // [E + 1]
+  uint32_t* status;
+  int E, N, K, P, gated;
+  int stages;                    // f16 weight-tile stages
+  int rstages;                   // raw stages (codes and token rows)
+  // Optional down-LoRA expand in the epilogue (as GemmParams' lora_v path)
+  const float* lora_v;           // [P, R] or null
+  const __nv_bfloat16* lora_B;   // [S, E, N, R], or [S, 1, N, R] with lora_b_e1
+  int lora_b_e1;
+  const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
+  LoraSlots slots;
+};
+int gemm_nvfp4_smem_bytes(int bn, int stages, int rstages, int E, int lora_R);
+int gemm_nvfp4_stage_bytes(int bn);    // one f16 weight tile
+int gemm_nvfp4_rstage_bytes(int bn);   // one raw stage: codes then the token rows
+constexpr int kNv4RawBlocks = 4;                // 64-wide K blocks per raw stage
+constexpr int kNv4RawStageBytes = 128 * 32 * kNv4RawBlocks;   // 128 weight rows x 256 e2m1 codes
+cudaError_t launch_grouped_gemm_nvfp4(const GemmNv4Params& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
+// NVFP4 quantisation of rows (row q from src row perm[q] / k, or q without perm): per row
+//   g = max(amax, 1e-10) / 2688, per 16 values s = e4m3(amax_16 / (6 g)), q = e2m1(v / (s g))
+// (float32 operations, round to nearest even, saturating).  Writes the row scale g[q] and any
+// of: deq [P, K] f16 = q * s (exact), codes [P, K/2] (packed), sf [P, K/16] (e4m3 codes).
+cudaError_t launch_quant_nvfp4(const __nv_bfloat16* src, const int32_t* perm, int k, int P, int K, float* g,
+                               __half* deq, uint8_t* codes, uint8_t* sf, cudaStream_t stream, bool pdl = false,
+                               const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr);
 
 
 struct FinalizeParams {

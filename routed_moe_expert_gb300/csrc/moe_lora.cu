@@ -393,6 +393,45 @@ moe_lora_status enqueue_gemm_fp8(moe_lora_handle* h, GemmF8Params& gp, const uin
   return MOE_LORA_OK;
 }
 
+// The NVFP4 grouped GEMM: packed codes W [E*N, K/2], f16 inputs X [P, K], token tiles of bn
+// (16..64).  Five f16 weight-tile stages; the rest of the budget goes to raw stages (codes and
+// token rows), the kernel's bytes in flight.
+moe_lora_status enqueue_gemm_nvfp4(moe_lora_handle* h, GemmNv4Params& gp, const uint8_t* W, const __half* X, int P,
+                                   int bn, cudaStream_t stream, bool pdl) {
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(gp.K / 2), static_cast<cuuint64_t>(gp.E) * gp.N};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(gp.K / 2)};
+    cuuint32_t box[2] = {128, 64};
+    cuuint32_t estr[2] = {1, 1};
+    if (h->encode(&gp.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_LORA_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(gp.K), static_cast<cuuint64_t>(P)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(gp.K) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bn)};
+    cuuint32_t estr[2] = {1, 1};
+    if (h->encode(&gp.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(X), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MOE_LORA_ERR_CUDA;
+  }
+  const int lora_R = gp.lora_v != nullptr ? gp.slots.R : 0;
+  // (the weight stream is a quarter of the bf16 GEMM's: the kernel is short, and the whole
+  // shared memory serves its rings even beside the side-stream LoRA kernel)
+  const int budget = kMaxGemmSmem;
+  gp.stages = 5;
+  int rs = (budget - gemm_nvfp4_smem_bytes(bn, gp.stages, 0, gp.E, lora_R)) / (gemm_nvfp4_rstage_bytes(bn) + 16);
+  if (rs > 8) rs = 8;
+  if (rs < 2) return MOE_LORA_ERR_UNSUPPORTED;
+  gp.rstages = rs;
+  gp.P = P;
+  ML_LAUNCH(h, launch_grouped_gemm_nvfp4(gp, bn, h->num_sms, stream, pdl), "grouped_gemm_nvfp4 launch");
+  return MOE_LORA_OK;
+}
+
 LoraSlots make_slots(const moe_lora_args* a) {
   LoraSlots L;
   std::memset(&L, 0, sizeof(L));
@@ -509,7 +548,8 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
                                           int32_t* pair_slot, __nv_bfloat16* ub, const LoraSlots& slots,
                                           uint32_t* status, cudaStream_t stream,
                                           const moe_lora_fp8_weights* f8 = nullptr,
-                                          const __nv_bfloat16** dn_delta = nullptr) {
+                                          const __nv_bfloat16** dn_delta = nullptr,
+                                          const moe_lora_nvfp4_weights* f4 = nullptr) {
   (void)ids;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const int P = T * k;
@@ -523,9 +563,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   // bf16 delta: the pages round the gate_up GEMM output and the delta to bf16 separately,
   // and adding the delta inside the accumulator would round their sum once instead.
   // At 16-token tiles (decode) the epilogue expand costs less than an extra K-stage.
-  // FP8 weights: token tiles of at most 64 and the down expand in the GEMM's epilogue
-  const int bn = f8 != nullptr ? std::min(pick_bn(P, E), 64) : pick_bn(P, E);
-  const bool fused = f8 == nullptr && lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && bn >= 32 &&
+  // FP8 and NVFP4 weights: token tiles of at most 64 and the down expand in the GEMM's epilogue
+  const bool q8 = f8 != nullptr || f4 != nullptr;
+  const int bn = q8 ? std::min(pick_bn(P, E), 64) : pick_bn(P, E);
+  const bool fused = !q8 && lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && bn >= 32 &&
                      !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
   // FP8 GEMM inputs: the permuted hidden codes in the xp region, the activation codes in
   // the g region (written after the activation has read g), and their group scales
@@ -533,6 +574,10 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   uint8_t* a8 = reinterpret_cast<uint8_t*>(g);
   float* sx = reinterpret_cast<float*>(ws + L.sx);
   float* sa = reinterpret_cast<float*>(ws + L.sa);
+  // NVFP4 GEMM inputs: the exact f16 values of the quantised permuted hidden rows in the xp
+  // region, of the quantised activation in the g region; their row scales in sx and sa
+  __half* xq4 = reinterpret_cast<__half*>(xp);
+  __half* aq4 = reinterpret_cast<__half*>(g);
   const bool fused_gu = false;
   // 32-pair LoRA tiles when experts carry many pairs and the staged rows fit in smem
   const int lora_ntl = (P >= 32 * E && lora_smem_bytes(4, R, 2 * I, true, E) <= 200 * 1024) ? 4 : 1;
@@ -598,13 +643,17 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
   // The down LoRA beside the down GEMM (flag): shrink and expand in one kernel on the side
   // stream, into a bf16 delta per pair that the finalize adds; the activation runs alone.
-  const bool dn_side = lora && two && !fused && f8 == nullptr && (a->flags & MOE_LORA_FLAG_DOWN_LORA_SIDE);
+  const bool dn_side = lora && two && !fused && !q8 && (a->flags & MOE_LORA_FLAG_DOWN_LORA_SIDE);
   // the pairs' adapter slots ride along with the permute for the activation + down shrink
   const bool act_shrink = lora && !fused && !fused_gu && !dn_side;
   if (f8 != nullptr) {   // permute and quantise in one pass
     ML_LAUNCH(h, launch_quant_fp8(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, k, P, H, xp8, sx, stream,
                                   pdl, a->slot_idx, act_shrink ? pair_slot : nullptr),
               "permute + quant launch");
+  } else if (f4 != nullptr) {   // permute and NVFP4-quantise in one pass
+    ML_LAUNCH(h, launch_quant_nvfp4(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, k, P, H, sx, xq4, nullptr,
+                                    nullptr, stream, pdl, a->slot_idx, act_shrink ? pair_slot : nullptr),
+              "permute + NVFP4 quant launch");
   } else {
     ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
                                 a->slot_idx, act_shrink ? pair_slot : nullptr),
@@ -640,6 +689,20 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
     gq.K = H;
     gq.gated = 1;
     st = enqueue_gemm_fp8(h, gq, f8->w1, xp8, P, bn, stream, pdl);
+  } else if (f4 != nullptr) {
+    GemmNv4Params gq;
+    std::memset(&gq, 0, sizeof(gq));
+    gq.w_sf = f4->w1_sf;
+    gq.w_gs = f4->w1_gs;
+    gq.x_gs = sx;
+    gq.out = g;
+    gq.offsets = offsets;
+    gq.status = status;
+    gq.E = E;
+    gq.N = 2 * I;
+    gq.K = H;
+    gq.gated = 1;
+    st = enqueue_gemm_nvfp4(h, gq, f4->w1, xq4, P, bn, stream, pdl);
   } else {
     st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl && !(fused_gu && two));
   }
@@ -762,8 +825,9 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   // the epilogue's staged LoRA rows grow with the tile: narrow it until two stages fit
   int bn_dn = bn;
   while (!fused && lora && !dn_side && bn_dn > 16 &&
-         (f8 != nullptr ? gemm_fp8_smem_bytes(bn_dn, 2, E, R) : gemm_smem_bytes(bn_dn, 1, 2, E, R, 0, 1)) >
-             kMaxGemmSmem)
+         (f8 != nullptr   ? gemm_fp8_smem_bytes(bn_dn, 2, E, R)
+          : f4 != nullptr ? gemm_nvfp4_smem_bytes(bn_dn, 5, 2, E, R)
+                          : gemm_smem_bytes(bn_dn, 1, 2, E, R, 0, 1)) > kMaxGemmSmem)
     bn_dn >>= 1;
   if (f8 != nullptr) {   // the activation's group quantisation, then the FP8 down GEMM
     ML_LAUNCH(h, launch_quant_fp8(act, nullptr, 1, P, I, a8, sa, stream, pdl), "activation quant launch");
@@ -786,6 +850,33 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
       dq.slots = slots;
     }
     st = enqueue_gemm_fp8(h, dq, f8->w2, a8, P, bn_dn, stream, pdl);
+    if (st != MOE_LORA_OK) return st;
+    prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+    return MOE_LORA_OK;
+  }
+  if (f4 != nullptr) {   // the activation's NVFP4 quantisation, then the NVFP4 down GEMM
+    ML_LAUNCH(h, launch_quant_nvfp4(act, nullptr, 1, P, I, sa, aq4, nullptr, nullptr, stream, pdl),
+              "activation NVFP4 quant launch");
+    GemmNv4Params dq;
+    std::memset(&dq, 0, sizeof(dq));
+    dq.w_sf = f4->w2_sf;
+    dq.w_gs = f4->w2_gs;
+    dq.x_gs = sa;
+    dq.out_f32 = y;
+    dq.offsets = offsets;
+    dq.status = status;
+    dq.E = E;
+    dq.N = H;
+    dq.K = I;
+    dq.gated = 0;
+    if (lora) {
+      dq.lora_v = v;
+      dq.lora_B = reinterpret_cast<const __nv_bfloat16*>(a->lora_B_dn);
+      dq.lora_b_e1 = so ? 1 : 0;
+      dq.pair_slot = pair_slot;
+      dq.slots = slots;
+    }
+    st = enqueue_gemm_nvfp4(h, dq, f4->w2, aq4, P, bn_dn, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
     return MOE_LORA_OK;
@@ -847,7 +938,7 @@ namespace {
 // comes packed and the output may stay unfinalized).  Arguments are validated.
 moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_routed* ext,
                              moe_lora_bf16* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                             const moe_lora_fp8_weights* f8 = nullptr) {
+                             const moe_lora_fp8_weights* f8 = nullptr, const moe_lora_nvfp4_weights* f4 = nullptr) {
   moe_lora_status st = MOE_LORA_OK;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   const bool lora = lora_active(a);
@@ -904,7 +995,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
   const int bn0 = pick_bn(P, E);
   const bool fuse_all = lora && (R % 8 == 0) && a->S <= kMaxFusedSlots && a->S * R <= 256 && bn0 >= 32 &&
                         !(a->flags & MOE_LORA_FLAG_UNFUSED_LORA);
-  const bool act_in_gemm = f8 == nullptr && (fuse_all || (!lora && bn0 >= 32));
+  const bool act_in_gemm = f8 == nullptr && f4 == nullptr && (fuse_all || (!lora && bn0 >= 32));
   const bool y_bf16 = act_in_gemm && finalize && bn0 >= kBf16YMinBn;
   const __nv_bfloat16* dn_delta = nullptr;   // the down-LoRA delta computed beside the down GEMM
   if (act_in_gemm) {
@@ -993,7 +1084,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
   } else {
     st = enqueue_unfused_lora_path(h, a, lora, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub,
-                                   slots, status, stream, f8, &dn_delta);
+                                   slots, status, stream, f8, &dn_delta, f4);
     if (st != MOE_LORA_OK) return st;
   }
 
@@ -1124,6 +1215,70 @@ moe_lora_status moe_lora_grouped_gemm_fp8(moe_lora_handle* h, const uint8_t* w, 
   gq.K = K;
   gq.gated = 0;
   return enqueue_gemm_fp8(h, gq, w, x, P, std::min(pick_bn(P, E), 64), stream, false);
+}
+
+moe_lora_status moe_lora_forward_nvfp4(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_nvfp4_weights* w,
+                                       moe_lora_bf16* out, void* workspace, size_t workspace_bytes,
+                                       moe_lora_stream stream) {
+  if (a == nullptr || w == nullptr || h == nullptr || workspace == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  // a->w1 / a->w2 are not read: check the rest with the packed codes in their place
+  moe_lora_args b = *a;
+  b.w1 = reinterpret_cast<const moe_lora_bf16*>(w->w1);
+  b.w2 = reinterpret_cast<const moe_lora_bf16*>(w->w2);
+  b.flags |= MOE_LORA_FLAG_UNFUSED_LORA;
+  moe_lora_status st = moe_lora_validate(&b);
+  if (st != MOE_LORA_OK) return st;
+  if (b.H % 128 != 0 || b.I % 64 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (b.T > 0) {
+    if (out == nullptr || !aligned16(out)) return MOE_LORA_ERR_INVALID_ARG;
+    if (w->w1_sf == nullptr || w->w2_sf == nullptr || w->w1_gs == nullptr || w->w2_gs == nullptr ||
+        !aligned4(w->w1_sf) || !aligned4(w->w2_sf) || !aligned4(w->w1_gs) || !aligned4(w->w2_gs))
+      return MOE_LORA_ERR_INVALID_ARG;
+  }
+  return forward_impl(h, &b, nullptr, out, workspace, workspace_bytes, stream, nullptr, w);
+}
+
+moe_lora_status moe_lora_quant_nvfp4(moe_lora_handle* h, const moe_lora_bf16* src, const int32_t* perm, int rows,
+                                     int K, int top_k, float* g, uint8_t* codes, uint8_t* block_scales,
+                                     uint16_t* deq_f16, moe_lora_stream stream) {
+  if (h == nullptr || rows < 0 || K < 16 || K % 16 != 0 || K > 65536) return MOE_LORA_ERR_INVALID_ARG;
+  if (codes != nullptr && K % 32 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (perm != nullptr && top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_LORA_OK;
+  if (src == nullptr || g == nullptr || !aligned16(src) || !aligned4(g) || (perm != nullptr && !aligned4(perm)) ||
+      (codes != nullptr && !aligned16(codes)) || (deq_f16 != nullptr && !aligned16(deq_f16)))
+    return MOE_LORA_ERR_INVALID_ARG;
+  ML_LAUNCH(h, launch_quant_nvfp4(reinterpret_cast<const __nv_bfloat16*>(src), perm, perm != nullptr ? top_k : 1, rows,
+                                  K, g, reinterpret_cast<__half*>(deq_f16), codes, block_scales, stream),
+            "NVFP4 quant launch");
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_grouped_gemm_nvfp4(moe_lora_handle* h, const uint8_t* w, const uint8_t* w_sf,
+                                            const float* w_gs, const uint16_t* x, const float* x_gs,
+                                            const int32_t* expert_offsets, int E, int N, int K, int P, float* out,
+                                            moe_lora_stream stream) {
+  if (h == nullptr || E < 1 || E > kMaxExperts || N < 128 || N % 128 != 0 || K < 64 || K % 64 != 0 || P < 0 ||
+      N > 65536 || K > 65536)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (static_cast<long long>(E) * N > 0x7fffffffLL) return MOE_LORA_ERR_INVALID_ARG;
+  if (P == 0) return MOE_LORA_OK;
+  if (!w || !w_sf || !w_gs || !x || !x_gs || !expert_offsets || !out || !aligned16(w) || !aligned16(x) ||
+      !aligned16(out) || !aligned4(w_sf) || !aligned4(w_gs) || !aligned4(x_gs) || !aligned4(expert_offsets))
+    return MOE_LORA_ERR_INVALID_ARG;
+  GemmNv4Params gq;
+  std::memset(&gq, 0, sizeof(gq));
+  gq.w_sf = w_sf;
+  gq.w_gs = w_gs;
+  gq.x_gs = x_gs;
+  gq.out_f32 = out;
+  gq.offsets = expert_offsets;
+  gq.E = E;
+  gq.N = N;
+  gq.K = K;
+  gq.gated = 0;
+  return enqueue_gemm_nvfp4(h, gq, w, reinterpret_cast<const __half*>(x), P, std::min(pick_bn(P, E), 64), stream,
+                            false);
 }
 
 moe_lora_status moe_lora_launch_count(const moe_lora_handle* h, uint64_t* count) {

@@ -130,3 +130,59 @@ def nvfp4_dense_check(orc_mod, seed):
 @pytest.mark.parametrize("seed", [0, 1])
 def test_nvfp4_layer_matches_dense_bruteforce(seed):
     assert nvfp4_dense_check(orc, seed)
+
+
+def test_nvfp4_tolerance_covers_rounding_flips():
+    """Derivation of the NVFP4 parity bounds (gpu_helpers: ten times the bf16 elementwise
+    bounds, five times its relative L2 bound).  The NVFP4 GEMMs' products are exact and their
+    sums fp32; model those sums' rounding by the probabilistic bound of a K-term sum,
+    NVFP4_LAMBDA * sqrt(K) * 2^-24 times its sum of |terms|, and plant errors of that size
+    (uniform within it) on the gate_up sums before their bf16 rounding, in a copy of the
+    oracle.  The bf16 layer then stays inside the bf16 bounds.  The NVFP4 layer moves much
+    further, because both of its GEMM inputs are re-quantised to e2m1: a one-ulp bf16 change
+    of a gate_up value, or of a row's largest activation (its row scale), moves codes by a
+    whole e2m1 step.  It leaves the bf16 bounds and stays inside the NVFP4 ones."""
+    import types
+    import os
+    import gpu_helpers as gh
+
+    src = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "moe_lora_oracle.py")).read()
+    anchor = "g = round_bf16(xg @ W1.T)"
+    assert src.count(anchor) == 1
+    noisy = types.ModuleType("oracle_noisy")
+    noise = (f"g = round_bf16((xg @ W1.T) + {gh.NVFP4_LAMBDA} * np.sqrt(xg.shape[1]) * 2.0 ** -24"
+             " * (np.abs(xg) @ np.abs(W1).T) * _NOISE.uniform(-1.0, 1.0, (xg.shape[0], W1.shape[0])))")
+    exec(compile(src.replace(anchor, noise), "oracle_noisy", "exec"), noisy.__dict__)
+
+    def rel(a, b):
+        return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+    def within(got, ref, atol, rtol, rl):
+        return bool(np.all(np.abs(got - ref) <= atol + rtol * np.abs(ref))) and rel(got, ref) <= rl
+
+    cfgs = [wl.LayerConfig("n4a", T=40, H=256, I=256, E=8, top_k=2, ranks=(8, 16), scalings=(2.0, 0.5),
+                           slot_mode="uniform_none10"),
+            wl.LayerConfig("n4b", T=70, H=384, I=64, E=16, top_k=4, method=wl.DEEPSEEK_V3, bias_std=0.1, rsf=2.5,
+                           ranks=(16,), scalings=(1.0,))]
+    outside_bf16 = 0
+    for cfg in cfgs:
+        for seed in (11, 12):
+            inp = wl.make_inputs(cfg, seed=seed)
+            w1 = tuple(t.numpy() for t in wl.quantize_weights_nvfp4(inp["w1"]))
+            w2 = tuple(t.numpy() for t in wl.quantize_weights_nvfp4(inp["w2"]))
+            lora = (np_(inp["lora_A_gu"]), np_(inp["lora_B_gu"]), np_(inp["lora_A_dn"]), np_(inp["lora_B_dn"]),
+                    inp["slot_idx"].numpy(), inp["ranks"], inp["scalings"])
+            head = (np_(inp["hidden"]), np_(inp["router_logits"]))
+            tail = (cfg.top_k, inp["method"], np_(inp["correction_bias"]), inp["rsf"]) + lora
+            noisy._NOISE = np.random.default_rng(seed)
+            n4_noisy = noisy.moe_lora_forward_nvfp4(*head, w1, w2, *tail)["out"]
+            n4 = orc.moe_lora_forward_nvfp4(*head, w1, w2, *tail)["out"]
+            assert within(n4_noisy, n4, gh.ATOL_NVFP4, gh.RTOL_NVFP4, gh.REL_L2_NVFP4), (cfg.name, seed)
+            outside_bf16 += not within(n4_noisy, n4, gh.ATOL, gh.RTOL, gh.REL_L2)
+            W1 = np.stack([orc.dequant_weight_nvfp4(w1[0][e], w1[1][e], w1[2][e]) for e in range(cfg.E)])
+            W2 = np.stack([orc.dequant_weight_nvfp4(w2[0][e], w2[1][e], w2[2][e]) for e in range(cfg.E)])
+            noisy._NOISE = np.random.default_rng(seed)
+            b16_noisy = noisy.moe_lora_forward(*head, W1, W2, *tail)["out"]
+            b16 = orc.moe_lora_forward(*head, W1, W2, *tail)["out"]
+            assert within(b16_noisy, b16, gh.ATOL, gh.RTOL, gh.REL_L2), (cfg.name, seed)
+    assert outside_bf16 >= 2
