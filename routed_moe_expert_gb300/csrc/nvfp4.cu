@@ -532,6 +532,10 @@ cudaError_t launch_grouped_gemm_nvfp4(const GemmNv4Params& p, int bn, int grid, 
   if (p.stages < 2 || p.stages > kNv4MaxStages || p.rstages < 2 || p.rstages > kNv4MaxRStages || grid < 1)
     return cudaErrorInvalidValue;
   if (p.N % 128 != 0 || p.K % 64 != 0) return cudaErrorInvalidValue;
+  // The converter groups wait on the f16 stages' barriers by phase parity: a group may run up to
+  // G - 1 blocks ahead of the slowest, so fewer than G stages would let two waiters of one
+  // barrier be two phases apart.
+  if (p.stages < nv4_groups(bn)) return cudaErrorInvalidValue;
   const bool lora = p.lora_v != nullptr;
   switch (bn) {
     case 16: return lora ? launch_nv4_bn<16, true>(p, grid, stream, pdl) : launch_nv4_bn<16, false>(p, grid, stream, pdl);
