@@ -240,6 +240,13 @@ def _lora_off_ms(fwd, stream, steps, warmup, torch, pkg):
 
 
 def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
+    # The expand-ready LoRA B copies are made once, like the weights (a weight-load step of the
+    # library); the bf16 layer's fused LoRA stages read them.
+    packed = {}
+    if w8 is None and w4 is None and cfg.S > 0 and not args.per_slot_lora:
+        packed = dict(lora_B_gu_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_gu"], cfg.ranks, 1),
+                      lora_B_dn_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], cfg.ranks, 0))
+
     def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
         flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
         hid = g["hidden"] if hidden is None else hidden
@@ -253,7 +260,7 @@ def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
             return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw)
         if w4 is not None:
             return pkg.moe_lora_forward_nvfp4(h, hid, lg, *w4, k, **kw)
-        return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw)
+        return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw, **packed)
     return fwd
 
 
@@ -486,6 +493,8 @@ def run_gpu(args):
             "l2": f"inputs larger than L2: {touched} touched experts = {touched * w_bytes_expert / 1e9:.2f} GB of weights per step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "forward_flags": args.flags,
+            "lora_b": ("per slot" if (args.per_slot_lora or w8 is not None or w4 is not None)
+                       else "expand-ready copies (moe_lora_pack_lora_b, made once at set-up)"),
             "step_bytes": step_bytes, "step_flops": step_flops,
             "step_roofline_frac": max(step_bytes / (peaks["hbm_gbs"] * 1e9),
                                       step_flops / (tc_peak * 1e12)) / (agg["ms_per_step"] / 1e3),
@@ -720,6 +729,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--ref-steps", type=int, default=5)
     ap.add_argument("--flags", type=int, default=0, help="extra moe_lora_forward flags (e.g. 8: unfused LoRA)")
+    ap.add_argument("--per-slot-lora", action="store_true",
+                    help="no expand-ready LoRA B copies: the fused LoRA stages read B per slot")
     ap.add_argument("--stage-times", action="store_true", help="add per-stage device times (us) to the line")
     ap.add_argument("--fp8", action="store_true",
                     help="block-FP8 expert weights (e4m3, 128x128 scales) quantised from the drawn bf16 ones")

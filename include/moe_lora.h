@@ -117,6 +117,12 @@ typedef struct {
   /* Optional profiling: 2*MOE_LORA_NUM_STAGES cudaEvent_t handles (entries may be NULL);
      events 2i and 2i+1 are recorded around stage i on the stream that runs it. */
   void* const* prof_events;
+  /* Optional expand-ready copies of lora_B_gu and lora_B_dn made by moe_lora_pack_lora_b
+     (gated = 1 for lora_B_gu, 0 for lora_B_dn, E_b = 1 for a shared-outer lora_B_dn) from
+     the SAME h_ranks as this call's (a copy made for other ranks gives wrong results); NULL:
+     not given.  Used by the fused LoRA placement (see moe_lora_forward), 16-byte aligned. */
+  const moe_lora_bf16* lora_B_gu_packed;
+  const moe_lora_bf16* lora_B_dn_packed;
 } moe_lora_args;
 
 /* Create a handle on `device`: queries the device, creates the LoRA side stream and the
@@ -167,6 +173,28 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
                                  const int32_t* perm, int T, int H, int top_k,
                                  moe_lora_bf16* permuted, moe_lora_stream stream);
 
+/* Expand-ready copy of a stacked LoRA B for the fused LoRA K-stages of the expert GEMMs
+   (sglang PR #28466 section 1, the expand half of merged_experts_fused_moe_lora_add; the
+   pages keep B as [S, E, N, R] and reach it per slot).  B: [S, E_b, N, R] bf16 (lora_B_gu
+   with N = 2I and gated = 1, or lora_B_dn with N = H and gated = 0; E_b = E, or 1 for a
+   shared-outer lora_B_dn).  packed: [E_b * NT * 128, Rs] bf16, caller-owned, 16-byte
+   aligned, moe_lora_packed_lora_b_size() bytes, NT = N/128 (gated) or ceil(N/128); row
+   (e * NT + nt) * 128 + r is the weight row that row r of the GEMM's 128-row tile nt
+   multiplies (gated: gate row 64 nt + r for r < 64, up row N/2 + 64 nt + r - 64 above;
+   otherwise row 128 nt + r, zero past N), and its columns hold every slot side by side:
+   slot s's B[s, e, n, 0 .. ranks[s]) at columns [coff[s], coff[s] + ranks[s]), zero up to
+   coff[s+1] = coff[s] + ranks[s] rounded up to 16; Rs = coff[S].  Columns r >= ranks[s] of
+   B are never read.  A weight-load step: call it once when the adapters in the slots
+   change, with the ranks every later forward passes; the copy is then read by each forward
+   as full 128-byte rows (two per slot and row otherwise).  Enqueued on `stream`.
+   Errors: INVALID_ARG (sizes, ranks outside [0, R], all ranks 0, N not a multiple of 128
+   when gated, null or misaligned pointers), CUDA. */
+moe_lora_status moe_lora_packed_lora_b_size(int S, int E_b, int N, int R, int gated, const int32_t* h_ranks,
+                                            size_t* bytes);
+moe_lora_status moe_lora_pack_lora_b(moe_lora_handle* h, const moe_lora_bf16* B, int S, int E_b, int N, int R,
+                                     int gated, const int32_t* h_ranks, moe_lora_bf16* packed,
+                                     moe_lora_stream stream);
+
 /* The whole layer: out [T, H] bf16.  `workspace` holds moe_lora_workspace_size() bytes;
    its contents on entry do not matter.
    LoRA placement follows the GEMMs' token tile BN (twice the mean pairs per expert,
@@ -176,6 +204,10 @@ moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden
      expands run inside the expert GEMMs as extra tensor-core K-stages (the gate_up delta
      in its own accumulator, so the GEMM output and the delta are rounded to bf16
      separately, as the pages do), and the activation runs in the gate_up GEMM's epilogue.
+     With lora_B_dn_packed the down expand's K-stages read the packed copy, one stage per 64
+     stacked rank columns; with lora_B_gu_packed so does the gate_up expand when the gate_up
+     shrink is the tensor-core kernel (more than 32 stacked active ranks).  The results equal
+     those of the per-slot stages.
    - otherwise: the gate_up LoRA chain (shrink + expand into a bf16 delta) runs on the side
      stream beside the permute and gate_up GEMM and joins before the activation (sglang PR
      #28466 section 1 flow (B)).  When the down expand cannot be K-stages (BN 16, R not a

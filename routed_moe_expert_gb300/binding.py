@@ -37,7 +37,8 @@ EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "mo
             "moe_lora_workspace_size", "moe_lora_validate", "moe_lora_route", "moe_lora_permute",
             "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed",
             "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8", "moe_lora_grouped_gemm_fp8",
-            "moe_lora_forward_nvfp4", "moe_lora_quant_nvfp4", "moe_lora_grouped_gemm_nvfp4"]
+            "moe_lora_forward_nvfp4", "moe_lora_quant_nvfp4", "moe_lora_grouped_gemm_nvfp4",
+            "moe_lora_packed_lora_b_size", "moe_lora_pack_lora_b"]
 
 
 class MoELoRAError(RuntimeError):
@@ -67,6 +68,7 @@ class Args(ctypes.Structure):
         ("h_scalings", ctypes.POINTER(c_float)), ("flags", c_uint),
         ("topk_ids", c_void_p), ("topk_weights", c_void_p), ("expert_offsets", c_void_p),
         ("perm", c_void_p), ("inv_perm", c_void_p), ("prof_events", c_void_p),
+        ("lora_B_gu_packed", c_void_p), ("lora_B_dn_packed", c_void_p),
     ]
 
 
@@ -126,6 +128,10 @@ def lib() -> ctypes.CDLL:
                                        c_void_p, c_void_p, c_void_p]
     L.moe_lora_grouped_gemm_nvfp4.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                               c_int, c_int, c_int, c_int, c_void_p, c_void_p]
+    L.moe_lora_packed_lora_b_size.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(ctypes.c_int32),
+                                              ctypes.POINTER(c_size_t)]
+    L.moe_lora_pack_lora_b.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                       ctypes.POINTER(ctypes.c_int32), c_void_p, c_void_p]
     for name in EXPORTED:
         if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
             getattr(L, name).restype = c_int
@@ -205,6 +211,43 @@ def moe_lora_workspace_size(T, H, I, E, top_k, S=0, R=0) -> int:
 
 def alloc_workspace(T, H, I, E, top_k, S=0, R=0, device="cuda") -> torch.Tensor:
     return torch.empty(moe_lora_workspace_size(T, H, I, E, top_k, S, R), dtype=torch.uint8, device=device)
+
+
+def packed_lora_b_shape(E_b: int, N: int, gated: int, ranks: Sequence[int]):
+    """Shape of the expand-ready LoRA B copy: (E_b * NT * 128, Rs), NT = N/128 (gated) or
+    ceil(N/128), Rs = the sum of the ranks each rounded up to 16 (the C ABI's layout)."""
+    NT = N // 128 if gated else (N + 127) // 128
+    rs = sum((int(r) + 15) // 16 * 16 for r in ranks if int(r) > 0)
+    return (int(E_b) * NT * 128, rs)
+
+
+def moe_lora_packed_lora_b_size(S, E_b, N, R, gated, ranks) -> int:
+    """Bytes of the expand-ready LoRA B copy (host only)."""
+    ranks_arr = (ctypes.c_int32 * max(len(ranks), 1))(*[int(r) for r in ranks])
+    n = c_size_t(0)
+    _check(lib().moe_lora_packed_lora_b_size(int(S), int(E_b), int(N), int(R), int(gated), ranks_arr,
+                                             ctypes.byref(n)), "moe_lora_packed_lora_b_size")
+    return int(n.value)
+
+
+def moe_lora_pack_lora_b(handle: Handle, B: torch.Tensor, ranks: Sequence[int], gated: int, out=None,
+                         stream=None) -> torch.Tensor:
+    """Expand-ready copy of a stacked LoRA B [S, E_b, N, R] (lora_B_gu with gated=1,
+    lora_B_dn with gated=0) for the given slot ranks; returns [E_b * NT * 128, Rs] bf16."""
+    if B.dim() != 4 or B.dtype != torch.bfloat16 or not B.is_contiguous():
+        raise ValueError("B must be a contiguous bf16 [S, E_b, N, R] tensor")
+    S, Eb, N, R = (int(x) for x in B.shape)
+    if len(ranks) != S:
+        raise ValueError(f"need {S} ranks, got {len(ranks)}")
+    shape = packed_lora_b_shape(Eb, N, gated, ranks)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=B.device)
+    elif tuple(out.shape) != shape:
+        raise ValueError(f"out must have shape {shape}")
+    ranks_arr = (ctypes.c_int32 * S)(*[int(r) for r in ranks])
+    _check(lib().moe_lora_pack_lora_b(handle.ptr, _ptr(B, torch.bfloat16, "B"), S, Eb, N, R, int(gated), ranks_arr,
+                                      _ptr(out, torch.bfloat16, "out"), _stream(stream)), "moe_lora_pack_lora_b")
+    return out
 
 
 def moe_lora_route(handle: Handle, router_logits: torch.Tensor, top_k: int, routing_method: int = 0,
@@ -303,10 +346,19 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
               routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
               slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (), flags=0,
               outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1,
-              weight_dtype=torch.bfloat16, packed_k=False):
+              weight_dtype=torch.bfloat16, packed_k=False, lora_B_gu_packed=None, lora_B_dn_packed=None):
     """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
     check_shapes(hidden, router_logits, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
                  scalings, flags, correction_bias=correction_bias, packed_k=packed_k)
+    for t, name, Eb, N, gated in (
+            (lora_B_gu_packed, "lora_B_gu_packed", w1.shape[0], w1.shape[1], 1),
+            (lora_B_dn_packed, "lora_B_dn_packed", 1 if (int(flags) & FLAG_SHARED_OUTER) else w1.shape[0],
+             hidden.shape[1], 0)):
+        if t is not None:
+            want = packed_lora_b_shape(Eb, N, gated, ranks)
+            if tuple(t.shape) != want:
+                raise ValueError(f"{name} must have shape {want} (moe_lora_pack_lora_b with these ranks), "
+                                 f"got {tuple(t.shape)}")
     T, H = hidden.shape
     E, twoI, _ = w1.shape
     S = len(ranks)
@@ -336,6 +388,8 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
     a.expert_offsets = _ptr(o.get("expert_offsets"), torch.int32)
     a.perm = _ptr(o.get("perm"), torch.int32)
     a.inv_perm = _ptr(o.get("inv_perm"), torch.int32)
+    a.lora_B_gu_packed = _ptr(lora_B_gu_packed, torch.bfloat16, "lora_B_gu_packed")
+    a.lora_B_dn_packed = _ptr(lora_B_dn_packed, torch.bfloat16, "lora_B_dn_packed")
     ev_arr = None
     if prof_events is not None:
         ev_arr = (c_void_p * (2 * NUM_STAGES))(*[(e.cuda_event if e is not None else None) for e in prof_events])
@@ -347,11 +401,14 @@ def moe_lora_forward(handle: Handle, hidden, router_logits, w1, w2, top_k, routi
                      correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None,
                      lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(), flags=0,
                      out=None, workspace=None, outputs=None, prof_events=None, stream=None,
-                     n_group=1, topk_group=1) -> torch.Tensor:
-    """The whole layer: returns out [T, H] bf16 (written in place when `out` is given)."""
+                     n_group=1, topk_group=1, lora_B_gu_packed=None, lora_B_dn_packed=None) -> torch.Tensor:
+    """The whole layer: returns out [T, H] bf16 (written in place when `out` is given).
+    lora_B_gu_packed / lora_B_dn_packed: optional expand-ready copies (moe_lora_pack_lora_b)
+    made with the same ranks."""
     a, keep = make_args(hidden, router_logits, w1, w2, top_k, routing_method, correction_bias,
                         routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
-                        scalings, flags, outputs, prof_events, n_group, topk_group)
+                        scalings, flags, outputs, prof_events, n_group, topk_group,
+                        lora_B_gu_packed=lora_B_gu_packed, lora_B_dn_packed=lora_B_dn_packed)
     if out is None:
         out = torch.empty((a.T, a.H), dtype=torch.bfloat16, device=hidden.device)
     if workspace is None:

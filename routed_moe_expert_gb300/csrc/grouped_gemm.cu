@@ -122,6 +122,12 @@ MLDEV void lora_expand_chunk(const GemmParams& p, const int* lslot, const float*
   }
 }
 
+// Fused LoRA K-stages come either per slot (slot s's rows of B, its own rank as the K extent,
+// and its ub rows), or, with a packed B, per 64-column panel of every slot's ranks stacked
+// side by side (B rows of the tile from the expand-ready copy, the pairs' stacked ub rows):
+// a pair's ub row is zero outside its own slot's columns, so each panel's products of other
+// slots add exact zeros, and far fewer (full 128-byte) rows are fetched per tile.
+//
 // MODE: 0 plain epilogue, 1 CUDA-core LoRA expand in the epilogue, 2 fused LoRA K-stages,
 // 3 activation epilogue, 4 activation epilogue with fused LoRA K-stages into a delta
 // accumulator (so g and the delta are rounded to bf16 separately).  Each mode is its own
@@ -210,6 +216,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmap_w);
     tma_prefetch_desc(&p.tmap_x);
+    if (kFused && p.lora_packed) {
+      tma_prefetch_desc(&p.tmap_lbp);
+      tma_prefetch_desc(&p.tmap_lup);
+    }
   }
   if (warp == 1) {
     if constexpr (CG == 2) {
@@ -359,11 +369,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           tile_slot_ring[it_tile % kTileRing] = smask;
           const int lb_off = p.lora_b_e1 ? e * p.N : 0;   // a shared B has one expert's rows
           if (ok) ok = issue(&p.tmap_w, wr0, wr1, (kb_lora - 1) * 64, &p.tmap_x, xh);
-          for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
-            if (!((smask >> sl) & 1u)) continue;
-            const int nkb = lora_blocks(p.slots.ranks[sl], p.lora_kb);
-            for (int kb = 0; ok && kb < nkb; ++kb)
-              ok = issue(&p.tmap_lb[sl], wr0 - lb_off, wr1 - lb_off, kb * 64, &p.tmap_lu, sl * p.P + xh);
+          if (p.lora_packed) {   // LoRA expand stages over the stacked ranks, per 64-column panel
+            const int prow = ((p.lora_b_e1 ? 0 : e) * NT + nt) * 128;
+            const int npan = (p.lora_rs + 63) >> 6;
+            for (int j = 0; ok && j < npan; ++j)
+              if (smask & p.lora_panel_slots[j]) ok = issue(&p.tmap_lbp, prow, prow + 64, j * 64, &p.tmap_lup, xh);
+          } else {
+            for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {   // LoRA expand stages, per slot
+              if (!((smask >> sl) & 1u)) continue;
+              const int nkb = lora_blocks(p.slots.ranks[sl], p.lora_kb);
+              for (int kb = 0; ok && kb < nkb; ++kb)
+                ok = issue(&p.tmap_lb[sl], wr0 - lb_off, wr1 - lb_off, kb * 64, &p.tmap_lu, sl * p.P + xh);
+            }
           }
           for (int kb = kb_lora; ok && kb < KB; ++kb) ok = issue(&p.tmap_w, wr0, wr1, kb * 64, &p.tmap_x, xh);
         }
@@ -440,13 +457,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             }
           }
           bool first_delta = delta_acc;   // the delta accumulator starts fresh each tile
-          for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
-            if (!((smask >> sl) & 1u)) continue;
-            const int rank = p.slots.ranks[sl];
-            const int nkb = lora_blocks(rank, p.lora_kb);
-            for (int kb = 0; ok && kb < nkb; ++kb) {
-              ok = consume(dl, first_delta, lora_ksteps(rank, kb));
+          if (p.lora_packed) {
+            const int npan = (p.lora_rs + 63) >> 6;
+            for (int j = 0; ok && j < npan; ++j) {
+              if (!(smask & p.lora_panel_slots[j])) continue;
+              ok = consume(dl, first_delta, min(4, (p.lora_rs - 64 * j) >> 4));
               first_delta = false;
+            }
+          } else {
+            for (int sl = 0; ok && sl < kMaxFusedSlots; ++sl) {
+              if (!((smask >> sl) & 1u)) continue;
+              const int rank = p.slots.ranks[sl];
+              const int nkb = lora_blocks(rank, p.lora_kb);
+              for (int kb = 0; ok && kb < nkb; ++kb) {
+                ok = consume(dl, first_delta, lora_ksteps(rank, kb));
+                first_delta = false;
+              }
             }
           }
           // the delta is complete before the tile's last main stages: the epilogue can take it

@@ -15,6 +15,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxRouteCtas = 256;
 constexpr int kMaxFusedSlots = 8;   // slots the GEMMs can take as extra LoRA MMA stages
+constexpr int kMaxLoraPanels = 8;   // 64-column panels of the stacked ranks of a packed LoRA B
 
 // "where" tags of the device status word (bits 8 and up; the low byte is the code)
 enum : uint32_t {
@@ -99,6 +100,17 @@ struct GemmParams {
   int lora_b_e1;                 // 1: the LoRA B (epilogue or fused stages) is one set per slot
   const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
+  // Fused LoRA from the expand-ready copy of B (lora_packed = 1, replaces the per-slot stages):
+  // A' = the tile's 128 rows of the packed B (tmap_lbp: [Eb*NT*128 rows, Rs cols], rows in the
+  // tile's own order, slot s's ranks in columns [coff[s], coff[s] + ranks[s]), zero up to
+  // coff[s+1]), B' = the tile's rows of the stacked ub (tmap_lup: [P rows, Rs cols], zero
+  // outside the pair's own slot).  One stage per 64-column panel j, issued when a slot of
+  // lora_panel_slots[j] is present among the tile's pairs.
+  CUtensorMap tmap_lbp;          // box {64, 64}
+  CUtensorMap tmap_lup;          // box {64, BN / cta_pair}
+  int lora_packed;
+  int lora_rs;                   // Rs, a multiple of 16
+  uint32_t lora_panel_slots[kMaxLoraPanels];
 };
 constexpr int kMaxGemmSmem = 227 * 1024;   // dynamic shared memory a CTA may have
 int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int y_tma);
@@ -239,11 +251,23 @@ struct ShrinkTcParams {
   int k, P, K, E, S, R;
   int stages;                    // pipeline depth (set by the launcher)
   LoraSlots slots;
-  __nv_bfloat16* ub;             // [S, P, R]
+  __nv_bfloat16* ub;             // [S, P, R], or [P, rs] with ub_stacked
+  int ub_stacked;                // 1: each pair's row holds every slot's ranks, slot s at column coff[s]
+  int rs;                        // stacked columns (ub_stacked), a multiple of 16
+  int coff[kMaxFusedSlots + 1];
   int32_t* pair_slot;            // [P]
   uint32_t* status;
 };
 int lora_shrink_tc_nb(int rows);
+// Expand-ready (packed) LoRA B for the fused K-stages: see pack_lora_b_kernel.
+struct PackLoraBParams {
+  const __nv_bfloat16* B;        // [S, Eb, N, R]
+  __nv_bfloat16* Bp;             // [Eb * NT * 128, rs]
+  int S, Eb, N, R, NT, gated, rs;
+  int ranks[kMaxSlots];
+  int coff[kMaxSlots + 1];       // coff[s+1] - coff[s] = ranks[s] rounded up to 16
+};
+cudaError_t launch_pack_lora_b(const PackLoraBParams& p, cudaStream_t stream);
 cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl = false);
 

@@ -4,6 +4,9 @@
 //   ub[s, q, r] = bf16( scaling[s] * u[q, s, r] )  for s = the slot of q's token and r < ranks[s]
 //   ub[s', q, r] = 0                               for every other slot s' (and r >= ranks[s])
 //   pair_slot[q] = s, or -1 when q's token has no active adapter
+// or, with ub_stacked, the same values in one row per pair: ub[q, coff[s] + r], the columns
+// [coff[s], coff[s+1]) holding slot s's ranks padded with zeros to a multiple of 16 (the
+// column layout of the expand-ready LoRA B, so one K-stage of the GEMM covers every slot).
 //
 // This is the shrink (A) half of the per-expert LoRA of sglang PR #28466 (section 1,
 // merged_experts_fused_moe_lora_add) for the gate_up chain (X = permuted hidden) and the
@@ -238,11 +241,24 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               f[i] = (s2 == sl && r0 + i < rank) ? sc * __uint_as_float(v[8 * h8 + i]) : 0.0f;
-            *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s2) * p.P + q) * p.R + r0) = pack8(f);
+            if (p.ub_stacked) {   // slot s2's columns of the pair's stacked row
+              if (r0 < p.coff[s2 + 1] - p.coff[s2])
+                *reinterpret_cast<uint4*>(p.ub + static_cast<size_t>(q) * p.rs + p.coff[s2] + r0) = pack8(f);
+            } else {
+              *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s2) * p.P + q) * p.R + r0) = pack8(f);
+            }
           }
         }
       }
-      if (valid && p.per_slot) {
+      if (valid && p.ub_stacked) {   // the columns no accumulator column covered: zero
+        for (int s2 = 0; s2 < p.S; ++s2) {
+          const int ru = p.coff[s2 + 1] - p.coff[s2];
+          const int z0 = p.per_slot ? p.row_off[s2 + 1] - p.row_off[s2] : min(p.R, ru);
+          for (int r0 = z0; r0 < ru; r0 += 8)
+            *reinterpret_cast<uint4*>(p.ub + static_cast<size_t>(q) * p.rs + p.coff[s2] + r0) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else if (valid && p.per_slot) {
         for (int s2 = 0; s2 < p.S; ++s2)
           for (int r0 = p.row_off[s2 + 1] - p.row_off[s2]; r0 < p.R; r0 += 8)
             *reinterpret_cast<uint4*>(p.ub + (static_cast<size_t>(s2) * p.P + q) * p.R + r0) =
@@ -299,6 +315,47 @@ cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_
     case 256: return launch_nb<256>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Expand-ready copy of a stacked LoRA B [S, Eb, N, R] for the fused LoRA K-stages of the
+// grouped GEMM: row (eb * NT + nt) * 128 + r holds the weight row that is row r of 128-row
+// tile nt (for the gated gate_up layout: gate row 64 nt + r for r < 64, else up row
+// N/2 + 64 nt + r - 64; otherwise row 128 nt + r, zero past N), and its columns stack the
+// slots: slot s's ranks[s] values in [coff[s], coff[s] + ranks[s]), zero up to coff[s+1]
+// (ranks rounded up to 16).  One thread per 8 output columns (one 16-byte store).
+__global__ void pack_lora_b_kernel(const __grid_constant__ PackLoraBParams p) {
+  const int cv = p.rs >> 3;
+  const long long total = static_cast<long long>(p.Eb) * p.NT * 128 * cv;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long prow = i / cv;
+    const int c0 = static_cast<int>(i - prow * cv) * 8;
+    const int r = static_cast<int>(prow & 127);
+    const long long tn = prow >> 7;
+    const int nt = static_cast<int>(tn % p.NT);
+    const int eb = static_cast<int>(tn / p.NT);
+    const int n = p.gated ? (r < 64 ? 64 * nt + r : (p.N >> 1) + 64 * nt + (r - 64)) : 128 * nt + r;
+    int s = 0;
+    while (p.coff[s + 1] <= c0) ++s;   // c0 < coff[S], so s < S
+    const int rr0 = c0 - p.coff[s];
+    const __nv_bfloat16* src = p.B + ((static_cast<size_t>(s) * p.Eb + eb) * p.N + n) * p.R;
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[j] = 0.0f;
+      if (n < p.N && rr0 + j < p.ranks[s]) f[j] = bf2f(src[rr0 + j]);   // the rank tail is never read
+    }
+    *reinterpret_cast<uint4*>(p.Bp + prow * p.rs + c0) = pack8(f);
+  }
+}
+
+cudaError_t launch_pack_lora_b(const PackLoraBParams& p, cudaStream_t stream) {
+  const long long total = static_cast<long long>(p.Eb) * p.NT * 128 * (p.rs >> 3);
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  pack_lora_b_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace mlk

@@ -87,7 +87,8 @@ Layout layout_for(int T, int H, int I, int E, int k, int R, int S) {
   L.v = take(P * R * 4);
   L.y = take(P * H * 4);
   L.pslot = take(R > 0 ? P * 4 : 0);
-  L.ub = take(static_cast<size_t>(S) * P * ((R + 7) / 8 * 8) * 2);
+  // per-slot rows [S, P, R rounded up to 8], or stacked rows [P, sum of ranks rounded up to 16]
+  L.ub = take(static_cast<size_t>(S) * P * ((R + 15) / 16 * 16) * 2);
   // The FP8 path keeps its e4m3 GEMM inputs in the xp region ([P, H] bytes) and in the g
   // region ([P, I] bytes, written after the activation has read g); their group scales:
   L.sx = take(P * ((static_cast<size_t>(H) + 127) / 128) * 4);
@@ -184,6 +185,7 @@ moe_lora_status moe_lora_validate(const moe_lora_args* a) {
       if (!aligned16(a->lora_A_gu) || !aligned16(a->lora_A_dn) || !aligned16(a->lora_B_gu) ||
           !aligned16(a->lora_B_dn) || !aligned4(a->slot_idx))
         return MOE_LORA_ERR_INVALID_ARG;
+      if (!aligned16(a->lora_B_gu_packed) || !aligned16(a->lora_B_dn_packed)) return MOE_LORA_ERR_INVALID_ARG;
     }
   }
   const void* opt[] = {a->topk_ids, a->topk_weights, a->expert_offsets, a->perm, a->inv_perm};
@@ -477,15 +479,59 @@ bool fuse_lora_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, 
   return true;
 }
 
+// Stacked LoRA columns of the packed layout: slot s's ranks at coff[s], each slot's block
+// rounded up to 16 columns (one MMA K-step), from the ranks alone.  Returns Rs = coff[S].
+int stacked_cols(const int32_t* ranks, int S, int* coff) {
+  coff[0] = 0;
+  for (int s = 0; s < S; ++s) coff[s + 1] = coff[s] + (ranks[s] > 0 ? (ranks[s] + 15) / 16 * 16 : 0);
+  return coff[S];
+}
+
+// Tensor maps of the fused LoRA stages from the expand-ready (packed) B [Eb*NT*128, Rs] and
+// the stacked ub [P, Rs], and the slots whose columns meet each 64-column panel.
+bool fuse_lora_maps_packed(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* Bp,
+                           int N, const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn,
+                           bool b_e1 = false) {
+  int coff[kMaxFusedSlots + 1];
+  const int rs = stacked_cols(a->h_ranks, a->S, coff);
+  const int npan = (rs + 63) / 64;
+  if (a->S > kMaxFusedSlots || rs == 0 || npan > kMaxLoraPanels) return false;
+  const int NT = gp.gated ? (N >> 7) : ((N + 127) >> 7);
+  const int Eb = b_e1 ? 1 : a->E;
+  if (!make_tmap(h->encode, &gp.tmap_lbp, Bp, static_cast<uint64_t>(Eb) * NT * 128, static_cast<uint64_t>(rs), 64))
+    return false;
+  if (!make_tmap(h->encode, &gp.tmap_lup, ub, static_cast<uint64_t>(P), static_cast<uint64_t>(rs),
+                 static_cast<uint32_t>(bn / (gp.cta_pair == 2 ? 2 : 1))))
+    return false;
+  for (int j = 0; j < kMaxLoraPanels; ++j) gp.lora_panel_slots[j] = 0;
+  for (int s = 0; s < a->S; ++s) {
+    if (a->h_ranks[s] <= 0 || a->h_scalings[s] == 0.0f) continue;   // never in pair_slot
+    for (int j = coff[s] / 64; j * 64 < coff[s + 1]; ++j) gp.lora_panel_slots[j] |= 1u << s;
+  }
+  gp.lora_fused = 1;
+  gp.lora_packed = 1;
+  gp.lora_rs = rs;
+  gp.lora_b_e1 = b_e1 ? 1 : 0;
+  gp.slots = make_slots(a);
+  gp.P = P;
+  gp.pair_slot = pair_slot;
+  return true;
+}
+
 // Tensor-core shrink of every slot: X [P, K] (permuted hidden or activation) against the
 // stacked LoRA A [S*E*R, K]; writes ub and pair_slot.
 moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, const void* X, const moe_lora_bf16* A,
                                   int K, const int32_t* offsets, const int32_t* perm, const LoraSlots& slots,
                                   __nv_bfloat16* ub, int32_t* pair_slot, uint32_t* status, cudaStream_t stream,
-                                  bool pdl, bool a_e1 = false) {
+                                  bool pdl, bool a_e1 = false, bool stacked = false) {
   const int P = a->T * a->top_k;
   ShrinkTcParams sp;
   std::memset(&sp, 0, sizeof(sp));
+  if (stacked) {   // ub rows in the packed-B column layout
+    if (a->S > kMaxFusedSlots) return MOE_LORA_ERR_UNSUPPORTED;
+    sp.ub_stacked = 1;
+    sp.rs = stacked_cols(a->h_ranks, a->S, sp.coff);
+  }
   // pairs per tile from the mean pairs per expert, so small experts read only their rows
   const long long m2 = 2LL * ((P + a->E - 1) / a->E);
   sp.tb = m2 <= 16 ? 16 : m2 <= 32 ? 32 : m2 <= 64 ? 64 : 128;
@@ -919,6 +965,52 @@ moe_lora_status moe_lora_route(moe_lora_handle* h, const moe_lora_bf16* router_l
                        topk_ids, topk_weights, expert_offsets, perm, inv_perm, ws, L, stream);
 }
 
+// Size and checks of the expand-ready LoRA B copy (see include/moe_lora.h).
+static moe_lora_status packed_lora_b_dims(int S, int E_b, int N, int R, int gated, const int32_t* h_ranks,
+                                          int* NT, int* rs, int* coff) {
+  if (S < 1 || S > kMaxSlots || E_b < 1 || E_b > kMaxExperts || N < 1 || R < 1 || R > kMaxRank || h_ranks == nullptr)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (gated != 0 && gated != 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (gated && N % 128 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  for (int s = 0; s < S; ++s)
+    if (h_ranks[s] < 0 || h_ranks[s] > R) return MOE_LORA_ERR_INVALID_ARG;
+  *NT = gated ? N / 128 : (N + 127) / 128;
+  *rs = stacked_cols(h_ranks, S, coff);
+  if (*rs == 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (static_cast<long long>(E_b) * *NT * 128 > 0x7fffffffLL) return MOE_LORA_ERR_INVALID_ARG;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_packed_lora_b_size(int S, int E_b, int N, int R, int gated, const int32_t* h_ranks,
+                                            size_t* bytes) {
+  if (bytes == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  int NT = 0, rs = 0, coff[kMaxSlots + 1];
+  const moe_lora_status st = packed_lora_b_dims(S, E_b, N, R, gated, h_ranks, &NT, &rs, coff);
+  if (st != MOE_LORA_OK) return st;
+  *bytes = static_cast<size_t>(E_b) * NT * 128 * rs * 2;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_pack_lora_b(moe_lora_handle* h, const moe_lora_bf16* B, int S, int E_b, int N, int R,
+                                     int gated, const int32_t* h_ranks, moe_lora_bf16* packed,
+                                     moe_lora_stream stream) {
+  if (h == nullptr || B == nullptr || packed == nullptr || !aligned16(packed)) return MOE_LORA_ERR_INVALID_ARG;
+  PackLoraBParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  moe_lora_status st = packed_lora_b_dims(S, E_b, N, R, gated, h_ranks, &pp.NT, &pp.rs, pp.coff);
+  if (st != MOE_LORA_OK) return st;
+  pp.B = reinterpret_cast<const __nv_bfloat16*>(B);
+  pp.Bp = reinterpret_cast<__nv_bfloat16*>(packed);
+  pp.S = S;
+  pp.Eb = E_b;
+  pp.N = N;
+  pp.R = R;
+  pp.gated = gated;
+  for (int s = 0; s < S; ++s) pp.ranks[s] = h_ranks[s];
+  ML_LAUNCH(h, launch_pack_lora_b(pp, stream), "pack LoRA B launch");
+  return MOE_LORA_OK;
+}
+
 moe_lora_status moe_lora_permute(moe_lora_handle* h, const moe_lora_bf16* hidden, const int32_t* perm, int T, int H,
                                  int top_k, moe_lora_bf16* permuted, moe_lora_stream stream) {
   if (h == nullptr || T < 0 || H < 8 || H % 8 != 0 || top_k < 1) return MOE_LORA_ERR_INVALID_ARG;
@@ -1008,6 +1100,10 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     for (int s = 0; s < a->S && lora; ++s)
       if (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) nr_active += slots.ranks[s];
     const bool permute_shrink = fuse_all && nr_active <= kPermuteShrinkMaxRows;
+    // the expand-ready B copies, where given, replace the per-slot LoRA stages (the gate_up one
+    // needs the tensor-core shrink, which can write the stacked ub rows)
+    const bool gu_packed = fuse_all && !permute_shrink && a->lora_B_gu_packed != nullptr;
+    const bool dn_packed = fuse_all && a->lora_B_dn_packed != nullptr;
     if (permute_shrink) {   // the permute and the gate_up LoRA shrink in one pass over the token rows
       PermuteShrinkParams ps;
       std::memset(&ps, 0, sizeof(ps));
@@ -1039,7 +1135,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       if (fuse_all) {
         prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
         st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
-                               so);
+                               so, gu_packed);
         if (st != MOE_LORA_OK) return st;
         prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
       }
@@ -1055,13 +1151,16 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     gu.K = H;
     gu.gated = 2;
     gu.cta_pair = pair_tiles(bn, 2 * I);
-    if (fuse_all && !fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)) return MOE_LORA_ERR_CUDA;
+    if (fuse_all && !(gu_packed ? fuse_lora_maps_packed(h, gu, a, a->lora_B_gu_packed, 2 * I, ub, pair_slot, P, bn)
+                                : fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)))
+      return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
     if (fuse_all) {
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
-      st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl);
+      st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
+                             false, dn_packed);
       if (st != MOE_LORA_OK) return st;
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
     }
@@ -1078,7 +1177,9 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     dn.gated = 0;
     dn.cta_pair = pair_tiles(bn0, H);
     // the down GEMM adds its LoRA stages to the main accumulator, so it keeps the full tile
-    if (fuse_all && !fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)) return MOE_LORA_ERR_CUDA;
+    if (fuse_all && !(dn_packed ? fuse_lora_maps_packed(h, dn, a, a->lora_B_dn_packed, H, ub, pair_slot, P, bn0, so)
+                                : fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)))
+      return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, dn, a->w2, act, P, bn0, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);

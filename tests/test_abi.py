@@ -49,6 +49,26 @@ def test_workspace_size_host_only(built_lib):
     assert B.moe_lora_workspace_size(0, 128, 64, 8, 2) > 0
 
 
+def test_packed_lora_b_size_host_only(built_lib):
+    """The expand-ready LoRA B copy's size follows its layout rule (rows: experts x 128-row
+    tiles; columns: every slot's rank rounded up to 16), the Python shape helper agrees, and
+    the host checks reject what the header says they reject."""
+    # gate_up: 4 experts, N = 2I = 512 (4 tiles), ranks 8, 16, 32, 64 -> 16+16+32+64 columns
+    assert B.moe_lora_packed_lora_b_size(4, 4, 512, 64, 1, (8, 16, 32, 64)) == 4 * 4 * 128 * 128 * 2
+    assert B.packed_lora_b_shape(4, 512, 1, (8, 16, 32, 64)) == (4 * 4 * 128, 128)
+    # down, N = 200 (2 tiles, zero rows past N), a rank-0 slot and a rank of 24
+    assert B.moe_lora_packed_lora_b_size(3, 2, 200, 24, 0, (24, 0, 8)) == 2 * 2 * 128 * 48 * 2
+    assert B.packed_lora_b_shape(2, 200, 0, (24, 0, 8)) == (2 * 2 * 128, 48)
+    for bad in (dict(ranks=(0, 0)),                  # no stacked column at all
+                dict(ranks=(8, 40)),                 # a rank above R
+                dict(N=200, gated=1),                # gated needs whole 128-row tiles of gate+up rows
+                dict(S=0, ranks=())):
+        kw = dict(S=2, Eb=2, N=256, R=32, gated=1, ranks=(8, 16))
+        kw.update(bad)
+        with pytest.raises(B.MoELoRAError):
+            B.moe_lora_packed_lora_b_size(kw["S"], kw["Eb"], kw["N"], kw["R"], kw["gated"], kw["ranks"])
+
+
 FAKE = 0x7f0000000000          # 16-byte aligned fake device address (never dereferenced)
 
 

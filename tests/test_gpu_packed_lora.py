@@ -1,0 +1,134 @@
+"""Expand-ready (packed) LoRA B copies: the pack's layout, bit for bit, against the layout rule
+written out in torch; the layer with packed copies against the same layer with the per-slot
+LoRA stages (equal outputs: a pair's stacked shrink row is zero outside its own slot, so the
+other slots' columns add exact zeros) and against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import routed_moe_expert_gb300 as pkg
+from routed_moe_expert_gb300 import workloads as wl
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def handle():
+    h = pkg.Handle(0)
+    yield h
+    h.close()
+
+
+def _packed_reference(B: torch.Tensor, ranks, gated: int) -> torch.Tensor:
+    """The layout of moe_lora_pack_lora_b, from its definition: row (e * NT + nt) * 128 + r is
+    row r of 128-row weight tile nt (gated: gate rows then up rows), slot s's ranks side by side
+    from column coff[s], each slot's block rounded up to 16 columns."""
+    S, Eb, N, R = B.shape
+    NT = N // 128 if gated else (N + 127) // 128
+    ru = [(r + 15) // 16 * 16 if r > 0 else 0 for r in ranks]
+    coff = np.concatenate([[0], np.cumsum(ru)]).astype(int)
+    out = torch.zeros((Eb, NT, 128, int(coff[-1])), dtype=torch.bfloat16)
+    rows = torch.arange(128)
+    for nt in range(NT):
+        n = torch.where(rows < 64, 64 * nt + rows, N // 2 + 64 * nt + rows - 64) if gated else 128 * nt + rows
+        ok = n < N
+        for s in range(S):
+            if ranks[s] > 0:
+                out[:, nt, ok, coff[s]:coff[s] + ranks[s]] = B[s][:, n[ok], :ranks[s]]
+    return out.reshape(Eb * NT * 128, -1)
+
+
+@pytest.mark.parametrize("S,Eb,N,R,ranks,gated", [
+    (4, 3, 256, 64, (8, 0, 24, 64), 1),     # gate_up layout, a rank-0 slot, a rank not a multiple of 16
+    (2, 5, 200, 32, (32, 16), 0),           # down layout, N not a multiple of 128 (zero rows)
+    (3, 1, 384, 16, (16, 8, 16), 0),        # shared-outer down B: one expert set
+    (1, 2, 128, 128, (128,), 1),            # one slot at the largest rank (two panels)
+], ids=["gate_up", "down-ragged", "shared", "rank128"])
+def test_pack_lora_b_layout_bit_exact(handle, S, Eb, N, R, ranks, gated):
+    g = torch.Generator().manual_seed(N + R)
+    B = torch.randn((S, Eb, N, R), generator=g).to(torch.bfloat16)
+    for s, r in enumerate(ranks):   # the rank tails must never be read
+        B[s, :, :, r:] = float("nan")
+    got = pkg.moe_lora_pack_lora_b(handle, B.cuda(), ranks, gated)
+    torch.cuda.synchronize()
+    ref = _packed_reference(B, ranks, gated)
+    assert tuple(got.shape) == tuple(ref.shape) == pkg.packed_lora_b_shape(Eb, N, gated, ranks)
+    assert pkg.moe_lora_packed_lora_b_size(S, Eb, N, R, gated, ranks) == ref.numel() * 2
+    assert torch.equal(got.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def _run_pair(h, cfg, seed, flags=0, device_inputs=False):
+    """The layer twice on the same inputs, per-slot and packed LoRA stages; returns both outputs
+    (checked against each other and the oracle)."""
+    inp = wl.make_inputs(cfg, seed=seed, device="cuda" if device_inputs else "cpu")
+    g = gh.to_dev(inp)
+    ws = pkg.alloc_workspace(g["T"], cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
+    base = gh.forward(h, g, flags=flags, workspace=ws)
+    torch.cuda.synchronize()
+    st, word = pkg.moe_lora_check_status(ws)
+    assert st == 0, f"device status {word:#x}"
+    so = bool(flags & pkg.FLAG_SHARED_OUTER)
+    bgu = pkg.moe_lora_pack_lora_b(h, g["lora_B_gu"], g["ranks"], 1)
+    bdn = pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], g["ranks"], 0)
+    assert bdn.shape[0] == (1 if so else cfg.E) * ((cfg.H + 127) // 128) * 128
+    out = pkg.moe_lora_forward(
+        h, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], routing_method=g["method"],
+        correction_bias=g["correction_bias"], routed_scaling_factor=g["rsf"],
+        lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"],
+        slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"], flags=flags, workspace=ws,
+        lora_B_gu_packed=bgu, lora_B_dn_packed=bdn)
+    torch.cuda.synchronize()
+    st, word = pkg.moe_lora_check_status(ws)
+    assert st == 0, f"device status {word:#x}"
+    assert torch.equal(out, base), f"packed and per-slot LoRA stages differ: {int((out != base).sum())} elements"
+    ref = gh.oracle(inp, lazy=device_inputs)
+    gh.assert_close(out.float().cpu().numpy(), ref["out"], cfg.name)
+    return base, out
+
+
+@pytest.mark.parametrize("T,E,k,ranks,scalings,shared", [
+    (96, 16, 4, (8, 16, 32, 64), (2.0, 1.0, 0.5, 0.25), False),   # 64-token tiles, tensor-core shrinks
+    (96, 16, 4, (8, 16), (2.0, 0.5), False),                      # <= 32 stacked ranks: permute + shrink
+    (64, 16, 4, (8, 32), (2.0, 0.5), True),                       # shared-outer down B
+    (96, 16, 4, (16, 24, 0, 8), (1.0, 0.0, 1.0, 2.0), False),     # a disabled slot and a rank-0 slot
+    (600, 8, 2, (8, 16, 32, 64), (2.0, 1.0, 0.5, 0.25), False),   # 256-token CTA-pair tiles
+], ids=["four-slots", "few-ranks", "shared-outer", "disabled-slots", "pair-tiles"])
+def test_packed_lora_b_equals_per_slot_stages(handle, T, E, k, ranks, scalings, shared):
+    cfg = wl.LayerConfig("pk", T=T, H=512, I=256, E=E, top_k=k, ranks=ranks, scalings=scalings,
+                         slot_mode="uniform_none10", shared_outer=shared)
+    _run_pair(handle, cfg, seed=T + len(ranks), flags=pkg.FLAG_SHARED_OUTER if shared else 0)
+
+
+def test_packed_lora_b_multi_slot_config(handle):
+    _run_pair(handle, wl.CONFIGS["multi_slot"], seed=0, device_inputs=True)
+
+
+def test_packed_lora_b_graph_replay(handle):
+    """Captured once, replayed: the packed stages read only buffers that exist before capture."""
+    cfg = wl.LayerConfig("pkg", T=96, H=512, I=256, E=16, top_k=4, ranks=(8, 16, 32, 64),
+                         scalings=(2.0, 1.0, 0.5, 0.25), slot_mode="uniform_none10")
+    base, _ = _run_pair(handle, cfg, seed=5)
+    inp = wl.make_inputs(cfg, seed=5)
+    g = gh.to_dev(inp)
+    ws = pkg.alloc_workspace(g["T"], cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
+    bgu = pkg.moe_lora_pack_lora_b(handle, g["lora_B_gu"], g["ranks"], 1)
+    bdn = pkg.moe_lora_pack_lora_b(handle, g["lora_B_dn"], g["ranks"], 0)
+    out = torch.empty_like(base)
+    kw = dict(routing_method=g["method"], correction_bias=g["correction_bias"], routed_scaling_factor=g["rsf"],
+              lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
+              lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"],
+              workspace=ws, out=out, lora_B_gu_packed=bgu, lora_B_dn_packed=bdn)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkg.moe_lora_forward(handle, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], stream=s, **kw)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        pkg.moe_lora_forward(handle, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], stream=s, **kw)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, base)
