@@ -70,6 +70,8 @@ typedef enum {
 #define MOE_LORA_FLAG_SHARED_OUTER       32u /* shared-outer LoRA: lora_A_gu [S,1,R,H], lora_B_dn [S,1,H,R] */
 #define MOE_LORA_FLAG_DOWN_LORA_SIDE     64u /* narrow placement, two streams: the down LoRA on the side
                                                  stream beside the down GEMM (see forward) */
+#define MOE_LORA_FLAG_SEPARATE_SHRINK   128u /* fused placement with packed B: run the LoRA shrinks as
+                                                 their own kernels, not as tiles of the GEMMs */
 
 /* Stages that moe_lora_args.prof_events can bracket (two events per stage). */
 enum {
@@ -207,7 +209,11 @@ moe_lora_status moe_lora_pack_lora_b(moe_lora_handle* h, const moe_lora_bf16* B,
      With lora_B_dn_packed the down expand's K-stages read the packed copy, one stage per 64
      stacked rank columns; with lora_B_gu_packed so does the gate_up expand when the gate_up
      shrink is the tensor-core kernel (more than 32 stacked active ranks).  The results equal
-     those of the per-slot stages.
+     those of the per-slot stages.  With a packed B, single-CTA token tiles (BN <= 128) and
+     at most 128 active rank rows (each active rank a multiple of 8), the shrink itself runs
+     as the first tiles of that GEMM (one per expert token tile; a GEMM tile waits for its
+     own shrink tile before its LoRA stages) instead of a kernel of its own, unless
+     MOE_LORA_FLAG_SEPARATE_SHRINK.
    - otherwise: the gate_up LoRA chain (shrink + expand into a bf16 delta) runs on the side
      stream beside the permute and gate_up GEMM and joins before the activation (sglang PR
      #28466 section 1 flow (B)).  When the down expand cannot be K-stages (BN 16, R not a

@@ -10,6 +10,6 @@ from .binding import (  # noqa: F401
     moe_lora_status_string, moe_lora_validate, moe_lora_pack_lora_b, moe_lora_packed_lora_b_size,
     packed_lora_b_shape,
     moe_lora_workspace_size, FLAG_LORA_OFF, FLAG_FORCE_SINGLE_STREAM, FLAG_FORCE_TWO_STREAM, FLAG_UNFUSED_LORA, FLAG_NO_PDL, FLAG_SHARED_OUTER,
-    FLAG_DOWN_LORA_SIDE,
+    FLAG_DOWN_LORA_SIDE, FLAG_SEPARATE_SHRINK,
     ROUTE_RENORMALIZE, ROUTE_DEEPSEEK_V3, STAGES, NUM_STAGES,
 )

@@ -29,6 +29,7 @@ FLAG_UNFUSED_LORA = 8
 FLAG_NO_PDL = 16
 FLAG_SHARED_OUTER = 32
 FLAG_DOWN_LORA_SIDE = 64
+FLAG_SEPARATE_SHRINK = 128
 STAGES = ["route", "permute", "gate_up_gemm", "lora_gate_up", "activation", "down_gemm",
           "lora_down", "finalize"]
 NUM_STAGES = len(STAGES)

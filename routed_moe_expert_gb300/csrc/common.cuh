@@ -247,6 +247,33 @@ MLDEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" 
 MLDEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
 MLDEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Global memory written through the generic proxy (st.global) and read by the async proxy
+// (TMA), or the reverse.
+MLDEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Cross-CTA ready flags: a release increment after this thread's (and, through a preceding
+// block barrier, its block's) global writes, and a bounded acquire wait for a count.
+MLDEV void red_release_add(int* flag, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+MLDEV int ld_acquire(const int* flag) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
+MLDEV bool wait_flag_geq(const int* flag, int target, volatile int* abort_flag, uint32_t* status, uint32_t where) {
+  if (ld_acquire(flag) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire(flag) < target) {
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      record_status(status, kDevTimeout, where);
+      return false;
+    }
+  }
+  return true;
+}
 
 MLDEV uint64_t l2_policy_evict_first() {
   uint64_t p;

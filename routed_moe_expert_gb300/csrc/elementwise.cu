@@ -13,13 +13,16 @@ namespace mlk {
 // permute: xp[q, :] = x[perm[q] / k, :]   (sglang PR #28466, Files changed, launcher
 // row: "moe::dev::permute (bf16 gather)").  One warp per permuted row, 16-byte vectors.
 // With slot_out set it also gathers each pair's adapter slot, slot_out[q] = slot_idx[t]
-// (checked later by the kernel that uses it).
+// (checked later by the kernel that uses it).  zero_out[0, zero_n) is cleared (the ready
+// flags of the GEMMs that follow).
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                                                       int P, int k, int H8, uint4* __restrict__ xp,
-                                                      const int32_t* __restrict__ slot_idx, int32_t* slot_out) {
+                                                      const int32_t* __restrict__ slot_idx, int32_t* slot_out,
+                                                      int* zero_out, int zero_n) {
   pdl_wait();
   pdl_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x) zero_out[i] = 0;
   const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (q >= P) return;
   const int t = perm[q] / k;
@@ -33,10 +36,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
 
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
                            __nv_bfloat16* xp, cudaStream_t stream, bool pdl, const int32_t* slot_idx,
-                           int32_t* slot_out) {
+                           int32_t* slot_out, int* zero_out, int zero_n) {
   if (P == 0) return cudaSuccess;
   return launch_k(permute_kernel, dim3((P + 7) / 8), dim3(256), 0, stream, pdl, reinterpret_cast<const uint4*>(x),
-                  perm, P, k, H / 8, reinterpret_cast<uint4*>(xp), slot_idx, slot_out);
+                  perm, P, k, H / 8, reinterpret_cast<uint4*>(xp), slot_idx, slot_out, zero_out, zero_n);
 }
 
 // ---------------------------------------------------------------------------------

@@ -241,7 +241,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = tile_start[E];
+  // With shrink_in_gemm the LoRA shrink tiles (one per expert token tile) come first.
+  constexpr bool kShrinkable = kFused && CG == 1 && !kDeltaIdle;
+  const int nshrink = (kShrinkable && p.shrink_in_gemm) ? tile_start[E] / (NT / CG) : 0;
+  const int total = nshrink + tile_start[E];
+
+  auto decode_shrink = [&](int t, int& e, int& qt) {   // shrink tile t: expert e, token tile qt
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] / (NT / CG) <= t) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    qt = t - tile_start[e] / (NT / CG);
+  };
+  // the active LoRA slot of pair q (from the token's slot; -1: none or disabled)
+  auto pair_lora_slot = [&](int q) -> int {
+    const int sl = p.slot_idx[p.perm[q] / p.k];
+    if (sl < 0 || sl >= p.slots.S) return -1;
+    return (p.slots.ranks[sl] > 0 && p.slots.scal[sl] != 0.0f) ? sl : -1;
+  };
 
   auto decode = [&](int tile, int& e, int& nt, int& qt) {
     int lo = 0, hi = E - 1;   // last expert with tile_start <= tile (empty experts skipped)
@@ -265,6 +284,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     } else {
       mbar_arrive(bar);
     }
+  };
+
+  // (epilogue warps) shrink tile t in accumulator `acc`: each thread holds one stacked A row
+  // (its TMEM lane) for the tile's tokens and writes that row's ub column of every token's
+  // stacked row, scaled and rounded to bf16 where the token's slot is the row's slot, zero
+  // elsewhere; the columns no row covers (rank padding, disabled slots) are zeroed by the
+  // threads in turn; pair_slot is written; then the tile's ready flag is released.
+  auto shrink_epilogue = [&](int t, int acc, uint32_t aphase) -> bool {
+    const int quarter = warp & 3;
+    const int etid = threadIdx.x - 64;
+    const int row = quarter * 32 + lane;
+    int e, qt;
+    decode_shrink(t, e, qt);
+    const int q0 = seg[e] + qt * BN;
+    const int nvalid = min(BN, seg[e + 1] - q0);
+    epi_bar();   // every reader of the previous tile's buffers (which lslot may share) is done
+    for (int j = etid; j < nvalid; j += 128) {
+      int sl = p.slot_idx[p.perm[q0 + j] / p.k];
+      if (sl < -1 || sl >= p.slots.S) {
+        record_status(p.status, kDevBadSlot, kWhereGemmEpilogue);
+        sl = -1;
+      } else if (sl >= 0 && (p.slots.ranks[sl] <= 0 || p.slots.scal[sl] == 0.0f)) {
+        sl = -1;
+      }
+      lslot[j] = sl;
+      p.pair_slot_out[q0 + j] = sl;
+    }
+    epi_bar();
+    int s_row = -1, col = 0;
+    float sc = 0.0f;
+    if (row < p.sa_row_off[kMaxFusedSlots]) {
+      s_row = 0;
+      while (p.sa_row_off[s_row + 1] <= row) ++s_row;
+      col = p.coff[s_row] + row - p.sa_row_off[s_row];
+      sc = p.slots.scal[s_row];
+    }
+    // this thread's zero columns, etid + 128 i (i < 3: the host keeps lora_rs <= 384), as bits
+    uint32_t zmask = 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int c = etid + 128 * i;
+      if (c < p.lora_rs) {
+        int s2 = 0;
+        while (p.coff[s2 + 1] <= c) ++s2;
+        if (c - p.coff[s2] >= p.sa_row_off[s2 + 1] - p.sa_row_off[s2]) zmask |= 1u << i;
+      }
+    }
+    if (!mbar_wait(&tfull[acc], aphase, abort_flag, p.status, kWhereGemmEpilogue)) return false;
+    tc_fence_after();
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+    for (int c = 0; c < nvalid; c += 16) {   // warp-uniform bound
+      uint32_t v[16];
+      __syncwarp();   // tcgen05.ld is .aligned
+      tmem_ld_x16(taddr + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c + j < nvalid) {
+          __nv_bfloat16* urow = p.ub_out + static_cast<size_t>(q0 + c + j) * p.lora_rs;
+          if (s_row >= 0) urow[col] = __float2bfloat16_rn(lslot[c + j] == s_row ? sc * __uint_as_float(v[j]) : 0.0f);
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+            if ((zmask >> i) & 1u) urow[etid + 128 * i] = __float2bfloat16_rn(0.0f);
+        }
+      }
+    }
+    __threadfence();
+    fence_proxy_async_global();   // read next by other CTAs' TMA copies
+    tc_fence_before();
+    epi_bar();                    // every thread's rows are written (and lslot is free again)
+    if (etid == 0) red_release_add(p.shrink_ready + t, 1);
+    return true;
   };
 
   if (warp >= 2) pdl_wait();   // the epilogues read the previous kernel's LoRA rows and slots
@@ -311,9 +403,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     // Weights are constants of the layer and the tile schedule comes from the expert
     // offsets, so the weight halves of the first tile's first stages go out before the
     // previous kernel (which writes the token rows) has finished.
-    if (lane == 0 && cta0 < total) {
+    if (lane == 0 && cta0 >= nshrink && cta0 < total) {
       int e, nt, qt, wr0, wr1;
-      decode(cta0, e, nt, qt);
+      decode(cta0 - nshrink, e, nt, qt);
       weight_rows(e, nt, wr0, wr1);
       npre = min(S, kFused ? lora_stage_pos(KB) : KB);   // main stages only: the LoRA stages follow later
       for (int s2 = 0; s2 < npre; ++s2) {
@@ -339,8 +431,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     } else {   // the whole warp: lanes gather each tile's pair slots for lane 0
       int it_tile = 0;
       for (int tile = cta0; tile < total; tile += ncta, ++it_tile) {
+        if (tile < nshrink) {   // shrink tile: every active slot's A rows x the tile's token rows
+          int e, qt;
+          decode_shrink(tile, e, qt);
+          const int xr = seg[e] + qt * BN;
+          if (lane == 0) {
+            tile_slot_ring[it_tile % kTileRing] = 0u;   // no LoRA stages in a shrink tile
+            const int ea = p.sa_e1 ? 0 : e;
+            const uint32_t bytes = static_cast<uint32_t>(p.sa_row_off[kMaxFusedSlots] + BNH) * 128u;
+            for (int kb = 0; ok && kb < KB; ++kb) {
+              if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status, kWhereGemmProducer)) {
+                ok = 0;
+                break;
+              }
+              uint8_t* a = smem + stage * STAGE;
+              mbar_arrive_expect_tx(&full[stage], bytes);
+              for (int sl = 0; sl < kMaxFusedSlots; ++sl)
+                if (p.sa_row_off[sl + 1] > p.sa_row_off[sl])
+                  load(a + p.sa_row_off[sl] * 128, &p.tmap_sa[sl], stage, kb * 64,
+                       (sl * (p.sa_e1 ? 1 : E) + ea) * p.sa_R, pol_x);
+              load(a + A_BYTES, &p.tmap_x, stage, kb * 64, xr, pol_x);
+              issued_mask |= 1u << stage;
+              issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+              if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+          continue;
+        }
         int e, nt, qt, wr0, wr1;
-        decode(tile, e, nt, qt);
+        decode(tile - nshrink, e, nt, qt);
         weight_rows(e, nt, wr0, wr1);
         const int xr = seg[e] + qt * BN;
         const int xh = xr + static_cast<int>(crank) * BNH;   // this CTA's token rows
@@ -353,7 +476,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
         for (int u = 0; u < kSlotLoads; ++u) {
           const int j = lane + 32 * u;
-          slv[u] = j < nv ? p.pair_slot[xr + j] : -1;
+          slv[u] = j >= nv ? -1 : (nshrink > 0 ? pair_lora_slot(xr + j) : p.pair_slot[xr + j]);
         }
         const int kb_lora = lora_stage_pos(KB);
         if (lane == 0)
@@ -369,6 +492,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           tile_slot_ring[it_tile % kTileRing] = smask;
           const int lb_off = p.lora_b_e1 ? e * p.N : 0;   // a shared B has one expert's rows
           if (ok) ok = issue(&p.tmap_w, wr0, wr1, (kb_lora - 1) * 64, &p.tmap_x, xh);
+          if (ok && smask != 0u && nshrink > 0) {   // this tile's ub rows come from its shrink tile
+            ok = wait_flag_geq(p.shrink_ready + tile_start[e] / (NT / CG) + qt, 1, abort_flag, p.status,
+                               kWhereGemmProducer);
+            fence_proxy_async_global();   // written by st.global, read next by TMA
+          }
           if (p.lora_packed) {   // LoRA expand stages over the stacked ranks, per 64-column panel
             const int prow = ((p.lora_b_e1 ? 0 : e) * NT + nt) * 128;
             const int npan = (p.lora_rs + 63) >> 6;
@@ -497,15 +625,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     int acc = 0, chunk = 0;   // chunk: the xchg buffer alternates per 16-token chunk
     uint32_t aphase = 0, dfphase = 0;
     for (int tile = cta0; tile < total; tile += ncta) {
+      if (tile < nshrink) {
+        if (!shrink_epilogue(tile, acc, aphase)) break;
+        release(&tempty[acc]);
+        if (++acc == kAccBufs) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+        continue;
+      }
       int e, nt, qt;
-      decode(tile, e, nt, qt);
+      decode(tile - nshrink, e, nt, qt);
       const int q0 = seg[e] + qt * BN;
       const int nvalid = min(BN, seg[e + 1] - q0);
       // the delta accumulator holds this tile's LoRA only if some slot was present
       unsigned lmask = 0;
       if (delta_acc) {
         for (int j = lane; j < nvalid; j += 32) {
-          const int sl = p.pair_slot[q0 + j];
+          const int sl = nshrink > 0 ? pair_lora_slot(q0 + j) : p.pair_slot[q0 + j];
           if (sl >= 0 && sl < kMaxFusedSlots) lmask |= 1u << sl;
         }
         lmask = __reduce_or_sync(0xffffffffu, lmask);
@@ -624,8 +761,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     int acc = 0;
     uint32_t aphase = 0;
     for (int tile = cta0; tile < total; tile += ncta) {
+      if (tile < nshrink) {
+        if (!shrink_epilogue(tile, acc, aphase)) break;
+        release(&tempty[acc]);
+        if (++acc == kAccBufs) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+        continue;
+      }
       int e, nt, qt;
-      decode(tile, e, nt, qt);
+      decode(tile - nshrink, e, nt, qt);
       const int col = nt * 128 + row;
       const int q0 = seg[e] + qt * BN;
       const int nvalid = min(BN, seg[e + 1] - q0);

@@ -111,6 +111,27 @@ struct GemmParams {
   int lora_packed;
   int lora_rs;                   // Rs, a multiple of 16
   uint32_t lora_panel_slots[kMaxLoraPanels];
+  // The LoRA shrink as tiles of this GEMM (shrink_in_gemm = 1; packed B, single-CTA tiles):
+  // one shrink tile per (expert, token tile), all of them in front of the GEMM tiles in the
+  // schedule.  Its stages hold every active slot's rank rows of A for the expert (tmap_sa[s],
+  // box rows = ranks[s], at row sa_row_off[s] of the weight half; at most 128 rows) and the
+  // tile's token rows of X (tmap_x, as the GEMM tiles); its epilogue writes the tile's
+  // stacked ub rows (ub_out [P, lora_rs], columns coff) and pair_slot, then counts
+  // shrink_ready[shrink tile] up (release).  A GEMM tile's producer waits for its own shrink
+  // tile (acquire) before it issues the LoRA stages that read those ub rows.  The pairs'
+  // slots for the slot masks come from slot_idx and perm.
+  int shrink_in_gemm;
+  CUtensorMap tmap_sa[kMaxFusedSlots];
+  int sa_row_off[kMaxFusedSlots + 1];
+  int sa_e1;                     // A is [S, 1, R, K]: one set per slot
+  int sa_R;                      // rank stride of A's rows: (s * Ea + e) * sa_R
+  int coff[kMaxFusedSlots + 1];  // stacked ub columns of slot s
+  __nv_bfloat16* ub_out;         // [P, lora_rs]
+  int32_t* pair_slot_out;        // [P]
+  const int32_t* perm;           // [P]
+  const int32_t* slot_idx;       // [T]
+  int k;
+  int* shrink_ready;             // [shrink tiles], zero when the kernel starts
 };
 constexpr int kMaxGemmSmem = 227 * 1024;   // dynamic shared memory a CTA may have
 int gemm_smem_bytes(int bn, int cg, int stages, int E, int lora_R, int act_fused, int y_tma);
@@ -146,7 +167,8 @@ cudaError_t launch_grouped_gemm_fp8(const GemmF8Params& p, int bn, int grid, cud
 // ---------------------------------------------------------------- elementwise
 cudaError_t launch_permute(const __nv_bfloat16* x, const int32_t* perm, int P, int k, int H,
                            __nv_bfloat16* xp, cudaStream_t stream, bool pdl = false,
-                           const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr);
+                           const int32_t* slot_idx = nullptr, int32_t* slot_out = nullptr,
+                           int* zero_out = nullptr, int zero_n = 0);
 cudaError_t launch_activation(const __nv_bfloat16* g, const __nv_bfloat16* d, int P, int I,
                               __nv_bfloat16* a, cudaStream_t stream, bool pdl = false);
 // FP8 group quantisation of rows (gathered through perm[q] / k when perm is set):
@@ -288,6 +310,8 @@ struct PermuteShrinkParams {
   __nv_bfloat16* ub;             // [S, P, RU]
   int32_t* pair_slot;            // [P]
   uint32_t* status;
+  int* zero_out;                 // [zero_n] cleared (ready flags of the GEMMs that follow), or null
+  int zero_n;
 };
 constexpr int kPermuteShrinkMaxRows = 32;   // stacked active rank rows the fused kernel takes
 size_t permute_shrink_smem_bytes(int nr_max, int E, int H);

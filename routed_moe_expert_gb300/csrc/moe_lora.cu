@@ -57,8 +57,11 @@ struct Layout {
   size_t header, ids, wts, offsets, perm, inv, hist, base, total;
   size_t xp, g, d, a, v, y, pslot, ub;
   size_t sx, sa;   // FP8 path: group scales of the gate_up and down GEMM inputs
+  size_t ready;    // ready flags of the shrink tiles inside the gate_up and down GEMMs
   size_t bytes;
 };
+// Shrink tiles of one GEMM: one per (expert, token tile), at most P / 16 + E.
+size_t ready_flags(size_t P, int E) { return P / 16 + static_cast<size_t>(E) + 2; }
 
 Layout layout_for(int T, int H, int I, int E, int k, int R, int S) {
   Layout L;
@@ -93,6 +96,7 @@ Layout layout_for(int T, int H, int I, int E, int k, int R, int S) {
   // region ([P, I] bytes, written after the activation has read g); their group scales:
   L.sx = take(P * ((static_cast<size_t>(H) + 127) / 128) * 4);
   L.sa = take(P * ((static_cast<size_t>(I) + 127) / 128) * 4);
+  L.ready = take(R > 0 ? 2 * ready_flags(P, E) * 4 : 0);
   L.bytes = off;
   return L;
 }
@@ -515,6 +519,39 @@ bool fuse_lora_maps_packed(moe_lora_handle* h, GemmParams& gp, const moe_lora_ar
   gp.slots = make_slots(a);
   gp.P = P;
   gp.pair_slot = pair_slot;
+  return true;
+}
+
+// The LoRA shrink as the first tiles of a fused-LoRA GEMM with a packed B (see GemmParams):
+// per active slot a tensor map of its rank rows of A [S*Ea*R rows, K], the stacked ub and
+// pair_slot outputs, and the ready flags.  Needs the active ranks to be multiples of 8 (each
+// slot's rows then start on a swizzle-atom boundary) and at most 128 of them (one MMA M);
+// returns false when they are not, and the separate shrink kernel runs instead.
+bool shrink_in_gemm_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* A, int K,
+                         bool a_e1, __nv_bfloat16* ub, int32_t* pair_slot, int* ready) {
+  if (a->S > kMaxFusedSlots) return false;
+  const uint64_t a_rows = static_cast<uint64_t>(a->S) * (a_e1 ? 1 : a->E) * a->R;
+  int off = 0;
+  for (int s = 0; s < kMaxFusedSlots; ++s) {
+    gp.sa_row_off[s] = off;
+    const int rows = (s < a->S && a->h_ranks[s] > 0 && a->h_scalings[s] != 0.0f) ? a->h_ranks[s] : 0;
+    if (rows % 8 != 0) return false;
+    if (rows > 0 && !make_tmap(h->encode, &gp.tmap_sa[s], A, a_rows, K, static_cast<uint32_t>(rows))) return false;
+    off += rows;
+  }
+  gp.sa_row_off[kMaxFusedSlots] = off;
+  if (off == 0 || off > 128) return false;
+  int coff[kMaxFusedSlots + 1];
+  const int rs = stacked_cols(a->h_ranks, a->S, coff);
+  if (rs != gp.lora_rs || rs > 384) return false;
+  for (int s = 0; s <= kMaxFusedSlots; ++s) gp.coff[s] = coff[s <= a->S ? s : a->S];
+  gp.sa_e1 = a_e1 ? 1 : 0;
+  gp.sa_R = a->R;
+  gp.ub_out = ub;
+  gp.pair_slot_out = pair_slot;
+  gp.perm = nullptr;   // set by the caller
+  gp.shrink_ready = ready;
+  gp.shrink_in_gemm = 1;
   return true;
 }
 
@@ -1104,6 +1141,46 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     // needs the tensor-core shrink, which can write the stacked ub rows)
     const bool gu_packed = fuse_all && !permute_shrink && a->lora_B_gu_packed != nullptr;
     const bool dn_packed = fuse_all && a->lora_B_dn_packed != nullptr;
+    // The GEMMs' parameters first: with a packed B on single-CTA tiles the LoRA shrink runs as
+    // the first tiles of the GEMM itself (no shrink kernel), when its A rows fit one MMA.
+    const bool shrink_ok = !(a->flags & MOE_LORA_FLAG_SEPARATE_SHRINK) && bn <= 128;
+    int* ready = reinterpret_cast<int*>(ws + L.ready);
+    const size_t nflags = ready_flags(static_cast<size_t>(P), E);
+    GemmParams gu;
+    std::memset(&gu, 0, sizeof(gu));
+    gu.out = act;   // the activation, written by the GEMM's epilogue
+    gu.offsets = offsets;
+    gu.status = status;
+    gu.E = E;
+    gu.N = 2 * I;
+    gu.K = H;
+    gu.gated = 2;
+    gu.cta_pair = pair_tiles(bn, 2 * I);
+    if (fuse_all && !(gu_packed ? fuse_lora_maps_packed(h, gu, a, a->lora_B_gu_packed, 2 * I, ub, pair_slot, P, bn)
+                                : fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)))
+      return MOE_LORA_ERR_CUDA;
+    const bool gu_in_gemm = gu_packed && shrink_ok && gu.cta_pair == 1 &&
+                            shrink_in_gemm_maps(h, gu, a, a->lora_A_gu, H, so, ub, pair_slot, ready);
+    GemmParams dn;
+    std::memset(&dn, 0, sizeof(dn));
+    if (y_bf16) dn.out = reinterpret_cast<__nv_bfloat16*>(y);
+    else dn.out_f32 = y;
+    dn.offsets = offsets;
+    dn.status = status;
+    dn.E = E;
+    dn.N = H;
+    dn.K = I;
+    dn.gated = 0;
+    dn.cta_pair = pair_tiles(bn0, H);
+    // the down GEMM adds its LoRA stages to the main accumulator, so it keeps the full tile
+    if (fuse_all && !(dn_packed ? fuse_lora_maps_packed(h, dn, a, a->lora_B_dn_packed, H, ub, pair_slot, P, bn0, so)
+                                : fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)))
+      return MOE_LORA_ERR_CUDA;
+    const bool dn_in_gemm = dn_packed && shrink_ok && dn.cta_pair == 1 &&
+                            shrink_in_gemm_maps(h, dn, a, a->lora_A_dn, I, false, ub, pair_slot, ready + nflags);
+    gu.perm = dn.perm = perm;
+    gu.slot_idx = dn.slot_idx = a->slot_idx;
+    gu.k = dn.k = k;
     if (permute_shrink) {   // the permute and the gate_up LoRA shrink in one pass over the token rows
       PermuteShrinkParams ps;
       std::memset(&ps, 0, sizeof(ps));
@@ -1124,62 +1201,46 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       ps.ub = ub;
       ps.pair_slot = pair_slot;
       ps.status = status;
+      if (gu_in_gemm || dn_in_gemm) {   // it also clears the ready flags of the GEMMs' shrink tiles
+        ps.zero_out = ready;
+        ps.zero_n = static_cast<int>(2 * nflags);
+      }
       int grid = (P + 63) / 64 + E;   // tiles of 64 pairs (at most), two CTAs per SM
       if (grid > 2 * h->num_sms) grid = 2 * h->num_sms;
       ML_LAUNCH(h, launch_permute_shrink(ps, grid, stream, pdl), "permute + LoRA shrink launch");
       prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     } else {
-      ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl),
+      // the permute also clears the ready flags of the GEMMs' shrink tiles
+      const bool flags_used = gu_in_gemm || dn_in_gemm;
+      ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
+                                  nullptr, nullptr, flags_used ? ready : nullptr,
+                                  flags_used ? static_cast<int>(2 * nflags) : 0),
                 "permute launch");
       prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
       if (fuse_all) {
         prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
-        st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
-                               so, gu_packed);
-        if (st != MOE_LORA_OK) return st;
+        if (!gu_in_gemm) {
+          st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
+                                 so, gu_packed);
+          if (st != MOE_LORA_OK) return st;
+        }
         prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
       }
     }
     prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
-    GemmParams gu;
-    std::memset(&gu, 0, sizeof(gu));
-    gu.out = act;   // the activation, written by the GEMM's epilogue
-    gu.offsets = offsets;
-    gu.status = status;
-    gu.E = E;
-    gu.N = 2 * I;
-    gu.K = H;
-    gu.gated = 2;
-    gu.cta_pair = pair_tiles(bn, 2 * I);
-    if (fuse_all && !(gu_packed ? fuse_lora_maps_packed(h, gu, a, a->lora_B_gu_packed, 2 * I, ub, pair_slot, P, bn)
-                                : fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)))
-      return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, gu, a->w1, xp, P, bn, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
     if (fuse_all) {
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
-      st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
-                             false, dn_packed);
-      if (st != MOE_LORA_OK) return st;
+      if (!dn_in_gemm) {
+        st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
+                               false, dn_packed);
+        if (st != MOE_LORA_OK) return st;
+      }
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
     }
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
-    GemmParams dn;
-    std::memset(&dn, 0, sizeof(dn));
-    if (y_bf16) dn.out = reinterpret_cast<__nv_bfloat16*>(y);
-    else dn.out_f32 = y;
-    dn.offsets = offsets;
-    dn.status = status;
-    dn.E = E;
-    dn.N = H;
-    dn.K = I;
-    dn.gated = 0;
-    dn.cta_pair = pair_tiles(bn0, H);
-    // the down GEMM adds its LoRA stages to the main accumulator, so it keeps the full tile
-    if (fuse_all && !(dn_packed ? fuse_lora_maps_packed(h, dn, a, a->lora_B_dn_packed, H, ub, pair_slot, P, bn0, so)
-                                : fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)))
-      return MOE_LORA_ERR_CUDA;
     st = enqueue_gemm(h, dn, a->w2, act, P, bn0, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);

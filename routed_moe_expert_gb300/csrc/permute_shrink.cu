@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(kPsThreads, 2) permute_shrink_kernel(const Per
   const uint64_t pol_stream = l2_policy_evict_first();
   pdl_wait();    // the routing (perm, offsets) comes from the previous kernel
   pdl_trigger();
+  // the ready flags of the shrink tiles of the GEMMs that follow start at zero
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n; i += gridDim.x * blockDim.x) p.zero_out[i] = 0;
   if (warp == 1) build_tile_schedule(p.offsets, E, kPsTile, 1, seg, tile_start);
   tc_fence_before();
   __syncthreads();

@@ -1,7 +1,8 @@
 """Expand-ready (packed) LoRA B copies: the pack's layout, bit for bit, against the layout rule
-written out in torch; the layer with packed copies against the same layer with the per-slot
-LoRA stages (equal outputs: a pair's stacked shrink row is zero outside its own slot, so the
-other slots' columns add exact zeros) and against the oracle."""
+written out in torch; the layer with packed copies and separate shrink kernels against the same
+layer with the per-slot LoRA stages (equal outputs: a pair's stacked shrink row is zero outside
+its own slot, so the other slots' columns add exact zeros); and the layer with the shrinks run
+as tiles of the expert GEMMs against the oracle, with the launches it saves counted."""
 import numpy as np
 import pytest
 import torch
@@ -58,9 +59,11 @@ def test_pack_lora_b_layout_bit_exact(handle, S, Eb, N, R, ranks, gated):
     assert torch.equal(got.cpu().view(torch.int16), ref.view(torch.int16))
 
 
-def _run_pair(h, cfg, seed, flags=0, device_inputs=False):
-    """The layer twice on the same inputs, per-slot and packed LoRA stages; returns both outputs
-    (checked against each other and the oracle)."""
+def _run_pair(h, cfg, seed, flags=0, device_inputs=False, saved_launches=None):
+    """The layer on the same inputs with per-slot LoRA stages, with packed stages and separate
+    shrink kernels (equal to the first), and with packed stages and the shrinks as tiles of the
+    GEMMs where they fit (the shrink's products are then accumulated with the operands'
+    roles swapped, so it is held to the oracle's tolerance); returns the first and the last."""
     inp = wl.make_inputs(cfg, seed=seed, device="cuda" if device_inputs else "cpu")
     g = gh.to_dev(inp)
     ws = pkg.alloc_workspace(g["T"], cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
@@ -72,36 +75,49 @@ def _run_pair(h, cfg, seed, flags=0, device_inputs=False):
     bgu = pkg.moe_lora_pack_lora_b(h, g["lora_B_gu"], g["ranks"], 1)
     bdn = pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], g["ranks"], 0)
     assert bdn.shape[0] == (1 if so else cfg.E) * ((cfg.H + 127) // 128) * 128
-    out = pkg.moe_lora_forward(
-        h, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], routing_method=g["method"],
-        correction_bias=g["correction_bias"], routed_scaling_factor=g["rsf"],
-        lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"], lora_B_dn=g["lora_B_dn"],
-        slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"], flags=flags, workspace=ws,
-        lora_B_gu_packed=bgu, lora_B_dn_packed=bdn)
-    torch.cuda.synchronize()
-    st, word = pkg.moe_lora_check_status(ws)
-    assert st == 0, f"device status {word:#x}"
-    assert torch.equal(out, base), f"packed and per-slot LoRA stages differ: {int((out != base).sum())} elements"
+    def packed(extra):
+        o = pkg.moe_lora_forward(
+            h, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], routing_method=g["method"],
+            correction_bias=g["correction_bias"], routed_scaling_factor=g["rsf"],
+            lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
+            lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"],
+            flags=flags | extra, workspace=ws, lora_B_gu_packed=bgu, lora_B_dn_packed=bdn)
+        torch.cuda.synchronize()
+        st, word = pkg.moe_lora_check_status(ws)
+        assert st == 0, f"device status {word:#x}"
+        return o
+
+    n0 = h.launch_count()
+    sep = packed(pkg.FLAG_SEPARATE_SHRINK)
+    n1 = h.launch_count()
+    assert torch.equal(sep, base), f"packed and per-slot LoRA stages differ: {int((sep != base).sum())} elements"
+    out = packed(0)
+    n2 = h.launch_count()
+    if saved_launches is not None:   # shrink kernels that ran as GEMM tiles instead
+        assert (n1 - n0) - (n2 - n1) == saved_launches, ((n1 - n0), (n2 - n1))
     ref = gh.oracle(inp, lazy=device_inputs)
     gh.assert_close(out.float().cpu().numpy(), ref["out"], cfg.name)
+    gh.assert_close(out.float().cpu().numpy(), base.float().cpu().numpy(), cfg.name + " vs per-slot")
     return base, out
 
 
-@pytest.mark.parametrize("T,E,k,ranks,scalings,shared", [
-    (96, 16, 4, (8, 16, 32, 64), (2.0, 1.0, 0.5, 0.25), False),   # 64-token tiles, tensor-core shrinks
-    (96, 16, 4, (8, 16), (2.0, 0.5), False),                      # <= 32 stacked ranks: permute + shrink
-    (64, 16, 4, (8, 32), (2.0, 0.5), True),                       # shared-outer down B
-    (96, 16, 4, (16, 24, 0, 8), (1.0, 0.0, 1.0, 2.0), False),     # a disabled slot and a rank-0 slot
-    (600, 8, 2, (8, 16, 32, 64), (2.0, 1.0, 0.5, 0.25), False),   # 256-token CTA-pair tiles
-], ids=["four-slots", "few-ranks", "shared-outer", "disabled-slots", "pair-tiles"])
-def test_packed_lora_b_equals_per_slot_stages(handle, T, E, k, ranks, scalings, shared):
+@pytest.mark.parametrize("T,E,k,ranks,scalings,shared,saved", [
+    (96, 16, 4, (8, 16, 32, 64), (2.0, 1.0, 0.5, 0.25), False, 2),   # 64-token tiles: both shrinks in the GEMMs
+    (96, 16, 4, (8, 16), (2.0, 0.5), False, 1),                      # <= 32 stacked ranks: permute + shrink
+    (64, 16, 4, (8, 32), (2.0, 0.5), True, 2),                       # shared-outer, 32-token tiles
+    (96, 16, 4, (16, 24, 0, 8), (1.0, 0.0, 1.0, 2.0), False, 1),     # a disabled slot and a rank-0 slot
+    (600, 8, 2, (8, 16, 32, 64), (2.0, 1.0, 0.5, 0.25), False, 0),   # 256-token CTA-pair tiles
+    (96, 16, 4, (64, 64, 8), (1.0, 0.5, 2.0), False, 0),             # 136 active rank rows: too many
+], ids=["four-slots", "few-ranks", "shared-outer", "disabled-slots", "pair-tiles", "many-ranks"])
+def test_packed_lora_b_equals_per_slot_stages(handle, T, E, k, ranks, scalings, shared, saved):
     cfg = wl.LayerConfig("pk", T=T, H=512, I=256, E=E, top_k=k, ranks=ranks, scalings=scalings,
                          slot_mode="uniform_none10", shared_outer=shared)
-    _run_pair(handle, cfg, seed=T + len(ranks), flags=pkg.FLAG_SHARED_OUTER if shared else 0)
+    _run_pair(handle, cfg, seed=T + len(ranks), flags=pkg.FLAG_SHARED_OUTER if shared else 0,
+              saved_launches=saved)
 
 
 def test_packed_lora_b_multi_slot_config(handle):
-    _run_pair(handle, wl.CONFIGS["multi_slot"], seed=0, device_inputs=True)
+    _run_pair(handle, wl.CONFIGS["multi_slot"], seed=0, device_inputs=True, saved_launches=2)
 
 
 def test_packed_lora_b_graph_replay(handle):
@@ -127,8 +143,10 @@ def test_packed_lora_b_graph_replay(handle):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
         pkg.moe_lora_forward(handle, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], stream=s, **kw)
+    eager = out.clone()   # the warm-up forward's output (the shrinks ran inside the GEMMs)
     for _ in range(3):
         out.zero_()
         graph.replay()
         torch.cuda.synchronize()
-        assert torch.equal(out, base)
+        assert torch.equal(out, eager)
+    gh.assert_close(eager.float().cpu().numpy(), base.float().cpu().numpy(), "graph vs per-slot")
