@@ -243,7 +243,7 @@ def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
     # The expand-ready LoRA B copies are made once, like the weights (a weight-load step of the
     # library); the bf16 layer's fused LoRA stages read them.
     packed = {}
-    if w8 is None and w4 is None and cfg.S > 0 and not args.per_slot_lora:
+    if w4 is None and cfg.S > 0 and not args.per_slot_lora:
         packed = dict(lora_B_gu_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_gu"], cfg.ranks, 1),
                       lora_B_dn_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], cfg.ranks, 0))
 
@@ -257,7 +257,7 @@ def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
                   slot_idx=g["slot_idx"] if slot is None else slot, ranks=cfg.ranks, scalings=cfg.scalings,
                   flags=flags, out=o, workspace=ws, prof_events=prof, outputs=outputs)
         if w8 is not None:
-            return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw)
+            return pkg.moe_lora_forward_fp8(h, hid, lg, *w8, k, **kw, **packed)
         if w4 is not None:
             return pkg.moe_lora_forward_nvfp4(h, hid, lg, *w4, k, **kw)
         return pkg.moe_lora_forward(h, hid, lg, g["w1"], g["w2"], k, **kw, **packed)
@@ -493,7 +493,7 @@ def run_gpu(args):
             "l2": f"inputs larger than L2: {touched} touched experts = {touched * w_bytes_expert / 1e9:.2f} GB of weights per step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "forward_flags": args.flags,
-            "lora_b": ("per slot" if (args.per_slot_lora or w8 is not None or w4 is not None)
+            "lora_b": ("per slot" if (args.per_slot_lora or w4 is not None)
                        else "expand-ready copies (moe_lora_pack_lora_b, made once at set-up)"),
             "step_bytes": step_bytes, "step_flops": step_flops,
             "step_roofline_frac": max(step_bytes / (peaks["hbm_gbs"] * 1e9),

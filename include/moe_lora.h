@@ -291,11 +291,15 @@ typedef struct {
    GEMM and the bf16 activation for the down GEMM; each GEMM sums, per 128-wide K block,
    the e4m3 products times the two block scales, in fp32.  The LoRA weights and the LoRA
    chain stay bf16 and read the unquantised hidden rows and activation, as in the pages'
-   FP8 flow.  Every other rule (routing, rounding points, slots, ranks, scalings, flags
-   except MOE_LORA_FLAG_UNFUSED_LORA, which is implied) is that of moe_lora_forward; the
-   LoRA placement is the narrow one (side-stream gate_up LoRA, down expand in the down
-   GEMM's epilogue) at every token count, with token tiles of at most 64.  H and I must
-   be multiples of 128.  The workspace is moe_lora_workspace_size() of the same shape.
+   FP8 flow.  Every other rule (routing, rounding points, slots, ranks, scalings, flags) is
+   that of moe_lora_forward, with token tiles of at most 64.  LoRA placement: with both
+   expand-ready B copies (lora_B_gu_packed, lora_B_dn_packed) and the fused conditions of
+   moe_lora_forward (32-token tiles or wider, R a multiple of 8, S <= 8, S*R <= 256, no
+   MOE_LORA_FLAG_UNFUSED_LORA), the fused one: tensor-core shrinks on the bf16 permuted
+   rows and activation, the expands as bf16 K-stages inside the FP8 GEMMs (the gate_up
+   delta kept in its own accumulator and written as its own bf16 tensor, which the
+   activation adds, as the pages do); otherwise the narrow one (side-stream gate_up LoRA,
+   down expand in the down GEMM's epilogue).  H and I must be multiples of 128.  The workspace is moe_lora_workspace_size() of the same shape.
    Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
 moe_lora_status moe_lora_forward_fp8(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_fp8_weights* w,
                                      moe_lora_bf16* out, void* workspace, size_t workspace_bytes,

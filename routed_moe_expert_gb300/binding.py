@@ -490,14 +490,16 @@ def moe_lora_forward_fp8(handle: Handle, hidden, router_logits, w1_q, w1_scale, 
                          routing_method=0, correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None,
                          lora_B_gu=None, lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(),
                          flags=0, out=None, workspace=None, outputs=None, prof_events=None, stream=None,
-                         n_group=1, topk_group=1) -> torch.Tensor:
+                         n_group=1, topk_group=1, lora_B_gu_packed=None, lora_B_dn_packed=None) -> torch.Tensor:
     """The layer with FP8 block-scale expert weights: w1_q [E, 2I, H] and w2_q [E, H, I] hold
     e4m3 bit patterns (uint8), w1_scale [E, 2I/128, H/128] and w2_scale [E, H/128, I/128]
-    the float32 scales of their 128 x 128 blocks.  Returns out [T, H] bf16."""
+    the float32 scales of their 128 x 128 blocks.  With both expand-ready LoRA B copies
+    (moe_lora_pack_lora_b) the fused LoRA placement runs.  Returns out [T, H] bf16."""
     check_fp8_weights(w1_q, w1_scale, w2_q, w2_scale)
     a, keep = make_args(hidden, router_logits, w1_q, w2_q, top_k, routing_method, correction_bias,
                         routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
-                        scalings, flags, outputs, prof_events, n_group, topk_group, weight_dtype=torch.uint8)
+                        scalings, flags, outputs, prof_events, n_group, topk_group, weight_dtype=torch.uint8,
+                        lora_B_gu_packed=lora_B_gu_packed, lora_B_dn_packed=lora_B_dn_packed)
     w = Fp8Weights()
     w.w1 = _ptr(w1_q, torch.uint8, "w1_q")
     w.w1_scale = _ptr(w1_scale, torch.float32, "w1_scale")

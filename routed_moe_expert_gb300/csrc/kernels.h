@@ -159,8 +159,21 @@ struct GemmF8Params {
   int lora_b_e1;
   const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
+  // Fused LoRA expand from the expand-ready B (lora_packed = 1, replaces lora_v): after a
+  // tile's main K blocks, one bf16 stage per 64-column panel of the stacked ranks (A' = the
+  // tile's rows of the packed B, tmap_lbp; B' = the tile's stacked ub rows, tmap_lup), issued
+  // when a slot of lora_panel_slots[j] is among the tile's pairs (pair_slot), as tcgen05
+  // kind::f16 MMAs into a delta accumulator.  The epilogue adds the delta to the fp32 sum
+  // (gated = 0), or stores it rounded to bf16 as d_out [P, N] in the logical column order,
+  // zero for pairs without an adapter (gated = 1: the gate_up delta the activation adds).
+  CUtensorMap tmap_lbp;          // [Eb*NT*128 rows, Rs cols] bf16, box {64, 64}
+  CUtensorMap tmap_lup;          // [P rows, Rs cols] bf16, box {64, BN}
+  int lora_packed;
+  int lora_rs;
+  uint32_t lora_panel_slots[kMaxLoraPanels];
+  __nv_bfloat16* d_out;
 };
-int gemm_fp8_smem_bytes(int bn, int stages, int E, int lora_R);
+int gemm_fp8_smem_bytes(int bn, int stages, int E, int lora_R, int lora_packed = 0);
 int gemm_fp8_stage_bytes(int bn);
 cudaError_t launch_grouped_gemm_fp8(const GemmF8Params& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 

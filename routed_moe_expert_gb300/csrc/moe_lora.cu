@@ -389,8 +389,9 @@ moe_lora_status enqueue_gemm_fp8(moe_lora_handle* h, GemmF8Params& gp, const uin
     return MOE_LORA_ERR_CUDA;
   if (!make_tmap_e4m3(h->encode, &gp.tmap_x, X, static_cast<uint64_t>(P), gp.K, bn)) return MOE_LORA_ERR_CUDA;
   const int lora_R = gp.lora_v != nullptr ? gp.slots.R : 0;
-  const int budget = (bn <= 32 && gp.gated != 0 ? 160 : 200) * 1024;
-  int stages = (budget - gemm_fp8_smem_bytes(bn, 0, gp.E, lora_R)) / (gemm_fp8_stage_bytes(bn) + 16);
+  // narrow gate_up tiles leave room for the side-stream LoRA kernel (none beside packed stages)
+  const int budget = (bn <= 32 && gp.gated != 0 && !gp.lora_packed ? 160 : 200) * 1024;
+  int stages = (budget - gemm_fp8_smem_bytes(bn, 0, gp.E, lora_R, gp.lora_packed)) / (gemm_fp8_stage_bytes(bn) + 16);
   if (stages > 16) stages = 16;
   if (stages < 2) stages = 2;
   gp.stages = stages;
@@ -493,25 +494,36 @@ int stacked_cols(const int32_t* ranks, int S, int* coff) {
 
 // Tensor maps of the fused LoRA stages from the expand-ready (packed) B [Eb*NT*128, Rs] and
 // the stacked ub [P, Rs], and the slots whose columns meet each 64-column panel.
+bool packed_lora_tmaps(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_bf16* Bp, int N, bool gated,
+                       bool b_e1, const __nv_bfloat16* ub, int P, int ub_box_rows, CUtensorMap* lbp, CUtensorMap* lup,
+                       int* rs_out, uint32_t* panel_slots) {
+  int coff[kMaxFusedSlots + 1];
+  if (a->S > kMaxFusedSlots) return false;
+  const int rs = stacked_cols(a->h_ranks, a->S, coff);
+  const int npan = (rs + 63) / 64;
+  if (rs == 0 || npan > kMaxLoraPanels) return false;
+  const int NT = gated ? (N >> 7) : ((N + 127) >> 7);
+  const int Eb = b_e1 ? 1 : a->E;
+  if (!make_tmap(h->encode, lbp, Bp, static_cast<uint64_t>(Eb) * NT * 128, static_cast<uint64_t>(rs), 64)) return false;
+  if (!make_tmap(h->encode, lup, ub, static_cast<uint64_t>(P), static_cast<uint64_t>(rs),
+                 static_cast<uint32_t>(ub_box_rows)))
+    return false;
+  for (int j = 0; j < kMaxLoraPanels; ++j) panel_slots[j] = 0;
+  for (int s = 0; s < a->S; ++s) {
+    if (a->h_ranks[s] <= 0 || a->h_scalings[s] == 0.0f) continue;   // never in pair_slot
+    for (int j = coff[s] / 64; j * 64 < coff[s + 1]; ++j) panel_slots[j] |= 1u << s;
+  }
+  *rs_out = rs;
+  return true;
+}
+
 bool fuse_lora_maps_packed(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* Bp,
                            int N, const __nv_bfloat16* ub, const int32_t* pair_slot, int P, int bn,
                            bool b_e1 = false) {
-  int coff[kMaxFusedSlots + 1];
-  const int rs = stacked_cols(a->h_ranks, a->S, coff);
-  const int npan = (rs + 63) / 64;
-  if (a->S > kMaxFusedSlots || rs == 0 || npan > kMaxLoraPanels) return false;
-  const int NT = gp.gated ? (N >> 7) : ((N + 127) >> 7);
-  const int Eb = b_e1 ? 1 : a->E;
-  if (!make_tmap(h->encode, &gp.tmap_lbp, Bp, static_cast<uint64_t>(Eb) * NT * 128, static_cast<uint64_t>(rs), 64))
+  int rs = 0;
+  if (!packed_lora_tmaps(h, a, Bp, N, gp.gated != 0, b_e1, ub, P, bn / (gp.cta_pair == 2 ? 2 : 1), &gp.tmap_lbp,
+                         &gp.tmap_lup, &rs, gp.lora_panel_slots))
     return false;
-  if (!make_tmap(h->encode, &gp.tmap_lup, ub, static_cast<uint64_t>(P), static_cast<uint64_t>(rs),
-                 static_cast<uint32_t>(bn / (gp.cta_pair == 2 ? 2 : 1))))
-    return false;
-  for (int j = 0; j < kMaxLoraPanels; ++j) gp.lora_panel_slots[j] = 0;
-  for (int s = 0; s < a->S; ++s) {
-    if (a->h_ranks[s] <= 0 || a->h_scalings[s] == 0.0f) continue;   // never in pair_slot
-    for (int j = coff[s] / 64; j * 64 < coff[s + 1]; ++j) gp.lora_panel_slots[j] |= 1u << s;
-  }
   gp.lora_fused = 1;
   gp.lora_packed = 1;
   gp.lora_rs = rs;
@@ -975,6 +987,101 @@ moe_lora_status enqueue_unfused_lora_path(moe_lora_handle* h, const moe_lora_arg
   return MOE_LORA_OK;
 }
 
+// FP8 block-scale weights with the fused LoRA placement (needs the expand-ready B copies):
+// permute + quantise the hidden rows for the FP8 gate_up GEMM and permute them in bf16 for
+// the LoRA shrink; the tensor-core shrink writes the stacked ub rows; the FP8 gate_up GEMM
+// runs the gate_up expand as bf16 K-stages into its own accumulator and writes g and the
+// bf16 delta d separately; the activation adds them (as on the side-stream placement); the
+// down shrink reads the bf16 activation, which is then quantised for the FP8 down GEMM, whose
+// LoRA K-stages add the down delta to its fp32 sum.
+moe_lora_status enqueue_fp8_fused_lora(moe_lora_handle* h, const moe_lora_args* a, uint8_t* ws, const Layout& L,
+                                       int32_t* perm, int32_t* offsets, __nv_bfloat16* xp, __nv_bfloat16* g,
+                                       __nv_bfloat16* d, __nv_bfloat16* act, float* y, int32_t* pair_slot,
+                                       __nv_bfloat16* ub, const LoraSlots& slots, uint32_t* status,
+                                       cudaStream_t stream, const moe_lora_fp8_weights* f8) {
+  const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
+  const int P = T * k;
+  const bool so = (a->flags & MOE_LORA_FLAG_SHARED_OUTER) != 0;
+  const bool pdl = !(a->flags & MOE_LORA_FLAG_NO_PDL);
+  const int bn = std::min(pick_bn(P, E), 64);
+  uint8_t* xp8 = reinterpret_cast<uint8_t*>(xp);   // e4m3 permuted hidden rows [P, H] bytes
+  uint8_t* a8 = reinterpret_cast<uint8_t*>(g);     // e4m3 activation [P, I] (after g is read)
+  float* sx = reinterpret_cast<float*>(ws + L.sx);
+  float* sa = reinterpret_cast<float*>(ws + L.sa);
+  __nv_bfloat16* xp16 = reinterpret_cast<__nv_bfloat16*>(y);   // bf16 permuted rows: y is free until the down GEMM
+  moe_lora_status st = MOE_LORA_OK;
+
+  prof(a, MOE_LORA_STAGE_PERMUTE, 0, stream);
+  ML_LAUNCH(h, launch_quant_fp8(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, k, P, H, xp8, sx, stream,
+                                pdl),
+            "permute + quant launch");
+  ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp16, stream, pdl),
+            "permute launch");
+  prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
+  prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
+  st = enqueue_shrink_tc(h, a, xp16, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl, so,
+                         true);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
+
+  prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 0, stream);
+  GemmF8Params gq;
+  std::memset(&gq, 0, sizeof(gq));
+  gq.w_scale = f8->w1_scale;
+  gq.x_scale = sx;
+  gq.out = g;
+  gq.d_out = d;
+  gq.offsets = offsets;
+  gq.status = status;
+  gq.E = E;
+  gq.N = 2 * I;
+  gq.K = H;
+  gq.gated = 1;
+  gq.pair_slot = pair_slot;
+  gq.slots = slots;
+  gq.lora_packed = 1;
+  if (!packed_lora_tmaps(h, a, a->lora_B_gu_packed, 2 * I, true, false, ub, P, bn, &gq.tmap_lbp, &gq.tmap_lup,
+                         &gq.lora_rs, gq.lora_panel_slots))
+    return MOE_LORA_ERR_CUDA;
+  st = enqueue_gemm_fp8(h, gq, f8->w1, xp8, P, bn, stream, pdl);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_GATE_UP_GEMM, 1, stream);
+
+  prof(a, MOE_LORA_STAGE_ACTIVATION, 0, stream);
+  ML_LAUNCH(h, launch_activation(g, d, P, I, act, stream, pdl), "activation launch");
+  prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
+  prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
+  st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl, false,
+                         true);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
+
+  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 0, stream);
+  ML_LAUNCH(h, launch_quant_fp8(act, nullptr, 1, P, I, a8, sa, stream, pdl), "activation quant launch");
+  GemmF8Params dq;
+  std::memset(&dq, 0, sizeof(dq));
+  dq.w_scale = f8->w2_scale;
+  dq.x_scale = sa;
+  dq.out_f32 = y;
+  dq.offsets = offsets;
+  dq.status = status;
+  dq.E = E;
+  dq.N = H;
+  dq.K = I;
+  dq.gated = 0;
+  dq.pair_slot = pair_slot;
+  dq.slots = slots;
+  dq.lora_packed = 1;
+  dq.lora_b_e1 = so ? 1 : 0;
+  if (!packed_lora_tmaps(h, a, a->lora_B_dn_packed, H, false, so, ub, P, bn, &dq.tmap_lbp, &dq.tmap_lup, &dq.lora_rs,
+                         dq.lora_panel_slots))
+    return MOE_LORA_ERR_CUDA;
+  st = enqueue_gemm_fp8(h, dq, f8->w2, a8, P, bn, stream, pdl);
+  if (st != MOE_LORA_OK) return st;
+  prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+  return MOE_LORA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1244,6 +1351,10 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
     st = enqueue_gemm(h, dn, a->w2, act, P, bn0, stream, pdl);
     if (st != MOE_LORA_OK) return st;
     prof(a, MOE_LORA_STAGE_DOWN_GEMM, 1, stream);
+  } else if (f8 != nullptr && fuse_all && a->lora_B_gu_packed != nullptr && a->lora_B_dn_packed != nullptr) {
+    st = enqueue_fp8_fused_lora(h, a, ws, L, perm, offsets, xp, g, d, act, y, pair_slot, ub, slots, status, stream,
+                                f8);
+    if (st != MOE_LORA_OK) return st;
   } else {
     st = enqueue_unfused_lora_path(h, a, lora, ws, L, perm, offsets, ids, xp, g, d, act, v, y, pair_slot, ub,
                                    slots, status, stream, f8, &dn_delta, f4);
@@ -1329,7 +1440,8 @@ moe_lora_status moe_lora_forward_fp8(moe_lora_handle* h, const moe_lora_args* a,
   moe_lora_args b = *a;
   b.w1 = reinterpret_cast<const moe_lora_bf16*>(w->w1);
   b.w2 = reinterpret_cast<const moe_lora_bf16*>(w->w2);
-  b.flags |= MOE_LORA_FLAG_UNFUSED_LORA;
+  // the fused LoRA placement needs both expand-ready B copies; otherwise the side-stream one
+  if (a->lora_B_gu_packed == nullptr || a->lora_B_dn_packed == nullptr) b.flags |= MOE_LORA_FLAG_UNFUSED_LORA;
   moe_lora_status st = moe_lora_validate(&b);
   if (st != MOE_LORA_OK) return st;
   if (b.H % 128 != 0 || b.I % 128 != 0) return MOE_LORA_ERR_INVALID_ARG;

@@ -11,13 +11,16 @@ from oracle import moe_lora_oracle as orc
 # Float tolerance of the layer output: |gpu - ref| <= ATOL + RTOL * |ref| elementwise,
 # and relative L2 error <= REL_L2.
 ATOL, RTOL, REL_L2 = 1e-2, 2e-2, 5e-3
-# The FP8 path: three times the bf16 bounds.  Its activation is quantised to e4m3 after the
-# bf16 rounding, so a rounding difference upstream (the e4m3 tensor-core accumulation of
-# the gate_up GEMM) comes out about three times larger than in the bf16 layer; the
+# The FP8 path: three times the bf16 relative L2 bound, ten times its elementwise bounds.
+# Its activation is quantised to e4m3 after the bf16 rounding, so a rounding difference
+# upstream (the e4m3 tensor-core accumulation of the gate_up GEMM) comes out about three
+# times larger than in the bf16 layer in relative L2; on single elements more: a change of
+# a 128-value group's largest activation changes the group's scale (amax / 448) and every
+# code in it, which with one group per row (I = 128) moves a token's whole output row.  The
 # derivation is pinned on the CPU by
 # tests/test_oracle_fp8.py::test_fp8_tolerance_covers_accumulation_noise, from the
-# accumulation model below.
-ATOL_FP8, RTOL_FP8, REL_L2_FP8 = 3e-2, 6e-2, 1.5e-2
+# accumulation model below, over the shapes of the GPU tests and several inputs.
+ATOL_FP8, RTOL_FP8, REL_L2_FP8 = 1e-1, 2e-1, 1.5e-2
 # Accumulation model of the block-scaled FP8 GEMM behind those bounds: every product of two
 # e4m3 values is exact (4 x 4 significant bits); the tensor cores sum a 128-wide K block's
 # products as a tree of depth 7 whose adders keep at least FP8_ACC_BITS significant bits, so

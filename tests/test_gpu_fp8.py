@@ -243,3 +243,55 @@ def test_fp8_graph_capture_and_replay(handle):
         eager = _forward_fp8(handle, g, w8)
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
+
+
+FP8_FUSED_CASES = [
+    # four slots of mixed rank, 64-token tiles
+    wl.LayerConfig("f8f_four", T=96, H=512, I=256, E=16, top_k=4, ranks=(8, 16, 32, 64),
+                   scalings=(2.0, 1.0, 0.5, 0.25), slot_mode="uniform_none10"),
+    # shared-outer, 32-token tiles
+    wl.LayerConfig("f8f_shared", T=64, H=512, I=256, E=16, top_k=4, ranks=(8, 32), scalings=(2.0, 0.5),
+                   slot_mode="uniform_none10", shared_outer=True),
+    # a disabled slot and a rank-0 slot; 256-token tiles are capped at 64 on the FP8 path
+    wl.LayerConfig("f8f_disabled", T=600, H=256, I=128, E=8, top_k=2, ranks=(16, 24, 0, 8),
+                   scalings=(1.0, 0.0, 1.0, 2.0), slot_mode="uniform_none10"),
+    # the multi-adapter workload's shape
+    wl.CONFIGS["multi_slot"],
+]
+
+
+@pytest.mark.parametrize("cfg", FP8_FUSED_CASES, ids=[c.name for c in FP8_FUSED_CASES])
+def test_fp8_fused_lora_with_packed_b_matches_oracle(handle, cfg):
+    """With both expand-ready LoRA B copies the FP8 layer runs the fused LoRA placement (the
+    tensor-core shrinks and bf16 LoRA K-stages inside the FP8 GEMMs): against the FP8 oracle,
+    and against the side-stream placement of the same layer."""
+    inp = wl.make_inputs(cfg, seed=13)
+    g = gh.to_dev(inp)
+    w8 = _fp8_weights(inp)
+    flags = pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0
+    bgu = pkg.moe_lora_pack_lora_b(handle, g["lora_B_gu"], g["ranks"], 1)
+    bdn = pkg.moe_lora_pack_lora_b(handle, g["lora_B_dn"], g["ranks"], 0)
+    ws = pkg.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.S, cfg.R)
+    w1q, w1s, w2q, w2s = w8
+    kw = dict(routing_method=g["method"], correction_bias=g["correction_bias"], routed_scaling_factor=g["rsf"],
+              lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
+              lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"],
+              flags=flags, workspace=ws)
+    n0 = handle.launch_count()
+    out = pkg.moe_lora_forward_fp8(handle, g["hidden"], g["router_logits"], w1q, w1s, w2q, w2s, g["top_k"],
+                                   lora_B_gu_packed=bgu, lora_B_dn_packed=bdn, **kw)
+    torch.cuda.synchronize()
+    n1 = handle.launch_count()
+    st, word = pkg.moe_lora_check_status(ws)
+    assert st == 0, f"device status {word:#x}"
+    # route, permute + quant, bf16 permute, shrink, gate_up, activation, shrink, quant, down, finalize
+    assert n1 - n0 == 10
+    ref = _oracle_fp8(inp, w8)
+    gh.assert_close(out.float().cpu().numpy(), ref["out"], f"{cfg.name} fused fp8", gh.ATOL_FP8, gh.RTOL_FP8,
+                    gh.REL_L2_FP8)
+    side = pkg.moe_lora_forward_fp8(handle, g["hidden"], g["router_logits"], w1q, w1s, w2q, w2s, g["top_k"], **kw)
+    torch.cuda.synchronize()
+    # the two placements share the base GEMMs and differ only in the LoRA sums' order: they
+    # agree within the FP8 elementwise bounds and the bf16 relative L2 bound
+    gh.assert_close(out.float().cpu().numpy(), side.float().cpu().numpy(), f"{cfg.name} fused vs side-stream",
+                    gh.ATOL_FP8, gh.RTOL_FP8, gh.REL_L2)
