@@ -255,9 +255,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     e = lo;
     qt = t - tile_start[e] / (NT / CG);
   };
-  // the active LoRA slot of pair q (from the token's slot; -1: none or disabled)
+  // the active LoRA slot of pair q, from the token's slot that the permute gathered into
+  // pair_slot (one load, no chain through perm; -1: none, disabled or out of range)
   auto pair_lora_slot = [&](int q) -> int {
-    const int sl = p.slot_idx[p.perm[q] / p.k];
+    const int sl = p.pair_slot[q];
     if (sl < 0 || sl >= p.slots.S) return -1;
     return (p.slots.ranks[sl] > 0 && p.slots.scal[sl] != 0.0f) ? sl : -1;
   };
@@ -290,7 +291,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   // (its TMEM lane) for the tile's tokens and writes that row's ub column of every token's
   // stacked row, scaled and rounded to bf16 where the token's slot is the row's slot, zero
   // elsewhere; the columns no row covers (rank padding, disabled slots) are zeroed by the
-  // threads in turn; pair_slot is written; then the tile's ready flag is released.
+  // threads in turn; then the tile's ready flag is released.  A slot index outside [-1, S)
+  // is reported here.
   auto shrink_epilogue = [&](int t, int acc, uint32_t aphase) -> bool {
     const int quarter = warp & 3;
     const int etid = threadIdx.x - 64;
@@ -309,7 +311,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         sl = -1;
       }
       lslot[j] = sl;
-      p.pair_slot_out[q0 + j] = sl;
     }
     epi_bar();
     int s_row = -1, col = 0;

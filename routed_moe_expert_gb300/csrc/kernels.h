@@ -116,10 +116,10 @@ struct GemmParams {
   // schedule.  Its stages hold every active slot's rank rows of A for the expert (tmap_sa[s],
   // box rows = ranks[s], at row sa_row_off[s] of the weight half; at most 128 rows) and the
   // tile's token rows of X (tmap_x, as the GEMM tiles); its epilogue writes the tile's
-  // stacked ub rows (ub_out [P, lora_rs], columns coff) and pair_slot, then counts
+  // stacked ub rows (ub_out [P, lora_rs], columns coff), then counts
   // shrink_ready[shrink tile] up (release).  A GEMM tile's producer waits for its own shrink
-  // tile (acquire) before it issues the LoRA stages that read those ub rows.  The pairs'
-  // slots for the slot masks come from slot_idx and perm.
+  // tile (acquire) before it issues the LoRA stages that read those ub rows.  pair_slot
+  // then holds each pair's token slot as the permute gathered it (checked where it is read).
   int shrink_in_gemm;
   CUtensorMap tmap_sa[kMaxFusedSlots];
   int sa_row_off[kMaxFusedSlots + 1];
@@ -127,7 +127,6 @@ struct GemmParams {
   int sa_R;                      // rank stride of A's rows: (s * Ea + e) * sa_R
   int coff[kMaxFusedSlots + 1];  // stacked ub columns of slot s
   __nv_bfloat16* ub_out;         // [P, lora_rs]
-  int32_t* pair_slot_out;        // [P]
   const int32_t* perm;           // [P]
   const int32_t* slot_idx;       // [T]
   int k;

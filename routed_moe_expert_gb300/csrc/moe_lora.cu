@@ -560,7 +560,7 @@ bool shrink_in_gemm_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args
   gp.sa_e1 = a_e1 ? 1 : 0;
   gp.sa_R = a->R;
   gp.ub_out = ub;
-  gp.pair_slot_out = pair_slot;
+  gp.pair_slot = pair_slot;   // the token slots the permute gathers
   gp.perm = nullptr;   // set by the caller
   gp.shrink_ready = ready;
   gp.shrink_in_gemm = 1;
@@ -1317,11 +1317,12 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       ML_LAUNCH(h, launch_permute_shrink(ps, grid, stream, pdl), "permute + LoRA shrink launch");
       prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
     } else {
-      // the permute also clears the ready flags of the GEMMs' shrink tiles
+      // the permute also clears the ready flags of the GEMMs' shrink tiles and gathers the
+      // pairs' token slots for their slot masks
       const bool flags_used = gu_in_gemm || dn_in_gemm;
       ML_LAUNCH(h, launch_permute(reinterpret_cast<const __nv_bfloat16*>(a->hidden), perm, P, k, H, xp, stream, pdl,
-                                  nullptr, nullptr, flags_used ? ready : nullptr,
-                                  flags_used ? static_cast<int>(2 * nflags) : 0),
+                                  flags_used ? a->slot_idx : nullptr, flags_used ? pair_slot : nullptr,
+                                  flags_used ? ready : nullptr, flags_used ? static_cast<int>(2 * nflags) : 0),
                 "permute launch");
       prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
       if (fuse_all) {
