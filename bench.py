@@ -245,7 +245,9 @@ def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
     packed = {}
     if w4 is None and cfg.S > 0 and not args.per_slot_lora:
         packed = dict(lora_B_gu_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_gu"], cfg.ranks, 1),
-                      lora_B_dn_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], cfg.ranks, 0))
+                      lora_B_dn_packed=pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], cfg.ranks, 0),
+                      lora_A_gu_packed=pkg.moe_lora_pack_lora_a(h, g["lora_A_gu"], cfg.ranks),
+                      lora_A_dn_packed=pkg.moe_lora_pack_lora_a(h, g["lora_A_dn"], cfg.ranks))
 
     def fwd(flags=0, prof=None, hidden=None, logits=None, slot=None, o=out, outputs=None):
         flags |= args.flags | (pkg.FLAG_SHARED_OUTER if cfg.shared_outer else 0)
@@ -494,7 +496,7 @@ def run_gpu(args):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "forward_flags": args.flags,
             "lora_b": ("per slot" if (args.per_slot_lora or w4 is not None)
-                       else "expand-ready copies (moe_lora_pack_lora_b, made once at set-up)"),
+                       else "expand- and shrink-ready copies (moe_lora_pack_lora_b / _a, made once at set-up)"),
             "step_bytes": step_bytes, "step_flops": step_flops,
             "step_roofline_frac": max(step_bytes / (peaks["hbm_gbs"] * 1e9),
                                       step_flops / (tc_peak * 1e12)) / (agg["ms_per_step"] / 1e3),

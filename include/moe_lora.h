@@ -125,6 +125,11 @@ typedef struct {
      not given.  Used by the fused LoRA placement (see moe_lora_forward), 16-byte aligned. */
   const moe_lora_bf16* lora_B_gu_packed;
   const moe_lora_bf16* lora_B_dn_packed;
+  /* Optional shrink-ready copies of lora_A_gu and lora_A_dn made by moe_lora_pack_lora_a
+     (E_a = 1 for a shared-outer lora_A_gu) from the SAME h_ranks; NULL: not given.  Read by
+     the tensor-core shrinks (kernels or GEMM tiles) of the fused placement, 16-byte aligned. */
+  const moe_lora_bf16* lora_A_gu_packed;
+  const moe_lora_bf16* lora_A_dn_packed;
 } moe_lora_args;
 
 /* Create a handle on `device`: queries the device, creates the LoRA side stream and the
@@ -196,6 +201,21 @@ moe_lora_status moe_lora_packed_lora_b_size(int S, int E_b, int N, int R, int ga
 moe_lora_status moe_lora_pack_lora_b(moe_lora_handle* h, const moe_lora_bf16* B, int S, int E_b, int N, int R,
                                      int gated, const int32_t* h_ranks, moe_lora_bf16* packed,
                                      moe_lora_stream stream);
+
+/* Shrink-ready copy of a stacked LoRA A for the tensor-core shrinks (sglang PR #28466 section 1,
+   the shrink half of merged_experts_fused_moe_lora_add).  A: [S, E_a, R, K] bf16 (lora_A_gu
+   with K = H, E_a = E or 1 when shared-outer; lora_A_dn with K = I, E_a = E).  packed:
+   [E_a * RS, K] bf16, caller-owned, 16-byte aligned, moe_lora_packed_lora_a_size() bytes:
+   row e * RS + aoff[s] + r is A[s, e, r, :] for r < ranks[s], zero up to aoff[s+1] =
+   aoff[s] + ranks[s] rounded up to 8; RS = aoff[S].  Every slot's rank rows of an expert are
+   then one block, which a shrink copies in one piece per K step instead of one piece per slot
+   (used when RS <= 128 by the shrink tiles of the GEMMs, RS <= 256 by the shrink kernel).
+   Rows r >= ranks[s] of A are never read.  A weight-load step, as moe_lora_pack_lora_b.
+   K a multiple of 8.  Errors: INVALID_ARG (sizes, ranks outside [0, R], all ranks 0, null or
+   misaligned pointers), CUDA. */
+moe_lora_status moe_lora_packed_lora_a_size(int S, int E_a, int K, int R, const int32_t* h_ranks, size_t* bytes);
+moe_lora_status moe_lora_pack_lora_a(moe_lora_handle* h, const moe_lora_bf16* A, int S, int E_a, int K, int R,
+                                     const int32_t* h_ranks, moe_lora_bf16* packed, moe_lora_stream stream);
 
 /* The whole layer: out [T, H] bf16.  `workspace` holds moe_lora_workspace_size() bytes;
    its contents on entry do not matter.

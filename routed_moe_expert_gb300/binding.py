@@ -39,7 +39,8 @@ EXPORTED = ["moe_lora_create", "moe_lora_destroy", "moe_lora_status_string", "mo
             "moe_lora_forward", "moe_lora_check_status", "moe_lora_route_noalloc", "moe_lora_forward_routed",
             "moe_lora_launch_count", "moe_lora_forward_fp8", "moe_lora_quant_fp8", "moe_lora_grouped_gemm_fp8",
             "moe_lora_forward_nvfp4", "moe_lora_quant_nvfp4", "moe_lora_grouped_gemm_nvfp4",
-            "moe_lora_packed_lora_b_size", "moe_lora_pack_lora_b"]
+            "moe_lora_packed_lora_b_size", "moe_lora_pack_lora_b", "moe_lora_packed_lora_a_size",
+            "moe_lora_pack_lora_a"]
 
 
 class MoELoRAError(RuntimeError):
@@ -70,6 +71,7 @@ class Args(ctypes.Structure):
         ("topk_ids", c_void_p), ("topk_weights", c_void_p), ("expert_offsets", c_void_p),
         ("perm", c_void_p), ("inv_perm", c_void_p), ("prof_events", c_void_p),
         ("lora_B_gu_packed", c_void_p), ("lora_B_dn_packed", c_void_p),
+        ("lora_A_gu_packed", c_void_p), ("lora_A_dn_packed", c_void_p),
     ]
 
 
@@ -132,6 +134,10 @@ def lib() -> ctypes.CDLL:
     L.moe_lora_packed_lora_b_size.argtypes = [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(ctypes.c_int32),
                                               ctypes.POINTER(c_size_t)]
     L.moe_lora_pack_lora_b.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                       ctypes.POINTER(ctypes.c_int32), c_void_p, c_void_p]
+    L.moe_lora_packed_lora_a_size.argtypes = [c_int, c_int, c_int, c_int, ctypes.POINTER(ctypes.c_int32),
+                                              ctypes.POINTER(c_size_t)]
+    L.moe_lora_pack_lora_a.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                        ctypes.POINTER(ctypes.c_int32), c_void_p, c_void_p]
     for name in EXPORTED:
         if name not in ("moe_lora_status_string", "moe_lora_last_cuda_error"):
@@ -251,6 +257,42 @@ def moe_lora_pack_lora_b(handle: Handle, B: torch.Tensor, ranks: Sequence[int], 
     return out
 
 
+def packed_lora_a_shape(E_a: int, K: int, ranks: Sequence[int]):
+    """Shape of the shrink-ready LoRA A copy: (E_a * RS, K), RS = the sum of the ranks each
+    rounded up to 8 (the C ABI's layout)."""
+    rs = sum((int(r) + 7) // 8 * 8 for r in ranks if int(r) > 0)
+    return (int(E_a) * rs, int(K))
+
+
+def moe_lora_packed_lora_a_size(S, E_a, K, R, ranks) -> int:
+    """Bytes of the shrink-ready LoRA A copy (host only)."""
+    ranks_arr = (ctypes.c_int32 * max(len(ranks), 1))(*[int(r) for r in ranks])
+    n = c_size_t(0)
+    _check(lib().moe_lora_packed_lora_a_size(int(S), int(E_a), int(K), int(R), ranks_arr, ctypes.byref(n)),
+           "moe_lora_packed_lora_a_size")
+    return int(n.value)
+
+
+def moe_lora_pack_lora_a(handle: Handle, A: torch.Tensor, ranks: Sequence[int], out=None,
+                         stream=None) -> torch.Tensor:
+    """Shrink-ready copy of a stacked LoRA A [S, E_a, R, K] for the given slot ranks;
+    returns [E_a * RS, K] bf16."""
+    if A.dim() != 4 or A.dtype != torch.bfloat16 or not A.is_contiguous():
+        raise ValueError("A must be a contiguous bf16 [S, E_a, R, K] tensor")
+    S, Ea, R, K = (int(x) for x in A.shape)
+    if len(ranks) != S:
+        raise ValueError(f"need {S} ranks, got {len(ranks)}")
+    shape = packed_lora_a_shape(Ea, K, ranks)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=A.device)
+    elif tuple(out.shape) != shape:
+        raise ValueError(f"out must have shape {shape}")
+    ranks_arr = (ctypes.c_int32 * S)(*[int(r) for r in ranks])
+    _check(lib().moe_lora_pack_lora_a(handle.ptr, _ptr(A, torch.bfloat16, "A"), S, Ea, K, R, ranks_arr,
+                                      _ptr(out, torch.bfloat16, "out"), _stream(stream)), "moe_lora_pack_lora_a")
+    return out
+
+
 def moe_lora_route(handle: Handle, router_logits: torch.Tensor, top_k: int, routing_method: int = 0,
                    correction_bias: Optional[torch.Tensor] = None, routed_scaling_factor: float = 1.0,
                    n_group: int = 1, topk_group: int = 1, outputs: Optional[dict] = None,
@@ -347,7 +389,8 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
               routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None, lora_A_dn=None, lora_B_dn=None,
               slot_idx=None, ranks: Sequence[int] = (), scalings: Sequence[float] = (), flags=0,
               outputs: Optional[dict] = None, prof_events=None, n_group=1, topk_group=1,
-              weight_dtype=torch.bfloat16, packed_k=False, lora_B_gu_packed=None, lora_B_dn_packed=None):
+              weight_dtype=torch.bfloat16, packed_k=False, lora_B_gu_packed=None, lora_B_dn_packed=None,
+              lora_A_gu_packed=None, lora_A_dn_packed=None):
     """Fill the C argument struct.  Returns (Args, keepalive) -- keep both alive for the call."""
     check_shapes(hidden, router_logits, w1, w2, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
                  scalings, flags, correction_bias=correction_bias, packed_k=packed_k)
@@ -359,6 +402,15 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
             want = packed_lora_b_shape(Eb, N, gated, ranks)
             if tuple(t.shape) != want:
                 raise ValueError(f"{name} must have shape {want} (moe_lora_pack_lora_b with these ranks), "
+                                 f"got {tuple(t.shape)}")
+    for t, name, Ea, K in (
+            (lora_A_gu_packed, "lora_A_gu_packed", 1 if (int(flags) & FLAG_SHARED_OUTER) else w1.shape[0],
+             hidden.shape[1]),
+            (lora_A_dn_packed, "lora_A_dn_packed", w1.shape[0], w1.shape[1] // 2)):
+        if t is not None:
+            want = packed_lora_a_shape(Ea, K, ranks)
+            if tuple(t.shape) != want:
+                raise ValueError(f"{name} must have shape {want} (moe_lora_pack_lora_a with these ranks), "
                                  f"got {tuple(t.shape)}")
     T, H = hidden.shape
     E, twoI, _ = w1.shape
@@ -391,6 +443,8 @@ def make_args(hidden, router_logits, w1, w2, top_k, routing_method=0, correction
     a.inv_perm = _ptr(o.get("inv_perm"), torch.int32)
     a.lora_B_gu_packed = _ptr(lora_B_gu_packed, torch.bfloat16, "lora_B_gu_packed")
     a.lora_B_dn_packed = _ptr(lora_B_dn_packed, torch.bfloat16, "lora_B_dn_packed")
+    a.lora_A_gu_packed = _ptr(lora_A_gu_packed, torch.bfloat16, "lora_A_gu_packed")
+    a.lora_A_dn_packed = _ptr(lora_A_dn_packed, torch.bfloat16, "lora_A_dn_packed")
     ev_arr = None
     if prof_events is not None:
         ev_arr = (c_void_p * (2 * NUM_STAGES))(*[(e.cuda_event if e is not None else None) for e in prof_events])
@@ -402,14 +456,16 @@ def moe_lora_forward(handle: Handle, hidden, router_logits, w1, w2, top_k, routi
                      correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None, lora_B_gu=None,
                      lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(), flags=0,
                      out=None, workspace=None, outputs=None, prof_events=None, stream=None,
-                     n_group=1, topk_group=1, lora_B_gu_packed=None, lora_B_dn_packed=None) -> torch.Tensor:
+                     n_group=1, topk_group=1, lora_B_gu_packed=None, lora_B_dn_packed=None,
+                     lora_A_gu_packed=None, lora_A_dn_packed=None) -> torch.Tensor:
     """The whole layer: returns out [T, H] bf16 (written in place when `out` is given).
-    lora_B_gu_packed / lora_B_dn_packed: optional expand-ready copies (moe_lora_pack_lora_b)
-    made with the same ranks."""
+    lora_B_*_packed / lora_A_*_packed: optional expand-ready and shrink-ready copies
+    (moe_lora_pack_lora_b / moe_lora_pack_lora_a) made with the same ranks."""
     a, keep = make_args(hidden, router_logits, w1, w2, top_k, routing_method, correction_bias,
                         routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
                         scalings, flags, outputs, prof_events, n_group, topk_group,
-                        lora_B_gu_packed=lora_B_gu_packed, lora_B_dn_packed=lora_B_dn_packed)
+                        lora_B_gu_packed=lora_B_gu_packed, lora_B_dn_packed=lora_B_dn_packed,
+                        lora_A_gu_packed=lora_A_gu_packed, lora_A_dn_packed=lora_A_dn_packed)
     if out is None:
         out = torch.empty((a.T, a.H), dtype=torch.bfloat16, device=hidden.device)
     if workspace is None:
@@ -490,7 +546,8 @@ def moe_lora_forward_fp8(handle: Handle, hidden, router_logits, w1_q, w1_scale, 
                          routing_method=0, correction_bias=None, routed_scaling_factor=1.0, lora_A_gu=None,
                          lora_B_gu=None, lora_A_dn=None, lora_B_dn=None, slot_idx=None, ranks=(), scalings=(),
                          flags=0, out=None, workspace=None, outputs=None, prof_events=None, stream=None,
-                         n_group=1, topk_group=1, lora_B_gu_packed=None, lora_B_dn_packed=None) -> torch.Tensor:
+                         n_group=1, topk_group=1, lora_B_gu_packed=None, lora_B_dn_packed=None,
+                         lora_A_gu_packed=None, lora_A_dn_packed=None) -> torch.Tensor:
     """The layer with FP8 block-scale expert weights: w1_q [E, 2I, H] and w2_q [E, H, I] hold
     e4m3 bit patterns (uint8), w1_scale [E, 2I/128, H/128] and w2_scale [E, H/128, I/128]
     the float32 scales of their 128 x 128 blocks.  With both expand-ready LoRA B copies
@@ -499,7 +556,8 @@ def moe_lora_forward_fp8(handle: Handle, hidden, router_logits, w1_q, w1_scale, 
     a, keep = make_args(hidden, router_logits, w1_q, w2_q, top_k, routing_method, correction_bias,
                         routed_scaling_factor, lora_A_gu, lora_B_gu, lora_A_dn, lora_B_dn, slot_idx, ranks,
                         scalings, flags, outputs, prof_events, n_group, topk_group, weight_dtype=torch.uint8,
-                        lora_B_gu_packed=lora_B_gu_packed, lora_B_dn_packed=lora_B_dn_packed)
+                        lora_B_gu_packed=lora_B_gu_packed, lora_B_dn_packed=lora_B_dn_packed,
+                        lora_A_gu_packed=lora_A_gu_packed, lora_A_dn_packed=lora_A_dn_packed)
     w = Fp8Weights()
     w.w1 = _ptr(w1_q, torch.uint8, "w1_q")
     w.w1_scale = _ptr(w1_scale, torch.float32, "w1_scale")

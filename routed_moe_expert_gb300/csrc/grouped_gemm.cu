@@ -447,10 +447,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
               }
               uint8_t* a = smem + stage * STAGE;
               mbar_arrive_expect_tx(&full[stage], bytes);
-              for (int sl = 0; sl < kMaxFusedSlots; ++sl)
-                if (p.sa_row_off[sl + 1] > p.sa_row_off[sl])
-                  load(a + p.sa_row_off[sl] * 128, &p.tmap_sa[sl], stage, kb * 64,
-                       (sl * (p.sa_e1 ? 1 : E) + ea) * p.sa_R, pol_x);
+              if (p.sa_packed) {   // every slot's rows of the expert: one block of the shrink-ready A
+                load(a, &p.tmap_sa[0], stage, kb * 64, ea * p.sa_R, pol_x);
+              } else {
+                for (int sl = 0; sl < kMaxFusedSlots; ++sl)
+                  if (p.sa_row_off[sl + 1] > p.sa_row_off[sl])
+                    load(a + p.sa_row_off[sl] * 128, &p.tmap_sa[sl], stage, kb * 64,
+                         (sl * (p.sa_e1 ? 1 : E) + ea) * p.sa_R, pol_x);
+              }
               load(a + A_BYTES, &p.tmap_x, stage, kb * 64, xr, pol_x);
               issued_mask |= 1u << stage;
               issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);

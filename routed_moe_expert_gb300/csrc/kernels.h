@@ -123,6 +123,8 @@ struct GemmParams {
   int shrink_in_gemm;
   CUtensorMap tmap_sa[kMaxFusedSlots];
   int sa_row_off[kMaxFusedSlots + 1];
+  int sa_packed;                 // 1: tmap_sa[0] is the shrink-ready A [Ea*RS rows, K] (box RS rows), one
+                                 //    copy per stage; sa_row_off its slot offsets, sa_R = RS
   int sa_e1;                     // A is [S, 1, R, K]: one set per slot
   int sa_R;                      // rank stride of A's rows: (s * Ea + e) * sa_R
   int coff[kMaxFusedSlots + 1];  // stacked ub columns of slot s
@@ -286,6 +288,8 @@ struct ShrinkTcParams {
   int stages;                    // pipeline depth (set by the launcher)
   LoraSlots slots;
   __nv_bfloat16* ub;             // [S, P, R], or [P, rs] with ub_stacked
+  int packed_a;                  // 1: tmap_a is the shrink-ready A [Ea*RS rows, K], box RS rows, row_off its
+                                 //    slot offsets (per_slot set); one copy per stage
   int ub_stacked;                // 1: each pair's row holds every slot's ranks, slot s at column coff[s]
   int rs;                        // stacked columns (ub_stacked), a multiple of 16
   int coff[kMaxFusedSlots + 1];
@@ -302,6 +306,15 @@ struct PackLoraBParams {
   int coff[kMaxSlots + 1];       // coff[s+1] - coff[s] = ranks[s] rounded up to 16
 };
 cudaError_t launch_pack_lora_b(const PackLoraBParams& p, cudaStream_t stream);
+// Shrink-ready (packed) LoRA A: see pack_lora_a_kernel.
+struct PackLoraAParams {
+  const __nv_bfloat16* A;        // [S, Ea, R, K]
+  __nv_bfloat16* Ap;             // [Ea * RS, K]
+  int S, Ea, R, K, RS;
+  int ranks[kMaxSlots];
+  int aoff[kMaxSlots + 1];       // aoff[s+1] - aoff[s] = ranks[s] rounded up to 8
+};
+cudaError_t launch_pack_lora_a(const PackLoraAParams& p, cudaStream_t stream);
 cudaError_t launch_lora_shrink_tc(const ShrinkTcParams& p, int grid, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_lora(const LoraParams& p, int ntl, int grid, cudaStream_t stream, bool pdl = false);
 

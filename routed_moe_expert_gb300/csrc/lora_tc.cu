@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmap_x);
-    if (p.per_slot) {
+    if (p.per_slot && !p.packed_a) {
       for (int s = 0; s < p.S; ++s)
         if (p.row_off[s + 1] > p.row_off[s]) tma_prefetch_desc(&p.tmap_a_slot[s]);
     } else {
@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(kShrinkThreads, 1) lora_shrink_tc_kernel(const
           // lanes and columns that are never read)
           mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(p.tb + nrows) * 128u);
           tma_load_2d(a, &p.tmap_x, &full[stage], kb * 64, xr, pol_x);
-          if (p.per_slot) {   // each active slot's rank rows of A for expert e, packed
+          if (p.packed_a) {   // every slot's rank rows for expert e, contiguous in the shrink-ready A
+            tma_load_2d(a + A_BYTES, &p.tmap_a, &full[stage], kb * 64, (p.a_e1 ? 0 : e) * nrows, pol_a);
+          } else if (p.per_slot) {   // each active slot's rank rows of A for expert e, packed
             for (int s = 0; s < p.S; ++s)
               if (p.row_off[s + 1] > p.row_off[s])
                 tma_load_2d(a + A_BYTES + p.row_off[s] * 128, &p.tmap_a_slot[s], &full[stage], kb * 64,
@@ -355,6 +357,38 @@ cudaError_t launch_pack_lora_b(const PackLoraBParams& p, cudaStream_t stream) {
   long long blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   pack_lora_b_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Shrink-ready copy of a stacked LoRA A [S, Ea, R, K] for the tensor-core shrinks: row
+// e * RS + aoff[s] + r is A[s, e, r, :] for r < ranks[s] and zero up to aoff[s+1] (ranks
+// rounded up to 8), so every slot's rank rows of an expert are one contiguous block of RS
+// rows.  One thread per 8 values (one 16-byte store); the rank tails of A are never read.
+__global__ void pack_lora_a_kernel(const __grid_constant__ PackLoraAParams p) {
+  const int cv = p.K >> 3;
+  const long long total = static_cast<long long>(p.Ea) * p.RS * cv;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long prow = i / cv;
+    const int c0 = static_cast<int>(i - prow * cv) * 8;
+    const int e = static_cast<int>(prow / p.RS);
+    const int j = static_cast<int>(prow - static_cast<long long>(e) * p.RS);
+    int s = 0;
+    while (p.aoff[s + 1] <= j) ++s;   // j < aoff[S], so s < S
+    const int r = j - p.aoff[s];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < p.ranks[s])
+      v = *reinterpret_cast<const uint4*>(p.A + ((static_cast<size_t>(s) * p.Ea + e) * p.R + r) * p.K + c0);
+    *reinterpret_cast<uint4*>(p.Ap + prow * p.K + c0) = v;
+  }
+}
+
+cudaError_t launch_pack_lora_a(const PackLoraAParams& p, cudaStream_t stream) {
+  const long long total = static_cast<long long>(p.Ea) * p.RS * (p.K >> 3);
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  pack_lora_a_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -189,7 +189,9 @@ moe_lora_status moe_lora_validate(const moe_lora_args* a) {
       if (!aligned16(a->lora_A_gu) || !aligned16(a->lora_A_dn) || !aligned16(a->lora_B_gu) ||
           !aligned16(a->lora_B_dn) || !aligned4(a->slot_idx))
         return MOE_LORA_ERR_INVALID_ARG;
-      if (!aligned16(a->lora_B_gu_packed) || !aligned16(a->lora_B_dn_packed)) return MOE_LORA_ERR_INVALID_ARG;
+      if (!aligned16(a->lora_B_gu_packed) || !aligned16(a->lora_B_dn_packed) || !aligned16(a->lora_A_gu_packed) ||
+          !aligned16(a->lora_A_dn_packed))
+        return MOE_LORA_ERR_INVALID_ARG;
     }
   }
   const void* opt[] = {a->topk_ids, a->topk_weights, a->expert_offsets, a->perm, a->inv_perm};
@@ -492,6 +494,14 @@ int stacked_cols(const int32_t* ranks, int S, int* coff) {
   return coff[S];
 }
 
+// Stacked rows of the shrink-ready A: slot s's ranks at row aoff[s] of an expert's block, each
+// slot's block rounded up to 8 rows (a swizzle atom), from the ranks alone.  Returns RS = aoff[S].
+int stacked_rows(const int32_t* ranks, int S, int* aoff) {
+  aoff[0] = 0;
+  for (int s = 0; s < S; ++s) aoff[s + 1] = aoff[s] + (ranks[s] > 0 ? (ranks[s] + 7) / 8 * 8 : 0);
+  return aoff[S];
+}
+
 // Tensor maps of the fused LoRA stages from the expand-ready (packed) B [Eb*NT*128, Rs] and
 // the stacked ub [P, Rs], and the slots whose columns meet each 64-column panel.
 bool packed_lora_tmaps(moe_lora_handle* h, const moe_lora_args* a, const moe_lora_bf16* Bp, int N, bool gated,
@@ -540,25 +550,38 @@ bool fuse_lora_maps_packed(moe_lora_handle* h, GemmParams& gp, const moe_lora_ar
 // slot's rows then start on a swizzle-atom boundary) and at most 128 of them (one MMA M);
 // returns false when they are not, and the separate shrink kernel runs instead.
 bool shrink_in_gemm_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args* a, const moe_lora_bf16* A, int K,
-                         bool a_e1, __nv_bfloat16* ub, int32_t* pair_slot, int* ready) {
+                         bool a_e1, __nv_bfloat16* ub, int32_t* pair_slot, int* ready,
+                         const moe_lora_bf16* Ap = nullptr) {
   if (a->S > kMaxFusedSlots) return false;
-  const uint64_t a_rows = static_cast<uint64_t>(a->S) * (a_e1 ? 1 : a->E) * a->R;
-  int off = 0;
-  for (int s = 0; s < kMaxFusedSlots; ++s) {
-    gp.sa_row_off[s] = off;
-    const int rows = (s < a->S && a->h_ranks[s] > 0 && a->h_scalings[s] != 0.0f) ? a->h_ranks[s] : 0;
-    if (rows % 8 != 0) return false;
-    if (rows > 0 && !make_tmap(h->encode, &gp.tmap_sa[s], A, a_rows, K, static_cast<uint32_t>(rows))) return false;
-    off += rows;
+  const int Ea = a_e1 ? 1 : a->E;
+  if (Ap != nullptr) {   // the shrink-ready A: every slot's rows of an expert in one block
+    int aoff[kMaxFusedSlots + 1];
+    const int RS = stacked_rows(a->h_ranks, a->S, aoff);
+    if (RS == 0 || RS > 128) return false;
+    if (!make_tmap(h->encode, &gp.tmap_sa[0], Ap, static_cast<uint64_t>(Ea) * RS, K, static_cast<uint32_t>(RS)))
+      return false;
+    for (int s = 0; s <= kMaxFusedSlots; ++s) gp.sa_row_off[s] = aoff[s <= a->S ? s : a->S];
+    gp.sa_packed = 1;
+    gp.sa_R = RS;
+  } else {
+    const uint64_t a_rows = static_cast<uint64_t>(a->S) * Ea * a->R;
+    int off = 0;
+    for (int s = 0; s < kMaxFusedSlots; ++s) {
+      gp.sa_row_off[s] = off;
+      const int rows = (s < a->S && a->h_ranks[s] > 0 && a->h_scalings[s] != 0.0f) ? a->h_ranks[s] : 0;
+      if (rows % 8 != 0) return false;
+      if (rows > 0 && !make_tmap(h->encode, &gp.tmap_sa[s], A, a_rows, K, static_cast<uint32_t>(rows))) return false;
+      off += rows;
+    }
+    gp.sa_row_off[kMaxFusedSlots] = off;
+    if (off == 0 || off > 128) return false;
+    gp.sa_R = a->R;
   }
-  gp.sa_row_off[kMaxFusedSlots] = off;
-  if (off == 0 || off > 128) return false;
   int coff[kMaxFusedSlots + 1];
   const int rs = stacked_cols(a->h_ranks, a->S, coff);
   if (rs != gp.lora_rs || rs > 384) return false;
   for (int s = 0; s <= kMaxFusedSlots; ++s) gp.coff[s] = coff[s <= a->S ? s : a->S];
   gp.sa_e1 = a_e1 ? 1 : 0;
-  gp.sa_R = a->R;
   gp.ub_out = ub;
   gp.pair_slot = pair_slot;   // the token slots the permute gathers
   gp.perm = nullptr;   // set by the caller
@@ -572,7 +595,8 @@ bool shrink_in_gemm_maps(moe_lora_handle* h, GemmParams& gp, const moe_lora_args
 moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, const void* X, const moe_lora_bf16* A,
                                   int K, const int32_t* offsets, const int32_t* perm, const LoraSlots& slots,
                                   __nv_bfloat16* ub, int32_t* pair_slot, uint32_t* status, cudaStream_t stream,
-                                  bool pdl, bool a_e1 = false, bool stacked = false) {
+                                  bool pdl, bool a_e1 = false, bool stacked = false,
+                                  const moe_lora_bf16* Ap = nullptr) {
   const int P = a->T * a->top_k;
   ShrinkTcParams sp;
   std::memset(&sp, 0, sizeof(sp));
@@ -588,11 +612,22 @@ moe_lora_status enqueue_shrink_tc(moe_lora_handle* h, const moe_lora_args* a, co
   const uint64_t a_rows = static_cast<uint64_t>(a->S) * (a_e1 ? 1 : a->E) * a->R;
   sp.a_e1 = a_e1 ? 1 : 0;
   if (!make_tmap(h->encode, &sp.tmap_a, A, a_rows, K, a->R)) return MOE_LORA_ERR_CUDA;
+  // the shrink-ready A: every slot's rank rows of an expert in one block of RS rows
+  int aoff[kMaxFusedSlots + 1];
+  const int RS = (Ap != nullptr && a->S <= kMaxFusedSlots) ? stacked_rows(a->h_ranks, a->S, aoff) : 0;
+  if (RS > 0 && RS <= 256) {
+    if (!make_tmap(h->encode, &sp.tmap_a, Ap, static_cast<uint64_t>(a_e1 ? 1 : a->E) * RS, K,
+                   static_cast<uint32_t>(RS)))
+      return MOE_LORA_ERR_CUDA;
+    sp.packed_a = 1;
+    sp.per_slot = 1;
+    for (int s = 0; s <= a->S; ++s) sp.row_off[s] = aoff[s];
+  }
   // only the active slots' rank rows, when every such rank is a multiple of 8 (each slot's
   // rows then start on a swizzle-atom boundary of the stacked tile)
-  sp.per_slot = a->S <= kMaxFusedSlots ? 1 : 0;
+  if (!sp.packed_a) sp.per_slot = a->S <= kMaxFusedSlots ? 1 : 0;
   sp.row_off[0] = 0;
-  for (int s = 0; s < a->S && sp.per_slot; ++s) {
+  for (int s = 0; s < a->S && sp.per_slot && !sp.packed_a; ++s) {
     const int rows = (slots.ranks[s] > 0 && slots.scal[s] != 0.0f) ? slots.ranks[s] : 0;
     if (rows % 8 != 0) sp.per_slot = 0;
     sp.row_off[s + 1] = sp.row_off[s] + rows;
@@ -1020,7 +1055,7 @@ moe_lora_status enqueue_fp8_fused_lora(moe_lora_handle* h, const moe_lora_args* 
   prof(a, MOE_LORA_STAGE_PERMUTE, 1, stream);
   prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
   st = enqueue_shrink_tc(h, a, xp16, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl, so,
-                         true);
+                         true, a->lora_A_gu_packed);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
 
@@ -1052,7 +1087,7 @@ moe_lora_status enqueue_fp8_fused_lora(moe_lora_handle* h, const moe_lora_args* 
   prof(a, MOE_LORA_STAGE_ACTIVATION, 1, stream);
   prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
   st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl, false,
-                         true);
+                         true, a->lora_A_dn_packed);
   if (st != MOE_LORA_OK) return st;
   prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);
 
@@ -1152,6 +1187,46 @@ moe_lora_status moe_lora_pack_lora_b(moe_lora_handle* h, const moe_lora_bf16* B,
   pp.gated = gated;
   for (int s = 0; s < S; ++s) pp.ranks[s] = h_ranks[s];
   ML_LAUNCH(h, launch_pack_lora_b(pp, stream), "pack LoRA B launch");
+  return MOE_LORA_OK;
+}
+
+static moe_lora_status packed_lora_a_dims(int S, int E_a, int K, int R, const int32_t* h_ranks, int* RS, int* aoff) {
+  if (S < 1 || S > kMaxSlots || E_a < 1 || E_a > kMaxExperts || K < 8 || K % 8 != 0 || R < 1 || R > kMaxRank ||
+      h_ranks == nullptr)
+    return MOE_LORA_ERR_INVALID_ARG;
+  for (int s = 0; s < S; ++s)
+    if (h_ranks[s] < 0 || h_ranks[s] > R) return MOE_LORA_ERR_INVALID_ARG;
+  *RS = stacked_rows(h_ranks, S, aoff);
+  if (*RS == 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (static_cast<long long>(E_a) * *RS > 0x7fffffffLL) return MOE_LORA_ERR_INVALID_ARG;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_packed_lora_a_size(int S, int E_a, int K, int R, const int32_t* h_ranks, size_t* bytes) {
+  if (bytes == nullptr) return MOE_LORA_ERR_INVALID_ARG;
+  int RS = 0, aoff[kMaxSlots + 1];
+  const moe_lora_status st = packed_lora_a_dims(S, E_a, K, R, h_ranks, &RS, aoff);
+  if (st != MOE_LORA_OK) return st;
+  *bytes = static_cast<size_t>(E_a) * RS * K * 2;
+  return MOE_LORA_OK;
+}
+
+moe_lora_status moe_lora_pack_lora_a(moe_lora_handle* h, const moe_lora_bf16* A, int S, int E_a, int K, int R,
+                                     const int32_t* h_ranks, moe_lora_bf16* packed, moe_lora_stream stream) {
+  if (h == nullptr || A == nullptr || packed == nullptr || !aligned16(A) || !aligned16(packed))
+    return MOE_LORA_ERR_INVALID_ARG;
+  PackLoraAParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  moe_lora_status st = packed_lora_a_dims(S, E_a, K, R, h_ranks, &pp.RS, pp.aoff);
+  if (st != MOE_LORA_OK) return st;
+  pp.A = reinterpret_cast<const __nv_bfloat16*>(A);
+  pp.Ap = reinterpret_cast<__nv_bfloat16*>(packed);
+  pp.S = S;
+  pp.Ea = E_a;
+  pp.R = R;
+  pp.K = K;
+  for (int s = 0; s < S; ++s) pp.ranks[s] = h_ranks[s];
+  ML_LAUNCH(h, launch_pack_lora_a(pp, stream), "pack LoRA A launch");
   return MOE_LORA_OK;
 }
 
@@ -1267,7 +1342,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
                                 : fuse_lora_maps(h, gu, a, a->lora_B_gu, 2 * I, ub, pair_slot, P, bn)))
       return MOE_LORA_ERR_CUDA;
     const bool gu_in_gemm = gu_packed && shrink_ok && gu.cta_pair == 1 &&
-                            shrink_in_gemm_maps(h, gu, a, a->lora_A_gu, H, so, ub, pair_slot, ready);
+                            shrink_in_gemm_maps(h, gu, a, a->lora_A_gu, H, so, ub, pair_slot, ready, a->lora_A_gu_packed);
     GemmParams dn;
     std::memset(&dn, 0, sizeof(dn));
     if (y_bf16) dn.out = reinterpret_cast<__nv_bfloat16*>(y);
@@ -1284,7 +1359,8 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
                                 : fuse_lora_maps(h, dn, a, a->lora_B_dn, H, ub, pair_slot, P, bn0, so)))
       return MOE_LORA_ERR_CUDA;
     const bool dn_in_gemm = dn_packed && shrink_ok && dn.cta_pair == 1 &&
-                            shrink_in_gemm_maps(h, dn, a, a->lora_A_dn, I, false, ub, pair_slot, ready + nflags);
+                            shrink_in_gemm_maps(h, dn, a, a->lora_A_dn, I, false, ub, pair_slot, ready + nflags,
+                                                a->lora_A_dn_packed);
     gu.perm = dn.perm = perm;
     gu.slot_idx = dn.slot_idx = a->slot_idx;
     gu.k = dn.k = k;
@@ -1329,7 +1405,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
         prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 0, stream);
         if (!gu_in_gemm) {
           st = enqueue_shrink_tc(h, a, xp, a->lora_A_gu, H, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
-                                 so, gu_packed);
+                                 so, gu_packed, a->lora_A_gu_packed);
           if (st != MOE_LORA_OK) return st;
         }
         prof(a, MOE_LORA_STAGE_LORA_GATE_UP, 1, stream);
@@ -1343,7 +1419,7 @@ moe_lora_status forward_impl(moe_lora_handle* h, const moe_lora_args* a, const m
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 0, stream);
       if (!dn_in_gemm) {
         st = enqueue_shrink_tc(h, a, act, a->lora_A_dn, I, offsets, perm, slots, ub, pair_slot, status, stream, pdl,
-                               false, dn_packed);
+                               false, dn_packed, a->lora_A_dn_packed);
         if (st != MOE_LORA_OK) return st;
       }
       prof(a, MOE_LORA_STAGE_LORA_DOWN, 1, stream);

@@ -69,6 +69,19 @@ def test_packed_lora_b_size_host_only(built_lib):
             B.moe_lora_packed_lora_b_size(kw["S"], kw["Eb"], kw["N"], kw["R"], kw["gated"], kw["ranks"])
 
 
+def test_packed_lora_a_size_host_only(built_lib):
+    """The shrink-ready LoRA A copy: rows are experts x every slot's rank rounded up to 8."""
+    assert B.moe_lora_packed_lora_a_size(4, 3, 2048, 64, (8, 16, 32, 64)) == 3 * 120 * 2048 * 2
+    assert B.packed_lora_a_shape(3, 2048, (8, 16, 32, 64)) == (3 * 120, 2048)
+    assert B.moe_lora_packed_lora_a_size(3, 2, 256, 24, (5, 0, 24)) == 2 * 32 * 256 * 2
+    assert B.packed_lora_a_shape(2, 256, (5, 0, 24)) == (2 * 32, 256)
+    for bad in (dict(ranks=(0, 0)), dict(ranks=(8, 40)), dict(K=100), dict(S=0, ranks=())):
+        kw = dict(S=2, Ea=2, K=256, R=32, ranks=(8, 16))
+        kw.update(bad)
+        with pytest.raises(B.MoELoRAError):
+            B.moe_lora_packed_lora_a_size(kw["S"], kw["Ea"], kw["K"], kw["R"], kw["ranks"])
+
+
 FAKE = 0x7f0000000000          # 16-byte aligned fake device address (never dereferenced)
 
 

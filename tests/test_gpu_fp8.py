@@ -277,9 +277,12 @@ def test_fp8_fused_lora_with_packed_b_matches_oracle(handle, cfg):
               lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
               lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"],
               flags=flags, workspace=ws)
+    agu = pkg.moe_lora_pack_lora_a(handle, g["lora_A_gu"], g["ranks"])
+    adn = pkg.moe_lora_pack_lora_a(handle, g["lora_A_dn"], g["ranks"])
     n0 = handle.launch_count()
     out = pkg.moe_lora_forward_fp8(handle, g["hidden"], g["router_logits"], w1q, w1s, w2q, w2s, g["top_k"],
-                                   lora_B_gu_packed=bgu, lora_B_dn_packed=bdn, **kw)
+                                   lora_B_gu_packed=bgu, lora_B_dn_packed=bdn, lora_A_gu_packed=agu,
+                                   lora_A_dn_packed=adn, **kw)
     torch.cuda.synchronize()
     n1 = handle.launch_count()
     st, word = pkg.moe_lora_check_status(ws)

@@ -59,6 +59,37 @@ def test_pack_lora_b_layout_bit_exact(handle, S, Eb, N, R, ranks, gated):
     assert torch.equal(got.cpu().view(torch.int16), ref.view(torch.int16))
 
 
+def _packed_a_reference(A: torch.Tensor, ranks) -> torch.Tensor:
+    """The layout of moe_lora_pack_lora_a, from its definition: for each expert, every slot's
+    rank rows one after another, each slot's block rounded up to 8 rows of zeros."""
+    S, Ea, R, K = A.shape
+    ro = [(r + 7) // 8 * 8 if r > 0 else 0 for r in ranks]
+    aoff = np.concatenate([[0], np.cumsum(ro)]).astype(int)
+    out = torch.zeros((Ea, int(aoff[-1]), K), dtype=torch.bfloat16)
+    for s in range(S):
+        if ranks[s] > 0:
+            out[:, aoff[s]:aoff[s] + ranks[s], :] = A[s, :, :ranks[s], :]
+    return out.reshape(Ea * int(aoff[-1]), K)
+
+
+@pytest.mark.parametrize("S,Ea,R,K,ranks", [
+    (4, 3, 64, 256, (8, 16, 32, 64)),   # the multi-slot ranks
+    (4, 2, 24, 128, (16, 24, 0, 5)),    # a rank-0 slot and ranks that are not multiples of 8
+    (2, 1, 16, 384, (16, 8)),           # shared-outer A: one expert set
+], ids=["four", "ragged", "shared"])
+def test_pack_lora_a_layout_bit_exact(handle, S, Ea, R, K, ranks):
+    g = torch.Generator().manual_seed(K + R)
+    A = torch.randn((S, Ea, R, K), generator=g).to(torch.bfloat16)
+    for s, r in enumerate(ranks):   # the rank tails must never be read
+        A[s, :, r:, :] = float("nan")
+    got = pkg.moe_lora_pack_lora_a(handle, A.cuda(), ranks)
+    torch.cuda.synchronize()
+    ref = _packed_a_reference(A, ranks)
+    assert tuple(got.shape) == tuple(ref.shape) == pkg.packed_lora_a_shape(Ea, K, ranks)
+    assert pkg.moe_lora_packed_lora_a_size(S, Ea, K, R, ranks) == ref.numel() * 2
+    assert torch.equal(got.cpu().view(torch.int16), ref.view(torch.int16))
+
+
 def _run_pair(h, cfg, seed, flags=0, device_inputs=False, saved_launches=None):
     """The layer on the same inputs with per-slot LoRA stages, with packed stages and separate
     shrink kernels (equal to the first), and with packed stages and the shrinks as tiles of the
@@ -75,13 +106,17 @@ def _run_pair(h, cfg, seed, flags=0, device_inputs=False, saved_launches=None):
     bgu = pkg.moe_lora_pack_lora_b(h, g["lora_B_gu"], g["ranks"], 1)
     bdn = pkg.moe_lora_pack_lora_b(h, g["lora_B_dn"], g["ranks"], 0)
     assert bdn.shape[0] == (1 if so else cfg.E) * ((cfg.H + 127) // 128) * 128
-    def packed(extra):
+    agu = pkg.moe_lora_pack_lora_a(h, g["lora_A_gu"], g["ranks"])
+    adn = pkg.moe_lora_pack_lora_a(h, g["lora_A_dn"], g["ranks"])
+
+    def packed(extra, with_a=False):
+        more = dict(lora_A_gu_packed=agu, lora_A_dn_packed=adn) if with_a else {}
         o = pkg.moe_lora_forward(
             h, g["hidden"], g["router_logits"], g["w1"], g["w2"], g["top_k"], routing_method=g["method"],
             correction_bias=g["correction_bias"], routed_scaling_factor=g["rsf"],
             lora_A_gu=g["lora_A_gu"], lora_B_gu=g["lora_B_gu"], lora_A_dn=g["lora_A_dn"],
             lora_B_dn=g["lora_B_dn"], slot_idx=g["slot_idx"], ranks=g["ranks"], scalings=g["scalings"],
-            flags=flags | extra, workspace=ws, lora_B_gu_packed=bgu, lora_B_dn_packed=bdn)
+            flags=flags | extra, workspace=ws, lora_B_gu_packed=bgu, lora_B_dn_packed=bdn, **more)
         torch.cuda.synchronize()
         st, word = pkg.moe_lora_check_status(ws)
         assert st == 0, f"device status {word:#x}"
@@ -98,6 +133,11 @@ def _run_pair(h, cfg, seed, flags=0, device_inputs=False, saved_launches=None):
     ref = gh.oracle(inp, lazy=device_inputs)
     gh.assert_close(out.float().cpu().numpy(), ref["out"], cfg.name)
     gh.assert_close(out.float().cpu().numpy(), base.float().cpu().numpy(), cfg.name + " vs per-slot")
+    # the shrink-ready A copies change only where each rank row comes from (one copy per K step)
+    sep_a = packed(pkg.FLAG_SEPARATE_SHRINK, with_a=True)
+    assert torch.equal(sep_a, base), f"shrink-ready A, shrink kernels: {int((sep_a != base).sum())} elements differ"
+    out_a = packed(0, with_a=True)
+    assert torch.equal(out_a, out), f"shrink-ready A, shrink tiles: {int((out_a != out).sum())} elements differ"
     return base, out
 
 
