@@ -218,6 +218,9 @@ struct GemmNv4Params {
   int lora_b_e1;
   const int32_t* pair_slot;      // [P], -1 = no LoRA for the pair
   LoraSlots slots;
+  // The same operands by address, for the narrow-tile kernel (mma.sync, no tensor maps)
+  const uint8_t* w_codes;        // [E*N, K/2] packed codes
+  const __half* x16;             // [P, K] f16 inputs
 };
 int gemm_nvfp4_smem_bytes(int bn, int stages, int rstages, int E, int lora_R);
 int gemm_nvfp4_stage_bytes(int bn);    // one f16 weight tile
@@ -225,6 +228,9 @@ int gemm_nvfp4_rstage_bytes(int bn);   // one raw stage: codes then the token ro
 constexpr int kNv4RawBlocks = 4;                // 64-wide K blocks per raw stage
 constexpr int kNv4RawStageBytes = 128 * 32 * kNv4RawBlocks;   // 128 weight rows x 256 e2m1 codes
 cudaError_t launch_grouped_gemm_nvfp4(const GemmNv4Params& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
+// The NVFP4 grouped GEMM for narrow token tiles (up to 16 tokens of an expert per tile): the
+// codes are decoded to f16 in registers and multiplied on mma.sync, no shared-memory staging.
+cudaError_t launch_grouped_gemm_nvfp4_narrow(const GemmNv4Params& p, int grid, cudaStream_t stream, bool pdl = false);
 // NVFP4 quantisation of rows (row q from src row perm[q] / k, or q without perm): per row
 //   g = max(amax, 1e-10) / 2688, per 16 values s = e4m3(amax_16 / (6 g)), q = e2m1(v / (s g))
 // (float32 operations, round to nearest even, saturating).  Writes the row scale g[q] and any

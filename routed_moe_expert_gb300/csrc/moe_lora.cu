@@ -427,6 +427,13 @@ moe_lora_status enqueue_gemm_nvfp4(moe_lora_handle* h, GemmNv4Params& gp, const 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MOE_LORA_ERR_CUDA;
   }
+  gp.w_codes = W;
+  gp.x16 = X;
+  gp.P = P;
+  if (bn <= 16 && gp.K % 256 == 0) {   // a few tokens per expert: the codes decoded in registers, mma.sync
+    ML_LAUNCH(h, launch_grouped_gemm_nvfp4_narrow(gp, 2 * h->num_sms, stream, pdl), "grouped_gemm_nvfp4 launch");
+    return MOE_LORA_OK;
+  }
   const int lora_R = gp.lora_v != nullptr ? gp.slots.R : 0;
   // (the weight stream is a quarter of the bf16 GEMM's: the kernel is short, and the whole
   // shared memory serves its rings even beside the side-stream LoRA kernel)

@@ -85,15 +85,19 @@ def _nvfp4_gemm_reference(wq, wsf, wgs, x, xgs, offsets):
     return ref, bnd
 
 
-def test_nvfp4_grouped_gemm_within_accumulation_bound(handle):
+@pytest.mark.parametrize("offsets", [[0, 17, 17, 60, 96, 130], [0, 20, 20, 27, 35, 40]],
+                         ids=["wide-tiles", "narrow-tiles"])
+def test_nvfp4_grouped_gemm_within_accumulation_bound(handle, offsets):
     """The NVFP4 grouped GEMM alone, element by element against the float64 product: random
     codes over all 16 values, random e4m3 block scales (subnormals included), five experts of
     ragged sizes with one empty, inputs from the quantiser.  The same data with the two nibbles
     of each byte swapped, or the block scales of neighbouring blocks swapped (plausible slips),
-    lies far outside the bound."""
+    lies far outside the bound.  130 pairs take the 64-token tcgen05 kernel; 40 pairs (an
+    expert of 20: two 16-token tiles) the narrow-tile mma.sync kernel."""
     g = torch.Generator().manual_seed(321)
-    E, N, K, P = 5, 384, 1024, 130
-    offsets = np.array([0, 17, 17, 60, 96, 130], dtype=np.int32)
+    E, N, K = 5, 384, 1024
+    offsets = np.array(offsets, dtype=np.int32)
+    P = int(offsets[-1])
     wq = torch.randint(0, 256, (E, N, K // 2), generator=g, dtype=torch.int32).to(torch.uint8)
     sf = torch.randint(0, 126, (E, N, K // 16), generator=g, dtype=torch.int32).to(torch.uint8)   # finite e4m3
     gs = torch.exp2(torch.empty(E).uniform_(-14, -6, generator=g)).float()
@@ -159,6 +163,9 @@ NVFP4_CASES = [
     wl.CONFIGS["decode"],
     # shared-outer adapter
     wl.LayerConfig("nv4_shared", T=48, H=256, I=256, E=8, top_k=4, ranks=(16, 8), scalings=(2.0, 1.0),
+                   slot_mode="uniform_none10", shared_outer=True),
+    # 16-token tiles (the narrow-tile kernel) with a shared-outer adapter of mixed ranks
+    wl.LayerConfig("nv4_narrow_shared", T=24, H=256, I=256, E=16, top_k=4, ranks=(16, 8), scalings=(2.0, 1.0),
                    slot_mode="uniform_none10", shared_outer=True),
 ]
 
