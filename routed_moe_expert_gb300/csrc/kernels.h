@@ -229,7 +229,8 @@ constexpr int kNv4RawBlocks = 4;                // 64-wide K blocks per raw stag
 constexpr int kNv4RawStageBytes = 128 * 32 * kNv4RawBlocks;   // 128 weight rows x 256 e2m1 codes
 cudaError_t launch_grouped_gemm_nvfp4(const GemmNv4Params& p, int bn, int grid, cudaStream_t stream, bool pdl = false);
 // The NVFP4 grouped GEMM for narrow token tiles (up to 16 tokens of an expert per tile): the
-// codes are decoded to f16 in registers and multiplied on mma.sync, no shared-memory staging.
+// codes stream through a per-warp cp.async ring, are decoded to f16 in registers and multiplied
+// on mma.sync.  K a multiple of 256; w_codes and w_sf 16-byte aligned.
 cudaError_t launch_grouped_gemm_nvfp4_narrow(const GemmNv4Params& p, int grid, cudaStream_t stream, bool pdl = false);
 // NVFP4 quantisation of rows (row q from src row perm[q] / k, or q without perm): per row
 //   g = max(amax, 1e-10) / 2688, per 16 values s = e4m3(amax_16 / (6 g)), q = e2m1(v / (s g))

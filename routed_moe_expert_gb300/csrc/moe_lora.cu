@@ -430,7 +430,9 @@ moe_lora_status enqueue_gemm_nvfp4(moe_lora_handle* h, GemmNv4Params& gp, const 
   gp.w_codes = W;
   gp.x16 = X;
   gp.P = P;
-  if (bn <= 16 && gp.K % 256 == 0) {   // a few tokens per expert: the codes decoded in registers, mma.sync
+  // a few tokens per expert: the codes decoded in registers, mma.sync (its scale rows are copied
+  // 16 bytes at a time)
+  if (bn <= 16 && gp.K % 256 == 0 && aligned16(gp.w_sf)) {
     ML_LAUNCH(h, launch_grouped_gemm_nvfp4_narrow(gp, 2 * h->num_sms, stream, pdl), "grouped_gemm_nvfp4 launch");
     return MOE_LORA_OK;
   }

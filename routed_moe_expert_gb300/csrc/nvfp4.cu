@@ -658,22 +658,28 @@ cudaError_t launch_quant_nvfp4(const __nv_bfloat16* src, const int32_t* perm, in
 
 // ---------------------------------------------------------------------------------
 // Narrow token tiles (decode: a handful of tokens per expert).  A tile is 128 weight rows of
-// one expert x up to 16 of its tokens; each of the 8 warps takes 16 of the rows and streams
-// their codes straight from global memory, kNv4nAhead 256-value K regions (128 bytes of a row)
-// ahead, with no shared-memory staging: each thread decodes its own A-fragment values (cvt
-// e2m1x2 -> f16x2, times the block's e4m3 scale: exact in f16) and multiplies on mma.sync
-// m16n8k16 (f16 in, fp32 accumulate) against the tokens' f16 rows, staged per 1024-value K
-// chunk in shared memory in B-fragment order (one conflict-free 8-byte read per lane and MMA).
-// Within a region, thread (g, t) of the warp (g = lane / 4, t = lane % 4) loads bytes
-// 32t .. 32t+31 (codes 64t .. 64t+63) of rows g and g+8, so each load instruction of the warp
-// covers whole 128-byte lines (few memory requests per byte).  MMA step j (0..15) uses codes
+// one expert x up to 16 of its tokens; each of the 8 warps takes 16 of the rows.  A warp streams
+// its rows' codes and scales one 256-value K region at a time (128 code bytes and 16 scale bytes
+// per row) through its own ring of kNv4nRing regions in shared memory, with 16-byte cp.async
+// copies issued kNv4nRing regions ahead; the stream runs on across the warp's tiles, so the
+// next tile's first regions are in flight while this tile finishes.  Each thread decodes its own
+// A-fragment values from the ring (cvt e2m1x2 -> f16x2, times the block's e4m3 scale: exact in
+// f16) and multiplies on mma.sync m16n8k16 (f16 in, fp32 accumulate) against the tokens' f16
+// rows, staged per 1024-value K chunk in shared memory in B-fragment order (one conflict-free
+// 8-byte read per lane and MMA).  Within a region thread (g, t) of the warp (g = lane / 4,
+// t = lane % 4) takes bytes 32t .. 32t+31 (codes 64t .. 64t+63) of rows g and g+8 (16-byte
+// chunks 2t and 2t+1; chunk c of row r sits at chunk c ^ (r % 8) of its 128-byte ring row, so
+// that neither the copies nor the reads conflict).  MMA step j (0..15) uses codes
 // 64t + 4j .. +3: its k indices 2t, 2t+1 stand for K offsets 64t + 4j, +1 and 2t+8, 2t+9 for
 // 64t + 4j + 2, +3; the tokens' B fragments take the same offsets, so the sum over K is the
 // same sum.  The four codes of a step lie in 16-value block 4t + j/4 of the row: one scale.
 constexpr int kNv4nThreads = 256;   // 8 warps x 16 rows = one 128-row weight tile
 constexpr int kNv4nTok = 16;        // tokens per tile: two 8-token MMA column blocks
-constexpr int kNv4nAhead = 2;       // 256-value K regions (128 bytes of a row) loaded ahead per warp
 constexpr int kNv4nKC = 1024;      // K values of the token rows staged in shared memory at a time
+constexpr int kNv4nPieces = kNv4nKC / 256 * 16 * 32;   // 8-byte B pieces of one 8-token block and K chunk
+constexpr int kNv4nRing = 3;        // regions in flight per warp (shared-memory ring)
+constexpr int kNv4nSlot = 16 * 128 + 16 * 16;   // one region of a warp's 16 rows: codes, then scales
+constexpr int kNv4nSmem = 2 * kNv4nPieces * 8 + (kNv4nThreads / 32) * kNv4nRing * kNv4nSlot;
 
 MLDEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -692,48 +698,100 @@ MLDEV __half2 e4m3_byte_half2(uint32_t w, int i) {
   return __half2(h, h);
 }
 
+MLDEV void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 template <bool LORA>
 __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_kernel(
     const __grid_constant__ GemmNv4Params p) {
   __shared__ int tile_start[kMaxExperts + 1];
   __shared__ int seg[kMaxExperts + 1];
-  // the tile's token rows for one K chunk, in B-fragment order: 8-byte piece (region r, step j,
-  // token g, t) holds K offsets 256 r + 64t + 4j .. +3 of token g of the 8-token block
-  __shared__ uint2 sB[2][kNv4nKC / 256 * 16 * 32];
+  // dynamic: the tile's token rows for one K chunk in B-fragment order (two 8-token blocks:
+  // 8-byte piece (region r, step j, token g, t) holds K offsets 256 r + 64t + 4j .. +3), then
+  // each warp's ring of regions (its 16 rows' codes, 128-byte swizzled, then their scales)
+  extern __shared__ __align__(128) uint8_t nsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  uint2* sB0 = reinterpret_cast<uint2*>(nsm);
+  uint2* sB1 = sB0 + kNv4nPieces;
+  uint8_t* ring = nsm + 2 * kNv4nPieces * 8 + warp * kNv4nRing * kNv4nSlot;
+  const uint32_t ring_s = smem_u32(ring);
   const int E = p.E, N = p.N, K = p.K;
   const int NT = N >> 7;    // 128-row weight tiles per expert
+  const int NR = K >> 8;    // 256-value K regions per row
   pdl_wait();   // the f16 inputs and their row scales come from the previous kernel
   pdl_trigger();
   if (warp == 0) build_tile_schedule(p.offsets, E, kNv4nTok, NT, seg, tile_start);
   __syncthreads();
   const int total = tile_start[E];
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  auto decode = [&](int tile, int& e, int& nt, int& qt) {
     int lo = 0, hi = E - 1;   // last expert with tile_start <= tile (empty experts skipped)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
     }
-    const int e = lo;
+    e = lo;
     const int local = tile - tile_start[e];
     const int nq = (seg[e + 1] - seg[e] + kNv4nTok - 1) / kNv4nTok;
-    const int nt = local / nq, qt = local - nt * nq;
+    nt = local / nq;
+    qt = local - nt * nq;
+  };
+  auto weight_row = [&](int nt, int r) {   // the weight row of row r of tile nt
+    return p.gated ? (r < 64 ? nt * 64 + r : (N >> 1) + nt * 64 + r - 64) : nt * 128 + r;
+  };
+  // ---- the warp's stream of regions over its tiles, copied kNv4nRing regions ahead: lane l
+  // copies 16-byte chunks l, l+32, l+64, l+96 of a region's 16 rows x 128 bytes (row 4i + l/8,
+  // chunk l % 8) and, lanes 0..15, the 16 scale bytes of row l
+  int is_tile = blockIdx.x, is_r = 0;
+  const uint8_t* cbase[4];
+  const uint8_t* sbase = nullptr;
+  auto issue_rows = [&](int tile) {
+    int e, nt, qt;
+    decode(tile, e, nt, qt);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      cbase[i] = p.w_codes + (static_cast<size_t>(e) * N + weight_row(nt, warp * 16 + 4 * i + (lane >> 3))) *
+                                 (K >> 1);
+    sbase = p.w_sf + (static_cast<size_t>(e) * N + weight_row(nt, warp * 16 + (lane & 15))) * (K >> 4);
+  };
+  int issued = 0;
+  auto issue_next = [&]() {
+    if (is_tile < total) {
+      const uint32_t dst = ring_s + static_cast<uint32_t>((issued % kNv4nRing) * kNv4nSlot);
+      const int c = lane & 7;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = 4 * i + (lane >> 3);
+        cp_async16(dst + row * 128 + ((c ^ (row & 7)) << 4), cbase[i] + is_r * 128 + c * 16);
+      }
+      if (lane < 16) cp_async16(dst + 2048 + lane * 16, sbase + is_r * 16);
+      if (++is_r == NR) {
+        is_r = 0;
+        is_tile += gridDim.x;
+        if (is_tile < total) issue_rows(is_tile);
+      }
+    }
+    cp_async_commit();   // an empty group past the end keeps one group per region
+    ++issued;
+  };
+  if (is_tile < total) issue_rows(is_tile);
+#pragma unroll 1
+  for (int d = 0; d < kNv4nRing; ++d) issue_next();
+  int consumed = 0;
+
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int e, nt, qt;
+    decode(tile, e, nt, qt);
     const int q0 = seg[e] + qt * kNv4nTok;
     const int nvalid = min(kNv4nTok, seg[e + 1] - q0);
     const bool tv1 = nvalid > 8;   // the second 8-token column block has tokens (warp-uniform)
     // this thread's two weight rows (tile rows r0, r1; weight rows n0, n1)
     const int r0 = warp * 16 + g, r1 = r0 + 8;
-    const int n0 = p.gated ? (r0 < 64 ? nt * 64 + r0 : (N >> 1) + nt * 64 + r0 - 64) : nt * 128 + r0;
-    const int n1 = p.gated ? (r1 < 64 ? nt * 64 + r1 : (N >> 1) + nt * 64 + r1 - 64) : nt * 128 + r1;
-    const size_t w0 = static_cast<size_t>(e) * N + n0, w1 = static_cast<size_t>(e) * N + n1;
-    const uint4* c0p = reinterpret_cast<const uint4*>(p.w_codes + w0 * (K >> 1) + 32 * t);
-    const uint4* c1p = reinterpret_cast<const uint4*>(p.w_codes + w1 * (K >> 1) + 32 * t);
-    const uint32_t* s0p = reinterpret_cast<const uint32_t*>(p.w_sf + w0 * (K >> 4) + 4 * t);
-    const uint32_t* s1p = reinterpret_cast<const uint32_t*>(p.w_sf + w1 * (K >> 4) + 4 * t);
+    const int n0 = weight_row(nt, r0), n1 = weight_row(nt, r1);
     float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     for (int kc0 = 0; kc0 < K; kc0 += kNv4nKC) {
-      const int kcl = min(kNv4nKC, K - kc0);   // a multiple of 64
+      const int kcl = min(kNv4nKC, K - kc0);   // a multiple of 256
       const int npc = kcl >> 2;                 // 8-byte pieces per token row
       __syncthreads();   // every warp is done with the previous chunk's rows
       for (int idx = threadIdx.x; idx < kNv4nTok * npc; idx += kNv4nThreads) {
@@ -741,52 +799,46 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
         const int rr = c >> 6, tt = (c >> 4) & 3, jj = c & 15;
         uint2 v = make_uint2(0u, 0u);   // zero rows past the tile's tokens
         if (tok < nvalid) v = __ldg(reinterpret_cast<const uint2*>(p.x16 + static_cast<size_t>(q0 + tok) * K + kc0) + c);
-        sB[tok >> 3][((rr * 16 + jj) * 8 + (tok & 7)) * 4 + tt] = v;
+        (tok < 8 ? sB0 : sB1)[((rr * 16 + jj) * 8 + (tok & 7)) * 4 + tt] = v;
       }
       __syncthreads();
-      const int rg0 = kc0 >> 8, nrg = kcl >> 8;
-      for (int rg1 = 0; rg1 < nrg; rg1 += kNv4nAhead) {
-        uint4 cl0[kNv4nAhead], ch0[kNv4nAhead], cl1[kNv4nAhead], ch1[kNv4nAhead];
-        uint32_t sw0[kNv4nAhead], sw1[kNv4nAhead];
+      const int nrg = kcl >> 8;
+#pragma unroll 1
+      for (int rl = 0; rl < nrg; ++rl) {
+        cp_async_wait<kNv4nRing - 1>();   // this thread's copies of the oldest region have landed
+        __syncwarp();                     // ... and every lane's
+        const uint8_t* sl = ring + (consumed % kNv4nRing) * kNv4nSlot;
+        // this thread's 32 code bytes of rows g and g+8 (chunks 2t, 2t+1; rows g and g+8 share
+        // the swizzle) and the scales of its four blocks of 16
+        const int x0 = ((2 * t) ^ (g & 7)) << 4, x1 = ((2 * t + 1) ^ (g & 7)) << 4;
+        const uint4 cl0 = *reinterpret_cast<const uint4*>(sl + g * 128 + x0);
+        const uint4 ch0 = *reinterpret_cast<const uint4*>(sl + g * 128 + x1);
+        const uint4 cl1 = *reinterpret_cast<const uint4*>(sl + (g + 8) * 128 + x0);
+        const uint4 ch1 = *reinterpret_cast<const uint4*>(sl + (g + 8) * 128 + x1);
+        const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(sl + 2048 + g * 16 + 4 * t);
+        const uint32_t sw1 = *reinterpret_cast<const uint32_t*>(sl + 2048 + (g + 8) * 16 + 4 * t);
+        __syncwarp();   // every lane has read the slot: it takes the next region
+        issue_next();
+        ++consumed;
 #pragma unroll
-        for (int i = 0; i < kNv4nAhead; ++i) {   // the codes and scales of the next regions, in flight together
-          const int rg = rg0 + rg1 + i;
-          if (rg1 + i < nrg) {
-            cl0[i] = __ldg(c0p + rg * 8);       // 128 bytes of codes per row and region:
-            ch0[i] = __ldg(c0p + rg * 8 + 1);   // this thread's 32 of them
-            cl1[i] = __ldg(c1p + rg * 8);
-            ch1[i] = __ldg(c1p + rg * 8 + 1);
-            sw0[i] = __ldg(s0p + rg * 4);       // the scales of its 4 blocks of 16
-            sw1[i] = __ldg(s1p + rg * 4);
-          } else {
-            cl0[i] = ch0[i] = cl1[i] = ch1[i] = make_uint4(0u, 0u, 0u, 0u);
-            sw0[i] = sw1[i] = 0u;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < kNv4nAhead; ++i) {
-          const int rl = rg1 + i;   // the region within the chunk
-          if (rl >= nrg) break;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint4& qa = j < 8 ? cl0[i] : ch0[i];
-            const uint4& qb = j < 8 ? cl1[i] : ch1[i];
-            const int w = (j & 7) >> 1;
-            const uint32_t wa = w == 0 ? qa.x : w == 1 ? qa.y : w == 2 ? qa.z : qa.w;
-            const uint32_t wb = w == 0 ? qb.x : w == 1 ? qb.y : w == 2 ? qb.z : qb.w;
-            const int sh = 16 * (j & 1);
-            const __half2 s0 = e4m3_byte_half2(sw0[i], j >> 2), s1 = e4m3_byte_half2(sw1[i], j >> 2);
-            uint32_t a[4];
-            a[0] = half2_bits(__hmul2(e2m1x2_to_half2(wa >> sh), s0));         // row g,   k 2t, 2t+1
-            a[1] = half2_bits(__hmul2(e2m1x2_to_half2(wb >> sh), s1));         // row g+8, k 2t, 2t+1
-            a[2] = half2_bits(__hmul2(e2m1x2_to_half2(wa >> (sh + 8)), s0));   // row g,   k 2t+8, 2t+9
-            a[3] = half2_bits(__hmul2(e2m1x2_to_half2(wb >> (sh + 8)), s1));   // row g+8, k 2t+8, 2t+9
-            const uint2 b0 = sB[0][(rl * 16 + j) * 32 + lane];
-            mma_f16_16816(acc0, a, b0.x, b0.y);
-            if (tv1) {
-              const uint2 b1 = sB[1][(rl * 16 + j) * 32 + lane];
-              mma_f16_16816(acc1, a, b1.x, b1.y);
-            }
+        for (int j = 0; j < 16; ++j) {
+          const uint4& qa = j < 8 ? cl0 : ch0;
+          const uint4& qb = j < 8 ? cl1 : ch1;
+          const int w = (j & 7) >> 1;
+          const uint32_t wa = w == 0 ? qa.x : w == 1 ? qa.y : w == 2 ? qa.z : qa.w;
+          const uint32_t wb = w == 0 ? qb.x : w == 1 ? qb.y : w == 2 ? qb.z : qb.w;
+          const int sh = 16 * (j & 1);
+          const __half2 s0 = e4m3_byte_half2(sw0, j >> 2), s1 = e4m3_byte_half2(sw1, j >> 2);
+          uint32_t a[4];
+          a[0] = half2_bits(__hmul2(e2m1x2_to_half2(wa >> sh), s0));         // row g,   k 2t, 2t+1
+          a[1] = half2_bits(__hmul2(e2m1x2_to_half2(wb >> sh), s1));         // row g+8, k 2t, 2t+1
+          a[2] = half2_bits(__hmul2(e2m1x2_to_half2(wa >> (sh + 8)), s0));   // row g,   k 2t+8, 2t+9
+          a[3] = half2_bits(__hmul2(e2m1x2_to_half2(wb >> (sh + 8)), s1));   // row g+8, k 2t+8, 2t+9
+          const uint2 b0 = sB0[(rl * 16 + j) * 32 + lane];
+          mma_f16_16816(acc0, a, b0.x, b0.y);
+          if (tv1) {
+            const uint2 b1 = sB1[(rl * 16 + j) * 32 + lane];
+            mma_f16_16816(acc1, a, b1.x, b1.y);
           }
         }
       }
@@ -830,11 +882,18 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
 }
 
 cudaError_t launch_grouped_gemm_nvfp4_narrow(const GemmNv4Params& p, int grid, cudaStream_t stream, bool pdl) {
-  if (grid < 1 || p.N % 128 != 0 || p.K % 256 != 0 || p.w_codes == nullptr || p.x16 == nullptr)
+  if (grid < 1 || p.N % 128 != 0 || p.K % 256 != 0 || p.w_codes == nullptr || p.x16 == nullptr ||
+      (reinterpret_cast<uintptr_t>(p.w_codes) & 15u) != 0 || (reinterpret_cast<uintptr_t>(p.w_sf) & 15u) != 0)
     return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_nvfp4_narrow_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kNv4nSmem);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(grouped_gemm_nvfp4_narrow_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kNv4nSmem);
+  if (err != cudaSuccess) return err;
   if (p.lora_v != nullptr)
-    return launch_k(grouped_gemm_nvfp4_narrow_kernel<true>, dim3(grid), dim3(kNv4nThreads), 0, stream, pdl, p);
-  return launch_k(grouped_gemm_nvfp4_narrow_kernel<false>, dim3(grid), dim3(kNv4nThreads), 0, stream, pdl, p);
+    return launch_k(grouped_gemm_nvfp4_narrow_kernel<true>, dim3(grid), dim3(kNv4nThreads), kNv4nSmem, stream, pdl, p);
+  return launch_k(grouped_gemm_nvfp4_narrow_kernel<false>, dim3(grid), dim3(kNv4nThreads), kNv4nSmem, stream, pdl, p);
 }
 
 }  // namespace mlk
