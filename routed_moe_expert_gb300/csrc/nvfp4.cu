@@ -676,6 +676,7 @@ cudaError_t launch_quant_nvfp4(const __nv_bfloat16* src, const int32_t* perm, in
 constexpr int kNv4nThreads = 256;   // 8 warps x 16 rows = one 128-row weight tile
 constexpr int kNv4nTok = 16;        // tokens per tile: two 8-token MMA column blocks
 constexpr int kNv4nKC = 1024;      // K values of the token rows staged in shared memory at a time
+static_assert(kNv4nKC / 4 == kNv4nThreads, "one 8-byte piece of each token row per thread");
 constexpr int kNv4nPieces = kNv4nKC / 256 * 16 * 32;   // 8-byte B pieces of one 8-token block and K chunk
 constexpr int kNv4nRing = 3;        // regions in flight per warp (shared-memory ring)
 constexpr int kNv4nSlot = 16 * 128 + 16 * 16;   // one region of a warp's 16 rows: codes, then scales
@@ -696,6 +697,24 @@ MLDEV __half2 e4m3_byte_half2(uint32_t w, int i) {
   const __half_raw r = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((w >> (8 * i)) & 0xFFu), __NV_E4M3);
   const __half h(r);
   return __half2(h, h);
+}
+
+// f16x2 values of the 8 e2m1 codes of w: h[i] holds the codes of byte i (low nibble in the low
+// half), exact
+MLDEV void e2m1x8_to_half2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, c2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+MLDEV uint32_t hmul2_bits(uint32_t a, __half2 s) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 MLDEV void cp_async16(uint32_t dst, const void* src) {
@@ -794,12 +813,20 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
       const int kcl = min(kNv4nKC, K - kc0);   // a multiple of 256
       const int npc = kcl >> 2;                 // 8-byte pieces per token row
       __syncthreads();   // every warp is done with the previous chunk's rows
-      for (int idx = threadIdx.x; idx < kNv4nTok * npc; idx += kNv4nThreads) {
-        const int tok = idx / npc, c = idx - tok * npc;   // piece c: K offsets kc0 + 4c .. +3
-        const int rr = c >> 6, tt = (c >> 4) & 3, jj = c & 15;
-        uint2 v = make_uint2(0u, 0u);   // zero rows past the tile's tokens
-        if (tok < nvalid) v = __ldg(reinterpret_cast<const uint2*>(p.x16 + static_cast<size_t>(q0 + tok) * K + kc0) + c);
-        (tok < 8 ? sB0 : sB1)[((rr * 16 + jj) * 8 + (tok & 7)) * 4 + tt] = v;
+      // thread c stages piece c (K offsets kc0 + 4c .. +3) of each of the tile's token rows, all
+      // loads first; rows past the tile's tokens are not staged: their accumulator columns are
+      // never stored
+      if (threadIdx.x < npc) {
+        const int c = threadIdx.x;
+        const int so = (((c >> 6) * 16 + (c & 15)) * 8) * 4 + ((c >> 4) & 3);
+        const uint2* src = reinterpret_cast<const uint2*>(p.x16 + static_cast<size_t>(q0) * K + kc0) + c;
+        uint2 v[kNv4nTok];
+#pragma unroll
+        for (int tok = 0; tok < kNv4nTok; ++tok)
+          if (tok < nvalid) v[tok] = __ldg(src + static_cast<size_t>(tok) * (K >> 2));
+#pragma unroll
+        for (int tok = 0; tok < kNv4nTok; ++tok)
+          if (tok < nvalid) (tok < 8 ? sB0 : sB1)[so + (tok & 7) * 4] = v[tok];
       }
       __syncthreads();
       const int nrg = kcl >> 8;
@@ -821,24 +848,28 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
         issue_next();
         ++consumed;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint4& qa = j < 8 ? cl0 : ch0;
-          const uint4& qb = j < 8 ? cl1 : ch1;
-          const int w = (j & 7) >> 1;
-          const uint32_t wa = w == 0 ? qa.x : w == 1 ? qa.y : w == 2 ? qa.z : qa.w;
-          const uint32_t wb = w == 0 ? qb.x : w == 1 ? qb.y : w == 2 ? qb.z : qb.w;
-          const int sh = 16 * (j & 1);
-          const __half2 s0 = e4m3_byte_half2(sw0, j >> 2), s1 = e4m3_byte_half2(sw1, j >> 2);
-          uint32_t a[4];
-          a[0] = half2_bits(__hmul2(e2m1x2_to_half2(wa >> sh), s0));         // row g,   k 2t, 2t+1
-          a[1] = half2_bits(__hmul2(e2m1x2_to_half2(wb >> sh), s1));         // row g+8, k 2t, 2t+1
-          a[2] = half2_bits(__hmul2(e2m1x2_to_half2(wa >> (sh + 8)), s0));   // row g,   k 2t+8, 2t+9
-          a[3] = half2_bits(__hmul2(e2m1x2_to_half2(wb >> (sh + 8)), s1));   // row g+8, k 2t+8, 2t+9
-          const uint2 b0 = sB0[(rl * 16 + j) * 32 + lane];
-          mma_f16_16816(acc0, a, b0.x, b0.y);
-          if (tv1) {
-            const uint2 b1 = sB1[(rl * 16 + j) * 32 + lane];
-            mma_f16_16816(acc1, a, b1.x, b1.y);
+        for (int w = 0; w < 8; ++w) {   // word w: steps 2w and 2w + 1
+          const uint4& qa = w < 4 ? cl0 : ch0;
+          const uint4& qb = w < 4 ? cl1 : ch1;
+          const int ww = w & 3;
+          uint32_t ha[4], hb[4];
+          e2m1x8_to_half2x4(ww == 0 ? qa.x : ww == 1 ? qa.y : ww == 2 ? qa.z : qa.w, ha);
+          e2m1x8_to_half2x4(ww == 0 ? qb.x : ww == 1 ? qb.y : ww == 2 ? qb.z : qb.w, hb);
+          const __half2 s0 = e4m3_byte_half2(sw0, w >> 1), s1 = e4m3_byte_half2(sw1, w >> 1);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = 2 * w + u;
+            uint32_t a[4];
+            a[0] = hmul2_bits(ha[2 * u], s0);       // row g,   k 2t, 2t+1
+            a[1] = hmul2_bits(hb[2 * u], s1);       // row g+8, k 2t, 2t+1
+            a[2] = hmul2_bits(ha[2 * u + 1], s0);   // row g,   k 2t+8, 2t+9
+            a[3] = hmul2_bits(hb[2 * u + 1], s1);   // row g+8, k 2t+8, 2t+9
+            const uint2 b0 = sB0[(rl * 16 + j) * 32 + lane];
+            mma_f16_16816(acc0, a, b0.x, b0.y);
+            if (tv1) {
+              const uint2 b1 = sB1[(rl * 16 + j) * 32 + lane];
+              mma_f16_16816(acc1, a, b1.x, b1.y);
+            }
           }
         }
       }
