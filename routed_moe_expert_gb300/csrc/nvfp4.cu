@@ -717,6 +717,54 @@ MLDEV uint32_t hmul2_bits(uint32_t a, __half2 s) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+MLDEV void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+
+// The down-LoRA expand of one 8-token column block c of a narrow tile for this thread (tokens
+// 8c + 2t + i, slots ts[i], negative: none; weight rows n0, n1), rows of R = 8 NC values:
+// ls[i][half] = sum_{r < ranks[s]} lora_B[s, e, n, r] * lora_v[q, r], in order of r.  Every
+// load is issued first (from a valid row for a token without a slot, whose rank counts as 0).
+template <int NC>
+MLDEV void nv4n_lora_expand(const GemmNv4Params& p, int e, int q0, int c, int t, int n0, int n1, const int (&ts)[2],
+                            float (&ls)[2][2]) {
+  const int R = 8 * NC, N = p.N;
+  uint4 bw[2][2][NC];
+  float4 vv[2][2 * NC];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int s = ts[i] >= 0 ? ts[i] : 0;
+    const int q = q0 + (ts[i] >= 0 ? 8 * c + 2 * t + i : 0);
+    const size_t be = p.lora_b_e1 ? static_cast<size_t>(s) : static_cast<size_t>(s) * p.E + e;
+    const float4* vq = reinterpret_cast<const float4*>(p.lora_v + static_cast<size_t>(q) * R);
+#pragma unroll
+    for (int h = 0; h < 2 * NC; ++h) vv[i][h] = __ldg(vq + h);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint4* Brow = reinterpret_cast<const uint4*>(p.lora_B + (be * N + (hh == 0 ? n0 : n1)) * R);
+#pragma unroll
+      for (int ch = 0; ch < NC; ++ch) bw[i][hh][ch] = __ldg(Brow + ch);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int rank = ts[i] >= 0 ? p.slots.ranks[ts[i]] : 0;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int ch = 0; ch < NC; ++ch) {
+        float bv[8];
+        unpack8(bw[i][hh][ch], bv);
+        const float v8[8] = {vv[i][2 * ch].x,     vv[i][2 * ch].y,     vv[i][2 * ch].z,     vv[i][2 * ch].w,
+                             vv[i][2 * ch + 1].x, vv[i][2 * ch + 1].y, vv[i][2 * ch + 1].z, vv[i][2 * ch + 1].w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (8 * ch + u < rank) sum = fmaf(bv[u], v8[u], sum);
+      }
+      ls[i][hh] = sum;
+    }
+  }
+}
+
 MLDEV void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -809,26 +857,64 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
     const int r0 = warp * 16 + g, r1 = r0 + 8;
     const int n0 = weight_row(nt, r0), n1 = weight_row(nt, r1);
     float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // the down-LoRA slots of this thread's tokens 8c + 2t + i (negative: none); their B and v
+    // rows are prefetched into L2 once the first K chunk is staged and read in the epilogue
+    int tslot[2][2] = {{-1, -1}, {-1, -1}};
+    if constexpr (LORA) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int j = 8 * c + 2 * t + i;
+          if (j < nvalid) {
+            const int sl = __ldg(p.pair_slot + q0 + j);
+            tslot[c][i] = sl < p.slots.S ? sl : -1;
+          }
+        }
+      }
+    }
     for (int kc0 = 0; kc0 < K; kc0 += kNv4nKC) {
       const int kcl = min(kNv4nKC, K - kc0);   // a multiple of 256
       const int npc = kcl >> 2;                 // 8-byte pieces per token row
       __syncthreads();   // every warp is done with the previous chunk's rows
-      // thread c stages piece c (K offsets kc0 + 4c .. +3) of each of the tile's token rows, all
-      // loads first; rows past the tile's tokens are not staged: their accumulator columns are
-      // never stored
+      // thread c stages piece c (K offsets kc0 + 4c .. +3) of each of the tile's token rows, per
+      // 8-token block all loads first; rows past the tile's tokens are not staged: their
+      // accumulator columns are never stored
       if (threadIdx.x < npc) {
         const int c = threadIdx.x;
         const int so = (((c >> 6) * 16 + (c & 15)) * 8) * 4 + ((c >> 4) & 3);
         const uint2* src = reinterpret_cast<const uint2*>(p.x16 + static_cast<size_t>(q0) * K + kc0) + c;
-        uint2 v[kNv4nTok];
 #pragma unroll
-        for (int tok = 0; tok < kNv4nTok; ++tok)
-          if (tok < nvalid) v[tok] = __ldg(src + static_cast<size_t>(tok) * (K >> 2));
+        for (int blk = 0; blk < 2; ++blk) {
+          if (blk == 1 && !tv1) break;
+          uint2* sB = blk == 0 ? sB0 : sB1;
+          uint2 v[8];
 #pragma unroll
-        for (int tok = 0; tok < kNv4nTok; ++tok)
-          if (tok < nvalid) (tok < 8 ? sB0 : sB1)[so + (tok & 7) * 4] = v[tok];
+          for (int tok = 0; tok < 8; ++tok)
+            if (8 * blk + tok < nvalid) v[tok] = __ldg(src + static_cast<size_t>(8 * blk + tok) * (K >> 2));
+#pragma unroll
+          for (int tok = 0; tok < 8; ++tok)
+            if (8 * blk + tok < nvalid) sB[so + tok * 4] = v[tok];
+        }
       }
       __syncthreads();
+      if constexpr (LORA) {
+        if (kc0 == 0) {
+          const int R = p.slots.R;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int sl = tslot[c][i];
+              if (sl < 0) continue;
+              const size_t be = p.lora_b_e1 ? static_cast<size_t>(sl) : static_cast<size_t>(sl) * E + e;
+              prefetch_l2(p.lora_B + (be * N + n0) * R);
+              prefetch_l2(p.lora_B + (be * N + n1) * R);
+              prefetch_l2(p.lora_v + static_cast<size_t>(q0 + 8 * c + 2 * t + i) * R);
+            }
+          }
+        }
+      }
       const int nrg = kcl >> 8;
 #pragma unroll 1
       for (int rl = 0; rl < nrg; ++rl) {
@@ -876,7 +962,39 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
     }
     // epilogue: accumulator (row, token) = acc_c[2 * half + i] for row g (+8 when half = 1),
     // token 8c + 2t + i; times the token's and the expert's scales, plus the down-LoRA expand
-    const float gw = __ldg(p.w_gs + e);
+    // lsum[c][i][half] = sum_{r < ranks[s]} lora_B[s, e, n, r] * lora_v[q, r] (s = pair_slot[q]),
+    // summed in order of r; for rows of 8 or 16 values all loads are issued before the sums
+    float lsum[2][2][2] = {{{0.0f, 0.0f}, {0.0f, 0.0f}}, {{0.0f, 0.0f}, {0.0f, 0.0f}}};
+    if constexpr (LORA) {
+      const int R = p.slots.R;
+      const bool al = ((reinterpret_cast<uintptr_t>(p.lora_B) | reinterpret_cast<uintptr_t>(p.lora_v)) & 15u) == 0;
+      if (al && R == 16) {
+        nv4n_lora_expand<2>(p, e, q0, 0, t, n0, n1, tslot[0], lsum[0]);
+        if (tv1) nv4n_lora_expand<2>(p, e, q0, 1, t, n0, n1, tslot[1], lsum[1]);
+      } else if (al && R == 8) {
+        nv4n_lora_expand<1>(p, e, q0, 0, t, n0, n1, tslot[0], lsum[0]);
+        if (tv1) nv4n_lora_expand<1>(p, e, q0, 1, t, n0, n1, tslot[1], lsum[1]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int sl = tslot[c][i];
+            if (sl < 0) continue;
+            const int q = q0 + 8 * c + 2 * t + i, rank = p.slots.ranks[sl];
+            const size_t be = p.lora_b_e1 ? static_cast<size_t>(sl) : static_cast<size_t>(sl) * E + e;
+            const float* vq = p.lora_v + static_cast<size_t>(q) * R;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const __nv_bfloat16* Brow = p.lora_B + (be * N + (hh == 0 ? n0 : n1)) * static_cast<size_t>(R);
+              float sum = 0.0f;
+              for (int r = 0; r < rank; ++r) sum = fmaf(bf2f(Brow[r]), __ldg(vq + r), sum);
+              lsum[c][i][hh] = sum;
+            }
+          }
+        }
+      }
+    }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -884,24 +1002,11 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
         const int j = 8 * c + 2 * t + i;
         if (j >= nvalid) continue;
         const int q = q0 + j;
-        const float sc = __fmul_rn(__ldg(p.x_gs + q), gw);
-        int sl = -1;
-        if constexpr (LORA) sl = p.pair_slot[q];
+        const float sc = __fmul_rn(__ldg(p.x_gs + q), __ldg(p.w_gs + e));
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float val = (c == 0 ? acc0[2 * hh + i] : acc1[2 * hh + i]) * sc;
-          const int n = hh == 0 ? n0 : n1;
-          if constexpr (LORA) {
-            if (sl >= 0 && sl < p.slots.S) {
-              const int R = p.slots.R, rank = p.slots.ranks[sl];
-              const size_t be = p.lora_b_e1 ? static_cast<size_t>(sl) : static_cast<size_t>(sl) * E + e;
-              const __nv_bfloat16* Brow = p.lora_B + (be * N + n) * static_cast<size_t>(R);
-              const float* vq = p.lora_v + static_cast<size_t>(q) * R;
-              float sum = 0.0f;
-              for (int r = 0; r < rank; ++r) sum += bf2f(Brow[r]) * vq[r];
-              val += sum;
-            }
-          }
+          if constexpr (LORA) val += lsum[c][i][hh];
           const int col = nt * 128 + (hh == 0 ? r0 : r1);   // the output's column order (gated: interleaved)
           const size_t off = static_cast<size_t>(q) * N + col;
           if (p.out_f32 != nullptr) p.out_f32[off] = val;

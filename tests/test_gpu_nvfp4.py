@@ -167,6 +167,12 @@ NVFP4_CASES = [
     # 16-token tiles (the narrow-tile kernel) with a shared-outer adapter of mixed ranks
     wl.LayerConfig("nv4_narrow_shared", T=24, H=256, I=256, E=16, top_k=4, ranks=(16, 8), scalings=(2.0, 1.0),
                    slot_mode="uniform_none10", shared_outer=True),
+    # 16-token tiles, down-LoRA rows of 8 values (the expand's one-piece rows)
+    wl.LayerConfig("nv4_narrow_r8", T=20, H=512, I=256, E=8, top_k=2, ranks=(8, 4), scalings=(1.0, 2.0),
+                   slot_mode="uniform_none10"),
+    # 16-token tiles, down-LoRA rows of 12 values (the expand's element-wise rows)
+    wl.LayerConfig("nv4_narrow_r12", T=24, H=256, I=256, E=16, top_k=4, ranks=(4, 12), scalings=(2.0, 1.0),
+                   slot_mode="uniform_none10"),
 ]
 
 
