@@ -43,6 +43,8 @@
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -692,11 +694,14 @@ MLDEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uin
 
 MLDEV uint32_t half2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
-// {s, s} for the e4m3 code in byte `i` of w
-MLDEV __half2 e4m3_byte_half2(uint32_t w, int i) {
-  const __half_raw r = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((w >> (8 * i)) & 0xFFu), __NV_E4M3);
-  const __half h(r);
-  return __half2(h, h);
+// s[i] = {v, v} for v the e4m3 code in byte i of w, exact in f16
+MLDEV void e4m3x4_to_half2_bcast(uint32_t w, __half2 (&s)[4]) {
+  const __half2 lo(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3));
+  const __half2 hi(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3));
+  s[0] = __low2half2(lo);
+  s[1] = __high2half2(lo);
+  s[2] = __low2half2(hi);
+  s[3] = __high2half2(hi);
 }
 
 // f16x2 values of the 8 e2m1 codes of w: h[i] holds the codes of byte i (low nibble in the low
@@ -822,10 +827,10 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
                                  (K >> 1);
     sbase = p.w_sf + (static_cast<size_t>(e) * N + weight_row(nt, warp * 16 + (lane & 15))) * (K >> 4);
   };
-  int issued = 0;
+  int islot = 0;   // ring slot of the next region copied
   auto issue_next = [&]() {
     if (is_tile < total) {
-      const uint32_t dst = ring_s + static_cast<uint32_t>((issued % kNv4nRing) * kNv4nSlot);
+      const uint32_t dst = ring_s + static_cast<uint32_t>(islot * kNv4nSlot);
       const int c = lane & 7;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -840,12 +845,12 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
       }
     }
     cp_async_commit();   // an empty group past the end keeps one group per region
-    ++issued;
+    if (++islot == kNv4nRing) islot = 0;
   };
   if (is_tile < total) issue_rows(is_tile);
 #pragma unroll 1
   for (int d = 0; d < kNv4nRing; ++d) issue_next();
-  int consumed = 0;
+  int cslot = 0;   // ring slot of the next region used
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
     int e, nt, qt;
@@ -920,7 +925,7 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
       for (int rl = 0; rl < nrg; ++rl) {
         cp_async_wait<kNv4nRing - 1>();   // this thread's copies of the oldest region have landed
         __syncwarp();                     // ... and every lane's
-        const uint8_t* sl = ring + (consumed % kNv4nRing) * kNv4nSlot;
+        const uint8_t* sl = ring + cslot * kNv4nSlot;
         // this thread's 32 code bytes of rows g and g+8 (chunks 2t, 2t+1; rows g and g+8 share
         // the swizzle) and the scales of its four blocks of 16
         const int x0 = ((2 * t) ^ (g & 7)) << 4, x1 = ((2 * t + 1) ^ (g & 7)) << 4;
@@ -932,32 +937,42 @@ __global__ void __launch_bounds__(kNv4nThreads, 2) grouped_gemm_nvfp4_narrow_ker
         const uint32_t sw1 = *reinterpret_cast<const uint32_t*>(sl + 2048 + (g + 8) * 16 + 4 * t);
         __syncwarp();   // every lane has read the slot: it takes the next region
         issue_next();
-        ++consumed;
+        if (++cslot == kNv4nRing) cslot = 0;
+        __half2 sc0[4], sc1[4];   // the block scales of rows g and g+8, one per 16 values
+        e4m3x4_to_half2_bcast(sw0, sc0);
+        e4m3x4_to_half2_bcast(sw1, sc1);
+        const uint2* b0p = sB0 + rl * 16 * 32 + lane;
+        const uint2* b1p = sB1 + rl * 16 * 32 + lane;
+        // the region's 16 MMA steps, with the second 8-token block or without it
+        auto steps = [&](auto two) {
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {   // word w: steps 2w and 2w + 1
-          const uint4& qa = w < 4 ? cl0 : ch0;
-          const uint4& qb = w < 4 ? cl1 : ch1;
-          const int ww = w & 3;
-          uint32_t ha[4], hb[4];
-          e2m1x8_to_half2x4(ww == 0 ? qa.x : ww == 1 ? qa.y : ww == 2 ? qa.z : qa.w, ha);
-          e2m1x8_to_half2x4(ww == 0 ? qb.x : ww == 1 ? qb.y : ww == 2 ? qb.z : qb.w, hb);
-          const __half2 s0 = e4m3_byte_half2(sw0, w >> 1), s1 = e4m3_byte_half2(sw1, w >> 1);
+          for (int w = 0; w < 8; ++w) {   // word w: steps 2w and 2w + 1
+            const uint4& qa = w < 4 ? cl0 : ch0;
+            const uint4& qb = w < 4 ? cl1 : ch1;
+            const int ww = w & 3;
+            uint32_t ha[4], hb[4];
+            e2m1x8_to_half2x4(ww == 0 ? qa.x : ww == 1 ? qa.y : ww == 2 ? qa.z : qa.w, ha);
+            e2m1x8_to_half2x4(ww == 0 ? qb.x : ww == 1 ? qb.y : ww == 2 ? qb.z : qb.w, hb);
+            const __half2 s0 = sc0[w >> 1], s1 = sc1[w >> 1];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = 2 * w + u;
-            uint32_t a[4];
-            a[0] = hmul2_bits(ha[2 * u], s0);       // row g,   k 2t, 2t+1
-            a[1] = hmul2_bits(hb[2 * u], s1);       // row g+8, k 2t, 2t+1
-            a[2] = hmul2_bits(ha[2 * u + 1], s0);   // row g,   k 2t+8, 2t+9
-            a[3] = hmul2_bits(hb[2 * u + 1], s1);   // row g+8, k 2t+8, 2t+9
-            const uint2 b0 = sB0[(rl * 16 + j) * 32 + lane];
-            mma_f16_16816(acc0, a, b0.x, b0.y);
-            if (tv1) {
-              const uint2 b1 = sB1[(rl * 16 + j) * 32 + lane];
-              mma_f16_16816(acc1, a, b1.x, b1.y);
+            for (int u = 0; u < 2; ++u) {
+              const int j = 2 * w + u;
+              uint32_t a[4];
+              a[0] = hmul2_bits(ha[2 * u], s0);       // row g,   k 2t, 2t+1
+              a[1] = hmul2_bits(hb[2 * u], s1);       // row g+8, k 2t, 2t+1
+              a[2] = hmul2_bits(ha[2 * u + 1], s0);   // row g,   k 2t+8, 2t+9
+              a[3] = hmul2_bits(hb[2 * u + 1], s1);   // row g+8, k 2t+8, 2t+9
+              const uint2 b0 = b0p[j * 32];
+              mma_f16_16816(acc0, a, b0.x, b0.y);
+              if constexpr (decltype(two)::value) {
+                const uint2 b1 = b1p[j * 32];
+                mma_f16_16816(acc1, a, b1.x, b1.y);
+              }
             }
           }
-        }
+        };
+        if (tv1) steps(std::true_type{});
+        else steps(std::false_type{});
       }
     }
     // epilogue: accumulator (row, token) = acc_c[2 * half + i] for row g (+8 when half = 1),
