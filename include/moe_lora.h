@@ -403,8 +403,9 @@ moe_lora_status moe_lora_quant_nvfp4(moe_lora_handle* h, const moe_lora_bf16* sr
    codes (16-byte aligned), w_sf [E, N, K/16] e4m3 block scales and w_gs [E], x_gs [P] float32
    (4-byte aligned), expert_offsets [E + 1] int32 (non-decreasing, offsets[E] = P), out [P, N]
    float32 (16-byte aligned).  The products are exact; the tensor cores sum them in fp32.  N a
-   multiple of 128, K of 64, P >= 0.  Rows of no expert are not written.  Errors: INVALID_ARG,
-   UNSUPPORTED, CUDA. */
+   multiple of 128, K of 64, P >= 0.  Rows of no expert are not written.  With a few rows per
+   expert, K a multiple of 256 and w_sf 16-byte aligned, a kernel for narrow token tiles runs
+   (same results up to the order of the fp32 sums).  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 moe_lora_status moe_lora_grouped_gemm_nvfp4(moe_lora_handle* h, const uint8_t* w, const uint8_t* w_sf,
                                             const float* w_gs, const uint16_t* x, const float* x_gs,
                                             const int32_t* expert_offsets, int E, int N, int K, int P, float* out,
