@@ -692,8 +692,6 @@ MLDEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uin
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-MLDEV uint32_t half2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
-
 // s[i] = {v, v} for v the e4m3 code in byte i of w, exact in f16
 MLDEV void e4m3x4_to_half2_bcast(uint32_t w, __half2 (&s)[4]) {
   const __half2 lo(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3));
