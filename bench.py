@@ -266,7 +266,8 @@ def _make_fwd(pkg, h, cfg, g, ws, out, k, args, w8=None, w4=None):
     return fwd
 
 
-# the BASELINE configurations timed beside the headline decode workload, in this order
+# the benchmark's other configurations (multi-slot, skewed prefill, Kimi-like decode and
+# prefill), timed beside the headline decode workload, in this order
 SIDE_WORKLOADS = ["multi_slot", "prefill_zipf", "kimi_decode", "kimi_prefill"]
 SIDE_BUDGET_S = 4.0   # timed seconds per side workload (LoRA on); steps are capped to fit
 
@@ -550,7 +551,7 @@ def run_gpu(args):
                 if vals:
                     st_ms[name] = round(1e3 * statistics.median(vals), 2)
             line.setdefault("stage_us", {})[label] = st_ms
-    # the other BASELINE configurations, one after another on the same GPU (rank 0 of a
+    # the other benchmark configurations, one after another on the same GPU (rank 0 of a
     # single-GPU run only: replicas would repeat the same numbers), each freed before the next
     side = [] if (quant or world > 1 or args.workload != "decode" or args.no_workloads) else \
         [w for w in SIDE_WORKLOADS if args.only_workloads is None or w in args.only_workloads.split(",")]
